@@ -1,0 +1,438 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05, sm_103a) with the
+// step's fused epilogues: plain store, fp32 store/accumulate, ReLU^2 (stores
+// u and relu(u)^2), ReLU^2 backward, cross-entropy forward partials
+// (per-row max / sum-exp / argmax / target logit over each 256-wide vocabulary
+// tile, so the logits are never written) and cross-entropy backward
+// (softmax - onehot).
+//
+// Structure: persistent CTAs (one per SM), 128x256 output tiles, 64-deep k
+// slices of bf16 staged by TMA into 128-byte-swizzled shared memory in a
+// 4-stage mbarrier ring; warp 0 issues TMA, one thread of warp 1 issues
+// tcgen05.mma into a TMEM accumulator (two 256-column buffers, so the
+// epilogue of tile i overlaps the main loop of tile i+1), warps 2..5 read the
+// accumulator with tcgen05.ld (one thread per output row) and run the
+// epilogue. Every wait is bounded; on timeout the kernel records
+// DEV_TIMEOUT, unwinds, frees its TMEM and returns.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "ops.cuh"
+#include "tc_ptx.cuh"
+
+namespace nc {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BN * BK * 2;   // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+
+struct TcParams {
+  GemmArgs g;
+  int num_m, num_n, num_kb, total;
+};
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* v) {
+  uint4 r;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  return r;
+}
+
+__device__ __forceinline__ void unpack8_bf16(uint4 r, float* v) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    float2 f = __bfloat1622float2(h);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+
+// Epilogue for one 32-column chunk of one row. v holds alpha*acc.
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int nc0, float* v) {
+  if (EPI == EPI_STORE || EPI == EPI_RELU2) {
+    bf16* c = static_cast<bf16*>(g.C) + (size_t)m * g.ldc + nc0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (nc0 + 8 * j < g.N) *reinterpret_cast<uint4*>(c + 8 * j) = pack8_bf16(v + 8 * j);
+    if (EPI == EPI_RELU2) {
+      bf16* c2 = static_cast<bf16*>(g.C2) + (size_t)m * g.ldc2 + nc0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float u = fmaxf(v[8 * j + i], 0.f);
+          a[i] = u * u;
+        }
+        if (nc0 + 8 * j < g.N) *reinterpret_cast<uint4*>(c2 + 8 * j) = pack8_bf16(a);
+      }
+    }
+  } else if (EPI == EPI_STORE_F32) {
+    float* c = static_cast<float*>(g.C) + (size_t)m * g.ldc + nc0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (nc0 + 4 * j < g.N) {
+        float4 o = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        if (g.beta != 0.f) {
+          float4 p = *reinterpret_cast<const float4*>(c + 4 * j);
+          o.x += g.beta * p.x; o.y += g.beta * p.y; o.z += g.beta * p.z; o.w += g.beta * p.w;
+        }
+        *reinterpret_cast<float4*>(c + 4 * j) = o;
+      }
+    }
+  } else if (EPI == EPI_RELU2_BWD) {
+    const bf16* u = static_cast<const bf16*>(g.C2) + (size_t)m * g.ldc2 + nc0;
+    bf16* c = static_cast<bf16*>(g.C) + (size_t)m * g.ldc + nc0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (nc0 + 8 * j < g.N) {
+        float uf[8], o[8];
+        unpack8_bf16(*reinterpret_cast<const uint4*>(u + 8 * j), uf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = v[8 * j + i] * 2.f * fmaxf(uf[i], 0.f);
+        *reinterpret_cast<uint4*>(c + 8 * j) = pack8_bf16(o);
+      }
+    }
+  } else if (EPI == EPI_CE_BWD) {
+    float l = g.row_f[m];
+    int t = g.row_i[m];
+    bf16* c = static_cast<bf16*>(g.C) + (size_t)m * g.ldc + nc0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (nc0 + 8 * j < g.N) {
+        float o[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          int n = nc0 + 8 * j + i;
+          o[i] = __expf(v[8 * j + i] - l) - (n == t ? 1.f : 0.f);
+        }
+        *reinterpret_cast<uint4*>(c + 8 * j) = pack8_bf16(o);
+      }
+    }
+  }
+}
+
+template <int EPI, int A_MN, int B_MN>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    gemm_tc_k(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+              const __grid_constant__ TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const GemmArgs& g = p.g;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(full + s, 1);
+      tc::mbar_init(empty + s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(tfull + b, 1);
+      tc::mbar_init(tempty + b, 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tc::prefetch_tmap(&ta);
+    tc::prefetch_tmap(&tb);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  bool failed = false;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued_phase[STAGES];
+      bool issued[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
+      for (int tile = blockIdx.x; tile < p.total && !failed; tile += gridDim.x) {
+        const int m0 = (tile / p.num_n) * BM, n0 = (tile % p.num_n) * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
+          const int k0 = kb * BK;
+          uint8_t* a = sA + stage * A_BYTES;
+          uint8_t* b = sB + stage * B_BYTES;
+          if (A_MN) {
+            tc::tma_load_2d(a, &ta, m0, k0, full + stage);
+            tc::tma_load_2d(a + 8192, &ta, m0 + 64, k0, full + stage);
+          } else {
+            tc::tma_load_2d(a, &ta, k0, m0, full + stage);
+          }
+          if (B_MN) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tc::tma_load_2d(b + j * 8192, &tb, n0 + 64 * j, k0, full + stage);
+          } else {
+            tc::tma_load_2d(b, &tb, k0, n0, full + stage);
+          }
+          issued[stage] = true;
+          issued_phase[stage] = phase;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        // let every copy this thread started land before the CTA exits
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) tc::mbar_wait(full + s, issued_phase[s], nullptr, kWaitNs);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int cnt = 0;
+      bool any_mma = false;
+      for (int tile = blockIdx.x; tile < p.total && !failed; tile += gridDim.x, ++cnt) {
+        const int ab = cnt & 1;
+        const uint32_t aph = (cnt >> 1) & 1;
+        if (!tc::mbar_wait(tempty + ab, aph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+        tc::tc_fence_after();
+        const uint32_t dtm = tmem_base + ab * BN;
+        for (int kb = 0; kb < p.num_kb; ++kb) {
+          if (!tc::mbar_wait(full + stage, phase, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::tc_fence_after();
+          const uint32_t a_addr = tc::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_addr = tc::smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = A_MN ? tc::sdesc_sw128(a_addr + k * 2048, 8192, 1024)
+                                     : tc::sdesc_sw128(a_addr + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? tc::sdesc_sw128(b_addr + k * 2048, 8192, 1024)
+                                     : tc::sdesc_sw128(b_addr + k * 32, 16, 1024);
+            tc::mma_bf16(dtm, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc::mma_commit(empty + stage);
+          any_mma = true;
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (failed) break;
+        tc::mma_commit(tfull + ab);
+      }
+      if (failed) {
+        *abort_flag = 1;
+        if (any_mma) {
+          // wait for the MMAs already issued before the TMEM is released
+          tc::mma_commit(drain);
+          tc::mbar_wait(drain, 0, nullptr, kWaitNs);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue warps
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int row = q * 32 + lane;
+    int cnt = 0;
+    for (int tile = blockIdx.x; tile < p.total && !failed; tile += gridDim.x, ++cnt) {
+      const int ab = cnt & 1;
+      const uint32_t aph = (cnt >> 1) & 1;
+      const int mb = tile / p.num_n, nb = tile % p.num_n;
+      const int m0 = mb * BM, n0 = nb * BN;
+      const bool ok = tc::mbar_wait(tfull + ab, aph, abort_flag, kWaitNs);
+      if (!__all_sync(0xffffffffu, ok)) { failed = true; *abort_flag = 1; break; }
+      tc::tc_fence_after();
+      const int m = m0 + row;
+      const bool row_ok = m < g.M;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * BN;
+      if (EPI == EPI_CE_FWD) {
+        float mx = -INFINITY, sum = 0.f, tl = 0.f;
+        int arg = 0;
+        const int t = row_ok ? g.row_i[m] : -1;
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          if (p.num_kb > 0) tc::tmem_ld32(taddr + c * 32, v);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          const int nc0 = n0 + c * 32;
+          if (nc0 >= g.N) continue;
+          float lm = -INFINITY;
+          int la = nc0;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            float x = v[i] * g.alpha;
+            v[i] = x;
+            if (nc0 + i < g.N && x > lm) { lm = x; la = nc0 + i; }
+            if (nc0 + i == t) tl = x;
+          }
+          if (lm > mx) {
+            sum *= __expf(mx - lm);
+            mx = lm;
+            arg = la;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (nc0 + i < g.N) sum += __expf(v[i] - mx);
+        }
+        if (row_ok) {
+          const size_t pi = (size_t)nb * g.M + m;
+          g.p_max[pi] = mx;
+          g.p_sum[pi] = sum;
+          g.p_arg[pi] = arg;
+          if (t >= n0 && t < n0 + BN) g.p_tgt[m] = tl;
+        }
+      } else {
+        for (int c = 0; c < BN / 32; ++c) {
+          float v[32];
+          if (p.num_kb > 0) tc::tmem_ld32(taddr + c * 32, v);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.f;
+          const int nc0 = n0 + c * 32;
+          if (!row_ok || nc0 >= g.N) continue;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= g.alpha;
+          epi_chunk<EPI>(g, m, nc0, v);
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(tempty + ab);
+    }
+  }
+
+  if (failed) {
+    set_status(g.status, DEV_TIMEOUT);
+    *abort_flag = 1;
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+int g_num_sms = 0;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 tensor map: inner (contiguous) extent, outer extent, row pitch in
+// elements, box of box_inner x box_outer, 128-byte swizzle, zero fill.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch,
+              uint32_t box_inner, uint32_t box_outer) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+typedef void (*KernFn)(CUtensorMap, CUtensorMap, TcParams);
+
+template <int EPI>
+KernFn pick(int a_mn, int b_mn) {
+  if (!a_mn && !b_mn) return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 0, 0>);
+  if (!a_mn && b_mn) return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 0, 1>);
+  if (a_mn && !b_mn) return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 1, 0>);
+  return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 1, 1>);
+}
+
+KernFn pick_kernel(int epi, int a_mn, int b_mn) {
+  switch (epi) {
+    case EPI_STORE: return pick<EPI_STORE>(a_mn, b_mn);
+    case EPI_STORE_F32: return pick<EPI_STORE_F32>(a_mn, b_mn);
+    case EPI_RELU2: return pick<EPI_RELU2>(a_mn, b_mn);
+    case EPI_RELU2_BWD: return pick<EPI_RELU2_BWD>(a_mn, b_mn);
+    case EPI_CE_BWD: return pick<EPI_CE_BWD>(a_mn, b_mn);
+    case EPI_CE_FWD: return pick<EPI_CE_FWD>(a_mn, b_mn);
+    default: return nullptr;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+
+bool gemm_tc_supports(const GemmArgs& g) {
+  if (g.M < 0 || g.N < 0 || g.K < 0) return false;
+  if (g.N % 8 || g.lda % 8 || g.ldb % 8) return false;
+  if (!aligned16(g.A) || !aligned16(g.B)) return false;
+  if (g.epi == EPI_CE_FWD) return g.p_max && g.p_sum && g.p_arg && g.p_tgt && g.row_i;
+  if (g.ldc % 8 || !aligned16(g.C)) return false;
+  if ((g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD) && (g.ldc2 % 8 || !aligned16(g.C2))) return false;
+  if (g.epi == EPI_CE_BWD && (!g.row_f || !g.row_i)) return false;
+  return g.epi >= EPI_STORE && g.epi <= EPI_CE_FWD;
+}
+
+cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
+  if (!gemm_tc_supports(g)) return cudaErrorNotSupported;
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  if (!get_encode()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  // TMA needs an extent of at least one element; an empty K reads nothing.
+  uint64_t K = g.K > 0 ? (uint64_t)g.K : 1;
+  bool ok = g.a_kmajor ? make_map(&ta, g.A, K, g.M, g.lda, 64, 128) : make_map(&ta, g.A, g.M, K, g.lda, 64, 64);
+  ok = ok && (g.b_kmajor ? make_map(&tb, g.B, K, g.N, g.ldb, 64, 256) : make_map(&tb, g.B, g.N, K, g.ldb, 64, 64));
+  if (!ok) return cudaErrorInvalidValue;
+  TcParams p;
+  p.g = g;
+  p.num_m = (g.M + BM - 1) / BM;
+  p.num_n = (g.N + BN - 1) / BN;
+  p.num_kb = (g.K + BK - 1) / BK;
+  p.total = p.num_m * p.num_n;
+  KernFn fn = pick_kernel(g.epi, !g.a_kmajor, !g.b_kmajor);
+  if (!fn) return cudaErrorNotSupported;
+  cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  int grid = p.total < g_num_sms ? p.total : g_num_sms;
+  fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace nc

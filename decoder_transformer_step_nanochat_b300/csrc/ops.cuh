@@ -1,0 +1,90 @@
+// Internal launch API of the step kernels. Every launcher enqueues on
+// `stream` and returns the cudaError_t of the launch.
+#pragma once
+
+#include "common.cuh"
+
+namespace nc {
+
+// ------------------------------------------------------------------ GEMM
+// C[m,n] = alpha * sum_k A(m,k) B(n,k), then an epilogue.
+//   A(m,k) = a_kmajor ? A[m*lda + k] : A[k*lda + m]
+//   B(n,k) = b_kmajor ? B[n*ldb + k] : B[k*ldb + n]
+enum Epi : int {
+  EPI_STORE = 0,       // C (elem) = alpha*acc
+  EPI_STORE_F32 = 1,   // C (f32)  = alpha*acc + beta*C
+  EPI_RELU2 = 2,       // C (elem) = u = alpha*acc ; C2 (elem) = max(u,0)^2
+  EPI_RELU2_BWD = 3,   // C (elem) = alpha*acc * 2*max(u,0), u read from C2
+  EPI_CE_BWD = 4,      // C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])
+  EPI_CE_FWD = 5,      // per (row, 256-column tile) softmax partials (tensor-core path)
+  EPI_QKNORM_ROPE = 6, // C (elem) = qkv with per-head RMSNorm + RoPE on the q,k columns
+};
+
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  const void* A = nullptr; long long lda = 0; int a_kmajor = 1;
+  const void* B = nullptr; long long ldb = 0; int b_kmajor = 1;
+  int epi = EPI_STORE;
+  float alpha = 1.f, beta = 0.f;
+  void* C = nullptr; long long ldc = 0;
+  void* C2 = nullptr; long long ldc2 = 0;
+  const float* row_f = nullptr;  // CE bwd: lse per row
+  const int* row_i = nullptr;    // CE fwd/bwd: target id per row
+  // CE forward partials, [n_tiles][M] each (tensor-core path)
+  float* p_max = nullptr; float* p_sum = nullptr; int* p_arg = nullptr;
+  float* p_tgt = nullptr;        // [M]: logit of the target column
+  // QK-norm + RoPE epilogue
+  const float* rope_cos = nullptr; const float* rope_sin = nullptr;  // [T,64]
+  float* rqk = nullptr;          // [M, 2H] rstd of q heads then k heads
+  int seq_len = 0, d_model = 0;
+  int* status = nullptr;
+};
+
+// Plain fp32-FMA tiled GEMM (any majorness, any sizes). elem = float or bf16.
+template <typename T> cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
+
+// tcgen05 / TMEM / TMA GEMM for bf16 operands. Returns cudaErrorNotSupported
+// for shapes it cannot serve (the caller treats that as a hard error).
+cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s);
+bool gemm_tc_supports(const GemmArgs& g);
+
+// ------------------------------------------------------------------ rows
+template <typename T>
+cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int V, int* status,
+                      cudaStream_t s);
+template <typename T>
+cudaError_t embed_bwd(const int* tok, const T* dx_unused, const float* dx, float* dwte, int M,
+                      int d, int V, cudaStream_t s);
+template <typename T>
+cudaError_t rmsnorm_fwd(const float* x, T* y, float* r, int M, int d, cudaStream_t s);
+// dx (f32) = (accumulate ? dx : 0) + r*(dy - y*mean(dy*y)); also dx_e = elem copy (if non-null)
+template <typename T>
+cudaError_t rmsnorm_bwd(const float* dy, const T* y, const float* r, float* dx, T* dx_e, int M,
+                        int d, int accumulate, cudaStream_t s);
+template <typename T>
+cudaError_t qk_norm_rope_fwd(T* qkv, float* rqk, const float* cs, const float* sn, int M, int T_,
+                             int H, cudaStream_t s);
+template <typename T>
+cudaError_t qk_norm_rope_bwd(const float* dqk, const T* qkv, const float* rqk, const float* cs,
+                             const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s);
+
+// ------------------------------------------------------------------ attention
+template <typename T>
+cudaError_t attn_fwd_simt(const T* qkv, T* o, float* lse, int B, int T_, int H, cudaStream_t s);
+template <typename T>
+cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, int H,
+                        cudaStream_t s);
+template <typename T>
+cudaError_t attn_bwd_simt(const T* qkv, const T* dout, const float* lse, const float* Drow,
+                          float* dqk, T* dqkv, int B, int T_, int H, cudaStream_t s);
+
+// ------------------------------------------------------------------ loss
+cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,
+                                int* amax, int M, int V, int* status, cudaStream_t s);
+cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int* p_arg,
+                               const float* p_tgt, int n_tiles, float* lse, float* nll,
+                               int* amax, int M, cudaStream_t s);
+cudaError_t mean_loss(const float* nll, int M, float* loss, cudaStream_t s);
+cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s);
+
+}  // namespace nc

@@ -1,0 +1,404 @@
+// Row-wise, memory-bound kernels of the step: embedding gather/scatter,
+// parameter-free RMSNorm forward/backward, per-head QK-norm + RoPE forward
+// and backward, softmax cross-entropy row reductions and the mean loss.
+//
+// One warp owns one row (or one 128-wide head row); lanes stride the row so
+// every warp-wide access is coalesced, and reductions use warp shuffles.
+#include "ops.cuh"
+
+namespace nc {
+
+namespace {
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const bf16* p) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x);
+  __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
+  float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+  return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(bf16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+constexpr int kRowWarps = 8;  // warps per CTA in the one-warp-per-row kernels
+
+// x[m,:] = wte[tok[m],:] (fp32 residual stream). The embedding is used as is:
+// no scaling and no normalisation after the lookup.
+template <typename T>
+__global__ void embed_fwd_k(const int* __restrict__ tok, const T* __restrict__ wte,
+                            float* __restrict__ x, int M, int d, int V, int* status) {
+  int m = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (m >= M) return;
+  int id = tok[m];
+  float* xr = x + (size_t)m * d;
+  if (id < 0 || id >= V) {
+    if (lane == 0) set_status(status, DEV_BAD_TOKEN);
+    for (int c = lane * 4; c < d; c += 128) st4(xr + c, make_float4(0.f, 0.f, 0.f, 0.f));
+    return;
+  }
+  const T* wr = wte + (size_t)id * d;
+  for (int c = lane * 4; c < d; c += 128) st4(xr + c, ld4(wr + c));
+}
+
+// dwte[tok[m],:] += dx[m,:]; dwte must be zeroed first. Rows of ids that no
+// position holds stay exactly zero.
+__global__ void embed_bwd_k(const int* __restrict__ tok, const float* __restrict__ dx,
+                            float* __restrict__ dwte, int M, int d, int V) {
+  int m = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (m >= M) return;
+  int id = tok[m];
+  if (id < 0 || id >= V) return;
+  const float* g = dx + (size_t)m * d;
+  float* w = dwte + (size_t)id * d;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 v = ld4(g + c);
+    atomicAdd(reinterpret_cast<float4*>(w + c), v);
+  }
+}
+
+// y = x * r, r = 1/sqrt(mean(x^2) + eps).
+template <typename T>
+__global__ void rmsnorm_fwd_k(const float* __restrict__ x, T* __restrict__ y, float* __restrict__ r,
+                              int M, int d) {
+  int m = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (m >= M) return;
+  const float* xr = x + (size_t)m * d;
+  float ss = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 v = ld4(xr + c);
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  float rr = rsqrtf(ss / (float)d + kEps);
+  T* yr = y + (size_t)m * d;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 v = ld4(xr + c);
+    st4(yr + c, make_float4(v.x * rr, v.y * rr, v.z * rr, v.w * rr));
+  }
+  if (lane == 0) r[m] = rr;
+}
+
+// dx = [dx +] r * (dy - y * mean(dy * y)); optional copy in the element type.
+template <typename T>
+__global__ void rmsnorm_bwd_k(const float* __restrict__ dy, const T* __restrict__ y,
+                              const float* __restrict__ r, float* __restrict__ dx, T* __restrict__ dxe,
+                              int M, int d, int accumulate) {
+  int m = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (m >= M) return;
+  const float* g = dy + (size_t)m * d;
+  const T* yr = y + (size_t)m * d;
+  float dot = 0.f;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 a = ld4(g + c), b = ld4(yr + c);
+    dot += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+  }
+  dot = warp_sum(dot) / (float)d;
+  float rr = r[m];
+  float* o = dx + (size_t)m * d;
+  T* oe = dxe ? dxe + (size_t)m * d : nullptr;
+  for (int c = lane * 4; c < d; c += 128) {
+    float4 a = ld4(g + c), b = ld4(yr + c);
+    float4 v = make_float4(rr * (a.x - b.x * dot), rr * (a.y - b.y * dot), rr * (a.z - b.z * dot),
+                           rr * (a.w - b.w * dot));
+    if (accumulate) {
+      float4 p = ld4(o + c);
+      v.x += p.x; v.y += p.y; v.z += p.z; v.w += p.w;
+    }
+    st4(o + c, v);
+    if (oe) st4(oe + c, v);
+  }
+}
+
+// Per-head QK-norm then RoPE, in place on the q and k columns of qkv[M,3d].
+// Lane L owns head dims L, L+32, L+64, L+96, so the RoPE partners (j, j+64)
+// sit in the same lane. rqk[m, which*H + h] = 1/sqrt(mean(q^2)+eps).
+template <typename T>
+__global__ void qk_norm_rope_fwd_k(T* __restrict__ qkv, float* __restrict__ rqk,
+                                   const float* __restrict__ cs, const float* __restrict__ sn,
+                                   int M, int Tlen, int H) {
+  int w = blockIdx.x * kRowWarps + threadIdx.x / 32;  // (m, which, h)
+  int lane = threadIdx.x & 31;
+  if (w >= M * 2 * H) return;
+  int m = w / (2 * H), wh = w % (2 * H);
+  int d = H * kHeadDim;
+  T* p = qkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;  // q heads then k heads
+  float v[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) v[c] = ldf(p + lane + 32 * c);
+  float ss = warp_sum(v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3]);
+  float rr = rsqrtf(ss / (float)kHeadDim + kEps);
+  int t = m % Tlen;
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    int j = lane + 32 * c;
+    float co = cs[t * kHalf + j], si = sn[t * kHalf + j];
+    float a = v[c] * rr, b = v[c + 2] * rr;
+    stf(p + j, a * co - b * si);
+    stf(p + j + kHalf, a * si + b * co);
+  }
+  if (lane == 0) rqk[(size_t)m * 2 * H + wh] = rr;
+}
+
+// Backward of q_hat = rope(rmsnorm(q)): dq_n = R^T dq_hat, q_n = R^T q_hat,
+// dq = r * (dq_n - q_n * mean(dq_n * q_n)). dqk is fp32 [M, 2d] (dq_hat then
+// dk_hat); results go to the q,k columns of dqkv[M,3d].
+template <typename T>
+__global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __restrict__ qkv,
+                                   const float* __restrict__ rqk, const float* __restrict__ cs,
+                                   const float* __restrict__ sn, T* __restrict__ dqkv, int M,
+                                   int Tlen, int H) {
+  int w = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  int lane = threadIdx.x & 31;
+  if (w >= M * 2 * H) return;
+  int m = w / (2 * H), wh = w % (2 * H);
+  int d = H * kHeadDim;
+  const float* g = dqk + (size_t)m * 2 * d + (size_t)wh * kHeadDim;
+  const T* q = qkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
+  int t = m % Tlen;
+  float gn[4], qn[4];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    int j = lane + 32 * c;
+    float co = cs[t * kHalf + j], si = sn[t * kHalf + j];
+    float g1 = g[j], g2 = g[j + kHalf];
+    gn[c] = g1 * co + g2 * si;
+    gn[c + 2] = -g1 * si + g2 * co;
+    float q1 = ldf(q + j), q2 = ldf(q + j + kHalf);
+    qn[c] = q1 * co + q2 * si;
+    qn[c + 2] = -q1 * si + q2 * co;
+  }
+  float dot = warp_sum(gn[0] * qn[0] + gn[1] * qn[1] + gn[2] * qn[2] + gn[3] * qn[3]) / (float)kHeadDim;
+  float rr = rqk[(size_t)m * 2 * H + wh];
+  T* o = dqkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) stf(o + lane + 32 * c, rr * (gn[c] - qn[c] * dot));
+}
+
+// D[b,h,t] = sum_e dout[m, h*128+e] * o[m, h*128+e]  (softmax backward term)
+template <typename T>
+__global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ o,
+                              float* __restrict__ Drow, int B, int Tlen, int H) {
+  int w = blockIdx.x * kRowWarps + threadIdx.x / 32;  // (m, h)
+  int lane = threadIdx.x & 31;
+  int M = B * Tlen;
+  if (w >= M * H) return;
+  int m = w / H, h = w % H;
+  size_t base = (size_t)m * H * kHeadDim + (size_t)h * kHeadDim;
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) s += ldf(dout + base + lane + 32 * c) * ldf(o + base + lane + 32 * c);
+  s = warp_sum(s);
+  int b = m / Tlen, t = m % Tlen;
+  if (lane == 0) Drow[((size_t)b * H + h) * Tlen + t] = s;
+}
+
+// One CTA per row of a materialised fp32 logits block: logsumexp, loss
+// lse - logit[target], argmax (lowest index among ties).
+__global__ void ce_rows_k(const float* __restrict__ logits, const int* __restrict__ tgt,
+                          float* __restrict__ lse, float* __restrict__ nll, int* __restrict__ amax,
+                          int V, int* status) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  int m = blockIdx.x;
+  const float* row = logits + (size_t)m * V;
+  float best = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int n = threadIdx.x; n < V; n += blockDim.x) {
+    float v = row[n];
+    if (v > best) { best = v; bi = n; }
+  }
+  // warp then block argmax with lowest-index tie break
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, best, o);
+    int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+  }
+  int wid = threadIdx.x / 32, lane = threadIdx.x & 31, nw = blockDim.x / 32;
+  if (lane == 0) { sv[wid] = best; si[wid] = bi; }
+  __syncthreads();
+  if (wid == 0) {
+    best = lane < nw ? sv[lane] : -INFINITY;
+    bi = lane < nw ? si[lane] : 0x7fffffff;
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    if (lane == 0) { sv[0] = best; si[0] = bi; }
+  }
+  __syncthreads();
+  float mx = sv[0];
+  int amx = si[0];
+  __syncthreads();
+  float s = 0.f;
+  for (int n = threadIdx.x; n < V; n += blockDim.x) s += expf(row[n] - mx);
+  s = warp_sum(s);
+  if (lane == 0) sv[wid] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int i = 0; i < nw; ++i) tot += sv[i];
+    float l = mx + logf(tot);
+    int t = tgt[m];
+    lse[m] = l;
+    amax[m] = amx;
+    if (t < 0 || t >= V) {
+      set_status(status, DEV_BAD_TOKEN);
+      nll[m] = 0.f;
+    } else {
+      nll[m] = l - row[t];
+    }
+  }
+}
+
+// Combine per-tile softmax partials (max, sum of exp(logit - max), argmax)
+// of every 256-column vocabulary tile into lse, loss and argmax per row.
+__global__ void ce_reduce_k(const float* __restrict__ pm, const float* __restrict__ ps,
+                            const int* __restrict__ pa, const float* __restrict__ pt, int nt,
+                            float* __restrict__ lse, float* __restrict__ nll, int* __restrict__ amax,
+                            int M) {
+  int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  float mx = -INFINITY;
+  int arg = 0;
+  for (int t = 0; t < nt; ++t) {
+    float v = pm[(size_t)t * M + m];
+    if (v > mx) { mx = v; arg = pa[(size_t)t * M + m]; }  // first tile wins ties
+  }
+  float s = 0.f;
+  for (int t = 0; t < nt; ++t) s += ps[(size_t)t * M + m] * expf(pm[(size_t)t * M + m] - mx);
+  float l = mx + logf(s);
+  lse[m] = l;
+  nll[m] = l - pt[m];
+  amax[m] = arg;
+}
+
+// loss = mean(nll), fixed summation order (one CTA, float64 partials).
+__global__ void mean_loss_k(const float* __restrict__ nll, int M, float* __restrict__ loss) {
+  __shared__ double sh[1024];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < M; i += blockDim.x) s += (double)nll[i];
+  sh[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = (float)(sh[0] / (double)M);
+}
+
+__global__ void check_ids_k(const int* __restrict__ ids, int n, int V, int* status) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) {
+    int v = ids[i];
+    if (v < 0 || v >= V) set_status(status, DEV_BAD_TOKEN);
+  }
+}
+
+inline int row_blocks(long long rows) { return (int)((rows + kRowWarps - 1) / kRowWarps); }
+
+}  // namespace
+
+template <typename T>
+cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int V, int* status,
+                      cudaStream_t s) {
+  embed_fwd_k<T><<<row_blocks(M), 32 * kRowWarps, 0, s>>>(tok, wte, x, M, d, V, status);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t embed_bwd(const int* tok, const T*, const float* dx, float* dwte, int M, int d, int V,
+                      cudaStream_t s) {
+  embed_bwd_k<<<row_blocks(M), 32 * kRowWarps, 0, s>>>(tok, dx, dwte, M, d, V);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rmsnorm_fwd(const float* x, T* y, float* r, int M, int d, cudaStream_t s) {
+  rmsnorm_fwd_k<T><<<row_blocks(M), 32 * kRowWarps, 0, s>>>(x, y, r, M, d);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rmsnorm_bwd(const float* dy, const T* y, const float* r, float* dx, T* dx_e, int M,
+                        int d, int accumulate, cudaStream_t s) {
+  rmsnorm_bwd_k<T><<<row_blocks(M), 32 * kRowWarps, 0, s>>>(dy, y, r, dx, dx_e, M, d, accumulate);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t qk_norm_rope_fwd(T* qkv, float* rqk, const float* cs, const float* sn, int M, int T_,
+                             int H, cudaStream_t s) {
+  qk_norm_rope_fwd_k<T><<<row_blocks((long long)M * 2 * H), 32 * kRowWarps, 0, s>>>(qkv, rqk, cs, sn, M, T_, H);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t qk_norm_rope_bwd(const float* dqk, const T* qkv, const float* rqk, const float* cs,
+                             const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s) {
+  qk_norm_rope_bwd_k<T><<<row_blocks((long long)M * 2 * H), 32 * kRowWarps, 0, s>>>(dqk, qkv, rqk, cs, sn, dqkv, M, T_, H);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, int H,
+                        cudaStream_t s) {
+  attn_rowdot_k<T><<<row_blocks((long long)B * T_ * H), 32 * kRowWarps, 0, s>>>(dout, o, Drow, B, T_, H);
+  return cudaGetLastError();
+}
+
+cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,
+                                int* amax, int M, int V, int* status, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  ce_rows_k<<<M, 512, 0, s>>>(logits, tgt, lse, nll, amax, V, status);
+  return cudaGetLastError();
+}
+
+cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int* p_arg,
+                               const float* p_tgt, int n_tiles, float* lse, float* nll, int* amax,
+                               int M, cudaStream_t s) {
+  ce_reduce_k<<<(M + 255) / 256, 256, 0, s>>>(p_max, p_sum, p_arg, p_tgt, n_tiles, lse, nll, amax, M);
+  return cudaGetLastError();
+}
+
+cudaError_t mean_loss(const float* nll, int M, float* loss, cudaStream_t s) {
+  mean_loss_k<<<1, 1024, 0, s>>>(nll, M, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s) {
+  if (n == 0) return cudaSuccess;
+  check_ids_k<<<(n + 255) / 256, 256, 0, s>>>(ids, n, V, status);
+  return cudaGetLastError();
+}
+
+#define NC_INST(T)                                                                               \
+  template cudaError_t embed_fwd<T>(const int*, const T*, float*, int, int, int, int*,          \
+                                    cudaStream_t);                                               \
+  template cudaError_t embed_bwd<T>(const int*, const T*, const float*, float*, int, int, int,  \
+                                    cudaStream_t);                                               \
+  template cudaError_t rmsnorm_fwd<T>(const float*, T*, float*, int, int, cudaStream_t);         \
+  template cudaError_t rmsnorm_bwd<T>(const float*, const T*, const float*, float*, T*, int,     \
+                                      int, int, cudaStream_t);                                   \
+  template cudaError_t qk_norm_rope_fwd<T>(T*, float*, const float*, const float*, int, int,     \
+                                           int, cudaStream_t);                                   \
+  template cudaError_t qk_norm_rope_bwd<T>(const float*, const T*, const float*, const float*,   \
+                                           const float*, T*, int, int, int, cudaStream_t);       \
+  template cudaError_t attn_rowdot<T>(const T*, const T*, float*, int, int, int, cudaStream_t);
+NC_INST(float)
+NC_INST(bf16)
+#undef NC_INST
+
+}  // namespace nc

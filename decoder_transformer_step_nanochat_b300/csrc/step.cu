@@ -1,0 +1,603 @@
+// Context, workspace layout and launch sequence of the nanochat pretraining
+// step (forward, mean next-token cross-entropy, analytic backward) behind the
+// C ABI of include/nc.h and include/nc_ops.h.
+//
+// The step follows the nanochat explainer: pre-norm decoder blocks with
+// parameter-free RMSNorm, QK-norm + RoPE attention, ReLU^2 MLP
+// ("Architecture Choices", "RoPE Intuition", "ReLU^2 Sparsity"), untied
+// embedding / lm_head, and the cross-entropy of "Pretraining".
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/nc.h"
+#include "../../include/nc_ops.h"
+#include "ops.cuh"
+
+using namespace nc;
+
+namespace {
+
+thread_local std::string g_err;
+
+nc_status fail(nc_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+nc_status fail(nc_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+#define CK(expr)                                                                              \
+  do {                                                                                        \
+    cudaError_t e_ = (expr);                                                                  \
+    if (e_ != cudaSuccess)                                                                    \
+      return fail(NC_ERR_CUDA, "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(e_), __FILE__, \
+                  __LINE__);                                                                  \
+  } while (0)
+
+#define CKS(expr)                          \
+  do {                                     \
+    nc_status s_ = (expr);                 \
+    if (s_ != NC_OK) return s_;            \
+  } while (0)
+
+constexpr size_t kAlign = 1024;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+}  // namespace
+
+struct nc_ctx {
+  // model shape
+  int L = 0, d = 0, H = 0, T = 0, V = 0, F = 0;
+  // configuration
+  int B = 0, M = 0, prec = -1, esz = 0;
+  cudaStream_t stream = nullptr;
+  int device = -1;
+  bool use_tc = false;      // tensor-core GEMMs for the bf16 mode
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  int* status = nullptr;    // device status word
+  // workspace
+  char* ws = nullptr;
+  size_t ws_bytes = 0, ws_need = 0;
+  int ce_rows = 0;          // rows per lm_head / cross-entropy chunk
+  int ce_tiles = 0;         // 256-wide vocabulary tiles (tensor-core CE partials)
+  struct Off {
+    size_t xn1, r1, qkv, rqk, o, lse_att, xn2, r2, u, a;  // per-layer stash (stride below)
+    size_t layer_stride;
+    size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
+    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt;
+  } off{};
+  // last forward
+  const void* params = nullptr;
+  const int* tok = nullptr;
+  const int* tgt = nullptr;
+  bool have_fwd = false;
+};
+
+namespace {
+
+template <typename P>
+P* wsp(nc_ctx* c, size_t off) { return reinterpret_cast<P*>(c->ws + off); }
+
+size_t param_offset(const nc_ctx* c, int index, int* rows, int* cols) {
+  size_t d = c->d, V = c->V, F = c->F;
+  size_t per_layer = 3 * d * d + d * d + F * d + d * F;
+  if (index == 0) { *rows = c->V; *cols = c->d; return 0; }
+  if (index == 1 + 4 * c->L) { *rows = c->V; *cols = c->d; return V * d + (size_t)c->L * per_layer; }
+  int l = (index - 1) / 4, k = (index - 1) % 4;
+  size_t base = V * d + (size_t)l * per_layer;
+  switch (k) {
+    case 0: *rows = 3 * c->d; *cols = c->d; return base;
+    case 1: *rows = c->d; *cols = c->d; return base + 3 * d * d;
+    case 2: *rows = c->F; *cols = c->d; return base + 4 * d * d;
+    default: *rows = c->d; *cols = c->F; return base + 4 * d * d + F * d;
+  }
+}
+
+void plan_workspace(nc_ctx* c) {
+  size_t M = c->M, d = c->d, F = c->F, H = c->H, V = c->V, e = c->esz;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o += align_up(bytes); return r; };
+  auto& f = c->off;
+  f.xn1 = take(M * d * e);
+  f.r1 = take(M * 4);
+  f.qkv = take(M * 3 * d * e);
+  f.rqk = take(M * 2 * H * 4);
+  f.o = take(M * d * e);
+  f.lse_att = take(M * H * 4);
+  f.xn2 = take(M * d * e);
+  f.r2 = take(M * 4);
+  f.u = take(M * F * e);
+  f.a = take(M * F * e);
+  f.layer_stride = o;
+  o = f.layer_stride * c->L;
+  f.x = take(M * d * 4);
+  f.hf = take(M * d * e);
+  f.rf = take(M * 4);
+  f.lse = take(M * 4);
+  f.nll = take(M * 4);
+  f.amax = take(M * 4);
+  f.loss = take(4);
+  c->ce_tiles = (int)((V + 255) / 256);
+  f.pmax = take((size_t)c->ce_tiles * M * 4);
+  f.psum = take((size_t)c->ce_tiles * M * 4);
+  f.parg = take((size_t)c->ce_tiles * M * 4);
+  f.ptgt = take(M * 4);
+  c->ce_rows = (int)(M < 4096 ? M : 4096);
+  f.chunk = take((size_t)c->ce_rows * V * 4);  // fp32 logits (debug) or element-typed g
+  f.dx = take(M * d * 4);
+  f.dxe = take(M * d * e);
+  f.dy = take(M * d * 4);
+  f.du = take(M * F * e);
+  f.dout = take(M * d * e);
+  f.dqkv = take(M * 3 * d * e);
+  f.dqk = take(M * 2 * d * 4);
+  f.drow = take(M * H * 4);
+  f.tok = take(M * 4);
+  f.tgt = take(M * 4);
+  c->ws_need = o;
+}
+
+nc_status check_ready(nc_ctx* c) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  if (c->prec < 0) return fail(NC_ERR_STATE, "nc_configure has not been called");
+  if (!c->ws) return fail(NC_ERR_STATE, "nc_set_workspace has not been called");
+  int dev = -1;
+  CK(cudaGetDevice(&dev));
+  if (dev != c->device) return fail(NC_ERR_STATE, "current device %d differs from the configured %d", dev, c->device);
+  return NC_OK;
+}
+
+nc_status read_status(nc_ctx* c) {
+  int st = 0;
+  CK(cudaMemcpyAsync(&st, c->status, sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  if (st == DEV_OK) return NC_OK;
+  CK(cudaMemsetAsync(c->status, 0, sizeof(int), c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  if (st == DEV_TIMEOUT) return fail(NC_ERR_TIMEOUT, "a device pipeline wait exceeded its iteration limit");
+  if (st == DEV_BAD_TOKEN) return fail(NC_ERR_DEVICE, "a token or target id is outside [0, vocab)");
+  return fail(NC_ERR_DEVICE, "device status %d", st);
+}
+
+// ------------------------------------------------------------------ GEMM dispatch
+
+nc_status gemm(nc_ctx* c, GemmArgs g) {
+  g.status = c->status;
+  cudaError_t e;
+  if (c->prec == NC_FP32_DEBUG) {
+    e = gemm_simt<float>(g, c->stream);
+  } else if (c->use_tc) {
+    if (!gemm_tc_supports(g))
+      return fail(NC_ERR_UNSUPPORTED, "tensor-core GEMM cannot serve M=%d N=%d K=%d epi=%d", g.M, g.N, g.K, g.epi);
+    e = gemm_tc(g, c->stream);
+  } else {
+    e = gemm_simt<bf16>(g, c->stream);
+  }
+  if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm M=%d N=%d K=%d epi=%d: %s", g.M, g.N, g.K, g.epi, cudaGetErrorString(e));
+  return NC_OK;
+}
+
+GemmArgs mk(int M, int N, int K, const void* A, long long lda, int ak, const void* B, long long ldb,
+            int bk, int epi, void* C, long long ldc, float alpha = 1.f, float beta = 0.f) {
+  GemmArgs g;
+  g.M = M; g.N = N; g.K = K;
+  g.A = A; g.lda = lda; g.a_kmajor = ak;
+  g.B = B; g.ldb = ldb; g.b_kmajor = bk;
+  g.epi = epi; g.C = C; g.ldc = ldc; g.alpha = alpha; g.beta = beta;
+  return g;
+}
+
+// ------------------------------------------------------------------ step pieces
+
+template <typename T>
+nc_status lmhead_ce_forward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt, int M, float* lse,
+                            float* nll, int* amax) {
+  int d = c->d, V = c->V;
+  if (c->prec == NC_BF16 && c->use_tc) {
+    GemmArgs g = mk(M, V, d, hf, d, 1, wlm, d, 1, EPI_CE_FWD, nullptr, 0);
+    g.row_i = tgt;
+    g.p_max = wsp<float>(c, c->off.pmax);
+    g.p_sum = wsp<float>(c, c->off.psum);
+    g.p_arg = wsp<int>(c, c->off.parg);
+    g.p_tgt = wsp<float>(c, c->off.ptgt);
+    CKS(gemm(c, g));
+    CK(ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, c->ce_tiles, lse, nll, amax, M, c->stream));
+    return NC_OK;
+  }
+  float* logits = wsp<float>(c, c->off.chunk);
+  for (int r0 = 0; r0 < M; r0 += c->ce_rows) {
+    int rows = M - r0 < c->ce_rows ? M - r0 : c->ce_rows;
+    CKS(gemm(c, mk(rows, V, d, hf + (size_t)r0 * d, d, 1, wlm, d, 1, EPI_STORE_F32, logits, V)));
+    CK(ce_rows_from_logits(logits, tgt + r0, lse + r0, nll + r0, amax + r0, rows, V, c->status, c->stream));
+  }
+  return NC_OK;
+}
+
+// g = softmax - onehot per chunk; dhf = g W_lm / M ; dW_lm = g^T hf / M
+template <typename T>
+nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt, const float* lse,
+                             int M, float inv_count, float* dhf, float* dwlm) {
+  int d = c->d, V = c->V;
+  T* g = wsp<T>(c, c->off.chunk);
+  for (int r0 = 0; r0 < M; r0 += c->ce_rows) {
+    int rows = M - r0 < c->ce_rows ? M - r0 : c->ce_rows;
+    GemmArgs a = mk(rows, V, d, hf + (size_t)r0 * d, d, 1, wlm, d, 1, EPI_CE_BWD, g, V);
+    a.row_f = lse + r0;
+    a.row_i = tgt + r0;
+    CKS(gemm(c, a));
+    CKS(gemm(c, mk(rows, d, V, g, V, 1, wlm, d, 0, EPI_STORE_F32, dhf + (size_t)r0 * d, d, inv_count)));
+    CKS(gemm(c, mk(V, d, rows, g, V, 0, hf + (size_t)r0 * d, d, 0, EPI_STORE_F32, dwlm, d, inv_count,
+                   r0 == 0 ? 0.f : 1.f)));
+  }
+  return NC_OK;
+}
+
+template <typename T>
+nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* d_loss) {
+  int M = c->M, d = c->d, H = c->H, F = c->F, V = c->V, Tn = c->T;
+  cudaStream_t s = c->stream;
+  CK(check_ids(tok, M, V, c->status, s));
+  CK(check_ids(tgt, M, V, c->status, s));
+  float* x = wsp<float>(c, c->off.x);
+  int rows, cols;
+  CK(embed_fwd<T>(tok, P, x, M, d, V, c->status, s));
+  for (int l = 0; l < c->L; ++l) {
+    size_t lb = (size_t)l * c->off.layer_stride;
+    T* xn1 = wsp<T>(c, lb + c->off.xn1);
+    float* r1 = wsp<float>(c, lb + c->off.r1);
+    T* qkv = wsp<T>(c, lb + c->off.qkv);
+    float* rqk = wsp<float>(c, lb + c->off.rqk);
+    T* o = wsp<T>(c, lb + c->off.o);
+    float* lse_att = wsp<float>(c, lb + c->off.lse_att);
+    T* xn2 = wsp<T>(c, lb + c->off.xn2);
+    float* r2 = wsp<float>(c, lb + c->off.r2);
+    T* u = wsp<T>(c, lb + c->off.u);
+    T* a = wsp<T>(c, lb + c->off.a);
+    const T* Wqkv = P + param_offset(c, 1 + 4 * l, &rows, &cols);
+    const T* Wo = P + param_offset(c, 2 + 4 * l, &rows, &cols);
+    const T* Wfc = P + param_offset(c, 3 + 4 * l, &rows, &cols);
+    const T* Wproj = P + param_offset(c, 4 + 4 * l, &rows, &cols);
+
+    CK(rmsnorm_fwd<T>(x, xn1, r1, M, d, s));
+    CKS(gemm(c, mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_STORE, qkv, 3 * d)));
+    CK(qk_norm_rope_fwd<T>(qkv, rqk, c->rope_cos, c->rope_sin, M, Tn, H, s));
+    CK(attn_fwd_simt<T>(qkv, o, lse_att, c->B, Tn, H, s));
+    CKS(gemm(c, mk(M, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
+    CK(rmsnorm_fwd<T>(x, xn2, r2, M, d, s));
+    GemmArgs up = mk(M, F, d, xn2, d, 1, Wfc, d, 1, EPI_RELU2, u, F);
+    up.C2 = a; up.ldc2 = F;
+    CKS(gemm(c, up));
+    CKS(gemm(c, mk(M, d, F, a, F, 1, Wproj, F, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
+  }
+  T* hf = wsp<T>(c, c->off.hf);
+  float* rf = wsp<float>(c, c->off.rf);
+  CK(rmsnorm_fwd<T>(x, hf, rf, M, d, s));
+  const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
+  CKS(lmhead_ce_forward<T>(c, hf, Wlm, tgt, M, wsp<float>(c, c->off.lse), wsp<float>(c, c->off.nll),
+                           wsp<int>(c, c->off.amax)));
+  CK(mean_loss(wsp<float>(c, c->off.nll), M, d_loss, s));
+  return NC_OK;
+}
+
+template <typename T>
+nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* G) {
+  int M = c->M, d = c->d, H = c->H, F = c->F, V = c->V, Tn = c->T;
+  cudaStream_t s = c->stream;
+  int rows, cols;
+  float* dx = wsp<float>(c, c->off.dx);
+  T* dxe = wsp<T>(c, c->off.dxe);
+  float* dy = wsp<float>(c, c->off.dy);
+  T* du = wsp<T>(c, c->off.du);
+  T* dout = wsp<T>(c, c->off.dout);
+  T* dqkv = wsp<T>(c, c->off.dqkv);
+  float* dqk = wsp<float>(c, c->off.dqk);
+  float* drow = wsp<float>(c, c->off.drow);
+  const T* hf = wsp<T>(c, c->off.hf);
+  size_t o_lm = param_offset(c, 1 + 4 * c->L, &rows, &cols);
+  CKS(lmhead_ce_backward<T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, 1.f / (float)M, dy, G + o_lm));
+  CK(rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
+  for (int l = c->L - 1; l >= 0; --l) {
+    size_t lb = (size_t)l * c->off.layer_stride;
+    const T* xn1 = wsp<T>(c, lb + c->off.xn1);
+    const float* r1 = wsp<float>(c, lb + c->off.r1);
+    const T* qkv = wsp<T>(c, lb + c->off.qkv);
+    const float* rqk = wsp<float>(c, lb + c->off.rqk);
+    const T* o = wsp<T>(c, lb + c->off.o);
+    const float* lse_att = wsp<float>(c, lb + c->off.lse_att);
+    const T* xn2 = wsp<T>(c, lb + c->off.xn2);
+    const float* r2 = wsp<float>(c, lb + c->off.r2);
+    T* u = wsp<T>(c, lb + c->off.u);
+    const T* a = wsp<T>(c, lb + c->off.a);
+    size_t oq = param_offset(c, 1 + 4 * l, &rows, &cols);
+    size_t oo = param_offset(c, 2 + 4 * l, &rows, &cols);
+    size_t of = param_offset(c, 3 + 4 * l, &rows, &cols);
+    size_t op = param_offset(c, 4 + 4 * l, &rows, &cols);
+    // MLP: x += relu2(xn2 Wfc^T) Wproj^T
+    CKS(gemm(c, mk(d, F, M, dxe, d, 0, a, F, 0, EPI_STORE_F32, G + op, F)));
+    GemmArgs g1 = mk(M, F, d, dxe, d, 1, P + op, F, 0, EPI_RELU2_BWD, du, F);
+    g1.C2 = u; g1.ldc2 = F;
+    CKS(gemm(c, g1));
+    CKS(gemm(c, mk(F, d, M, du, F, 0, xn2, d, 0, EPI_STORE_F32, G + of, d)));
+    CKS(gemm(c, mk(M, d, F, du, F, 1, P + of, d, 0, EPI_STORE_F32, dy, d)));
+    CK(rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
+    // attention: x += attn(xn1) Wo^T
+    CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
+    CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
+    CK(attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s));
+    CK(attn_bwd_simt<T>(qkv, dout, lse_att, drow, dqk, dqkv, c->B, Tn, H, s));
+    CK(qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s));
+    CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d)));
+    CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, EPI_STORE_F32, dy, d)));
+    CK(rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
+  }
+  CK(cudaMemsetAsync(G, 0, (size_t)V * d * sizeof(float), s));
+  CK(embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s));
+  return NC_OK;
+}
+
+nc_status forward_any(nc_ctx* c, const void* params, const int32_t* tok, const int32_t* tgt, float* d_loss) {
+  if (!params || !tok || !tgt || !d_loss) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_ready(c));
+  c->have_fwd = false;
+  nc_status st = c->prec == NC_BF16
+                     ? forward_impl<bf16>(c, static_cast<const bf16*>(params), tok, tgt, d_loss)
+                     : forward_impl<float>(c, static_cast<const float*>(params), tok, tgt, d_loss);
+  if (st != NC_OK) return st;
+  c->params = params; c->tok = tok; c->tgt = tgt; c->have_fwd = true;
+  return NC_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+nc_status nc_create(int depth, int d_model, int n_head, int seq_len, int vocab, nc_ctx** out) {
+  if (!out) return fail(NC_ERR_ARG, "out is null");
+  *out = nullptr;
+  if (depth < 1 || depth > 512) return fail(NC_ERR_ARG, "depth %d outside [1, 512]", depth);
+  if (n_head < 1 || d_model != 128 * n_head)
+    return fail(NC_ERR_ARG, "d_model (%d) must equal 128 * n_head (%d): head_dim is 128", d_model, n_head);
+  if (vocab < 128 || vocab > (1 << 20) || vocab % 128 != 0)
+    return fail(NC_ERR_ARG, "vocab %d must be a multiple of 128 in [128, 2^20]", vocab);
+  if (seq_len < 1 || seq_len > (1 << 16)) return fail(NC_ERR_ARG, "seq_len %d outside [1, 65536]", seq_len);
+  nc_ctx* c = new (std::nothrow) nc_ctx();
+  if (!c) return fail(NC_ERR_ARG, "out of host memory");
+  c->L = depth; c->d = d_model; c->H = n_head; c->T = seq_len; c->V = vocab; c->F = 4 * d_model;
+  *out = c;
+  g_err.clear();
+  return NC_OK;
+}
+
+nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  if (batch < 1) return fail(NC_ERR_ARG, "batch %d < 1", batch);
+  if ((long long)batch * c->T > (1LL << 22)) return fail(NC_ERR_ARG, "batch*seq_len too large");
+  if (precision != NC_BF16 && precision != NC_FP32_DEBUG) return fail(NC_ERR_ARG, "unknown precision %d", precision);
+  if (precision == NC_BF16 && c->T % 128 != 0)
+    return fail(NC_ERR_ARG, "NC_BF16 needs seq_len %% 128 == 0 (got %d)", c->T);
+  int dev = -1;
+  CK(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  CK(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(NC_ERR_UNSUPPORTED, "this library is built for sm_103a (B300); device is sm_%d%d", prop.major, prop.minor);
+  if (c->rope_cos) { cudaFree(c->rope_cos); c->rope_cos = nullptr; }
+  if (c->rope_sin) { cudaFree(c->rope_sin); c->rope_sin = nullptr; }
+  if (!c->status) CK(cudaMalloc(&c->status, sizeof(int)));
+  // RoPE table: angle pos * 10000^(-j/64) formed in float64, stored fp32.
+  std::vector<float> hc((size_t)c->T * kHalf), hs((size_t)c->T * kHalf);
+  for (int t = 0; t < c->T; ++t)
+    for (int j = 0; j < kHalf; ++j) {
+      double ang = (double)t * pow(10000.0, -(double)j / (double)kHalf);
+      hc[(size_t)t * kHalf + j] = (float)cos(ang);
+      hs[(size_t)t * kHalf + j] = (float)sin(ang);
+    }
+  CK(cudaMalloc(&c->rope_cos, hc.size() * sizeof(float)));
+  CK(cudaMalloc(&c->rope_sin, hs.size() * sizeof(float)));
+  c->stream = static_cast<cudaStream_t>(stream);
+  CK(cudaMemcpyAsync(c->rope_cos, hc.data(), hc.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->rope_sin, hs.data(), hs.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemsetAsync(c->status, 0, sizeof(int), c->stream));
+  CK(cudaStreamSynchronize(c->stream));
+  c->device = dev;
+  c->B = batch; c->M = batch * c->T; c->prec = precision;
+  c->esz = precision == NC_BF16 ? 2 : 4;
+  c->use_tc = precision == NC_BF16;
+  plan_workspace(c);
+  c->ws = nullptr; c->ws_bytes = 0; c->have_fwd = false;
+  return NC_OK;
+}
+
+size_t nc_param_count(const nc_ctx* c) {
+  if (!c) return 0;
+  return 2 * (size_t)c->V * c->d + 12 * (size_t)c->L * c->d * c->d;
+}
+
+nc_status nc_param_offset(const nc_ctx* c, int index, size_t* offset, int* rows, int* cols) {
+  if (!c || !offset || !rows || !cols) return fail(NC_ERR_ARG, "null argument");
+  if (index < 0 || index > 1 + 4 * c->L) return fail(NC_ERR_ARG, "index %d outside [0, %d]", index, 1 + 4 * c->L);
+  *offset = param_offset(c, index, rows, cols);
+  return NC_OK;
+}
+
+size_t nc_workspace_bytes(const nc_ctx* c) { return c && c->prec >= 0 ? c->ws_need : 0; }
+
+nc_status nc_set_workspace(nc_ctx* c, void* p, size_t bytes) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  if (c->prec < 0) return fail(NC_ERR_STATE, "nc_configure has not been called");
+  if (!p) return fail(NC_ERR_ARG, "null workspace");
+  if (reinterpret_cast<uintptr_t>(p) % kAlign) return fail(NC_ERR_ARG, "workspace must be %zu-byte aligned", kAlign);
+  if (bytes < c->ws_need) return fail(NC_ERR_ARG, "workspace has %zu bytes, needs %zu", bytes, c->ws_need);
+  c->ws = static_cast<char*>(p);
+  c->ws_bytes = bytes;
+  c->have_fwd = false;
+  return NC_OK;
+}
+
+nc_status nc_forward_loss_async(nc_ctx* c, const void* params, const int32_t* tok, const int32_t* tgt, float* d_loss) {
+  return forward_any(c, params, tok, tgt, d_loss);
+}
+
+nc_status nc_forward_loss(nc_ctx* c, const void* params, const int32_t* tok, const int32_t* tgt, float* loss) {
+  if (!loss) return fail(NC_ERR_ARG, "loss is null");
+  CKS(check_ready(c));
+  float* dl = wsp<float>(c, c->off.loss);
+  CKS(forward_any(c, params, tok, tgt, dl));
+  CK(cudaMemcpyAsync(loss, dl, sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+  nc_status st = read_status(c);
+  if (st != NC_OK) c->have_fwd = false;
+  return st;
+}
+
+nc_status nc_backward(nc_ctx* c, float* grads) {
+  if (!grads) return fail(NC_ERR_ARG, "grads is null");
+  CKS(check_ready(c));
+  if (!c->have_fwd) return fail(NC_ERR_STATE, "nc_backward needs a successful forward first");
+  return c->prec == NC_BF16
+             ? backward_impl<bf16>(c, static_cast<const bf16*>(c->params), c->tok, c->tgt, grads)
+             : backward_impl<float>(c, static_cast<const float*>(c->params), c->tok, c->tgt, grads);
+}
+
+nc_status nc_train_step_host(nc_ctx* c, const void* params, const int32_t* h_tok, const int32_t* h_tgt,
+                             float* grads, float* h_loss) {
+  if (!params || !h_tok || !h_tgt || !grads || !h_loss) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_ready(c));
+  int* dt = wsp<int>(c, c->off.tok);
+  int* dg = wsp<int>(c, c->off.tgt);
+  CK(cudaMemcpyAsync(dt, h_tok, (size_t)c->M * 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(dg, h_tgt, (size_t)c->M * 4, cudaMemcpyHostToDevice, c->stream));
+  float* dl = wsp<float>(c, c->off.loss);
+  CKS(forward_any(c, params, dt, dg, dl));
+  CKS(nc_backward(c, grads));
+  CK(cudaMemcpyAsync(h_loss, dl, sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+  return read_status(c);
+}
+
+nc_status nc_get_token_outputs(nc_ctx* c, float* d_lse, float* d_nll, int32_t* d_argmax) {
+  CKS(check_ready(c));
+  if (!c->have_fwd) return fail(NC_ERR_STATE, "no forward has run");
+  size_t n = (size_t)c->M * 4;
+  if (d_lse) CK(cudaMemcpyAsync(d_lse, c->ws + c->off.lse, n, cudaMemcpyDeviceToDevice, c->stream));
+  if (d_nll) CK(cudaMemcpyAsync(d_nll, c->ws + c->off.nll, n, cudaMemcpyDeviceToDevice, c->stream));
+  if (d_argmax) CK(cudaMemcpyAsync(d_argmax, c->ws + c->off.amax, n, cudaMemcpyDeviceToDevice, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_get_hidden(nc_ctx* c, void* d_hf) {
+  CKS(check_ready(c));
+  if (!c->have_fwd) return fail(NC_ERR_STATE, "no forward has run");
+  if (!d_hf) return fail(NC_ERR_ARG, "d_hf is null");
+  CK(cudaMemcpyAsync(d_hf, c->ws + c->off.hf, (size_t)c->M * c->d * c->esz, cudaMemcpyDeviceToDevice, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_sync(nc_ctx* c) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  if (c->prec < 0) return fail(NC_ERR_STATE, "nc_configure has not been called");
+  CK(cudaStreamSynchronize(c->stream));
+  return read_status(c);
+}
+
+const char* nc_last_error(const nc_ctx*) { return g_err.c_str(); }
+
+void nc_destroy(nc_ctx* c) {
+  if (!c) return;
+  if (c->rope_cos) cudaFree(c->rope_cos);
+  if (c->rope_sin) cudaFree(c->rope_sin);
+  if (c->status) cudaFree(c->status);
+  delete c;
+}
+
+// ---------------------------------------------------------------- op-level entry points
+
+nc_status nc_op_gemm(nc_ctx* c, int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                     const void* B, long long ldb, int b_kmajor, int epi, float alpha, float beta,
+                     void* C, long long ldc, void* C2, long long ldc2, const float* row_f,
+                     const int32_t* row_i) {
+  if (!c || c->prec < 0) return fail(NC_ERR_STATE, "context not configured");
+  if (M < 0 || N < 0 || K < 0) return fail(NC_ERR_ARG, "negative size");
+  if (epi < EPI_STORE || epi > EPI_CE_BWD) return fail(NC_ERR_ARG, "epilogue %d not available here", epi);
+  if (!A || !B || !C) return fail(NC_ERR_ARG, "null operand");
+  if ((epi == EPI_RELU2 || epi == EPI_RELU2_BWD) && !C2) return fail(NC_ERR_ARG, "epilogue needs C2");
+  if (epi == EPI_CE_BWD && (!row_f || !row_i)) return fail(NC_ERR_ARG, "epilogue needs row_f/row_i");
+  GemmArgs g = mk(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, epi, C, ldc, alpha, beta);
+  g.C2 = C2; g.ldc2 = ldc2; g.row_f = row_f; g.row_i = row_i;
+  return gemm(c, g);
+}
+
+nc_status nc_op_lmhead_ce_fwd(nc_ctx* c, const void* hf, const void* w_lm, const int32_t* tgt,
+                              float* lse, float* nll, int32_t* argmax) {
+  CKS(check_ready(c));
+  if (!hf || !w_lm || !tgt || !lse || !nll || !argmax) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  return c->prec == NC_BF16
+             ? lmhead_ce_forward<bf16>(c, (const bf16*)hf, (const bf16*)w_lm, tgt, c->M, lse, nll, argmax)
+             : lmhead_ce_forward<float>(c, (const float*)hf, (const float*)w_lm, tgt, c->M, lse, nll, argmax);
+}
+
+nc_status nc_op_lmhead_ce_bwd(nc_ctx* c, const void* hf, const void* w_lm, const int32_t* tgt,
+                              const float* lse, float* dhf, float* dw_lm) {
+  CKS(check_ready(c));
+  if (!hf || !w_lm || !tgt || !lse || !dhf || !dw_lm) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  float inv = 1.f / (float)c->M;
+  return c->prec == NC_BF16
+             ? lmhead_ce_backward<bf16>(c, (const bf16*)hf, (const bf16*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm)
+             : lmhead_ce_backward<float>(c, (const float*)hf, (const float*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm);
+}
+
+nc_status nc_op_attention_fwd(nc_ctx* c, const void* qkv, void* o, float* lse) {
+  CKS(check_ready(c));
+  if (!qkv || !o || !lse) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  if (c->prec == NC_BF16) CK(attn_fwd_simt<bf16>((const bf16*)qkv, (bf16*)o, lse, c->B, c->T, c->H, c->stream));
+  else CK(attn_fwd_simt<float>((const float*)qkv, (float*)o, lse, c->B, c->T, c->H, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_op_attention_bwd(nc_ctx* c, const void* qkv, const void* o, const void* dout,
+                              const float* lse, float* dqk, void* dqkv) {
+  CKS(check_ready(c));
+  if (!qkv || !o || !dout || !lse || !dqk || !dqkv) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  float* drow = wsp<float>(c, c->off.drow);
+  if (c->prec == NC_BF16) {
+    CK(attn_rowdot<bf16>((const bf16*)dout, (const bf16*)o, drow, c->B, c->T, c->H, c->stream));
+    CK(attn_bwd_simt<bf16>((const bf16*)qkv, (const bf16*)dout, lse, drow, dqk, (bf16*)dqkv, c->B, c->T, c->H, c->stream));
+  } else {
+    CK(attn_rowdot<float>((const float*)dout, (const float*)o, drow, c->B, c->T, c->H, c->stream));
+    CK(attn_bwd_simt<float>((const float*)qkv, (const float*)dout, lse, drow, dqk, (float*)dqkv, c->B, c->T, c->H, c->stream));
+  }
+  return NC_OK;
+}
+
+nc_status nc_op_qk_norm_rope_fwd(nc_ctx* c, void* qkv, float* rqk) {
+  CKS(check_ready(c));
+  if (!qkv || !rqk) return fail(NC_ERR_ARG, "null pointer argument");
+  if (c->prec == NC_BF16) CK(qk_norm_rope_fwd<bf16>((bf16*)qkv, rqk, c->rope_cos, c->rope_sin, c->M, c->T, c->H, c->stream));
+  else CK(qk_norm_rope_fwd<float>((float*)qkv, rqk, c->rope_cos, c->rope_sin, c->M, c->T, c->H, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_op_rmsnorm_fwd(nc_ctx* c, const float* x, void* y, float* r) {
+  CKS(check_ready(c));
+  if (!x || !y || !r) return fail(NC_ERR_ARG, "null pointer argument");
+  if (c->prec == NC_BF16) CK(rmsnorm_fwd<bf16>(x, (bf16*)y, r, c->M, c->d, c->stream));
+  else CK(rmsnorm_fwd<float>(x, (float*)y, r, c->M, c->d, c->stream));
+  return NC_OK;
+}
+
+}  // extern "C"

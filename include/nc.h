@@ -1,0 +1,150 @@
+/*
+ * nc.h -- C ABI of the nanochat pretraining step on one B300 (sm_103a).
+ *
+ * The step is the one the nanochat pages describe for pretraining: the
+ * depth-dialled decoder-only GPT (nanochat explainer, "Architecture Choices"
+ * and "How dimensions are derived") run forward, scored with the mean
+ * next-token cross-entropy (same page, "The Full Pipeline" / "Pretraining":
+ * given tokens 1..N predict N+1), and differentiated analytically w.r.t.
+ * every parameter.
+ *
+ * Model: untied token embedding wte[V,d]; `depth` pre-norm blocks, each
+ *   xn1 = rmsnorm(x); q,k,v = split(xn1 W_qkv^T);
+ *   q,k <- rope(rmsnorm_per_head(q,k)) (QK-norm + RoPE, half-split pairs,
+ *          angle pos * 10000^(-j/64));
+ *   o = causal softmax(q k^T / sqrt(128)) v;  x += o W_o^T;
+ *   xn2 = rmsnorm(x); x += relu(xn2 W_fc^T)^2 W_proj^T;
+ * then hf = rmsnorm(x), logits = hf lm_head^T. RMSNorm is parameter-free,
+ * y = z / sqrt(mean(z^2) + 1e-6). Loss = mean over all B*T positions of
+ * logsumexp(logits) - logit[target], in nats.
+ *
+ * Conventions shared by every call:
+ *  - Every call returns nc_status; no C++ exception crosses the ABI.
+ *    nc_last_error() gives a message for the calling thread's last failure.
+ *  - Device pointers are plain CUDA device addresses owned by the caller; the
+ *    library never frees them. The library itself allocates only a small
+ *    RoPE cos/sin table and a device status word (at nc_configure).
+ *  - All work is enqueued on the stream given to nc_configure (0 = legacy
+ *    default stream) and is asynchronous unless stated otherwise.
+ *  - Kernels never trap. A device-side failure (token id out of range, a
+ *    pipeline wait that exceeded its iteration limit) sets the status word;
+ *    the next synchronising call returns NC_ERR_DEVICE or NC_ERR_TIMEOUT.
+ */
+#ifndef NC_H
+#define NC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct nc_ctx nc_ctx;
+
+typedef enum {
+  NC_OK = 0,
+  NC_ERR_ARG = 1,         /* bad shape, null pointer, misaligned buffer */
+  NC_ERR_STATE = 2,       /* call out of order (e.g. backward before forward) */
+  NC_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the code) */
+  NC_ERR_TIMEOUT = 4,     /* a device pipeline wait exceeded its limit */
+  NC_ERR_DEVICE = 5,      /* device-side check failed (e.g. token id >= vocab) */
+  NC_ERR_UNSUPPORTED = 6  /* valid request this build does not implement */
+} nc_status;
+
+/* Precision modes for nc_configure. */
+enum {
+  NC_BF16 = 0,       /* bf16 params and stored activations, fp32 accumulate,
+                        tcgen05 tensor-core kernels */
+  NC_FP32_DEBUG = 1  /* fp32 params and activations, plain fp32 FMA kernels */
+};
+
+/* Create a context for one model shape. Host only; touches no GPU.
+ * depth >= 1; d_model == 128 * n_head (head_dim is fixed at 128, nanochat
+ * explainer "How dimensions are derived"); vocab % 128 == 0 and
+ * 128 <= vocab <= 2^20; seq_len >= 1. d_model = 64 * depth is the pages'
+ * rule but is not enforced, so that a depth-2 model of width 128 exists.
+ * On success *out owns the context (free with nc_destroy). */
+nc_status nc_create(int depth, int d_model, int n_head, int seq_len, int vocab, nc_ctx** out);
+
+/* Fix the batch size and precision and bind a CUDA stream (a cudaStream_t,
+ * may be NULL). Uses the current CUDA device. Allocates the RoPE table
+ * (fp32 [seq_len, 64], angles formed in float64 on the host) and the status
+ * word. NC_BF16 requires seq_len % 128 == 0 and d_model % 128 == 0.
+ * Can be called again to change batch or precision; the workspace must then
+ * be set again. */
+nc_status nc_configure(nc_ctx* ctx, int batch, int precision, void* cuda_stream);
+
+/* Number of parameters: 2*V*d + 12*depth*d^2. */
+size_t nc_param_count(const nc_ctx* ctx);
+
+/* Layout of the flat parameter (and gradient) vector, in elements.
+ * index 0 = wte[V,d]; for layer l, 1+4l = w_qkv[3d,d] (rows: q, then k,
+ * then v; row h*128+j is dim j of head h), 2+4l = w_o[d,d],
+ * 3+4l = w_fc[4d,d], 4+4l = w_proj[d,4d]; index 1+4*depth = lm_head[V,d].
+ * Matrices are row-major [out, in]; every offset is a multiple of 128. */
+nc_status nc_param_offset(const nc_ctx* ctx, int index, size_t* offset, int* rows, int* cols);
+
+/* Bytes of device workspace the configured step needs (activation stash
+ * for the backward pass plus scratch). 0 before nc_configure. */
+size_t nc_workspace_bytes(const nc_ctx* ctx);
+
+/* Hand the context a caller-owned device buffer of at least
+ * nc_workspace_bytes() bytes, 1024-byte aligned. The buffer must outlive
+ * every later call that uses it. */
+nc_status nc_set_workspace(nc_ctx* ctx, void* dev_ptr, size_t bytes);
+
+/* Forward pass + mean next-token cross-entropy.
+ * params: device, nc_param_count() elements, bf16 (NC_BF16) or fp32
+ *   (NC_FP32_DEBUG), layout of nc_param_offset.
+ * tokens, targets: device int32 [batch, seq_len] row-major, ids in
+ *   [0, vocab); an id out of range makes the step return NC_ERR_DEVICE.
+ * loss: HOST float*; the call synchronises the stream and writes the loss.
+ * The context keeps params/tokens/targets pointers for nc_backward: the
+ * caller must not change those buffers (or the workspace) in between. */
+nc_status nc_forward_loss(nc_ctx* ctx, const void* params, const int32_t* tokens,
+                          const int32_t* targets, float* loss);
+
+/* As nc_forward_loss but writes the loss to DEVICE memory d_loss (one
+ * float) and does not synchronise. */
+nc_status nc_forward_loss_async(nc_ctx* ctx, const void* params, const int32_t* tokens,
+                                const int32_t* targets, float* d_loss);
+
+/* Backward pass of the last forward: writes the gradient of the mean loss
+ * w.r.t. every parameter as fp32 into grads (device, nc_param_count()
+ * floats, same layout as params; overwritten, not accumulated). Rows of
+ * wte that no token uses get exactly 0. NC_ERR_STATE without a preceding
+ * successful forward. Asynchronous. */
+nc_status nc_backward(nc_ctx* ctx, float* grads);
+
+/* One training step from HOST token buffers: copies tokens and targets
+ * (host int32 [batch, seq_len], ideally pinned) to the device, runs the
+ * forward and backward on device-resident params/grads, and copies the loss
+ * back to *h_loss. Synchronises the stream. */
+nc_status nc_train_step_host(nc_ctx* ctx, const void* params, const int32_t* h_tokens,
+                             const int32_t* h_targets, float* grads, float* h_loss);
+
+/* Per-position results of the last forward, copied device-to-device:
+ * d_lse, d_nll: fp32 [batch*seq_len]; d_argmax: int32 [batch*seq_len]
+ * (lowest vocabulary index among ties). Any pointer may be NULL. */
+nc_status nc_get_token_outputs(nc_ctx* ctx, float* d_lse, float* d_nll, int32_t* d_argmax);
+
+/* Final hidden state of the last forward (the RMS-normalised input of
+ * lm_head), copied device-to-device into d_hf: elem [batch*seq_len, d_model]
+ * (bf16 in NC_BF16, fp32 in NC_FP32_DEBUG). */
+nc_status nc_get_hidden(nc_ctx* ctx, void* d_hf);
+
+/* Synchronise the stream and report a pending device-side failure. */
+nc_status nc_sync(nc_ctx* ctx);
+
+/* Message for the calling thread's last failing call ("" if none). */
+const char* nc_last_error(const nc_ctx* ctx);
+
+/* Free the context and what the library allocated. NULL is allowed. */
+void nc_destroy(nc_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NC_H */

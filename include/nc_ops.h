@@ -1,0 +1,89 @@
+/*
+ * nc_ops.h -- op-level entry points of the nanochat step (one call per step
+ * of the path), for parity tests and for callers that assemble their own
+ * step. All take a context that nc_configure has set up (its precision,
+ * stream, batch, shapes and RoPE table are used) and, where stated, its
+ * workspace for scratch. Element type ("elem") is bf16 for NC_BF16 and fp32
+ * for NC_FP32_DEBUG. Pointers are device pointers owned by the caller.
+ * Every call is asynchronous on the context's stream and returns nc_status
+ * (NC_ERR_STATE when the context is not configured or has no workspace).
+ * A call here invalidates the context's saved forward (nc_backward then
+ * returns NC_ERR_STATE until the next nc_forward_loss).
+ */
+#ifndef NC_OPS_H
+#define NC_OPS_H
+
+#include "nc.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Epilogue codes for nc_op_gemm. */
+enum {
+  NC_EPI_STORE = 0,      /* C (elem) = alpha * acc                                  */
+  NC_EPI_STORE_F32 = 1,  /* C (fp32) = alpha * acc + beta * C                       */
+  NC_EPI_RELU2 = 2,      /* C (elem) = u = alpha * acc ; C2 (elem) = max(u, 0)^2    */
+  NC_EPI_RELU2_BWD = 3,  /* C (elem) = alpha * acc * 2 * max(u, 0), u read from C2  */
+  NC_EPI_CE_BWD = 4      /* C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])  */
+};
+
+/* Linear-layer contraction of the step (the QKV, out-projection, MLP and
+ * lm_head matmuls and their backward products):
+ *   acc[m,n] = sum_k A(m,k) B(n,k), m < M, n < N, k < K,
+ *   A(m,k) = a_kmajor ? A[m*lda + k] : A[k*lda + m]   (elem)
+ *   B(n,k) = b_kmajor ? B[n*ldb + k] : B[k*ldb + n]   (elem)
+ * then the epilogue above writes C[m*ldc + n] (and C2[m*ldc2 + n]).
+ * The ReLU^2 epilogues follow the nanochat explainer's "ReLU^2 Sparsity";
+ * the CE_BWD epilogue forms softmax(logits) - onehot(target) of
+ * "Pretraining"'s cross-entropy. In NC_BF16 the operands' leading
+ * dimensions must be multiples of 8 elements and the base addresses 16-byte
+ * aligned (tensor-core path); NC_ERR_UNSUPPORTED otherwise. */
+nc_status nc_op_gemm(nc_ctx* ctx, int M, int N, int K, const void* A, long long lda, int a_kmajor,
+                     const void* B, long long ldb, int b_kmajor, int epi, float alpha, float beta,
+                     void* C, long long ldc, void* C2, long long ldc2, const float* row_f,
+                     const int32_t* row_i);
+
+/* Fused lm_head + softmax cross-entropy forward over M = batch*seq_len rows
+ * (nanochat explainer, "Pretraining": cross-entropy between the predicted
+ * logits and the next tokens). hf: elem [M, d]; w_lm: elem [V, d];
+ * tgt: int32 [M]. Outputs lse, nll: fp32 [M]; argmax: int32 [M] (lowest
+ * index among ties). The full [M, V] logits are never stored; scratch comes
+ * from the context's workspace. */
+nc_status nc_op_lmhead_ce_fwd(nc_ctx* ctx, const void* hf, const void* w_lm, const int32_t* tgt,
+                              float* lse, float* nll, int32_t* argmax);
+
+/* Backward of the mean cross-entropy w.r.t. hf and w_lm, recomputing the
+ * logits: g = (softmax - onehot(tgt)) / M; dhf = g w_lm (fp32 [M, d]);
+ * dw_lm = g^T hf (fp32 [V, d], overwritten). lse from nc_op_lmhead_ce_fwd. */
+nc_status nc_op_lmhead_ce_bwd(nc_ctx* ctx, const void* hf, const void* w_lm, const int32_t* tgt,
+                              const float* lse, float* dhf, float* dw_lm);
+
+/* Causal multi-head attention forward (nanochat explainer, "Multi-Head
+ * Attention (what nanochat uses)"), scale 1/sqrt(128).
+ * qkv: elem [B*T, 3d], columns q_hat | k_hat | v, head h at h*128 (q_hat,
+ * k_hat already QK-normed and rotated). o: elem [B*T, d]; lse: fp32 [B, H, T]. */
+nc_status nc_op_attention_fwd(nc_ctx* ctx, const void* qkv, void* o, float* lse);
+
+/* Attention backward. dout: elem [B*T, d]; lse from the forward.
+ * dqk: fp32 [B*T, 2d] receives dq_hat | dk_hat; dqkv: elem [B*T, 3d]
+ * receives dv in its v columns (q,k columns untouched). Scratch from the
+ * workspace. */
+nc_status nc_op_attention_bwd(nc_ctx* ctx, const void* qkv, const void* o, const void* dout,
+                              const float* lse, float* dqk, void* dqkv);
+
+/* QK-norm + RoPE in place on the q and k columns of qkv (elem [B*T, 3d]):
+ * per head, q <- rope(q / sqrt(mean(q^2) + 1e-6)), half-split pairs (j, j+64),
+ * angle pos * 10000^(-j/64) (nanochat explainer, "RoPE Intuition").
+ * rqk: fp32 [B*T, 2H], the per-head reciprocal RMS of q heads then k heads. */
+nc_status nc_op_qk_norm_rope_fwd(nc_ctx* ctx, void* qkv, float* rqk);
+
+/* Parameter-free RMSNorm of the fp32 residual stream x [B*T, d]:
+ * y (elem) = x * r, r (fp32 [B*T]) = 1/sqrt(mean(x^2) + 1e-6). */
+nc_status nc_op_rmsnorm_fwd(nc_ctx* ctx, const float* x, void* y, float* r);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NC_OPS_H */

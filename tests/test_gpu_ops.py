@@ -1,0 +1,270 @@
+"""Op-level parity: each step of the path through the C ABI against the
+oracle's piece (or the textbook routine the oracle uses for it), on seeded
+inputs that span several tiles and a ragged tail."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workload as W
+from gpu_util import load_nc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def nc():
+    return load_nc()
+
+
+def torch_of(a, prec, nc):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    return (t.to(torch.bfloat16) if prec == nc.NC_BF16 else t).cuda()
+
+
+def host(t):
+    import torch
+    return t.float().cpu().numpy() if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+
+def rounded(a, prec):
+    return W.round_bf16(a) if prec == 0 else np.asarray(a, dtype=np.float32)
+
+
+class Ctx:
+    def __init__(self, nc, depth, d, H, T, V, B, prec):
+        self.step = nc.Step(depth, d, H, T, V, B, prec)
+        self.ctx = self.step.ctx
+
+    def close(self):
+        self.step.close()
+
+
+def close_enough(got, ref, prec, rel_bf16=8e-3, rel_f32=2e-5):
+    ref = np.asarray(ref, dtype=np.float64)
+    scale = np.sqrt(np.mean(ref * ref)) + 1e-30
+    rel = rel_bf16 if prec == 0 else rel_f32
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    return np.all(err <= rel * np.abs(ref) + rel * scale), float((err / scale).max())
+
+
+# ---------------------------------------------------------------- GEMM
+
+M_, N_, K_ = 304, 520, 200  # 2 full 128-row tiles + 48, 2 full 256-col tiles + 8, 3 k-slices + 8
+
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("ak,bk", [(1, 1), (1, 0), (0, 0), (0, 1)], ids=["TN", "NN_b", "MN_ab", "MN_a"])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4], ids=["store", "store_f32", "relu2", "relu2_bwd", "ce_bwd"])
+def test_gemm_epilogues(nc, prec, ak, bk, epi):
+    import torch
+    rng = np.random.default_rng(100 + 10 * ak + bk + 3 * epi)
+    A = rounded(rng.standard_normal((M_, K_)) * 0.5, prec)
+    Bm = rounded(rng.standard_normal((N_, K_)) * 0.5, prec)
+    acc = A.astype(np.float64) @ Bm.astype(np.float64).T
+    alpha = 0.75
+    a_st = A if ak else np.ascontiguousarray(A.T)
+    b_st = Bm if bk else np.ascontiguousarray(Bm.T)
+    lda = K_ if ak else M_
+    ldb = K_ if bk else N_
+    c = Ctx(nc, 1, 128, 1, 128, 1024, 1, prec)
+    try:
+        dA, dB = torch_of(a_st, prec, nc), torch_of(b_st, prec, nc)
+        elem = torch.bfloat16 if prec == 0 else torch.float32
+        C2 = None
+        row_f = row_i = None
+        beta = 0.0
+        if epi == 1:
+            C0 = rng.standard_normal((M_, N_)).astype(np.float32)
+            C = torch.from_numpy(C0).cuda()
+            beta = 0.5
+            ref = alpha * acc + beta * C0
+        else:
+            C = torch.zeros((M_, N_), dtype=elem, device="cuda")
+        if epi == 0:
+            ref = alpha * acc
+        elif epi == 2:
+            C2 = torch.zeros((M_, N_), dtype=elem, device="cuda")
+            u = alpha * acc
+            ref = u
+            ref2 = np.square(np.maximum(u, 0))  # the kernel squares the fp32 u, then rounds
+        elif epi == 3:
+            u_in = rounded(rng.standard_normal((M_, N_)), prec)
+            C2 = torch_of(u_in, prec, nc)
+            ref = alpha * acc * 2 * np.maximum(u_in, 0)
+        elif epi == 4:
+            lse = np.log(np.sum(np.exp(alpha * acc), axis=1)).astype(np.float32)
+            tgt = rng.integers(0, N_, M_).astype(np.int32)
+            row_f = torch.from_numpy(lse).cuda()
+            row_i = torch.from_numpy(tgt).cuda()
+            ref = np.exp(alpha * acc - lse[:, None].astype(np.float64))
+            ref[np.arange(M_), tgt] -= 1.0
+        nc.nc_op_gemm(c.ctx, M_, N_, K_, dA.data_ptr(), lda, ak, dB.data_ptr(), ldb, bk, epi, alpha, beta,
+                      C.data_ptr(), N_, C2.data_ptr() if C2 is not None else None, N_ if C2 is not None else 0,
+                      row_f.data_ptr() if row_f is not None else None,
+                      row_i.data_ptr() if row_i is not None else None)
+        nc.nc_sync(c.ctx)
+        ok, err = close_enough(host(C), ref, prec if epi != 1 else 1, rel_f32=5e-5 if prec == 0 else 2e-5)
+        assert ok, err
+        if epi == 2:
+            ok, err = close_enough(host(C2), ref2, prec)
+            assert ok, err
+            assert np.all(host(C2)[host(C) <= 0] == 0.0)  # exact zeros of ReLU^2
+    finally:
+        c.close()
+
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+def test_gemm_degenerate_sizes(nc, prec):
+    import torch
+    c = Ctx(nc, 1, 128, 1, 128, 1024, 1, prec)
+    try:
+        elem = torch.bfloat16 if prec == 0 else torch.float32
+        A = torch.ones((64, 64), dtype=elem, device="cuda")
+        C = torch.full((64, 64), 7.0, dtype=torch.float32, device="cuda")
+        # K = 0: the product is empty, C = alpha*0 + beta*C
+        nc.nc_op_gemm(c.ctx, 64, 64, 0, A.data_ptr(), 64, 1, A.data_ptr(), 64, 1, 1, 1.0, 0.5, C.data_ptr(), 64)
+        # M = 0 and N = 0: nothing is written
+        nc.nc_op_gemm(c.ctx, 0, 64, 64, A.data_ptr(), 64, 1, A.data_ptr(), 64, 1, 1, 1.0, 0.0, C.data_ptr(), 64)
+        nc.nc_op_gemm(c.ctx, 64, 0, 64, A.data_ptr(), 64, 1, A.data_ptr(), 64, 1, 1, 1.0, 0.0, C.data_ptr(), 64)
+        nc.nc_sync(c.ctx)
+        assert np.all(C.cpu().numpy() == 3.5)
+    finally:
+        c.close()
+
+
+# ---------------------------------------------------------------- attention
+
+def _qkv(rng, B, T, H, prec):
+    D = 128
+    q = rng.standard_normal((B, T, H, D))
+    k = rng.standard_normal((B, T, H, D))
+    q = q / np.sqrt(np.mean(q * q, -1, keepdims=True))
+    k = k / np.sqrt(np.mean(k * k, -1, keepdims=True))
+    v = rng.standard_normal((B, T, H, D))
+    qkv = np.concatenate([q.reshape(B, T, -1), k.reshape(B, T, -1), v.reshape(B, T, -1)], -1)
+    return rounded(qkv, prec).reshape(B * T, 3 * H * D)
+
+
+@pytest.mark.parametrize("prec,T", [(0, 256), (1, 100)], ids=["bf16_T256", "fp32_T100"])
+def test_attention_fwd_bwd(nc, prec, T):
+    import torch
+    B, H, D = 2, 2, 128
+    d = H * D
+    rng = np.random.default_rng(7)
+    qkv = _qkv(rng, B, T, H, prec)
+    dout = rounded(rng.standard_normal((B * T, d)), prec)
+    c = Ctx(nc, 1, d, H, T, 1024, B, prec)
+    try:
+        elem = torch.bfloat16 if prec == 0 else torch.float32
+        dq = torch_of(qkv, prec, nc)
+        o = torch.zeros((B * T, d), dtype=elem, device="cuda")
+        lse = torch.zeros((B, H, T), dtype=torch.float32, device="cuda")
+        nc.nc_op_attention_fwd(c.ctx, dq.data_ptr(), o.data_ptr(), lse.data_ptr())
+        ddo = torch_of(dout, prec, nc)
+        dqk = torch.zeros((B * T, 2 * d), dtype=torch.float32, device="cuda")
+        dqkv = torch.zeros((B * T, 3 * d), dtype=elem, device="cuda")
+        nc.nc_op_attention_bwd(c.ctx, dq.data_ptr(), o.data_ptr(), ddo.data_ptr(), lse.data_ptr(),
+                               dqk.data_ptr(), dqkv.data_ptr())
+        nc.nc_sync(c.ctx)
+        o_h, lse_h, dqk_h, dqkv_h = host(o), lse.cpu().numpy(), dqk.cpu().numpy(), host(dqkv)
+        tol = 1e-2 if prec == 0 else 1e-5
+        for b in range(B):
+            x = qkv.reshape(B, T, 3, H, D)[b].astype(np.float64)
+            q, k, v = x[:, 0], x[:, 1], x[:, 2]
+            o_ref, lse_ref = oracle.causal_attention(q, k, v)
+            ob = o_h.reshape(B, T, H, D)[b]
+            assert np.linalg.norm(ob - o_ref) <= tol * np.linalg.norm(o_ref)
+            np.testing.assert_allclose(lse_h[b], lse_ref, atol=tol)
+            # the backward is checked with the forward output the kernel produced
+            g = dout.reshape(B, T, H, D)[b].astype(np.float64)
+            dq_r, dk_r, dv_r = oracle.causal_attention_backward(q, k, v, g)
+            got = dqk_h.reshape(B, T, 2, H, D)[b]
+            for gg, rr in ((got[:, 0], dq_r), (got[:, 1], dk_r), (dqkv_h.reshape(B, T, 3, H, D)[b][:, 2], dv_r)):
+                assert np.linalg.norm(gg - rr) <= 2 * tol * np.linalg.norm(rr)
+        assert np.all(dqkv_h.reshape(B, T, 3, d)[:, :, :2] == 0)  # q,k columns untouched
+    finally:
+        c.close()
+
+
+# ---------------------------------------------------------------- lm_head + CE
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+def test_lmhead_cross_entropy(nc, prec):
+    import torch
+    d, H, T, B, V = 256, 2, 128, 3, 4224  # 16.5 vocabulary tiles of 256
+    M = B * T
+    rng = np.random.default_rng(11)
+    hf = rng.standard_normal((M, d))
+    hf = rounded(hf / np.sqrt(np.mean(hf * hf, -1, keepdims=True)), prec)
+    wl = rounded(rng.standard_normal((V, d)) * 0.05, prec)
+    tgt = rng.integers(0, V, M).astype(np.int32)
+    c = Ctx(nc, 1, d, H, T, V, B, prec)
+    try:
+        dh, dw, dt = torch_of(hf, prec, nc), torch_of(wl, prec, nc), torch.from_numpy(tgt).cuda()
+        lse = torch.zeros(M, dtype=torch.float32, device="cuda")
+        nll = torch.zeros(M, dtype=torch.float32, device="cuda")
+        am = torch.zeros(M, dtype=torch.int32, device="cuda")
+        nc.nc_op_lmhead_ce_fwd(c.ctx, dh.data_ptr(), dw.data_ptr(), dt.data_ptr(), lse.data_ptr(),
+                               nll.data_ptr(), am.data_ptr())
+        dhf = torch.zeros((M, d), dtype=torch.float32, device="cuda")
+        dwl = torch.full((V, d), 3.0, dtype=torch.float32, device="cuda")  # must be overwritten
+        nc.nc_op_lmhead_ce_bwd(c.ctx, dh.data_ptr(), dw.data_ptr(), dt.data_ptr(), lse.data_ptr(),
+                               dhf.data_ptr(), dwl.data_ptr())
+        nc.nc_sync(c.ctx)
+        h64, w64 = hf.astype(np.float64), wl.astype(np.float64)
+        lse_r, nll_r, am_r = oracle.cross_entropy_rows(h64, w64, tgt)
+        tol = 1e-3 if prec == 0 else 1e-5
+        np.testing.assert_allclose(lse.cpu().numpy(), lse_r, atol=tol)
+        np.testing.assert_allclose(nll.cpu().numpy(), nll_r, atol=tol)
+        lg = h64 @ w64.T
+        top2 = np.partition(lg, -2, axis=1)[:, -2:]
+        sure = (top2[:, 1] - top2[:, 0]) > 1e-4
+        np.testing.assert_array_equal(am.cpu().numpy()[sure], am_r[sure])
+        dhf_r, dw_r = oracle.cross_entropy_backward(h64, w64, tgt, lse_r)
+        rel = 2e-2 if prec == 0 else 1e-5
+        assert np.linalg.norm(dhf.cpu().numpy() - dhf_r) <= rel * np.linalg.norm(dhf_r)
+        assert np.linalg.norm(dwl.cpu().numpy() - dw_r) <= rel * np.linalg.norm(dw_r)
+    finally:
+        c.close()
+
+
+# ---------------------------------------------------------------- norms
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+def test_qk_norm_rope_and_rmsnorm(nc, prec):
+    import torch
+    B, T, H = 2, 256, 3
+    d, D = H * 128, 128
+    rng = np.random.default_rng(5)
+    qkv = rounded(rng.standard_normal((B * T, 3 * d)) * 0.3, prec)
+    x = rng.standard_normal((B * T, d)).astype(np.float32) * 2
+    c = Ctx(nc, 1, d, H, T, 1024, B, prec)
+    try:
+        dq = torch_of(qkv, prec, nc)
+        rqk = torch.zeros((B * T, 2 * H), dtype=torch.float32, device="cuda")
+        nc.nc_op_qk_norm_rope_fwd(c.ctx, dq.data_ptr(), rqk.data_ptr())
+        dx = torch.from_numpy(x).cuda()
+        elem = torch.bfloat16 if prec == 0 else torch.float32
+        y = torch.zeros((B * T, d), dtype=elem, device="cuda")
+        r = torch.zeros(B * T, dtype=torch.float32, device="cuda")
+        nc.nc_op_rmsnorm_fwd(c.ctx, dx.data_ptr(), y.data_ptr(), r.data_ptr())
+        nc.nc_sync(c.ctx)
+        cos, sin = oracle.rope_angles(T)
+        got = host(dq).reshape(B, T, 3, H, D)
+        src = qkv.reshape(B, T, 3, H, D).astype(np.float64)
+        for which in (0, 1):
+            for b in range(B):
+                n, rr = oracle.rmsnorm(src[b, :, which])
+                ref = oracle.rope(n, cos, sin)
+                ok, err = close_enough(got[b, :, which], ref, prec)
+                assert ok, err
+                np.testing.assert_allclose(rqk.cpu().numpy().reshape(B, T, 2, H)[b, :, which], rr[..., 0], rtol=1e-5)
+        np.testing.assert_array_equal(got[:, :, 2], qkv.reshape(B, T, 3, H, D)[:, :, 2])  # v untouched
+        yn, rn = oracle.rmsnorm(x.astype(np.float64))
+        ok, err = close_enough(host(y), yn, prec)
+        assert ok, err
+        np.testing.assert_allclose(r.cpu().numpy(), rn[:, 0], rtol=1e-5)
+    finally:
+        c.close()
