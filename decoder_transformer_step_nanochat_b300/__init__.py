@@ -20,6 +20,11 @@ LIB_PATH = os.path.join(HERE, "libnc.so")
 NC_BF16 = 0
 NC_FP32_DEBUG = 1
 
+NC_FAM_GEMM = 0
+NC_FAM_ATTN_FWD = 1
+NC_FAM_ATTN_BWD = 2
+NC_FAM_ROWS = 3
+
 NC_EPI_STORE = 0
 NC_EPI_STORE_F32 = 1
 NC_EPI_RELU2 = 2
@@ -58,6 +63,11 @@ _SIGS = {
     "nc_get_token_outputs": (_I, [_P, _P, _P, _P]),
     "nc_get_hidden": (_I, [_P, _P]),
     "nc_sync": (_I, [_P]),
+    "nc_launch_count": (ctypes.c_ulonglong, [_P]),
+    "nc_profile_enable": (_I, [_P, _I]),
+    "nc_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_LL),
+                            ctypes.POINTER(ctypes.c_double)]),
+    "nc_profile_reset": (_I, [_P]),
     "nc_last_error": (ctypes.c_char_p, [_P]),
     "nc_destroy": (None, [_P]),
     "nc_op_gemm": (_I, [_P, _I, _I, _I, _P, _LL, _I, _P, _LL, _I, _I, _F, _F, _P, _LL, _P, _LL, _P, _P]),
@@ -152,6 +162,25 @@ def nc_get_hidden(ctx, d_hf):
 
 def nc_sync(ctx):
     _check(lib().nc_sync(ctx), ctx)
+
+
+def nc_launch_count(ctx) -> int:
+    return int(lib().nc_launch_count(ctx))
+
+
+def nc_profile_enable(ctx, enable):
+    _check(lib().nc_profile_enable(ctx, 1 if enable else 0), ctx)
+
+
+def nc_profile_read(ctx, family):
+    """(device ms, launches, algorithmic work) summed over the recorded launches."""
+    ms, n, w = ctypes.c_double(), _LL(), ctypes.c_double()
+    _check(lib().nc_profile_read(ctx, family, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(w)), ctx)
+    return float(ms.value), int(n.value), float(w.value)
+
+
+def nc_profile_reset(ctx):
+    _check(lib().nc_profile_reset(ctx), ctx)
 
 
 def nc_last_error(ctx=None) -> str:

@@ -77,6 +77,13 @@ struct nc_ctx {
     size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
     size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt;
   } off{};
+  // launch accounting and optional per-family event timing
+  unsigned long long launches = 0;
+  bool prof = false;
+  struct Rec { cudaEvent_t a, b; int fam; double work; };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> pool;
+  size_t pool_next = 0;
   // last forward
   const void* params = nullptr;
   const int* tok = nullptr;
@@ -88,6 +95,47 @@ namespace {
 
 template <typename P>
 P* wsp(nc_ctx* c, size_t off) { return reinterpret_cast<P*>(c->ws + off); }
+
+// ------------------------------------------------------------------ accounting
+
+nc_status next_event(nc_ctx* c, cudaEvent_t* ev) {
+  if (c->pool_next == c->pool.size()) {
+    cudaEvent_t e;
+    CK(cudaEventCreate(&e));
+    c->pool.push_back(e);
+  }
+  *ev = c->pool[c->pool_next++];
+  return NC_OK;
+}
+
+nc_status prof_begin(nc_ctx* c, cudaEvent_t* a) {
+  if (!c->prof) return NC_OK;
+  CKS(next_event(c, a));
+  CK(cudaEventRecord(*a, c->stream));
+  return NC_OK;
+}
+
+nc_status prof_end(nc_ctx* c, cudaEvent_t a, int fam, double work, int n) {
+  c->launches += (unsigned long long)n;
+  if (!c->prof) return NC_OK;
+  cudaEvent_t b;
+  CKS(next_event(c, &b));
+  CK(cudaEventRecord(b, c->stream));
+  c->recs.push_back({a, b, fam, work});
+  return NC_OK;
+}
+
+// Launch `expr` (a launcher returning cudaError_t that starts `n` kernels),
+// counting it and, when profiling, timing it under family `fam` with
+// algorithmic work `work` (FLOPs or bytes).
+#define KL(fam, work, n, expr)                                                                  \
+  do {                                                                                          \
+    cudaEvent_t ev_a_ = nullptr;                                                                \
+    CKS(prof_begin(c, &ev_a_));                                                                 \
+    cudaError_t e_ = (expr);                                                                    \
+    if (e_ != cudaSuccess) return fail(NC_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_));  \
+    CKS(prof_end(c, ev_a_, (fam), (double)(work), (n)));                                        \
+  } while (0)
 
 size_t param_offset(const nc_ctx* c, int index, int* rows, int* cols) {
   size_t d = c->d, V = c->V, F = c->F;
@@ -175,6 +223,8 @@ nc_status read_status(nc_ctx* c) {
 nc_status gemm(nc_ctx* c, GemmArgs g) {
   g.status = c->status;
   cudaError_t e;
+  cudaEvent_t ev_a = nullptr;
+  CKS(prof_begin(c, &ev_a));
   if (c->prec == NC_FP32_DEBUG) {
     e = gemm_simt<float>(g, c->stream);
   } else if (c->use_tc) {
@@ -185,7 +235,8 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
     e = gemm_simt<bf16>(g, c->stream);
   }
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm M=%d N=%d K=%d epi=%d: %s", g.M, g.N, g.K, g.epi, cudaGetErrorString(e));
-  return NC_OK;
+  int n = (g.M > 0 && g.N > 0) ? 1 : 0;
+  return prof_end(c, ev_a, NC_FAM_GEMM, 2.0 * g.M * g.N * (double)g.K, n);
 }
 
 GemmArgs mk(int M, int N, int K, const void* A, long long lda, int ak, const void* B, long long ldb,
@@ -196,6 +247,12 @@ GemmArgs mk(int M, int N, int K, const void* A, long long lda, int ak, const voi
   g.B = B; g.ldb = ldb; g.b_kmajor = bk;
   g.epi = epi; g.C = C; g.ldc = ldc; g.alpha = alpha; g.beta = beta;
   return g;
+}
+
+// Algorithmic FLOPs of one causal attention forward over the configured
+// batch: QK^T and PV over the lower triangle, 2*D*T*(T+1) per (b, h).
+double attn_fwd_flops(const nc_ctx* c) {
+  return 2.0 * kHeadDim * (double)c->T * (c->T + 1) * c->B * c->H;
 }
 
 // ------------------------------------------------------------------ step pieces
@@ -212,14 +269,16 @@ nc_status lmhead_ce_forward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt
     g.p_arg = wsp<int>(c, c->off.parg);
     g.p_tgt = wsp<float>(c, c->off.ptgt);
     CKS(gemm(c, g));
-    CK(ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, c->ce_tiles, lse, nll, amax, M, c->stream));
+    KL(NC_FAM_ROWS, 12.0 * c->ce_tiles * M + 16.0 * M, 1,
+       ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, c->ce_tiles, lse, nll, amax, M, c->stream));
     return NC_OK;
   }
   float* logits = wsp<float>(c, c->off.chunk);
   for (int r0 = 0; r0 < M; r0 += c->ce_rows) {
     int rows = M - r0 < c->ce_rows ? M - r0 : c->ce_rows;
     CKS(gemm(c, mk(rows, V, d, hf + (size_t)r0 * d, d, 1, wlm, d, 1, EPI_STORE_F32, logits, V)));
-    CK(ce_rows_from_logits(logits, tgt + r0, lse + r0, nll + r0, amax + r0, rows, V, c->status, c->stream));
+    KL(NC_FAM_ROWS, 8.0 * rows * V, rows > 0 ? 1 : 0,
+       ce_rows_from_logits(logits, tgt + r0, lse + r0, nll + r0, amax + r0, rows, V, c->status, c->stream));
   }
   return NC_OK;
 }
@@ -247,11 +306,11 @@ template <typename T>
 nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* d_loss) {
   int M = c->M, d = c->d, H = c->H, F = c->F, V = c->V, Tn = c->T;
   cudaStream_t s = c->stream;
-  CK(check_ids(tok, M, V, c->status, s));
-  CK(check_ids(tgt, M, V, c->status, s));
+  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tok, M, V, c->status, s));
+  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tgt, M, V, c->status, s));
   float* x = wsp<float>(c, c->off.x);
   int rows, cols;
-  CK(embed_fwd<T>(tok, P, x, M, d, V, c->status, s));
+  KL(NC_FAM_ROWS, (double)M * d * (sizeof(T) + 4) + 4.0 * M, 1, embed_fwd<T>(tok, P, x, M, d, V, c->status, s));
   for (int l = 0; l < c->L; ++l) {
     size_t lb = (size_t)l * c->off.layer_stride;
     T* xn1 = wsp<T>(c, lb + c->off.xn1);
@@ -269,12 +328,12 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
     const T* Wfc = P + param_offset(c, 3 + 4 * l, &rows, &cols);
     const T* Wproj = P + param_offset(c, 4 + 4 * l, &rows, &cols);
 
-    CK(rmsnorm_fwd<T>(x, xn1, r1, M, d, s));
+    KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn1, r1, M, d, s));
     CKS(gemm(c, mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_STORE, qkv, 3 * d)));
-    CK(qk_norm_rope_fwd<T>(qkv, rqk, c->rope_cos, c->rope_sin, M, Tn, H, s));
-    CK(attn_fwd_simt<T>(qkv, o, lse_att, c->B, Tn, H, s));
+    KL(NC_FAM_ROWS, 4.0 * M * d * sizeof(T) + 8.0 * M * H, 1, qk_norm_rope_fwd<T>(qkv, rqk, c->rope_cos, c->rope_sin, M, Tn, H, s));
+    KL(NC_FAM_ATTN_FWD, attn_fwd_flops(c), 1, attn_fwd_simt<T>(qkv, o, lse_att, c->B, Tn, H, s));
     CKS(gemm(c, mk(M, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
-    CK(rmsnorm_fwd<T>(x, xn2, r2, M, d, s));
+    KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn2, r2, M, d, s));
     GemmArgs up = mk(M, F, d, xn2, d, 1, Wfc, d, 1, EPI_RELU2, u, F);
     up.C2 = a; up.ldc2 = F;
     CKS(gemm(c, up));
@@ -282,11 +341,11 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
   }
   T* hf = wsp<T>(c, c->off.hf);
   float* rf = wsp<float>(c, c->off.rf);
-  CK(rmsnorm_fwd<T>(x, hf, rf, M, d, s));
+  KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, hf, rf, M, d, s));
   const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
   CKS(lmhead_ce_forward<T>(c, hf, Wlm, tgt, M, wsp<float>(c, c->off.lse), wsp<float>(c, c->off.nll),
                            wsp<int>(c, c->off.amax)));
-  CK(mean_loss(wsp<float>(c, c->off.nll), M, d_loss, s));
+  KL(NC_FAM_ROWS, 4.0 * M, 1, mean_loss(wsp<float>(c, c->off.nll), M, d_loss, s));
   return NC_OK;
 }
 
@@ -306,7 +365,7 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
   const T* hf = wsp<T>(c, c->off.hf);
   size_t o_lm = param_offset(c, 1 + 4 * c->L, &rows, &cols);
   CKS(lmhead_ce_backward<T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, 1.f / (float)M, dy, G + o_lm));
-  CK(rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
+  KL(NC_FAM_ROWS, (double)M * d * (8 + 2 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
   for (int l = c->L - 1; l >= 0; --l) {
     size_t lb = (size_t)l * c->off.layer_stride;
     const T* xn1 = wsp<T>(c, lb + c->off.xn1);
@@ -330,19 +389,19 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     CKS(gemm(c, g1));
     CKS(gemm(c, mk(F, d, M, du, F, 0, xn2, d, 0, EPI_STORE_F32, G + of, d)));
     CKS(gemm(c, mk(M, d, F, du, F, 1, P + of, d, 0, EPI_STORE_F32, dy, d)));
-    CK(rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
+    KL(NC_FAM_ROWS, (double)M * d * (12 + 2 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
     // attention: x += attn(xn1) Wo^T
     CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
     CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
-    CK(attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s));
-    CK(attn_bwd_simt<T>(qkv, dout, lse_att, drow, dqk, dqkv, c->B, Tn, H, s));
-    CK(qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s));
+    KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + 4.0 * M * H, 1, attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s));
+    KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), 2, attn_bwd_simt<T>(qkv, dout, lse_att, drow, dqk, dqkv, c->B, Tn, H, s));
+    KL(NC_FAM_ROWS, 2.0 * M * d * (4 + 2 * sizeof(T)) + 8.0 * M * H, 1, qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s));
     CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d)));
     CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, EPI_STORE_F32, dy, d)));
-    CK(rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
+    KL(NC_FAM_ROWS, (double)M * d * (12 + 2 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
   }
   CK(cudaMemsetAsync(G, 0, (size_t)V * d * sizeof(float), s));
-  CK(embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s));
+  KL(NC_FAM_ROWS, 8.0 * M * d + 4.0 * M, 1, embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s));
   return NC_OK;
 }
 
@@ -511,10 +570,47 @@ nc_status nc_sync(nc_ctx* c) {
   return read_status(c);
 }
 
+unsigned long long nc_launch_count(const nc_ctx* c) { return c ? c->launches : 0; }
+
+nc_status nc_profile_enable(nc_ctx* c, int enable) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  c->prof = enable != 0;
+  c->recs.clear();
+  c->pool_next = 0;
+  return NC_OK;
+}
+
+nc_status nc_profile_read(nc_ctx* c, int family, double* ms, long long* launches, double* work) {
+  if (!c || !ms || !launches || !work) return fail(NC_ERR_ARG, "null argument");
+  if (family < 0 || family >= NC_FAM_COUNT) return fail(NC_ERR_ARG, "family %d unknown", family);
+  CK(cudaStreamSynchronize(c->stream));
+  double t = 0, w = 0;
+  long long n = 0;
+  for (auto& r : c->recs) {
+    if (r.fam != family) continue;
+    float x = 0.f;
+    CK(cudaEventElapsedTime(&x, r.a, r.b));
+    t += x;
+    w += r.work;
+    ++n;
+  }
+  *ms = t; *launches = n; *work = w;
+  return NC_OK;
+}
+
+nc_status nc_profile_reset(nc_ctx* c) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  CK(cudaStreamSynchronize(c->stream));
+  c->recs.clear();
+  c->pool_next = 0;
+  return NC_OK;
+}
+
 const char* nc_last_error(const nc_ctx*) { return g_err.c_str(); }
 
 void nc_destroy(nc_ctx* c) {
   if (!c) return;
+  for (auto e : c->pool) cudaEventDestroy(e);
   if (c->rope_cos) cudaFree(c->rope_cos);
   if (c->rope_sin) cudaFree(c->rope_sin);
   if (c->status) cudaFree(c->status);

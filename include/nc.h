@@ -137,6 +137,30 @@ nc_status nc_get_hidden(nc_ctx* ctx, void* d_hf);
 /* Synchronise the stream and report a pending device-side failure. */
 nc_status nc_sync(nc_ctx* ctx);
 
+/* ---- measurement ----
+ * Kernel families for nc_profile_read. */
+enum {
+  NC_FAM_GEMM = 0,      /* tensor-core (or fp32 debug) GEMMs; work = 2*M*N*K FLOPs */
+  NC_FAM_ATTN_FWD = 1,  /* causal attention forward; work = 2*128*T*(T+1)*B*H FLOPs */
+  NC_FAM_ATTN_BWD = 2,  /* attention backward; work = 2x the forward's FLOPs */
+  NC_FAM_ROWS = 3,      /* norms, embedding, QK-norm/RoPE, CE reductions; work = bytes */
+  NC_FAM_COUNT = 4
+};
+
+/* Number of kernels the context has launched since nc_create. */
+unsigned long long nc_launch_count(const nc_ctx* ctx);
+
+/* Turn per-launch CUDA-event timing on (1) or off (0) and clear the record.
+ * With it on, every launch is bracketed by events on the context's stream. */
+nc_status nc_profile_enable(nc_ctx* ctx, int enable);
+
+/* Synchronise and sum, over the launches recorded since the last reset, the
+ * device time (ms), the number of launches and their algorithmic work. */
+nc_status nc_profile_read(nc_ctx* ctx, int family, double* ms, long long* launches, double* work);
+
+/* Synchronise and clear the recorded launches (profiling stays as set). */
+nc_status nc_profile_reset(nc_ctx* ctx);
+
 /* Message for the calling thread's last failing call ("" if none). */
 const char* nc_last_error(const nc_ctx* ctx);
 

@@ -29,13 +29,14 @@ def declared_functions():
             continue
         src = open(os.path.join(inc, f)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*(nc_[a-z0-9_]+)\s*\(", src, flags=re.M)
+        names += re.findall(r"^\s*(?:[A-Za-z_]\w*[\s\*]+)+(nc_[a-z0-9_]+)\s*\(", src, flags=re.M)
     return sorted(set(names))
 
 
 def test_library_exports_every_declared_symbol(nc):
     names = declared_functions()
     assert "nc_create" in names and "nc_forward_loss" in names and "nc_backward" in names
+    assert "nc_launch_count" in names and "nc_last_error" in names
     L = ctypes.CDLL(nc.LIB_PATH)
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing

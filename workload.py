@@ -18,8 +18,8 @@ n_head = d_model / 128, head_dim 128, FFN width 4 * d_model; vocabulary
 The tiny workload breaks the 64*depth rule on purpose (depth 2, width 128)
 so that a single 128-wide head exists.
 
-Parameter recipe: numpy Generator(PCG64(seed)) standard normals, drawn in the
-order of the flat parameter layout, scaled by 0.02 (the tiny workload scales
+Parameter recipe: numpy Generator(PCG64(seed)) float32 standard normals,
+drawn in the order of the flat parameter layout, scaled by 0.02 (the tiny workload scales
 its lm_head block by 0.001 instead). bf16 workloads round every parameter to
 bf16 (round to nearest even) and both sides read the rounded values.
 
@@ -100,11 +100,16 @@ def n_params(w: Workload) -> int:
 
 
 def round_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even), as float32."""
+    """Round finite float32 values to the nearest bf16 (ties to even), as float32."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    out = np.empty_like(x)
+    xf, of = x.reshape(-1), out.reshape(-1)
+    step = 1 << 24
+    for s in range(0, xf.size, step):
+        u = xf[s:s + step].view(np.uint32)
+        r = u + (np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1)))
+        of[s:s + step] = (r & np.uint32(0xFFFF0000)).view(np.float32)
+    return out
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -123,11 +128,11 @@ def make_params(w: Workload, seed: int = 0) -> np.ndarray:
         n = r * c
         std = w.lm_head_std if name == "lm_head" else w.std
         blk = out[off:off + n]
-        # draw in slabs to bound the float64 temporary
         step = 1 << 24
         for s in range(0, n, step):
             e = min(n, s + step)
-            blk[s:e] = rng.standard_normal(e - s) * std
+            rng.standard_normal(e - s, dtype=np.float32, out=blk[s:e])
+            blk[s:e] *= np.float32(std)
         off += n
     if w.dtype == "bf16":
         out = round_bf16(out)
