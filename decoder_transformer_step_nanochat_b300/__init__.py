@@ -77,6 +77,7 @@ _SIGS = {
     "nc_op_attention_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "nc_op_qk_norm_rope_fwd": (_I, [_P, _P, _P]),
     "nc_op_rmsnorm_fwd": (_I, [_P, _P, _P, _P]),
+    "nc_lmhead_ce_fwd_static": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
 }
 
 
@@ -220,6 +221,11 @@ def nc_op_qk_norm_rope_fwd(ctx, qkv, rqk):
 
 def nc_op_rmsnorm_fwd(ctx, x, y, r):
     _check(lib().nc_op_rmsnorm_fwd(ctx, x, y, r), ctx)
+
+
+def nc_lmhead_ce_fwd_static(hf, w_lm, tgt, M, d, V, lse, nll, argmax, d_status=None, stream=None):
+    """Allocation-free lm_head + cross-entropy forward (static device scratch)."""
+    _check(lib().nc_lmhead_ce_fwd_static(hf, w_lm, tgt, M, d, V, lse, nll, argmax, d_status, stream))
 
 
 # ------------------------------------------------------------------ convenience

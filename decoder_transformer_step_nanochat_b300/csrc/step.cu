@@ -55,6 +55,14 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 }  // namespace
 
+namespace nc {
+// Record a message for nc_last_error from other translation units.
+nc_status set_last_error(nc_status st, const char* msg) {
+  g_err = msg;
+  return st;
+}
+}  // namespace nc
+
 struct nc_ctx {
   // model shape
   int L = 0, d = 0, H = 0, T = 0, V = 0, F = 0;

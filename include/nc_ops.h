@@ -82,6 +82,29 @@ nc_status nc_op_qk_norm_rope_fwd(nc_ctx* ctx, void* qkv, float* rqk);
  * y (elem) = x * r, r (fp32 [B*T]) = 1/sqrt(mean(x^2) + 1e-6). */
 nc_status nc_op_rmsnorm_fwd(nc_ctx* ctx, const float* x, void* y, float* r);
 
+/* Fused lm_head + cross-entropy forward that allocates no device memory.
+ * The nanochat pages have no counterpart of this call; it exists for callers
+ * that must not call cudaMalloc where they need the loss (code inside another
+ * framework's memory pool or allocation budget). It computes what
+ * nc_op_lmhead_ce_fwd computes, in bf16 only, with no context:
+ * hf: bf16 [M, d]; w_lm: bf16 [V, d] (both 16-byte aligned); tgt: int32 [M];
+ * lse, nll: fp32 [M]; argmax: int32 [M] (lowest index among ties);
+ * d_status: optional device int32, set to 0, or to 1 if a target id is out of
+ * range, or to 2 if a pipeline wait timed out; cuda_stream: a cudaStream_t
+ * (NULL = legacy default stream). d and V must be multiples of 8.
+ * Scratch is a 16 MiB array in the library's static device memory, held by
+ * every GPU that loads the library until the process exits; a call needs
+ * M * (12 * ceil(V/256) + 4) bytes of it (at V = 65536: at most 5454 rows per
+ * call), larger requests return NC_ERR_UNSUPPORTED with a message. The first
+ * call on a device looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it, so make that first call before any stream capture. Calls
+ * share the one array: calls that overlap on the GPU (on different streams,
+ * or on different host threads) race and give wrong results. Asynchronous;
+ * nothing is allocated and no allocating library routine is called. */
+nc_status nc_lmhead_ce_fwd_static(const void* hf, const void* w_lm, const int32_t* tgt, int M, int d, int V,
+                                  float* lse, float* nll, int32_t* argmax, int32_t* d_status,
+                                  void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
