@@ -7,7 +7,8 @@
 // probabilities recomputed from the forward's logsumexp, no atomics.
 //
 // qkv is [B*T, 3d] holding q_hat (QK-normed and rotated), k_hat, v; o is
-// [B*T, d]; lse and D are [B, H, T]; scale is 1/sqrt(128).
+// [B*T, d]; lse and D are [B, H, T]; scale is 1/sqrt(128). The backward
+// writes dq_hat and dk_hat as two fp32 [B*T, d] planes of dqk.
 #include "ops.cuh"
 
 namespace nc {
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(256) attn_bwd_dq_simt_k(const T* __restrict__ 
     }
   }
   if (t < Tlen) {
-    float* row = dqk + ((size_t)b * Tlen + t) * 2 * d + h * kHeadDim;
+    float* row = dqk + ((size_t)b * Tlen + t) * d + h * kHeadDim;  // dq_hat plane
 #pragma unroll
     for (int c = 0; c < 4; ++c) row[lane + 32 * c] = acc[c] * scale;
   }
@@ -205,7 +206,7 @@ __global__ void __launch_bounds__(256) attn_bwd_dkv_simt_k(const T* __restrict__
   }
   if (j < Tlen) {
     size_t m = (size_t)b * Tlen + j;
-    float* krow = dqk + m * 2 * d + d + h * kHeadDim;
+    float* krow = dqk + (size_t)gridDim.z * Tlen * d + m * d + h * kHeadDim;  // dk_hat plane
     T* vrow = dqkv + m * 3 * d + 2 * d + h * kHeadDim;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {

@@ -74,9 +74,17 @@ cudaError_t attn_fwd_simt(const T* qkv, T* o, float* lse, int B, int T_, int H, 
 template <typename T>
 cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, int H,
                         cudaStream_t s);
+// dqk is planar fp32 [2, B*T, d]: dq_hat plane, then dk_hat plane.
 template <typename T>
 cudaError_t attn_bwd_simt(const T* qkv, const T* dout, const float* lse, const float* Drow,
                           float* dqk, T* dqkv, int B, int T_, int H, cudaStream_t s);
+
+// tcgen05 flash attention (bf16, T % 128 == 0).
+bool attn_tc_supports(int T);
+cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int H, int* status, cudaStream_t s);
+// dq (zeroed here, then accumulated) and dk are fp32 [B*T, d]; dv goes to dqkv's v columns.
+cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* Drow, float* dq,
+                        float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s);
 
 // ------------------------------------------------------------------ loss
 cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,

@@ -152,8 +152,8 @@ __global__ void qk_norm_rope_fwd_k(T* __restrict__ qkv, float* __restrict__ rqk,
 }
 
 // Backward of q_hat = rope(rmsnorm(q)): dq_n = R^T dq_hat, q_n = R^T q_hat,
-// dq = r * (dq_n - q_n * mean(dq_n * q_n)). dqk is fp32 [M, 2d] (dq_hat then
-// dk_hat); results go to the q,k columns of dqkv[M,3d].
+// dq = r * (dq_n - q_n * mean(dq_n * q_n)). dqk is fp32 [2, M, d] (dq_hat
+// plane, then dk_hat plane); results go to the q,k columns of dqkv[M,3d].
 template <typename T>
 __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __restrict__ qkv,
                                    const float* __restrict__ rqk, const float* __restrict__ cs,
@@ -164,7 +164,8 @@ __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __res
   if (w >= M * 2 * H) return;
   int m = w / (2 * H), wh = w % (2 * H);
   int d = H * kHeadDim;
-  const float* g = dqk + (size_t)m * 2 * d + (size_t)wh * kHeadDim;
+  const int which = wh / H, hh = wh % H;
+  const float* g = dqk + (size_t)which * M * d + (size_t)m * d + (size_t)hh * kHeadDim;
   const T* q = qkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
   int t = m % Tlen;
   float gn[4], qn[4];

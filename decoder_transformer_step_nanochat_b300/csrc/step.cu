@@ -263,6 +263,26 @@ double attn_fwd_flops(const nc_ctx* c) {
   return 2.0 * kHeadDim * (double)c->T * (c->T + 1) * c->B * c->H;
 }
 
+// Causal attention: tcgen05 kernels for bf16, fp32 FMA kernels for the fp32
+// debug mode. dqk is the planar fp32 [2, M, d] (dq_hat, dk_hat) scratch.
+template <typename T>
+cudaError_t attn_fwd(nc_ctx* c, const T* qkv, T* o, float* lse) {
+  if constexpr (sizeof(T) == 2)
+    return attn_fwd_tc(qkv, o, lse, c->B, c->T, c->H, c->status, c->stream);
+  else
+    return attn_fwd_simt<T>(qkv, o, lse, c->B, c->T, c->H, c->stream);
+}
+
+template <typename T>
+cudaError_t attn_bwd(nc_ctx* c, const T* qkv, const T* dout, const float* lse, const float* drow, float* dqk,
+                     T* dqkv) {
+  if constexpr (sizeof(T) == 2)
+    return attn_bwd_tc(qkv, dout, lse, drow, dqk, dqk + (size_t)c->M * c->d, dqkv, c->B, c->T, c->H, c->status,
+                       c->stream);
+  else
+    return attn_bwd_simt<T>(qkv, dout, lse, drow, dqk, dqkv, c->B, c->T, c->H, c->stream);
+}
+
 // ------------------------------------------------------------------ step pieces
 
 template <typename T>
@@ -339,7 +359,7 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
     KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn1, r1, M, d, s));
     CKS(gemm(c, mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_STORE, qkv, 3 * d)));
     KL(NC_FAM_ROWS, 4.0 * M * d * sizeof(T) + 8.0 * M * H, 1, qk_norm_rope_fwd<T>(qkv, rqk, c->rope_cos, c->rope_sin, M, Tn, H, s));
-    KL(NC_FAM_ATTN_FWD, attn_fwd_flops(c), 1, attn_fwd_simt<T>(qkv, o, lse_att, c->B, Tn, H, s));
+    KL(NC_FAM_ATTN_FWD, attn_fwd_flops(c), 1, attn_fwd<T>(c, qkv, o, lse_att));
     CKS(gemm(c, mk(M, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
     KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn2, r2, M, d, s));
     GemmArgs up = mk(M, F, d, xn2, d, 1, Wfc, d, 1, EPI_RELU2, u, F);
@@ -402,7 +422,8 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
     CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
     KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + 4.0 * M * H, 1, attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s));
-    KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), 2, attn_bwd_simt<T>(qkv, dout, lse_att, drow, dqk, dqkv, c->B, Tn, H, s));
+    KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), c->prec == NC_BF16 ? 1 : 2,
+       attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv));
     KL(NC_FAM_ROWS, 2.0 * M * d * (4 + 2 * sizeof(T)) + 8.0 * M * H, 1, qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s));
     CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d)));
     CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, EPI_STORE_F32, dy, d)));
@@ -667,8 +688,8 @@ nc_status nc_op_attention_fwd(nc_ctx* c, const void* qkv, void* o, float* lse) {
   CKS(check_ready(c));
   if (!qkv || !o || !lse) return fail(NC_ERR_ARG, "null pointer argument");
   c->have_fwd = false;
-  if (c->prec == NC_BF16) CK(attn_fwd_simt<bf16>((const bf16*)qkv, (bf16*)o, lse, c->B, c->T, c->H, c->stream));
-  else CK(attn_fwd_simt<float>((const float*)qkv, (float*)o, lse, c->B, c->T, c->H, c->stream));
+  if (c->prec == NC_BF16) CK(attn_fwd<bf16>(c, (const bf16*)qkv, (bf16*)o, lse));
+  else CK(attn_fwd<float>(c, (const float*)qkv, (float*)o, lse));
   return NC_OK;
 }
 
@@ -680,10 +701,10 @@ nc_status nc_op_attention_bwd(nc_ctx* c, const void* qkv, const void* o, const v
   float* drow = wsp<float>(c, c->off.drow);
   if (c->prec == NC_BF16) {
     CK(attn_rowdot<bf16>((const bf16*)dout, (const bf16*)o, drow, c->B, c->T, c->H, c->stream));
-    CK(attn_bwd_simt<bf16>((const bf16*)qkv, (const bf16*)dout, lse, drow, dqk, (bf16*)dqkv, c->B, c->T, c->H, c->stream));
+    CK(attn_bwd<bf16>(c, (const bf16*)qkv, (const bf16*)dout, lse, drow, dqk, (bf16*)dqkv));
   } else {
     CK(attn_rowdot<float>((const float*)dout, (const float*)o, drow, c->B, c->T, c->H, c->stream));
-    CK(attn_bwd_simt<float>((const float*)qkv, (const float*)dout, lse, drow, dqk, (float*)dqkv, c->B, c->T, c->H, c->stream));
+    CK(attn_bwd<float>(c, (const float*)qkv, (const float*)dout, lse, drow, dqk, (float*)dqkv));
   }
   return NC_OK;
 }

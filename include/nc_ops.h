@@ -66,9 +66,10 @@ nc_status nc_op_lmhead_ce_bwd(nc_ctx* ctx, const void* hf, const void* w_lm, con
 nc_status nc_op_attention_fwd(nc_ctx* ctx, const void* qkv, void* o, float* lse);
 
 /* Attention backward. dout: elem [B*T, d]; lse from the forward.
- * dqk: fp32 [B*T, 2d] receives dq_hat | dk_hat; dqkv: elem [B*T, 3d]
- * receives dv in its v columns (q,k columns untouched). Scratch from the
- * workspace. */
+ * dqk: fp32 [2, B*T, d] receives the dq_hat plane then the dk_hat plane;
+ * dqkv: elem [B*T, 3d] receives dv in its v columns (q,k columns untouched).
+ * Scratch (the softmax-backward row sums) from the workspace. NC_BF16 needs
+ * seq_len % 128 == 0 (tensor-core kernels). */
 nc_status nc_op_attention_bwd(nc_ctx* ctx, const void* qkv, const void* o, const void* dout,
                               const float* lse, float* dqk, void* dqkv);
 

@@ -147,7 +147,7 @@ def _qkv(rng, B, T, H, prec):
     return rounded(qkv, prec).reshape(B * T, 3 * H * D)
 
 
-@pytest.mark.parametrize("prec,T", [(0, 256), (1, 100)], ids=["bf16_T256", "fp32_T100"])
+@pytest.mark.parametrize("prec,T", [(0, 256), (0, 640), (1, 100)], ids=["bf16_T256", "bf16_T640", "fp32_T100"])
 def test_attention_fwd_bwd(nc, prec, T):
     import torch
     B, H, D = 2, 2, 128
@@ -163,7 +163,7 @@ def test_attention_fwd_bwd(nc, prec, T):
         lse = torch.zeros((B, H, T), dtype=torch.float32, device="cuda")
         nc.nc_op_attention_fwd(c.ctx, dq.data_ptr(), o.data_ptr(), lse.data_ptr())
         ddo = torch_of(dout, prec, nc)
-        dqk = torch.zeros((B * T, 2 * d), dtype=torch.float32, device="cuda")
+        dqk = torch.zeros((2, B * T, d), dtype=torch.float32, device="cuda")
         dqkv = torch.zeros((B * T, 3 * d), dtype=elem, device="cuda")
         nc.nc_op_attention_bwd(c.ctx, dq.data_ptr(), o.data_ptr(), ddo.data_ptr(), lse.data_ptr(),
                                dqk.data_ptr(), dqkv.data_ptr())
@@ -180,8 +180,8 @@ def test_attention_fwd_bwd(nc, prec, T):
             # the backward is checked with the forward output the kernel produced
             g = dout.reshape(B, T, H, D)[b].astype(np.float64)
             dq_r, dk_r, dv_r = oracle.causal_attention_backward(q, k, v, g)
-            got = dqk_h.reshape(B, T, 2, H, D)[b]
-            for gg, rr in ((got[:, 0], dq_r), (got[:, 1], dk_r), (dqkv_h.reshape(B, T, 3, H, D)[b][:, 2], dv_r)):
+            got = dqk_h.reshape(2, B, T, H, D)[:, b]
+            for gg, rr in ((got[0], dq_r), (got[1], dk_r), (dqkv_h.reshape(B, T, 3, H, D)[b][:, 2], dv_r)):
                 assert np.linalg.norm(gg - rr) <= 2 * tol * np.linalg.norm(rr)
         assert np.all(dqkv_h.reshape(B, T, 3, d)[:, :, :2] == 0)  # q,k columns untouched
     finally:
