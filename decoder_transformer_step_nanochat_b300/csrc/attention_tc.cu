@@ -10,9 +10,9 @@
 // (rows = K index) by choosing the descriptor. Softmax threads own one row
 // each (TMEM lane = row) and write P / dS tiles in the same swizzled layout.
 //
-// Forward, one CTA per (b, h, 128-query tile): S = Q K^T into TMEM, online
-// softmax in registers (log2 domain), P (bf16) to shared memory, P V into a
-// second TMEM buffer, output accumulated in registers. Backward, one CTA per
+// Forward, one CTA per (b, h, 128-query tile): S = Q K^T into one of two TMEM
+// buffers, online softmax in registers (log2 domain), P (bf16) to shared
+// memory, O += P V accumulated in TMEM. Backward, one CTA per
 // (b, h, 128-key tile): per query tile S^T = K Q^T and dP^T = V dO^T, then
 // P^T, dS^T = P^T (dP^T - D) to shared memory, dV += P^T dO and dK += dS^T Q
 // accumulate in TMEM, dQ = dS K goes to TMEM and is added to an fp32 global
@@ -88,6 +88,17 @@ struct AttnParams {
 };
 
 // ============================================================== forward
+//
+// MMA issue order per CTA: S_0, S_1, PV_0, S_2, PV_1, ... : S_{j+1} (into the
+// other TMEM S buffer) runs while the softmax threads work on S_j, and PV_j
+// accumulates straight into the TMEM output O. The softmax keeps, per row, a
+// reference maximum m (log2 units) and exponentiates against it; only when a
+// tile's maximum exceeds m by more than 8 (so p could exceed 2^8) does the
+// warp move m up and rescale its rows of O and the running sum l, after the
+// previous PV has landed. P_j goes to shared-memory buffer j % 2; PV_{j-2}
+// (the last reader of that buffer) finished before S_j's completion fired.
+
+constexpr float kRescaleLog2 = 8.f;
 
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ AttnParams p) {
@@ -96,17 +107,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + TILE_BYTES;          // 2 stages
   uint8_t* sV = sK + 2 * TILE_BYTES;      // 2 stages
-  uint8_t* sP = sV + 2 * TILE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + TILE_BYTES);
+  uint8_t* sP = sV + 2 * TILE_BYTES;      // 2 buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * TILE_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;   // [2]
   uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* pv_full = bars + 7;
-  uint64_t* pv_free = bars + 8;
-  uint64_t* drain = bars + 9;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* p_full = bars + 7;    // [2]
+  uint64_t* pv_done = bars + 9;
+  uint64_t* o_full = bars + 10;
+  uint64_t* drain = bars + 11;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -122,24 +133,24 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(kv_full + s, 1);
       tc::mbar_init(kv_empty + s, 1);
+      tc::mbar_init(s_full + s, 1);
+      tc::mbar_init(p_full + s, 128);
     }
-    tc::mbar_init(s_full, 1);
-    tc::mbar_init(p_full, 128);
-    tc::mbar_init(pv_full, 1);
-    tc::mbar_init(pv_free, 128);
+    tc::mbar_init(pv_done, 1);
+    tc::mbar_init(o_full, 1);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_holder, 256);
+    tc::tmem_alloc(tmem_holder, 512);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tS = tmem, tPV = tmem + 128;
+  const uint32_t tO = tmem + 256;  // S buffers at columns 0 and 128
   bool failed = false;
 
   if (warp == 0) {
@@ -174,26 +185,33 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);
-      const uint32_t aQ = tc::smem_u32(sQ), aP = tc::smem_u32(sP);
+      const uint32_t aQ = tc::smem_u32(sQ);
       bool any = false;
       if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
+      // PV_i = P_i V_i accumulated into O, once the softmax threads released P_i
+      auto issue_pv = [&](int i) -> bool {
+        const int s = i & 1;
+        if (!tc::mbar_wait(p_full + s, (i >> 1) & 1, abort_flag, kWaitNs)) return false;
+        tc::tc_fence_after();
+        mma_tile(tO, tc::smem_u32(sP + s * TILE_BYTES), false, tc::smem_u32(sV + s * TILE_BYTES), true, idesc_pv,
+                 i > 0);
+        tc::mma_commit(pv_done);
+        tc::mma_commit(kv_empty + s);
+        return true;
+      };
       for (int j = 0; j < nkv && !failed; ++j) {
         const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!tc::mbar_wait(kv_full + s, ph, abort_flag, kWaitNs)) { failed = true; break; }
+        if (!tc::mbar_wait(kv_full + s, (j >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
         tc::tc_fence_after();
-        // S_j = Q K_j^T (the softmax threads read S_{j-1} before they arrived on p_full)
-        mma_tile(tS, aQ, false, tc::smem_u32(sK + s * TILE_BYTES), false, idesc, false);
-        tc::mma_commit(s_full);
+        // S_j into buffer s: its previous reader (softmax of S_{j-2}) released
+        // it before PV_{j-2} was issued.
+        mma_tile(tmem + s * 128, aQ, false, tc::smem_u32(sK + s * TILE_BYTES), false, idesc, false);
+        tc::mma_commit(s_full + s);
         any = true;
-        if (!tc::mbar_wait(p_full, j & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        if (j > 0 && !tc::mbar_wait(pv_free, (j - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        tc::tc_fence_after();
-        // PV_j = P_j V_j  (V is the MN-major B operand: rows = keys)
-        mma_tile(tPV, aP, false, tc::smem_u32(sV + s * TILE_BYTES), true, idesc_pv, false);
-        tc::mma_commit(pv_full);
-        tc::mma_commit(kv_empty + s);
+        if (j > 0 && !issue_pv(j - 1)) { failed = true; break; }
       }
+      if (!failed && !issue_pv(nkv - 1)) failed = true;
+      if (!failed) tc::mma_commit(o_full);
       if (failed) {
         *abort_flag = 1;
         if (any) {
@@ -209,69 +227,80 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = kLog2e * rsqrtf(128.f);
     float m = -INFINITY, l = 0.f;
-    float o[128];
-#pragma unroll
-    for (int i = 0; i < 128; ++i) o[i] = 0.f;
     for (int j = 0; j < nkv; ++j) {
-      bool ok = tc::mbar_wait(s_full, j & 1, abort_flag, kWaitNs);
+      const int s = j & 1;
+      bool ok = tc::mbar_wait(s_full + s, (j >> 1) & 1, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
       const bool diag = (j == qt);
+      float v[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + s * 128 + lane_off + c * 32, v + c * 32);
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(tS + lane_off + c * 32, v);
+      for (int i = 0; i < 128; ++i) {
+        v[i] *= sl2;
+        if (!diag || i <= r) mx = fmaxf(mx, v[i]);
+      }
+      const bool grow = mx > m + kRescaleLog2;
+      if (__any_sync(0xffffffffu, grow)) {
+        // move this warp's reference maxima up; rows of O that already hold
+        // partial sums are rescaled once the previous PV has landed
+        const float m_new = grow ? mx : m;
+        const float alpha = exp2f(m - m_new);  // 0 for the first tile (m = -inf)
+        l *= alpha;
+        m = m_new;
+        if (j > 0) {
+          ok = tc::mbar_wait(pv_done, (j - 1) & 1, abort_flag, kWaitNs);
+          if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+          tc::tc_fence_after();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool keep = !diag || (c * 32 + i <= r);
-          if (keep) mx = fmaxf(mx, v[i]);
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tc::tmem_ld32(tO + lane_off + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tc::tmem_st32(tO + lane_off + c * 32, o);
+          }
         }
       }
-      const float m_new = fmaxf(m, mx * sl2);
-      const float alpha = exp2f(m - m_new);
       float rs = 0.f;
+      uint8_t* pbuf = sP + s * TILE_BYTES;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(tS + lane_off + c * 32, v);
+      for (int g = 0; g < 16; ++g) {
+        float e[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const bool keep = !diag || (c * 32 + i <= r);
-          const float e = keep ? exp2f(v[i] * sl2 - m_new) : 0.f;
-          v[i] = e;
-          rs += e;
+        for (int i = 0; i < 8; ++i) {
+          const int k = g * 8 + i;
+          e[i] = (!diag || k <= r) ? exp2f(v[k] - m) : 0.f;
+          rs += e[i];
         }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) st_tile8(sP, r, c * 4 + g, pack8(v + 8 * g));
+        st_tile8(pbuf, r, g, pack8(e));
       }
-      l = l * alpha + rs;
-      m = m_new;
+      l += rs;
       fence_async_smem();
       tc::tc_fence_before();
-      tc::mbar_arrive(p_full);
-      ok = tc::mbar_wait(pv_full, j & 1, abort_flag, kWaitNs);
-      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-      tc::tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tc::tmem_ld32(tPV + lane_off + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c * 32 + i] = o[c * 32 + i] * alpha + v[i];
-      }
-      tc::tc_fence_before();
-      tc::mbar_arrive(pv_free);
+      tc::mbar_arrive(p_full + s);
     }
     if (!failed) {
+      bool ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
+      if (!__all_sync(0xffffffffu, ok)) failed = true;
+    }
+    if (!failed) {
+      tc::tc_fence_after();
       const float inv = 1.f / l;
       bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128;
 #pragma unroll
-      for (int g = 0; g < 16; ++g) {
-        float v[8];
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tc::tmem_ld32(tO + lane_off + c * 32, o);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = o[g * 8 + i] * inv;
-        *reinterpret_cast<uint4*>(orow + g * 8) = pack8(v);
+        for (int g = 0; g < 4; ++g) {
+          float w8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w8[i] = o[g * 8 + i] * inv;
+          *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = pack8(w8);
+        }
       }
       p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
     } else {
@@ -284,7 +313,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -530,7 +559,7 @@ bool map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int FWD_SMEM = 6 * TILE_BYTES + 1024 + 256;
+constexpr int FWD_SMEM = 7 * TILE_BYTES + 1024 + 256;
 constexpr int BWD_SMEM = 6 * TILE_BYTES + 1024 + 256;
 
 }  // namespace

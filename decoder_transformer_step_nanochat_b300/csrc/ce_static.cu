@@ -63,13 +63,13 @@ extern "C" nc_status nc_lmhead_ce_fwd_static(const void* hf, const void* w_lm, c
   if (M < 0 || d < 1 || V < 1 || d % 8 != 0 || V % 8 != 0)
     return set_last_error(NC_ERR_ARG, "nc_lmhead_ce_fwd_static: need M >= 0 and d, V positive multiples of 8");
   if (M == 0) return NC_OK;
-  const size_t tiles = (size_t)(V + 255) / 256;
+  const size_t tiles = (size_t)(V + 127) / 128;
   const size_t part = align256((size_t)M * tiles * 4);
   const size_t need = 3 * part + align256((size_t)M * 4);
   if (need > kStaticScratchBytes)
     return set_last_error(NC_ERR_UNSUPPORTED,
-                          "nc_lmhead_ce_fwd_static: M * (12 * ceil(V/256) + 4) bytes of scratch exceed the "
-                          "16 MiB static buffer (at V = 65536 at most 5454 rows per call)");
+                          "nc_lmhead_ce_fwd_static: M * (12 * ceil(V/128) + 4) bytes of scratch exceed the "
+                          "16 MiB static buffer (at V = 65536 at most 2728 rows per call)");
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   void* base = nullptr;
   if (scratch_address(&base) != cudaSuccess)

@@ -9,9 +9,10 @@
 // slices of bf16 staged by TMA into 128-byte-swizzled shared memory in a
 // 4-stage mbarrier ring; warp 0 issues TMA, one thread of warp 1 issues
 // tcgen05.mma into a TMEM accumulator (two 256-column buffers, so the
-// epilogue of tile i overlaps the main loop of tile i+1), warps 2..5 read the
-// accumulator with tcgen05.ld (one thread per output row) and run the
-// epilogue. Every wait is bounded; on timeout the kernel records
+// epilogue of tile i overlaps the main loop of tile i+1), warps 2..9 read the
+// accumulator with tcgen05.ld (one thread per output row and 128-column half)
+// and run the epilogue. Weight-gradient shapes (few output tiles, K = tokens)
+// split K across CTAs into fp32 partial slabs that a reduction kernel sums. Every wait is bounded; on timeout the kernel records
 // DEV_TIMEOUT, unwinds, frees its TMEM and returns.
 #include <cudaTypedefs.h>
 
@@ -28,15 +29,26 @@ constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NTHREADS = 192;
+constexpr int NEPI_WARPS = 8;           // two per TMEM lane quadrant, each half the columns
+constexpr int NTHREADS = 64 + 32 * NEPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 
 struct TcParams {
   GemmArgs g;
-  int num_m, num_n, num_kb, total;
+  int num_m, num_n, num_kb, total;  // total = tiles * splits work units
+  int splits, kb_per_split;
 };
+
+// Work unit u covers output tile u / splits and k-blocks [kb0, kb1).
+__device__ __forceinline__ void unit_range(const TcParams& p, int u, int& tile, int& split, int& kb0, int& kb1) {
+  tile = u / p.splits;
+  split = u % p.splits;
+  kb0 = split * p.kb_per_split;
+  kb1 = min(p.num_kb, kb0 + p.kb_per_split);
+  if (kb1 < kb0) kb1 = kb0;
+}
 
 __device__ __forceinline__ uint4 pack8_bf16(const float* v) {
   uint4 r;
@@ -152,7 +164,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tfull + b, 1);
-      tc::mbar_init(tempty + b, 128);
+      tc::mbar_init(tempty + b, 32 * NEPI_WARPS);
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -180,9 +192,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t issued_phase[STAGES];
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
-      for (int tile = blockIdx.x; tile < p.total && !failed; tile += gridDim.x) {
+      for (int u = blockIdx.x; u < p.total && !failed; u += gridDim.x) {
+        int tile, split, kb0, kb1;
+        unit_range(p, u, tile, split, kb0, kb1);
         const int m0 = (tile / p.num_n) * BM, n0 = (tile % p.num_n) * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
           tc::mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
           const int k0 = kb * BK;
@@ -220,13 +234,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t phase = 0;
       int cnt = 0;
       bool any_mma = false;
-      for (int tile = blockIdx.x; tile < p.total && !failed; tile += gridDim.x, ++cnt) {
+      for (int u = blockIdx.x; u < p.total && !failed; u += gridDim.x, ++cnt) {
+        int tile, split, kb0, kb1;
+        unit_range(p, u, tile, split, kb0, kb1);
         const int ab = cnt & 1;
         const uint32_t aph = (cnt >> 1) & 1;
         if (!tc::mbar_wait(tempty + ab, aph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
         tc::tc_fence_after();
         const uint32_t dtm = tmem_base + ab * BN;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(full + stage, phase, abort_flag, kWaitNs)) { failed = true; break; }
           tc::tc_fence_after();
           const uint32_t a_addr = tc::smem_u32(sA + stage * A_BYTES);
@@ -237,7 +253,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                      : tc::sdesc_sw128(a_addr + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? tc::sdesc_sw128(b_addr + k * 2048, 8192, 1024)
                                      : tc::sdesc_sw128(b_addr + k * 32, 16, 1024);
-            tc::mma_bf16(dtm, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            tc::mma_bf16(dtm, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           tc::mma_commit(empty + stage);
           any_mma = true;
@@ -257,27 +273,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- epilogue warps
-    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int q = warp & 3;            // TMEM lane quadrant this warp may read
+    const int ch = (warp - 2) >> 2;    // which 128-column half of the tile
     const int row = q * 32 + lane;
     int cnt = 0;
-    for (int tile = blockIdx.x; tile < p.total && !failed; tile += gridDim.x, ++cnt) {
+    for (int u = blockIdx.x; u < p.total && !failed; u += gridDim.x, ++cnt) {
+      int tile, split, kb0, kb1;
+      unit_range(p, u, tile, split, kb0, kb1);
       const int ab = cnt & 1;
       const uint32_t aph = (cnt >> 1) & 1;
       const int mb = tile / p.num_n, nb = tile % p.num_n;
-      const int m0 = mb * BM, n0 = nb * BN;
+      const int m0 = mb * BM, n0 = nb * BN + ch * (BN / 2);
       const bool ok = tc::mbar_wait(tfull + ab, aph, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; *abort_flag = 1; break; }
       tc::tc_fence_after();
       const int m = m0 + row;
       const bool row_ok = m < g.M;
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * BN;
+      const bool have_acc = kb1 > kb0;
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + ab * BN + ch * (BN / 2);
       if (EPI == EPI_CE_FWD) {
         float mx = -INFINITY, sum = 0.f, tl = 0.f;
         int arg = 0;
         const int t = row_ok ? g.row_i[m] : -1;
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < BN / 64; ++c) {
           float v[32];
-          if (p.num_kb > 0) tc::tmem_ld32(taddr + c * 32, v);
+          if (have_acc) tc::tmem_ld32(taddr + c * 32, v);
           else
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -301,17 +321,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int i = 0; i < 32; ++i)
             if (nc0 + i < g.N) sum += __expf(v[i] - mx);
         }
-        if (row_ok) {
-          const size_t pi = (size_t)nb * g.M + m;
+        if (row_ok && n0 < g.N) {
+          const size_t pi = (size_t)(nb * 2 + ch) * g.M + m;
           g.p_max[pi] = mx;
           g.p_sum[pi] = sum;
           g.p_arg[pi] = arg;
-          if (t >= n0 && t < n0 + BN) g.p_tgt[m] = tl;
+          if (t >= n0 && t < n0 + BN / 2) g.p_tgt[m] = tl;
         }
       } else {
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < BN / 64; ++c) {
           float v[32];
-          if (p.num_kb > 0) tc::tmem_ld32(taddr + c * 32, v);
+          if (have_acc) tc::tmem_ld32(taddr + c * 32, v);
           else
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.f;
@@ -319,7 +339,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!row_ok || nc0 >= g.N) continue;
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= g.alpha;
-          epi_chunk<EPI>(g, m, nc0, v);
+          if (EPI == EPI_STORE_F32 && p.splits > 1) {
+            // raw partial sum of this k-split; the reduction adds beta*C
+            float* c0 = g.partial + ((size_t)split * g.M + m) * g.N + nc0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (nc0 + 4 * j < g.N)
+                *reinterpret_cast<float4*>(c0 + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          } else {
+            epi_chunk<EPI>(g, m, nc0, v);
+          }
         }
       }
       tc::tc_fence_before();
@@ -403,6 +432,7 @@ bool gemm_tc_supports(const GemmArgs& g) {
   if (g.N % 8 || g.lda % 8 || g.ldb % 8) return false;
   if (!aligned16(g.A) || !aligned16(g.B)) return false;
   if (g.epi == EPI_CE_FWD) return g.p_max && g.p_sum && g.p_arg && g.p_tgt && g.row_i;
+  if (g.splits > 1 && (g.epi != EPI_STORE_F32 || !g.partial || g.N % 4)) return false;
   if (g.ldc % 8 || !aligned16(g.C)) return false;
   if ((g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD) && (g.ldc2 % 8 || !aligned16(g.C2))) return false;
   if (g.epi == EPI_CE_BWD && (!g.row_f || !g.row_i)) return false;
@@ -424,7 +454,9 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   p.num_m = (g.M + BM - 1) / BM;
   p.num_n = (g.N + BN - 1) / BN;
   p.num_kb = (g.K + BK - 1) / BK;
-  p.total = p.num_m * p.num_n;
+  p.splits = (g.splits > 1 && g.epi == EPI_STORE_F32 && g.partial) ? g.splits : 1;
+  p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
+  p.total = p.num_m * p.num_n * p.splits;
   KernFn fn = pick_kernel(g.epi, !g.a_kmajor, !g.b_kmajor);
   if (!fn) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -432,7 +464,32 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   int grid = p.total < g_num_sms ? p.total : g_num_sms;
   fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, p);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.splits == 1) return e;
+  return splitk_reduce(g.partial, p.splits, static_cast<float*>(g.C), g.ldc, g.M, g.N, g.beta, s);
+}
+
+// Choose k-splits for fp32-output GEMMs whose output tiles underfill the SMs
+// (the weight gradients, K = tokens): minimise the estimated time of
+// ceil(units / SMs) waves of ceil(kblocks / splits) k-blocks each, plus the
+// partial-sum traffic (write + read of splits * M * N fp32).
+int gemm_tc_pick_splits(const GemmArgs& g) {
+  if (g.epi != EPI_STORE_F32 || g.M == 0 || g.N == 0) return 1;
+  get_encode();
+  const long long tiles = (long long)((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  const long long kb = (g.K + BK - 1) / BK;
+  if (kb < 16 || tiles >= 4LL * g_num_sms) return 1;
+  const double t_kb = 0.28e-6;                 // one 128x256x64 k-block per SM, seconds
+  const double bw = 6.0e12;                    // bytes/s for the partial-sum round trip
+  int best = 1;
+  double best_t = 1e30;
+  for (int s = 1; s <= 8; ++s) {
+    const long long per = (kb + s - 1) / s;
+    const long long waves = (tiles * s + g_num_sms - 1) / g_num_sms;
+    const double t = waves * per * t_kb + (s > 1 ? 8.0 * s * g.M * (double)g.N / bw : 0.0);
+    if (t < best_t * 0.97) { best_t = t; best = s; }
+  }
+  return best;
 }
 
 }  // namespace nc

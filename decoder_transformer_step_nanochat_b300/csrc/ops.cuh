@@ -16,7 +16,7 @@ enum Epi : int {
   EPI_RELU2 = 2,       // C (elem) = u = alpha*acc ; C2 (elem) = max(u,0)^2
   EPI_RELU2_BWD = 3,   // C (elem) = alpha*acc * 2*max(u,0), u read from C2
   EPI_CE_BWD = 4,      // C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])
-  EPI_CE_FWD = 5,      // per (row, 256-column tile) softmax partials (tensor-core path)
+  EPI_CE_FWD = 5,      // per (row, 128-column tile) softmax partials (tensor-core path)
   EPI_QKNORM_ROPE = 6, // C (elem) = qkv with per-head RMSNorm + RoPE on the q,k columns
 };
 
@@ -30,15 +30,25 @@ struct GemmArgs {
   void* C2 = nullptr; long long ldc2 = 0;
   const float* row_f = nullptr;  // CE bwd: lse per row
   const int* row_i = nullptr;    // CE fwd/bwd: target id per row
-  // CE forward partials, [n_tiles][M] each (tensor-core path)
+  // CE forward partials, [n_tiles][M] each, one tile per 128 vocabulary columns
   float* p_max = nullptr; float* p_sum = nullptr; int* p_arg = nullptr;
   float* p_tgt = nullptr;        // [M]: logit of the target column
   // QK-norm + RoPE epilogue
   const float* rope_cos = nullptr; const float* rope_sin = nullptr;  // [T,64]
   float* rqk = nullptr;          // [M, 2H] rstd of q heads then k heads
   int seq_len = 0, d_model = 0;
+  // split-K (EPI_STORE_F32 only): splits > 1 writes alpha*partial sums to
+  // `partial` ([splits, M, N] fp32) and a reduction kernel forms C.
+  int splits = 1;
+  float* partial = nullptr;
   int* status = nullptr;
 };
+
+// Number of k-splits the tensor-core GEMM would use for this problem (1 = none).
+int gemm_tc_pick_splits(const GemmArgs& g);
+// C[m*ldc+n] = sum_s partial[s][m][n] + beta * C[m*ldc+n]   (fp32)
+cudaError_t splitk_reduce(const float* partial, int splits, float* C, long long ldc, int M, int N, float beta,
+                          cudaStream_t s);
 
 // Plain fp32-FMA tiled GEMM (any majorness, any sizes). elem = float or bf16.
 template <typename T> cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);

@@ -308,6 +308,30 @@ __global__ void check_ids_k(const int* __restrict__ ids, int n, int V, int* stat
   }
 }
 
+// C[m, n] = sum_s partial[s, m, n] + beta * C[m, n]; the split order is fixed,
+// so the result does not depend on scheduling.
+__global__ void splitk_reduce_k(const float* __restrict__ part, int splits, float* __restrict__ C, long long ldc,
+                                int M, int N, float beta) {
+  const long long n4 = (long long)N / 4;
+  const long long total = (long long)M * n4;
+  const size_t plane = (size_t)M * N;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const long long m = i / n4, c = (i % n4) * 4;
+    const float* src = part + (size_t)m * N + c;
+    float4 a = ld4(src);
+    for (int s = 1; s < splits; ++s) {
+      float4 b = ld4(src + s * plane);
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    float* dst = C + (size_t)m * ldc + c;
+    if (beta != 0.f) {
+      float4 o = ld4(dst);
+      a.x += beta * o.x; a.y += beta * o.y; a.z += beta * o.z; a.w += beta * o.w;
+    }
+    st4(dst, a);
+  }
+}
+
 inline int row_blocks(long long rows) { return (int)((rows + kRowWarps - 1) / kRowWarps); }
 
 }  // namespace
@@ -371,6 +395,16 @@ cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int
                                const float* p_tgt, int n_tiles, float* lse, float* nll, int* amax,
                                int M, cudaStream_t s) {
   ce_reduce_k<<<(M + 255) / 256, 256, 0, s>>>(p_max, p_sum, p_arg, p_tgt, n_tiles, lse, nll, amax, M);
+  return cudaGetLastError();
+}
+
+cudaError_t splitk_reduce(const float* partial, int splits, float* C, long long ldc, int M, int N, float beta,
+                          cudaStream_t s) {
+  long long total = (long long)M * (N / 4);
+  if (total == 0) return cudaSuccess;
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 148 * 16) blocks = 148 * 16;
+  splitk_reduce_k<<<blocks, 256, 0, s>>>(partial, splits, C, ldc, M, N, beta);
   return cudaGetLastError();
 }
 

@@ -78,12 +78,13 @@ struct nc_ctx {
   char* ws = nullptr;
   size_t ws_bytes = 0, ws_need = 0;
   int ce_rows = 0;          // rows per lm_head / cross-entropy chunk
-  int ce_tiles = 0;         // 256-wide vocabulary tiles (tensor-core CE partials)
+  int ce_tiles = 0;         // 128-wide vocabulary tiles (tensor-core CE partials)
+  size_t partial_bytes = 0; // split-K partial sums of the weight-gradient GEMMs
   struct Off {
     size_t xn1, r1, qkv, rqk, o, lse_att, xn2, r2, u, a;  // per-layer stash (stride below)
     size_t layer_stride;
     size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
-    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt;
+    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial;
   } off{};
   // launch accounting and optional per-family event timing
   unsigned long long launches = 0;
@@ -184,7 +185,7 @@ void plan_workspace(nc_ctx* c) {
   f.nll = take(M * 4);
   f.amax = take(M * 4);
   f.loss = take(4);
-  c->ce_tiles = (int)((V + 255) / 256);
+  c->ce_tiles = (int)((V + 127) / 128);
   f.pmax = take((size_t)c->ce_tiles * M * 4);
   f.psum = take((size_t)c->ce_tiles * M * 4);
   f.parg = take((size_t)c->ce_tiles * M * 4);
@@ -201,6 +202,10 @@ void plan_workspace(nc_ctx* c) {
   f.drow = take(M * H * 4);
   f.tok = take(M * 4);
   f.tgt = take(M * 4);
+  // up to 8 k-splits of the largest weight gradient (4d x d), at least 64 MiB
+  c->partial_bytes = 8 * 4 * d * d * 4;
+  if (c->partial_bytes < (size_t(64) << 20)) c->partial_bytes = size_t(64) << 20;
+  f.partial = take(c->partial_bytes);
   c->ws_need = o;
 }
 
@@ -236,6 +241,13 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
   if (c->prec == NC_FP32_DEBUG) {
     e = gemm_simt<float>(g, c->stream);
   } else if (c->use_tc) {
+    if (g.epi == EPI_STORE_F32 && c->ws) {
+      const int sp = gemm_tc_pick_splits(g);
+      if (sp > 1 && (size_t)sp * g.M * g.N * 4 <= c->partial_bytes) {
+        g.splits = sp;
+        g.partial = wsp<float>(c, c->off.partial);
+      }
+    }
     if (!gemm_tc_supports(g))
       return fail(NC_ERR_UNSUPPORTED, "tensor-core GEMM cannot serve M=%d N=%d K=%d epi=%d", g.M, g.N, g.K, g.epi);
     e = gemm_tc(g, c->stream);
@@ -243,7 +255,7 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
     e = gemm_simt<bf16>(g, c->stream);
   }
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm M=%d N=%d K=%d epi=%d: %s", g.M, g.N, g.K, g.epi, cudaGetErrorString(e));
-  int n = (g.M > 0 && g.N > 0) ? 1 : 0;
+  int n = (g.M > 0 && g.N > 0) ? (g.splits > 1 ? 2 : 1) : 0;  // split-K adds its reduction kernel
   return prof_end(c, ev_a, NC_FAM_GEMM, 2.0 * g.M * g.N * (double)g.K, n);
 }
 

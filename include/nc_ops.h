@@ -34,6 +34,9 @@ enum {
  *   A(m,k) = a_kmajor ? A[m*lda + k] : A[k*lda + m]   (elem)
  *   B(n,k) = b_kmajor ? B[n*ldb + k] : B[k*ldb + n]   (elem)
  * then the epilogue above writes C[m*ldc + n] (and C2[m*ldc2 + n]).
+ * With a workspace set, fp32-output products with many k-blocks and few
+ * output tiles (the weight gradients) are split along K into partial sums
+ * in the workspace and reduced in a fixed order (deterministic).
  * The ReLU^2 epilogues follow the nanochat explainer's "ReLU^2 Sparsity";
  * the CE_BWD epilogue forms softmax(logits) - onehot(target) of
  * "Pretraining"'s cross-entropy. In NC_BF16 the operands' leading
@@ -95,7 +98,7 @@ nc_status nc_op_rmsnorm_fwd(nc_ctx* ctx, const float* x, void* y, float* r);
  * (NULL = legacy default stream). d and V must be multiples of 8.
  * Scratch is a 16 MiB array in the library's static device memory, held by
  * every GPU that loads the library until the process exits; a call needs
- * M * (12 * ceil(V/256) + 4) bytes of it (at V = 65536: at most 5454 rows per
+ * M * (12 * ceil(V/128) + 4) bytes of it (at V = 65536: at most 2728 rows per
  * call), larger requests return NC_ERR_UNSUPPORTED with a message. The first
  * call on a device looks up the array's device address (cudaGetSymbolAddress)
  * and caches it, so make that first call before any stream capture. Calls

@@ -29,7 +29,7 @@ def _inputs(rng, M, d, V):
 def test_static_scratch_ce_matches_workspace_entry_point_on_two_calls():
     import torch
     nc = load_nc()
-    d, H, T, B, V = 256, 2, 128, 16, 65536  # M = 2048 rows, 256 vocabulary tiles
+    d, H, T, B, V = 256, 2, 128, 16, 65536  # M = 2048 rows, 512 vocabulary tiles of 128
     M = B * T
     step = nc.Step(1, d, H, T, V, B, nc.NC_BF16)
     try:
@@ -70,9 +70,9 @@ def test_static_scratch_ce_matches_workspace_entry_point_on_two_calls():
 
 def test_static_scratch_ce_rejects_sizes_beyond_its_buffer():
     nc = load_nc()
-    # 5455 rows at V = 65536 need more than the 16 MiB static scratch; the
+    # 2729 rows at V = 65536 need more than the 16 MiB static scratch; the
     # call is rejected on the host before any device work
     with pytest.raises(nc.NcError) as ei:
-        nc.nc_lmhead_ce_fwd_static(256, 256, 256, 5455, 256, 65536, 256, 256, 256)
+        nc.nc_lmhead_ce_fwd_static(256, 256, 256, 2729, 256, 65536, 256, 256, 256)
     assert ei.value.status == 6  # NC_ERR_UNSUPPORTED
     assert "16 MiB" in nc.nc_last_error()
