@@ -31,7 +31,6 @@ namespace {
 constexpr int TILE = 128;
 constexpr int HALF_BYTES = TILE * 128;        // 128 rows x 128 B
 constexpr int TILE_BYTES = 2 * HALF_BYTES;    // 32 KB
-constexpr int NTHREADS = 192;
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -99,11 +98,23 @@ struct AttnParams {
 // (the last reader of that buffer) finished before S_j's completion fired.
 
 constexpr float kRescaleLog2 = 8.f;
+constexpr int FWD_WARPS = 10;
+constexpr int FWD_THREADS = 32 * FWD_WARPS;
+constexpr int FWD_SOFT = 32 * (FWD_WARPS - 2);  // 256 softmax threads
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+__device__ __forceinline__ void bar_pair(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+
+__global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // the 128-byte swizzle needs 1024-byte aligned tiles; the dynamic window
+  // starts aligned on this architecture, and a launch where it does not is
+  // refused rather than run wrong
+  if (tc::smem_u32(smem_raw) & 1023) {
+    if (threadIdx.x == 0) set_status(p.status, DEV_BAD_LAUNCH);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + TILE_BYTES;          // 2 stages
   uint8_t* sV = sK + 2 * TILE_BYTES;      // 2 stages
@@ -119,11 +130,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* drain = bars + 11;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // row-max exchange between the two softmax warps of a lane quadrant,
+  // [quadrant][column half][lane], and their ok flags [quadrant][half]
+  float* xmax = reinterpret_cast<float*>(tmem_holder + 4);
+  volatile int* xok = reinterpret_cast<volatile int*>(xmax + 4 * 2 * 32);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
-  const int qt = p.nq - 1 - (int)(blockIdx.x / BH);  // heaviest query tiles first
-  const int bh = blockIdx.x % BH, b = bh / p.H, h = bh % p.H;
+  // (batch, head)-major order: the CTAs running together share one head's K/V
+  // in L2; within a head the heaviest query tiles go first
+  const int bh = (int)(blockIdx.x / p.nq), b = bh / p.H, h = bh % p.H;
+  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);
   const int d = p.H * 128;
   const int row0 = b * p.T + qt * TILE;
   const int nkv = qt + 1;
@@ -134,7 +150,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc::mbar_init(kv_full + s, 1);
       tc::mbar_init(kv_empty + s, 1);
       tc::mbar_init(s_full + s, 1);
-      tc::mbar_init(p_full + s, 128);
+      tc::mbar_init(p_full + s, FWD_SOFT);
     }
     tc::mbar_init(pv_done, 1);
     tc::mbar_init(o_full, 1);
@@ -222,26 +238,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ---------------------------------------------------------------- softmax warps
-    const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;  // query row within the tile = TMEM lane
+    const int q4 = warp & 3;          // TMEM lane quadrant
+    const int ch = (warp - 2) >> 2;   // 64-column half of S (keys) and of O (dims)
+    const int r = q4 * 32 + lane;     // query row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = kLog2e * rsqrtf(128.f);
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;     // l: this warp's half of the row sum
     for (int j = 0; j < nkv; ++j) {
       const int s = j & 1;
-      bool ok = tc::mbar_wait(s_full + s, (j >> 1) & 1, abort_flag, kWaitNs);
-      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-      tc::tc_fence_after();
+      // a failure is only acted on at the pair exchange below, so that both
+      // warps of a quadrant leave the loop at the same barrier
+      bool ok = !failed && tc::mbar_wait(s_full + s, (j >> 1) & 1, abort_flag, kWaitNs);
+      ok = __all_sync(0xffffffffu, ok);
       const bool diag = (j == qt);
-      float v[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + s * 128 + lane_off + c * 32, v + c * 32);
+      float v[64];
       float mx = -INFINITY;
+      if (ok) {
+        tc::tc_fence_after();
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        v[i] *= sl2;
-        if (!diag || i <= r) mx = fmaxf(mx, v[i]);
+        for (int c = 0; c < 2; ++c) tc::tmem_ld32(tmem + s * 128 + lane_off + ch * 64 + c * 32, v + c * 32);
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (ch * 64 + i <= r) mx = fmaxf(mx, v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
+        }
+        mx *= sl2;  // the scale is positive, so it commutes with the max
       }
+      // both warps of the quadrant always meet here, whatever their waits gave;
+      // the second barrier keeps the slots until both have read them
+      const int slot = (q4 * 2 + ch) * 32 + lane, oslot = (q4 * 2 + (ch ^ 1)) * 32 + lane;
+      xmax[slot] = mx;
+      if (lane == 0) xok[q4 * 2 + ch] = ok ? 1 : 0;
+      bar_pair(1 + q4);
+      const bool ok_both = ok && xok[q4 * 2 + (ch ^ 1)] != 0;
+      mx = fmaxf(mx, xmax[oslot]);
+      bar_pair(1 + q4);
+      if (!ok_both) { failed = true; break; }
       const bool grow = mx > m + kRescaleLog2;
       if (__any_sync(0xffffffffu, grow)) {
         // move this warp's reference maxima up; rows of O that already hold
@@ -252,48 +287,68 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         m = m_new;
         if (j > 0) {
           ok = tc::mbar_wait(pv_done, (j - 1) & 1, abort_flag, kWaitNs);
-          if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-          tc::tc_fence_after();
+          if (!__all_sync(0xffffffffu, ok)) {
+            failed = true;  // reported to the partner at the next exchange
+          } else {
+            tc::tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tc::tmem_ld32(tO + lane_off + c * 32, o);
+            for (int c = 0; c < 2; ++c) {
+              float o[32];
+              tc::tmem_ld32(tO + lane_off + ch * 64 + c * 32, o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc::tmem_st32(tO + lane_off + c * 32, o);
+              for (int i = 0; i < 32; ++i) o[i] *= alpha;
+              tc::tmem_st32(tO + lane_off + ch * 64 + c * 32, o);
+            }
           }
         }
       }
       float rs = 0.f;
       uint8_t* pbuf = sP + s * TILE_BYTES;
+      const float nm = -m;
 #pragma unroll
-      for (int g = 0; g < 16; ++g) {
+      for (int g = 0; g < 8; ++g) {
         float e[8];
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k = g * 8 + i;
-          e[i] = (!diag || k <= r) ? exp2f(v[k] - m) : 0.f;
-          rs += e[i];
+          for (int i = 0; i < 8; ++i) {
+            const int k = g * 8 + i;
+            e[i] = (ch * 64 + k <= r) ? tc::ex2(fmaf(v[k], sl2, nm)) : 0.f;
+            rs += e[i];
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            e[i] = tc::ex2(fmaf(v[g * 8 + i], sl2, nm));
+            rs += e[i];
+          }
         }
-        st_tile8(pbuf, r, g, pack8(e));
+        st_tile8(pbuf, r, ch * 8 + g, pack8(e));
       }
       l += rs;
       fence_async_smem();
       tc::tc_fence_before();
       tc::mbar_arrive(p_full + s);
     }
-    if (!failed) {
-      bool ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
-      if (!__all_sync(0xffffffffu, ok)) failed = true;
+    bool ok = !failed;
+    if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
+    ok = __all_sync(0xffffffffu, ok);
+    // combine the two halves of the row sum
+    {
+      const int slot = (q4 * 2 + ch) * 32 + lane, oslot = (q4 * 2 + (ch ^ 1)) * 32 + lane;
+      xmax[slot] = l;
+      if (lane == 0) xok[q4 * 2 + ch] = ok ? 1 : 0;
+      bar_pair(1 + q4);
+      ok = ok && xok[q4 * 2 + (ch ^ 1)] != 0;
+      l += xmax[oslot];
     }
-    if (!failed) {
+    if (__all_sync(0xffffffffu, ok)) {
       tc::tc_fence_after();
       const float inv = 1.f / l;
-      bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128;
+      bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128 + ch * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[32];
-        tc::tmem_ld32(tO + lane_off + c * 32, o);
+        tc::tmem_ld32(tO + lane_off + ch * 64 + c * 32, o);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           float w8[8];
@@ -302,8 +357,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = pack8(w8);
         }
       }
-      p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
+      if (ch == 0) p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
     } else {
+      failed = true;
       *abort_flag = 1;
     }
   }
@@ -318,47 +374,70 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 // ============================================================== backward
+//
+// One CTA per (b, h, 128-key tile); 10 warps: TMA producer, MMA issuer and
+// eight softmax/epilogue warps (two per TMEM lane quadrant, each owning 64 of
+// the 128 query columns). TMEM: [0,128) S^T, overwritten in place by P^T as
+// packed bf16 (query half c at columns 64c .. 64c+31), [128,256) dP^T and
+// then dQ, [256,384) dV, [384,512) dK. Shared memory: K, V, two Q/dO stages
+// (the next query tile loads while this one computes) and dS^T.
+// Per query tile: S^T = K Q^T and dP^T = V dO^T; P^T = exp(S^T - lse),
+// dS^T = P^T (dP^T - D); dV += P^T dO (A operand read from TMEM),
+// dK += dS^T Q, dQ = dS K; dQ is added to the fp32 plane with vector atomics
+// while the next tile's S^T is already being computed.
 
-__global__ void __launch_bounds__(NTHREADS, 1)
+constexpr int BWD_WARPS = 10;
+constexpr int BWD_THREADS = 32 * BWD_WARPS;
+constexpr int BWD_SOFT = 32 * (BWD_WARPS - 2);  // 256 softmax threads
+
+__global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ AttnParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (tc::smem_u32(smem_raw) & 1023) {  // see the forward kernel
+    if (threadIdx.x == 0) set_status(p.status, DEV_BAD_LAUNCH);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem;
   uint8_t* sV = sK + TILE_BYTES;
-  uint8_t* sQ = sV + TILE_BYTES;
-  uint8_t* sdO = sQ + TILE_BYTES;
-  uint8_t* sPt = sdO + TILE_BYTES;
-  uint8_t* sdSt = sPt + TILE_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sdSt + TILE_BYTES);
+  uint8_t* sQ = sV + TILE_BYTES;      // 2 stages
+  uint8_t* sdO = sQ + 2 * TILE_BYTES; // 2 stages
+  uint8_t* sdSt = sdO + 2 * TILE_BYTES;
+  float* sLD = reinterpret_cast<float*>(sdSt + TILE_BYTES);  // [stage][lse 128 | D 128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + 2 * 2 * TILE);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;
-  uint64_t* q_empty = bars + 2;
-  uint64_t* st_full = bars + 3;
-  uint64_t* p_full = bars + 4;
-  uint64_t* dq_full = bars + 5;
-  uint64_t* tm_free = bars + 6;
-  uint64_t* acc_full = bars + 7;
-  uint64_t* drain = bars + 8;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* q_full = bars + 1;    // [2]
+  uint64_t* q_empty = bars + 3;   // [2]
+  uint64_t* st_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* dq_full = bars + 7;
+  uint64_t* tm_free = bars + 8;
+  uint64_t* acc_full = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int BH = p.B * p.H;
-  const int kt = (int)(blockIdx.x / BH);  // key tile; small kt has the most query tiles
-  const int bh = blockIdx.x % BH, b = bh / p.H, h = bh % p.H;
+  // (batch, head)-major order: the CTAs running together share one head's
+  // Q, dO and dq rows in L2 (dq is accumulated with atomics); within a head
+  // the key tiles with the most query tiles (small kt) go first
+  const int bh = (int)(blockIdx.x / p.nq), b = bh / p.H, h = bh % p.H;
+  const int kt = (int)(blockIdx.x % p.nq);
   const int d = p.H * 128;
   const int krow0 = b * p.T + kt * TILE;
   const int nit = p.nq - kt;  // query tiles qt = kt .. nq-1
 
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
-    tc::mbar_init(q_full, 1);
-    tc::mbar_init(q_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      tc::mbar_init(q_full + s, 1);
+      tc::mbar_init(q_empty + s, 1);
+    }
     tc::mbar_init(st_full, 1);
-    tc::mbar_init(p_full, 128);
+    tc::mbar_init(p_full, BWD_SOFT);
     tc::mbar_init(dq_full, 1);
-    tc::mbar_init(tm_free, 128);
+    tc::mbar_init(tm_free, BWD_SOFT);
     tc::mbar_init(acc_full, 1);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -373,7 +452,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
-  const uint32_t tdQ = tS;  // S^T is consumed before dQ is formed
+  const uint32_t tdQ = tdP;  // dP^T is consumed before dQ is formed
   bool failed = false;
 
   if (warp == 0) {
@@ -385,21 +464,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc::tma_load_2d(sK + HALF_BYTES, &tqkv, d + h * 128 + 64, krow0, kv_full);
       tc::tma_load_2d(sV, &tqkv, 2 * d + h * 128, krow0, kv_full);
       tc::tma_load_2d(sV + HALF_BYTES, &tqkv, 2 * d + h * 128 + 64, krow0, kv_full);
-      int last = -1;
+      bool issued[2] = {false, false};
+      uint32_t iphase[2] = {0, 0};
       for (int it = 0; it < nit; ++it) {
-        if (!tc::mbar_wait(q_empty, (it & 1) ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!tc::mbar_wait(q_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
         const int qr = b * p.T + (kt + it) * TILE;
-        tc::mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
-        tc::tma_load_2d(sQ, &tqkv, h * 128, qr, q_full);
-        tc::tma_load_2d(sQ + HALF_BYTES, &tqkv, h * 128 + 64, qr, q_full);
-        tc::tma_load_2d(sdO, &tdo, h * 128, qr, q_full);
-        tc::tma_load_2d(sdO + HALF_BYTES, &tdo, h * 128 + 64, qr, q_full);
-        last = it;
+        const size_t lrow = ((size_t)b * p.H + h) * p.T + (size_t)(kt + it) * TILE;
+        tc::mbar_arrive_expect_tx(q_full + s, 2 * TILE_BYTES + 2 * TILE * 4);
+        tc::bulk_load(sLD + s * 2 * TILE, p.lse + lrow, TILE * 4, q_full + s);
+        tc::bulk_load(sLD + s * 2 * TILE + TILE, p.Drow + lrow, TILE * 4, q_full + s);
+        tc::tma_load_2d(sQ + s * TILE_BYTES, &tqkv, h * 128, qr, q_full + s);
+        tc::tma_load_2d(sQ + s * TILE_BYTES + HALF_BYTES, &tqkv, h * 128 + 64, qr, q_full + s);
+        tc::tma_load_2d(sdO + s * TILE_BYTES, &tdo, h * 128, qr, q_full + s);
+        tc::tma_load_2d(sdO + s * TILE_BYTES + HALF_BYTES, &tdo, h * 128 + 64, qr, q_full + s);
+        issued[s] = true;
+        iphase[s] = ph;
       }
       if (failed) {
         *abort_flag = 1;
         tc::mbar_wait(kv_full, 0, nullptr, kWaitNs);
-        if (last >= 0) tc::mbar_wait(q_full, last & 1, nullptr, kWaitNs);
+        for (int s = 0; s < 2; ++s)
+          if (issued[s]) tc::mbar_wait(q_full + s, iphase[s], nullptr, kWaitNs);
       }
     }
   } else if (warp == 1) {
@@ -407,25 +494,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t id_kk = tc::idesc_bf16(128, 128, 0, 0);   // both K-major
       const uint32_t id_kmn = tc::idesc_bf16(128, 128, 0, 1);  // B MN-major
       const uint32_t id_mnmn = tc::idesc_bf16(128, 128, 1, 1); // A and B MN-major
-      const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aQ = tc::smem_u32(sQ);
-      const uint32_t adO = tc::smem_u32(sdO), aPt = tc::smem_u32(sPt), adSt = tc::smem_u32(sdSt);
+      const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), adSt = tc::smem_u32(sdSt);
       bool any = false;
       if (!tc::mbar_wait(kv_full, 0, abort_flag, kWaitNs)) failed = true;
       for (int it = 0; it < nit && !failed; ++it) {
-        if (!tc::mbar_wait(q_full, it & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        const int s = it & 1;
+        const uint32_t aQ = tc::smem_u32(sQ + s * TILE_BYTES), adO = tc::smem_u32(sdO + s * TILE_BYTES);
+        if (!tc::mbar_wait(q_full + s, (it >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        // S^T overwrites P^T of the previous tile: wait until its products finished
+        if (it > 0 && !tc::mbar_wait(dq_full, (it - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        tc::tc_fence_after();
+        mma_tile(tS, aK, false, aQ, false, id_kk, false);       // S^T  = K Q^T
+        any = true;
+        // dP^T overwrites dQ of the previous tile: wait until it was read out
         if (it > 0 && !tc::mbar_wait(tm_free, (it - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
         tc::tc_fence_after();
-        mma_tile(tS, aK, false, aQ, false, id_kk, false);     // S^T  = K Q^T
-        mma_tile(tdP, aV, false, adO, false, id_kk, false);   // dP^T = V dO^T
+        mma_tile(tdP, aV, false, adO, false, id_kk, false);     // dP^T = V dO^T
         tc::mma_commit(st_full);
-        any = true;
         if (!tc::mbar_wait(p_full, it & 1, abort_flag, kWaitNs)) { failed = true; break; }
         tc::tc_fence_after();
-        mma_tile(tdV, aPt, false, adO, true, id_kmn, it > 0);   // dV += P^T dO
+        // dV += P^T dO with P^T in TMEM: k-step k reads query columns 16k..16k+15
+#pragma unroll
+        for (int k = 0; k < TILE / 16; ++k)
+          tc::mma_bf16_tmem_a(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn,
+                              (it > 0 || k > 0) ? 1u : 0u);
         mma_tile(tdK, adSt, false, aQ, true, id_kmn, it > 0);   // dK += dS^T Q
         mma_tile(tdQ, adSt, true, aK, true, id_mnmn, false);    // dQ  = dS K
         tc::mma_commit(dq_full);
-        tc::mma_commit(q_empty);
+        tc::mma_commit(q_empty + s);
       }
       if (!failed) tc::mma_commit(acc_full);
       if (failed) {
@@ -439,43 +535,53 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else {
     // ---------------------------------------------------------------- softmax / epilogue warps
     const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;  // key row of this CTA (and query row of the dQ tile)
+    const int ch = (warp - 2) >> 2;  // query-column half owned by this warp
+    const int r = q4 * 32 + lane;    // key row of this CTA (and query row of the dQ tile)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = kLog2e * rsqrtf(128.f);
     const float scale = rsqrtf(128.f);
-    const size_t bhT = ((size_t)b * p.H + h) * p.T;
     for (int it = 0; it < nit; ++it) {
       const int qt = kt + it;
-      const float* Lq = p.lse + bhT + qt * TILE;   // same 128 values for every thread: L1 broadcast
-      const float* Dq = p.Drow + bhT + qt * TILE;
+      const int s = it & 1;
+      const float* Lq = sLD + s * 2 * TILE + ch * 64;        // lse of this warp's 64 query columns
+      const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
       bool ok = tc::mbar_wait(st_full, it & 1, abort_flag, kWaitNs);
+      // the lse / D rows arrived with this tile's Q (already complete here)
+      ok = ok && tc::mbar_wait(q_full + s, (it >> 1) & 1, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
       const bool diag = (it == 0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float sv[32], dp[32];
-        tc::tmem_ld32(tS + lane_off + c * 32, sv);
-        tc::tmem_ld32(tdP + lane_off + c * 32, dp);
+        tc::tmem_ld32(tS + lane_off + ch * 64 + c * 32, sv);
+        tc::tmem_ld32(tdP + lane_off + ch * 64 + c * 32, dp);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const float4 l0 = __ldg(reinterpret_cast<const float4*>(Lq + c * 32 + g * 8));
-          const float4 l1 = __ldg(reinterpret_cast<const float4*>(Lq + c * 32 + g * 8 + 4));
-          const float4 d0 = __ldg(reinterpret_cast<const float4*>(Dq + c * 32 + g * 8));
-          const float4 d1 = __ldg(reinterpret_cast<const float4*>(Dq + c * 32 + g * 8 + 4));
+          const float4 l0 = *reinterpret_cast<const float4*>(Lq + c * 32 + g * 8);
+          const float4 l1 = *reinterpret_cast<const float4*>(Lq + c * 32 + g * 8 + 4);
+          const float4 d0 = *reinterpret_cast<const float4*>(Dq + c * 32 + g * 8);
+          const float4 d1 = *reinterpret_cast<const float4*>(Dq + c * 32 + g * 8 + 4);
           const float Lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
           const float Dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            const int qc = c * 32 + g * 8 + i;  // query column within the tile
-            const bool keep = !diag || (qc >= r);
-            const float pr = keep ? exp2f(fmaf(sv[g * 8 + i], sl2, -Lv[i] * kLog2e)) : 0.f;
+            const int qc = ch * 64 + c * 32 + g * 8 + i;  // query column within the tile
+            float pr = tc::ex2(fmaf(sv[g * 8 + i], sl2, -Lv[i] * kLog2e));
+            if (diag && qc < r) pr = 0.f;
             sv[g * 8 + i] = pr;
             dp[g * 8 + i] = pr * (dp[g * 8 + i] - Dv[i]);
           }
-          st_tile8(sPt, r, c * 4 + g, pack8(sv + 8 * g));
-          st_tile8(sdSt, r, c * 4 + g, pack8(dp + 8 * g));
+          st_tile8(sdSt, r, ch * 8 + c * 4 + g, pack8(dp + 8 * g));
         }
+        // P^T of these 32 query columns -> 16 packed bf16 pairs in TMEM
+        float pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * i], sv[2 * i + 1]);
+          pk[i] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
+        }
+        tc::tmem_st16(tS + lane_off + ch * 64 + c * 16, pk);
       }
       fence_async_smem();
       tc::tc_fence_before();
@@ -483,12 +589,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = tc::mbar_wait(dq_full, it & 1, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
-      // dQ tile row r (query qt*128 + r): add scale * dQ into the fp32 buffer
-      float* dqrow = p.dq + (size_t)(b * p.T + qt * TILE + r) * d + h * 128;
+      // dQ tile row r (query qt*128 + r), this warp's 64 columns
+      float* dqrow = p.dq + (size_t)(b * p.T + qt * TILE + r) * d + h * 128 + ch * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tc::tmem_ld32(tdQ + lane_off + c * 32, v);
+        tc::tmem_ld32(tdQ + lane_off + ch * 64 + c * 32, v);
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           atomicAdd(reinterpret_cast<float4*>(dqrow + c * 32 + g * 4),
@@ -504,17 +610,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (!failed) {
       tc::tc_fence_after();
       const size_t m = (size_t)krow0 + r;
-      float* dkrow = p.dk + m * d + h * 128;
-      bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128;
+      float* dkrow = p.dk + m * d + h * 128 + ch * 64;
+      bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128 + ch * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tc::tmem_ld32(tdK + lane_off + c * 32, v);
+        tc::tmem_ld32(tdK + lane_off + ch * 64 + c * 32, v);
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           *reinterpret_cast<float4*>(dkrow + c * 32 + g * 4) =
               make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
-        tc::tmem_ld32(tdV + lane_off + c * 32, v);
+        tc::tmem_ld32(tdV + lane_off + ch * 64 + c * 32, v);
 #pragma unroll
         for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dvrow + c * 32 + g * 8) = pack8(v + 8 * g);
       }
@@ -559,8 +665,8 @@ bool map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int FWD_SMEM = 7 * TILE_BYTES + 1024 + 256;
-constexpr int BWD_SMEM = 6 * TILE_BYTES + 1024 + 256;
+constexpr int FWD_SMEM = 7 * TILE_BYTES + 2048;  // tiles, barriers + exchange
+constexpr int BWD_SMEM = 7 * TILE_BYTES + 2 * 2 * TILE * 4 + 256;
 
 }  // namespace
 
@@ -577,7 +683,7 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
   p.o = o; p.lse = lse; p.status = status;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_fwd_tc_k<<<B * H * p.nq, NTHREADS, FWD_SMEM, s>>>(tq, p);
+  attn_fwd_tc_k<<<B * H * p.nq, FWD_THREADS, FWD_SMEM, s>>>(tq, p);
   return cudaGetLastError();
 }
 
@@ -596,7 +702,7 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_bwd_tc_k<<<B * H * p.nq, NTHREADS, BWD_SMEM, s>>>(tq, tdo, p);
+  attn_bwd_tc_k<<<B * H * p.nq, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, p);
   return cudaGetLastError();
 }
 
