@@ -12,11 +12,16 @@
 // epilogue of tile i overlaps the main loop of tile i+1), warps 2..9 read the
 // accumulator with tcgen05.ld (one thread per output row and 128-column half)
 // and run the epilogue. Weight-gradient shapes (few output tiles, K = tokens)
-// split K across CTAs into fp32 partial slabs that a reduction kernel sums. Every wait is bounded; on timeout the kernel records
+// split K across CTAs into fp32 partial slabs that a reduction kernel sums.
+// CTAs run as 2-CTA clusters on vertically adjacent tiles: each loads its own
+// A rows and half of the shared B tile, multicast into both CTAs' shared
+// memory, so each CTA pulls 32 KB instead of 48 KB from L2 per k-slice; a
+// stage is free again once the MMAs of both CTAs have committed. Every wait is bounded; on timeout the kernel records
 // DEV_TIMEOUT, unwinds, frees its TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "ops.cuh"
 #include "tc_ptx.cuh"
@@ -41,10 +46,17 @@ struct TcParams {
   int splits, kb_per_split;
 };
 
-// Work unit u covers output tile u / splits and k-blocks [kb0, kb1).
-__device__ __forceinline__ void unit_range(const TcParams& p, int u, int& tile, int& split, int& kb0, int& kb1) {
-  tile = u / p.splits;
-  split = u % p.splits;
+// Work unit v of a CTA (CL = 1) or of a CTA pair (CL = 2: the two CTAs of a
+// cluster take vertically adjacent 128-row blocks that share the B tile):
+// row offset m0, column block nb, k-split and its k-blocks [kb0, kb1).
+template <int CL>
+__device__ __forceinline__ void unit_of(const TcParams& p, int v, int rank, int& m0, int& nb, int& split, int& kb0,
+                                        int& kb1) {
+  const int t = v / p.splits;
+  split = v % p.splits;
+  const int mb = (CL == 1) ? t / p.num_n : 2 * (t / p.num_n) + rank;
+  nb = t % p.num_n;
+  m0 = mb * BM;
   kb0 = split * p.kb_per_split;
   kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   if (kb1 < kb0) kb1 = kb0;
@@ -138,7 +150,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int nc0, flo
   }
 }
 
-template <int EPI, int A_MN, int B_MN>
+template <int EPI, int A_MN, int B_MN, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_k(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
               const __grid_constant__ TcParams p) {
@@ -156,11 +168,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   const GemmArgs& g = p.g;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+  const int rank = (CL == 2) ? (int)tc::cluster_ctarank() : 0;
+  const int v_first = (CL == 2) ? (int)blockIdx.x / 2 : (int)blockIdx.x;
+  const int v_step = (CL == 2) ? (int)gridDim.x / 2 : (int)gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, 1);
+      tc::mbar_init(empty + s, CL);  // each CTA of the pair releases the stage
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tfull + b, 1);
@@ -180,6 +195,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  if (CL == 2) tc::cluster_sync();  // the peer's barriers exist before any multicast
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   bool failed = false;
@@ -192,10 +208,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t issued_phase[STAGES];
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
-      for (int u = blockIdx.x; u < p.total && !failed; u += gridDim.x) {
-        int tile, split, kb0, kb1;
-        unit_range(p, u, tile, split, kb0, kb1);
-        const int m0 = (tile / p.num_n) * BM, n0 = (tile % p.num_n) * BN;
+      for (int v = v_first; v < p.total && !failed; v += v_step) {
+        int m0, nb, split, kb0, kb1;
+        unit_of<CL>(p, v, rank, m0, nb, split, kb0, kb1);
+        const int n0 = nb * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
           tc::mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
@@ -208,7 +224,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           } else {
             tc::tma_load_2d(a, &ta, k0, m0, full + stage);
           }
-          if (B_MN) {
+          if (CL == 2) {
+            // this CTA fetches half of the shared B tile for both CTAs
+            if (B_MN) {
+#pragma unroll
+              for (int j = 2 * rank; j < 2 * rank + 2; ++j)
+                tc::tma_load_2d_multicast(b + j * 8192, &tb, n0 + 64 * j, k0, full + stage, 0x3);
+            } else {
+              tc::tma_load_2d_multicast(b + rank * (B_BYTES / 2), &tb, k0, n0 + (BN / 2) * rank, full + stage, 0x3);
+            }
+          } else if (B_MN) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) tc::tma_load_2d(b + j * 8192, &tb, n0 + 64 * j, k0, full + stage);
           } else {
@@ -234,9 +259,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       uint32_t phase = 0;
       int cnt = 0;
       bool any_mma = false;
-      for (int u = blockIdx.x; u < p.total && !failed; u += gridDim.x, ++cnt) {
-        int tile, split, kb0, kb1;
-        unit_range(p, u, tile, split, kb0, kb1);
+      for (int v = v_first; v < p.total && !failed; v += v_step, ++cnt) {
+        int m0, nb, split, kb0, kb1;
+        unit_of<CL>(p, v, rank, m0, nb, split, kb0, kb1);
         const int ab = cnt & 1;
         const uint32_t aph = (cnt >> 1) & 1;
         if (!tc::mbar_wait(tempty + ab, aph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
@@ -255,7 +280,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                      : tc::sdesc_sw128(b_addr + k * 32, 16, 1024);
             tc::mma_bf16(dtm, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
-          tc::mma_commit(empty + stage);
+          if (CL == 2) tc::mma_commit_multicast(empty + stage, 0x3);  // frees the stage in both CTAs
+          else tc::mma_commit(empty + stage);
           any_mma = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -277,13 +303,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int ch = (warp - 2) >> 2;    // which 128-column half of the tile
     const int row = q * 32 + lane;
     int cnt = 0;
-    for (int u = blockIdx.x; u < p.total && !failed; u += gridDim.x, ++cnt) {
-      int tile, split, kb0, kb1;
-      unit_range(p, u, tile, split, kb0, kb1);
+    for (int v = v_first; v < p.total && !failed; v += v_step, ++cnt) {
+      int m0, nb, split, kb0, kb1;
+      unit_of<CL>(p, v, rank, m0, nb, split, kb0, kb1);
       const int ab = cnt & 1;
       const uint32_t aph = (cnt >> 1) & 1;
-      const int mb = tile / p.num_n, nb = tile % p.num_n;
-      const int m0 = mb * BM, n0 = nb * BN + ch * (BN / 2);
+      const int n0 = nb * BN + ch * (BN / 2);
       const bool ok = tc::mbar_wait(tfull + ab, aph, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; *abort_flag = 1; break; }
       tc::tc_fence_after();
@@ -366,6 +391,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  // neither CTA of a pair may leave while the other can still multicast
+  // into its shared memory or arrive on its barriers
+  if (CL == 2) tc::cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -403,24 +431,50 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
 
 typedef void (*KernFn)(CUtensorMap, CUtensorMap, TcParams);
 
-template <int EPI>
+template <int EPI, int CL>
 KernFn pick(int a_mn, int b_mn) {
-  if (!a_mn && !b_mn) return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 0, 0>);
-  if (!a_mn && b_mn) return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 0, 1>);
-  if (a_mn && !b_mn) return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 1, 0>);
-  return reinterpret_cast<KernFn>(gemm_tc_k<EPI, 1, 1>);
+  if (!a_mn && !b_mn) return gemm_tc_k<EPI, 0, 0, CL>;
+  if (!a_mn && b_mn) return gemm_tc_k<EPI, 0, 1, CL>;
+  if (a_mn && !b_mn) return gemm_tc_k<EPI, 1, 0, CL>;
+  return gemm_tc_k<EPI, 1, 1, CL>;
 }
 
+template <int CL>
 KernFn pick_kernel(int epi, int a_mn, int b_mn) {
   switch (epi) {
-    case EPI_STORE: return pick<EPI_STORE>(a_mn, b_mn);
-    case EPI_STORE_F32: return pick<EPI_STORE_F32>(a_mn, b_mn);
-    case EPI_RELU2: return pick<EPI_RELU2>(a_mn, b_mn);
-    case EPI_RELU2_BWD: return pick<EPI_RELU2_BWD>(a_mn, b_mn);
-    case EPI_CE_BWD: return pick<EPI_CE_BWD>(a_mn, b_mn);
-    case EPI_CE_FWD: return pick<EPI_CE_FWD>(a_mn, b_mn);
+    case EPI_STORE: return pick<EPI_STORE, CL>(a_mn, b_mn);
+    case EPI_STORE_F32: return pick<EPI_STORE_F32, CL>(a_mn, b_mn);
+    case EPI_RELU2: return pick<EPI_RELU2, CL>(a_mn, b_mn);
+    case EPI_RELU2_BWD: return pick<EPI_RELU2_BWD, CL>(a_mn, b_mn);
+    case EPI_CE_BWD: return pick<EPI_CE_BWD, CL>(a_mn, b_mn);
+    case EPI_CE_FWD: return pick<EPI_CE_FWD, CL>(a_mn, b_mn);
     default: return nullptr;
   }
+}
+
+// Most 2-CTA clusters of a kernel that can be resident at once (cached).
+std::mutex g_cl_mu;
+std::unordered_map<const void*, int> g_cl_max;
+
+int max_clusters(KernFn fn) {
+  std::lock_guard<std::mutex> lock(g_cl_mu);
+  auto it = g_cl_max.find(reinterpret_cast<const void*>(fn));
+  if (it != g_cl_max.end()) return it->second;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (g_num_sms / 2));
+  cfg.blockDim = dim3(NTHREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess || n < 1) n = g_num_sms / 2;
+  g_cl_max[reinterpret_cast<const void*>(fn)] = n;
+  return n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -443,11 +497,14 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   if (!gemm_tc_supports(g)) return cudaErrorNotSupported;
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (!get_encode()) return cudaErrorNotSupported;
+  // CTA pairs sharing the B tile whenever there are at least two row blocks
+  const int CLn = (g.M > BM) ? 2 : 1;
   CUtensorMap ta, tb;
   // TMA needs an extent of at least one element; an empty K reads nothing.
   uint64_t K = g.K > 0 ? (uint64_t)g.K : 1;
   bool ok = g.a_kmajor ? make_map(&ta, g.A, K, g.M, g.lda, 64, 128) : make_map(&ta, g.A, g.M, K, g.lda, 64, 64);
-  ok = ok && (g.b_kmajor ? make_map(&tb, g.B, K, g.N, g.ldb, 64, 256) : make_map(&tb, g.B, g.N, K, g.ldb, 64, 64));
+  ok = ok && (g.b_kmajor ? make_map(&tb, g.B, K, g.N, g.ldb, 64, CLn == 2 ? 128 : 256)
+                         : make_map(&tb, g.B, g.N, K, g.ldb, 64, 64));
   if (!ok) return cudaErrorInvalidValue;
   TcParams p;
   p.g = g;
@@ -456,15 +513,35 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   p.num_kb = (g.K + BK - 1) / BK;
   p.splits = (g.splits > 1 && g.epi == EPI_STORE_F32 && g.partial) ? g.splits : 1;
   p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
-  p.total = p.num_m * p.num_n * p.splits;
-  KernFn fn = pick_kernel(g.epi, !g.a_kmajor, !g.b_kmajor);
+  KernFn fn = CLn == 2 ? pick_kernel<2>(g.epi, !g.a_kmajor, !g.b_kmajor) : pick_kernel<1>(g.epi, !g.a_kmajor, !g.b_kmajor);
   if (!fn) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  int grid = p.total < g_num_sms ? p.total : g_num_sms;
-  fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, p);
-  e = cudaGetLastError();
+  if (CLn == 2) {
+    // work units are pairs of row blocks; one 2-CTA cluster per unit at a time
+    p.total = ((p.num_m + 1) / 2) * p.num_n * p.splits;
+    int clusters = max_clusters(fn);
+    if (clusters > p.total) clusters = p.total;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, p);
+  } else {
+    p.total = p.num_m * p.num_n * p.splits;
+    int grid = p.total < g_num_sms ? p.total : g_num_sms;
+    fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, p);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess || p.splits == 1) return e;
   return splitk_reduce(g.partial, p.splits, static_cast<float*>(g.C), g.ldc, g.M, g.N, g.beta, s);
 }
