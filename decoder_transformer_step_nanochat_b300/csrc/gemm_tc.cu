@@ -353,6 +353,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           g.p_arg[pi] = arg;
           if (t >= n0 && t < n0 + BN / 2) g.p_tgt[m] = tl;
         }
+      } else if (EPI == EPI_QKNORM_ROPE) {
+        // this warp's 128 columns are one head of q, k or v for its row:
+        // q and k heads get RMSNorm (eps 1e-6) then the half-split rotation
+        // by the position's angles; v heads are stored as they are
+        float v[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (have_acc) tc::tmem_ld32(taddr + c * 32, v + c * 32);
+          else
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[c * 32 + i] = 0.f;
+        }
+        if (row_ok && n0 < g.N) {
+          float ss = 0.f;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            v[i] *= g.alpha;
+            ss += v[i] * v[i];
+          }
+          if (n0 < 2 * g.d_model) {
+            const float rr = rsqrtf(ss * (1.f / 128.f) + kEps);
+            const int t = m % g.seq_len;
+            const float* cs = g.rope_cos + (size_t)t * 64;
+            const float* sn = g.rope_sin + (size_t)t * 64;
+#pragma unroll
+            for (int j4 = 0; j4 < 16; ++j4) {
+              const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs) + j4);
+              const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn) + j4);
+              const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int j = j4 * 4 + u;
+                const float a = v[j] * rr, b = v[j + 64] * rr;
+                v[j] = a * cc[u] - b * sv[u];
+                v[j + 64] = a * sv[u] + b * cc[u];
+              }
+            }
+            g.rqk[(size_t)m * (2 * g.d_model / 128) + n0 / 128] = rr;
+          }
+          bf16* crow = static_cast<bf16*>(g.C) + (size_t)m * g.ldc + n0;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) *reinterpret_cast<uint4*>(crow + 8 * j) = pack8_bf16(v + 8 * j);
+        }
       } else {
         for (int c = 0; c < BN / 64; ++c) {
           float v[32];
@@ -448,6 +491,7 @@ KernFn pick_kernel(int epi, int a_mn, int b_mn) {
     case EPI_RELU2_BWD: return pick<EPI_RELU2_BWD, CL>(a_mn, b_mn);
     case EPI_CE_BWD: return pick<EPI_CE_BWD, CL>(a_mn, b_mn);
     case EPI_CE_FWD: return pick<EPI_CE_FWD, CL>(a_mn, b_mn);
+    case EPI_QKNORM_ROPE: return pick<EPI_QKNORM_ROPE, CL>(a_mn, b_mn);
     default: return nullptr;
   }
 }
@@ -490,7 +534,10 @@ bool gemm_tc_supports(const GemmArgs& g) {
   if (g.ldc % 8 || !aligned16(g.C)) return false;
   if ((g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD) && (g.ldc2 % 8 || !aligned16(g.C2))) return false;
   if (g.epi == EPI_CE_BWD && (!g.row_f || !g.row_i)) return false;
-  return g.epi >= EPI_STORE && g.epi <= EPI_CE_FWD;
+  if (g.epi == EPI_QKNORM_ROPE &&
+      (!g.rope_cos || !g.rope_sin || !g.rqk || g.seq_len < 1 || g.d_model % 128 || g.N != 3 * g.d_model))
+    return false;
+  return g.epi >= EPI_STORE && g.epi <= EPI_QKNORM_ROPE;
 }
 
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {

@@ -369,8 +369,16 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
     const T* Wproj = P + param_offset(c, 4 + 4 * l, &rows, &cols);
 
     KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn1, r1, M, d, s));
-    CKS(gemm(c, mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_STORE, qkv, 3 * d)));
-    KL(NC_FAM_ROWS, 4.0 * M * d * sizeof(T) + 8.0 * M * H, 1, qk_norm_rope_fwd<T>(qkv, rqk, c->rope_cos, c->rope_sin, M, Tn, H, s));
+    if (c->use_tc) {
+      // QK-norm + RoPE fused into the QKV GEMM epilogue
+      GemmArgs gq = mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_QKNORM_ROPE, qkv, 3 * d);
+      gq.rope_cos = c->rope_cos; gq.rope_sin = c->rope_sin; gq.rqk = rqk;
+      gq.seq_len = Tn; gq.d_model = d;
+      CKS(gemm(c, gq));
+    } else {
+      CKS(gemm(c, mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_STORE, qkv, 3 * d)));
+      KL(NC_FAM_ROWS, 4.0 * M * d * sizeof(T) + 8.0 * M * H, 1, qk_norm_rope_fwd<T>(qkv, rqk, c->rope_cos, c->rope_sin, M, Tn, H, s));
+    }
     KL(NC_FAM_ATTN_FWD, attn_fwd_flops(c), 1, attn_fwd<T>(c, qkv, o, lse_att));
     CKS(gemm(c, mk(M, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
     KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn2, r2, M, d, s));
@@ -666,12 +674,20 @@ nc_status nc_op_gemm(nc_ctx* c, int M, int N, int K, const void* A, long long ld
                      const int32_t* row_i) {
   if (!c || c->prec < 0) return fail(NC_ERR_STATE, "context not configured");
   if (M < 0 || N < 0 || K < 0) return fail(NC_ERR_ARG, "negative size");
-  if (epi < EPI_STORE || epi > EPI_CE_BWD) return fail(NC_ERR_ARG, "epilogue %d not available here", epi);
+  if (epi < EPI_STORE || epi > EPI_QKNORM_ROPE || epi == EPI_CE_FWD)
+    return fail(NC_ERR_ARG, "epilogue %d not available here", epi);
+  if (epi == EPI_QKNORM_ROPE && (!c->use_tc || N != 3 * c->d || M != c->M || !C2))
+    return fail(NC_ERR_ARG, "the QK-norm + RoPE epilogue needs NC_BF16, N = 3*d_model, M = batch*seq_len and C2 = rqk");
   if (!A || !B || !C) return fail(NC_ERR_ARG, "null operand");
   if ((epi == EPI_RELU2 || epi == EPI_RELU2_BWD) && !C2) return fail(NC_ERR_ARG, "epilogue needs C2");
   if (epi == EPI_CE_BWD && (!row_f || !row_i)) return fail(NC_ERR_ARG, "epilogue needs row_f/row_i");
   GemmArgs g = mk(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, epi, C, ldc, alpha, beta);
   g.C2 = C2; g.ldc2 = ldc2; g.row_f = row_f; g.row_i = row_i;
+  if (epi == EPI_QKNORM_ROPE) {
+    g.C2 = nullptr;
+    g.rqk = static_cast<float*>(C2);
+    g.rope_cos = c->rope_cos; g.rope_sin = c->rope_sin; g.seq_len = c->T; g.d_model = c->d;
+  }
   return gemm(c, g);
 }
 

@@ -163,6 +163,39 @@ def test_gemm_split_k_weight_gradient_shape(nc, ak, bk):
         c.close()
 
 
+def test_qkv_gemm_with_fused_qk_norm_rope(nc):
+    # the QKV projection with QK-norm + RoPE in its epilogue, against the
+    # oracle's rmsnorm and rotation applied to the float64 product
+    import torch
+    B, T, H = 2, 256, 3
+    d, D = H * 128, 128
+    M = B * T
+    rng = np.random.default_rng(17)
+    x = rounded(rng.standard_normal((M, d)), 0)
+    w = rounded(rng.standard_normal((3 * d, d)) * 0.05, 0)
+    c = Ctx(nc, 1, d, H, T, 1024, B, 0)
+    try:
+        qkv = torch.zeros((M, 3 * d), dtype=torch.bfloat16, device="cuda")
+        rqk = torch.zeros((M, 2 * H), dtype=torch.float32, device="cuda")
+        dx, dw = torch_of(x, 0, nc), torch_of(w, 0, nc)
+        nc.nc_op_gemm(c.ctx, M, 3 * d, d, dx.data_ptr(), d, 1, dw.data_ptr(), d, 1, nc.NC_EPI_QKNORM_ROPE,
+                      1.0, 0.0, qkv.data_ptr(), 3 * d, rqk.data_ptr(), 0)
+        nc.nc_sync(c.ctx)
+        acc = (x.astype(np.float64) @ w.astype(np.float64).T).reshape(B, T, 3, H, D)
+        got = host(qkv).reshape(B, T, 3, H, D)
+        cos, sin = oracle.rope_angles(T)
+        for b in range(B):
+            for which in (0, 1):
+                n, rr = oracle.rmsnorm(acc[b, :, which])
+                ok, err = close_enough(got[b, :, which], oracle.rope(n, cos, sin), 0)
+                assert ok, err
+                np.testing.assert_allclose(rqk.cpu().numpy().reshape(B, T, 2, H)[b, :, which], rr[..., 0], rtol=1e-4)
+            ok, err = close_enough(got[b, :, 2], acc[b, :, 2], 0)
+            assert ok, err
+    finally:
+        c.close()
+
+
 # ---------------------------------------------------------------- attention
 
 def _qkv(rng, B, T, H, prec):
