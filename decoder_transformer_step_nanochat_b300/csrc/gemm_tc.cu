@@ -38,7 +38,8 @@ constexpr int NEPI_WARPS = 8;           // two per TMEM lane quadrant, each half
 constexpr int NTHREADS = 64 + 32 * NEPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int STAGING_BYTES = 4096;  // per epilogue warp: 32 rows x 128 B, 128B-swizzled
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NEPI_WARPS * STAGING_BYTES + 1024 + 256;
 
 struct TcParams {
   GemmArgs g;
@@ -150,15 +151,58 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int nc0, flo
   }
 }
 
+// One 32-row x 128-byte chunk of an epilogue warp goes out through its
+// staging buffer: each lane writes its row's 8 16-byte pieces in the
+// 128-byte swizzle the output tensor map expects, then lane 0 issues one
+// bulk tensor store (or fp32 reduce-add). The buffer is reused only after the
+// previous store has read it.
+struct Stager {
+  uint8_t* buf;
+  int lane;
+  __device__ __forceinline__ void begin() {
+    if (lane == 0) tc::bulk_wait_read();
+    __syncwarp();
+  }
+  __device__ __forceinline__ void put(int j, uint4 v) {
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+  }
+  __device__ __forceinline__ void store(const CUtensorMap* map, int x, int y, bool add) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      if (add) tc::tma_reduce_add_2d(map, buf, x, y);
+      else tc::tma_store_2d(map, buf, x, y);
+      tc::bulk_commit();
+    }
+  }
+  __device__ __forceinline__ void store3(const CUtensorMap* map, int x, int y, int z) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                       reinterpret_cast<uint64_t>(map)),
+                   "r"(tc::smem_u32(buf)), "r"(x), "r"(y), "r"(z)
+                   : "memory");
+      tc::bulk_commit();
+    }
+  }
+};
+
+__device__ __forceinline__ uint4 f4u(float a, float b, float c, float d) {
+  return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
+}
+
 template <int EPI, int A_MN, int B_MN, int CL>
 __global__ void __launch_bounds__(NTHREADS, 1)
     gemm_tc_k(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
+              const __grid_constant__ CUtensorMap tc_, const __grid_constant__ CUtensorMap tc2,
               const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * B_BYTES);
+  uint8_t* sStage = sB + STAGES * B_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + NEPI_WARPS * STAGING_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -302,6 +346,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int q = warp & 3;            // TMEM lane quadrant this warp may read
     const int ch = (warp - 2) >> 2;    // which 128-column half of the tile
     const int row = q * 32 + lane;
+    Stager stg{sStage + (warp - 2) * STAGING_BYTES, lane};
     int cnt = 0;
     for (int v = v_first; v < p.total && !failed; v += v_step, ++cnt) {
       int m0, nb, split, kb0, kb1;
@@ -353,75 +398,139 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           g.p_arg[pi] = arg;
           if (t >= n0 && t < n0 + BN / 2) g.p_tgt[m] = tl;
         }
-      } else if (EPI == EPI_QKNORM_ROPE) {
-        // this warp's 128 columns are one head of q, k or v for its row:
-        // q and k heads get RMSNorm (eps 1e-6) then the half-split rotation
-        // by the position's angles; v heads are stored as they are
-        float v[128];
+      } else {
+        // ---- outputs leave through the staging buffer as bulk tensor stores
+        const int rblk = m0 + q * 32;  // first row of this warp's 32-row block
+        const bool blk_ok = rblk < g.M;
+        if (EPI == EPI_STORE_F32) {
+          const bool direct = (p.splits == 1 && g.beta != 0.f && g.beta != 1.f);
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            if (have_acc) tc::tmem_ld32(taddr + c * 32, v);
+            else
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          if (have_acc) tc::tmem_ld32(taddr + c * 32, v + c * 32);
-          else
+              for (int i = 0; i < 32; ++i) v[i] = 0.f;
+            const int nc0 = n0 + c * 32;
+            if (!blk_ok || nc0 >= g.N) continue;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[c * 32 + i] = 0.f;
-        }
-        if (row_ok && n0 < g.N) {
-          float ss = 0.f;
+            for (int i = 0; i < 32; ++i) v[i] *= g.alpha;
+            if (direct) {  // general beta: read-modify-write from registers
+              if (row_ok) epi_chunk<EPI>(g, m, nc0, v);
+              continue;
+            }
+            stg.begin();
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            v[i] *= g.alpha;
-            ss += v[i] * v[i];
+            for (int j = 0; j < 8; ++j) stg.put(j, f4u(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            if (p.splits > 1) stg.store3(&tc2, nc0, rblk, split);    // this split's partial slab
+            else stg.store(&tc_, nc0, rblk, g.beta == 1.f);          // C = acc, or C += acc
           }
-          if (n0 < 2 * g.d_model) {
-            const float rr = rsqrtf(ss * (1.f / 128.f) + kEps);
-            const int t = m % g.seq_len;
-            const float* cs = g.rope_cos + (size_t)t * 64;
-            const float* sn = g.rope_sin + (size_t)t * 64;
+        } else {
+          // bf16 outputs: two chunks of 64 columns
+          float v[128];
+          if (EPI == EPI_QKNORM_ROPE) {
 #pragma unroll
-            for (int j4 = 0; j4 < 16; ++j4) {
-              const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs) + j4);
-              const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn) + j4);
-              const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+            for (int c = 0; c < 4; ++c) {
+              if (have_acc) tc::tmem_ld32(taddr + c * 32, v + c * 32);
+              else
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int j = j4 * 4 + u;
-                const float a = v[j] * rr, b = v[j + 64] * rr;
-                v[j] = a * cc[u] - b * sv[u];
-                v[j + 64] = a * sv[u] + b * cc[u];
+                for (int i = 0; i < 32; ++i) v[c * 32 + i] = 0.f;
+            }
+            if (row_ok && n0 < g.N) {
+              // this warp's 128 columns are one head of q, k or v for its row:
+              // q and k heads get RMSNorm (eps 1e-6) then the half-split
+              // rotation by the position's angles; v heads pass through
+              float ss = 0.f;
+#pragma unroll
+              for (int i = 0; i < 128; ++i) {
+                v[i] *= g.alpha;
+                ss += v[i] * v[i];
+              }
+              if (n0 < 2 * g.d_model) {
+                const float rr = rsqrtf(ss * (1.f / 128.f) + kEps);
+                const int t = m % g.seq_len;
+                const float* cs = g.rope_cos + (size_t)t * 64;
+                const float* sn = g.rope_sin + (size_t)t * 64;
+#pragma unroll
+                for (int j4 = 0; j4 < 16; ++j4) {
+                  const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs) + j4);
+                  const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn) + j4);
+                  const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+                  for (int u = 0; u < 4; ++u) {
+                    const int j = j4 * 4 + u;
+                    const float a = v[j] * rr, b = v[j + 64] * rr;
+                    v[j] = a * cc[u] - b * sv[u];
+                    v[j + 64] = a * sv[u] + b * cc[u];
+                  }
+                }
+                g.rqk[(size_t)m * (2 * g.d_model / 128) + n0 / 128] = rr;
               }
             }
-            g.rqk[(size_t)m * (2 * g.d_model / 128) + n0 / 128] = rr;
           }
-          bf16* crow = static_cast<bf16*>(g.C) + (size_t)m * g.ldc + n0;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) *reinterpret_cast<uint4*>(crow + 8 * j) = pack8_bf16(v + 8 * j);
-        }
-      } else {
-        for (int c = 0; c < BN / 64; ++c) {
-          float v[32];
-          if (have_acc) tc::tmem_ld32(taddr + c * 32, v);
-          else
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float* w = v + h2 * 64;
+            if (EPI != EPI_QKNORM_ROPE) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.f;
-          const int nc0 = n0 + c * 32;
-          if (!row_ok || nc0 >= g.N) continue;
+              for (int c = 0; c < 2; ++c) {
+                if (have_acc) tc::tmem_ld32(taddr + h2 * 64 + c * 32, w + c * 32);
+                else
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= g.alpha;
-          if (EPI == EPI_STORE_F32 && p.splits > 1) {
-            // raw partial sum of this k-split; the reduction adds beta*C
-            float* c0 = g.partial + ((size_t)split * g.M + m) * g.N + nc0;
+                  for (int i = 0; i < 32; ++i) w[c * 32 + i] = 0.f;
+              }
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (nc0 + 4 * j < g.N)
-                *reinterpret_cast<float4*>(c0 + 4 * j) = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          } else {
-            epi_chunk<EPI>(g, m, nc0, v);
+              for (int i = 0; i < 64; ++i) w[i] *= g.alpha;
+            }
+            const int nc0 = n0 + h2 * 64;
+            if (!blk_ok || nc0 >= g.N) continue;
+            if (EPI == EPI_RELU2_BWD) {
+              if (row_ok) {
+                const bf16* u = static_cast<const bf16*>(g.C2) + (size_t)m * g.ldc2 + nc0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  float uf[8];
+                  if (nc0 + 8 * j < g.N) unpack8_bf16(*reinterpret_cast<const uint4*>(u + 8 * j), uf);
+                  else
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) uf[i] = 0.f;
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) w[8 * j + i] *= 2.f * fmaxf(uf[i], 0.f);
+                }
+              }
+            } else if (EPI == EPI_CE_BWD) {
+              if (row_ok) {
+                const float l = g.row_f[m];
+                const int t = g.row_i[m];
+#pragma unroll
+                for (int i = 0; i < 64; ++i) w[i] = __expf(w[i] - l) - (nc0 + i == t ? 1.f : 0.f);
+              }
+            }
+            stg.begin();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) stg.put(j, pack8_bf16(w + 8 * j));
+            stg.store(&tc_, nc0, rblk, false);
+            if (EPI == EPI_RELU2) {  // second output a = relu(u)^2
+              float a8[8];
+              stg.begin();
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const float uu = fmaxf(w[8 * j + i], 0.f);
+                  a8[i] = uu * uu;
+                }
+                stg.put(j, pack8_bf16(a8));
+              }
+              stg.store(&tc2, nc0, rblk, false);
+            }
           }
         }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(tempty + ab);
     }
+    if (lane == 0) tc::bulk_wait_all();  // this warp's stores have landed
+    __syncwarp();
   }
 
   if (failed) {
@@ -472,7 +581,29 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS;
 }
 
-typedef void (*KernFn)(CUtensorMap, CUtensorMap, TcParams);
+typedef void (*KernFn)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TcParams);
+
+// Output maps: 32-row x 128-byte boxes, 128-byte swizzle (the staging layout).
+bool make_out_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t cols, uint64_t rows, uint64_t pitch) {
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {pitch * (f32 ? 4 : 2)};
+  cuuint32_t box[2] = {f32 ? 32u : 64u, 32u};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr),
+                  dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// fp32 [splits, M, N] partial slabs: a 3-D map so a box is clipped at M per split.
+bool make_partial_map(CUtensorMap* m, const void* ptr, uint64_t N, uint64_t M, uint64_t splits) {
+  cuuint64_t dims[3] = {N, M, splits};
+  cuuint64_t strides[2] = {N * 4, N * M * 4};
+  cuuint32_t box[3] = {32u, 32u, 1u};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 template <int EPI, int CL>
 KernFn pick(int a_mn, int b_mn) {
@@ -553,6 +684,11 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   ok = ok && (g.b_kmajor ? make_map(&tb, g.B, K, g.N, g.ldb, 64, CLn == 2 ? 128 : 256)
                          : make_map(&tb, g.B, g.N, K, g.ldb, 64, 64));
   if (!ok) return cudaErrorInvalidValue;
+  CUtensorMap tcm = ta, tcm2 = ta;  // unused maps stay valid copies
+  const bool f32out = g.epi == EPI_STORE_F32;
+  if (g.epi != EPI_CE_FWD) ok = make_out_map(&tcm, g.C, f32out, g.N, g.M, g.ldc);
+  if (ok && g.epi == EPI_RELU2) ok = make_out_map(&tcm2, g.C2, false, g.N, g.M, g.ldc2);
+  if (!ok) return cudaErrorInvalidValue;
   TcParams p;
   p.g = g;
   p.num_m = (g.M + BM - 1) / BM;
@@ -560,6 +696,7 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   p.num_kb = (g.K + BK - 1) / BK;
   p.splits = (g.splits > 1 && g.epi == EPI_STORE_F32 && g.partial) ? g.splits : 1;
   p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
+  if (p.splits > 1 && !make_partial_map(&tcm2, g.partial, g.N, g.M, p.splits)) return cudaErrorInvalidValue;
   KernFn fn = CLn == 2 ? pick_kernel<2>(g.epi, !g.a_kmajor, !g.b_kmajor) : pick_kernel<1>(g.epi, !g.a_kmajor, !g.b_kmajor);
   if (!fn) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -582,11 +719,11 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, p);
+    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tcm, tcm2, p);
   } else {
     p.total = p.num_m * p.num_n * p.splits;
     int grid = p.total < g_num_sms ? p.total : g_num_sms;
-    fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, p);
+    fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, tcm, tcm2, p);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess || p.splits == 1) return e;
