@@ -383,8 +383,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 // (the next query tile loads while this one computes) and dS^T.
 // Per query tile: S^T = K Q^T and dP^T = V dO^T; P^T = exp(S^T - lse),
 // dS^T = P^T (dP^T - D); dV += P^T dO (A operand read from TMEM),
-// dK += dS^T Q, dQ = dS K; dQ is added to the fp32 plane with vector atomics
-// while the next tile's S^T is already being computed.
+// dK += dS^T Q, dQ = dS K; dQ is added to the fp32 plane by bulk tensor
+// reduce-adds staged in the dS^T tile, while the next tile's S^T is already
+// being computed.
 
 constexpr int BWD_WARPS = 10;
 constexpr int BWD_THREADS = 32 * BWD_WARPS;
@@ -392,7 +393,7 @@ constexpr int BWD_SOFT = 32 * (BWD_WARPS - 2);  // 256 softmax threads
 
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
-                  const __grid_constant__ AttnParams p) {
+                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (tc::smem_u32(smem_raw) & 1023) {  // see the forward kernel
     if (threadIdx.x == 0) set_status(p.status, DEV_BAD_LAUNCH);
@@ -540,6 +541,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = kLog2e * rsqrtf(128.f);
     const float scale = rsqrtf(128.f);
+    // this warp's 4 KB block of the dS^T tile (its rows, its column half) is
+    // also its staging buffer for the dQ bulk reduce-adds
+    uint8_t* blk = sdSt + ch * HALF_BYTES + q4 * 32 * 128;
     for (int it = 0; it < nit; ++it) {
       const int qt = kt + it;
       const int s = it & 1;
@@ -550,6 +554,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ok = ok && tc::mbar_wait(q_full + s, (it >> 1) & 1, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
+      // the previous tile's dQ reduce-adds must have read the block first
+      if (lane == 0) tc::bulk_wait_read();
+      __syncwarp();
       const bool diag = (it == 0);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -589,20 +596,33 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       ok = tc::mbar_wait(dq_full, it & 1, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
-      // dQ tile row r (query qt*128 + r), this warp's 64 columns
-      float* dqrow = p.dq + (size_t)(b * p.T + qt * TILE + r) * d + h * 128 + ch * 64;
+      // dQ rows q4*32.. (queries qt*128 + q4*32 + lane), this warp's 64
+      // columns as two 32 x 32 fp32 chunks, each staged in the (now free) dS^T
+      // block and added to the dq plane by a bulk tensor reduce-add
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float v[32];
         tc::tmem_ld32(tdQ + lane_off + ch * 64 + c * 32, v);
+        if (c > 0) {
+          if (lane == 0) tc::bulk_wait_read();
+          __syncwarp();
+        }
 #pragma unroll
         for (int g = 0; g < 8; ++g)
-          atomicAdd(reinterpret_cast<float4*>(dqrow + c * 32 + g * 4),
-                    make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale));
+          *reinterpret_cast<float4*>(blk + lane * 128 + ((g ^ (lane & 7)) << 4)) =
+              make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_reduce_add_2d(&tdq, blk, h * 128 + ch * 64 + c * 32, b * p.T + qt * TILE + q4 * 32);
+          tc::bulk_commit();
+        }
       }
       tc::tc_fence_before();
       tc::mbar_arrive(tm_free);
     }
+    if (lane == 0) tc::bulk_wait_all();  // this warp's dQ reduce-adds have landed
+    __syncwarp();
     if (!failed) {
       bool ok = tc::mbar_wait(acc_full, 0, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) failed = true;
@@ -692,9 +712,20 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   if (!attn_tc_supports(T)) return cudaErrorNotSupported;
   if (B * T == 0) return cudaSuccess;
   if (!encoder()) return cudaErrorNotSupported;
-  CUtensorMap tq, tdo;
+  CUtensorMap tq, tdo, tdq;
   if (!map_rows(&tq, qkv, 3ull * H * 128, (uint64_t)B * T)) return cudaErrorInvalidValue;
   if (!map_rows(&tdo, dout, 1ull * H * 128, (uint64_t)B * T)) return cudaErrorInvalidValue;
+  {
+    // dq fp32 [B*T, d]: 32 x 32 boxes, 128-byte swizzle (the staging layout)
+    cuuint64_t dims[2] = {(uint64_t)H * 128, (uint64_t)B * T};
+    cuuint64_t strides[1] = {(uint64_t)H * 128 * 4};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t es[2] = {1, 1};
+    if (g_enc(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dq, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   AttnParams p{};
   p.B = B; p.T = T; p.H = H; p.nq = T / TILE;
   p.lse = const_cast<float*>(lse); p.Drow = Drow; p.dq = dq; p.dk = dk; p.dqkv = dqkv; p.status = status;
@@ -702,7 +733,7 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_bwd_tc_k<<<B * H * p.nq, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, p);
+  attn_bwd_tc_k<<<B * H * p.nq, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, tdq, p);
   return cudaGetLastError();
 }
 

@@ -50,14 +50,25 @@ struct TcParams {
 // Work unit v of a CTA (CL = 1) or of a CTA pair (CL = 2: the two CTAs of a
 // cluster take vertically adjacent 128-row blocks that share the B tile):
 // row offset m0, column block nb, k-split and its k-blocks [kb0, kb1).
+// Order, for L2 reuse of the operand panels: split-major (the units running
+// together share one k-range), then groups of kGroupRows row blocks (or row
+// pairs) that sweep every column block together, rows fastest.
+constexpr int kGroupRows = 16;
+
 template <int CL>
 __device__ __forceinline__ void unit_of(const TcParams& p, int v, int rank, int& m0, int& nb, int& split, int& kb0,
                                         int& kb1) {
-  const int t = v / p.splits;
-  split = v % p.splits;
-  const int mb = (CL == 1) ? t / p.num_n : 2 * (t / p.num_n) + rank;
-  nb = t % p.num_n;
-  m0 = mb * BM;
+  const int rows = (CL == 1) ? p.num_m : (p.num_m + 1) / 2;  // row blocks or row-block pairs
+  const int tiles = rows * p.num_n;
+  split = v / tiles;
+  const int t = v % tiles;
+  const int per_group = kGroupRows * p.num_n;
+  const int g0 = (t / per_group) * kGroupRows;
+  const int gsize = min(kGroupRows, rows - g0);
+  const int w = t % per_group;
+  const int r = g0 + w % gsize;
+  nb = w / gsize;
+  m0 = ((CL == 1) ? r : 2 * r + rank) * BM;
   kb0 = split * p.kb_per_split;
   kb1 = min(p.num_kb, kb0 + p.kb_per_split);
   if (kb1 < kb0) kb1 = kb0;
