@@ -255,8 +255,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       float mx = -INFINITY;
       if (ok) {
         tc::tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 2; ++c) tc::tmem_ld32(tmem + s * 128 + lane_off + ch * 64 + c * 32, v + c * 32);
+        tc::tmem_ld32x2(tmem + s * 128 + lane_off + ch * 64, tmem + s * 128 + lane_off + ch * 64 + 32, v, v + 32);
         if (diag) {
 #pragma unroll
           for (int i = 0; i < 64; ++i)
@@ -291,14 +290,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
             failed = true;  // reported to the partner at the next exchange
           } else {
             tc::tc_fence_after();
+            float o[64];
+            tc::tmem_ld32x2(tO + lane_off + ch * 64, tO + lane_off + ch * 64 + 32, o, o + 32);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              float o[32];
-              tc::tmem_ld32(tO + lane_off + ch * 64 + c * 32, o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] *= alpha;
-              tc::tmem_st32(tO + lane_off + ch * 64 + c * 32, o);
-            }
+            for (int i = 0; i < 64; ++i) o[i] *= alpha;
+            tc::tmem_st32(tO + lane_off + ch * 64, o);
+            tc::tmem_st32(tO + lane_off + ch * 64 + 32, o + 32);
           }
         }
       }
@@ -345,17 +342,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       tc::tc_fence_after();
       const float inv = 1.f / l;
       bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128 + ch * 64;
+      float o[64];
+      tc::tmem_ld32x2(tO + lane_off + ch * 64, tO + lane_off + ch * 64 + 32, o, o + 32);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float o[32];
-        tc::tmem_ld32(tO + lane_off + ch * 64 + c * 32, o);
+      for (int g = 0; g < 8; ++g) {
+        float w8[8];
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float w8[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) w8[i] = o[g * 8 + i] * inv;
-          *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = pack8(w8);
-        }
+        for (int i = 0; i < 8; ++i) w8[i] = o[g * 8 + i] * inv;
+        *reinterpret_cast<uint4*>(orow + g * 8) = pack8(w8);
       }
       if (ch == 0) p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
     } else {
@@ -561,8 +555,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         float sv[32], dp[32];
-        tc::tmem_ld32(tS + lane_off + ch * 64 + c * 32, sv);
-        tc::tmem_ld32(tdP + lane_off + ch * 64 + c * 32, dp);
+        tc::tmem_ld32x2(tS + lane_off + ch * 64 + c * 32, tdP + lane_off + ch * 64 + c * 32, sv, dp);
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const float4 l0 = *reinterpret_cast<const float4*>(Lq + c * 32 + g * 8);
@@ -599,10 +592,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // dQ rows q4*32.. (queries qt*128 + q4*32 + lane), this warp's 64
       // columns as two 32 x 32 fp32 chunks, each staged in the (now free) dS^T
       // block and added to the dq plane by a bulk tensor reduce-add
+      float vq[64];
+      tc::tmem_ld32x2(tdQ + lane_off + ch * 64, tdQ + lane_off + ch * 64 + 32, vq, vq + 32);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tc::tmem_ld32(tdQ + lane_off + ch * 64 + c * 32, v);
+        const float* v = vq + c * 32;
         if (c > 0) {
           if (lane == 0) tc::bulk_wait_read();
           __syncwarp();
@@ -634,15 +628,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128 + ch * 64;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        float v[32];
-        tc::tmem_ld32(tdK + lane_off + ch * 64 + c * 32, v);
+        float v[32], w[32];
+        tc::tmem_ld32x2(tdK + lane_off + ch * 64 + c * 32, tdV + lane_off + ch * 64 + c * 32, v, w);
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           *reinterpret_cast<float4*>(dkrow + c * 32 + g * 4) =
               make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
-        tc::tmem_ld32(tdV + lane_off + ch * 64 + c * 32, v);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dvrow + c * 32 + g * 8) = pack8(v + 8 * g);
+        for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dvrow + c * 32 + g * 8) = pack8(w + 8 * g);
       }
     } else {
       *abort_flag = 1;

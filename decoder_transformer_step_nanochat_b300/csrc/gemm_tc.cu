@@ -439,13 +439,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // bf16 outputs: two chunks of 64 columns
           float v[128];
           if (EPI == EPI_QKNORM_ROPE) {
+            if (have_acc) tc::tmem_ld32x4(taddr, taddr + 32, taddr + 64, taddr + 96, v, v + 32, v + 64, v + 96);
+            else
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              if (have_acc) tc::tmem_ld32(taddr + c * 32, v + c * 32);
-              else
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[c * 32 + i] = 0.f;
-            }
+              for (int i = 0; i < 128; ++i) v[i] = 0.f;
             if (row_ok && n0 < g.N) {
               // this warp's 128 columns are one head of q, k or v for its row:
               // q and k heads get RMSNorm (eps 1e-6) then the half-split
@@ -482,13 +479,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           for (int h2 = 0; h2 < 2; ++h2) {
             float* w = v + h2 * 64;
             if (EPI != EPI_QKNORM_ROPE) {
+              if (have_acc) tc::tmem_ld32x2(taddr + h2 * 64, taddr + h2 * 64 + 32, w, w + 32);
+              else
 #pragma unroll
-              for (int c = 0; c < 2; ++c) {
-                if (have_acc) tc::tmem_ld32(taddr + h2 * 64 + c * 32, w + c * 32);
-                else
-#pragma unroll
-                  for (int i = 0; i < 32; ++i) w[c * 32 + i] = 0.f;
-              }
+                for (int i = 0; i < 64; ++i) w[i] = 0.f;
 #pragma unroll
               for (int i = 0; i < 64; ++i) w[i] *= g.alpha;
             }

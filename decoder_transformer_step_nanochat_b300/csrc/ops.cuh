@@ -69,7 +69,7 @@ template <typename T>
 cudaError_t rmsnorm_fwd(const float* x, T* y, float* r, int M, int d, cudaStream_t s);
 // dx (f32) = (accumulate ? dx : 0) + r*(dy - y*mean(dy*y)); also dx_e = elem copy (if non-null)
 template <typename T>
-cudaError_t rmsnorm_bwd(const float* dy, const T* y, const float* r, float* dx, T* dx_e, int M,
+cudaError_t rmsnorm_bwd(const T* dy, const T* y, const float* r, float* dx, T* dx_e, int M,
                         int d, int accumulate, cudaStream_t s);
 template <typename T>
 cudaError_t qk_norm_rope_fwd(T* qkv, float* rqk, const float* cs, const float* sn, int M, int T_,

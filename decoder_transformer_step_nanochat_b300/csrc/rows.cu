@@ -90,14 +90,15 @@ __global__ void rmsnorm_fwd_k(const float* __restrict__ x, T* __restrict__ y, fl
 }
 
 // dx = [dx +] r * (dy - y * mean(dy * y)); optional copy in the element type.
+// dy arrives in the element type (bf16 in the bf16 mode); dx stays fp32.
 template <typename T>
-__global__ void rmsnorm_bwd_k(const float* __restrict__ dy, const T* __restrict__ y,
+__global__ void rmsnorm_bwd_k(const T* __restrict__ dy, const T* __restrict__ y,
                               const float* __restrict__ r, float* __restrict__ dx, T* __restrict__ dxe,
                               int M, int d, int accumulate) {
   int m = blockIdx.x * kRowWarps + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   if (m >= M) return;
-  const float* g = dy + (size_t)m * d;
+  const T* g = dy + (size_t)m * d;
   const T* yr = y + (size_t)m * d;
   float dot = 0.f;
   for (int c = lane * 4; c < d; c += 128) {
@@ -159,6 +160,8 @@ __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __res
                                    const float* __restrict__ rqk, const float* __restrict__ cs,
                                    const float* __restrict__ sn, T* __restrict__ dqkv, int M,
                                    int Tlen, int H) {
+  // lane L owns the rotation pairs j = 2L and 2L+1 (partners 2L+64, 2L+65),
+  // so every access is a coalesced 2-element vector
   int w = blockIdx.x * kRowWarps + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
   if (w >= M * 2 * H) return;
@@ -167,24 +170,31 @@ __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __res
   const int which = wh / H, hh = wh % H;
   const float* g = dqk + (size_t)which * M * d + (size_t)m * d + (size_t)hh * kHeadDim;
   const T* q = qkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
-  int t = m % Tlen;
+  const int t = m % Tlen, j = 2 * lane;
+  const float2 co = *reinterpret_cast<const float2*>(cs + t * kHalf + j);
+  const float2 si = *reinterpret_cast<const float2*>(sn + t * kHalf + j);
+  const float2 g1 = *reinterpret_cast<const float2*>(g + j);
+  const float2 g2 = *reinterpret_cast<const float2*>(g + j + kHalf);
+  float q1[2], q2[2];
+  q1[0] = ldf(q + j); q1[1] = ldf(q + j + 1);
+  q2[0] = ldf(q + j + kHalf); q2[1] = ldf(q + j + kHalf + 1);
+  const float c2[2] = {co.x, co.y}, s2[2] = {si.x, si.y};
+  const float a1[2] = {g1.x, g1.y}, a2[2] = {g2.x, g2.y};
   float gn[4], qn[4];
 #pragma unroll
-  for (int c = 0; c < 2; ++c) {
-    int j = lane + 32 * c;
-    float co = cs[t * kHalf + j], si = sn[t * kHalf + j];
-    float g1 = g[j], g2 = g[j + kHalf];
-    gn[c] = g1 * co + g2 * si;
-    gn[c + 2] = -g1 * si + g2 * co;
-    float q1 = ldf(q + j), q2 = ldf(q + j + kHalf);
-    qn[c] = q1 * co + q2 * si;
-    qn[c + 2] = -q1 * si + q2 * co;
+  for (int u = 0; u < 2; ++u) {
+    gn[u] = a1[u] * c2[u] + a2[u] * s2[u];
+    gn[u + 2] = -a1[u] * s2[u] + a2[u] * c2[u];
+    qn[u] = q1[u] * c2[u] + q2[u] * s2[u];
+    qn[u + 2] = -q1[u] * s2[u] + q2[u] * c2[u];
   }
   float dot = warp_sum(gn[0] * qn[0] + gn[1] * qn[1] + gn[2] * qn[2] + gn[3] * qn[3]) / (float)kHeadDim;
   float rr = rqk[(size_t)m * 2 * H + wh];
   T* o = dqkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) stf(o + lane + 32 * c, rr * (gn[c] - qn[c] * dot));
+  stf(o + j, rr * (gn[0] - qn[0] * dot));
+  stf(o + j + 1, rr * (gn[1] - qn[1] * dot));
+  stf(o + j + kHalf, rr * (gn[2] - qn[2] * dot));
+  stf(o + j + kHalf + 1, rr * (gn[3] - qn[3] * dot));
 }
 
 // D[b,h,t] = sum_e dout[m, h*128+e] * o[m, h*128+e]  (softmax backward term)
@@ -357,7 +367,7 @@ cudaError_t rmsnorm_fwd(const float* x, T* y, float* r, int M, int d, cudaStream
 }
 
 template <typename T>
-cudaError_t rmsnorm_bwd(const float* dy, const T* y, const float* r, float* dx, T* dx_e, int M,
+cudaError_t rmsnorm_bwd(const T* dy, const T* y, const float* r, float* dx, T* dx_e, int M,
                         int d, int accumulate, cudaStream_t s) {
   rmsnorm_bwd_k<T><<<row_blocks(M), 32 * kRowWarps, 0, s>>>(dy, y, r, dx, dx_e, M, d, accumulate);
   return cudaGetLastError();
@@ -425,7 +435,7 @@ cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s)
   template cudaError_t embed_bwd<T>(const int*, const T*, const float*, float*, int, int, int,  \
                                     cudaStream_t);                                               \
   template cudaError_t rmsnorm_fwd<T>(const float*, T*, float*, int, int, cudaStream_t);         \
-  template cudaError_t rmsnorm_bwd<T>(const float*, const T*, const float*, float*, T*, int,     \
+  template cudaError_t rmsnorm_bwd<T>(const T*, const T*, const float*, float*, T*, int,         \
                                       int, int, cudaStream_t);                                   \
   template cudaError_t qk_norm_rope_fwd<T>(T*, float*, const float*, const float*, int, int,     \
                                            int, cudaStream_t);                                   \

@@ -323,10 +323,11 @@ nc_status lmhead_ce_forward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt
   return NC_OK;
 }
 
-// g = softmax - onehot per chunk; dhf = g W_lm / M ; dW_lm = g^T hf / M
-template <typename T>
+// g = softmax - onehot per chunk; dhf = g W_lm / M ; dW_lm = g^T hf / M.
+// dhf is written in DT (the element type inside the step, fp32 for the op).
+template <typename T, typename DT>
 nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt, const float* lse,
-                             int M, float inv_count, float* dhf, float* dwlm) {
+                             int M, float inv_count, DT* dhf, float* dwlm) {
   int d = c->d, V = c->V;
   T* g = wsp<T>(c, c->off.chunk);
   for (int r0 = 0; r0 < M; r0 += c->ce_rows) {
@@ -335,7 +336,8 @@ nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tg
     a.row_f = lse + r0;
     a.row_i = tgt + r0;
     CKS(gemm(c, a));
-    CKS(gemm(c, mk(rows, d, V, g, V, 1, wlm, d, 0, EPI_STORE_F32, dhf + (size_t)r0 * d, d, inv_count)));
+    CKS(gemm(c, mk(rows, d, V, g, V, 1, wlm, d, 0, sizeof(DT) == 4 ? EPI_STORE_F32 : EPI_STORE,
+                   dhf + (size_t)r0 * d, d, inv_count)));
     CKS(gemm(c, mk(V, d, rows, g, V, 0, hf + (size_t)r0 * d, d, 0, EPI_STORE_F32, dwlm, d, inv_count,
                    r0 == 0 ? 0.f : 1.f)));
   }
@@ -404,7 +406,7 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
   int rows, cols;
   float* dx = wsp<float>(c, c->off.dx);
   T* dxe = wsp<T>(c, c->off.dxe);
-  float* dy = wsp<float>(c, c->off.dy);
+  T* dy = wsp<T>(c, c->off.dy);  // gradient into each RMSNorm, element type
   T* du = wsp<T>(c, c->off.du);
   T* dout = wsp<T>(c, c->off.dout);
   T* dqkv = wsp<T>(c, c->off.dqkv);
@@ -412,8 +414,8 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
   float* drow = wsp<float>(c, c->off.drow);
   const T* hf = wsp<T>(c, c->off.hf);
   size_t o_lm = param_offset(c, 1 + 4 * c->L, &rows, &cols);
-  CKS(lmhead_ce_backward<T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, 1.f / (float)M, dy, G + o_lm));
-  KL(NC_FAM_ROWS, (double)M * d * (8 + 2 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
+  CKS((lmhead_ce_backward<T, T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, 1.f / (float)M, dy, G + o_lm)));
+  KL(NC_FAM_ROWS, (double)M * d * (4 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
   for (int l = c->L - 1; l >= 0; --l) {
     size_t lb = (size_t)l * c->off.layer_stride;
     const T* xn1 = wsp<T>(c, lb + c->off.xn1);
@@ -436,8 +438,8 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     g1.C2 = u; g1.ldc2 = F;
     CKS(gemm(c, g1));
     CKS(gemm(c, mk(F, d, M, du, F, 0, xn2, d, 0, EPI_STORE_F32, G + of, d)));
-    CKS(gemm(c, mk(M, d, F, du, F, 1, P + of, d, 0, EPI_STORE_F32, dy, d)));
-    KL(NC_FAM_ROWS, (double)M * d * (12 + 2 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
+    CKS(gemm(c, mk(M, d, F, du, F, 1, P + of, d, 0, sizeof(T) == 4 ? EPI_STORE_F32 : EPI_STORE, dy, d)));
+    KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
     // attention: x += attn(xn1) Wo^T
     CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
     CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
@@ -446,8 +448,8 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
        attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv));
     KL(NC_FAM_ROWS, 2.0 * M * d * (4 + 2 * sizeof(T)) + 8.0 * M * H, 1, qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s));
     CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d)));
-    CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, EPI_STORE_F32, dy, d)));
-    KL(NC_FAM_ROWS, (double)M * d * (12 + 2 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
+    CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, sizeof(T) == 4 ? EPI_STORE_F32 : EPI_STORE, dy, d)));
+    KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
   }
   CK(cudaMemsetAsync(G, 0, (size_t)V * d * sizeof(float), s));
   KL(NC_FAM_ROWS, 8.0 * M * d + 4.0 * M, 1, embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s));
@@ -708,8 +710,8 @@ nc_status nc_op_lmhead_ce_bwd(nc_ctx* c, const void* hf, const void* w_lm, const
   c->have_fwd = false;
   float inv = 1.f / (float)c->M;
   return c->prec == NC_BF16
-             ? lmhead_ce_backward<bf16>(c, (const bf16*)hf, (const bf16*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm)
-             : lmhead_ce_backward<float>(c, (const float*)hf, (const float*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm);
+             ? lmhead_ce_backward<bf16, float>(c, (const bf16*)hf, (const bf16*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm)
+             : lmhead_ce_backward<float, float>(c, (const float*)hf, (const float*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm);
 }
 
 nc_status nc_op_attention_fwd(nc_ctx* c, const void* qkv, void* o, float* lse) {
