@@ -161,6 +161,25 @@ def dist_setup():
     return ws, rank, local
 
 
+def reduce_over_ranks(ms: float, launches: int, device) -> tuple:
+    """(max of ms, sum of launches) over all ranks of the default process
+    group (NCCL on GPUs, gloo works as well); identity without one."""
+    import torch
+    import torch.distributed as dist
+
+    t_ms = torch.tensor([ms], dtype=torch.float64, device=device)
+    t_n = torch.tensor([float(launches)], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+        dist.all_reduce(t_n, op=dist.ReduceOp.SUM)
+    return float(t_ms.item()), int(t_n.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_max: float) -> float:
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1000.0)
+
+
 def reference_arm(args):
     ws, rank, _ = dist_setup()
     if rank != 0:
@@ -244,14 +263,8 @@ def our_arm(args):
         fam[name] = nc.nc_profile_read(st.ctx, f)
     nc.nc_profile_enable(st.ctx, False)
 
-    t = torch.tensor([ms, float(launches)], dtype=torch.float64, device="cuda")
-    if ws > 1:
-        tmax = t.clone()
-        dist.all_reduce(tmax[:1], op=dist.ReduceOp.MAX)
-        dist.all_reduce(t[1:], op=dist.ReduceOp.SUM)
-        t[0] = tmax[0]
-    ms_max, launches_all = float(t[0]), int(t[1])
-    value = ws * M / (ms_max / 1000.0)
+    ms_max, launches_all = reduce_over_ranks(ms, launches, "cuda")
+    value = job_tokens_per_s(ws, M, ms_max)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -264,10 +277,8 @@ def our_arm(args):
         t0 = time.perf_counter()
         for _ in range(args.steps):
             nc.nc_train_step_host(st.ctx, params.data_ptr(), h_tok.data_ptr(), h_tgt.data_ptr(), grads.data_ptr())
-        dt = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device="cuda")
-        if ws > 1:
-            dist.all_reduce(dt, op=dist.ReduceOp.MAX)
-        e2e = {"value": ws * M * args.steps / float(dt), "unit": UNIT,
+        dt_max, _ = reduce_over_ranks(1000.0 * (time.perf_counter() - t0) / args.steps, 0, "cuda")
+        e2e = {"value": job_tokens_per_s(ws, M, dt_max), "unit": UNIT,
                "h2d_bytes_per_step": 2 * M * 4, "d2h_bytes_per_step": 4}
 
     # ---- roofline of the dominant kernel family (live CUDA-event records)

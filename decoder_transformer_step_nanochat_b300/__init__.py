@@ -285,6 +285,7 @@ class Step:
         if self.ctx is not None:
             nc_destroy(self.ctx)
             self.ctx = None
+        self._ws = None  # hand the workspace back to torch's allocator now
 
     def __del__(self):
         try:
