@@ -220,8 +220,10 @@ def our_arm(args):
     params_np = W.make_params(w)
     tok_np, tgt_np = W.make_tokens(w, seed=rank)
     stream = torch.cuda.Stream()
-    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, w.batch, nc.NC_BF16, stream=stream)
-    params = torch.from_numpy(params_np).to(torch.bfloat16).cuda()
+    prec = nc.NC_FP32_DEBUG if w.dtype == "fp32" else nc.NC_BF16
+    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, w.batch, prec, stream=stream)
+    params = torch.from_numpy(params_np)
+    params = (params if prec == nc.NC_FP32_DEBUG else params.to(torch.bfloat16)).cuda()
     tok = torch.from_numpy(tok_np).cuda()
     tgt = torch.from_numpy(tgt_np).cuda()
     grads = torch.empty(st.n_params, dtype=torch.float32, device="cuda")
@@ -313,7 +315,7 @@ def our_arm(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f32" if prec == nc.NC_FP32_DEBUG else "bf16", "data": "synthetic",
             "config": {"workload": workload_desc(w), "global_batch": w.batch * ws, "seq_len": w.seq_len,
                        "tokens_per_step": M * ws,
                        "parallelism": f"{ws} independent data-parallel replicas (no collective)",
