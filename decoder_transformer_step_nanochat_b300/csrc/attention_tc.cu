@@ -61,6 +61,16 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
   return r;
 }
 
+__device__ __forceinline__ void unpack8(uint4 u, float* f) {
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -81,8 +91,13 @@ struct AttnParams {
   float* lse;     // forward output / backward input
   const float* Drow;
   float* dq;      // backward: fp32 [B*T, d], accumulated with atomics (pre-zeroed)
-  float* dk;      // backward: fp32 [B*T, d]
-  bf16* dqkv;     // backward: dv goes to its v columns
+  float* dk;      // backward: fp32 [B*T, d] (dk_hat), unless the k half is finished in-kernel
+  bf16* dqkv;     // backward: dv goes to its v columns (and dk to its k columns when finished)
+  // finishing the k half in-kernel (QK-norm + RoPE backward of k): needs rstd of
+  // the k heads (rqk [B*T, 2H]) and the RoPE table ([T, 64] cos / sin)
+  const float* rqk;
+  const float* rope_cos;
+  const float* rope_sin;
   int* status;
 };
 
@@ -624,18 +639,95 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     if (!failed) {
       tc::tc_fence_after();
       const size_t m = (size_t)krow0 + r;
-      float* dkrow = p.dk + m * d + h * 128 + ch * 64;
-      bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128 + ch * 64;
+      if (p.rqk) {
+        // warp ch = 0 finishes dk for whole head rows; warp ch = 1 writes dv
+        if (ch == 0) {
+          // dk_hat = scale * acc; dk_n = R^T dk_hat and k_n = R^T k_hat (k_hat from
+          // the K tile in shared memory); dk = rk * (dk_n - k_n * mean(dk_n * k_n)).
+          // Pass 1 rotates 32 pairs at a time back into the dK columns of TMEM and
+          // accumulates the dot; pass 2 finishes and stores.
+          const int t = kt * TILE + r;
+          const float* cs = p.rope_cos + (size_t)t * 64;
+          const float* sn = p.rope_sin + (size_t)t * 64;
+          const uint32_t tk = tdK + lane_off;
+          float dot = 0.f;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float v[32], w[32];
-        tc::tmem_ld32x2(tdK + lane_off + ch * 64 + c * 32, tdV + lane_off + ch * 64 + c * 32, v, w);
+          for (int pass = 0; pass < 2; ++pass) {
+            const float rk = pass ? p.rqk[m * 2 * p.H + p.H + h] : 0.f;
+            const float dmean = dot * (1.f / 128.f);
 #pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<float4*>(dkrow + c * 32 + g * 4) =
-              make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
+            for (int c = 0; c < 4; ++c) {  // 16 rotation pairs at a time
+              float g1[16], g2[16];
+              tc::tmem_ld16x2(tk + c * 16, tk + 64 + c * 16, g1, g2);
 #pragma unroll
-        for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dvrow + c * 32 + g * 8) = pack8(w + 8 * g);
+              for (int c8 = 0; c8 < 2; ++c8) {
+                const int q8 = c * 2 + c8;  // 8-column piece of the first half
+                const int sw = ((q8 ^ (r & 7)) << 4) + r * 128;
+                float k1[8], k2[8];
+                unpack8(*reinterpret_cast<const uint4*>(sK + sw), k1);
+                unpack8(*reinterpret_cast<const uint4*>(sK + HALF_BYTES + sw), k2);
+                const float4 ca = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8);
+                const float4 cb = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8 + 1);
+                const float4 sa = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8);
+                const float4 sb = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8 + 1);
+                const float cc[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+                const float ss[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  const int e = c8 * 8 + i;
+                  const float kn1 = k1[i] * cc[i] + k2[i] * ss[i];
+                  const float kn2 = -k1[i] * ss[i] + k2[i] * cc[i];
+                  if (pass == 0) {
+                    const float a = g1[e] * scale, b = g2[e] * scale;
+                    g1[e] = a * cc[i] + b * ss[i];
+                    g2[e] = -a * ss[i] + b * cc[i];
+                    dot += g1[e] * kn1 + g2[e] * kn2;
+                  } else {
+                    g1[e] = rk * (g1[e] - kn1 * dmean);
+                    g2[e] = rk * (g2[e] - kn2 * dmean);
+                  }
+                }
+              }
+              if (pass == 0) {
+                tc::tmem_st16(tk + c * 16, g1);
+                tc::tmem_st16(tk + 64 + c * 16, g2);
+              } else {
+                bf16* row = p.dqkv + m * 3 * d + d + h * 128;
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                  *reinterpret_cast<uint4*>(row + c * 16 + g * 8) = pack8(g1 + 8 * g);
+                  *reinterpret_cast<uint4*>(row + 64 + c * 16 + g * 8) = pack8(g2 + 8 * g);
+                }
+              }
+            }
+          }
+        } else {
+          bf16* row = p.dqkv + m * 3 * d + 2 * d + h * 128;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float a[32], b[32];
+            tc::tmem_ld32x2(tdV + lane_off + c * 64, tdV + lane_off + c * 64 + 32, a, b);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              *reinterpret_cast<uint4*>(row + c * 64 + g * 8) = pack8(a + 8 * g);
+              *reinterpret_cast<uint4*>(row + c * 64 + 32 + g * 8) = pack8(b + 8 * g);
+            }
+          }
+        }
+      } else {
+        float* dkrow = p.dk + m * d + h * 128 + ch * 64;
+        bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128 + ch * 64;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float v[32], w[32];
+          tc::tmem_ld32x2(tdK + lane_off + ch * 64 + c * 32, tdV + lane_off + ch * 64 + c * 32, v, w);
+#pragma unroll
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<float4*>(dkrow + c * 32 + g * 4) =
+                make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dvrow + c * 32 + g * 8) = pack8(w + 8 * g);
+        }
       }
     } else {
       *abort_flag = 1;
@@ -701,7 +793,8 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
 }
 
 cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* Drow, float* dq,
-                        float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s) {
+                        float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s, const float* rqk,
+                        const float* rope_cos, const float* rope_sin) {
   if (!attn_tc_supports(T)) return cudaErrorNotSupported;
   if (B * T == 0) return cudaSuccess;
   if (!encoder()) return cudaErrorNotSupported;
@@ -722,6 +815,7 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   AttnParams p{};
   p.B = B; p.T = T; p.H = H; p.nq = T / TILE;
   p.lse = const_cast<float*>(lse); p.Drow = Drow; p.dq = dq; p.dk = dk; p.dqkv = dqkv; p.status = status;
+  p.rqk = rqk; p.rope_cos = rope_cos; p.rope_sin = rope_sin;
   cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)B * T * H * 128 * sizeof(float), s);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);

@@ -74,9 +74,10 @@ cudaError_t rmsnorm_bwd(const T* dy, const T* y, const float* r, float* dx, T* d
 template <typename T>
 cudaError_t qk_norm_rope_fwd(T* qkv, float* rqk, const float* cs, const float* sn, int M, int T_,
                              int H, cudaStream_t s);
+// heads = 2 (q and k heads) or 1 (q heads only: k was finished elsewhere)
 template <typename T>
 cudaError_t qk_norm_rope_bwd(const float* dqk, const T* qkv, const float* rqk, const float* cs,
-                             const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s);
+                             const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s, int heads = 2);
 
 // ------------------------------------------------------------------ attention
 template <typename T>
@@ -92,9 +93,13 @@ cudaError_t attn_bwd_simt(const T* qkv, const T* dout, const float* lse, const f
 // tcgen05 flash attention (bf16, T % 128 == 0).
 bool attn_tc_supports(int T);
 cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int H, int* status, cudaStream_t s);
-// dq (zeroed here, then accumulated) and dk are fp32 [B*T, d]; dv goes to dqkv's v columns.
+// dq (zeroed here, then accumulated) is fp32 [B*T, d]; dv goes to dqkv's v columns. Without rqk,
+// dk_hat goes to the fp32 plane dk; with rqk (+ the RoPE table) the k half of the QK-norm + RoPE
+// backward runs in the kernel and the final dk goes to dqkv's k columns.
 cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* Drow, float* dq,
-                        float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s);
+                        float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s,
+                        const float* rqk = nullptr, const float* rope_cos = nullptr,
+                        const float* rope_sin = nullptr);
 
 // ------------------------------------------------------------------ loss
 cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,

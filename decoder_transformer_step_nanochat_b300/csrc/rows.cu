@@ -159,13 +159,14 @@ template <typename T>
 __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __restrict__ qkv,
                                    const float* __restrict__ rqk, const float* __restrict__ cs,
                                    const float* __restrict__ sn, T* __restrict__ dqkv, int M,
-                                   int Tlen, int H) {
+                                   int Tlen, int H, int heads) {
   // lane L owns the rotation pairs j = 2L and 2L+1 (partners 2L+64, 2L+65),
-  // so every access is a coalesced 2-element vector
+  // so every access is a coalesced 2-element vector; heads = 1 covers only
+  // the q heads of each row
   int w = blockIdx.x * kRowWarps + threadIdx.x / 32;
   int lane = threadIdx.x & 31;
-  if (w >= M * 2 * H) return;
-  int m = w / (2 * H), wh = w % (2 * H);
+  if (w >= M * heads * H) return;
+  int m = w / (heads * H), wh = w % (heads * H);
   int d = H * kHeadDim;
   const int which = wh / H, hh = wh % H;
   const float* g = dqk + (size_t)which * M * d + (size_t)m * d + (size_t)hh * kHeadDim;
@@ -382,8 +383,9 @@ cudaError_t qk_norm_rope_fwd(T* qkv, float* rqk, const float* cs, const float* s
 
 template <typename T>
 cudaError_t qk_norm_rope_bwd(const float* dqk, const T* qkv, const float* rqk, const float* cs,
-                             const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s) {
-  qk_norm_rope_bwd_k<T><<<row_blocks((long long)M * 2 * H), 32 * kRowWarps, 0, s>>>(dqk, qkv, rqk, cs, sn, dqkv, M, T_, H);
+                             const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s, int heads) {
+  qk_norm_rope_bwd_k<T><<<row_blocks((long long)M * heads * H), 32 * kRowWarps, 0, s>>>(dqk, qkv, rqk, cs, sn, dqkv, M,
+                                                                                    T_, H, heads);
   return cudaGetLastError();
 }
 
@@ -440,7 +442,7 @@ cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s)
   template cudaError_t qk_norm_rope_fwd<T>(T*, float*, const float*, const float*, int, int,     \
                                            int, cudaStream_t);                                   \
   template cudaError_t qk_norm_rope_bwd<T>(const float*, const T*, const float*, const float*,   \
-                                           const float*, T*, int, int, int, cudaStream_t);       \
+                                           const float*, T*, int, int, int, cudaStream_t, int);  \
   template cudaError_t attn_rowdot<T>(const T*, const T*, float*, int, int, int, cudaStream_t);
 NC_INST(float)
 NC_INST(bf16)

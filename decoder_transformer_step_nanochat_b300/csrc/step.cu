@@ -285,12 +285,14 @@ cudaError_t attn_fwd(nc_ctx* c, const T* qkv, T* o, float* lse) {
     return attn_fwd_simt<T>(qkv, o, lse, c->B, c->T, c->H, c->stream);
 }
 
+// With rqk (the step), the tensor-core kernel also finishes the k half of the
+// QK-norm + RoPE backward; without it (the op-level call) it leaves dk_hat.
 template <typename T>
 cudaError_t attn_bwd(nc_ctx* c, const T* qkv, const T* dout, const float* lse, const float* drow, float* dqk,
-                     T* dqkv) {
+                     T* dqkv, const float* rqk = nullptr) {
   if constexpr (sizeof(T) == 2)
     return attn_bwd_tc(qkv, dout, lse, drow, dqk, dqk + (size_t)c->M * c->d, dqkv, c->B, c->T, c->H, c->status,
-                       c->stream);
+                       c->stream, rqk, rqk ? c->rope_cos : nullptr, rqk ? c->rope_sin : nullptr);
   else
     return attn_bwd_simt<T>(qkv, dout, lse, drow, dqk, dqkv, c->B, c->T, c->H, c->stream);
 }
@@ -444,9 +446,11 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
     CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
     KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + 4.0 * M * H, 1, attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s));
-    KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), c->prec == NC_BF16 ? 1 : 2,
-       attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv));
-    KL(NC_FAM_ROWS, 2.0 * M * d * (4 + 2 * sizeof(T)) + 8.0 * M * H, 1, qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s));
+    const bool fused_k = c->prec == NC_BF16;  // k half of the QK-norm/RoPE backward inside the kernel
+    KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), fused_k ? 1 : 2,
+       attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv, fused_k ? rqk : nullptr));
+    KL(NC_FAM_ROWS, (fused_k ? 1.0 : 2.0) * M * d * (4 + 2 * sizeof(T)) + 8.0 * M * H, 1,
+       qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s, fused_k ? 1 : 2));
     CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d)));
     CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, sizeof(T) == 4 ? EPI_STORE_F32 : EPI_STORE, dy, d)));
     KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
