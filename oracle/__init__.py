@@ -10,3 +10,4 @@ from .model import (EPS, HEAD_DIM, ROPE_BASE, Shape, backward, causal_attention,
                     cross_entropy_rows, forward, layout, param_count, relu2,
                     relu2_backward, rmsnorm, rmsnorm_backward, rope,
                     rope_angles, rope_backward, step, unpack)
+from . import optim
