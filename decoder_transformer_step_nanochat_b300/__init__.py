@@ -6,7 +6,7 @@ and streams; this module takes raw device pointers (ints) and never computes
 anything itself. Importing it loads libnc.so and fails loudly if it is
 missing: there is no fallback implementation.
 
-Names follow include/nc.h and include/nc_ops.h.
+Names follow include/nc.h, include/nc_ops.h and include/nc_optim.h.
 """
 
 from __future__ import annotations
@@ -24,6 +24,8 @@ NC_FAM_GEMM = 0
 NC_FAM_ATTN_FWD = 1
 NC_FAM_ATTN_BWD = 2
 NC_FAM_ROWS = 3
+NC_FAM_OPT_NS = 4
+NC_FAM_OPT_ELEM = 5
 
 NC_EPI_STORE = 0
 NC_EPI_STORE_F32 = 1
@@ -31,6 +33,7 @@ NC_EPI_RELU2 = 2
 NC_EPI_RELU2_BWD = 3
 NC_EPI_CE_BWD = 4
 NC_EPI_QKNORM_ROPE = 6
+NC_EPI_AXPBY = 7
 
 STATUS = {0: "NC_OK", 1: "NC_ERR_ARG", 2: "NC_ERR_STATE", 3: "NC_ERR_CUDA",
           4: "NC_ERR_TIMEOUT", 5: "NC_ERR_DEVICE", 6: "NC_ERR_UNSUPPORTED"}
@@ -79,6 +82,13 @@ _SIGS = {
     "nc_op_qk_norm_rope_fwd": (_I, [_P, _P, _P]),
     "nc_op_rmsnorm_fwd": (_I, [_P, _P, _P, _P]),
     "nc_lmhead_ce_fwd_static": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "nc_op_gemm_batched": (_I, [_P, _I, _I, _I, _I, _P, _LL, _I, _LL, _P, _LL, _I, _LL, _I, _F, _F, _P, _LL,
+                                _P, _LL, _LL]),
+    "nc_optim_state_bytes": (_SZ, [_P]),
+    "nc_optim_init": (_I, [_P, _P, _P]),
+    "nc_optim_set_hparams": (_I, [_P, _F, _F, _F, _F, _I]),
+    "nc_optim_step": (_I, [_P, _P, _P, _P, _I, _F, _F, _F, _F, _P]),
+    "nc_lr_at": (ctypes.c_double, [_LL, _LL, _LL, ctypes.c_double, ctypes.c_double]),
 }
 
 
@@ -227,6 +237,33 @@ def nc_op_rmsnorm_fwd(ctx, x, y, r):
 def nc_lmhead_ce_fwd_static(hf, w_lm, tgt, M, d, V, lse, nll, argmax, d_status=None, stream=None):
     """Allocation-free lm_head + cross-entropy forward (static device scratch)."""
     _check(lib().nc_lmhead_ce_fwd_static(hf, w_lm, tgt, M, d, V, lse, nll, argmax, d_status, stream))
+
+
+def nc_op_gemm_batched(ctx, batch, M, N, K, A, lda, a_kmajor, a_brows, B, ldb, b_kmajor, b_brows, epi, alpha,
+                       beta, C, ldc, C2=None, ldc2=0, c_brows=0):
+    _check(lib().nc_op_gemm_batched(ctx, batch, M, N, K, A, lda, a_kmajor, a_brows, B, ldb, b_kmajor, b_brows,
+                                    epi, alpha, beta, C, ldc, C2, ldc2, c_brows), ctx)
+
+
+def nc_optim_state_bytes(ctx) -> int:
+    return int(lib().nc_optim_state_bytes(ctx))
+
+
+def nc_optim_init(ctx, params, state):
+    _check(lib().nc_optim_init(ctx, params, state), ctx)
+
+
+def nc_optim_set_hparams(ctx, beta1, beta2, eps, momentum, ns_steps):
+    _check(lib().nc_optim_set_hparams(ctx, beta1, beta2, eps, momentum, ns_steps), ctx)
+
+
+def nc_optim_step(ctx, params, grads, state, t, lr_adamw, lr_muon, weight_decay, max_grad_norm, stats=None):
+    _check(lib().nc_optim_step(ctx, params, grads, state, t, lr_adamw, lr_muon, weight_decay, max_grad_norm,
+                               stats), ctx)
+
+
+def nc_lr_at(step, warmup, total, peak, final_frac=0.0) -> float:
+    return float(lib().nc_lr_at(step, warmup, total, peak, final_frac))
 
 
 # ------------------------------------------------------------------ convenience

@@ -25,8 +25,11 @@ template <typename T>
 __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs g) {
   __shared__ float As[BK][BM];
   __shared__ float Bs[BK][BN];
-  const T* A = static_cast<const T*>(g.A);
-  const T* B = static_cast<const T*>(g.B);
+  // blockIdx.z selects one problem of a stacked batch
+  const size_t bz = blockIdx.z;
+  const T* A = static_cast<const T*>(g.A) + bz * g.a_brows * g.lda;
+  const T* B = static_cast<const T*>(g.B) + bz * g.b_brows * g.ldb;
+  const size_t c_off = bz * g.c_brows * g.ldc, c2_off = bz * g.c_brows * g.ldc2;
   int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
   int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   float acc[8][8];
@@ -71,7 +74,7 @@ __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs g) {
       int n = n0 + tx + 16 * j;
       if (n >= g.N) continue;
       float v = g.alpha * acc[i][j];
-      size_t ci = (size_t)m * g.ldc + n;
+      size_t ci = c_off + (size_t)m * g.ldc + n;
       switch (g.epi) {
         case EPI_STORE:
           stf(static_cast<T*>(g.C) + ci, v);
@@ -84,17 +87,22 @@ __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs g) {
         case EPI_RELU2: {
           stf(static_cast<T*>(g.C) + ci, v);
           float u = fmaxf(v, 0.f);
-          stf(static_cast<T*>(g.C2) + (size_t)m * g.ldc2 + n, u * u);
+          stf(static_cast<T*>(g.C2) + c2_off + (size_t)m * g.ldc2 + n, u * u);
           break;
         }
         case EPI_RELU2_BWD: {
-          float u = ldf(static_cast<const T*>(g.C2) + (size_t)m * g.ldc2 + n);
+          float u = ldf(static_cast<const T*>(g.C2) + c2_off + (size_t)m * g.ldc2 + n);
           stf(static_cast<T*>(g.C) + ci, v * 2.f * fmaxf(u, 0.f));
           break;
         }
         case EPI_CE_BWD: {
           float p = expf(v - g.row_f[m]);
           stf(static_cast<T*>(g.C) + ci, p - (n == g.row_i[m] ? 1.f : 0.f));
+          break;
+        }
+        case EPI_AXPBY: {
+          float c2 = ldf(static_cast<const T*>(g.C2) + c2_off + (size_t)m * g.ldc2 + n);
+          stf(static_cast<T*>(g.C) + ci, v + g.beta * c2);
           break;
         }
         default:
@@ -109,8 +117,10 @@ __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs g) {
 template <typename T>
 cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s) {
   if (g.epi == EPI_CE_FWD || g.epi == EPI_QKNORM_ROPE) return cudaErrorNotSupported;
+  if (g.batch < 1 || g.batch > 65535) return cudaErrorNotSupported;
+  if (g.batch > 1 && (g.epi == EPI_CE_BWD || g.splits > 1)) return cudaErrorNotSupported;
   if (g.M == 0 || g.N == 0) return cudaSuccess;
-  dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM);
+  dim3 grid((g.N + BN - 1) / BN, (g.M + BM - 1) / BM, g.batch);
   gemm_simt_k<T><<<grid, 256, 0, s>>>(g);
   return cudaGetLastError();
 }

@@ -49,18 +49,21 @@ struct TcParams {
 
 // Work unit v of a CTA (CL = 1) or of a CTA pair (CL = 2: the two CTAs of a
 // cluster take vertically adjacent 128-row blocks that share the B tile):
-// row offset m0, column block nb, k-split and its k-blocks [kb0, kb1).
-// Order, for L2 reuse of the operand panels: split-major (the units running
-// together share one k-range), then groups of kGroupRows row blocks (or row
-// pairs) that sweep every column block together, rows fastest.
+// problem bt of a batch, row offset m0, column block nb, k-split and its
+// k-blocks [kb0, kb1). Order, for L2 reuse of the operand panels: split-major
+// (the units running together share one k-range), then problem, then groups
+// of kGroupRows row blocks (or row pairs) that sweep every column block
+// together, rows fastest.
 constexpr int kGroupRows = 16;
 
 template <int CL>
-__device__ __forceinline__ void unit_of(const TcParams& p, int v, int rank, int& m0, int& nb, int& split, int& kb0,
-                                        int& kb1) {
+__device__ __forceinline__ void unit_of(const TcParams& p, int v, int rank, int& bt, int& m0, int& nb, int& split,
+                                        int& kb0, int& kb1) {
   const int rows = (CL == 1) ? p.num_m : (p.num_m + 1) / 2;  // row blocks or row-block pairs
   const int tiles = rows * p.num_n;
-  split = v / tiles;
+  const int slab = v / tiles;
+  split = slab / p.g.batch;
+  bt = slab - split * p.g.batch;
   const int t = v % tiles;
   const int per_group = kGroupRows * p.num_n;
   const int g0 = (t / per_group) * kGroupRows;
@@ -264,9 +267,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bool issued[STAGES];
       for (int s = 0; s < STAGES; ++s) issued[s] = false, issued_phase[s] = 0;
       for (int v = v_first; v < p.total && !failed; v += v_step) {
-        int m0, nb, split, kb0, kb1;
-        unit_of<CL>(p, v, rank, m0, nb, split, kb0, kb1);
+        int bt, m0, nb, split, kb0, kb1;
+        unit_of<CL>(p, v, rank, bt, m0, nb, split, kb0, kb1);
         const int n0 = nb * BN;
+        const int a_off = (int)(bt * g.a_brows), b_off = (int)(bt * g.b_brows);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
           tc::mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
@@ -274,25 +278,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           uint8_t* a = sA + stage * A_BYTES;
           uint8_t* b = sB + stage * B_BYTES;
           if (A_MN) {
-            tc::tma_load_2d(a, &ta, m0, k0, full + stage);
-            tc::tma_load_2d(a + 8192, &ta, m0 + 64, k0, full + stage);
+            tc::tma_load_2d(a, &ta, m0, k0 + a_off, full + stage);
+            tc::tma_load_2d(a + 8192, &ta, m0 + 64, k0 + a_off, full + stage);
           } else {
-            tc::tma_load_2d(a, &ta, k0, m0, full + stage);
+            tc::tma_load_2d(a, &ta, k0, m0 + a_off, full + stage);
           }
           if (CL == 2) {
             // this CTA fetches half of the shared B tile for both CTAs
             if (B_MN) {
 #pragma unroll
               for (int j = 2 * rank; j < 2 * rank + 2; ++j)
-                tc::tma_load_2d_multicast(b + j * 8192, &tb, n0 + 64 * j, k0, full + stage, 0x3);
+                tc::tma_load_2d_multicast(b + j * 8192, &tb, n0 + 64 * j, k0 + b_off, full + stage, 0x3);
             } else {
-              tc::tma_load_2d_multicast(b + rank * (B_BYTES / 2), &tb, k0, n0 + (BN / 2) * rank, full + stage, 0x3);
+              tc::tma_load_2d_multicast(b + rank * (B_BYTES / 2), &tb, k0, n0 + (BN / 2) * rank + b_off, full + stage,
+                                        0x3);
             }
           } else if (B_MN) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tc::tma_load_2d(b + j * 8192, &tb, n0 + 64 * j, k0, full + stage);
+            for (int j = 0; j < 4; ++j) tc::tma_load_2d(b + j * 8192, &tb, n0 + 64 * j, k0 + b_off, full + stage);
           } else {
-            tc::tma_load_2d(b, &tb, k0, n0, full + stage);
+            tc::tma_load_2d(b, &tb, k0, n0 + b_off, full + stage);
           }
           issued[stage] = true;
           issued_phase[stage] = phase;
@@ -315,8 +320,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       int cnt = 0;
       bool any_mma = false;
       for (int v = v_first; v < p.total && !failed; v += v_step, ++cnt) {
-        int m0, nb, split, kb0, kb1;
-        unit_of<CL>(p, v, rank, m0, nb, split, kb0, kb1);
+        int bt, m0, nb, split, kb0, kb1;
+        unit_of<CL>(p, v, rank, bt, m0, nb, split, kb0, kb1);
         const int ab = cnt & 1;
         const uint32_t aph = (cnt >> 1) & 1;
         if (!tc::mbar_wait(tempty + ab, aph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
@@ -360,8 +365,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     Stager stg{sStage + (warp - 2) * STAGING_BYTES, lane};
     int cnt = 0;
     for (int v = v_first; v < p.total && !failed; v += v_step, ++cnt) {
-      int m0, nb, split, kb0, kb1;
-      unit_of<CL>(p, v, rank, m0, nb, split, kb0, kb1);
+      int bt, m0, nb, split, kb0, kb1;
+      unit_of<CL>(p, v, rank, bt, m0, nb, split, kb0, kb1);
       const int ab = cnt & 1;
       const uint32_t aph = (cnt >> 1) & 1;
       const int n0 = nb * BN + ch * (BN / 2);
@@ -411,8 +416,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       } else {
         // ---- outputs leave through the staging buffer as bulk tensor stores
-        const int rblk = m0 + q * 32;  // first row of this warp's 32-row block
-        const bool blk_ok = rblk < g.M;
+        const int rblk_local = m0 + q * 32;  // first row of this warp's 32-row block
+        const bool blk_ok = rblk_local < g.M;
+        const int rblk = rblk_local + (int)(bt * g.c_brows);  // in the stacked output
         if (EPI == EPI_STORE_F32) {
           const bool direct = (p.splits == 1 && g.beta != 0.f && g.beta != 1.f);
           for (int c = 0; c < 4; ++c) {
@@ -508,6 +514,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const int t = g.row_i[m];
 #pragma unroll
                 for (int i = 0; i < 64; ++i) w[i] = __expf(w[i] - l) - (nc0 + i == t ? 1.f : 0.f);
+              }
+            } else if (EPI == EPI_AXPBY) {
+              if (row_ok) {
+                const bf16* c2 = static_cast<const bf16*>(g.C2) + (size_t)(bt * g.c_brows + m) * g.ldc2 + nc0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  if (nc0 + 8 * j < g.N) {
+                    float cf[8];
+                    unpack8_bf16(*reinterpret_cast<const uint4*>(c2 + 8 * j), cf);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) w[8 * j + i] += g.beta * cf[i];
+                  }
+                }
               }
             }
             stg.begin();
@@ -628,6 +647,7 @@ KernFn pick_kernel(int epi, int a_mn, int b_mn) {
     case EPI_CE_BWD: return pick<EPI_CE_BWD, CL>(a_mn, b_mn);
     case EPI_CE_FWD: return pick<EPI_CE_FWD, CL>(a_mn, b_mn);
     case EPI_QKNORM_ROPE: return pick<EPI_QKNORM_ROPE, CL>(a_mn, b_mn);
+    case EPI_AXPBY: return pick<EPI_AXPBY, CL>(a_mn, b_mn);
     default: return nullptr;
   }
 }
@@ -665,6 +685,22 @@ bool gemm_tc_supports(const GemmArgs& g) {
   if (g.M < 0 || g.N < 0 || g.K < 0) return false;
   if (g.N % 8 || g.lda % 8 || g.ldb % 8) return false;
   if (!aligned16(g.A) || !aligned16(g.B)) return false;
+  if (g.batch < 1) return false;
+  if (g.batch > 1) {
+    // stacked problems: whole 128-row blocks per problem so no tile's rows
+    // reach into the next problem's output; 64-deep k slices per problem
+    // for operands stacked along k (the MN-major ones)
+    if (g.epi != EPI_STORE && g.epi != EPI_AXPBY) return false;
+    if (g.splits > 1 || g.M % BM) return false;
+    if (g.c_brows < g.M) return false;
+    if (g.a_brows < (g.a_kmajor ? g.M : g.K) || g.b_brows < (g.b_kmajor ? g.N : g.K)) return false;
+    if ((!g.a_kmajor && g.a_brows % BK) || (!g.b_kmajor && g.b_brows % BK)) return false;
+    const long long rows_max = 0x7fffffffLL;
+    if ((long long)g.batch * g.a_brows > rows_max || (long long)g.batch * g.b_brows > rows_max ||
+        (long long)g.batch * g.c_brows > rows_max)
+      return false;
+  }
+  if (g.epi == EPI_AXPBY && (!g.C2 || g.ldc2 % 8 || !aligned16(g.C2))) return false;
   if (g.epi == EPI_CE_FWD) return g.p_max && g.p_sum && g.p_arg && g.p_tgt && g.row_i;
   if (g.splits > 1 && (g.epi != EPI_STORE_F32 || !g.partial || g.N % 4)) return false;
   if (g.ldc % 8 || !aligned16(g.C)) return false;
@@ -673,7 +709,7 @@ bool gemm_tc_supports(const GemmArgs& g) {
   if (g.epi == EPI_QKNORM_ROPE &&
       (!g.rope_cos || !g.rope_sin || !g.rqk || g.seq_len < 1 || g.d_model % 128 || g.N != 3 * g.d_model))
     return false;
-  return g.epi >= EPI_STORE && g.epi <= EPI_QKNORM_ROPE;
+  return g.epi >= EPI_STORE && g.epi <= EPI_AXPBY;
 }
 
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
@@ -681,17 +717,22 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
   if (!get_encode()) return cudaErrorNotSupported;
   // CTA pairs sharing the B tile whenever there are at least two row blocks
-  const int CLn = (g.M > BM) ? 2 : 1;
+  // (in a batch: an even number per problem, so no pair spans two problems)
+  const int CLn = (g.M > BM && (g.batch == 1 || (g.M / BM) % 2 == 0)) ? 2 : 1;
   CUtensorMap ta, tb;
   // TMA needs an extent of at least one element; an empty K reads nothing.
   uint64_t K = g.K > 0 ? (uint64_t)g.K : 1;
-  bool ok = g.a_kmajor ? make_map(&ta, g.A, K, g.M, g.lda, 64, 128) : make_map(&ta, g.A, g.M, K, g.lda, 64, 64);
-  ok = ok && (g.b_kmajor ? make_map(&tb, g.B, K, g.N, g.ldb, 64, CLn == 2 ? 128 : 256)
-                         : make_map(&tb, g.B, g.N, K, g.ldb, 64, 64));
+  // outer extents cover every stacked problem
+  const uint64_t a_outer = g.batch > 1 ? (uint64_t)g.batch * g.a_brows : (g.a_kmajor ? (uint64_t)g.M : K);
+  const uint64_t b_outer = g.batch > 1 ? (uint64_t)g.batch * g.b_brows : (g.b_kmajor ? (uint64_t)g.N : K);
+  const uint64_t c_rows = g.batch > 1 ? (uint64_t)g.batch * g.c_brows : (uint64_t)g.M;
+  bool ok = g.a_kmajor ? make_map(&ta, g.A, K, a_outer, g.lda, 64, 128) : make_map(&ta, g.A, g.M, a_outer, g.lda, 64, 64);
+  ok = ok && (g.b_kmajor ? make_map(&tb, g.B, K, b_outer, g.ldb, 64, CLn == 2 ? 128 : 256)
+                         : make_map(&tb, g.B, g.N, b_outer, g.ldb, 64, 64));
   if (!ok) return cudaErrorInvalidValue;
   CUtensorMap tcm = ta, tcm2 = ta;  // unused maps stay valid copies
   const bool f32out = g.epi == EPI_STORE_F32;
-  if (g.epi != EPI_CE_FWD) ok = make_out_map(&tcm, g.C, f32out, g.N, g.M, g.ldc);
+  if (g.epi != EPI_CE_FWD) ok = make_out_map(&tcm, g.C, f32out, g.N, c_rows, g.ldc);
   if (ok && g.epi == EPI_RELU2) ok = make_out_map(&tcm2, g.C2, false, g.N, g.M, g.ldc2);
   if (!ok) return cudaErrorInvalidValue;
   TcParams p;
@@ -709,7 +750,7 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   if (CLn == 2) {
     // work units are pairs of row blocks; one 2-CTA cluster per unit at a time
-    p.total = ((p.num_m + 1) / 2) * p.num_n * p.splits;
+    p.total = ((p.num_m + 1) / 2) * p.num_n * p.splits * g.batch;
     int clusters = max_clusters(fn);
     if (clusters > p.total) clusters = p.total;
     cudaLaunchConfig_t cfg = {};
@@ -726,7 +767,7 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tcm, tcm2, p);
   } else {
-    p.total = p.num_m * p.num_n * p.splits;
+    p.total = p.num_m * p.num_n * p.splits * g.batch;
     int grid = p.total < g_num_sms ? p.total : g_num_sms;
     fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, tcm, tcm2, p);
     e = cudaGetLastError();

@@ -18,6 +18,7 @@ enum Epi : int {
   EPI_CE_BWD = 4,      // C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])
   EPI_CE_FWD = 5,      // per (row, 128-column tile) softmax partials (tensor-core path)
   EPI_QKNORM_ROPE = 6, // C (elem) = qkv with per-head RMSNorm + RoPE on the q,k columns
+  EPI_AXPBY = 7,       // C (elem) = alpha*acc + beta*C2 (C2 elem, same shape as C)
 };
 
 struct GemmArgs {
@@ -41,6 +42,12 @@ struct GemmArgs {
   // `partial` ([splits, M, N] fp32) and a reduction kernel forms C.
   int splits = 1;
   float* partial = nullptr;
+  // batched problems (EPI_STORE / EPI_AXPBY, M % 128 == 0 on the tensor
+  // cores): `batch` independent GEMMs whose operands are stacked along their
+  // outer (row) dimension; problem i reads A rows from i*a_brows, B rows from
+  // i*b_brows and writes C (and reads C2) rows from i*c_brows.
+  int batch = 1;
+  long long a_brows = 0, b_brows = 0, c_brows = 0;
   int* status = nullptr;
 };
 
@@ -109,5 +116,34 @@ cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int
                                int* amax, int M, cudaStream_t s);
 cudaError_t mean_loss(const float* nll, int M, float* loss, cudaStream_t s);
 cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s);
+
+// ------------------------------------------------------------------ optimizer
+// Chunk of the Muon passes (every block matrix holds a whole number of them:
+// d^2 is a multiple of 16384 when d is a multiple of 128) and the fixed block
+// count of the gradient-norm reduction.
+constexpr int kMuonChunk = 8192;
+constexpr int kNormBlocks = 1184;
+// stats[0] = ||g||_2 over n fp32 gradients, stats[1] = min(1, max_norm / (norm + 1e-6));
+// part = kNormBlocks fp64 partials. stats_out (may be null) gets a copy.
+cudaError_t grad_norm(const float* g, long long n, float max_norm, double* part, float* stats, float* stats_out,
+                      cudaStream_t s);
+// AdamW on two segments of seg elements each: parameter offsets [0, seg) and [off2, off2 + seg)
+template <typename T>
+cudaError_t adamw_update(float* master, T* param, const float* grad, float* m, float* v, long long seg, long long off2,
+                         const float* stats, float lr, float b1, float b2, float eps, float wd, float inv_bc1,
+                         float inv_bc2, cudaStream_t s);
+// buf <- mu buf + k g over n block-matrix elements; part[chunk] = sum of u^2, u = k g + mu buf
+cudaError_t muon_momentum(const float* grad, float* buf, long long n, const float* stats, float mu, double* part,
+                          cudaStream_t s);
+// per-matrix 1/(||u||+1e-7), then X[kind][l] = u * inv (stacked per kind: w_qkv, w_o, w_fc, w_proj)
+template <typename T>
+cudaError_t muon_normalize(const float* grad, const float* buf, const float* stats, float mu, const double* part,
+                           float* inv_norm, int L, int d, T* X, cudaStream_t s);
+// master <- master*decay - step*X ; param <- master, for one kind's stack [L, msize]
+template <typename T>
+cudaError_t muon_apply(float* master, T* param, const T* X, int L, long long msize, long long layer, long long pre,
+                       float decay, float step, cudaStream_t s);
+template <typename T>
+cudaError_t upcast(const T* p, float* master, long long n, cudaStream_t s);
 
 }  // namespace nc

@@ -17,6 +17,7 @@
 
 #include "../../include/nc.h"
 #include "../../include/nc_ops.h"
+#include "../../include/nc_optim.h"
 #include "ops.cuh"
 
 using namespace nc;
@@ -86,6 +87,15 @@ struct nc_ctx {
     size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
     size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial;
   } off{};
+  // optimizer scratch: overlays the step's workspace from offset 0 (the
+  // stash is dead once the backward has run)
+  struct OptOff {
+    size_t stats, part_norm, part_muon, inv_norm, x_all, pong, gram, poly;
+  } opt{};
+  // optimizer hyper-parameters fixed per context (nc_optim_set_hparams)
+  float opt_b1 = 0.9f, opt_b2 = 0.999f, opt_eps = 1e-8f, opt_mu = 0.95f;
+  int opt_ns = 5;
+  int gemm_fam = NC_FAM_GEMM;  // family the GEMM launches are timed under
   // launch accounting and optional per-family event timing
   unsigned long long launches = 0;
   bool prof = false;
@@ -207,6 +217,19 @@ void plan_workspace(nc_ctx* c) {
   if (c->partial_bytes < (size_t(64) << 20)) c->partial_bytes = size_t(64) << 20;
   f.partial = take(c->partial_bytes);
   c->ws_need = o;
+  // optimizer scratch, from offset 0
+  o = 0;
+  const size_t d2 = d * d, L = c->L, nb = 12 * L * d2;
+  auto& q = c->opt;
+  q.stats = take(2 * 4);
+  q.part_norm = take(kNormBlocks * 8);
+  q.part_muon = take(nb / kMuonChunk * 8);
+  q.inv_norm = take(4 * L * 4);
+  q.x_all = take(nb * e);          // Newton-Schulz input / iterate, stacked per kind
+  q.pong = take(4 * L * d2 * e);   // second iterate buffer (largest kind)
+  q.gram = take(L * d2 * e);       // X X^T per matrix
+  q.poly = take(L * d2 * e);       // b A + c A A per matrix
+  if (o > c->ws_need) c->ws_need = o;
 }
 
 nc_status check_ready(nc_ctx* c) {
@@ -256,7 +279,7 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
   }
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm M=%d N=%d K=%d epi=%d: %s", g.M, g.N, g.K, g.epi, cudaGetErrorString(e));
   int n = (g.M > 0 && g.N > 0) ? (g.splits > 1 ? 2 : 1) : 0;  // split-K adds its reduction kernel
-  return prof_end(c, ev_a, NC_FAM_GEMM, 2.0 * g.M * g.N * (double)g.K, n);
+  return prof_end(c, ev_a, c->gemm_fam, 2.0 * g.M * g.N * (double)g.K * g.batch, n);
 }
 
 GemmArgs mk(int M, int N, int K, const void* A, long long lda, int ak, const void* B, long long ldb,
@@ -472,6 +495,96 @@ nc_status forward_any(nc_ctx* c, const void* params, const int32_t* tok, const i
   return NC_OK;
 }
 
+
+// ------------------------------------------------------------------ optimizer
+
+// Quintic Newton-Schulz coefficients of Muon as Keller Jordan published it.
+constexpr float kNsA = 3.4445f, kNsB = -4.7750f, kNsC = 2.0315f;
+
+// Matrix kinds of a layer in flat order: rows, cols (in units of d) and the
+// offset inside the layer (units of d^2).
+struct Kind { int r, c, pre; };
+constexpr Kind kKinds[4] = {{3, 1, 0}, {1, 1, 3}, {4, 1, 4}, {1, 4, 8}};
+
+// ns_steps Newton-Schulz iterations on the stacked matrices of one kind
+// (all L layers per launch). X holds the normalised start; Y, A, Bp are
+// scratch; *out gets whichever of X / Y holds the result. Wide matrices
+// (rows <= cols) iterate X <- a X + Bp X with A = X X^T; tall ones iterate the
+// transpose Y = X^T directly: A = Y^T Y and Y <- a Y + Y Bp^T, which is the
+// same iteration read transposed, with no transpose in memory.
+template <typename T>
+nc_status newton_schulz(nc_ctx* c, int kind, T* X, T* Y, T* A, T* Bp, T** out) {
+  const long long d = c->d, r = kKinds[kind].r * d, cc = kKinds[kind].c * d;
+  const bool tall = r > cc;
+  const long long s = tall ? cc : r;
+  const int L = c->L;
+  T* cur = X;
+  T* nxt = Y;
+  for (int it = 0; it < c->opt_ns; ++it) {
+    GemmArgs g1 = tall ? mk((int)s, (int)s, (int)r, cur, cc, 0, cur, cc, 0, EPI_STORE, A, s)
+                       : mk((int)s, (int)s, (int)cc, cur, cc, 1, cur, cc, 1, EPI_STORE, A, s);
+    g1.batch = L; g1.a_brows = r; g1.b_brows = r; g1.c_brows = s;
+    CKS(gemm(c, g1));
+    GemmArgs g2 = mk((int)s, (int)s, (int)s, A, s, 1, A, s, 0, EPI_AXPBY, Bp, s, kNsC, kNsB);
+    g2.C2 = A; g2.ldc2 = s;
+    g2.batch = L; g2.a_brows = s; g2.b_brows = s; g2.c_brows = s;
+    CKS(gemm(c, g2));
+    GemmArgs g3 = tall ? mk((int)r, (int)cc, (int)cc, cur, cc, 1, Bp, s, 1, EPI_AXPBY, nxt, cc, 1.f, kNsA)
+                       : mk((int)r, (int)cc, (int)r, Bp, s, 1, cur, cc, 0, EPI_AXPBY, nxt, cc, 1.f, kNsA);
+    g3.C2 = cur; g3.ldc2 = cc;
+    g3.batch = L; g3.a_brows = tall ? r : s; g3.b_brows = tall ? s : r; g3.c_brows = r;
+    CKS(gemm(c, g3));
+    T* t = cur; cur = nxt; nxt = t;
+  }
+  *out = cur;
+  return NC_OK;
+}
+
+template <typename T>
+nc_status optim_step(nc_ctx* c, T* param, const float* grads, float* state, int t, float lr_a, float lr_m, float wd,
+                     float max_norm, float* stats_out) {
+  const long long d = c->d, V = c->V, L = c->L, d2 = d * d;
+  const long long P = 2 * V * d + 12 * L * d2, Vd = V * d, nb = 12 * L * d2;
+  const size_t e = sizeof(T);
+  float* master = state;
+  float* m1 = master + P;
+  float* m2 = m1 + 2 * Vd;
+  float* buf = m2 + 2 * Vd;
+  auto& q = c->opt;
+  float* stats = wsp<float>(c, q.stats);
+  double* part_norm = wsp<double>(c, q.part_norm);
+  double* part_muon = wsp<double>(c, q.part_muon);
+  float* inv_norm = wsp<float>(c, q.inv_norm);
+  T* x_all = wsp<T>(c, q.x_all);
+  T* pong = wsp<T>(c, q.pong);
+  T* gram = wsp<T>(c, q.gram);
+  T* poly = wsp<T>(c, q.poly);
+  const float b1 = c->opt_b1, b2 = c->opt_b2;
+  const float inv_bc1 = (float)(1.0 / (1.0 - pow((double)b1, t)));
+  const float inv_bc2 = (float)(1.0 / (1.0 - pow((double)b2, t)));
+  KL(NC_FAM_OPT_ELEM, 4.0 * P, 2, grad_norm(grads, P, max_norm, part_norm, stats, stats_out, c->stream));
+  KL(NC_FAM_OPT_ELEM, 2.0 * Vd * (7 * 4 + e), 1,
+     adamw_update<T>(master, param, grads, m1, m2, Vd, P - Vd, stats, lr_a, b1, b2, c->opt_eps, wd, inv_bc1, inv_bc2,
+                     c->stream));
+  KL(NC_FAM_OPT_ELEM, 12.0 * nb, 1, muon_momentum(grads + Vd, buf, nb, stats, c->opt_mu, part_muon, c->stream));
+  KL(NC_FAM_OPT_ELEM, (8.0 + e) * nb, 2,
+     muon_normalize<T>(grads + Vd, buf, stats, c->opt_mu, part_muon, inv_norm, (int)L, (int)d, x_all, c->stream));
+  for (int k = 0; k < 4; ++k) {
+    const Kind& kd = kKinds[k];
+    const long long msize = (long long)kd.r * kd.c * d2;
+    T* fin = nullptr;
+    c->gemm_fam = NC_FAM_OPT_NS;
+    nc_status st = newton_schulz<T>(c, k, x_all + (long long)kd.pre * L * d2, pong, gram, poly, &fin);
+    c->gemm_fam = NC_FAM_GEMM;
+    CKS(st);
+    const float scale = (float)sqrt(fmax(1.0, (double)kd.r / kd.c));
+    KL(NC_FAM_OPT_ELEM, (double)L * msize * (2 * e + 8), 1,
+       muon_apply<T>(master + Vd, param + Vd, fin, (int)L, msize, 12 * d2, (long long)kd.pre * d2, 1.f - lr_m * wd,
+                     lr_m * scale, c->stream));
+  }
+  return NC_OK;
+}
+
 }  // namespace
 
 // ====================================================================== ABI
@@ -680,12 +793,12 @@ nc_status nc_op_gemm(nc_ctx* c, int M, int N, int K, const void* A, long long ld
                      const int32_t* row_i) {
   if (!c || c->prec < 0) return fail(NC_ERR_STATE, "context not configured");
   if (M < 0 || N < 0 || K < 0) return fail(NC_ERR_ARG, "negative size");
-  if (epi < EPI_STORE || epi > EPI_QKNORM_ROPE || epi == EPI_CE_FWD)
+  if (epi < EPI_STORE || epi > EPI_AXPBY || epi == EPI_CE_FWD)
     return fail(NC_ERR_ARG, "epilogue %d not available here", epi);
   if (epi == EPI_QKNORM_ROPE && (!c->use_tc || N != 3 * c->d || M != c->M || !C2))
     return fail(NC_ERR_ARG, "the QK-norm + RoPE epilogue needs NC_BF16, N = 3*d_model, M = batch*seq_len and C2 = rqk");
   if (!A || !B || !C) return fail(NC_ERR_ARG, "null operand");
-  if ((epi == EPI_RELU2 || epi == EPI_RELU2_BWD) && !C2) return fail(NC_ERR_ARG, "epilogue needs C2");
+  if ((epi == EPI_RELU2 || epi == EPI_RELU2_BWD || epi == EPI_AXPBY) && !C2) return fail(NC_ERR_ARG, "epilogue needs C2");
   if (epi == EPI_CE_BWD && (!row_f || !row_i)) return fail(NC_ERR_ARG, "epilogue needs row_f/row_i");
   GemmArgs g = mk(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, epi, C, ldc, alpha, beta);
   g.C2 = C2; g.ldc2 = ldc2; g.row_f = row_f; g.row_i = row_i;
@@ -757,6 +870,82 @@ nc_status nc_op_rmsnorm_fwd(nc_ctx* c, const float* x, void* y, float* r) {
   if (c->prec == NC_BF16) CK(rmsnorm_fwd<bf16>(x, (bf16*)y, r, c->M, c->d, c->stream));
   else CK(rmsnorm_fwd<float>(x, (float*)y, r, c->M, c->d, c->stream));
   return NC_OK;
+}
+
+// ------------------------------------------------------------------ optimizer
+
+size_t nc_optim_state_bytes(const nc_ctx* c) {
+  if (!c || c->prec < 0) return 0;
+  const size_t P = nc_param_count(c), Vd = (size_t)c->V * c->d;
+  return 4 * (P + 4 * Vd + 12 * (size_t)c->L * c->d * c->d);
+}
+
+nc_status nc_optim_init(nc_ctx* c, const void* params, void* state) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  if (c->prec < 0) return fail(NC_ERR_STATE, "nc_configure has not been called");
+  if (!params || !state) return fail(NC_ERR_ARG, "null pointer argument");
+  if ((reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(state)) & 15)
+    return fail(NC_ERR_ARG, "params and state must be 16-byte aligned");
+  const long long P = (long long)nc_param_count(c);
+  float* master = static_cast<float*>(state);
+  KL(NC_FAM_OPT_ELEM, (double)P * (4 + c->esz), 1,
+     c->prec == NC_BF16 ? upcast<bf16>(static_cast<const bf16*>(params), master, P, c->stream)
+                        : upcast<float>(static_cast<const float*>(params), master, P, c->stream));
+  CK(cudaMemsetAsync(master + P, 0, nc_optim_state_bytes(c) - 4 * (size_t)P, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_optim_set_hparams(nc_ctx* c, float beta1, float beta2, float eps, float momentum, int ns_steps) {
+  if (!c) return fail(NC_ERR_ARG, "null context");
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) || !(momentum >= 0.f && momentum < 1.f))
+    return fail(NC_ERR_ARG, "beta1, beta2 and momentum must lie in [0, 1)");
+  if (!(eps > 0.f)) return fail(NC_ERR_ARG, "eps must be positive");
+  if (ns_steps < 1 || ns_steps > 32) return fail(NC_ERR_ARG, "ns_steps %d outside [1, 32]", ns_steps);
+  c->opt_b1 = beta1; c->opt_b2 = beta2; c->opt_eps = eps; c->opt_mu = momentum; c->opt_ns = ns_steps;
+  return NC_OK;
+}
+
+nc_status nc_optim_step(nc_ctx* c, void* params, const float* grads, void* state, int t, float lr_adamw,
+                        float lr_muon, float weight_decay, float max_grad_norm, float* stats) {
+  CKS(check_ready(c));
+  if (!params || !grads || !state) return fail(NC_ERR_ARG, "null pointer argument");
+  if ((reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(grads) |
+       reinterpret_cast<uintptr_t>(state)) & 15)
+    return fail(NC_ERR_ARG, "params, grads and state must be 16-byte aligned");
+  if (t < 1) return fail(NC_ERR_ARG, "step number t = %d must be >= 1", t);
+  if (!(lr_adamw >= 0.f) || !(lr_muon >= 0.f) || !(weight_decay >= 0.f) || !(max_grad_norm > 0.f))
+    return fail(NC_ERR_ARG, "learning rates and weight decay must be >= 0 and max_grad_norm > 0");
+  c->have_fwd = false;  // the workspace is scratch from here on
+  return c->prec == NC_BF16
+             ? optim_step<bf16>(c, static_cast<bf16*>(params), grads, static_cast<float*>(state), t, lr_adamw,
+                                lr_muon, weight_decay, max_grad_norm, stats)
+             : optim_step<float>(c, static_cast<float*>(params), grads, static_cast<float*>(state), t, lr_adamw,
+                                 lr_muon, weight_decay, max_grad_norm, stats);
+}
+
+double nc_lr_at(long long step, long long warmup, long long total, double peak, double final_frac) {
+  if (step < warmup) return peak * (double)(step + 1) / (double)warmup;
+  double span = (double)(total - warmup);
+  if (span < 1.0) span = 1.0;
+  double prog = (double)(step - warmup) / span;
+  if (prog > 1.0) prog = 1.0;
+  if (prog < 0.0) prog = 0.0;
+  return peak * (final_frac + (1.0 - final_frac) * 0.5 * (1.0 + cos(M_PI * prog)));
+}
+
+nc_status nc_op_gemm_batched(nc_ctx* c, int batch, int M, int N, int K, const void* A, long long lda,
+                             int a_kmajor, long long a_brows, const void* B, long long ldb, int b_kmajor,
+                             long long b_brows, int epi, float alpha, float beta, void* C, long long ldc,
+                             void* C2, long long ldc2, long long c_brows) {
+  if (!c || c->prec < 0) return fail(NC_ERR_STATE, "context not configured");
+  if (batch < 1 || M < 0 || N < 0 || K < 0) return fail(NC_ERR_ARG, "batch < 1 or negative size");
+  if (epi != EPI_STORE && epi != EPI_AXPBY) return fail(NC_ERR_ARG, "batched epilogue must be STORE or AXPBY");
+  if (!A || !B || !C || (epi == EPI_AXPBY && !C2)) return fail(NC_ERR_ARG, "null operand");
+  if (a_brows < 0 || b_brows < 0 || c_brows < 0) return fail(NC_ERR_ARG, "negative batch stride");
+  GemmArgs g = mk(M, N, K, A, lda, a_kmajor, B, ldb, b_kmajor, epi, C, ldc, alpha, beta);
+  g.C2 = C2; g.ldc2 = ldc2;
+  g.batch = batch; g.a_brows = a_brows; g.b_brows = b_brows; g.c_brows = c_brows;
+  return gemm(c, g);
 }
 
 }  // extern "C"

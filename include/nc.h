@@ -144,7 +144,9 @@ enum {
   NC_FAM_ATTN_FWD = 1,  /* causal attention forward; work = 2*128*T*(T+1)*B*H FLOPs */
   NC_FAM_ATTN_BWD = 2,  /* attention backward; work = 2x the forward's FLOPs */
   NC_FAM_ROWS = 3,      /* norms, embedding, QK-norm/RoPE, CE reductions; work = bytes */
-  NC_FAM_COUNT = 4
+  NC_FAM_OPT_NS = 4,    /* optimizer: Newton-Schulz GEMMs of Muon; work = FLOPs */
+  NC_FAM_OPT_ELEM = 5,  /* optimizer: norm, AdamW and Muon element passes; work = bytes */
+  NC_FAM_COUNT = 6
 };
 
 /* Number of kernels the context has launched since nc_create. */

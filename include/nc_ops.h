@@ -26,10 +26,11 @@ enum {
   NC_EPI_RELU2 = 2,      /* C (elem) = u = alpha * acc ; C2 (elem) = max(u, 0)^2    */
   NC_EPI_RELU2_BWD = 3,  /* C (elem) = alpha * acc * 2 * max(u, 0), u read from C2  */
   NC_EPI_CE_BWD = 4,     /* C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])  */
-  NC_EPI_QKNORM_ROPE = 6 /* NC_BF16 only; the QKV projection with QK-norm + RoPE:
+  NC_EPI_QKNORM_ROPE = 6, /* NC_BF16 only; the QKV projection with QK-norm + RoPE:
                             M = batch*seq_len, N = 3*d_model; C (elem [M, 3d]) gets
                             q, k heads RMS-normalised and rotated (position m % seq_len)
                             and v heads as computed; C2 = fp32 rqk [M, 2H]          */
+  NC_EPI_AXPBY = 7       /* C (elem) = alpha * acc + beta * C2 (elem, ldc2)          */
 };
 
 /* Linear-layer contraction of the step (the QKV, out-projection, MLP and
@@ -50,6 +51,20 @@ nc_status nc_op_gemm(nc_ctx* ctx, int M, int N, int K, const void* A, long long 
                      const void* B, long long ldb, int b_kmajor, int epi, float alpha, float beta,
                      void* C, long long ldc, void* C2, long long ldc2, const float* row_f,
                      const int32_t* row_i);
+
+/* A batch of independent contractions of the same shape whose operands are
+ * stacked along their outer (row) dimension: problem i uses
+ * A + i*a_brows*lda, B + i*b_brows*ldb, C + i*c_brows*ldc and
+ * C2 + i*c_brows*ldc2, each as in nc_op_gemm. This is the shape of Muon's
+ * Newton-Schulz products over the same-shaped matrices of every layer
+ * (nc_optim.h); epi is NC_EPI_STORE or NC_EPI_AXPBY. In NC_BF16, M must be a
+ * multiple of 128, a_brows >= (a_kmajor ? M : K), b_brows >= (b_kmajor ? N : K),
+ * c_brows >= M, and an operand stacked along k (not k-major) needs a multiple
+ * of 64 rows per problem; NC_ERR_UNSUPPORTED otherwise. */
+nc_status nc_op_gemm_batched(nc_ctx* ctx, int batch, int M, int N, int K, const void* A, long long lda,
+                             int a_kmajor, long long a_brows, const void* B, long long ldb, int b_kmajor,
+                             long long b_brows, int epi, float alpha, float beta, void* C, long long ldc,
+                             void* C2, long long ldc2, long long c_brows);
 
 /* Fused lm_head + softmax cross-entropy forward over M = batch*seq_len rows
  * (nanochat explainer, "Pretraining": cross-entropy between the predicted

@@ -139,6 +139,23 @@ def make_params(w: Workload, seed: int = 0) -> np.ndarray:
     return out
 
 
+def make_grads(w: Workload, seed: int = 100, std: float = 1e-3) -> np.ndarray:
+    """Flat float32 stand-in for a backward's output, for the optimizer step:
+    N(0, std^2) draws from PCG64(seed) in layout order; the wte rows of the
+    upper half of the vocabulary are zero, as rows of ids absent from a batch
+    are in a real gradient."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.empty(n_params(w), dtype=np.float32)
+    step = 1 << 24
+    for s in range(0, out.size, step):
+        e = min(out.size, s + step)
+        rng.standard_normal(e - s, dtype=np.float32, out=out[s:e])
+        out[s:e] *= np.float32(std)
+    V, d = w.vocab, w.d_model
+    out[(V // 2) * d:V * d] = 0.0
+    return out
+
+
 def zipf_cdf(vocab: int, s: float = 1.1) -> np.ndarray:
     k = np.arange(1, vocab + 1, dtype=np.float64)
     p = k ** (-s)
