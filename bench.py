@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--workload", default="d20", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-optimizer", action="store_true",
+                    help="skip timing the optimizer step (Muon + AdamW) after the fwd+bwd step")
     return ap.parse_args()
 
 
@@ -304,6 +306,47 @@ def our_arm(args):
     fpt = W.model_flops_per_token(w)
     mfu = value * fpt / (ws * pk["bf16_tflops"] * 1e12)
 
+    # ---- the optimizer step (clip, AdamW, Muon) on the same buffers, timed on its own
+    opt = None
+    if not args.no_optimizer:
+        lr_a, lr_m, wd, clip = 3e-3, 2e-2, 0.1, 1.0
+        state = torch.empty(nc.nc_optim_state_bytes(st.ctx) // 4, dtype=torch.float32, device="cuda")
+        stats = torch.zeros(2, dtype=torch.float32, device="cuda")
+        nc.nc_optim_init(st.ctx, params.data_ptr(), state.data_ptr())
+
+        def opt_step(t):
+            nc.nc_optim_step(st.ctx, params.data_ptr(), grads.data_ptr(), state.data_ptr(), t, lr_a, lr_m, wd, clip,
+                             stats.data_ptr())
+
+        for t in range(1, args.warmup + 1):
+            opt_step(t)
+        torch.cuda.synchronize()
+        nc.nc_profile_enable(st.ctx, True)
+        o0, o1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            o0.record(stream)
+            for t in range(args.steps):
+                opt_step(args.warmup + 1 + t)
+            o1.record(stream)
+        torch.cuda.synchronize()
+        ms_opt = o0.elapsed_time(o1) / args.steps
+        ns = nc.nc_profile_read(st.ctx, nc.NC_FAM_OPT_NS)
+        el = nc.nc_profile_read(st.ctx, nc.NC_FAM_OPT_ELEM)
+        nc.nc_profile_enable(st.ctx, False)
+        ms_opt_max, _ = reduce_over_ranks(ms_opt, 0, "cuda")
+        opt = {
+            "ms_per_step": ms_opt_max,
+            "newton_schulz": {"ms_per_step": ns[0] / args.steps, "launches_per_step": ns[1] / args.steps,
+                              "tflops": ns[2] / (ns[0] / 1000.0) / 1e12 if ns[0] > 0 else None},
+            "elementwise": {"ms_per_step": el[0] / args.steps, "launches_per_step": el[1] / args.steps,
+                            "gbs": el[2] / (el[0] / 1000.0) / 1e9 if el[0] > 0 else None},
+            "tokens_per_s_with_optimizer": job_tokens_per_s(ws, M, ms_max + ms_opt_max),
+            "hyper": {"lr_adamw": lr_a, "lr_muon": lr_m, "weight_decay": wd, "max_grad_norm": clip,
+                      "muon_momentum": 0.95, "ns_steps": 5},
+            "grad_norm": float(stats[0].item()),
+        }
+        del state
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tps, _ = oracle_tokens_per_s(w, params_np, w.seq_len, 1, 0)
@@ -325,7 +368,7 @@ def our_arm(args):
             "model_flops_per_token": fpt,
             "loss": loss0,
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches_all,
-            "roofline": roofline, "families": families, "cpu_baseline": cpu,
+            "roofline": roofline, "families": families, "optimizer": opt, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     st.close()

@@ -103,21 +103,37 @@ struct AttnParams {
 
 // ============================================================== forward
 //
-// MMA issue order per CTA: S_0, S_1, PV_0, S_2, PV_1, ... : S_{j+1} (into the
-// other TMEM S buffer) runs while the softmax threads work on S_j, and PV_j
-// accumulates straight into the TMEM output O. The softmax keeps, per row, a
-// reference maximum m (log2 units) and exponentiates against it; only when a
-// tile's maximum exceeds m by more than 8 (so p could exceed 2^8) does the
-// warp move m up and rescale its rows of O and the running sum l, after the
-// previous PV has landed. P_j goes to shared-memory buffer j % 2; PV_{j-2}
-// (the last reader of that buffer) finished before S_j's completion fired.
+// One CTA per (b, h, pair of 128-query tiles qa = 2i and qb = 2i + 1), so the
+// 256 query rows of a pair share every K/V tile the CTA loads. Warp 0 loads
+// by TMA, one thread of warp 1 issues the MMAs, warps 4-7 run the softmax of
+// tile a and warps 8-11 that of tile b with one thread per query row (TMEM
+// lane = row): a row's maximum and sum never leave its thread. Warps 2-3 only
+// take part in setup and teardown.
+//
+// TMEM: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512). The softmax
+// writes P (bf16, two keys per 32-bit column) over the first 64 columns of its
+// S buffer and O += P V reads it straight from TMEM.
+//
+// MMA order for key tile j: PV_a(j-1), S_a(j), PV_b(j-1), S_b(j). While the
+// softmax of one tile works on S(j), the tensor cores run the other tile's PV
+// and S. A commit covers every MMA issued before it, so once S_x(j) is seen
+// complete, PV_x(j-1) has landed as well: O_x is quiescent while softmax x
+// looks at it, and P_x(j-1) was read before S_x(j) overwrote it.
+//
+// The softmax keeps per row a reference maximum m (log2 units) and
+// exponentiates against it; only when a tile's maximum exceeds m by more than
+// 8 (so p could exceed 2^8) does it move m up and rescale the row of O and
+// the running sum.
 
 constexpr float kRescaleLog2 = 8.f;
-constexpr int FWD_WARPS = 10;
+constexpr int FWD_WARPS = 12;
 constexpr int FWD_THREADS = 32 * FWD_WARPS;
-constexpr int FWD_SOFT = 32 * (FWD_WARPS - 2);  // 256 softmax threads
-
-__device__ __forceinline__ void bar_pair(int id) { asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory"); }
+constexpr int FWD_SOFT = 128;  // threads per softmax warpgroup
+// Registers: launched at 168 per thread (384 threads, 64512 in all); the
+// load/MMA warpgroup drops to 56 and the two softmax warpgroups rise to 224:
+// 128 * 56 + 2 * 128 * 224 = 64512, within the launch's total.
+constexpr int FWD_REG_LAUNCH = 168, FWD_REG_LOW = 56, FWD_REG_HIGH = 224;
+static_assert(128 * FWD_REG_LOW + 2 * 128 * FWD_REG_HIGH <= FWD_THREADS * FWD_REG_LAUNCH, "register split");
 
 __global__ void __launch_bounds__(FWD_THREADS, 1)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ AttnParams p) {
@@ -130,34 +146,31 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     return;
   }
   uint8_t* smem = smem_raw;
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + TILE_BYTES;          // 2 stages
+  uint8_t* sQ = smem;                     // Q_a, Q_b
+  uint8_t* sK = sQ + 2 * TILE_BYTES;      // 2 stages
   uint8_t* sV = sK + 2 * TILE_BYTES;      // 2 stages
-  uint8_t* sP = sV + 2 * TILE_BYTES;      // 2 buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * TILE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * TILE_BYTES);
   uint64_t* q_full = bars + 0;
   uint64_t* kv_full = bars + 1;   // [2]
   uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_full = bars + 5;    // [2]: tile a, tile b
   uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* pv_done = bars + 9;
-  uint64_t* o_full = bars + 10;
-  uint64_t* drain = bars + 11;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
+  uint64_t* o_full = bars + 9;
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  // row-max exchange between the two softmax warps of a lane quadrant,
-  // [quadrant][column half][lane], and their ok flags [quadrant][half]
-  float* xmax = reinterpret_cast<float*>(tmem_holder + 4);
-  volatile int* xok = reinterpret_cast<volatile int*>(xmax + 4 * 2 * 32);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   // (batch, head)-major order: the CTAs running together share one head's K/V
-  // in L2; within a head the heaviest query tiles go first
-  const int bh = (int)(blockIdx.x / p.nq), b = bh / p.H, h = bh % p.H;
-  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);
+  // in L2; within a head the heaviest query-tile pairs go first
+  const int npair = (p.nq + 1) / 2;
+  const int bh = (int)(blockIdx.x / npair), b = bh / p.H, h = bh % p.H;
+  const int pi = npair - 1 - (int)(blockIdx.x % npair);
+  const int qa = 2 * pi;
+  const bool has_b = qa + 1 < p.nq;       // an odd tile count leaves the last pair single
+  const int nkv_a = qa + 1, nkv = has_b ? qa + 2 : qa + 1;
   const int d = p.H * 128;
-  const int row0 = b * p.T + qt * TILE;
-  const int nkv = qt + 1;
+  const int row0 = b * p.T + qa * TILE;   // first query row of tile a
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
@@ -167,7 +180,6 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       tc::mbar_init(s_full + s, 1);
       tc::mbar_init(p_full + s, FWD_SOFT);
     }
-    tc::mbar_init(pv_done, 1);
     tc::mbar_init(o_full, 1);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -181,192 +193,176 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  const uint32_t tO = tmem + 256;  // S buffers at columns 0 and 128
   bool failed = false;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      tc::prefetch_tmap(&tqkv);
-      tc::mbar_arrive_expect_tx(q_full, TILE_BYTES);
-      tc::tma_load_2d(sQ, &tqkv, h * 128, row0, q_full);
-      tc::tma_load_2d(sQ + HALF_BYTES, &tqkv, h * 128 + 64, row0, q_full);
-      bool issued[2] = {false, false};
-      uint32_t iphase[2] = {0, 0};
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!tc::mbar_wait(kv_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
-        const int kr = b * p.T + j * TILE;
-        tc::mbar_arrive_expect_tx(kv_full + s, 2 * TILE_BYTES);
-        tc::tma_load_2d(sK + s * TILE_BYTES, &tqkv, d + h * 128, kr, kv_full + s);
-        tc::tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tqkv, d + h * 128 + 64, kr, kv_full + s);
-        tc::tma_load_2d(sV + s * TILE_BYTES, &tqkv, 2 * d + h * 128, kr, kv_full + s);
-        tc::tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tqkv, 2 * d + h * 128 + 64, kr, kv_full + s);
-        issued[s] = true;
-        iphase[s] = ph;
+  if (warp < 4) {
+    tc::setmaxnreg_dec<FWD_REG_LOW>();
+    if (warp == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      if (lane == 0) {
+        tc::prefetch_tmap(&tqkv);
+        tc::mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * TILE_BYTES);
+        for (int t = 0; t < (has_b ? 2 : 1); ++t) {
+          tc::tma_load_2d(sQ + t * TILE_BYTES, &tqkv, h * 128, row0 + t * TILE, q_full);
+          tc::tma_load_2d(sQ + t * TILE_BYTES + HALF_BYTES, &tqkv, h * 128 + 64, row0 + t * TILE, q_full);
+        }
+        bool issued[2] = {false, false};
+        uint32_t iphase[2] = {0, 0};
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j & 1;
+          const uint32_t ph = (j >> 1) & 1;
+          if (!tc::mbar_wait(kv_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+          const int kr = b * p.T + j * TILE;
+          tc::mbar_arrive_expect_tx(kv_full + s, 2 * TILE_BYTES);
+          tc::tma_load_2d(sK + s * TILE_BYTES, &tqkv, d + h * 128, kr, kv_full + s);
+          tc::tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tqkv, d + h * 128 + 64, kr, kv_full + s);
+          tc::tma_load_2d(sV + s * TILE_BYTES, &tqkv, 2 * d + h * 128, kr, kv_full + s);
+          tc::tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tqkv, 2 * d + h * 128 + 64, kr, kv_full + s);
+          issued[s] = true;
+          iphase[s] = ph;
+        }
+        if (failed) {
+          *abort_flag = 1;
+          tc::mbar_wait(q_full, 0, nullptr, kWaitNs);
+          for (int s = 0; s < 2; ++s)
+            if (issued[s]) tc::mbar_wait(kv_full + s, iphase[s], nullptr, kWaitNs);
+        }
       }
-      if (failed) {
-        *abort_flag = 1;
-        tc::mbar_wait(q_full, 0, nullptr, kWaitNs);
-        for (int s = 0; s < 2; ++s)
-          if (issued[s]) tc::mbar_wait(kv_full + s, iphase[s], nullptr, kWaitNs);
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);
-      const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);
-      const uint32_t aQ = tc::smem_u32(sQ);
-      bool any = false;
-      if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
-      // PV_i = P_i V_i accumulated into O, once the softmax threads released P_i
-      auto issue_pv = [&](int i) -> bool {
-        const int s = i & 1;
-        if (!tc::mbar_wait(p_full + s, (i >> 1) & 1, abort_flag, kWaitNs)) return false;
-        tc::tc_fence_after();
-        mma_tile(tO, tc::smem_u32(sP + s * TILE_BYTES), false, tc::smem_u32(sV + s * TILE_BYTES), true, idesc_pv,
-                 i > 0);
-        tc::mma_commit(pv_done);
-        tc::mma_commit(kv_empty + s);
-        return true;
-      };
-      for (int j = 0; j < nkv && !failed; ++j) {
-        const int s = j & 1;
-        if (!tc::mbar_wait(kv_full + s, (j >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        tc::tc_fence_after();
-        // S_j into buffer s: its previous reader (softmax of S_{j-2}) released
-        // it before PV_{j-2} was issued.
-        mma_tile(tmem + s * 128, aQ, false, tc::smem_u32(sK + s * TILE_BYTES), false, idesc, false);
-        tc::mma_commit(s_full + s);
-        any = true;
-        if (j > 0 && !issue_pv(j - 1)) { failed = true; break; }
-      }
-      if (!failed && !issue_pv(nkv - 1)) failed = true;
-      if (!failed) tc::mma_commit(o_full);
-      if (failed) {
-        *abort_flag = 1;
-        if (any) {
-          tc::mma_commit(drain);
-          tc::mbar_wait(drain, 0, nullptr, kWaitNs);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      if (lane == 0) {
+        const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);     // S = Q K^T, both K-major
+        const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);  // O += P V, V MN-major
+        bool any = false;
+        if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
+        // O_x += P_x(i) V_i, P_x read from the first 64 columns of S_x
+        auto issue_pv = [&](int x, int i) -> bool {
+          if (!tc::mbar_wait(p_full + x, i & 1, abort_flag, kWaitNs)) return false;
+          tc::tc_fence_after();
+          const uint32_t tP = tmem + x * 128, tO = tmem + 256 + x * 128;
+          const uint32_t aV = tc::smem_u32(sV + (i & 1) * TILE_BYTES);
+  #pragma unroll
+          for (int k = 0; k < TILE / 16; ++k)
+            tc::mma_bf16_tmem_a(tO, tP + k * 8, desc_mn(aV, k), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+          return true;
+        };
+        for (int j = 0; j < nkv && !failed; ++j) {
+          const int s = j & 1;
+          if (j > 0 && j - 1 < nkv_a && !issue_pv(0, j - 1)) { failed = true; break; }
+          if (!tc::mbar_wait(kv_full + s, (j >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::tc_fence_after();
+          const uint32_t aK = tc::smem_u32(sK + s * TILE_BYTES);
+          if (j < nkv_a) {
+            mma_tile(tmem, tc::smem_u32(sQ), false, aK, false, idesc, false);
+            tc::mma_commit(s_full + 0);
+            any = true;
+          }
+          if (has_b) {
+            if (j > 0 && !issue_pv(1, j - 1)) { failed = true; break; }
+            mma_tile(tmem + 128, tc::smem_u32(sQ + TILE_BYTES), false, aK, false, idesc, false);
+            tc::mma_commit(s_full + 1);
+            any = true;
+          }
+          if (j > 0) tc::mma_commit(kv_empty + (s ^ 1));  // every reader of K_{j-1} / V_{j-1} is issued
+        }
+        // the last PV of each tile
+        if (!failed && !has_b && !issue_pv(0, nkv_a - 1)) failed = true;
+        if (!failed && has_b && !issue_pv(1, nkv - 1)) failed = true;
+        if (!failed) tc::mma_commit(o_full);
+        if (failed) {
+          *abort_flag = 1;
+          if (any) {
+            tc::mma_commit(drain);
+            tc::mbar_wait(drain, 0, nullptr, kWaitNs);
+          }
         }
       }
     }
-  } else {
-    // ---------------------------------------------------------------- softmax warps
-    const int q4 = warp & 3;          // TMEM lane quadrant
-    const int ch = (warp - 2) >> 2;   // 64-column half of S (keys) and of O (dims)
-    const int r = q4 * 32 + lane;     // query row within the tile = TMEM lane
+  } else if (warp < 8 || has_b) {
+    // ---------------------------------------------------------------- softmax warpgroups
+    tc::setmaxnreg_inc<FWD_REG_HIGH>();
+    const int x = (warp - 4) >> 2;          // 0: tile a, 1: tile b
+    const int qt = qa + x;                  // this tile's index; its diagonal key tile is qt
+    const int q4 = warp & 3;                // TMEM lane quadrant
+    const int r = q4 * 32 + lane;           // query row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_off, tO = tmem + 256 + x * 128 + lane_off;
     const float sl2 = kLog2e * rsqrtf(128.f);
-    float m = -INFINITY, l = 0.f;     // l: this warp's half of the row sum
-    for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
-      // a failure is only acted on at the pair exchange below, so that both
-      // warps of a quadrant leave the loop at the same barrier
-      bool ok = !failed && tc::mbar_wait(s_full + s, (j >> 1) & 1, abort_flag, kWaitNs);
-      ok = __all_sync(0xffffffffu, ok);
+    float m = -INFINITY, l = 0.f;
+    for (int j = 0; j <= qt; ++j) {
+      bool ok = tc::mbar_wait(s_full + x, j & 1, abort_flag, kWaitNs);
+      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+      tc::tc_fence_after();
+      float v[128];
+      tc::tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, v, v + 32, v + 64, v + 96);
       const bool diag = (j == qt);
-      float v[64];
-      float mx = -INFINITY;
-      if (ok) {
-        tc::tc_fence_after();
-        tc::tmem_ld32x2(tmem + s * 128 + lane_off + ch * 64, tmem + s * 128 + lane_off + ch * 64 + 32, v, v + 32);
-        if (diag) {
+      if (diag) {
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (ch * 64 + i <= r) mx = fmaxf(mx, v[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) mx = fmaxf(mx, v[i]);
-        }
-        mx *= sl2;  // the scale is positive, so it commutes with the max
+        for (int i = 0; i < 128; ++i)
+          if (i > r) v[i] = -INFINITY;
       }
-      // both warps of the quadrant always meet here, whatever their waits gave;
-      // the second barrier keeps the slots until both have read them
-      const int slot = (q4 * 2 + ch) * 32 + lane, oslot = (q4 * 2 + (ch ^ 1)) * 32 + lane;
-      xmax[slot] = mx;
-      if (lane == 0) xok[q4 * 2 + ch] = ok ? 1 : 0;
-      bar_pair(1 + q4);
-      const bool ok_both = ok && xok[q4 * 2 + (ch ^ 1)] != 0;
-      mx = fmaxf(mx, xmax[oslot]);
-      bar_pair(1 + q4);
-      if (!ok_both) { failed = true; break; }
+      float mx4[4] = {v[0], v[1], v[2], v[3]};
+#pragma unroll
+      for (int i = 4; i < 128; i += 4) {
+        mx4[0] = fmaxf(mx4[0], v[i]);
+        mx4[1] = fmaxf(mx4[1], v[i + 1]);
+        mx4[2] = fmaxf(mx4[2], v[i + 2]);
+        mx4[3] = fmaxf(mx4[3], v[i + 3]);
+      }
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;  // scale > 0 commutes with max
       const bool grow = mx > m + kRescaleLog2;
       if (__any_sync(0xffffffffu, grow)) {
-        // move this warp's reference maxima up; rows of O that already hold
-        // partial sums are rescaled once the previous PV has landed
         const float m_new = grow ? mx : m;
         const float alpha = exp2f(m - m_new);  // 0 for the first tile (m = -inf)
         l *= alpha;
         m = m_new;
-        if (j > 0) {
-          ok = tc::mbar_wait(pv_done, (j - 1) & 1, abort_flag, kWaitNs);
-          if (!__all_sync(0xffffffffu, ok)) {
-            failed = true;  // reported to the partner at the next exchange
-          } else {
-            tc::tc_fence_after();
-            float o[64];
-            tc::tmem_ld32x2(tO + lane_off + ch * 64, tO + lane_off + ch * 64 + 32, o, o + 32);
+        if (j > 0) {  // O holds partial sums: rescale this row (no PV on it is in flight)
 #pragma unroll
-            for (int i = 0; i < 64; ++i) o[i] *= alpha;
-            tc::tmem_st32(tO + lane_off + ch * 64, o);
-            tc::tmem_st32(tO + lane_off + ch * 64 + 32, o + 32);
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tc::tmem_ld32(tO + c * 32, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            tc::tmem_st32(tO + c * 32, o);
           }
         }
       }
-      float rs = 0.f;
-      uint8_t* pbuf = sP + s * TILE_BYTES;
       const float nm = -m;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t pk[64];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        float e[8];
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int k = g * 8 + i;
-            e[i] = (ch * 64 + k <= r) ? tc::ex2(fmaf(v[k], sl2, nm)) : 0.f;
-            rs += e[i];
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            e[i] = tc::ex2(fmaf(v[g * 8 + i], sl2, nm));
-            rs += e[i];
-          }
-        }
-        st_tile8(pbuf, r, ch * 8 + g, pack8(e));
+      for (int i = 0; i < 64; ++i) {
+        const float e0 = tc::ex2(fmaf(v[2 * i], sl2, nm));      // ex2(-inf) = 0 for masked keys
+        const float e1 = tc::ex2(fmaf(v[2 * i + 1], sl2, nm));
+        rs[i & 3] += e0 + e1;
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      l += rs;
-      fence_async_smem();
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      tc::tmem_st32(tS, reinterpret_cast<const float*>(pk));
+      tc::tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
       tc::tc_fence_before();
-      tc::mbar_arrive(p_full + s);
+      tc::mbar_arrive(p_full + x);
     }
     bool ok = !failed;
     if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
-    ok = __all_sync(0xffffffffu, ok);
-    // combine the two halves of the row sum
-    {
-      const int slot = (q4 * 2 + ch) * 32 + lane, oslot = (q4 * 2 + (ch ^ 1)) * 32 + lane;
-      xmax[slot] = l;
-      if (lane == 0) xok[q4 * 2 + ch] = ok ? 1 : 0;
-      bar_pair(1 + q4);
-      ok = ok && xok[q4 * 2 + (ch ^ 1)] != 0;
-      l += xmax[oslot];
-    }
     if (__all_sync(0xffffffffu, ok)) {
       tc::tc_fence_after();
       const float inv = 1.f / l;
-      bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128 + ch * 64;
-      float o[64];
-      tc::tmem_ld32x2(tO + lane_off + ch * 64, tO + lane_off + ch * 64 + 32, o, o + 32);
+      const int row = row0 + x * TILE + r;
+      bf16* orow = p.o + (size_t)row * d + h * 128;
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        float w8[8];
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tc::tmem_ld32(tO + c * 32, o);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) w8[i] = o[g * 8 + i] * inv;
-        *reinterpret_cast<uint4*>(orow + g * 8) = pack8(w8);
+        for (int g = 0; g < 4; ++g) {
+          float w8[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w8[i] = o[g * 8 + i] * inv;
+          *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = pack8(w8);
+        }
       }
-      if (ch == 0) p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
+      p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
     } else {
       failed = true;
       *abort_flag = 1;
@@ -770,7 +766,7 @@ bool map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int FWD_SMEM = 7 * TILE_BYTES + 2048;  // tiles, barriers + exchange
+constexpr int FWD_SMEM = 6 * TILE_BYTES + 256;  // Q pair, 2 K/V stages, barriers
 constexpr int BWD_SMEM = 7 * TILE_BYTES + 2 * 2 * TILE * 4 + 256;
 
 }  // namespace
@@ -788,7 +784,7 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
   p.o = o; p.lse = lse; p.status = status;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_fwd_tc_k<<<B * H * p.nq, FWD_THREADS, FWD_SMEM, s>>>(tq, p);
+  attn_fwd_tc_k<<<B * H * ((p.nq + 1) / 2), FWD_THREADS, FWD_SMEM, s>>>(tq, p);
   return cudaGetLastError();
 }
 

@@ -209,7 +209,8 @@ def _qkv(rng, B, T, H, prec):
     return rounded(qkv, prec).reshape(B * T, 3 * H * D)
 
 
-@pytest.mark.parametrize("prec,T", [(0, 256), (0, 640), (1, 100)], ids=["bf16_T256", "bf16_T640", "fp32_T100"])
+@pytest.mark.parametrize("prec,T", [(0, 128), (0, 256), (0, 384), (0, 640), (1, 100)],
+                         ids=["bf16_T128", "bf16_T256", "bf16_T384", "bf16_T640", "fp32_T100"])
 def test_attention_fwd_bwd(nc, prec, T):
     import torch
     B, H, D = 2, 2, 128
