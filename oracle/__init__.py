@@ -5,7 +5,7 @@ this package. It shares no code with the CUDA library and the library never
 calls it: there is no CPU fallback anywhere in the product path.
 """
 
-from .model import (EPS, HEAD_DIM, ROPE_BASE, Shape, backward, causal_attention,
+from .model import (EPS, HEAD_DIM, IGNORE, ROPE_BASE, Shape, backward, causal_attention,
                     causal_attention_backward, cross_entropy_backward,
                     cross_entropy_rows, forward, layout, param_count, relu2,
                     relu2_backward, rmsnorm, rmsnorm_backward, rope,

@@ -27,6 +27,12 @@ QK-norm); RoPE in the half-split pairing (dim j pairs with j + 64), angle
 pos * 10000^(-j/64), positions from 0 in every sequence, angles formed in
 float64; attention scale 1/sqrt(128); no biases, dropout or logit capping;
 loss = mean over all B*T positions in nats; argmax = lowest index among ties.
+
+The supervised fine-tuning variant ("Supervised Fine-Tuning (SFT)": the same
+cross-entropy, but only on the assistant's response tokens; the prompt tokens
+are masked from the loss) is expressed by the target id IGNORE (-1): such a
+position contributes no loss and no gradient, and the loss is the mean over
+the remaining positions (0 when there are none).
 """
 
 from __future__ import annotations
@@ -38,6 +44,7 @@ import numpy as np
 EPS = 1e-6
 ROPE_BASE = 10000.0
 HEAD_DIM = 128
+IGNORE = -1
 
 
 @dataclasses.dataclass(frozen=True)
@@ -195,7 +202,8 @@ def cross_entropy_rows(hf, w_lm, tgt, chunk: int = 2048):
 
     ("Pretraining": cross-entropy between the predicted logits and the actual
     next tokens.) Rows are processed in chunks only to bound memory.
-    Returns lse [M], nll [M], argmax [M] (lowest index on ties).
+    Returns lse [M], nll [M], argmax [M] (lowest index on ties). A target of
+    IGNORE gives nll 0 at that row (lse and argmax are still those of the row).
     """
     M = hf.shape[0]
     lse = np.empty(M, dtype=hf.dtype)
@@ -207,22 +215,31 @@ def cross_entropy_rows(hf, w_lm, tgt, chunk: int = 2048):
         m = np.max(logits, axis=-1, keepdims=True)
         z = np.log(np.sum(np.exp(logits - m), axis=-1, keepdims=True)) + m
         lse[s:e] = z[:, 0]
-        nll[s:e] = z[:, 0] - logits[np.arange(e - s), tgt[s:e]]
+        t = tgt[s:e]
+        keep = t != IGNORE
+        picked = logits[np.arange(e - s), np.where(keep, t, 0)]
+        nll[s:e] = np.where(keep, z[:, 0] - picked, 0.0)
         amax[s:e] = np.argmax(logits, axis=-1)
     return lse, nll, amax
 
 
 def cross_entropy_backward(hf, w_lm, tgt, lse, chunk: int = 2048):
-    """g = (softmax(logits) - onehot(tgt)) / M; dW_lm = g^T hf; dhf = g W_lm."""
+    """g = (softmax(logits) - onehot(tgt)) / n on the n rows whose target is
+    not IGNORE, 0 on the others; dW_lm = g^T hf; dhf = g W_lm."""
     M = hf.shape[0]
+    n = int(np.count_nonzero(np.asarray(tgt) != IGNORE))
     dhf = np.empty_like(hf)
     dw = np.zeros_like(w_lm)
     for s in range(0, M, chunk):
         e = min(M, s + chunk)
         logits = hf[s:e] @ w_lm.T
+        t = tgt[s:e]
+        keep = t != IGNORE
         g = np.exp(logits - lse[s:e, None])
-        g[np.arange(e - s), tgt[s:e]] -= 1
-        g /= M
+        g[np.arange(e - s)[keep], t[keep]] -= 1
+        g[~keep] = 0
+        if n:
+            g /= n
         dhf[s:e] = g @ w_lm
         dw += g.T @ hf[s:e]
     return dhf, dw
@@ -272,7 +289,8 @@ def forward(params, tokens, targets, s: Shape, dtype=np.float64, keep=True):
     hf, rf = rmsnorm(x)
     M = B * T
     lse, nll, amax = cross_entropy_rows(hf.reshape(M, d), P["lm_head"], tgt.reshape(M))
-    loss = float(np.mean(nll))
+    valid = tgt.reshape(M) != IGNORE
+    loss = float(np.sum(nll[valid]) / np.count_nonzero(valid)) if valid.any() else 0.0
     cache = dict(P=P, tok=tok, tgt=tgt, layers=layers, hf=hf, rf=rf, lse=lse,
                  nll=nll, argmax=amax, cos=cos, sin=sin, shape=s, dtype=dtype)
     return loss, cache

@@ -402,3 +402,35 @@ def test_inputs_are_deterministic_and_zipf_shaped():
     assert abs(frac0 - p0) < 0.02
     p = W.make_params(w)
     assert np.all(W.round_bf16(p) == p)
+
+
+# ------------------------------------------------------------ SFT: masked loss
+
+def test_masked_loss_is_the_mean_over_response_positions():
+    # explainer, "Supervised Fine-Tuning (SFT)": the same cross-entropy, only
+    # on the response tokens. Masking changes nothing before the loss, so the
+    # masked loss is the mean of the unmasked run's per-position losses over
+    # the kept positions, and masked positions report nll 0.
+    w, s, p, tok, tgt = tiny_case(vocab=1024)
+    sft = W.make_sft_targets(tgt, seed=3, mean_turn=16)
+    keep = sft != oracle.IGNORE
+    assert 0 < keep.sum() < keep.size
+    _, full = oracle.forward(p, tok, tgt, s, np.float64, keep=False)
+    loss, masked = oracle.forward(p, tok, sft, s, np.float64, keep=False)
+    assert abs(loss - float(np.mean(full["nll"][keep.reshape(-1)]))) < 1e-12
+    assert np.all(masked["nll"][~keep.reshape(-1)] == 0.0)
+    np.testing.assert_array_equal(masked["lse"], full["lse"])
+
+
+def test_fully_masked_batch_has_zero_loss_and_zero_gradient():
+    w, s, p, tok, tgt = tiny_case(vocab=1024)
+    none = np.full_like(tgt, oracle.IGNORE)
+    loss, grads, _ = oracle.step(p, tok, none, s, np.float64)
+    assert loss == 0.0 and not np.any(grads)
+
+
+def test_finite_differences_masked_loss():
+    # the analytic backward of the masked mean, against central differences
+    w, s, p, tok, tgt = tiny_case(vocab=1024)
+    sft = W.make_sft_targets(tgt, seed=4, mean_turn=16)
+    _fd_check(w, s, p, tok, sft, coords_per_tensor=8, seed=13)

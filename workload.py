@@ -156,6 +156,26 @@ def make_grads(w: Workload, seed: int = 100, std: float = 1e-3) -> np.ndarray:
     return out
 
 
+def make_sft_targets(targets: np.ndarray, seed: int = 200, mean_turn: int = 128) -> np.ndarray:
+    """Targets of the supervised fine-tuning variant: every sequence is a run
+    of alternating prompt and response turns, starting with a prompt, with
+    turn lengths uniform in [mean_turn / 4, 7 mean_turn / 4); targets inside
+    prompt turns become -1 (no loss there). Draws from PCG64(seed)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = np.array(targets, dtype=np.int32, copy=True)
+    B, T = out.shape
+    lo, hi = max(1, mean_turn // 4), max(2, (7 * mean_turn) // 4)
+    for b in range(B):
+        t, prompt = 0, True
+        while t < T:
+            n = int(rng.integers(lo, hi))
+            if prompt:
+                out[b, t:t + n] = -1
+            t += n
+            prompt = not prompt
+    return out
+
+
 def zipf_cdf(vocab: int, s: float = 1.1) -> np.ndarray:
     k = np.arange(1, vocab + 1, dtype=np.float64)
     p = k ** (-s)
