@@ -92,8 +92,8 @@ extern "C" nc_status nc_lmhead_ce_fwd_static(const void* hf, const void* w_lm, c
   // it so that an out-of-range target cannot pick up a previous call's value.
   if (cudaMemsetAsync(g.p_tgt, 0, (size_t)M * 4, s) != cudaSuccess ||
       (d_status && cudaMemsetAsync(d_status, 0, sizeof(int32_t), s) != cudaSuccess) ||
-      check_ids(tgt, M, V, d_status, s) != cudaSuccess || gemm_tc(g, s) != cudaSuccess ||
-      ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, (int)tiles, lse, nll, argmax, M, s) != cudaSuccess)
+      check_ids(tgt, M, 0, V, d_status, s) != cudaSuccess || gemm_tc(g, s) != cudaSuccess ||
+      ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, tgt, (int)tiles, lse, nll, argmax, M, s) != cudaSuccess)
     return set_last_error(NC_ERR_CUDA, "nc_lmhead_ce_fwd_static: a kernel launch failed");
   return NC_OK;
 }

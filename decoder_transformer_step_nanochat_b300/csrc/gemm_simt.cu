@@ -96,8 +96,10 @@ __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs g) {
           break;
         }
         case EPI_CE_BWD: {
+          const int t = g.row_i[m];
+          const float sc = t < 0 ? 0.f : (g.dscale ? *g.dscale : 1.f);  // masked rows: no gradient
           float p = expf(v - g.row_f[m]);
-          stf(static_cast<T*>(g.C) + ci, p - (n == g.row_i[m] ? 1.f : 0.f));
+          stf(static_cast<T*>(g.C) + ci, (p - (n == t ? 1.f : 0.f)) * sc);
           break;
         }
         case EPI_AXPBY: {

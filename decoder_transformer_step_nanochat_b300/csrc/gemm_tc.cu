@@ -146,22 +146,6 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int nc0, flo
         *reinterpret_cast<uint4*>(c + 8 * j) = pack8_bf16(o);
       }
     }
-  } else if (EPI == EPI_CE_BWD) {
-    float l = g.row_f[m];
-    int t = g.row_i[m];
-    bf16* c = static_cast<bf16*>(g.C) + (size_t)m * g.ldc + nc0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (nc0 + 8 * j < g.N) {
-        float o[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          int n = nc0 + 8 * j + i;
-          o[i] = __expf(v[8 * j + i] - l) - (n == t ? 1.f : 0.f);
-        }
-        *reinterpret_cast<uint4*>(c + 8 * j) = pack8_bf16(o);
-      }
-    }
   }
 }
 
@@ -512,8 +496,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               if (row_ok) {
                 const float l = g.row_f[m];
                 const int t = g.row_i[m];
+                const float sc = t < 0 ? 0.f : (g.dscale ? *g.dscale : 1.f);  // masked rows: no gradient
 #pragma unroll
-                for (int i = 0; i < 64; ++i) w[i] = __expf(w[i] - l) - (nc0 + i == t ? 1.f : 0.f);
+                for (int i = 0; i < 64; ++i) w[i] = (__expf(w[i] - l) - (nc0 + i == t ? 1.f : 0.f)) * sc;
               }
             } else if (EPI == EPI_AXPBY) {
               if (row_ok) {

@@ -15,7 +15,7 @@ enum Epi : int {
   EPI_STORE_F32 = 1,   // C (f32)  = alpha*acc + beta*C
   EPI_RELU2 = 2,       // C (elem) = u = alpha*acc ; C2 (elem) = max(u,0)^2
   EPI_RELU2_BWD = 3,   // C (elem) = alpha*acc * 2*max(u,0), u read from C2
-  EPI_CE_BWD = 4,      // C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])
+  EPI_CE_BWD = 4,      // C (elem) = (exp(alpha*acc - row_f[m]) - (n == row_i[m])) * s, s = *dscale (0 if row_i[m] < 0)
   EPI_CE_FWD = 5,      // per (row, 128-column tile) softmax partials (tensor-core path)
   EPI_QKNORM_ROPE = 6, // C (elem) = qkv with per-head RMSNorm + RoPE on the q,k columns
   EPI_AXPBY = 7,       // C (elem) = alpha*acc + beta*C2 (C2 elem, same shape as C)
@@ -30,7 +30,8 @@ struct GemmArgs {
   void* C = nullptr; long long ldc = 0;
   void* C2 = nullptr; long long ldc2 = 0;
   const float* row_f = nullptr;  // CE bwd: lse per row
-  const int* row_i = nullptr;    // CE fwd/bwd: target id per row
+  const int* row_i = nullptr;    // CE fwd/bwd: target id per row (negative: masked row)
+  const float* dscale = nullptr; // CE bwd: device scalar the unmasked rows are scaled by (null: 1)
   // CE forward partials, [n_tiles][M] each, one tile per 128 vocabulary columns
   float* p_max = nullptr; float* p_sum = nullptr; int* p_arg = nullptr;
   float* p_tgt = nullptr;        // [M]: logit of the target column
@@ -111,11 +112,15 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
 // ------------------------------------------------------------------ loss
 cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,
                                 int* amax, int M, int V, int* status, cudaStream_t s);
+// rows whose target is negative (masked) get nll 0
 cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int* p_arg,
-                               const float* p_tgt, int n_tiles, float* lse, float* nll,
+                               const float* p_tgt, const int* tgt, int n_tiles, float* lse, float* nll,
                                int* amax, int M, cudaStream_t s);
-cudaError_t mean_loss(const float* nll, int M, float* loss, cudaStream_t s);
-cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s);
+// loss = mean of nll over unmasked rows (tgt >= 0), inv_count = 1/their number (0 if none);
+// nll, loss and inv_count may be null
+cudaError_t mean_loss(const float* nll, const int* tgt, int M, float* loss, float* inv_count, cudaStream_t s);
+// status DEV_BAD_TOKEN unless lo <= id < V for every id
+cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStream_t s);
 
 // ------------------------------------------------------------------ optimizer
 // Chunk of the Muon passes (every block matrix holds a whole number of them:

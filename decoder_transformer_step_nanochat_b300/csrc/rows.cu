@@ -266,7 +266,9 @@ __global__ void ce_rows_k(const float* __restrict__ logits, const int* __restric
     int t = tgt[m];
     lse[m] = l;
     amax[m] = amx;
-    if (t < 0 || t >= V) {
+    if (t == -1) {
+      nll[m] = 0.f;  // masked position: no loss
+    } else if (t < 0 || t >= V) {
       set_status(status, DEV_BAD_TOKEN);
       nll[m] = 0.f;
     } else {
@@ -278,8 +280,8 @@ __global__ void ce_rows_k(const float* __restrict__ logits, const int* __restric
 // Combine per-tile softmax partials (max, sum of exp(logit - max), argmax)
 // of every 256-column vocabulary tile into lse, loss and argmax per row.
 __global__ void ce_reduce_k(const float* __restrict__ pm, const float* __restrict__ ps,
-                            const int* __restrict__ pa, const float* __restrict__ pt, int nt,
-                            float* __restrict__ lse, float* __restrict__ nll, int* __restrict__ amax,
+                            const int* __restrict__ pa, const float* __restrict__ pt, const int* __restrict__ tgt,
+                            int nt, float* __restrict__ lse, float* __restrict__ nll, int* __restrict__ amax,
                             int M) {
   int m = blockIdx.x * blockDim.x + threadIdx.x;
   if (m >= M) return;
@@ -293,29 +295,48 @@ __global__ void ce_reduce_k(const float* __restrict__ pm, const float* __restric
   for (int t = 0; t < nt; ++t) s += ps[(size_t)t * M + m] * expf(pm[(size_t)t * M + m] - mx);
   float l = mx + logf(s);
   lse[m] = l;
-  nll[m] = l - pt[m];
+  nll[m] = tgt[m] < 0 ? 0.f : l - pt[m];  // a masked position carries no loss
   amax[m] = arg;
 }
 
-// loss = mean(nll), fixed summation order (one CTA, float64 partials).
-__global__ void mean_loss_k(const float* __restrict__ nll, int M, float* __restrict__ loss) {
+// loss = mean of nll over the positions whose target is not masked (-1),
+// 0 when every position is masked; inv_count = 1 / that count (0 if none).
+// Fixed summation order (one CTA, float64 partials). nll may be null: then
+// only inv_count is formed.
+__global__ void mean_loss_k(const float* __restrict__ nll, const int* __restrict__ tgt, int M,
+                            float* __restrict__ loss, float* __restrict__ inv_count) {
   __shared__ double sh[1024];
+  __shared__ int shn[1024];
   double s = 0.0;
-  for (int i = threadIdx.x; i < M; i += blockDim.x) s += (double)nll[i];
+  int n = 0;
+  for (int i = threadIdx.x; i < M; i += blockDim.x) {
+    if (tgt[i] >= 0) {
+      if (nll) s += (double)nll[i];
+      ++n;
+    }
+  }
   sh[threadIdx.x] = s;
+  shn[threadIdx.x] = n;
   __syncthreads();
   for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-    if ((int)threadIdx.x < w) sh[threadIdx.x] += sh[threadIdx.x + w];
+    if ((int)threadIdx.x < w) {
+      sh[threadIdx.x] += sh[threadIdx.x + w];
+      shn[threadIdx.x] += shn[threadIdx.x + w];
+    }
     __syncthreads();
   }
-  if (threadIdx.x == 0) *loss = (float)(sh[0] / (double)M);
+  if (threadIdx.x == 0) {
+    const int cnt = shn[0];
+    if (loss) *loss = cnt > 0 ? (float)(sh[0] / (double)cnt) : 0.f;
+    if (inv_count) *inv_count = cnt > 0 ? (float)(1.0 / (double)cnt) : 0.f;
+  }
 }
 
-__global__ void check_ids_k(const int* __restrict__ ids, int n, int V, int* status) {
+__global__ void check_ids_k(const int* __restrict__ ids, int n, int lo, int V, int* status) {
   int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) {
     int v = ids[i];
-    if (v < 0 || v >= V) set_status(status, DEV_BAD_TOKEN);
+    if (v < lo || v >= V) set_status(status, DEV_BAD_TOKEN);
   }
 }
 
@@ -404,9 +425,9 @@ cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse,
 }
 
 cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int* p_arg,
-                               const float* p_tgt, int n_tiles, float* lse, float* nll, int* amax,
+                               const float* p_tgt, const int* tgt, int n_tiles, float* lse, float* nll, int* amax,
                                int M, cudaStream_t s) {
-  ce_reduce_k<<<(M + 255) / 256, 256, 0, s>>>(p_max, p_sum, p_arg, p_tgt, n_tiles, lse, nll, amax, M);
+  ce_reduce_k<<<(M + 255) / 256, 256, 0, s>>>(p_max, p_sum, p_arg, p_tgt, tgt, n_tiles, lse, nll, amax, M);
   return cudaGetLastError();
 }
 
@@ -420,14 +441,14 @@ cudaError_t splitk_reduce(const float* partial, int splits, float* C, long long 
   return cudaGetLastError();
 }
 
-cudaError_t mean_loss(const float* nll, int M, float* loss, cudaStream_t s) {
-  mean_loss_k<<<1, 1024, 0, s>>>(nll, M, loss);
+cudaError_t mean_loss(const float* nll, const int* tgt, int M, float* loss, float* inv_count, cudaStream_t s) {
+  mean_loss_k<<<1, 1024, 0, s>>>(nll, tgt, M, loss, inv_count);
   return cudaGetLastError();
 }
 
-cudaError_t check_ids(const int* ids, int n, int V, int* status, cudaStream_t s) {
+cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
-  check_ids_k<<<(n + 255) / 256, 256, 0, s>>>(ids, n, V, status);
+  check_ids_k<<<(n + 255) / 256, 256, 0, s>>>(ids, n, lo, V, status);
   return cudaGetLastError();
 }
 

@@ -85,7 +85,7 @@ struct nc_ctx {
     size_t xn1, r1, qkv, rqk, o, lse_att, xn2, r2, u, a;  // per-layer stash (stride below)
     size_t layer_stride;
     size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
-    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial;
+    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial, inv_count;
   } off{};
   // optimizer scratch: overlays the step's workspace from offset 0 (the
   // stash is dead once the backward has run)
@@ -216,6 +216,7 @@ void plan_workspace(nc_ctx* c) {
   c->partial_bytes = 8 * 4 * d * d * 4;
   if (c->partial_bytes < (size_t(64) << 20)) c->partial_bytes = size_t(64) << 20;
   f.partial = take(c->partial_bytes);
+  f.inv_count = take(4);  // 1 / number of unmasked targets of the last forward
   c->ws_need = o;
   // optimizer scratch, from offset 0
   o = 0;
@@ -335,7 +336,7 @@ nc_status lmhead_ce_forward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt
     g.p_tgt = wsp<float>(c, c->off.ptgt);
     CKS(gemm(c, g));
     KL(NC_FAM_ROWS, 12.0 * c->ce_tiles * M + 16.0 * M, 1,
-       ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, c->ce_tiles, lse, nll, amax, M, c->stream));
+       ce_reduce_partials(g.p_max, g.p_sum, g.p_arg, g.p_tgt, tgt, c->ce_tiles, lse, nll, amax, M, c->stream));
     return NC_OK;
   }
   float* logits = wsp<float>(c, c->off.chunk);
@@ -352,7 +353,7 @@ nc_status lmhead_ce_forward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt
 // dhf is written in DT (the element type inside the step, fp32 for the op).
 template <typename T, typename DT>
 nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt, const float* lse,
-                             int M, float inv_count, DT* dhf, float* dwlm) {
+                             int M, const float* d_inv_count, DT* dhf, float* dwlm) {
   int d = c->d, V = c->V;
   T* g = wsp<T>(c, c->off.chunk);
   for (int r0 = 0; r0 < M; r0 += c->ce_rows) {
@@ -360,10 +361,11 @@ nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tg
     GemmArgs a = mk(rows, V, d, hf + (size_t)r0 * d, d, 1, wlm, d, 1, EPI_CE_BWD, g, V);
     a.row_f = lse + r0;
     a.row_i = tgt + r0;
+    a.dscale = d_inv_count;  // g = (softmax - onehot) / (unmasked rows), 0 on masked rows
     CKS(gemm(c, a));
     CKS(gemm(c, mk(rows, d, V, g, V, 1, wlm, d, 0, sizeof(DT) == 4 ? EPI_STORE_F32 : EPI_STORE,
-                   dhf + (size_t)r0 * d, d, inv_count)));
-    CKS(gemm(c, mk(V, d, rows, g, V, 0, hf + (size_t)r0 * d, d, 0, EPI_STORE_F32, dwlm, d, inv_count,
+                   dhf + (size_t)r0 * d, d)));
+    CKS(gemm(c, mk(V, d, rows, g, V, 0, hf + (size_t)r0 * d, d, 0, EPI_STORE_F32, dwlm, d, 1.f,
                    r0 == 0 ? 0.f : 1.f)));
   }
   return NC_OK;
@@ -373,8 +375,8 @@ template <typename T>
 nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* d_loss) {
   int M = c->M, d = c->d, H = c->H, F = c->F, V = c->V, Tn = c->T;
   cudaStream_t s = c->stream;
-  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tok, M, V, c->status, s));
-  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tgt, M, V, c->status, s));
+  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tok, M, 0, V, c->status, s));
+  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tgt, M, -1, V, c->status, s));  // -1: masked target
   float* x = wsp<float>(c, c->off.x);
   int rows, cols;
   KL(NC_FAM_ROWS, (double)M * d * (sizeof(T) + 4) + 4.0 * M, 1, embed_fwd<T>(tok, P, x, M, d, V, c->status, s));
@@ -420,7 +422,7 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
   const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
   CKS(lmhead_ce_forward<T>(c, hf, Wlm, tgt, M, wsp<float>(c, c->off.lse), wsp<float>(c, c->off.nll),
                            wsp<int>(c, c->off.amax)));
-  KL(NC_FAM_ROWS, 4.0 * M, 1, mean_loss(wsp<float>(c, c->off.nll), M, d_loss, s));
+  KL(NC_FAM_ROWS, 8.0 * M, 1, mean_loss(wsp<float>(c, c->off.nll), tgt, M, d_loss, wsp<float>(c, c->off.inv_count), s));
   return NC_OK;
 }
 
@@ -439,7 +441,8 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
   float* drow = wsp<float>(c, c->off.drow);
   const T* hf = wsp<T>(c, c->off.hf);
   size_t o_lm = param_offset(c, 1 + 4 * c->L, &rows, &cols);
-  CKS((lmhead_ce_backward<T, T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, 1.f / (float)M, dy, G + o_lm)));
+  CKS((lmhead_ce_backward<T, T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, wsp<float>(c, c->off.inv_count),
+                                dy, G + o_lm)));
   KL(NC_FAM_ROWS, (double)M * d * (4 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
   for (int l = c->L - 1; l >= 0; --l) {
     size_t lb = (size_t)l * c->off.layer_stride;
@@ -825,7 +828,8 @@ nc_status nc_op_lmhead_ce_bwd(nc_ctx* c, const void* hf, const void* w_lm, const
   CKS(check_ready(c));
   if (!hf || !w_lm || !tgt || !lse || !dhf || !dw_lm) return fail(NC_ERR_ARG, "null pointer argument");
   c->have_fwd = false;
-  float inv = 1.f / (float)c->M;
+  float* inv = wsp<float>(c, c->off.inv_count);  // 1 / (unmasked targets)
+  KL(NC_FAM_ROWS, 4.0 * c->M, 1, mean_loss(nullptr, tgt, c->M, nullptr, inv, c->stream));
   return c->prec == NC_BF16
              ? lmhead_ce_backward<bf16, float>(c, (const bf16*)hf, (const bf16*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm)
              : lmhead_ce_backward<float, float>(c, (const float*)hf, (const float*)w_lm, tgt, lse, c->M, inv, dhf, dw_lm);

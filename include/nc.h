@@ -99,6 +99,10 @@ nc_status nc_set_workspace(nc_ctx* ctx, void* dev_ptr, size_t bytes);
  *   (NC_FP32_DEBUG), layout of nc_param_offset.
  * tokens, targets: device int32 [batch, seq_len] row-major, ids in
  *   [0, vocab); an id out of range makes the step return NC_ERR_DEVICE.
+ *   A target of -1 masks its position (the supervised fine-tuning variant
+ *   of the nanochat explainer, "Supervised Fine-Tuning (SFT)": the loss is
+ *   taken on the response tokens only): it adds no loss and no gradient,
+ *   and the loss is the mean over the other positions (0 if none).
  * loss: HOST float*; the call synchronises the stream and writes the loss.
  * The context keeps params/tokens/targets pointers for nc_backward: the
  * caller must not change those buffers (or the workspace) in between. */
@@ -126,7 +130,8 @@ nc_status nc_train_step_host(nc_ctx* ctx, const void* params, const int32_t* h_t
 
 /* Per-position results of the last forward, copied device-to-device:
  * d_lse, d_nll: fp32 [batch*seq_len]; d_argmax: int32 [batch*seq_len]
- * (lowest vocabulary index among ties). Any pointer may be NULL. */
+ * (lowest vocabulary index among ties); d_nll is 0 at masked positions.
+ * Any pointer may be NULL. */
 nc_status nc_get_token_outputs(nc_ctx* ctx, float* d_lse, float* d_nll, int32_t* d_argmax);
 
 /* Final hidden state of the last forward (the RMS-normalised input of

@@ -69,15 +69,16 @@ nc_status nc_op_gemm_batched(nc_ctx* ctx, int batch, int M, int N, int K, const 
 /* Fused lm_head + softmax cross-entropy forward over M = batch*seq_len rows
  * (nanochat explainer, "Pretraining": cross-entropy between the predicted
  * logits and the next tokens). hf: elem [M, d]; w_lm: elem [V, d];
- * tgt: int32 [M]. Outputs lse, nll: fp32 [M]; argmax: int32 [M] (lowest
- * index among ties). The full [M, V] logits are never stored; scratch comes
- * from the context's workspace. */
+ * tgt: int32 [M] (-1 masks a row: nll 0 there). Outputs lse, nll: fp32 [M];
+ * argmax: int32 [M] (lowest index among ties). The full [M, V] logits are
+ * never stored; scratch comes from the context's workspace. */
 nc_status nc_op_lmhead_ce_fwd(nc_ctx* ctx, const void* hf, const void* w_lm, const int32_t* tgt,
                               float* lse, float* nll, int32_t* argmax);
 
 /* Backward of the mean cross-entropy w.r.t. hf and w_lm, recomputing the
- * logits: g = (softmax - onehot(tgt)) / M; dhf = g w_lm (fp32 [M, d]);
- * dw_lm = g^T hf (fp32 [V, d], overwritten). lse from nc_op_lmhead_ce_fwd. */
+ * logits: g = (softmax - onehot(tgt)) / n on the n rows whose target is not
+ * -1 and 0 on the masked rows; dhf = g w_lm (fp32 [M, d]); dw_lm = g^T hf
+ * (fp32 [V, d], overwritten). lse from nc_op_lmhead_ce_fwd. */
 nc_status nc_op_lmhead_ce_bwd(nc_ctx* ctx, const void* hf, const void* w_lm, const int32_t* tgt,
                               const float* lse, float* dhf, float* dw_lm);
 
