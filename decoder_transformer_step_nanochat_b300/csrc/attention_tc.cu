@@ -133,6 +133,8 @@ constexpr int FWD_SOFT = 128;  // threads per softmax warpgroup
 // load/MMA warpgroup drops to 56 and the two softmax warpgroups rise to 224:
 // 128 * 56 + 2 * 128 * 224 = 64512, within the launch's total.
 constexpr int FWD_REG_LAUNCH = 168, FWD_REG_LOW = 56, FWD_REG_HIGH = 224;
+// K ring of 3 stages, V ring of 2 (Q pair + rings = 224 KB of shared memory)
+constexpr int FWD_KST = 3, FWD_VST = 2;
 static_assert(128 * FWD_REG_LOW + 2 * 128 * FWD_REG_HIGH <= FWD_THREADS * FWD_REG_LAUNCH, "register split");
 
 __global__ void __launch_bounds__(FWD_THREADS, 1)
@@ -146,18 +148,20 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
     return;
   }
   uint8_t* smem = smem_raw;
-  uint8_t* sQ = smem;                     // Q_a, Q_b
-  uint8_t* sK = sQ + 2 * TILE_BYTES;      // 2 stages
-  uint8_t* sV = sK + 2 * TILE_BYTES;      // 2 stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + 2 * TILE_BYTES);
+  uint8_t* sQ = smem;                            // Q_a, Q_b
+  uint8_t* sK = sQ + 2 * TILE_BYTES;             // FWD_KST stages
+  uint8_t* sV = sK + FWD_KST * TILE_BYTES;       // FWD_VST stages
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + FWD_VST * TILE_BYTES);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]: tile a, tile b
-  uint64_t* p_full = bars + 7;    // [2]
-  uint64_t* o_full = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* k_full = bars + 1;                   // [FWD_KST]
+  uint64_t* k_empty = k_full + FWD_KST;          // [FWD_KST]
+  uint64_t* v_full = k_empty + FWD_KST;          // [FWD_VST]
+  uint64_t* v_empty = v_full + FWD_VST;          // [FWD_VST]
+  uint64_t* s_full = v_empty + FWD_VST;          // [2]: tile a, tile b
+  uint64_t* p_full = s_full + 2;                 // [2]
+  uint64_t* o_full = p_full + 2;
+  uint64_t* drain = o_full + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -174,11 +178,17 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(kv_full + s, 1);
-      tc::mbar_init(kv_empty + s, 1);
-      tc::mbar_init(s_full + s, 1);
-      tc::mbar_init(p_full + s, FWD_SOFT);
+    for (int s = 0; s < FWD_KST; ++s) {
+      tc::mbar_init(k_full + s, 1);
+      tc::mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < FWD_VST; ++s) {
+      tc::mbar_init(v_full + s, 1);
+      tc::mbar_init(v_empty + s, 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      tc::mbar_init(s_full + x, 1);
+      tc::mbar_init(p_full + x, FWD_SOFT);
     }
     tc::mbar_init(o_full, 1);
     tc::mbar_init(drain, 1);
@@ -196,84 +206,106 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   bool failed = false;
   if (warp < 4) {
     tc::setmaxnreg_dec<FWD_REG_LOW>();
-    if (warp == 0) {
-      // ---------------------------------------------------------------- TMA producer
-      if (lane == 0) {
-        tc::prefetch_tmap(&tqkv);
+    if ((warp == 0 || warp == 2) && lane == 0) {
+      // ---------------------------------------------------------------- TMA producers
+      // warp 0 loads Q and the K ring, warp 2 the V ring, so a K tile never
+      // waits behind a V stage that is still being read
+      const bool kside = warp == 0;
+      const int nst = kside ? FWD_KST : FWD_VST;
+      uint64_t* full = kside ? k_full : v_full;
+      uint64_t* empty = kside ? k_empty : v_empty;
+      uint8_t* ring = kside ? sK : sV;
+      const int col = (kside ? d : 2 * d) + h * 128;
+      tc::prefetch_tmap(&tqkv);
+      if (kside) {
         tc::mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * TILE_BYTES);
         for (int t = 0; t < (has_b ? 2 : 1); ++t) {
           tc::tma_load_2d(sQ + t * TILE_BYTES, &tqkv, h * 128, row0 + t * TILE, q_full);
           tc::tma_load_2d(sQ + t * TILE_BYTES + HALF_BYTES, &tqkv, h * 128 + 64, row0 + t * TILE, q_full);
         }
-        bool issued[2] = {false, false};
-        uint32_t iphase[2] = {0, 0};
-        for (int j = 0; j < nkv; ++j) {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!tc::mbar_wait(kv_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
-          const int kr = b * p.T + j * TILE;
-          tc::mbar_arrive_expect_tx(kv_full + s, 2 * TILE_BYTES);
-          tc::tma_load_2d(sK + s * TILE_BYTES, &tqkv, d + h * 128, kr, kv_full + s);
-          tc::tma_load_2d(sK + s * TILE_BYTES + HALF_BYTES, &tqkv, d + h * 128 + 64, kr, kv_full + s);
-          tc::tma_load_2d(sV + s * TILE_BYTES, &tqkv, 2 * d + h * 128, kr, kv_full + s);
-          tc::tma_load_2d(sV + s * TILE_BYTES + HALF_BYTES, &tqkv, 2 * d + h * 128 + 64, kr, kv_full + s);
-          issued[s] = true;
-          iphase[s] = ph;
-        }
-        if (failed) {
-          *abort_flag = 1;
-          tc::mbar_wait(q_full, 0, nullptr, kWaitNs);
-          for (int s = 0; s < 2; ++s)
-            if (issued[s]) tc::mbar_wait(kv_full + s, iphase[s], nullptr, kWaitNs);
-        }
       }
-    } else if (warp == 1) {
+      int last = -1;  // last tile issued
+      for (int j = 0; j < nkv; ++j) {
+        const int s = j % nst;
+        const uint32_t ph = (uint32_t)(j / nst) & 1;
+        if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+        const int kr = b * p.T + j * TILE;
+        tc::mbar_arrive_expect_tx(full + s, TILE_BYTES);
+        tc::tma_load_2d(ring + s * TILE_BYTES, &tqkv, col, kr, full + s);
+        tc::tma_load_2d(ring + s * TILE_BYTES + HALF_BYTES, &tqkv, col + 64, kr, full + s);
+        last = j;
+      }
+      if (failed) {
+        *abort_flag = 1;
+        if (kside) tc::mbar_wait(q_full, 0, nullptr, kWaitNs);
+        // every copy this thread started lands before the CTA exits
+        for (int j = (last - nst + 1 > 0 ? last - nst + 1 : 0); j <= last; ++j)
+          tc::mbar_wait(full + j % nst, (uint32_t)(j / nst) & 1, nullptr, kWaitNs);
+      }
+    } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      if (lane == 0) {
-        const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);     // S = Q K^T, both K-major
-        const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);  // O += P V, V MN-major
-        bool any = false;
-        if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
-        // O_x += P_x(i) V_i, P_x read from the first 64 columns of S_x
-        auto issue_pv = [&](int x, int i) -> bool {
-          if (!tc::mbar_wait(p_full + x, i & 1, abort_flag, kWaitNs)) return false;
+      const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);     // S = Q K^T, both K-major
+      const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);  // O += P V, V MN-major
+      bool any = false;
+      if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
+      // O_x += P_x(i) V_i, P_x read from the first 64 columns of S_x
+      auto issue_pv = [&](int x, int i) -> bool {
+        if (!tc::mbar_wait(p_full + x, i & 1, abort_flag, kWaitNs)) return false;
+        tc::tc_fence_after();
+        const uint32_t tP = tmem + x * 128, tO = tmem + 256 + x * 128;
+        const uint32_t aV = tc::smem_u32(sV + (i % FWD_VST) * TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < TILE / 16; ++k)
+          tc::mma_bf16_tmem_a(tO, tP + k * 8, desc_mn(aV, k), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+        any = true;
+        return true;
+      };
+      // step j: PV_a(j-1), S_a(j), PV_b(j-1), S_b(j); the last step only
+      // finishes the PVs. A ring stage is released by a commit right after
+      // its last reader is issued.
+      for (int j = 0; j <= nkv && !failed; ++j) {
+        const bool has_s = j < nkv;
+        if (j > 0) {
+          const int i = j - 1;
+          if (!tc::mbar_wait(v_full + i % FWD_VST, (uint32_t)(i / FWD_VST) & 1, abort_flag, kWaitNs)) {
+            failed = true;
+            break;
+          }
+          if (i < nkv_a && !issue_pv(0, i)) { failed = true; break; }
+        }
+        if (has_s) {
+          if (!tc::mbar_wait(k_full + j % FWD_KST, (uint32_t)(j / FWD_KST) & 1, abort_flag, kWaitNs)) {
+            failed = true;
+            break;
+          }
           tc::tc_fence_after();
-          const uint32_t tP = tmem + x * 128, tO = tmem + 256 + x * 128;
-          const uint32_t aV = tc::smem_u32(sV + (i & 1) * TILE_BYTES);
-  #pragma unroll
-          for (int k = 0; k < TILE / 16; ++k)
-            tc::mma_bf16_tmem_a(tO, tP + k * 8, desc_mn(aV, k), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-          return true;
-        };
-        for (int j = 0; j < nkv && !failed; ++j) {
-          const int s = j & 1;
-          if (j > 0 && j - 1 < nkv_a && !issue_pv(0, j - 1)) { failed = true; break; }
-          if (!tc::mbar_wait(kv_full + s, (j >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          tc::tc_fence_after();
-          const uint32_t aK = tc::smem_u32(sK + s * TILE_BYTES);
           if (j < nkv_a) {
-            mma_tile(tmem, tc::smem_u32(sQ), false, aK, false, idesc, false);
+            mma_tile(tmem, tc::smem_u32(sQ), false, tc::smem_u32(sK + (j % FWD_KST) * TILE_BYTES), false, idesc,
+                     false);
             tc::mma_commit(s_full + 0);
             any = true;
           }
+        }
+        if (j > 0) {
+          if (has_b && !issue_pv(1, j - 1)) { failed = true; break; }
+          tc::mma_commit(v_empty + (j - 1) % FWD_VST);
+        }
+        if (has_s) {
           if (has_b) {
-            if (j > 0 && !issue_pv(1, j - 1)) { failed = true; break; }
-            mma_tile(tmem + 128, tc::smem_u32(sQ + TILE_BYTES), false, aK, false, idesc, false);
+            mma_tile(tmem + 128, tc::smem_u32(sQ + TILE_BYTES), false,
+                     tc::smem_u32(sK + (j % FWD_KST) * TILE_BYTES), false, idesc, false);
             tc::mma_commit(s_full + 1);
             any = true;
           }
-          if (j > 0) tc::mma_commit(kv_empty + (s ^ 1));  // every reader of K_{j-1} / V_{j-1} is issued
+          tc::mma_commit(k_empty + j % FWD_KST);
         }
-        // the last PV of each tile
-        if (!failed && !has_b && !issue_pv(0, nkv_a - 1)) failed = true;
-        if (!failed && has_b && !issue_pv(1, nkv - 1)) failed = true;
-        if (!failed) tc::mma_commit(o_full);
-        if (failed) {
-          *abort_flag = 1;
-          if (any) {
-            tc::mma_commit(drain);
-            tc::mbar_wait(drain, 0, nullptr, kWaitNs);
-          }
+      }
+      if (!failed) tc::mma_commit(o_full);
+      if (failed) {
+        *abort_flag = 1;
+        if (any) {
+          tc::mma_commit(drain);
+          tc::mbar_wait(drain, 0, nullptr, kWaitNs);
         }
       }
     }
@@ -766,7 +798,7 @@ bool map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int FWD_SMEM = 6 * TILE_BYTES + 256;  // Q pair, 2 K/V stages, barriers
+constexpr int FWD_SMEM = (2 + FWD_KST + FWD_VST) * TILE_BYTES + 256;  // Q pair, K and V rings, barriers
 constexpr int BWD_SMEM = 7 * TILE_BYTES + 2 * 2 * TILE * 4 + 256;
 
 }  // namespace
