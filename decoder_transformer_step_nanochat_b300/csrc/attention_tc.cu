@@ -551,13 +551,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         tc::mma_commit(st_full);
         if (!tc::mbar_wait(p_full, it & 1, abort_flag, kWaitNs)) { failed = true; break; }
         tc::tc_fence_after();
-        // dV += P^T dO with P^T in TMEM: k-step k reads query columns 16k..16k+15
+        // dV += P^T dO (P^T in TMEM: k-step k reads query columns 16k..16k+15),
+        // dK += dS^T Q and dQ = dS K, their k-steps interleaved: independent
+        // accumulators keep the tensor pipe full where one chain would wait on
+        // its own accumulation
 #pragma unroll
-        for (int k = 0; k < TILE / 16; ++k)
+        for (int k = 0; k < TILE / 16; ++k) {
           tc::mma_bf16_tmem_a(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn,
                               (it > 0 || k > 0) ? 1u : 0u);
-        mma_tile(tdK, adSt, false, aQ, true, id_kmn, it > 0);   // dK += dS^T Q
-        mma_tile(tdQ, adSt, true, aK, true, id_mnmn, false);    // dQ  = dS K
+          tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (it > 0 || k > 0) ? 1u : 0u);
+          tc::mma_bf16(tdQ, desc_mn(adSt, k), desc_mn(aK, k), id_mnmn, k > 0 ? 1u : 0u);
+        }
         tc::mma_commit(dq_full);
         tc::mma_commit(q_empty + s);
       }
