@@ -87,6 +87,7 @@ __device__ __forceinline__ void mma_tile(uint32_t d_tmem, uint32_t a, bool a_mn,
 
 struct AttnParams {
   int B, T, H, nq;
+  const bf16* qkv;  // backward: k_hat rows for the in-kernel QK-norm/RoPE backward of k
   bf16* o;        // forward output
   float* lse;     // forward output / backward input
   const float* Drow;
@@ -98,6 +99,7 @@ struct AttnParams {
   const float* rqk;
   const float* rope_cos;
   const float* rope_sin;
+  int* sched;     // backward: unit counter, zero at launch (dynamic scheduling)
   int* status;
 };
 
@@ -412,21 +414,42 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
 
 // ============================================================== backward
 //
-// One CTA per (b, h, 128-key tile); 10 warps: TMA producer, MMA issuer and
-// eight softmax/epilogue warps (two per TMEM lane quadrant, each owning 64 of
-// the 128 query columns). TMEM: [0,128) S^T, overwritten in place by P^T as
-// packed bf16 (query half c at columns 64c .. 64c+31), [128,256) dP^T and
-// then dQ, [256,384) dV, [384,512) dK. Shared memory: K, V, two Q/dO stages
-// (the next query tile loads while this one computes) and dS^T.
+// Persistent: one CTA per SM takes work units (b, h, 128-key tile) from a
+// global counter in (batch, head)-major order, heaviest key tile first within
+// a head, so the CTAs running together share a few heads' Q, dO and dq rows
+// in L2 and finish together. The producer thread draws each unit and hands
+// its index to the other roles through a shared-memory ring. 10 warps: TMA
+// producer, MMA issuer and eight softmax/epilogue warps (two per TMEM lane
+// quadrant, each owning 64 of the 128 query columns). TMEM: [0,128) S^T,
+// overwritten in place by P^T as packed bf16 (query half c at columns
+// 64c .. 64c+31), [128,256) dP^T and then dQ, [256,384) dV, [384,512) dK.
+// Shared memory: K, V, two Q/dO stages (the next query tile loads while this
+// one computes, across units too) and dS^T.
 // Per query tile: S^T = K Q^T and dP^T = V dO^T; P^T = exp(S^T - lse),
 // dS^T = P^T (dP^T - D); dV += P^T dO (A operand read from TMEM),
 // dK += dS^T Q, dQ = dS K; dQ is added to the fp32 plane by bulk tensor
 // reduce-adds staged in the dS^T tile, while the next tile's S^T is already
-// being computed.
+// being computed. Between units, the next K/V load as soon as the finished
+// unit's products are done and its first query tiles run while the epilogue
+// warps still drain dV/dK; only its first dV/dK products wait for that drain.
 
 constexpr int BWD_WARPS = 10;
 constexpr int BWD_THREADS = 32 * BWD_WARPS;
 constexpr int BWD_SOFT = 32 * (BWD_WARPS - 2);  // 256 softmax threads
+
+struct BwdUnit {
+  int b, h, kt, nit, krow0;
+};
+__device__ __forceinline__ BwdUnit bwd_unit(const AttnParams& p, int v) {
+  BwdUnit u;
+  const int bh = v / p.nq;
+  u.b = bh / p.H;
+  u.h = bh % p.H;
+  u.kt = v % p.nq;  // within a head the key tiles with the most query tiles come first
+  u.nit = p.nq - u.kt;
+  u.krow0 = u.b * p.T + u.kt * TILE;
+  return u;
+}
 
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
@@ -445,29 +468,30 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   float* sLD = reinterpret_cast<float*>(sdSt + TILE_BYTES);  // [stage][lse 128 | D 128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sLD + 2 * 2 * TILE);
   uint64_t* kv_full = bars + 0;
-  uint64_t* q_full = bars + 1;    // [2]
-  uint64_t* q_empty = bars + 3;   // [2]
-  uint64_t* st_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* dq_full = bars + 7;
-  uint64_t* tm_free = bars + 8;
-  uint64_t* acc_full = bars + 9;
-  uint64_t* drain = bars + 10;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* kv_empty = bars + 1;
+  uint64_t* q_full = bars + 2;    // [2]
+  uint64_t* q_empty = bars + 4;   // [2]
+  uint64_t* st_full = bars + 6;
+  uint64_t* p_full = bars + 7;
+  uint64_t* dq_full = bars + 8;
+  uint64_t* tm_free = bars + 9;
+  uint64_t* acc_full = bars + 10;
+  uint64_t* acc_free = bars + 11;
+  uint64_t* drain = bars + 12;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 13);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // unit index of this CTA's ul-th unit at slot ul % 4 (-1: no more units); it
+  // is written before the arrive that completes that unit's kv_full phase
+  // (and, for the end marker, a q_full phase), so a waiter on those sees it
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(tmem_holder + 2);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  // (batch, head)-major order: the CTAs running together share one head's
-  // Q, dO and dq rows in L2 (dq is accumulated with atomics); within a head
-  // the key tiles with the most query tiles (small kt) go first
-  const int bh = (int)(blockIdx.x / p.nq), b = bh / p.H, h = bh % p.H;
-  const int kt = (int)(blockIdx.x % p.nq);
   const int d = p.H * 128;
-  const int krow0 = b * p.T + kt * TILE;
-  const int nit = p.nq - kt;  // query tiles qt = kt .. nq-1
+  const int nunits = p.B * p.H * p.nq;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(kv_full, 1);
+    tc::mbar_init(kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(q_full + s, 1);
       tc::mbar_init(q_empty + s, 1);
@@ -477,6 +501,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tc::mbar_init(dq_full, 1);
     tc::mbar_init(tm_free, BWD_SOFT);
     tc::mbar_init(acc_full, 1);
+    tc::mbar_init(acc_free, BWD_SOFT);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
@@ -494,78 +519,117 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   bool failed = false;
 
   if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
       tc::prefetch_tmap(&tqkv);
       tc::prefetch_tmap(&tdo);
-      tc::mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
-      tc::tma_load_2d(sK, &tqkv, d + h * 128, krow0, kv_full);
-      tc::tma_load_2d(sK + HALF_BYTES, &tqkv, d + h * 128 + 64, krow0, kv_full);
-      tc::tma_load_2d(sV, &tqkv, 2 * d + h * 128, krow0, kv_full);
-      tc::tma_load_2d(sV + HALF_BYTES, &tqkv, 2 * d + h * 128 + 64, krow0, kv_full);
-      bool issued[2] = {false, false};
-      uint32_t iphase[2] = {0, 0};
-      for (int it = 0; it < nit; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        if (!tc::mbar_wait(q_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
-        const int qr = b * p.T + (kt + it) * TILE;
-        const size_t lrow = ((size_t)b * p.H + h) * p.T + (size_t)(kt + it) * TILE;
-        tc::mbar_arrive_expect_tx(q_full + s, 2 * TILE_BYTES + 2 * TILE * 4);
-        tc::bulk_load(sLD + s * 2 * TILE, p.lse + lrow, TILE * 4, q_full + s);
-        tc::bulk_load(sLD + s * 2 * TILE + TILE, p.Drow + lrow, TILE * 4, q_full + s);
-        tc::tma_load_2d(sQ + s * TILE_BYTES, &tqkv, h * 128, qr, q_full + s);
-        tc::tma_load_2d(sQ + s * TILE_BYTES + HALF_BYTES, &tqkv, h * 128 + 64, qr, q_full + s);
-        tc::tma_load_2d(sdO + s * TILE_BYTES, &tdo, h * 128, qr, q_full + s);
-        tc::tma_load_2d(sdO + s * TILE_BYTES + HALF_BYTES, &tdo, h * 128 + 64, qr, q_full + s);
-        issued[s] = true;
-        iphase[s] = ph;
+      int g = 0, ul = 0;                 // query tiles and units issued so far
+      int kv_last = -1;                  // unit whose K/V were issued last
+      for (;; ++ul) {
+        int v = atomicAdd(p.sched, 1);
+        if (v >= nunits) v = -1;
+        // K and V of the previous unit are free once its last products finished
+        // (and by then every role has read the older ring slots)
+        if (ul > 0 && !tc::mbar_wait(kv_empty, (ul - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        unit_ring[ul & 3] = v;
+        if (v < 0) {
+          // end marker: complete the phases the MMA thread (kv_full) and the
+          // softmax warps (q_full of the next tile) wait on next; that query
+          // stage's previous phase must be over first (its tile consumed)
+          tc::mbar_arrive(kv_full);
+          if (g >= 2 && !tc::mbar_wait(q_empty + (g & 1), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) {
+            failed = true;
+            break;
+          }
+          tc::mbar_arrive(q_full + (g & 1));
+          break;
+        }
+        const BwdUnit u = bwd_unit(p, v);
+        tc::mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
+        tc::tma_load_2d(sK, &tqkv, d + u.h * 128, u.krow0, kv_full);
+        tc::tma_load_2d(sK + HALF_BYTES, &tqkv, d + u.h * 128 + 64, u.krow0, kv_full);
+        tc::tma_load_2d(sV, &tqkv, 2 * d + u.h * 128, u.krow0, kv_full);
+        tc::tma_load_2d(sV + HALF_BYTES, &tqkv, 2 * d + u.h * 128 + 64, u.krow0, kv_full);
+        kv_last = ul;
+        for (int it = 0; it < u.nit; ++it, ++g) {
+          const int s = g & 1;
+          const uint32_t ph = (g >> 1) & 1;
+          if (!tc::mbar_wait(q_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+          const int qr = u.b * p.T + (u.kt + it) * TILE;
+          const size_t lrow = ((size_t)u.b * p.H + u.h) * p.T + (size_t)(u.kt + it) * TILE;
+          tc::mbar_arrive_expect_tx(q_full + s, 2 * TILE_BYTES + 2 * TILE * 4);
+          tc::bulk_load(sLD + s * 2 * TILE, p.lse + lrow, TILE * 4, q_full + s);
+          tc::bulk_load(sLD + s * 2 * TILE + TILE, p.Drow + lrow, TILE * 4, q_full + s);
+          tc::tma_load_2d(sQ + s * TILE_BYTES, &tqkv, u.h * 128, qr, q_full + s);
+          tc::tma_load_2d(sQ + s * TILE_BYTES + HALF_BYTES, &tqkv, u.h * 128 + 64, qr, q_full + s);
+          tc::tma_load_2d(sdO + s * TILE_BYTES, &tdo, u.h * 128, qr, q_full + s);
+          tc::tma_load_2d(sdO + s * TILE_BYTES + HALF_BYTES, &tdo, u.h * 128 + 64, qr, q_full + s);
+        }
+        if (failed) break;
       }
       if (failed) {
         *abort_flag = 1;
-        tc::mbar_wait(kv_full, 0, nullptr, kWaitNs);
-        for (int s = 0; s < 2; ++s)
-          if (issued[s]) tc::mbar_wait(q_full + s, iphase[s], nullptr, kWaitNs);
+        // every copy this thread started lands before the CTA exits: the last
+        // K/V (unit ul) and the last two query stages
+        if (kv_last >= 0) tc::mbar_wait(kv_full, kv_last & 1, nullptr, kWaitNs);
+        for (int gg = (g - 2 > 0 ? g - 2 : 0); gg < g; ++gg)
+          tc::mbar_wait(q_full + (gg & 1), (gg >> 1) & 1, nullptr, kWaitNs);
       }
     }
   } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_kk = tc::idesc_bf16(128, 128, 0, 0);   // both K-major
       const uint32_t id_kmn = tc::idesc_bf16(128, 128, 0, 1);  // B MN-major
       const uint32_t id_mnmn = tc::idesc_bf16(128, 128, 1, 1); // A and B MN-major
       const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), adSt = tc::smem_u32(sdSt);
       bool any = false;
-      if (!tc::mbar_wait(kv_full, 0, abort_flag, kWaitNs)) failed = true;
-      for (int it = 0; it < nit && !failed; ++it) {
-        const int s = it & 1;
-        const uint32_t aQ = tc::smem_u32(sQ + s * TILE_BYTES), adO = tc::smem_u32(sdO + s * TILE_BYTES);
-        if (!tc::mbar_wait(q_full + s, (it >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        // S^T overwrites P^T of the previous tile: wait until its products finished
-        if (it > 0 && !tc::mbar_wait(dq_full, (it - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        tc::tc_fence_after();
-        mma_tile(tS, aK, false, aQ, false, id_kk, false);       // S^T  = K Q^T
-        any = true;
-        // dP^T overwrites dQ of the previous tile: wait until it was read out
-        if (it > 0 && !tc::mbar_wait(tm_free, (it - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        tc::tc_fence_after();
-        mma_tile(tdP, aV, false, adO, false, id_kk, false);     // dP^T = V dO^T
-        tc::mma_commit(st_full);
-        if (!tc::mbar_wait(p_full, it & 1, abort_flag, kWaitNs)) { failed = true; break; }
-        tc::tc_fence_after();
-        // dV += P^T dO (P^T in TMEM: k-step k reads query columns 16k..16k+15),
-        // dK += dS^T Q and dQ = dS K, their k-steps interleaved: independent
-        // accumulators keep the tensor pipe full where one chain would wait on
-        // its own accumulation
+      int g = 0, ul = 0;
+      for (;; ++ul) {
+        if (!tc::mbar_wait(kv_full, ul & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        const int v = unit_ring[ul & 3];
+        if (v < 0) break;
+        const BwdUnit u = bwd_unit(p, v);
+        for (int it = 0; it < u.nit; ++it, ++g) {
+          const int s = g & 1;
+          const uint32_t aQ = tc::smem_u32(sQ + s * TILE_BYTES), adO = tc::smem_u32(sdO + s * TILE_BYTES);
+          if (!tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          // S^T overwrites P^T of the previous tile: wait until its products finished
+          if (g > 0 && !tc::mbar_wait(dq_full, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::tc_fence_after();
+          mma_tile(tS, aK, false, aQ, false, id_kk, false);       // S^T  = K Q^T
+          any = true;
+          // dP^T overwrites dQ of the previous tile: wait until it was read out
+          if (g > 0 && !tc::mbar_wait(tm_free, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::tc_fence_after();
+          mma_tile(tdP, aV, false, adO, false, id_kk, false);     // dP^T = V dO^T
+          tc::mma_commit(st_full);
+          if (!tc::mbar_wait(p_full, g & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          // the first dV/dK of a unit overwrite the accumulators of the previous
+          // one: wait until the epilogue warps have read them out
+          if (it == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, kWaitNs)) {
+            failed = true;
+            break;
+          }
+          tc::tc_fence_after();
+          // dV += P^T dO (P^T in TMEM: k-step k reads query columns 16k..16k+15),
+          // dK += dS^T Q and dQ = dS K, their k-steps interleaved: independent
+          // accumulators keep the tensor pipe full where one chain would wait on
+          // its own accumulation
 #pragma unroll
-        for (int k = 0; k < TILE / 16; ++k) {
-          tc::mma_bf16_tmem_a(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn,
-                              (it > 0 || k > 0) ? 1u : 0u);
-          tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (it > 0 || k > 0) ? 1u : 0u);
-          tc::mma_bf16(tdQ, desc_mn(adSt, k), desc_mn(aK, k), id_mnmn, k > 0 ? 1u : 0u);
+          for (int k = 0; k < TILE / 16; ++k) {
+            tc::mma_bf16_tmem_a(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn,
+                                (it > 0 || k > 0) ? 1u : 0u);
+            tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (it > 0 || k > 0) ? 1u : 0u);
+            tc::mma_bf16(tdQ, desc_mn(adSt, k), desc_mn(aK, k), id_mnmn, k > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(dq_full);
+          tc::mma_commit(q_empty + s);
         }
-        tc::mma_commit(dq_full);
-        tc::mma_commit(q_empty + s);
+        if (failed) break;
+        tc::mma_commit(acc_full);  // dV, dK of this unit complete
+        tc::mma_commit(kv_empty);  // and K, V no longer read
       }
-      if (!failed) tc::mma_commit(acc_full);
       if (failed) {
         *abort_flag = 1;
         if (any) {
@@ -585,102 +649,116 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // this warp's 4 KB block of the dS^T tile (its rows, its column half) is
     // also its staging buffer for the dQ bulk reduce-adds
     uint8_t* blk = sdSt + ch * HALF_BYTES + q4 * 32 * 128;
-    for (int it = 0; it < nit; ++it) {
-      const int qt = kt + it;
-      const int s = it & 1;
-      const float* Lq = sLD + s * 2 * TILE + ch * 64;        // lse of this warp's 64 query columns
-      const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
-      bool ok = tc::mbar_wait(st_full, it & 1, abort_flag, kWaitNs);
-      // the lse / D rows arrived with this tile's Q (already complete here)
-      ok = ok && tc::mbar_wait(q_full + s, (it >> 1) & 1, abort_flag, kWaitNs);
-      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-      tc::tc_fence_after();
-      // the previous tile's dQ reduce-adds must have read the block first
-      if (lane == 0) tc::bulk_wait_read();
-      __syncwarp();
-      const bool diag = (it == 0);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        float sv[32], dp[32];
-        tc::tmem_ld32x2(tS + lane_off + ch * 64 + c * 32, tdP + lane_off + ch * 64 + c * 32, sv, dp);
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const float4 l0 = *reinterpret_cast<const float4*>(Lq + c * 32 + g * 8);
-          const float4 l1 = *reinterpret_cast<const float4*>(Lq + c * 32 + g * 8 + 4);
-          const float4 d0 = *reinterpret_cast<const float4*>(Dq + c * 32 + g * 8);
-          const float4 d1 = *reinterpret_cast<const float4*>(Dq + c * 32 + g * 8 + 4);
-          const float Lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-          const float Dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int qc = ch * 64 + c * 32 + g * 8 + i;  // query column within the tile
-            float pr = tc::ex2(fmaf(sv[g * 8 + i], sl2, -Lv[i] * kLog2e));
-            if (diag && qc < r) pr = 0.f;
-            sv[g * 8 + i] = pr;
-            dp[g * 8 + i] = pr * (dp[g * 8 + i] - Dv[i]);
-          }
-          st_tile8(sdSt, r, ch * 8 + c * 4 + g, pack8(dp + 8 * g));
-        }
-        // P^T of these 32 query columns -> 16 packed bf16 pairs in TMEM
-        float pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * i], sv[2 * i + 1]);
-          pk[i] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
-        }
-        tc::tmem_st16(tS + lane_off + ch * 64 + c * 16, pk);
+    int g = 0, ul = 0;
+    for (;; ++ul) {
+      // the first query tile of the next unit (or the end marker) is announced
+      // on that tile's q_full phase
+      {
+        const bool ok = tc::mbar_wait(q_full + (g & 1), (g >> 1) & 1, abort_flag, kWaitNs);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       }
-      fence_async_smem();
-      tc::tc_fence_before();
-      tc::mbar_arrive(p_full);
-      ok = tc::mbar_wait(dq_full, it & 1, abort_flag, kWaitNs);
-      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-      tc::tc_fence_after();
-      // dQ rows q4*32.. (queries qt*128 + q4*32 + lane), this warp's 64
-      // columns as two 32 x 32 fp32 chunks, each staged in the (now free) dS^T
-      // block and added to the dq plane by a bulk tensor reduce-add
-      float vq[64];
-      tc::tmem_ld32x2(tdQ + lane_off + ch * 64, tdQ + lane_off + ch * 64 + 32, vq, vq + 32);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float* v = vq + c * 32;
-        if (c > 0) {
-          if (lane == 0) tc::bulk_wait_read();
-          __syncwarp();
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<float4*>(blk + lane * 128 + ((g ^ (lane & 7)) << 4)) =
-              make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
-        fence_async_smem();
+      const int v = unit_ring[ul & 3];
+      if (v < 0) break;
+      const BwdUnit u = bwd_unit(p, v);
+      for (int it = 0; it < u.nit; ++it, ++g) {
+        const int qt = u.kt + it;
+        const int s = g & 1;
+        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // lse of this warp's 64 query columns
+        const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
+        bool ok = tc::mbar_wait(st_full, g & 1, abort_flag, kWaitNs);
+        // the lse / D rows arrived with this tile's Q (already complete here)
+        ok = ok && tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+        tc::tc_fence_after();
+        // the previous tile's dQ reduce-adds must have read the block first
+        if (lane == 0) tc::bulk_wait_read();
         __syncwarp();
-        if (lane == 0) {
-          tc::tma_reduce_add_2d(&tdq, blk, h * 128 + ch * 64 + c * 32, b * p.T + qt * TILE + q4 * 32);
-          tc::bulk_commit();
+        const bool diag = (it == 0);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float sv[32], dp[32];
+          tc::tmem_ld32x2(tS + lane_off + ch * 64 + c * 32, tdP + lane_off + ch * 64 + c * 32, sv, dp);
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const float4 l0 = *reinterpret_cast<const float4*>(Lq + c * 32 + gq * 8);
+            const float4 l1 = *reinterpret_cast<const float4*>(Lq + c * 32 + gq * 8 + 4);
+            const float4 d0 = *reinterpret_cast<const float4*>(Dq + c * 32 + gq * 8);
+            const float4 d1 = *reinterpret_cast<const float4*>(Dq + c * 32 + gq * 8 + 4);
+            const float Lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+            const float Dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int qc = ch * 64 + c * 32 + gq * 8 + i;  // query column within the tile
+              float pr = tc::ex2(fmaf(sv[gq * 8 + i], sl2, -Lv[i] * kLog2e));
+              if (diag && qc < r) pr = 0.f;
+              sv[gq * 8 + i] = pr;
+              dp[gq * 8 + i] = pr * (dp[gq * 8 + i] - Dv[i]);
+            }
+            st_tile8(sdSt, r, ch * 8 + c * 4 + gq, pack8(dp + 8 * gq));
+          }
+          // P^T of these 32 query columns -> 16 packed bf16 pairs in TMEM
+          float pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(sv[2 * i], sv[2 * i + 1]);
+            pk[i] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
+          }
+          tc::tmem_st16(tS + lane_off + ch * 64 + c * 16, pk);
+        }
+        fence_async_smem();
+        tc::tc_fence_before();
+        tc::mbar_arrive(p_full);
+        ok = tc::mbar_wait(dq_full, g & 1, abort_flag, kWaitNs);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+        tc::tc_fence_after();
+        // dQ rows q4*32.. (queries qt*128 + q4*32 + lane), this warp's 64
+        // columns as two 32 x 32 fp32 chunks, each staged in the (now free) dS^T
+        // block and added to the dq plane by a bulk tensor reduce-add
+        float vq[64];
+        tc::tmem_ld32x2(tdQ + lane_off + ch * 64, tdQ + lane_off + ch * 64 + 32, vq, vq + 32);
+        // dQ is in registers: its TMEM columns may take the next dP^T at once,
+        // while the staging and reduce-adds below proceed off that path
+        tc::tc_fence_before();
+        tc::mbar_arrive(tm_free);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float* vv = vq + c * 32;
+          if (c > 0) {
+            if (lane == 0) tc::bulk_wait_read();
+            __syncwarp();
+          }
+#pragma unroll
+          for (int gq = 0; gq < 8; ++gq)
+            *reinterpret_cast<float4*>(blk + lane * 128 + ((gq ^ (lane & 7)) << 4)) =
+                make_float4(vv[gq * 4] * scale, vv[gq * 4 + 1] * scale, vv[gq * 4 + 2] * scale,
+                            vv[gq * 4 + 3] * scale);
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tc::tma_reduce_add_2d(&tdq, blk, u.h * 128 + ch * 64 + c * 32, u.b * p.T + qt * TILE + q4 * 32);
+            tc::bulk_commit();
+          }
         }
       }
-      tc::tc_fence_before();
-      tc::mbar_arrive(tm_free);
-    }
-    if (lane == 0) tc::bulk_wait_all();  // this warp's dQ reduce-adds have landed
-    __syncwarp();
-    if (!failed) {
-      bool ok = tc::mbar_wait(acc_full, 0, abort_flag, kWaitNs);
-      if (!__all_sync(0xffffffffu, ok)) failed = true;
-    }
-    if (!failed) {
+      if (failed) break;
+      // ---- this unit's dK / dV, read out while the next unit's first query
+      // tile already runs on the tensor cores
+      bool ok = tc::mbar_wait(acc_full, ul & 1, abort_flag, kWaitNs);
+      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
-      const size_t m = (size_t)krow0 + r;
+      const size_t m = (size_t)u.krow0 + r;
+      const int h = u.h;
       if (p.rqk) {
         // warp ch = 0 finishes dk for whole head rows; warp ch = 1 writes dv
         if (ch == 0) {
-          // dk_hat = scale * acc; dk_n = R^T dk_hat and k_n = R^T k_hat (k_hat from
-          // the K tile in shared memory); dk = rk * (dk_n - k_n * mean(dk_n * k_n)).
-          // Pass 1 rotates 32 pairs at a time back into the dK columns of TMEM and
-          // accumulates the dot; pass 2 finishes and stores.
-          const int t = kt * TILE + r;
+          // dk_hat = scale * acc; dk_n = R^T dk_hat and k_n = R^T k_hat (k_hat
+          // read back from qkv); dk = rk * (dk_n - k_n * mean(dk_n * k_n)).
+          // Pass 1 rotates 16 pairs at a time back into the dK columns of TMEM
+          // and accumulates the dot; pass 2 finishes and stores.
+          const int t = u.kt * TILE + r;
           const float* cs = p.rope_cos + (size_t)t * 64;
           const float* sn = p.rope_sin + (size_t)t * 64;
+          const bf16* krow = p.qkv + m * 3 * d + d + h * 128;
           const uint32_t tk = tdK + lane_off;
           float dot = 0.f;
 #pragma unroll
@@ -689,30 +767,37 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const float dmean = dot * (1.f / 128.f);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {  // 16 rotation pairs at a time
+              // operands from global memory first, so their latency overlaps the TMEM load
+              uint4 kr1[2], kr2[2];
+              float4 ca[2], cb[2], sa[2], sb[2];
+#pragma unroll
+              for (int c8 = 0; c8 < 2; ++c8) {
+                const int q8 = c * 2 + c8;
+                kr1[c8] = __ldg(reinterpret_cast<const uint4*>(krow) + q8);
+                kr2[c8] = __ldg(reinterpret_cast<const uint4*>(krow + 64) + q8);
+                ca[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8);
+                cb[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8 + 1);
+                sa[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8);
+                sb[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8 + 1);
+              }
               float g1[16], g2[16];
               tc::tmem_ld16x2(tk + c * 16, tk + 64 + c * 16, g1, g2);
 #pragma unroll
               for (int c8 = 0; c8 < 2; ++c8) {
-                const int q8 = c * 2 + c8;  // 8-column piece of the first half
-                const int sw = ((q8 ^ (r & 7)) << 4) + r * 128;
                 float k1[8], k2[8];
-                unpack8(*reinterpret_cast<const uint4*>(sK + sw), k1);
-                unpack8(*reinterpret_cast<const uint4*>(sK + HALF_BYTES + sw), k2);
-                const float4 ca = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8);
-                const float4 cb = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8 + 1);
-                const float4 sa = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8);
-                const float4 sb = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8 + 1);
-                const float cc[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
-                const float ss[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+                unpack8(kr1[c8], k1);
+                unpack8(kr2[c8], k2);
+                const float cc[8] = {ca[c8].x, ca[c8].y, ca[c8].z, ca[c8].w, cb[c8].x, cb[c8].y, cb[c8].z, cb[c8].w};
+                const float ss[8] = {sa[c8].x, sa[c8].y, sa[c8].z, sa[c8].w, sb[c8].x, sb[c8].y, sb[c8].z, sb[c8].w};
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                   const int e = c8 * 8 + i;
                   const float kn1 = k1[i] * cc[i] + k2[i] * ss[i];
                   const float kn2 = -k1[i] * ss[i] + k2[i] * cc[i];
                   if (pass == 0) {
-                    const float a = g1[e] * scale, b = g2[e] * scale;
-                    g1[e] = a * cc[i] + b * ss[i];
-                    g2[e] = -a * ss[i] + b * cc[i];
+                    const float a = g1[e] * scale, bb = g2[e] * scale;
+                    g1[e] = a * cc[i] + bb * ss[i];
+                    g2[e] = -a * ss[i] + bb * cc[i];
                     dot += g1[e] * kn1 + g2[e] * kn2;
                   } else {
                     g1[e] = rk * (g1[e] - kn1 * dmean);
@@ -726,9 +811,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               } else {
                 bf16* row = p.dqkv + m * 3 * d + d + h * 128;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                  *reinterpret_cast<uint4*>(row + c * 16 + g * 8) = pack8(g1 + 8 * g);
-                  *reinterpret_cast<uint4*>(row + 64 + c * 16 + g * 8) = pack8(g2 + 8 * g);
+                for (int gq = 0; gq < 2; ++gq) {
+                  *reinterpret_cast<uint4*>(row + c * 16 + gq * 8) = pack8(g1 + 8 * gq);
+                  *reinterpret_cast<uint4*>(row + 64 + c * 16 + gq * 8) = pack8(g2 + 8 * gq);
                 }
               }
             }
@@ -737,12 +822,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           bf16* row = p.dqkv + m * 3 * d + 2 * d + h * 128;
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            float a[32], b[32];
-            tc::tmem_ld32x2(tdV + lane_off + c * 64, tdV + lane_off + c * 64 + 32, a, b);
+            float a[32], bb[32];
+            tc::tmem_ld32x2(tdV + lane_off + c * 64, tdV + lane_off + c * 64 + 32, a, bb);
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              *reinterpret_cast<uint4*>(row + c * 64 + g * 8) = pack8(a + 8 * g);
-              *reinterpret_cast<uint4*>(row + c * 64 + 32 + g * 8) = pack8(b + 8 * g);
+            for (int gq = 0; gq < 4; ++gq) {
+              *reinterpret_cast<uint4*>(row + c * 64 + gq * 8) = pack8(a + 8 * gq);
+              *reinterpret_cast<uint4*>(row + c * 64 + 32 + gq * 8) = pack8(bb + 8 * gq);
             }
           }
         }
@@ -751,19 +836,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128 + ch * 64;
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          float v[32], w[32];
-          tc::tmem_ld32x2(tdK + lane_off + ch * 64 + c * 32, tdV + lane_off + ch * 64 + c * 32, v, w);
+          float vk[32], w[32];
+          tc::tmem_ld32x2(tdK + lane_off + ch * 64 + c * 32, tdV + lane_off + ch * 64 + c * 32, vk, w);
 #pragma unroll
-          for (int g = 0; g < 8; ++g)
-            *reinterpret_cast<float4*>(dkrow + c * 32 + g * 4) =
-                make_float4(v[g * 4] * scale, v[g * 4 + 1] * scale, v[g * 4 + 2] * scale, v[g * 4 + 3] * scale);
+          for (int gq = 0; gq < 8; ++gq)
+            *reinterpret_cast<float4*>(dkrow + c * 32 + gq * 4) =
+                make_float4(vk[gq * 4] * scale, vk[gq * 4 + 1] * scale, vk[gq * 4 + 2] * scale, vk[gq * 4 + 3] * scale);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(dvrow + c * 32 + g * 8) = pack8(w + 8 * g);
+          for (int gq = 0; gq < 4; ++gq) *reinterpret_cast<uint4*>(dvrow + c * 32 + gq * 8) = pack8(w + 8 * gq);
         }
       }
-    } else {
-      *abort_flag = 1;
+      // dV/dK may take the next unit's products
+      tc::tc_fence_before();
+      tc::mbar_arrive(acc_free);
     }
+    if (lane == 0) tc::bulk_wait_all();  // this warp's dQ reduce-adds have landed
+    __syncwarp();
+    if (failed) *abort_flag = 1;
   }
 
   if (failed) set_status(p.status, DEV_TIMEOUT);
@@ -846,13 +935,28 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   }
   AttnParams p{};
   p.B = B; p.T = T; p.H = H; p.nq = T / TILE;
+  p.qkv = qkv;
   p.lse = const_cast<float*>(lse); p.Drow = Drow; p.dq = dq; p.dk = dk; p.dqkv = dqkv; p.status = status;
   p.rqk = rqk; p.rope_cos = rope_cos; p.rope_sin = rope_sin;
+  int* sched = status + 1;
+  p.sched = sched;
   cudaError_t e = cudaMemsetAsync(dq, 0, (size_t)B * T * H * 128 * sizeof(float), s);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(attn_bwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, BWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_bwd_tc_k<<<B * H * p.nq, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, tdq, p);
+  // persistent: one CTA per SM (at most one per work unit), units drawn from
+  // a counter that starts at zero
+  e = cudaMemsetAsync(sched, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int units = B * H * p.nq;
+  attn_bwd_tc_k<<<units < sms ? units : sms, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, tdq, p);
   return cudaGetLastError();
 }
 

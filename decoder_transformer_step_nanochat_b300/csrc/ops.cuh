@@ -104,6 +104,8 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
 // dq (zeroed here, then accumulated) is fp32 [B*T, d]; dv goes to dqkv's v columns. Without rqk,
 // dk_hat goes to the fp32 plane dk; with rqk (+ the RoPE table) the k half of the QK-norm + RoPE
 // backward runs in the kernel and the final dk goes to dqkv's k columns.
+// status points at two device words: the status word and, after it, a counter
+// the kernel schedules its work units with (reset here before the launch).
 cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* Drow, float* dq,
                         float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s,
                         const float* rqk = nullptr, const float* rope_cos = nullptr,

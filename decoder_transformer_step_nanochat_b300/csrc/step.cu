@@ -626,7 +626,8 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
     return fail(NC_ERR_UNSUPPORTED, "this library is built for sm_103a (B300); device is sm_%d%d", prop.major, prop.minor);
   if (c->rope_cos) { cudaFree(c->rope_cos); c->rope_cos = nullptr; }
   if (c->rope_sin) { cudaFree(c->rope_sin); c->rope_sin = nullptr; }
-  if (!c->status) CK(cudaMalloc(&c->status, sizeof(int)));
+  // device words: [0] status, [1] work-unit counter of the persistent attention backward
+  if (!c->status) CK(cudaMalloc(&c->status, 16 * sizeof(int)));
   // RoPE table: angle pos * 10000^(-j/64) formed in float64, stored fp32.
   std::vector<float> hc((size_t)c->T * kHalf), hs((size_t)c->T * kHalf);
   for (int t = 0; t < c->T; ++t)
