@@ -10,4 +10,4 @@ from .model import (EPS, HEAD_DIM, IGNORE, ROPE_BASE, Shape, backward, causal_at
                     cross_entropy_rows, forward, layout, param_count, relu2,
                     relu2_backward, rmsnorm, rmsnorm_backward, rope,
                     rope_angles, rope_backward, step, unpack)
-from . import optim
+from . import infer, optim
