@@ -61,6 +61,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-optimizer", action="store_true",
                     help="skip timing the optimizer step (Muon + AdamW) after the fwd+bwd step")
+    ap.add_argument("--no-infer", action="store_true",
+                    help="skip timing generation (prefill + KV-cache decode steps)")
     return ap.parse_args()
 
 
@@ -347,6 +349,11 @@ def our_arm(args):
         }
         del state
 
+    # ---- generation: prefill of the batch's prompts, then greedy decode steps
+    inf = None
+    if not args.no_infer:
+        inf = infer_timing(nc, st, w, params, tok, stream, args, ws, pk)
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tps, _ = oracle_tokens_per_s(w, params_np, w.seq_len, 1, 0)
@@ -368,13 +375,75 @@ def our_arm(args):
             "model_flops_per_token": fpt,
             "loss": loss0,
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches_all,
-            "roofline": roofline, "families": families, "optimizer": opt, "cpu_baseline": cpu,
+            "roofline": roofline, "families": families, "optimizer": opt, "inference": inf,
+            "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)
     st.close()
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def infer_timing(nc, st, w, params, tok, stream, args, ws, pk):
+    """Prefill time and decode-step time through the generation ABI
+    (include/nc_infer.h), with the decode step's HBM roofline: the weights
+    the step streams plus the cached keys/values it reads."""
+    import torch
+
+    B, T, d, L = w.batch, w.seq_len, w.d_model, w.depth
+    steps = max(8, args.steps)
+    max_len = T + args.warmup + steps + 1
+    kv = torch.empty(nc.nc_kv_cache_bytes(st.ctx, max_len) + 256, dtype=torch.uint8, device="cuda")
+    kvp = (kv.data_ptr() + 255) // 256 * 256
+    nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+    cur = torch.empty(B, dtype=torch.int32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nc.nc_prefill(st.ctx, params.data_ptr(), tok.data_ptr(), kvp, max_len, nxt.data_ptr())  # warm-up
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        nc.nc_prefill(st.ctx, params.data_ptr(), tok.data_ptr(), kvp, max_len, nxt.data_ptr())
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_prefill = e0.elapsed_time(e1)
+    pos = T
+    for _ in range(args.warmup):
+        cur.copy_(nxt)
+        nc.nc_decode_step(st.ctx, params.data_ptr(), cur.data_ptr(), pos, kvp, max_len, nxt.data_ptr())
+        pos += 1
+    torch.cuda.synchronize()
+    nc.nc_profile_enable(st.ctx, True)
+    pos0 = pos
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps):
+            cur.copy_(nxt)
+            nc.nc_decode_step(st.ctx, params.data_ptr(), cur.data_ptr(), pos, kvp, max_len, nxt.data_ptr())
+            pos += 1
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_step = e0.elapsed_time(e1) / steps
+    fam = {k: nc.nc_profile_read(st.ctx, f) for k, f in (("gemm", nc.NC_FAM_DEC_GEMM), ("attn", nc.NC_FAM_DEC_ATTN),
+                                                         ("rows", nc.NC_FAM_DEC_ROWS))}
+    nc.nc_profile_enable(st.ctx, False)
+    esz = 2 if w.dtype == "bf16" else 4
+    weights = (12 * L * d * d + w.vocab * d) * esz       # every block matrix and lm_head, once
+    kv_read = 2 * L * B * d * esz * ((pos0 + pos - 1) / 2 + 1)  # mean cached length over the timed steps
+    step_bytes = weights + kv_read
+    gbs = step_bytes / (ms_step / 1000.0) / 1e9
+    ms_prefill_max, _ = reduce_over_ranks(ms_prefill, 0, "cuda")
+    ms_step_max, _ = reduce_over_ranks(ms_step, 0, "cuda")
+    del kv
+    return {
+        "prefill": {"ms": ms_prefill_max, "tokens_per_s": ws * B * T / (ms_prefill_max / 1000.0)},
+        "decode": {"ms_per_step": ms_step_max, "tokens_per_s": ws * B / (ms_step_max / 1000.0),
+                   "batch": B, "context": f"{pos0}..{pos - 1}", "launches_per_step": sum(v[1] for v in fam.values()) / steps,
+                   "families_ms_per_step": {k: v[0] / steps for k, v in fam.items()}},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                     "bytes_per_step": step_bytes,
+                     "note": "weights streamed once per step + cached keys/values read; per-step time includes launch gaps"},
+    }
 
 
 def read_traffic(family: str):

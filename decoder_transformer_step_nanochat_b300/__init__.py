@@ -6,7 +6,8 @@ and streams; this module takes raw device pointers (ints) and never computes
 anything itself. Importing it loads libnc.so and fails loudly if it is
 missing: there is no fallback implementation.
 
-Names follow include/nc.h, include/nc_ops.h and include/nc_optim.h.
+Names follow include/nc.h, include/nc_ops.h, include/nc_optim.h and
+include/nc_infer.h.
 """
 
 from __future__ import annotations
@@ -26,6 +27,9 @@ NC_FAM_ATTN_BWD = 2
 NC_FAM_ROWS = 3
 NC_FAM_OPT_NS = 4
 NC_FAM_OPT_ELEM = 5
+NC_FAM_DEC_GEMM = 6
+NC_FAM_DEC_ATTN = 7
+NC_FAM_DEC_ROWS = 8
 
 NC_EPI_STORE = 0
 NC_EPI_STORE_F32 = 1
@@ -89,6 +93,9 @@ _SIGS = {
     "nc_optim_set_hparams": (_I, [_P, _F, _F, _F, _F, _I]),
     "nc_optim_step": (_I, [_P, _P, _P, _P, _I, _F, _F, _F, _F, _P]),
     "nc_lr_at": (ctypes.c_double, [_LL, _LL, _LL, ctypes.c_double, ctypes.c_double]),
+    "nc_kv_cache_bytes": (_SZ, [_P, _I]),
+    "nc_prefill": (_I, [_P, _P, _P, _P, _I, _P, _P]),
+    "nc_decode_step": (_I, [_P, _P, _P, _I, _P, _I, _P, _P]),
 }
 
 
@@ -264,6 +271,18 @@ def nc_optim_step(ctx, params, grads, state, t, lr_adamw, lr_muon, weight_decay,
 
 def nc_lr_at(step, warmup, total, peak, final_frac=0.0) -> float:
     return float(lib().nc_lr_at(step, warmup, total, peak, final_frac))
+
+
+def nc_kv_cache_bytes(ctx, max_len) -> int:
+    return int(lib().nc_kv_cache_bytes(ctx, max_len))
+
+
+def nc_prefill(ctx, params, tokens, kv_cache, max_len, next_tokens, last_logits=None):
+    _check(lib().nc_prefill(ctx, params, tokens, kv_cache, max_len, next_tokens, last_logits), ctx)
+
+
+def nc_decode_step(ctx, params, tokens, pos, kv_cache, max_len, next_tokens, logits=None):
+    _check(lib().nc_decode_step(ctx, params, tokens, pos, kv_cache, max_len, next_tokens, logits), ctx)
 
 
 # ------------------------------------------------------------------ convenience

@@ -124,6 +124,26 @@ cudaError_t mean_loss(const float* nll, const int* tgt, int M, float* loss, floa
 // status DEV_BAD_TOKEN unless lo <= id < V for every id
 cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStream_t s);
 
+// ------------------------------------------------------------------ generation (KV cache)
+// cache layout per layer: K and V each [B][H][max_len][128] (elem)
+template <typename T>
+cudaError_t kv_from_qkv(const T* qkv, T* K, T* Vc, int B, int Tn, int H, int max_len, cudaStream_t s);
+// qkv fp32 [B, 3d] of the step's token -> q_hat elem [B, d]; k_hat, v into the cache at pos
+template <typename T>
+cudaError_t decode_qkv(const float* qkv, T* qh, T* K, T* Vc, const float* rc, const float* rs, int B, int H, int pos,
+                       int max_len, cudaStream_t s);
+// o elem [B, d] = attention of q_hat over cached positions 0..pos; part holds
+// B*H*ceil((pos+1)/chunk) partials of 132 floats
+constexpr int kDecodeChunk = 256;
+constexpr int kDecodePartFloats = 132;
+template <typename T>
+cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos, int max_len,
+                        int chunk, cudaStream_t s);
+template <typename T>
+cudaError_t relu2_rows(const float* u, T* a, long long n, cudaStream_t s);
+template <typename T>
+cudaError_t gather_last(const T* hf, T* out, int B, int Tn, int d, cudaStream_t s);
+
 // ------------------------------------------------------------------ optimizer
 // Chunk of the Muon passes (every block matrix holds a whole number of them:
 // d^2 is a multiple of 16384 when d is a multiple of 128) and the fixed block

@@ -18,6 +18,7 @@
 #include "../../include/nc.h"
 #include "../../include/nc_ops.h"
 #include "../../include/nc_optim.h"
+#include "../../include/nc_infer.h"
 #include "ops.cuh"
 
 using namespace nc;
@@ -92,6 +93,10 @@ struct nc_ctx {
   struct OptOff {
     size_t stats, part_norm, part_muon, inv_norm, x_all, pong, gram, poly;
   } opt{};
+  // decode scratch (one token per sequence), after the step's layout
+  struct DecOff {
+    size_t x, r, xn, qkv, qh, o, u, a, hf, lse, nll, tgt;
+  } dec{};
   // optimizer hyper-parameters fixed per context (nc_optim_set_hparams)
   float opt_b1 = 0.9f, opt_b2 = 0.999f, opt_eps = 1e-8f, opt_mu = 0.95f;
   int opt_ns = 5;
@@ -217,6 +222,23 @@ void plan_workspace(nc_ctx* c) {
   if (c->partial_bytes < (size_t(64) << 20)) c->partial_bytes = size_t(64) << 20;
   f.partial = take(c->partial_bytes);
   f.inv_count = take(4);  // 1 / number of unmasked targets of the last forward
+  // decode scratch: B rows of the step's activations
+  {
+    const size_t Bn = c->B;
+    auto& q = c->dec;
+    q.x = take(Bn * d * 4);
+    q.r = take(Bn * 4);
+    q.xn = take(Bn * d * e);
+    q.qkv = take(Bn * 3 * d * 4);
+    q.qh = take(Bn * d * e);
+    q.o = take(Bn * d * e);
+    q.u = take(Bn * F * 4);
+    q.a = take(Bn * F * e);
+    q.hf = take(Bn * d * e);
+    q.lse = take(Bn * 4);
+    q.nll = take(Bn * 4);
+    q.tgt = take(Bn * 4);
+  }
   c->ws_need = o;
   // optimizer scratch, from offset 0
   o = 0;
@@ -280,7 +302,10 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
   }
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm M=%d N=%d K=%d epi=%d: %s", g.M, g.N, g.K, g.epi, cudaGetErrorString(e));
   int n = (g.M > 0 && g.N > 0) ? (g.splits > 1 ? 2 : 1) : 0;  // split-K adds its reduction kernel
-  return prof_end(c, ev_a, c->gemm_fam, 2.0 * g.M * g.N * (double)g.K * g.batch, n);
+  // decode GEMMs stream their weights: their work is counted in bytes
+  const double work = c->gemm_fam == NC_FAM_DEC_GEMM ? (double)g.N * g.K * c->esz
+                                                     : 2.0 * g.M * g.N * (double)g.K * g.batch;
+  return prof_end(c, ev_a, c->gemm_fam, work, n);
 }
 
 GemmArgs mk(int M, int N, int K, const void* A, long long lda, int ak, const void* B, long long ldb,
@@ -372,11 +397,10 @@ nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tg
 }
 
 template <typename T>
-nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* d_loss) {
+nc_status forward_blocks(nc_ctx* c, const T* P, const int* tok) {
   int M = c->M, d = c->d, H = c->H, F = c->F, V = c->V, Tn = c->T;
   cudaStream_t s = c->stream;
   KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tok, M, 0, V, c->status, s));
-  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tgt, M, -1, V, c->status, s));  // -1: masked target
   float* x = wsp<float>(c, c->off.x);
   int rows, cols;
   KL(NC_FAM_ROWS, (double)M * d * (sizeof(T) + 4) + 4.0 * M, 1, embed_fwd<T>(tok, P, x, M, d, V, c->status, s));
@@ -419,6 +443,17 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
   T* hf = wsp<T>(c, c->off.hf);
   float* rf = wsp<float>(c, c->off.rf);
   KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, hf, rf, M, d, s));
+  return NC_OK;
+}
+
+template <typename T>
+nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* d_loss) {
+  const int M = c->M, V = c->V;
+  cudaStream_t s = c->stream;
+  KL(NC_FAM_ROWS, 4.0 * M, 1, check_ids(tgt, M, -1, V, c->status, s));  // -1: masked target
+  CKS(forward_blocks<T>(c, P, tok));
+  T* hf = wsp<T>(c, c->off.hf);
+  int rows, cols;
   const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
   CKS(lmhead_ce_forward<T>(c, hf, Wlm, tgt, M, wsp<float>(c, c->off.lse), wsp<float>(c, c->off.nll),
                            wsp<int>(c, c->off.amax)));
@@ -586,6 +621,133 @@ nc_status optim_step(nc_ctx* c, T* param, const float* grads, float* state, int 
                      lr_m * scale, c->stream));
   }
   return NC_OK;
+}
+
+
+// ------------------------------------------------------------------ generation
+
+// KV cache buffer: per layer K then V, each [B][H][max_len][128] elem; then the
+// RoPE table for max_len positions (cos, sin fp32 [max_len, 64]); then the
+// attention partials of one decode step.
+struct KvLayout {
+  size_t per, rc, rs, part, total;
+};
+KvLayout kv_layout(const nc_ctx* c, int max_len) {
+  KvLayout k;
+  const size_t Bn = c->B, H = c->H, L = c->L, ml = max_len;
+  k.per = align_up(Bn * H * ml * 128 * c->esz);
+  size_t o = 2 * L * k.per;
+  k.rc = o;
+  o += align_up(ml * 64 * 4);
+  k.rs = o;
+  o += align_up(ml * 64 * 4);
+  k.part = o;
+  const size_t nch = (ml + kDecodeChunk - 1) / kDecodeChunk;
+  o += align_up(Bn * H * nch * kDecodePartFloats * 4);
+  k.total = o;
+  return k;
+}
+
+// Greedy head over B rows of final hidden state: argmax (lowest index on
+// ties) into next; fp32 logits too when requested.
+template <typename T>
+nc_status decode_head(nc_ctx* c, const T* P, const T* hf, int32_t* next, float* logits) {
+  const int Bn = c->B, d = c->d, V = c->V;
+  int rows, cols;
+  const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
+  int* tgt = wsp<int>(c, c->dec.tgt);  // -1: no target, only lse and argmax
+  CK(cudaMemsetAsync(tgt, 0xff, (size_t)Bn * sizeof(int), c->stream));
+  c->gemm_fam = NC_FAM_DEC_GEMM;
+  nc_status st = lmhead_ce_forward<T>(c, hf, Wlm, tgt, Bn, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next);
+  if (st == NC_OK && logits) st = gemm(c, mk(Bn, V, d, hf, d, 1, Wlm, d, 1, EPI_STORE_F32, logits, V));
+  c->gemm_fam = NC_FAM_GEMM;
+  return st;
+}
+
+void rope_table(int n, std::vector<float>& hc, std::vector<float>& hs) {
+  hc.resize((size_t)n * kHalf);
+  hs.resize((size_t)n * kHalf);
+  for (int t = 0; t < n; ++t)
+    for (int j = 0; j < kHalf; ++j) {
+      const double ang = (double)t * pow(10000.0, -(double)j / (double)kHalf);
+      hc[(size_t)t * kHalf + j] = (float)cos(ang);
+      hs[(size_t)t * kHalf + j] = (float)sin(ang);
+    }
+}
+
+template <typename T>
+nc_status prefill_impl(nc_ctx* c, const T* P, const int* tok, char* kv, int max_len, int32_t* next, float* logits) {
+  const KvLayout kl = kv_layout(c, max_len);
+  std::vector<float> hc, hs;
+  rope_table(max_len, hc, hs);
+  CK(cudaMemcpyAsync(kv + kl.rc, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(kv + kl.rs, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice, c->stream));
+  CK(cudaStreamSynchronize(c->stream));  // the host tables go out of scope
+  CKS(forward_blocks<T>(c, P, tok));
+  for (int l = 0; l < c->L; ++l) {
+    const T* qkv = wsp<T>(c, (size_t)l * c->off.layer_stride + c->off.qkv);
+    T* K = reinterpret_cast<T*>(kv + (size_t)2 * l * kl.per);
+    T* Vc = reinterpret_cast<T*>(kv + (size_t)(2 * l + 1) * kl.per);
+    KL(NC_FAM_DEC_ROWS, 4.0 * c->M * c->d * c->esz, 1, kv_from_qkv<T>(qkv, K, Vc, c->B, c->T, c->H, max_len, c->stream));
+  }
+  T* hl = wsp<T>(c, c->dec.hf);
+  KL(NC_FAM_DEC_ROWS, 2.0 * c->B * c->d * c->esz, 1, gather_last<T>(wsp<T>(c, c->off.hf), hl, c->B, c->T, c->d, c->stream));
+  return decode_head<T>(c, P, hl, next, logits);
+}
+
+template <typename T>
+nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, char* kv, int max_len, int32_t* next,
+                      float* logits) {
+  const KvLayout kl = kv_layout(c, max_len);
+  const int Bn = c->B, d = c->d, H = c->H, F = c->F, V = c->V;
+  cudaStream_t s = c->stream;
+  const double e = c->esz;
+  float* x = wsp<float>(c, c->dec.x);
+  float* r = wsp<float>(c, c->dec.r);
+  T* xn = wsp<T>(c, c->dec.xn);
+  float* qkv = wsp<float>(c, c->dec.qkv);
+  T* qh = wsp<T>(c, c->dec.qh);
+  T* o = wsp<T>(c, c->dec.o);
+  float* u = wsp<float>(c, c->dec.u);
+  T* a = wsp<T>(c, c->dec.a);
+  T* hf = wsp<T>(c, c->dec.hf);
+  const float* rc = reinterpret_cast<const float*>(kv + kl.rc);
+  const float* rs = reinterpret_cast<const float*>(kv + kl.rs);
+  float* part = reinterpret_cast<float*>(kv + kl.part);
+  KL(NC_FAM_DEC_ROWS, (double)Bn * d * (e + 4) + 4.0 * Bn, 1, embed_fwd<T>(tok, P, x, Bn, d, V, c->status, s));
+  int rows, cols;
+  for (int l = 0; l < c->L; ++l) {
+    const T* Wqkv = P + param_offset(c, 1 + 4 * l, &rows, &cols);
+    const T* Wo = P + param_offset(c, 2 + 4 * l, &rows, &cols);
+    const T* Wfc = P + param_offset(c, 3 + 4 * l, &rows, &cols);
+    const T* Wproj = P + param_offset(c, 4 + 4 * l, &rows, &cols);
+    T* K = reinterpret_cast<T*>(kv + (size_t)2 * l * kl.per);
+    T* Vc = reinterpret_cast<T*>(kv + (size_t)(2 * l + 1) * kl.per);
+    KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
+    c->gemm_fam = NC_FAM_DEC_GEMM;
+    nc_status st = gemm(c, mk(Bn, 3 * d, d, xn, d, 1, Wqkv, d, 1, EPI_STORE_F32, qkv, 3 * d));
+    c->gemm_fam = NC_FAM_GEMM;
+    CKS(st);
+    KL(NC_FAM_DEC_ROWS, (double)Bn * 3 * d * (4 + e), 1, decode_qkv<T>(qkv, qh, K, Vc, rc, rs, Bn, H, pos, max_len, s));
+    KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * (pos + 1) * e, 2,
+       attn_decode<T>(qh, K, Vc, part, o, Bn, H, pos, max_len, kDecodeChunk, s));
+    c->gemm_fam = NC_FAM_DEC_GEMM;
+    st = gemm(c, mk(Bn, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f));
+    c->gemm_fam = NC_FAM_GEMM;
+    CKS(st);
+    KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
+    c->gemm_fam = NC_FAM_DEC_GEMM;
+    st = gemm(c, mk(Bn, F, d, xn, d, 1, Wfc, d, 1, EPI_STORE_F32, u, F));
+    c->gemm_fam = NC_FAM_GEMM;
+    CKS(st);
+    KL(NC_FAM_DEC_ROWS, (double)Bn * F * (4 + e), 1, relu2_rows<T>(u, a, (long long)Bn * F, s));
+    c->gemm_fam = NC_FAM_DEC_GEMM;
+    st = gemm(c, mk(Bn, d, F, a, F, 1, Wproj, F, 1, EPI_STORE_F32, x, d, 1.f, 1.f));
+    c->gemm_fam = NC_FAM_GEMM;
+    CKS(st);
+  }
+  KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, hf, r, Bn, d, s));
+  return decode_head<T>(c, P, hf, next, logits);
 }
 
 }  // namespace
@@ -951,6 +1113,48 @@ nc_status nc_op_gemm_batched(nc_ctx* c, int batch, int M, int N, int K, const vo
   g.C2 = C2; g.ldc2 = ldc2;
   g.batch = batch; g.a_brows = a_brows; g.b_brows = b_brows; g.c_brows = c_brows;
   return gemm(c, g);
+}
+
+// ------------------------------------------------------------------ generation
+
+size_t nc_kv_cache_bytes(const nc_ctx* c, int max_len) {
+  if (!c || c->prec < 0 || max_len < 1) return 0;
+  return kv_layout(c, max_len).total;
+}
+
+static nc_status check_kv(nc_ctx* c, const void* kv, int max_len) {
+  if (!kv) return fail(NC_ERR_ARG, "null KV cache");
+  if (reinterpret_cast<uintptr_t>(kv) % 256) return fail(NC_ERR_ARG, "the KV cache must be 256-byte aligned");
+  if (max_len < c->T || max_len > (1 << 16))
+    return fail(NC_ERR_ARG, "max_len %d outside [seq_len = %d, 65536]", max_len, c->T);
+  return NC_OK;
+}
+
+nc_status nc_prefill(nc_ctx* c, const void* params, const int32_t* tokens, void* kv_cache, int max_len,
+                     int32_t* next_tokens, float* last_logits) {
+  CKS(check_ready(c));
+  if (!params || !tokens || !next_tokens) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_kv(c, kv_cache, max_len));
+  c->have_fwd = false;
+  char* kv = static_cast<char*>(kv_cache);
+  return c->prec == NC_BF16
+             ? prefill_impl<bf16>(c, static_cast<const bf16*>(params), tokens, kv, max_len, next_tokens, last_logits)
+             : prefill_impl<float>(c, static_cast<const float*>(params), tokens, kv, max_len, next_tokens,
+                                   last_logits);
+}
+
+nc_status nc_decode_step(nc_ctx* c, const void* params, const int32_t* tokens, int pos, void* kv_cache, int max_len,
+                         int32_t* next_tokens, float* logits) {
+  CKS(check_ready(c));
+  if (!params || !tokens || !next_tokens) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_kv(c, kv_cache, max_len));
+  if (pos < 0 || pos >= max_len) return fail(NC_ERR_ARG, "position %d outside [0, max_len = %d)", pos, max_len);
+  c->have_fwd = false;
+  char* kv = static_cast<char*>(kv_cache);
+  return c->prec == NC_BF16
+             ? decode_impl<bf16>(c, static_cast<const bf16*>(params), tokens, pos, kv, max_len, next_tokens, logits)
+             : decode_impl<float>(c, static_cast<const float*>(params), tokens, pos, kv, max_len, next_tokens,
+                                  logits);
 }
 
 }  // extern "C"

@@ -151,7 +151,10 @@ enum {
   NC_FAM_ROWS = 3,      /* norms, embedding, QK-norm/RoPE, CE reductions; work = bytes */
   NC_FAM_OPT_NS = 4,    /* optimizer: Newton-Schulz GEMMs of Muon; work = FLOPs */
   NC_FAM_OPT_ELEM = 5,  /* optimizer: norm, AdamW and Muon element passes; work = bytes */
-  NC_FAM_COUNT = 6
+  NC_FAM_DEC_GEMM = 6,  /* generation: weight-streaming products; work = weight bytes */
+  NC_FAM_DEC_ATTN = 7,  /* generation: attention over the KV cache; work = cache bytes read */
+  NC_FAM_DEC_ROWS = 8,  /* generation: norms, embedding, QK-norm/RoPE, head reductions; bytes */
+  NC_FAM_COUNT = 9
 };
 
 /* Number of kernels the context has launched since nc_create. */

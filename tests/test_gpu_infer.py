@@ -1,0 +1,105 @@
+"""Generation with a KV cache (include/nc_infer.h) against the oracle
+(oracle/infer.py): prefill of the workload's prompts, then decode steps that
+feed back the GPU's own greedy tokens; the oracle runs the same token
+sequence. fp32 debug mode within 1e-4 relative on the logits with identical
+greedy tokens; bf16 within the step's bar (logits relative L2 <= 3e-2, lse
+within 5e-2 nats) with identical tokens wherever the oracle's top-1/top-2
+margin exceeds four times the largest logit difference seen."""
+
+import numpy as np
+import pytest
+
+import oracle
+import workload as W
+from gpu_util import load_nc, rel_l2, shape_of
+from oracle import infer
+
+pytestmark = pytest.mark.gpu
+
+
+def _lse(x):
+    m = x.max(-1, keepdims=True)
+    return (m + np.log(np.exp(x - m).sum(-1, keepdims=True)))[:, 0]
+
+
+def _generate_gpu(nc, w, params, prompt, steps, max_len, precision):
+    import torch
+    B, T = prompt.shape
+    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, B, precision)
+    try:
+        dt = torch.bfloat16 if precision == nc.NC_BF16 else torch.float32
+        dp = torch.from_numpy(params).to(dt).cuda()
+        kv = torch.empty(nc.nc_kv_cache_bytes(st.ctx, max_len) + 256, dtype=torch.uint8, device="cuda")
+        kvp = (kv.data_ptr() + 255) // 256 * 256
+        tok = torch.from_numpy(np.ascontiguousarray(prompt, dtype=np.int32)).cuda()
+        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+        logits = torch.empty((B, w.vocab), dtype=torch.float32, device="cuda")
+        nc.nc_prefill(st.ctx, dp.data_ptr(), tok.data_ptr(), kvp, max_len, nxt.data_ptr(), logits.data_ptr())
+        ids, lg = [nxt.cpu().numpy().copy()], [logits.cpu().numpy().copy()]
+        for i in range(steps):
+            cur = nxt.clone()
+            nc.nc_decode_step(st.ctx, dp.data_ptr(), cur.data_ptr(), T + i, kvp, max_len, nxt.data_ptr(),
+                              logits.data_ptr())
+            ids.append(nxt.cpu().numpy().copy())
+            lg.append(logits.cpu().numpy().copy())
+        nc.nc_sync(st.ctx)
+        return np.stack(ids, 1), lg
+    finally:
+        st.close()
+
+
+def _oracle_follow(w, params, prompt, ids, dtype):
+    """Oracle logits along the GPU's token sequence."""
+    s = shape_of(w)
+    cache, logits = infer.prefill(params.astype(dtype), prompt, s, dtype)
+    out = [logits]
+    for i in range(ids.shape[1] - 1):
+        cache, logits = infer.decode_step(params.astype(dtype), cache, ids[:, i], s, dtype)
+        out.append(logits)
+    return out
+
+
+def test_tiny_fp32_generation_matches_oracle():
+    nc = load_nc()
+    w = W.WORKLOADS["tiny"]
+    p = W.make_params(w)
+    tok, _ = W.make_tokens(w)
+    ids, lg = _generate_gpu(nc, w, p, tok, 4, w.seq_len + 8, nc.NC_FP32_DEBUG)
+    ref = _oracle_follow(w, p, tok, ids, np.float64)
+    for i, (g, r) in enumerate(zip(lg, ref)):
+        assert rel_l2(g, r) <= 1e-4, (i, rel_l2(g, r))
+        np.testing.assert_array_equal(ids[:, i], np.argmax(r, -1))
+
+
+def test_small_bf16_generation_matches_oracle():
+    nc = load_nc()
+    w = W.WORKLOADS["small"]
+    p = W.make_params(w)
+    tok, _ = W.make_tokens(w)
+    ids, lg = _generate_gpu(nc, w, p, tok, 4, w.seq_len + 64, nc.NC_BF16)
+    ref = _oracle_follow(w, p, tok, ids, np.float32)
+    for i, (g, r) in enumerate(zip(lg, ref)):
+        r = r.astype(np.float64)
+        assert rel_l2(g, r) <= 3e-2, (i, rel_l2(g, r))
+        assert np.abs(_lse(g.astype(np.float64)) - _lse(r)).max() <= 5e-2
+        top2 = np.sort(r, -1)[:, -2:]
+        sure = (top2[:, 1] - top2[:, 0]) > 4 * np.abs(g - r).max()
+        np.testing.assert_array_equal(ids[sure, i], np.argmax(r, -1)[sure])
+
+
+def test_generation_rejects_bad_arguments():
+    import torch
+    nc = load_nc()
+    w = W.WORKLOADS["tiny"]
+    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, w.batch, nc.NC_FP32_DEBUG)
+    try:
+        buf = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+        base = (buf.data_ptr() + 255) // 256 * 256
+        ml = w.seq_len + 4
+        for pos, kv, max_len in ((ml, base, ml), (0, base + 16, ml), (0, base, w.seq_len - 1)):
+            with pytest.raises(nc.NcError) as ei:
+                nc.nc_decode_step(st.ctx, base, base, pos, kv, max_len, base)
+            assert ei.value.status == 1
+        assert nc.nc_kv_cache_bytes(st.ctx, 0) == 0
+    finally:
+        st.close()
