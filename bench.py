@@ -393,7 +393,7 @@ def infer_timing(nc, st, w, params, tok, stream, args, ws, pk):
 
     B, T, d, L = w.batch, w.seq_len, w.d_model, w.depth
     steps = max(8, args.steps)
-    max_len = T + args.warmup + steps + 1
+    max_len = T + args.warmup + 2 * steps + 4
     kv = torch.empty(nc.nc_kv_cache_bytes(st.ctx, max_len) + 256, dtype=torch.uint8, device="cuda")
     kvp = (kv.data_ptr() + 255) // 256 * 256
     nxt = torch.empty(B, dtype=torch.int32, device="cuda")
@@ -427,22 +427,47 @@ def infer_timing(nc, st, w, params, tok, stream, args, ws, pk):
     fam = {k: nc.nc_profile_read(st.ctx, f) for k, f in (("gemm", nc.NC_FAM_DEC_GEMM), ("attn", nc.NC_FAM_DEC_ATTN),
                                                          ("rows", nc.NC_FAM_DEC_ROWS))}
     nc.nc_profile_enable(st.ctx, False)
+    # the same steps replayed from one captured CUDA graph (device position)
+    d_pos = torch.full((1,), pos, dtype=torch.int32, device="cuda")
+    with torch.cuda.stream(stream):
+        cur.copy_(nxt)
+        nc.nc_decode_step_dev(st.ctx, params.data_ptr(), cur.data_ptr(), d_pos.data_ptr(), kvp, max_len,
+                              nxt.data_ptr())
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        cur.copy_(nxt)
+        nc.nc_decode_step_dev(st.ctx, params.data_ptr(), cur.data_ptr(), d_pos.data_ptr(), kvp, max_len,
+                              nxt.data_ptr())
+    gsteps = min(steps, max_len - pos - 2)
+    graph.replay()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(gsteps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    ms_graph = e0.elapsed_time(e1) / max(1, gsteps)
+    nc.nc_sync(st.ctx)
     esz = 2 if w.dtype == "bf16" else 4
     weights = (12 * L * d * d + w.vocab * d) * esz       # every block matrix and lm_head, once
     kv_read = 2 * L * B * d * esz * ((pos0 + pos - 1) / 2 + 1)  # mean cached length over the timed steps
     step_bytes = weights + kv_read
-    gbs = step_bytes / (ms_step / 1000.0) / 1e9
     ms_prefill_max, _ = reduce_over_ranks(ms_prefill, 0, "cuda")
     ms_step_max, _ = reduce_over_ranks(ms_step, 0, "cuda")
-    del kv
+    ms_graph_max, _ = reduce_over_ranks(ms_graph, 0, "cuda")
+    gbs = step_bytes / (ms_graph_max / 1000.0) / 1e9
+    del kv, graph
     return {
         "prefill": {"ms": ms_prefill_max, "tokens_per_s": ws * B * T / (ms_prefill_max / 1000.0)},
         "decode": {"ms_per_step": ms_step_max, "tokens_per_s": ws * B / (ms_step_max / 1000.0),
+                   "graph_ms_per_step": ms_graph_max, "graph_tokens_per_s": ws * B / (ms_graph_max / 1000.0),
                    "batch": B, "context": f"{pos0}..{pos - 1}", "launches_per_step": sum(v[1] for v in fam.values()) / steps,
                    "families_ms_per_step": {k: v[0] / steps for k, v in fam.items()}},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
                      "bytes_per_step": step_bytes,
-                     "note": "weights streamed once per step + cached keys/values read; per-step time includes launch gaps"},
+                     "note": "graph-replayed decode step: weights streamed once + cached keys/values read"},
     }
 
 

@@ -96,6 +96,7 @@ _SIGS = {
     "nc_kv_cache_bytes": (_SZ, [_P, _I]),
     "nc_prefill": (_I, [_P, _P, _P, _P, _I, _P, _P]),
     "nc_decode_step": (_I, [_P, _P, _P, _I, _P, _I, _P, _P]),
+    "nc_decode_step_dev": (_I, [_P, _P, _P, _P, _P, _I, _P, _P]),
 }
 
 
@@ -283,6 +284,10 @@ def nc_prefill(ctx, params, tokens, kv_cache, max_len, next_tokens, last_logits=
 
 def nc_decode_step(ctx, params, tokens, pos, kv_cache, max_len, next_tokens, logits=None):
     _check(lib().nc_decode_step(ctx, params, tokens, pos, kv_cache, max_len, next_tokens, logits), ctx)
+
+
+def nc_decode_step_dev(ctx, params, tokens, d_pos, kv_cache, max_len, next_tokens, logits=None):
+    _check(lib().nc_decode_step_dev(ctx, params, tokens, d_pos, kv_cache, max_len, next_tokens, logits), ctx)
 
 
 # ------------------------------------------------------------------ convenience

@@ -67,8 +67,13 @@ __global__ void kv_from_qkv_k(const T* __restrict__ qkv, T* __restrict__ K, T* _
 // partner of dim j < 64 is j + 64, held by lane L ^ 16.
 template <typename T>
 __global__ void decode_qkv_k(const float* __restrict__ qkv, T* __restrict__ qh, T* __restrict__ K, T* __restrict__ Vc,
-                             const float* __restrict__ rc, const float* __restrict__ rs, int B, int H, int pos,
-                             int max_len) {
+                             const float* __restrict__ rc, const float* __restrict__ rs, int B, int H, int pos_arg,
+                             const int* __restrict__ d_pos, int max_len, int* status) {
+  const int pos = d_pos ? *d_pos : pos_arg;
+  if (pos < 0 || pos >= max_len) {  // a device position past the cache: report, touch nothing
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, DEV_BAD_TOKEN);
+    return;
+  }
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= B * H * 3) return;
@@ -114,10 +119,14 @@ constexpr int kDecWarps = 4;
 template <typename T>
 __global__ void __launch_bounds__(32 * kDecWarps)
     attn_decode_k(const T* __restrict__ qh, const T* __restrict__ K, const T* __restrict__ Vc,
-                  float* __restrict__ part, int H, int pos, int max_len, int chunk, int nchunks) {
+                  float* __restrict__ part, int H, int pos_arg, const int* __restrict__ d_pos, int max_len, int chunk,
+                  int nchunks) {
   __shared__ float sm_m[kDecWarps], sm_l[kDecWarps];
   __shared__ float sm_o[kDecWarps][128];
   const int bh = blockIdx.x, c = blockIdx.y;
+  const int pos = d_pos ? *d_pos : pos_arg;
+  if (pos < 0 || pos >= max_len) return;  // reported by decode_qkv
+  if (c * chunk > pos) return;  // a fixed grid (device position): chunks past pos are unused
   const int b = bh / H, h = bh % H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = H * 128;
@@ -202,11 +211,15 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 // One warp per (b, h): merge the chunk partials into o = sum_c w_c O_c / sum_c w_c L_c.
 template <typename T>
 __global__ void attn_decode_combine_k(const float* __restrict__ part, T* __restrict__ out, int BH, int H,
-                                      int nchunks) {
+                                      int nchunks_grid, const int* __restrict__ d_pos, int chunk) {
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= BH) return;
-  const float* pp = part + (size_t)wid * nchunks * kPart;
+  // partials are laid out with the grid's chunk count; only the chunks up to pos hold data
+  const int pd = d_pos ? *d_pos : 0;
+  const int nchunks = d_pos ? min(nchunks_grid, (max(pd, 0) + chunk) / chunk) : nchunks_grid;
+  const int stride = nchunks_grid;
+  const float* pp = part + (size_t)wid * stride * kPart;
   float M = -INFINITY;
   for (int c = 0; c < nchunks; ++c) M = fmaxf(M, pp[(size_t)c * kPart]);
   float L = 0.f;
@@ -259,20 +272,32 @@ cudaError_t kv_from_qkv(const T* qkv, T* K, T* Vc, int B, int Tn, int H, int max
 
 template <typename T>
 cudaError_t decode_qkv(const float* qkv, T* qh, T* K, T* Vc, const float* rc, const float* rs, int B, int H, int pos,
-                       int max_len, cudaStream_t s) {
+                       const int* d_pos, int max_len, int* status, cudaStream_t s) {
   const int warps = B * H * 3;
-  decode_qkv_k<T><<<(warps + 7) / 8, 256, 0, s>>>(qkv, qh, K, Vc, rc, rs, B, H, pos, max_len);
+  decode_qkv_k<T><<<(warps + 7) / 8, 256, 0, s>>>(qkv, qh, K, Vc, rc, rs, B, H, pos, d_pos, max_len, status);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos, int max_len,
-                        int chunk, cudaStream_t s) {
-  const int nchunks = (pos + 1 + chunk - 1) / chunk;
-  attn_decode_k<T><<<dim3(B * H, nchunks), 32 * kDecWarps, 0, s>>>(qh, K, Vc, part, H, pos, max_len, chunk, nchunks);
+cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos,
+                        const int* d_pos, int max_len, int chunk, cudaStream_t s) {
+  // with a device position the grid covers max_len (a graph replays it at any position)
+  const int span = d_pos ? max_len : pos + 1;
+  const int nchunks = (span + chunk - 1) / chunk;
+  attn_decode_k<T><<<dim3(B * H, nchunks), 32 * kDecWarps, 0, s>>>(qh, K, Vc, part, H, pos, d_pos, max_len, chunk,
+                                                                   nchunks);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  attn_decode_combine_k<T><<<(B * H + 7) / 8, 256, 0, s>>>(part, out, B * H, H, nchunks);
+  attn_decode_combine_k<T><<<(B * H + 7) / 8, 256, 0, s>>>(part, out, B * H, H, nchunks, d_pos, chunk);
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void advance_pos_k(int* d_pos) { *d_pos += 1; }
+}  // namespace
+
+cudaError_t advance_pos(int* d_pos, cudaStream_t s) {
+  advance_pos_k<<<1, 1, 0, s>>>(d_pos);
   return cudaGetLastError();
 }
 
@@ -290,10 +315,10 @@ cudaError_t gather_last(const T* hf, T* out, int B, int Tn, int d, cudaStream_t 
 
 #define NC_DEC_INST(T)                                                                                         \
   template cudaError_t kv_from_qkv<T>(const T*, T*, T*, int, int, int, int, cudaStream_t);                   \
-  template cudaError_t decode_qkv<T>(const float*, T*, T*, T*, const float*, const float*, int, int, int, int, \
-                                     cudaStream_t);                                                          \
-  template cudaError_t attn_decode<T>(const T*, const T*, const T*, float*, T*, int, int, int, int, int,      \
-                                      cudaStream_t);                                                         \
+  template cudaError_t decode_qkv<T>(const float*, T*, T*, T*, const float*, const float*, int, int, int,     \
+                                     const int*, int, int*, cudaStream_t);                                   \
+  template cudaError_t attn_decode<T>(const T*, const T*, const T*, float*, T*, int, int, int, const int*, int, \
+                                      int, cudaStream_t);                                                    \
   template cudaError_t relu2_rows<T>(const float*, T*, long long, cudaStream_t);                               \
   template cudaError_t gather_last<T>(const T*, T*, int, int, int, cudaStream_t);
 NC_DEC_INST(float)

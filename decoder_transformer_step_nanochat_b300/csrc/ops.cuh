@@ -129,16 +129,20 @@ cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStr
 template <typename T>
 cudaError_t kv_from_qkv(const T* qkv, T* K, T* Vc, int B, int Tn, int H, int max_len, cudaStream_t s);
 // qkv fp32 [B, 3d] of the step's token -> q_hat elem [B, d]; k_hat, v into the cache at pos
+// the position is pos, or *d_pos when d_pos is not null (graph-replayable
+// launches); a position outside [0, max_len) sets DEV_BAD_TOKEN and writes nothing
 template <typename T>
 cudaError_t decode_qkv(const float* qkv, T* qh, T* K, T* Vc, const float* rc, const float* rs, int B, int H, int pos,
-                       int max_len, cudaStream_t s);
+                       const int* d_pos, int max_len, int* status, cudaStream_t s);
 // o elem [B, d] = attention of q_hat over cached positions 0..pos; part holds
 // B*H*ceil((pos+1)/chunk) partials of 132 floats
 constexpr int kDecodeChunk = 256;
 constexpr int kDecodePartFloats = 132;
 template <typename T>
-cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos, int max_len,
-                        int chunk, cudaStream_t s);
+cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos,
+                        const int* d_pos, int max_len, int chunk, cudaStream_t s);
+// *d_pos += 1 (one thread)
+cudaError_t advance_pos(int* d_pos, cudaStream_t s);
 template <typename T>
 cudaError_t relu2_rows(const float* u, T* a, long long n, cudaStream_t s);
 template <typename T>

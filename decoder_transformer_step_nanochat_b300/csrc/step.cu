@@ -695,8 +695,10 @@ nc_status prefill_impl(nc_ctx* c, const T* P, const int* tok, char* kv, int max_
   return decode_head<T>(c, P, hl, next, logits);
 }
 
+// pos: the step's position, or -1 with d_pos: read it from device memory and
+// advance it after the step (graph-replayable: no host decision depends on it)
 template <typename T>
-nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, char* kv, int max_len, int32_t* next,
+nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos, char* kv, int max_len, int32_t* next,
                       float* logits) {
   const KvLayout kl = kv_layout(c, max_len);
   const int Bn = c->B, d = c->d, H = c->H, F = c->F, V = c->V;
@@ -728,9 +730,10 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, char* kv, 
     nc_status st = gemm(c, mk(Bn, 3 * d, d, xn, d, 1, Wqkv, d, 1, EPI_STORE_F32, qkv, 3 * d));
     c->gemm_fam = NC_FAM_GEMM;
     CKS(st);
-    KL(NC_FAM_DEC_ROWS, (double)Bn * 3 * d * (4 + e), 1, decode_qkv<T>(qkv, qh, K, Vc, rc, rs, Bn, H, pos, max_len, s));
-    KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * (pos + 1) * e, 2,
-       attn_decode<T>(qh, K, Vc, part, o, Bn, H, pos, max_len, kDecodeChunk, s));
+    KL(NC_FAM_DEC_ROWS, (double)Bn * 3 * d * (4 + e), 1,
+       decode_qkv<T>(qkv, qh, K, Vc, rc, rs, Bn, H, pos, d_pos, max_len, c->status, s));
+    KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * ((d_pos ? max_len : pos) + 1) * e, 2,
+       attn_decode<T>(qh, K, Vc, part, o, Bn, H, pos, d_pos, max_len, kDecodeChunk, s));
     c->gemm_fam = NC_FAM_DEC_GEMM;
     st = gemm(c, mk(Bn, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f));
     c->gemm_fam = NC_FAM_GEMM;
@@ -747,7 +750,9 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, char* kv, 
     CKS(st);
   }
   KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, hf, r, Bn, d, s));
-  return decode_head<T>(c, P, hf, next, logits);
+  CKS(decode_head<T>(c, P, hf, next, logits));
+  if (d_pos) KL(NC_FAM_DEC_ROWS, 8.0, 1, advance_pos(d_pos, s));
+  return NC_OK;
 }
 
 }  // namespace
@@ -1152,8 +1157,23 @@ nc_status nc_decode_step(nc_ctx* c, const void* params, const int32_t* tokens, i
   c->have_fwd = false;
   char* kv = static_cast<char*>(kv_cache);
   return c->prec == NC_BF16
-             ? decode_impl<bf16>(c, static_cast<const bf16*>(params), tokens, pos, kv, max_len, next_tokens, logits)
-             : decode_impl<float>(c, static_cast<const float*>(params), tokens, pos, kv, max_len, next_tokens,
+             ? decode_impl<bf16>(c, static_cast<const bf16*>(params), tokens, pos, nullptr, kv, max_len, next_tokens,
+                                 logits)
+             : decode_impl<float>(c, static_cast<const float*>(params), tokens, pos, nullptr, kv, max_len, next_tokens,
+                                  logits);
+}
+
+nc_status nc_decode_step_dev(nc_ctx* c, const void* params, const int32_t* tokens, int32_t* d_pos, void* kv_cache,
+                             int max_len, int32_t* next_tokens, float* logits) {
+  CKS(check_ready(c));
+  if (!params || !tokens || !next_tokens || !d_pos) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_kv(c, kv_cache, max_len));
+  c->have_fwd = false;
+  char* kv = static_cast<char*>(kv_cache);
+  return c->prec == NC_BF16
+             ? decode_impl<bf16>(c, static_cast<const bf16*>(params), tokens, -1, d_pos, kv, max_len, next_tokens,
+                                 logits)
+             : decode_impl<float>(c, static_cast<const float*>(params), tokens, -1, d_pos, kv, max_len, next_tokens,
                                   logits);
 }
 

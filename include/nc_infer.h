@@ -53,6 +53,17 @@ nc_status nc_prefill(nc_ctx* ctx, const void* params, const int32_t* tokens, voi
 nc_status nc_decode_step(nc_ctx* ctx, const void* params, const int32_t* tokens, int pos, void* kv_cache,
                          int max_len, int32_t* next_tokens, float* logits);
 
+/* As nc_decode_step, with the position read from device memory (*d_pos, an
+ * int32) and advanced by one after the step, so the call's launches do not
+ * depend on the position: a caller can capture one step in a CUDA graph and
+ * replay it for every position (the attention grid covers max_len; chunks
+ * past the position exit at once). A position outside [0, max_len) makes
+ * the step write nothing to the cache and report NC_ERR_DEVICE at the next
+ * synchronising call. The first call must not be made during capture (it
+ * sets up kernel attributes). */
+nc_status nc_decode_step_dev(nc_ctx* ctx, const void* params, const int32_t* tokens, int32_t* d_pos, void* kv_cache,
+                             int max_len, int32_t* next_tokens, float* logits);
+
 #ifdef __cplusplus
 }
 #endif

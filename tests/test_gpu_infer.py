@@ -103,3 +103,52 @@ def test_generation_rejects_bad_arguments():
         assert nc.nc_kv_cache_bytes(st.ctx, 0) == 0
     finally:
         st.close()
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_graph_replayed_decode_matches_host_position_steps(name):
+    """nc_decode_step_dev reads and advances a device position, so one
+    captured step replays for every position; its greedy tokens equal those
+    of the host-position steps."""
+    import torch
+    nc = load_nc()
+    w = W.WORKLOADS[name]
+    prec = nc.NC_FP32_DEBUG if w.dtype == "fp32" else nc.NC_BF16
+    p = W.make_params(w)
+    prompt, _ = W.make_tokens(w)
+    B, T = prompt.shape
+    steps, max_len = 4, w.seq_len + 16
+    ids_host, _ = _generate_gpu(nc, w, p, prompt, steps, max_len, prec)
+    stream = torch.cuda.Stream()
+    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, B, prec, stream=stream)
+    try:
+        dt = torch.bfloat16 if prec == nc.NC_BF16 else torch.float32
+        dp = torch.from_numpy(p).to(dt).cuda()
+        kv = torch.empty(nc.nc_kv_cache_bytes(st.ctx, max_len) + 256, dtype=torch.uint8, device="cuda")
+        kvp = (kv.data_ptr() + 255) // 256 * 256
+        tok = torch.from_numpy(np.ascontiguousarray(prompt, dtype=np.int32)).cuda()
+        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+        cur = torch.empty(B, dtype=torch.int32, device="cuda")
+        pos = torch.full((1,), T, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            nc.nc_prefill(st.ctx, dp.data_ptr(), tok.data_ptr(), kvp, max_len, nxt.data_ptr())
+            got = [nxt.clone()]
+            cur.copy_(nxt)
+            nc.nc_decode_step_dev(st.ctx, dp.data_ptr(), cur.data_ptr(), pos.data_ptr(), kvp, max_len, nxt.data_ptr())
+            got.append(nxt.clone())
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            cur.copy_(nxt)
+            nc.nc_decode_step_dev(st.ctx, dp.data_ptr(), cur.data_ptr(), pos.data_ptr(), kvp, max_len, nxt.data_ptr())
+        for _ in range(steps - 1):
+            g.replay()
+            got.append(nxt.clone())
+        torch.cuda.synchronize()
+        nc.nc_sync(st.ctx)
+        assert int(pos.item()) == T + steps
+        ids_dev = torch.stack(got, 1).cpu().numpy()
+    finally:
+        st.close()
+    np.testing.assert_array_equal(ids_dev, ids_host)
