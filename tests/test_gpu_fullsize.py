@@ -82,3 +82,80 @@ def test_full_size_step(name, sampled):
     V, d = w.vocab, w.d_model
     absent = np.setdiff1d(np.arange(V), np.unique(tok))
     assert np.all(g[:V * d].reshape(V, d)[absent] == 0.0)
+
+
+def test_full_size_d20_sft_masked_loss_sampled():
+    """d20 at the bench batch with SFT prompt/response masks: per-position
+    losses of two sampled sequences against the oracle (masked positions
+    exactly 0), and the loss equal to the mean over the kept positions."""
+    import torch
+    nc = load_nc()
+    w = W.WORKLOADS["d20"]
+    p = W.make_params(w)
+    tok, tgt = W.make_tokens(w)
+    sft = W.make_sft_targets(tgt, seed=9, mean_turn=256)
+    B, T = tok.shape
+    dp = to_device_params(p, nc.NC_BF16)
+    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, B, nc.NC_BF16)
+    try:
+        g = torch.empty(st.n_params, dtype=torch.float32, device="cuda")
+        loss, lse, nll, am = _step(nc, st, dp, tok, sft, g)
+    finally:
+        st.close()
+    keep = (sft != -1).reshape(-1)
+    assert np.all(nll[~keep] == 0.0)
+    assert abs(loss - float(np.mean(nll[keep].astype(np.float64)))) < 1e-4
+    assert np.all(np.isfinite(g.cpu().numpy()))
+    s = shape_of(w)
+    for b in (2, 13):
+        _, cache = oracle.forward(p, tok[b:b + 1, :PREFIX], sft[b:b + 1, :PREFIX], s, np.float32, keep=False)
+        g_nll = nll.reshape(B, T)[b, :PREFIX]
+        assert np.abs(g_nll - cache["nll"]).max() <= 1e-1
+        k = (sft[b, :PREFIX] != -1)
+        assert np.all(g_nll[~k] == 0.0) and np.all(cache["nll"][~k] == 0.0)
+
+
+def test_full_size_d20_generation_sampled():
+    """d20 generation at the bench batch (16 prompts of 2048 tokens), two
+    greedy decode steps: the logits of one sampled sequence against the
+    oracle's prefill and decode steps along the same tokens."""
+    import torch
+    from oracle import infer
+    nc = load_nc()
+    w = W.WORKLOADS["d20"]
+    p = W.make_params(w)
+    tok, _ = W.make_tokens(w)
+    B, T = tok.shape
+    max_len = T + 4
+    st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, B, nc.NC_BF16)
+    try:
+        dp = to_device_params(p, nc.NC_BF16)
+        kv = torch.empty(nc.nc_kv_cache_bytes(st.ctx, max_len) + 256, dtype=torch.uint8, device="cuda")
+        kvp = (kv.data_ptr() + 255) // 256 * 256
+        dt = to_device_i32(tok)
+        nxt = torch.empty(B, dtype=torch.int32, device="cuda")
+        lg = torch.empty((B, w.vocab), dtype=torch.float32, device="cuda")
+        nc.nc_prefill(st.ctx, dp.data_ptr(), dt.data_ptr(), kvp, max_len, nxt.data_ptr(), lg.data_ptr())
+        ids, logits = [nxt.cpu().numpy().copy()], [lg.cpu().numpy().copy()]
+        for i in range(2):
+            cur = nxt.clone()
+            nc.nc_decode_step(st.ctx, dp.data_ptr(), cur.data_ptr(), T + i, kvp, max_len, nxt.data_ptr(), lg.data_ptr())
+            ids.append(nxt.cpu().numpy().copy())
+            logits.append(lg.cpu().numpy().copy())
+        nc.nc_sync(st.ctx)
+    finally:
+        st.close()
+    b = 7
+    s = shape_of(w)
+    cache, ref = infer.prefill(p, tok[b:b + 1], s, np.float32)
+    refs = [ref]
+    for i in range(2):
+        cache, ref = infer.decode_step(p, cache, np.array([ids[i][b]]), s, np.float32)
+        refs.append(ref)
+    for i, r in enumerate(refs):
+        gi = logits[i][b].astype(np.float64)
+        ri = r[0].astype(np.float64)
+        assert rel_l2(gi, ri) <= 3e-2, (i, rel_l2(gi, ri))
+        top2 = np.sort(ri)[-2:]
+        if top2[1] - top2[0] > 4 * np.abs(gi - ri).max():
+            assert ids[i][b] == int(np.argmax(ri))
