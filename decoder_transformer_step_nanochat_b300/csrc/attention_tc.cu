@@ -105,100 +105,82 @@ struct AttnParams {
 
 // ============================================================== forward
 //
-// One CTA per (b, h, pair of 128-query tiles qa = 2i and qb = 2i + 1), so the
-// 256 query rows of a pair share every K/V tile the CTA loads. Warp 0 loads
-// by TMA, one thread of warp 1 issues the MMAs, warps 4-7 run the softmax of
-// tile a and warps 8-11 that of tile b with one thread per query row (TMEM
-// lane = row): a row's maximum and sum never leave its thread. Warps 2-3 only
-// take part in setup and teardown.
+// One CTA per (b, h, 128-query tile), two CTAs per SM: the tensor cores
+// interleave the independent products of the two CTAs, which a single
+// accumulator chain cannot keep busy (a 128x128x16 MMA issued back to back
+// into one accumulator runs at about 58% of the tensor rate; two chains
+// reach it). Eight warps: warp 0 loads Q and K, warp 2 loads V, one thread
+// of warp 1 issues the MMAs, warps 4-7 run the softmax with one thread per
+// query row (TMEM lane = row), so a row's max and sum never leave its thread.
+// TMEM (256 columns per CTA): S [0,128), with P written back over its first
+// 64 columns as packed bf16 that O += P V reads straight from TMEM, and O
+// [128,256). Shared memory: Q and single K and V buffers (96 KB).
 //
-// TMEM: S_a [0,128), S_b [128,256), O_a [256,384), O_b [384,512). The softmax
-// writes P (bf16, two keys per 32-bit column) over the first 64 columns of its
-// S buffer and O += P V reads it straight from TMEM.
-//
-// MMA order for key tile j: PV_a(j-1), S_a(j), PV_b(j-1), S_b(j). While the
-// softmax of one tile works on S(j), the tensor cores run the other tile's PV
-// and S. A commit covers every MMA issued before it, so once S_x(j) is seen
-// complete, PV_x(j-1) has landed as well: O_x is quiescent while softmax x
-// looks at it, and P_x(j-1) was read before S_x(j) overwrote it.
-//
-// The softmax keeps per row a reference maximum m (log2 units) and
-// exponentiates against it; only when a tile's maximum exceeds m by more than
-// 8 (so p could exceed 2^8) does it move m up and rescale the row of O and
-// the running sum.
+// MMA order: S(0), then per key tile j >= 1: PV(j-1), S(j). A commit covers
+// every MMA issued before it, so once S(j) is seen complete PV(j-1) has
+// landed too: O is quiescent while the softmax may rescale it, and P(j-1)
+// was read before S(j) overwrote it. The softmax keeps per row a reference
+// maximum m (log2 units); only when a tile's maximum exceeds m by more than
+// 8 does it move m up and rescale the row of O and the running sum.
 
 constexpr float kRescaleLog2 = 8.f;
-constexpr int FWD_WARPS = 12;
+constexpr int FWD_WARPS = 8;
 constexpr int FWD_THREADS = 32 * FWD_WARPS;
-constexpr int FWD_SOFT = 128;  // threads per softmax warpgroup
-// Registers: launched at 168 per thread (384 threads, 64512 in all); the
-// load/MMA warpgroup drops to 56 and the two softmax warpgroups rise to 224:
-// 128 * 56 + 2 * 128 * 224 = 64512, within the launch's total.
-constexpr int FWD_REG_LAUNCH = 168, FWD_REG_LOW = 56, FWD_REG_HIGH = 224;
-// K ring of 3 stages, V ring of 2 (Q pair + rings = 224 KB of shared memory)
-constexpr int FWD_KST = 3, FWD_VST = 2;
-static_assert(128 * FWD_REG_LOW + 2 * 128 * FWD_REG_HIGH <= FWD_THREADS * FWD_REG_LAUNCH, "register split");
+constexpr int FWD_SOFT = 128;
+// Registers: 128 per thread at launch (two CTAs of 256 threads per SM); the
+// load/MMA warpgroup drops to 56 and the softmax warpgroup rises to 200.
+constexpr int FWD_REG_LAUNCH = 128, FWD_REG_LOW = 56, FWD_REG_HIGH = 200;
+static_assert(128 * FWD_REG_LOW + 128 * FWD_REG_HIGH <= FWD_THREADS * FWD_REG_LAUNCH, "register split");
+constexpr int FWD_KST = 1, FWD_VST = 1;
 
-__global__ void __launch_bounds__(FWD_THREADS, 1)
+__global__ void __launch_bounds__(FWD_THREADS, 2)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // the 128-byte swizzle needs 1024-byte aligned tiles; the dynamic window
-  // starts aligned on this architecture, and a launch where it does not is
-  // refused rather than run wrong
   if (tc::smem_u32(smem_raw) & 1023) {
     if (threadIdx.x == 0) set_status(p.status, DEV_BAD_LAUNCH);
     return;
   }
   uint8_t* smem = smem_raw;
-  uint8_t* sQ = smem;                            // Q_a, Q_b
-  uint8_t* sK = sQ + 2 * TILE_BYTES;             // FWD_KST stages
-  uint8_t* sV = sK + FWD_KST * TILE_BYTES;       // FWD_VST stages
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + FWD_VST * TILE_BYTES);
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + TILE_BYTES;
+  uint8_t* sV = sK + TILE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + TILE_BYTES);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;                   // [FWD_KST]
-  uint64_t* k_empty = k_full + FWD_KST;          // [FWD_KST]
-  uint64_t* v_full = k_empty + FWD_KST;          // [FWD_VST]
-  uint64_t* v_empty = v_full + FWD_VST;          // [FWD_VST]
-  uint64_t* s_full = v_empty + FWD_VST;          // [2]: tile a, tile b
-  uint64_t* p_full = s_full + 2;                 // [2]
-  uint64_t* o_full = p_full + 2;
-  uint64_t* drain = o_full + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = bars + 2;
+  uint64_t* v_full = bars + 3;
+  uint64_t* v_empty = bars + 4;
+  uint64_t* s_full = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* o_full = bars + 7;
+  uint64_t* drain = bars + 8;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   // (batch, head)-major order: the CTAs running together share one head's K/V
-  // in L2; within a head the heaviest query-tile pairs go first
-  const int npair = (p.nq + 1) / 2;
-  const int bh = (int)(blockIdx.x / npair), b = bh / p.H, h = bh % p.H;
-  const int pi = npair - 1 - (int)(blockIdx.x % npair);
-  const int qa = 2 * pi;
-  const bool has_b = qa + 1 < p.nq;       // an odd tile count leaves the last pair single
-  const int nkv_a = qa + 1, nkv = has_b ? qa + 2 : qa + 1;
+  // in L2; within a head the heaviest query tiles go first
+  const int bh = (int)(blockIdx.x / p.nq), b = bh / p.H, h = bh % p.H;
+  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);
+  const int nkv = qt + 1;
   const int d = p.H * 128;
-  const int row0 = b * p.T + qa * TILE;   // first query row of tile a
+  const int row0 = b * p.T + qt * TILE;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
-    for (int s = 0; s < FWD_KST; ++s) {
-      tc::mbar_init(k_full + s, 1);
-      tc::mbar_init(k_empty + s, 1);
-    }
-    for (int s = 0; s < FWD_VST; ++s) {
-      tc::mbar_init(v_full + s, 1);
-      tc::mbar_init(v_empty + s, 1);
-    }
-    for (int x = 0; x < 2; ++x) {
-      tc::mbar_init(s_full + x, 1);
-      tc::mbar_init(p_full + x, FWD_SOFT);
-    }
+    tc::mbar_init(k_full, 1);
+    tc::mbar_init(k_empty, 1);
+    tc::mbar_init(v_full, 1);
+    tc::mbar_init(v_empty, 1);
+    tc::mbar_init(s_full, 1);
+    tc::mbar_init(p_full, FWD_SOFT);
     tc::mbar_init(o_full, 1);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_holder, 512);
+    tc::tmem_alloc(tmem_holder, 256);
     tc::tmem_relinquish();
   }
   tc::tc_fence_before();
@@ -209,97 +191,56 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   if (warp < 4) {
     tc::setmaxnreg_dec<FWD_REG_LOW>();
     if ((warp == 0 || warp == 2) && lane == 0) {
-      // ---------------------------------------------------------------- TMA producers
-      // warp 0 loads Q and the K ring, warp 2 the V ring, so a K tile never
-      // waits behind a V stage that is still being read
       const bool kside = warp == 0;
-      const int nst = kside ? FWD_KST : FWD_VST;
       uint64_t* full = kside ? k_full : v_full;
       uint64_t* empty = kside ? k_empty : v_empty;
-      uint8_t* ring = kside ? sK : sV;
+      uint8_t* buf = kside ? sK : sV;
       const int col = (kside ? d : 2 * d) + h * 128;
       tc::prefetch_tmap(&tqkv);
       if (kside) {
-        tc::mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * TILE_BYTES);
-        for (int t = 0; t < (has_b ? 2 : 1); ++t) {
-          tc::tma_load_2d(sQ + t * TILE_BYTES, &tqkv, h * 128, row0 + t * TILE, q_full);
-          tc::tma_load_2d(sQ + t * TILE_BYTES + HALF_BYTES, &tqkv, h * 128 + 64, row0 + t * TILE, q_full);
-        }
+        tc::mbar_arrive_expect_tx(q_full, TILE_BYTES);
+        tc::tma_load_2d(sQ, &tqkv, h * 128, row0, q_full);
+        tc::tma_load_2d(sQ + HALF_BYTES, &tqkv, h * 128 + 64, row0, q_full);
       }
-      int last = -1;  // last tile issued
+      int last = -1;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j % nst;
-        const uint32_t ph = (uint32_t)(j / nst) & 1;
-        if (!tc::mbar_wait(empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+        if (!tc::mbar_wait(empty, (j & 1) ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
         const int kr = b * p.T + j * TILE;
-        tc::mbar_arrive_expect_tx(full + s, TILE_BYTES);
-        tc::tma_load_2d(ring + s * TILE_BYTES, &tqkv, col, kr, full + s);
-        tc::tma_load_2d(ring + s * TILE_BYTES + HALF_BYTES, &tqkv, col + 64, kr, full + s);
+        tc::mbar_arrive_expect_tx(full, TILE_BYTES);
+        tc::tma_load_2d(buf, &tqkv, col, kr, full);
+        tc::tma_load_2d(buf + HALF_BYTES, &tqkv, col + 64, kr, full);
         last = j;
       }
       if (failed) {
         *abort_flag = 1;
         if (kside) tc::mbar_wait(q_full, 0, nullptr, kWaitNs);
-        // every copy this thread started lands before the CTA exits
-        for (int j = (last - nst + 1 > 0 ? last - nst + 1 : 0); j <= last; ++j)
-          tc::mbar_wait(full + j % nst, (uint32_t)(j / nst) & 1, nullptr, kWaitNs);
+        if (last >= 0) tc::mbar_wait(full, last & 1, nullptr, kWaitNs);
       }
     } else if (warp == 1 && lane == 0) {
-      // ---------------------------------------------------------------- MMA issuer
-      const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);     // S = Q K^T, both K-major
-      const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);  // O += P V, V MN-major
+      const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);
+      const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);
       bool any = false;
       if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
-      // O_x += P_x(i) V_i, P_x read from the first 64 columns of S_x
-      auto issue_pv = [&](int x, int i) -> bool {
-        if (!tc::mbar_wait(p_full + x, i & 1, abort_flag, kWaitNs)) return false;
-        tc::tc_fence_after();
-        const uint32_t tP = tmem + x * 128, tO = tmem + 256 + x * 128;
-        const uint32_t aV = tc::smem_u32(sV + (i % FWD_VST) * TILE_BYTES);
-#pragma unroll
-        for (int k = 0; k < TILE / 16; ++k)
-          tc::mma_bf16_tmem_a(tO, tP + k * 8, desc_mn(aV, k), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-        any = true;
-        return true;
-      };
-      // step j: PV_a(j-1), S_a(j), PV_b(j-1), S_b(j); the last step only
-      // finishes the PVs. A ring stage is released by a commit right after
-      // its last reader is issued.
       for (int j = 0; j <= nkv && !failed; ++j) {
-        const bool has_s = j < nkv;
-        if (j > 0) {
+        if (j > 0) {  // O += P(j-1) V(j-1), P read from the first 64 columns of S
           const int i = j - 1;
-          if (!tc::mbar_wait(v_full + i % FWD_VST, (uint32_t)(i / FWD_VST) & 1, abort_flag, kWaitNs)) {
-            failed = true;
-            break;
-          }
-          if (i < nkv_a && !issue_pv(0, i)) { failed = true; break; }
-        }
-        if (has_s) {
-          if (!tc::mbar_wait(k_full + j % FWD_KST, (uint32_t)(j / FWD_KST) & 1, abort_flag, kWaitNs)) {
-            failed = true;
-            break;
-          }
+          if (!tc::mbar_wait(v_full, i & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(p_full, i & 1, abort_flag, kWaitNs)) { failed = true; break; }
           tc::tc_fence_after();
-          if (j < nkv_a) {
-            mma_tile(tmem, tc::smem_u32(sQ), false, tc::smem_u32(sK + (j % FWD_KST) * TILE_BYTES), false, idesc,
-                     false);
-            tc::mma_commit(s_full + 0);
-            any = true;
-          }
+          const uint32_t aV = tc::smem_u32(sV);
+#pragma unroll
+          for (int k = 0; k < TILE / 16; ++k)
+            tc::mma_bf16_tmem_a(tmem + 128, tmem + k * 8, desc_mn(aV, k), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
+          any = true;
+          tc::mma_commit(v_empty);
         }
-        if (j > 0) {
-          if (has_b && !issue_pv(1, j - 1)) { failed = true; break; }
-          tc::mma_commit(v_empty + (j - 1) % FWD_VST);
-        }
-        if (has_s) {
-          if (has_b) {
-            mma_tile(tmem + 128, tc::smem_u32(sQ + TILE_BYTES), false,
-                     tc::smem_u32(sK + (j % FWD_KST) * TILE_BYTES), false, idesc, false);
-            tc::mma_commit(s_full + 1);
-            any = true;
-          }
-          tc::mma_commit(k_empty + j % FWD_KST);
+        if (j < nkv) {
+          if (!tc::mbar_wait(k_full, j & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::tc_fence_after();
+          mma_tile(tmem, tc::smem_u32(sQ), false, tc::smem_u32(sK), false, idesc, false);
+          any = true;
+          tc::mma_commit(s_full);
+          tc::mma_commit(k_empty);
         }
       }
       if (!failed) tc::mma_commit(o_full);
@@ -311,25 +252,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         }
       }
     }
-  } else if (warp < 8 || has_b) {
-    // ---------------------------------------------------------------- softmax warpgroups
+  } else {
     tc::setmaxnreg_inc<FWD_REG_HIGH>();
-    const int x = (warp - 4) >> 2;          // 0: tile a, 1: tile b
-    const int qt = qa + x;                  // this tile's index; its diagonal key tile is qt
-    const int q4 = warp & 3;                // TMEM lane quadrant
-    const int r = q4 * 32 + lane;           // query row within the tile = TMEM lane
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + lane_off, tO = tmem + 256 + x * 128 + lane_off;
+    const uint32_t tS = tmem + lane_off, tO = tmem + 128 + lane_off;
     const float sl2 = kLog2e * rsqrtf(128.f);
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j <= qt; ++j) {
-      bool ok = tc::mbar_wait(s_full + x, j & 1, abort_flag, kWaitNs);
+      bool ok = tc::mbar_wait(s_full, j & 1, abort_flag, kWaitNs);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
       float v[128];
       tc::tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, v, v + 32, v + 64, v + 96);
-      const bool diag = (j == qt);
-      if (diag) {
+      if (j == qt) {
 #pragma unroll
         for (int i = 0; i < 128; ++i)
           if (i > r) v[i] = -INFINITY;
@@ -342,14 +279,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
         mx4[2] = fmaxf(mx4[2], v[i + 2]);
         mx4[3] = fmaxf(mx4[3], v[i + 3]);
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;  // scale > 0 commutes with max
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       const bool grow = mx > m + kRescaleLog2;
       if (__any_sync(0xffffffffu, grow)) {
         const float m_new = grow ? mx : m;
-        const float alpha = exp2f(m - m_new);  // 0 for the first tile (m = -inf)
+        const float alpha = exp2f(m - m_new);
         l *= alpha;
         m = m_new;
-        if (j > 0) {  // O holds partial sums: rescale this row (no PV on it is in flight)
+        if (j > 0) {
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
             float o[32];
@@ -365,7 +302,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float e0 = tc::ex2(fmaf(v[2 * i], sl2, nm));      // ex2(-inf) = 0 for masked keys
+        const float e0 = tc::ex2(fmaf(v[2 * i], sl2, nm));
         const float e1 = tc::ex2(fmaf(v[2 * i + 1], sl2, nm));
         rs[i & 3] += e0 + e1;
         __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
@@ -375,15 +312,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
       tc::tmem_st32(tS, reinterpret_cast<const float*>(pk));
       tc::tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
       tc::tc_fence_before();
-      tc::mbar_arrive(p_full + x);
+      tc::mbar_arrive(p_full);
     }
     bool ok = !failed;
     if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
     if (__all_sync(0xffffffffu, ok)) {
       tc::tc_fence_after();
       const float inv = 1.f / l;
-      const int row = row0 + x * TILE + r;
-      bf16* orow = p.o + (size_t)row * d + h * 128;
+      bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float o[32];
@@ -408,7 +344,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 512);
+    tc::tmem_dealloc(tmem, 256);
   }
 }
 
@@ -891,7 +827,7 @@ bool map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr int FWD_SMEM = (2 + FWD_KST + FWD_VST) * TILE_BYTES + 256;  // Q pair, K and V rings, barriers
+constexpr int FWD_SMEM = (1 + FWD_KST + FWD_VST) * TILE_BYTES + 256;  // Q, K, V, barriers
 constexpr int BWD_SMEM = 7 * TILE_BYTES + 2 * 2 * TILE * 4 + 256;
 
 }  // namespace
@@ -909,7 +845,7 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
   p.o = o; p.lse = lse; p.status = status;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_fwd_tc_k<<<B * H * ((p.nq + 1) / 2), FWD_THREADS, FWD_SMEM, s>>>(tq, p);
+  attn_fwd_tc_k<<<B * H * p.nq, FWD_THREADS, FWD_SMEM, s>>>(tq, p);
   return cudaGetLastError();
 }
 

@@ -116,9 +116,9 @@ def test_full_size_d20_sft_masked_loss_sampled():
 
 
 def test_full_size_d20_generation_sampled():
-    """d20 generation at the bench batch (16 prompts of 2048 tokens), two
-    greedy decode steps: the logits of one sampled sequence against the
-    oracle's prefill and decode steps along the same tokens."""
+    """d20 generation at the bench batch (16 prompts of 2048 tokens) and two
+    decode steps fed with seeded tokens: the logits of one sampled sequence
+    against the oracle's prefill and decode steps on the same tokens."""
     import torch
     from oracle import infer
     nc = load_nc()
@@ -137,8 +137,9 @@ def test_full_size_d20_generation_sampled():
         lg = torch.empty((B, w.vocab), dtype=torch.float32, device="cuda")
         nc.nc_prefill(st.ctx, dp.data_ptr(), dt.data_ptr(), kvp, max_len, nxt.data_ptr(), lg.data_ptr())
         ids, logits = [nxt.cpu().numpy().copy()], [lg.cpu().numpy().copy()]
+        feed = W.make_decode_tokens(w, 2)
         for i in range(2):
-            cur = nxt.clone()
+            cur = to_device_i32(feed[:, i])
             nc.nc_decode_step(st.ctx, dp.data_ptr(), cur.data_ptr(), T + i, kvp, max_len, nxt.data_ptr(), lg.data_ptr())
             ids.append(nxt.cpu().numpy().copy())
             logits.append(lg.cpu().numpy().copy())
@@ -150,7 +151,7 @@ def test_full_size_d20_generation_sampled():
     cache, ref = infer.prefill(p, tok[b:b + 1], s, np.float32)
     refs = [ref]
     for i in range(2):
-        cache, ref = infer.decode_step(p, cache, np.array([ids[i][b]]), s, np.float32)
+        cache, ref = infer.decode_step(p, cache, feed[b:b + 1, i], s, np.float32)
         refs.append(ref)
     for i, r in enumerate(refs):
         gi = logits[i][b].astype(np.float64)

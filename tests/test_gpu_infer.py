@@ -1,10 +1,12 @@
 """Generation with a KV cache (include/nc_infer.h) against the oracle
-(oracle/infer.py): prefill of the workload's prompts, then decode steps that
-feed back the GPU's own greedy tokens; the oracle runs the same token
-sequence. fp32 debug mode within 1e-4 relative on the logits with identical
-greedy tokens; bf16 within the step's bar (logits relative L2 <= 3e-2, lse
-within 5e-2 nats) with identical tokens wherever the oracle's top-1/top-2
-margin exceeds four times the largest logit difference seen."""
+(oracle/infer.py): prefill of the workload's prompts, then decode steps fed
+with the same seeded continuation tokens on both sides. fp32 debug mode
+within 1e-4 relative on the logits, with the greedy token of every step equal
+to the argmax of the oracle's logits; bf16 within the step's bar (logits
+relative L2 <= 3e-2, lse within 5e-2 nats) with the greedy token equal
+wherever the oracle's top-1/top-2 margin exceeds four times the largest
+logit difference seen. The graph-replay test compares the device-position
+steps with the host-position steps (no oracle)."""
 
 import numpy as np
 import pytest
@@ -22,7 +24,10 @@ def _lse(x):
     return (m + np.log(np.exp(x - m).sum(-1, keepdims=True)))[:, 0]
 
 
-def _generate_gpu(nc, w, params, prompt, steps, max_len, precision):
+def _generate_gpu(nc, w, params, prompt, steps, max_len, precision, feed=None):
+    """Prefill + `steps` decode steps; step i is fed feed[:, i] when given,
+    else the previous greedy token. Returns greedy tokens [B, steps+1] and
+    the logits of every produced position."""
     import torch
     B, T = prompt.shape
     st = nc.Step(w.depth, w.d_model, w.n_head, w.seq_len, w.vocab, B, precision)
@@ -37,7 +42,7 @@ def _generate_gpu(nc, w, params, prompt, steps, max_len, precision):
         nc.nc_prefill(st.ctx, dp.data_ptr(), tok.data_ptr(), kvp, max_len, nxt.data_ptr(), logits.data_ptr())
         ids, lg = [nxt.cpu().numpy().copy()], [logits.cpu().numpy().copy()]
         for i in range(steps):
-            cur = nxt.clone()
+            cur = nxt.clone() if feed is None else torch.from_numpy(np.ascontiguousarray(feed[:, i])).cuda()
             nc.nc_decode_step(st.ctx, dp.data_ptr(), cur.data_ptr(), T + i, kvp, max_len, nxt.data_ptr(),
                               logits.data_ptr())
             ids.append(nxt.cpu().numpy().copy())
@@ -48,13 +53,13 @@ def _generate_gpu(nc, w, params, prompt, steps, max_len, precision):
         st.close()
 
 
-def _oracle_follow(w, params, prompt, ids, dtype):
-    """Oracle logits along the GPU's token sequence."""
+def _oracle_follow(w, params, prompt, feed, dtype):
+    """Oracle logits of the prompt's last position and of each fed token."""
     s = shape_of(w)
     cache, logits = infer.prefill(params.astype(dtype), prompt, s, dtype)
     out = [logits]
-    for i in range(ids.shape[1] - 1):
-        cache, logits = infer.decode_step(params.astype(dtype), cache, ids[:, i], s, dtype)
+    for i in range(feed.shape[1]):
+        cache, logits = infer.decode_step(params.astype(dtype), cache, feed[:, i], s, dtype)
         out.append(logits)
     return out
 
@@ -64,8 +69,9 @@ def test_tiny_fp32_generation_matches_oracle():
     w = W.WORKLOADS["tiny"]
     p = W.make_params(w)
     tok, _ = W.make_tokens(w)
-    ids, lg = _generate_gpu(nc, w, p, tok, 4, w.seq_len + 8, nc.NC_FP32_DEBUG)
-    ref = _oracle_follow(w, p, tok, ids, np.float64)
+    feed = W.make_decode_tokens(w, 4)
+    ids, lg = _generate_gpu(nc, w, p, tok, 4, w.seq_len + 8, nc.NC_FP32_DEBUG, feed)
+    ref = _oracle_follow(w, p, tok, feed, np.float64)
     for i, (g, r) in enumerate(zip(lg, ref)):
         assert rel_l2(g, r) <= 1e-4, (i, rel_l2(g, r))
         np.testing.assert_array_equal(ids[:, i], np.argmax(r, -1))
@@ -76,8 +82,9 @@ def test_small_bf16_generation_matches_oracle():
     w = W.WORKLOADS["small"]
     p = W.make_params(w)
     tok, _ = W.make_tokens(w)
-    ids, lg = _generate_gpu(nc, w, p, tok, 4, w.seq_len + 64, nc.NC_BF16)
-    ref = _oracle_follow(w, p, tok, ids, np.float32)
+    feed = W.make_decode_tokens(w, 4)
+    ids, lg = _generate_gpu(nc, w, p, tok, 4, w.seq_len + 64, nc.NC_BF16, feed)
+    ref = _oracle_follow(w, p, tok, feed, np.float32)
     for i, (g, r) in enumerate(zip(lg, ref)):
         r = r.astype(np.float64)
         assert rel_l2(g, r) <= 3e-2, (i, rel_l2(g, r))

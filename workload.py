@@ -176,6 +176,15 @@ def make_sft_targets(targets: np.ndarray, seed: int = 200, mean_turn: int = 128)
     return out
 
 
+def make_decode_tokens(w: Workload, steps: int, seed: int = 300) -> np.ndarray:
+    """Tokens fed to `steps` decode steps after a prompt, int32 [B, steps]:
+    Zipf(1.1) ids like the prompts', from PCG64(seed)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    cdf = zipf_cdf(w.vocab)
+    ids = np.searchsorted(cdf, rng.random(w.batch * steps), side="right")
+    return np.minimum(ids, w.vocab - 1).astype(np.int32).reshape(w.batch, steps)
+
+
 def zipf_cdf(vocab: int, s: float = 1.1) -> np.ndarray:
     k = np.arange(1, vocab + 1, dtype=np.float64)
     p = k ** (-s)
