@@ -355,19 +355,27 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 // a head, so the CTAs running together share a few heads' Q, dO and dq rows
 // in L2 and finish together. The producer thread draws each unit and hands
 // its index to the other roles through a shared-memory ring. 10 warps: TMA
-// producer, MMA issuer and eight softmax/epilogue warps (two per TMEM lane
-// quadrant, each owning 64 of the 128 query columns). TMEM: [0,128) S^T,
-// overwritten in place by P^T as packed bf16 (query half c at columns
-// 64c .. 64c+31), [128,256) dP^T and then dQ, [256,384) dV, [384,512) dK.
-// Shared memory: K, V, two Q/dO stages (the next query tile loads while this
-// one computes, across units too) and dS^T.
-// Per query tile: S^T = K Q^T and dP^T = V dO^T; P^T = exp(S^T - lse),
-// dS^T = P^T (dP^T - D); dV += P^T dO (A operand read from TMEM),
-// dK += dS^T Q, dQ = dS K; dQ is added to the fp32 plane by bulk tensor
-// reduce-adds staged in the dS^T tile, while the next tile's S^T is already
-// being computed. Between units, the next K/V load as soon as the finished
-// unit's products are done and its first query tiles run while the epilogue
-// warps still drain dV/dK; only its first dV/dK products wait for that drain.
+// producer, MMA issuer and eight softmax/epilogue warps; warps 2-5 work on
+// query columns 0-63 of each query tile and warps 6-9 on columns 64-127, one
+// key row per thread (TMEM lane).
+//
+// TMEM: S^T [0,128) and dP^T [128,256), each as two 64-query halves; P^T of
+// half h is written back packed (bf16 pairs) over the first 32 columns of its
+// S^T half and feeds dV from TMEM; dQ^T of half h (= K^T dS^T_h, head
+// dimension in the TMEM lane) replaces its dP^T half; dV [256,384) and dK
+// [384,512) accumulate over the unit. Shared memory: K, V, two Q/dO stages
+// (the next query tile loads while this one computes, across units too) and
+// dS^T, whose 4 KB block of each warp also stages that warp's dQ reduce-adds.
+//
+// Per query tile and half h: S^T_h = K Q_h^T and dP^T_h = V dO_h^T
+// (interleaved); P^T_h = exp(S^T_h - lse), dS^T_h = P^T_h (dP^T_h - D) by
+// that half's warps; then dV += P^T_h dO_h, dK += dS^T_h Q_h and dQ^T_h, their
+// k-steps interleaved. One half's softmax thus runs while the tensor cores
+// work on the other half. dQ^T_h is read out (its TMEM columns released at
+// once), staged transposed and added to the fp32 dq plane with bulk tensor
+// reduce-adds. Between units, the next K/V load as soon as the finished
+// unit's products are done and its first query tile runs while the epilogue
+// warps drain dV/dK; only its first dV/dK products wait for that drain.
 
 constexpr int BWD_WARPS = 10;
 constexpr int BWD_THREADS = 32 * BWD_WARPS;
@@ -407,14 +415,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;    // [2]
   uint64_t* q_empty = bars + 4;   // [2]
-  uint64_t* st_full = bars + 6;
-  uint64_t* p_full = bars + 7;
-  uint64_t* dq_full = bars + 8;
-  uint64_t* tm_free = bars + 9;
-  uint64_t* acc_full = bars + 10;
-  uint64_t* acc_free = bars + 11;
-  uint64_t* drain = bars + 12;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 13);
+  uint64_t* st_full = bars + 6;   // [2]: per 64-query half
+  uint64_t* p_full = bars + 8;    // [2]
+  uint64_t* dq_full = bars + 10;  // [2]
+  uint64_t* tm_free = bars + 12;  // [2]
+  uint64_t* acc_full = bars + 14;
+  uint64_t* acc_free = bars + 15;
+  uint64_t* drain = bars + 16;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   // unit index of this CTA's ul-th unit at slot ul % 4 (-1: no more units); it
   // is written before the arrive that completes that unit's kv_full phase
@@ -432,10 +440,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc::mbar_init(q_full + s, 1);
       tc::mbar_init(q_empty + s, 1);
     }
-    tc::mbar_init(st_full, 1);
-    tc::mbar_init(p_full, BWD_SOFT);
-    tc::mbar_init(dq_full, 1);
-    tc::mbar_init(tm_free, BWD_SOFT);
+    for (int hh = 0; hh < 2; ++hh) {
+      tc::mbar_init(st_full + hh, 1);
+      tc::mbar_init(p_full + hh, BWD_SOFT / 2);   // the four warps of that half
+      tc::mbar_init(dq_full + hh, 1);
+      tc::mbar_init(tm_free + hh, BWD_SOFT / 2);
+    }
     tc::mbar_init(acc_full, 1);
     tc::mbar_init(acc_free, BWD_SOFT);
     tc::mbar_init(drain, 1);
@@ -450,8 +460,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  // S^T and dP^T halves: query half h at columns 64h of each region; P^T of
+  // half h is packed over the first 32 columns of its S^T half; dQ^T of half
+  // h replaces its dP^T half once the softmax has read it
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
-  const uint32_t tdQ = tdP;  // dP^T is consumed before dQ is formed
   bool failed = false;
 
   if (warp == 0) {
@@ -515,9 +527,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_kk = tc::idesc_bf16(128, 128, 0, 0);   // both K-major
-      const uint32_t id_kmn = tc::idesc_bf16(128, 128, 0, 1);  // B MN-major
-      const uint32_t id_mnmn = tc::idesc_bf16(128, 128, 1, 1); // A and B MN-major
+      const uint32_t id_n64 = tc::idesc_bf16(128, 64, 0, 0);       // S^T_h, dP^T_h: both K-major
+      const uint32_t id_kmn = tc::idesc_bf16(128, 128, 0, 1);      // dV, dK: B MN-major
+      const uint32_t id_mnmn_n64 = tc::idesc_bf16(128, 64, 1, 1);  // dQ^T_h: A and B MN-major
       const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), adSt = tc::smem_u32(sdSt);
       bool any = false;
       int g = 0, ul = 0;
@@ -530,36 +542,49 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           const int s = g & 1;
           const uint32_t aQ = tc::smem_u32(sQ + s * TILE_BYTES), adO = tc::smem_u32(sdO + s * TILE_BYTES);
           if (!tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          // S^T overwrites P^T of the previous tile: wait until its products finished
-          if (g > 0 && !tc::mbar_wait(dq_full, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          tc::tc_fence_after();
-          mma_tile(tS, aK, false, aQ, false, id_kk, false);       // S^T  = K Q^T
-          any = true;
-          // dP^T overwrites dQ of the previous tile: wait until it was read out
-          if (g > 0 && !tc::mbar_wait(tm_free, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          tc::tc_fence_after();
-          mma_tile(tdP, aV, false, adO, false, id_kk, false);     // dP^T = V dO^T
-          tc::mma_commit(st_full);
-          if (!tc::mbar_wait(p_full, g & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          // the first dV/dK of a unit overwrite the accumulators of the previous
-          // one: wait until the epilogue warps have read them out
-          if (it == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, kWaitNs)) {
-            failed = true;
-            break;
-          }
-          tc::tc_fence_after();
-          // dV += P^T dO (P^T in TMEM: k-step k reads query columns 16k..16k+15),
-          // dK += dS^T Q and dQ = dS K, their k-steps interleaved: independent
-          // accumulators keep the tensor pipe full where one chain would wait on
-          // its own accumulation
+          // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for the two 64-query halves
+          // (rows 64h.. of the Q / dO tiles), each pair interleaved
+          for (int hh = 0; hh < 2 && !failed; ++hh) {
+            // dP^T_h replaces dQ^T_h of the previous tile: wait until it was read
+            // out (S^T_h replaces P^T_h, whose reader dV_h was issued earlier)
+            if (g > 0 && !tc::mbar_wait(tm_free + hh, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+            tc::tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < TILE / 16; ++k) {
-            tc::mma_bf16_tmem_a(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn,
-                                (it > 0 || k > 0) ? 1u : 0u);
-            tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (it > 0 || k > 0) ? 1u : 0u);
-            tc::mma_bf16(tdQ, desc_mn(adSt, k), desc_mn(aK, k), id_mnmn, k > 0 ? 1u : 0u);
+            for (int k = 0; k < TILE / 16; ++k) {
+              tc::mma_bf16(tS + 64 * hh, desc_k(aK, k), desc_k(aQ + 8192 * hh, k), id_n64, k > 0 ? 1u : 0u);
+              tc::mma_bf16(tdP + 64 * hh, desc_k(aV, k), desc_k(adO + 8192 * hh, k), id_n64, k > 0 ? 1u : 0u);
+            }
+            any = true;
+            tc::mma_commit(st_full + hh);
           }
-          tc::mma_commit(dq_full);
+          if (failed) break;
+          // per half: dV += P^T_h dO_h (P^T_h from TMEM), dK += dS^T_h Q_h and
+          // dQ^T_h = K^T dS^T_h (into the dP^T_h columns), interleaved
+          for (int hh = 0; hh < 2 && !failed; ++hh) {
+            if (!tc::mbar_wait(p_full + hh, g & 1, abort_flag, kWaitNs)) { failed = true; break; }
+            // the first dV/dK of a unit overwrite the accumulators of the previous
+            // one: wait until the epilogue warps have read them out
+            if (it == 0 && hh == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, kWaitNs)) {
+              failed = true;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t aSh = adSt + hh * HALF_BYTES;  // dS^T_h: [128 keys][64 queries]
+            const bool acc0 = it > 0 || hh > 0;
+#pragma unroll
+            for (int k = 0; k < TILE / 16; ++k) {
+              if (k < 4) {
+                tc::mma_bf16_tmem_a(tdV, tS + 64 * hh + k * 8, desc_mn(adO + 8192 * hh, k), id_kmn,
+                                    (acc0 || k > 0) ? 1u : 0u);
+                tc::mma_bf16(tdK, tc::sdesc_sw128(aSh + k * 32, 16, 1024), desc_mn(aQ + 8192 * hh, k), id_kmn,
+                             (acc0 || k > 0) ? 1u : 0u);
+              }
+              tc::mma_bf16(tdP + 64 * hh, desc_mn(aK, k), tc::sdesc_sw128(aSh + k * 2048, HALF_BYTES, 1024),
+                           id_mnmn_n64, k > 0 ? 1u : 0u);
+            }
+            tc::mma_commit(dq_full + hh);
+          }
+          if (failed) break;
           tc::mma_commit(q_empty + s);
         }
         if (failed) break;
@@ -577,8 +602,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   } else {
     // ---------------------------------------------------------------- softmax / epilogue warps
     const int q4 = warp & 3;
-    const int ch = (warp - 2) >> 2;  // query-column half owned by this warp
-    const int r = q4 * 32 + lane;    // key row of this CTA (and query row of the dQ tile)
+    const int ch = (warp - 2) >> 2;  // the 64-query half this warp works on
+    const int r = q4 * 32 + lane;    // key row of this CTA (TMEM lane; a head dimension for dQ^T)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = kLog2e * rsqrtf(128.f);
     const float scale = rsqrtf(128.f);
@@ -599,9 +624,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       for (int it = 0; it < u.nit; ++it, ++g) {
         const int qt = u.kt + it;
         const int s = g & 1;
-        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // lse of this warp's 64 query columns
+        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // lse of this half's 64 query columns
         const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
-        bool ok = tc::mbar_wait(st_full, g & 1, abort_flag, kWaitNs);
+        bool ok = tc::mbar_wait(st_full + ch, g & 1, abort_flag, kWaitNs);
         // the lse / D rows arrived with this tile's Q (already complete here)
         ok = ok && tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
@@ -643,35 +668,34 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         fence_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(p_full);
-        ok = tc::mbar_wait(dq_full, g & 1, abort_flag, kWaitNs);
+        tc::mbar_arrive(p_full + ch);
+        ok = tc::mbar_wait(dq_full + ch, g & 1, abort_flag, kWaitNs);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         tc::tc_fence_after();
-        // dQ rows q4*32.. (queries qt*128 + q4*32 + lane), this warp's 64
-        // columns as two 32 x 32 fp32 chunks, each staged in the (now free) dS^T
-        // block and added to the dq plane by a bulk tensor reduce-add
+        // dQ^T of this half: TMEM lane = head dim 32*q4 + lane, column = query
         float vq[64];
-        tc::tmem_ld32x2(tdQ + lane_off + ch * 64, tdQ + lane_off + ch * 64 + 32, vq, vq + 32);
-        // dQ is in registers: its TMEM columns may take the next dP^T at once,
+        tc::tmem_ld32x2(tdP + lane_off + ch * 64, tdP + lane_off + ch * 64 + 32, vq, vq + 32);
+        // dQ^T is in registers: its TMEM columns may take the next dP^T at once,
         // while the staging and reduce-adds below proceed off that path
         tc::tc_fence_before();
-        tc::mbar_arrive(tm_free);
+        tc::mbar_arrive(tm_free + ch);
+        // two [32 queries x 32 dims] fp32 chunks, each staged transposed in this
+        // warp's (now free) dS^T block and added to the dq plane by a bulk
+        // tensor reduce-add
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const float* vv = vq + c * 32;
-          if (c > 0) {
+        for (int rr = 0; rr < 2; ++rr) {
+          if (rr > 0) {
             if (lane == 0) tc::bulk_wait_read();
             __syncwarp();
           }
 #pragma unroll
-          for (int gq = 0; gq < 8; ++gq)
-            *reinterpret_cast<float4*>(blk + lane * 128 + ((gq ^ (lane & 7)) << 4)) =
-                make_float4(vv[gq * 4] * scale, vv[gq * 4 + 1] * scale, vv[gq * 4 + 2] * scale,
-                            vv[gq * 4 + 3] * scale);
+          for (int q = 0; q < 32; ++q)
+            *reinterpret_cast<float*>(blk + q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4) =
+                vq[rr * 32 + q] * scale;
           fence_async_smem();
           __syncwarp();
           if (lane == 0) {
-            tc::tma_reduce_add_2d(&tdq, blk, u.h * 128 + ch * 64 + c * 32, u.b * p.T + qt * TILE + q4 * 32);
+            tc::tma_reduce_add_2d(&tdq, blk, u.h * 128 + q4 * 32, u.b * p.T + qt * TILE + ch * 64 + rr * 32);
             tc::bulk_commit();
           }
         }
