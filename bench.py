@@ -369,7 +369,7 @@ def our_arm(args):
             "config": {"workload": workload_desc(w), "global_batch": w.batch * ws, "seq_len": w.seq_len,
                        "tokens_per_step": M * ws,
                        "parallelism": f"{ws} independent data-parallel replicas (no collective)",
-                       "l2": "inputs larger than L2: the step streams a ~27 GB activation stash"},
+                       "l2": "inputs larger than L2: the step streams a ~17 GB activation stash"},
             "mfu": mfu, "mfu_peak_tflops": pk["bf16_tflops"],
             "mfu_vs_sustained": value * fpt / (ws * pk["bf16_tflops_sustained"] * 1e12),
             "model_flops_per_token": fpt,

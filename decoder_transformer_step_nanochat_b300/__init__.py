@@ -38,6 +38,7 @@ NC_EPI_RELU2_BWD = 3
 NC_EPI_CE_BWD = 4
 NC_EPI_QKNORM_ROPE = 6
 NC_EPI_AXPBY = 7
+NC_EPI_RELU2A = 8
 
 STATUS = {0: "NC_OK", 1: "NC_ERR_ARG", 2: "NC_ERR_STATE", 3: "NC_ERR_CUDA",
           4: "NC_ERR_TIMEOUT", 5: "NC_ERR_DEVICE", 6: "NC_ERR_UNSUPPORTED"}

@@ -90,9 +90,14 @@ __global__ void __launch_bounds__(256) gemm_simt_k(GemmArgs g) {
           stf(static_cast<T*>(g.C2) + c2_off + (size_t)m * g.ldc2 + n, u * u);
           break;
         }
-        case EPI_RELU2_BWD: {
-          float u = ldf(static_cast<const T*>(g.C2) + c2_off + (size_t)m * g.ldc2 + n);
-          stf(static_cast<T*>(g.C) + ci, v * 2.f * fmaxf(u, 0.f));
+        case EPI_RELU2_BWD: {  // C2 holds a = relu(u)^2, so relu(u) = sqrt(a)
+          float a = ldf(static_cast<const T*>(g.C2) + c2_off + (size_t)m * g.ldc2 + n);
+          stf(static_cast<T*>(g.C) + ci, v * 2.f * sqrtf(fmaxf(a, 0.f)));
+          break;
+        }
+        case EPI_RELU2A: {
+          float u = fmaxf(v, 0.f);
+          stf(static_cast<T*>(g.C) + ci, u * u);
           break;
         }
         case EPI_CE_BWD: {

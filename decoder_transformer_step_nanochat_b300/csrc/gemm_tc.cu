@@ -142,7 +142,7 @@ __device__ __forceinline__ void epi_chunk(const GemmArgs& g, int m, int nc0, flo
         float uf[8], o[8];
         unpack8_bf16(*reinterpret_cast<const uint4*>(u + 8 * j), uf);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) o[i] = v[8 * j + i] * 2.f * fmaxf(uf[i], 0.f);
+        for (int i = 0; i < 8; ++i) o[i] = v[8 * j + i] * 2.f * tc::sqrt_approx(fmaxf(uf[i], 0.f));
         *reinterpret_cast<uint4*>(c + 8 * j) = pack8_bf16(o);
       }
     }
@@ -489,8 +489,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 8; ++i) uf[i] = 0.f;
 #pragma unroll
-                  for (int i = 0; i < 8; ++i) w[8 * j + i] *= 2.f * fmaxf(uf[i], 0.f);
+                  // C2 holds a = relu(u)^2, so relu(u) = sqrt(a)
+                  for (int i = 0; i < 8; ++i) w[8 * j + i] *= 2.f * tc::sqrt_approx(fmaxf(uf[i], 0.f));
                 }
+              }
+            } else if (EPI == EPI_RELU2A) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) {
+                const float uu = fmaxf(w[i], 0.f);
+                w[i] = uu * uu;
               }
             } else if (EPI == EPI_CE_BWD) {
               if (row_ok) {
@@ -633,6 +640,7 @@ KernFn pick_kernel(int epi, int a_mn, int b_mn) {
     case EPI_CE_FWD: return pick<EPI_CE_FWD, CL>(a_mn, b_mn);
     case EPI_QKNORM_ROPE: return pick<EPI_QKNORM_ROPE, CL>(a_mn, b_mn);
     case EPI_AXPBY: return pick<EPI_AXPBY, CL>(a_mn, b_mn);
+    case EPI_RELU2A: return pick<EPI_RELU2A, CL>(a_mn, b_mn);
     default: return nullptr;
   }
 }
@@ -694,7 +702,7 @@ bool gemm_tc_supports(const GemmArgs& g) {
   if (g.epi == EPI_QKNORM_ROPE &&
       (!g.rope_cos || !g.rope_sin || !g.rqk || g.seq_len < 1 || g.d_model % 128 || g.N != 3 * g.d_model))
     return false;
-  return g.epi >= EPI_STORE && g.epi <= EPI_AXPBY;
+  return g.epi >= EPI_STORE && g.epi <= EPI_RELU2A;
 }
 
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {

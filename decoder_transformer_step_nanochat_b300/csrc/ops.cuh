@@ -14,11 +14,12 @@ enum Epi : int {
   EPI_STORE = 0,       // C (elem) = alpha*acc
   EPI_STORE_F32 = 1,   // C (f32)  = alpha*acc + beta*C
   EPI_RELU2 = 2,       // C (elem) = u = alpha*acc ; C2 (elem) = max(u,0)^2
-  EPI_RELU2_BWD = 3,   // C (elem) = alpha*acc * 2*max(u,0), u read from C2
+  EPI_RELU2_BWD = 3,   // C (elem) = alpha*acc * 2*sqrt(a), a = relu(u)^2 read from C2
   EPI_CE_BWD = 4,      // C (elem) = (exp(alpha*acc - row_f[m]) - (n == row_i[m])) * s, s = *dscale (0 if row_i[m] < 0)
   EPI_CE_FWD = 5,      // per (row, 128-column tile) softmax partials (tensor-core path)
   EPI_QKNORM_ROPE = 6, // C (elem) = qkv with per-head RMSNorm + RoPE on the q,k columns
   EPI_AXPBY = 7,       // C (elem) = alpha*acc + beta*C2 (C2 elem, same shape as C)
+  EPI_RELU2A = 8,      // C (elem) = max(alpha*acc, 0)^2 only (the step keeps a, not u)
 };
 
 struct GemmArgs {

@@ -83,7 +83,7 @@ struct nc_ctx {
   int ce_tiles = 0;         // 128-wide vocabulary tiles (tensor-core CE partials)
   size_t partial_bytes = 0; // split-K partial sums of the weight-gradient GEMMs
   struct Off {
-    size_t xn1, r1, qkv, rqk, o, lse_att, xn2, r2, u, a;  // per-layer stash (stride below)
+    size_t xn1, r1, qkv, rqk, o, lse_att, xn2, r2, a;  // per-layer stash (stride below)
     size_t layer_stride;
     size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
     size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial, inv_count;
@@ -189,7 +189,6 @@ void plan_workspace(nc_ctx* c) {
   f.lse_att = take(M * H * 4);
   f.xn2 = take(M * d * e);
   f.r2 = take(M * 4);
-  f.u = take(M * F * e);
   f.a = take(M * F * e);
   f.layer_stride = o;
   o = f.layer_stride * c->L;
@@ -414,7 +413,6 @@ nc_status forward_blocks(nc_ctx* c, const T* P, const int* tok) {
     float* lse_att = wsp<float>(c, lb + c->off.lse_att);
     T* xn2 = wsp<T>(c, lb + c->off.xn2);
     float* r2 = wsp<float>(c, lb + c->off.r2);
-    T* u = wsp<T>(c, lb + c->off.u);
     T* a = wsp<T>(c, lb + c->off.a);
     const T* Wqkv = P + param_offset(c, 1 + 4 * l, &rows, &cols);
     const T* Wo = P + param_offset(c, 2 + 4 * l, &rows, &cols);
@@ -435,9 +433,8 @@ nc_status forward_blocks(nc_ctx* c, const T* P, const int* tok) {
     KL(NC_FAM_ATTN_FWD, attn_fwd_flops(c), 1, attn_fwd<T>(c, qkv, o, lse_att));
     CKS(gemm(c, mk(M, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
     KL(NC_FAM_ROWS, (double)M * d * (4 + sizeof(T)) + 4.0 * M, 1, rmsnorm_fwd<T>(x, xn2, r2, M, d, s));
-    GemmArgs up = mk(M, F, d, xn2, d, 1, Wfc, d, 1, EPI_RELU2, u, F);
-    up.C2 = a; up.ldc2 = F;
-    CKS(gemm(c, up));
+    // a = relu(u)^2 only: the backward recovers relu(u) as sqrt(a)
+    CKS(gemm(c, mk(M, F, d, xn2, d, 1, Wfc, d, 1, EPI_RELU2A, a, F)));
     CKS(gemm(c, mk(M, d, F, a, F, 1, Wproj, F, 1, EPI_STORE_F32, x, d, 1.f, 1.f)));
   }
   T* hf = wsp<T>(c, c->off.hf);
@@ -489,7 +486,6 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     const float* lse_att = wsp<float>(c, lb + c->off.lse_att);
     const T* xn2 = wsp<T>(c, lb + c->off.xn2);
     const float* r2 = wsp<float>(c, lb + c->off.r2);
-    T* u = wsp<T>(c, lb + c->off.u);
     const T* a = wsp<T>(c, lb + c->off.a);
     size_t oq = param_offset(c, 1 + 4 * l, &rows, &cols);
     size_t oo = param_offset(c, 2 + 4 * l, &rows, &cols);
@@ -498,7 +494,7 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     // MLP: x += relu2(xn2 Wfc^T) Wproj^T
     CKS(gemm(c, mk(d, F, M, dxe, d, 0, a, F, 0, EPI_STORE_F32, G + op, F)));
     GemmArgs g1 = mk(M, F, d, dxe, d, 1, P + op, F, 0, EPI_RELU2_BWD, du, F);
-    g1.C2 = u; g1.ldc2 = F;
+    g1.C2 = const_cast<T*>(a); g1.ldc2 = F;  // relu(u) = sqrt(a)
     CKS(gemm(c, g1));
     CKS(gemm(c, mk(F, d, M, du, F, 0, xn2, d, 0, EPI_STORE_F32, G + of, d)));
     CKS(gemm(c, mk(M, d, F, du, F, 1, P + of, d, 0, sizeof(T) == 4 ? EPI_STORE_F32 : EPI_STORE, dy, d)));
@@ -964,7 +960,7 @@ nc_status nc_op_gemm(nc_ctx* c, int M, int N, int K, const void* A, long long ld
                      const int32_t* row_i) {
   if (!c || c->prec < 0) return fail(NC_ERR_STATE, "context not configured");
   if (M < 0 || N < 0 || K < 0) return fail(NC_ERR_ARG, "negative size");
-  if (epi < EPI_STORE || epi > EPI_AXPBY || epi == EPI_CE_FWD)
+  if (epi < EPI_STORE || epi > EPI_RELU2A || epi == EPI_CE_FWD)
     return fail(NC_ERR_ARG, "epilogue %d not available here", epi);
   if (epi == EPI_QKNORM_ROPE && (!c->use_tc || N != 3 * c->d || M != c->M || !C2))
     return fail(NC_ERR_ARG, "the QK-norm + RoPE epilogue needs NC_BF16, N = 3*d_model, M = batch*seq_len and C2 = rqk");

@@ -92,6 +92,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Square root on the special-function unit (the PTX approximate square
+// root; its relative error is far below a bf16 ulp, which is all the
+// epilogues that use it keep).
+__device__ __forceinline__ float sqrt_approx(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // As tma_load_2d, but the tile lands at the same shared-memory offset in
 // every CTA of the cluster named by `mask` and completes bytes on the
 // mbarrier at the same offset in each of them.

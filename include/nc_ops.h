@@ -24,13 +24,15 @@ enum {
   NC_EPI_STORE = 0,      /* C (elem) = alpha * acc                                  */
   NC_EPI_STORE_F32 = 1,  /* C (fp32) = alpha * acc + beta * C                       */
   NC_EPI_RELU2 = 2,      /* C (elem) = u = alpha * acc ; C2 (elem) = max(u, 0)^2    */
-  NC_EPI_RELU2_BWD = 3,  /* C (elem) = alpha * acc * 2 * max(u, 0), u read from C2  */
+  NC_EPI_RELU2_BWD = 3,  /* C (elem) = alpha * acc * 2 * sqrt(a), a = max(u, 0)^2
+                            read from C2 (relu(u) recovered from the stored a)      */
   NC_EPI_CE_BWD = 4,     /* C (elem) = exp(alpha*acc - row_f[m]) - (n == row_i[m])  */
   NC_EPI_QKNORM_ROPE = 6, /* NC_BF16 only; the QKV projection with QK-norm + RoPE:
                             M = batch*seq_len, N = 3*d_model; C (elem [M, 3d]) gets
                             q, k heads RMS-normalised and rotated (position m % seq_len)
                             and v heads as computed; C2 = fp32 rqk [M, 2H]          */
-  NC_EPI_AXPBY = 7       /* C (elem) = alpha * acc + beta * C2 (elem, ldc2)          */
+  NC_EPI_AXPBY = 7,      /* C (elem) = alpha * acc + beta * C2 (elem, ldc2)          */
+  NC_EPI_RELU2A = 8      /* C (elem) = max(alpha * acc, 0)^2 (a alone, no u)         */
 };
 
 /* Linear-layer contraction of the step (the QKV, out-projection, MLP and

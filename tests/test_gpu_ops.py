@@ -56,7 +56,7 @@ M_, N_, K_ = 304, 520, 200  # 2 full 128-row tiles + 48, 2 full 256-col tiles + 
 
 @pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
 @pytest.mark.parametrize("ak,bk", [(1, 1), (1, 0), (0, 0), (0, 1)], ids=["TN", "NN_b", "MN_ab", "MN_a"])
-@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4], ids=["store", "store_f32", "relu2", "relu2_bwd", "ce_bwd"])
+@pytest.mark.parametrize("epi", [0, 1, 2, 3, 4, 8], ids=["store", "store_f32", "relu2", "relu2_bwd", "ce_bwd", "relu2a"])
 def test_gemm_epilogues(nc, prec, ak, bk, epi):
     import torch
     rng = np.random.default_rng(100 + 10 * ak + bk + 3 * epi)
@@ -90,9 +90,12 @@ def test_gemm_epilogues(nc, prec, ak, bk, epi):
             ref = u
             ref2 = np.square(np.maximum(u, 0))  # the kernel squares the fp32 u, then rounds
         elif epi == 3:
-            u_in = rounded(rng.standard_normal((M_, N_)), prec)
-            C2 = torch_of(u_in, prec, nc)
-            ref = alpha * acc * 2 * np.maximum(u_in, 0)
+            # C2 holds a = relu(u)^2 (what the forward keeps); relu(u) = sqrt(a)
+            a_in = rounded(np.square(np.maximum(rng.standard_normal((M_, N_)), 0)), prec)
+            C2 = torch_of(a_in, prec, nc)
+            ref = alpha * acc * 2 * np.sqrt(a_in)
+        elif epi == 8:
+            ref = np.square(np.maximum(alpha * acc, 0))  # a only
         elif epi == 4:
             lse = np.log(np.sum(np.exp(alpha * acc), axis=1)).astype(np.float32)
             tgt = rng.integers(0, N_, M_).astype(np.int32)
@@ -111,6 +114,8 @@ def test_gemm_epilogues(nc, prec, ak, bk, epi):
             ok, err = close_enough(host(C2), ref2, prec)
             assert ok, err
             assert np.all(host(C2)[host(C) <= 0] == 0.0)  # exact zeros of ReLU^2
+        if epi == 8:
+            assert np.all(host(C)[alpha * acc <= 0] == 0.0)
     finally:
         c.close()
 
