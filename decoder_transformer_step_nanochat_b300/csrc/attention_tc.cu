@@ -34,6 +34,7 @@ constexpr int TILE_BYTES = 2 * HALF_BYTES;    // 32 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kSqrt128 = 11.313708498984761f;
 
 __device__ __forceinline__ uint64_t desc_k(uint32_t base, int kstep) {
   return tc::sdesc_sw128(base + (kstep >> 2) * HALF_BYTES + (kstep & 3) * 32, 16, 1024);
@@ -89,7 +90,8 @@ struct AttnParams {
   int B, T, H, nq;
   const bf16* qkv;  // backward: k_hat rows for the in-kernel QK-norm/RoPE backward of k
   bf16* o;        // forward output
-  float* lse;     // forward output / backward input
+  float* lse;     // forward output
+  const float* L2row;  // backward: lse * log2(e) + 3.5 per (b, h, t) (base 2, score scale folded in)
   const float* Drow;
   float* dq;      // backward: fp32 [B*T, d], accumulated with atomics (pre-zeroed)
   float* dk;      // backward: fp32 [B*T, d] (dk_hat), unless the k half is finished in-kernel
@@ -359,23 +361,31 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 // query columns 0-63 of each query tile and warps 6-9 on columns 64-127, one
 // key row per thread (TMEM lane).
 //
-// TMEM: S^T [0,128) and dP^T [128,256), each as two 64-query halves; P^T of
-// half h is written back packed (bf16 pairs) over the first 32 columns of its
-// S^T half and feeds dV from TMEM; dQ^T of half h (= K^T dS^T_h, head
-// dimension in the TMEM lane) replaces its dP^T half; dV [256,384) and dK
-// [384,512) accumulate over the unit. Shared memory: K, V, two Q/dO stages
-// (the next query tile loads while this one computes, across units too) and
-// dS^T, whose 4 KB block of each warp also stages that warp's dQ reduce-adds.
+// TMEM: S^T [0,128) and dP^T [128,256) of one 128-query tile; the P^T of
+// query half h is written back packed (bf16 pairs) over columns 64h..64h+31
+// of S^T and feeds dV from TMEM; dQ^T (= K^T dS^T, head dimension in the
+// TMEM lane) replaces dP^T; dV [256,384) and dK [384,512) accumulate over the
+// unit. Shared memory: K, V, two Q/dO stages (the next query tile loads while
+// this one computes, across units too) and dS^T. Once a tile's products are
+// complete its Q/dO stage (64 KB) stages the tile's dQ for the reduce-adds,
+// and the softmax warps, not the tensor cores, hand the stage back to the
+// producer when those have read it.
 //
-// Per query tile and half h: S^T_h = K Q_h^T and dP^T_h = V dO_h^T
-// (interleaved); P^T_h = exp(S^T_h - lse), dS^T_h = P^T_h (dP^T_h - D) by
-// that half's warps; then dV += P^T_h dO_h, dK += dS^T_h Q_h and dQ^T_h, their
-// k-steps interleaved. One half's softmax thus runs while the tensor cores
-// work on the other half. dQ^T_h is read out (its TMEM columns released at
-// once), staged transposed and added to the fp32 dq plane with bulk tensor
-// reduce-adds. Between units, the next K/V load as soon as the finished
-// unit's products are done and its first query tile runs while the epilogue
-// warps drain dV/dK; only its first dV/dK products wait for that drain.
+// Per query tile: S^T = K Q^T and dP^T = V dO^T, two accumulator chains of
+// 128x128x16 products interleaved; P'^T = exp2(S^T log2(e)/sqrt(128) - L2)
+// and dS'^T = P'^T (dP^T - D) by the softmax warps, where L2 = lse log2(e) +
+// 3.5 makes P' = P/sqrt(128), so dS' = dS/sqrt(128) already carries the score
+// scale of dQ and dK (dV, accumulated from P', is multiplied back by sqrt(128)
+// once per unit); then dV += P'^T dO, dK += dS'^T Q and dQ^T = K^T dS'^T as
+// three interleaved chains. The tensor cores keep a single accumulator chain
+// of small products far below their rate (each product waits on the previous
+// one), so every phase runs two or three independent chains of N = 128
+// products. dQ^T is read out (its TMEM columns released at once), staged
+// transposed and added to the fp32 dq plane with one bulk tensor reduce-add
+// per warp, without waiting for it.
+// Between units, the next K/V load as soon as the finished unit's products are
+// done and its first query tile runs while the epilogue warps drain dV/dK;
+// only its first dV/dK products wait for that drain.
 
 constexpr int BWD_WARPS = 10;
 constexpr int BWD_THREADS = 32 * BWD_WARPS;
@@ -414,11 +424,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* kv_empty = bars + 1;
   uint64_t* q_full = bars + 2;    // [2]
-  uint64_t* q_empty = bars + 4;   // [2]
-  uint64_t* st_full = bars + 6;   // [2]: per 64-query half
-  uint64_t* p_full = bars + 8;    // [2]
-  uint64_t* dq_full = bars + 10;  // [2]
-  uint64_t* tm_free = bars + 12;  // [2]
+  uint64_t* q_empty = bars + 4;   // [2]: the stage's dq staging was read (one arrival per softmax warp)
+  uint64_t* st_full = bars + 6;   // S^T and dP^T of the query tile complete
+  uint64_t* p_full = bars + 8;    // P^T in TMEM and dS^T in shared memory (all softmax threads)
+  uint64_t* dq_full = bars + 10;  // dV, dK, dQ^T products of the tile complete
+  uint64_t* tm_free = bars + 12;  // dQ^T read out of TMEM (all softmax threads)
   uint64_t* acc_full = bars + 14;
   uint64_t* acc_free = bars + 15;
   uint64_t* drain = bars + 16;
@@ -438,14 +448,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tc::mbar_init(kv_empty, 1);
     for (int s = 0; s < 2; ++s) {
       tc::mbar_init(q_full + s, 1);
-      tc::mbar_init(q_empty + s, 1);
+      tc::mbar_init(q_empty + s, BWD_SOFT / 32);
     }
-    for (int hh = 0; hh < 2; ++hh) {
-      tc::mbar_init(st_full + hh, 1);
-      tc::mbar_init(p_full + hh, BWD_SOFT / 2);   // the four warps of that half
-      tc::mbar_init(dq_full + hh, 1);
-      tc::mbar_init(tm_free + hh, BWD_SOFT / 2);
-    }
+    tc::mbar_init(st_full, 1);
+    tc::mbar_init(p_full, BWD_SOFT);
+    tc::mbar_init(dq_full, 1);
+    tc::mbar_init(tm_free, BWD_SOFT);
     tc::mbar_init(acc_full, 1);
     tc::mbar_init(acc_free, BWD_SOFT);
     tc::mbar_init(drain, 1);
@@ -460,9 +468,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_holder;
-  // S^T and dP^T halves: query half h at columns 64h of each region; P^T of
-  // half h is packed over the first 32 columns of its S^T half; dQ^T of half
-  // h replaces its dP^T half once the softmax has read it
+  // S^T and dP^T: query column c at column c of each region; the P^T of
+  // query half h (columns 64h..64h+63) is packed over columns 64h..64h+31 of
+  // S^T; dQ^T (head dimension in the lane, query in the column) replaces dP^T
+  // once the softmax has read it
   const uint32_t tS = tmem, tdP = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
   bool failed = false;
 
@@ -506,7 +515,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           const int qr = u.b * p.T + (u.kt + it) * TILE;
           const size_t lrow = ((size_t)u.b * p.H + u.h) * p.T + (size_t)(u.kt + it) * TILE;
           tc::mbar_arrive_expect_tx(q_full + s, 2 * TILE_BYTES + 2 * TILE * 4);
-          tc::bulk_load(sLD + s * 2 * TILE, p.lse + lrow, TILE * 4, q_full + s);
+          tc::bulk_load(sLD + s * 2 * TILE, p.L2row + lrow, TILE * 4, q_full + s);
           tc::bulk_load(sLD + s * 2 * TILE + TILE, p.Drow + lrow, TILE * 4, q_full + s);
           tc::tma_load_2d(sQ + s * TILE_BYTES, &tqkv, u.h * 128, qr, q_full + s);
           tc::tma_load_2d(sQ + s * TILE_BYTES + HALF_BYTES, &tqkv, u.h * 128 + 64, qr, q_full + s);
@@ -527,9 +536,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t id_n64 = tc::idesc_bf16(128, 64, 0, 0);       // S^T_h, dP^T_h: both K-major
-      const uint32_t id_kmn = tc::idesc_bf16(128, 128, 0, 1);      // dV, dK: B MN-major
-      const uint32_t id_mnmn_n64 = tc::idesc_bf16(128, 64, 1, 1);  // dQ^T_h: A and B MN-major
+      const uint32_t id_kk = tc::idesc_bf16(128, 128, 0, 0);    // S^T, dP^T: both K-major
+      const uint32_t id_kmn = tc::idesc_bf16(128, 128, 0, 1);   // dV, dK: B MN-major
+      const uint32_t id_mnmn = tc::idesc_bf16(128, 128, 1, 1);  // dQ^T: A and B MN-major
       const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), adSt = tc::smem_u32(sdSt);
       bool any = false;
       int g = 0, ul = 0;
@@ -542,50 +551,40 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           const int s = g & 1;
           const uint32_t aQ = tc::smem_u32(sQ + s * TILE_BYTES), adO = tc::smem_u32(sdO + s * TILE_BYTES);
           if (!tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          // S^T_h = K Q_h^T and dP^T_h = V dO_h^T for the two 64-query halves
-          // (rows 64h.. of the Q / dO tiles), each pair interleaved
-          for (int hh = 0; hh < 2 && !failed; ++hh) {
-            // dP^T_h replaces dQ^T_h of the previous tile: wait until it was read
-            // out (S^T_h replaces P^T_h, whose reader dV_h was issued earlier)
-            if (g > 0 && !tc::mbar_wait(tm_free + hh, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
-            tc::tc_fence_after();
+          // dP^T replaces dQ^T of the previous tile: wait until it was read out
+          // (S^T replaces P^T, whose reader dV was issued before, and tcgen05
+          // products of one thread run in issue order)
+          if (g > 0 && !tc::mbar_wait(tm_free, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          tc::tc_fence_after();
+          // S^T = K Q^T and dP^T = V dO^T over the whole 128-query tile: two
+          // independent accumulator chains, interleaved
 #pragma unroll
-            for (int k = 0; k < TILE / 16; ++k) {
-              tc::mma_bf16(tS + 64 * hh, desc_k(aK, k), desc_k(aQ + 8192 * hh, k), id_n64, k > 0 ? 1u : 0u);
-              tc::mma_bf16(tdP + 64 * hh, desc_k(aV, k), desc_k(adO + 8192 * hh, k), id_n64, k > 0 ? 1u : 0u);
-            }
-            any = true;
-            tc::mma_commit(st_full + hh);
+          for (int k = 0; k < TILE / 16; ++k) {
+            tc::mma_bf16(tS, desc_k(aK, k), desc_k(aQ, k), id_kk, k > 0 ? 1u : 0u);
+            tc::mma_bf16(tdP, desc_k(aV, k), desc_k(adO, k), id_kk, k > 0 ? 1u : 0u);
           }
-          if (failed) break;
-          // per half: dV += P^T_h dO_h (P^T_h from TMEM), dK += dS^T_h Q_h and
-          // dQ^T_h = K^T dS^T_h (into the dP^T_h columns), interleaved
-          for (int hh = 0; hh < 2 && !failed; ++hh) {
-            if (!tc::mbar_wait(p_full + hh, g & 1, abort_flag, kWaitNs)) { failed = true; break; }
-            // the first dV/dK of a unit overwrite the accumulators of the previous
-            // one: wait until the epilogue warps have read them out
-            if (it == 0 && hh == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, kWaitNs)) {
-              failed = true;
-              break;
-            }
-            tc::tc_fence_after();
-            const uint32_t aSh = adSt + hh * HALF_BYTES;  // dS^T_h: [128 keys][64 queries]
-            const bool acc0 = it > 0 || hh > 0;
+          any = true;
+          tc::mma_commit(st_full);
+          if (!tc::mbar_wait(p_full, g & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          // the first dV/dK of a unit overwrite the accumulators of the previous
+          // one: wait until the epilogue warps have read them out
+          if (it == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, kWaitNs)) {
+            failed = true;
+            break;
+          }
+          tc::tc_fence_after();
+          // dV += P^T dO (P^T from TMEM), dK += dS^T Q and dQ^T = K^T dS^T (into
+          // the dP^T columns): three chains, their k-steps (16 queries for dV
+          // and dK, 16 keys for dQ^T) interleaved
+          const bool acc0 = it > 0;
 #pragma unroll
-            for (int k = 0; k < TILE / 16; ++k) {
-              if (k < 4) {
-                tc::mma_bf16_tmem_a(tdV, tS + 64 * hh + k * 8, desc_mn(adO + 8192 * hh, k), id_kmn,
-                                    (acc0 || k > 0) ? 1u : 0u);
-                tc::mma_bf16(tdK, tc::sdesc_sw128(aSh + k * 32, 16, 1024), desc_mn(aQ + 8192 * hh, k), id_kmn,
-                             (acc0 || k > 0) ? 1u : 0u);
-              }
-              tc::mma_bf16(tdP + 64 * hh, desc_mn(aK, k), tc::sdesc_sw128(aSh + k * 2048, HALF_BYTES, 1024),
-                           id_mnmn_n64, k > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(dq_full + hh);
+          for (int k = 0; k < TILE / 16; ++k) {
+            tc::mma_bf16_tmem_a(tdV, tS + 64 * (k >> 2) + (k & 3) * 8, desc_mn(adO, k), id_kmn,
+                                (acc0 || k > 0) ? 1u : 0u);
+            tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (acc0 || k > 0) ? 1u : 0u);
+            tc::mma_bf16(tdP, desc_mn(aK, k), desc_mn(adSt, k), id_mnmn, k > 0 ? 1u : 0u);
           }
-          if (failed) break;
-          tc::mma_commit(q_empty + s);
+          tc::mma_commit(dq_full);
         }
         if (failed) break;
         tc::mma_commit(acc_full);  // dV, dK of this unit complete
@@ -606,10 +605,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int r = q4 * 32 + lane;    // key row of this CTA (TMEM lane; a head dimension for dQ^T)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const float sl2 = kLog2e * rsqrtf(128.f);
-    const float scale = rsqrtf(128.f);
-    // this warp's 4 KB block of the dS^T tile (its rows, its column half) is
-    // also its staging buffer for the dQ bulk reduce-adds
-    uint8_t* blk = sdSt + ch * HALF_BYTES + q4 * 32 * 128;
+    // this warp's 8 KB staging block for its dQ bulk reduce-add: [64 queries
+    // x 32 dims] fp32 in the query tile's own Q (ch = 0) or dO (ch = 1) stage,
+    // which the tile's products no longer read once dQ^T is complete
+    const uint32_t stg_off = (ch ? 2 * TILE_BYTES : 0) + q4 * 8192;
     int g = 0, ul = 0;
     for (;; ++ul) {
       // the first query tile of the next unit (or the end marker) is announced
@@ -624,40 +623,43 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       for (int it = 0; it < u.nit; ++it, ++g) {
         const int qt = u.kt + it;
         const int s = g & 1;
-        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // lse of this half's 64 query columns
+        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // base-2 lse of this half's 64 query columns
         const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
-        bool ok = tc::mbar_wait(st_full + ch, g & 1, abort_flag, kWaitNs);
+        bool ok = tc::mbar_wait(st_full, g & 1, abort_flag, kWaitNs);
         // the lse / D rows arrived with this tile's Q (already complete here)
         ok = ok && tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         tc::tc_fence_after();
-        // the previous tile's dQ reduce-adds must have read the block first
-        if (lane == 0) tc::bulk_wait_read();
-        __syncwarp();
         const bool diag = (it == 0);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           float sv[32], dp[32];
           tc::tmem_ld32x2(tS + lane_off + ch * 64 + c * 32, tdP + lane_off + ch * 64 + c * 32, sv, dp);
+          // P' = exp2(S * log2(e)/sqrt(128) - L2) = P / sqrt(128): the score
+          // scale rides on P' into dS' = P' (dP - D) = dS / sqrt(128)
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
             const float4 l0 = *reinterpret_cast<const float4*>(Lq + c * 32 + gq * 8);
             const float4 l1 = *reinterpret_cast<const float4*>(Lq + c * 32 + gq * 8 + 4);
+            const float Lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sv[gq * 8 + i] = tc::ex2(fmaf(sv[gq * 8 + i], sl2, -Lv[i]));
+          }
+          if (diag) {  // the diagonal tile: query q sees key r only if q >= r
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (ch * 64 + c * 32 + i < r) sv[i] = 0.f;
+          }
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
             const float4 d0 = *reinterpret_cast<const float4*>(Dq + c * 32 + gq * 8);
             const float4 d1 = *reinterpret_cast<const float4*>(Dq + c * 32 + gq * 8 + 4);
-            const float Lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
             const float Dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int qc = ch * 64 + c * 32 + gq * 8 + i;  // query column within the tile
-              float pr = tc::ex2(fmaf(sv[gq * 8 + i], sl2, -Lv[i] * kLog2e));
-              if (diag && qc < r) pr = 0.f;
-              sv[gq * 8 + i] = pr;
-              dp[gq * 8 + i] = pr * (dp[gq * 8 + i] - Dv[i]);
-            }
+            for (int i = 0; i < 8; ++i) dp[gq * 8 + i] = sv[gq * 8 + i] * (dp[gq * 8 + i] - Dv[i]);
             st_tile8(sdSt, r, ch * 8 + c * 4 + gq, pack8(dp + 8 * gq));
           }
-          // P^T of these 32 query columns -> 16 packed bf16 pairs in TMEM
+          // P'^T of these 32 query columns -> 16 packed bf16 pairs in TMEM
           float pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -668,36 +670,35 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         fence_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(p_full + ch);
-        ok = tc::mbar_wait(dq_full + ch, g & 1, abort_flag, kWaitNs);
+        tc::mbar_arrive(p_full);
+        // while the tensor cores run this tile's dV/dK/dQ: the previous tile's
+        // stage may take new Q/dO once this warp's dq reduce-add has read its
+        // staging block there
+        if (g > 0 && lane == 0) {
+          tc::bulk_wait_read();
+          tc::mbar_arrive(q_empty + (s ^ 1));
+        }
+        ok = tc::mbar_wait(dq_full, g & 1, abort_flag, kWaitNs);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         tc::tc_fence_after();
         // dQ^T of this half: TMEM lane = head dim 32*q4 + lane, column = query
         float vq[64];
         tc::tmem_ld32x2(tdP + lane_off + ch * 64, tdP + lane_off + ch * 64 + 32, vq, vq + 32);
         // dQ^T is in registers: its TMEM columns may take the next dP^T at once,
-        // while the staging and reduce-adds below proceed off that path
+        // while the staging and reduce-add below proceed off that path
         tc::tc_fence_before();
-        tc::mbar_arrive(tm_free + ch);
-        // two [32 queries x 32 dims] fp32 chunks, each staged transposed in this
-        // warp's (now free) dS^T block and added to the dq plane by a bulk
-        // tensor reduce-add
+        tc::mbar_arrive(tm_free);
+        // [64 queries x 32 dims] staged transposed (128-byte swizzle) and added
+        // to the dq plane by one bulk tensor reduce-add
+        uint8_t* blk = sQ + s * TILE_BYTES + stg_off;
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          if (rr > 0) {
-            if (lane == 0) tc::bulk_wait_read();
-            __syncwarp();
-          }
-#pragma unroll
-          for (int q = 0; q < 32; ++q)
-            *reinterpret_cast<float*>(blk + q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4) =
-                vq[rr * 32 + q] * scale;
-          fence_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tc::tma_reduce_add_2d(&tdq, blk, u.h * 128 + q4 * 32, u.b * p.T + qt * TILE + ch * 64 + rr * 32);
-            tc::bulk_commit();
-          }
+        for (int q = 0; q < 64; ++q)
+          *reinterpret_cast<float*>(blk + q * 128 + ((((lane >> 2) ^ q) & 7) << 4) + (lane & 3) * 4) = vq[q];
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tc::tma_reduce_add_2d(&tdq, blk, u.h * 128 + q4 * 32, u.b * p.T + qt * TILE + ch * 64);
+          tc::bulk_commit();
         }
       }
       if (failed) break;
@@ -711,7 +712,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (p.rqk) {
         // warp ch = 0 finishes dk for whole head rows; warp ch = 1 writes dv
         if (ch == 0) {
-          // dk_hat = scale * acc; dk_n = R^T dk_hat and k_n = R^T k_hat (k_hat
+          // dk_hat = acc (dS' carried the score scale); dk_n = R^T dk_hat and k_n = R^T k_hat (k_hat
           // read back from qkv); dk = rk * (dk_n - k_n * mean(dk_n * k_n)).
           // Pass 1 rotates 16 pairs at a time back into the dK columns of TMEM
           // and accumulates the dot; pass 2 finishes and stores.
@@ -755,7 +756,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                   const float kn1 = k1[i] * cc[i] + k2[i] * ss[i];
                   const float kn2 = -k1[i] * ss[i] + k2[i] * cc[i];
                   if (pass == 0) {
-                    const float a = g1[e] * scale, bb = g2[e] * scale;
+                    const float a = g1[e], bb = g2[e];
                     g1[e] = a * cc[i] + bb * ss[i];
                     g2[e] = -a * ss[i] + bb * cc[i];
                     dot += g1[e] * kn1 + g2[e] * kn2;
@@ -785,6 +786,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             float a[32], bb[32];
             tc::tmem_ld32x2(tdV + lane_off + c * 64, tdV + lane_off + c * 64 + 32, a, bb);
 #pragma unroll
+            for (int i = 0; i < 32; ++i) {  // dV accumulated P' = P / sqrt(128)
+              a[i] *= kSqrt128;
+              bb[i] *= kSqrt128;
+            }
+#pragma unroll
             for (int gq = 0; gq < 4; ++gq) {
               *reinterpret_cast<uint4*>(row + c * 64 + gq * 8) = pack8(a + 8 * gq);
               *reinterpret_cast<uint4*>(row + c * 64 + 32 + gq * 8) = pack8(bb + 8 * gq);
@@ -801,7 +807,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
           for (int gq = 0; gq < 8; ++gq)
             *reinterpret_cast<float4*>(dkrow + c * 32 + gq * 4) =
-                make_float4(vk[gq * 4] * scale, vk[gq * 4 + 1] * scale, vk[gq * 4 + 2] * scale, vk[gq * 4 + 3] * scale);
+                make_float4(vk[gq * 4], vk[gq * 4 + 1], vk[gq * 4 + 2], vk[gq * 4 + 3]);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] *= kSqrt128;
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) *reinterpret_cast<uint4*>(dvrow + c * 32 + gq * 8) = pack8(w + 8 * gq);
         }
@@ -873,7 +881,7 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
   return cudaGetLastError();
 }
 
-cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* Drow, float* dq,
+cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, const float* Drow, float* dq,
                         float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s, const float* rqk,
                         const float* rope_cos, const float* rope_sin) {
   if (!attn_tc_supports(T)) return cudaErrorNotSupported;
@@ -883,10 +891,10 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   if (!map_rows(&tq, qkv, 3ull * H * 128, (uint64_t)B * T)) return cudaErrorInvalidValue;
   if (!map_rows(&tdo, dout, 1ull * H * 128, (uint64_t)B * T)) return cudaErrorInvalidValue;
   {
-    // dq fp32 [B*T, d]: 32 x 32 boxes, 128-byte swizzle (the staging layout)
+    // dq fp32 [B*T, d]: 32-dim x 64-query boxes, 128-byte swizzle (the staging layout)
     cuuint64_t dims[2] = {(uint64_t)H * 128, (uint64_t)B * T};
     cuuint64_t strides[1] = {(uint64_t)H * 128 * 4};
-    cuuint32_t box[2] = {32, 32};
+    cuuint32_t box[2] = {32, 64};
     cuuint32_t es[2] = {1, 1};
     if (g_enc(&tdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, dq, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -896,7 +904,7 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, con
   AttnParams p{};
   p.B = B; p.T = T; p.H = H; p.nq = T / TILE;
   p.qkv = qkv;
-  p.lse = const_cast<float*>(lse); p.Drow = Drow; p.dq = dq; p.dk = dk; p.dqkv = dqkv; p.status = status;
+  p.L2row = L2row; p.Drow = Drow; p.dq = dq; p.dk = dk; p.dqkv = dqkv; p.status = status;
   p.rqk = rqk; p.rope_cos = rope_cos; p.rope_sin = rope_sin;
   int* sched = status + 1;
   p.sched = sched;

@@ -93,7 +93,7 @@ template <typename T>
 cudaError_t attn_fwd_simt(const T* qkv, T* o, float* lse, int B, int T_, int H, cudaStream_t s);
 template <typename T>
 cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, int H,
-                        cudaStream_t s);
+                        cudaStream_t s, const float* lse = nullptr, float* L2 = nullptr);
 // dqk is planar fp32 [2, B*T, d]: dq_hat plane, then dk_hat plane.
 template <typename T>
 cudaError_t attn_bwd_simt(const T* qkv, const T* dout, const float* lse, const float* Drow,
@@ -107,7 +107,9 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
 // backward runs in the kernel and the final dk goes to dqkv's k columns.
 // status points at two device words: the status word and, after it, a counter
 // the kernel schedules its work units with (reset here before the launch).
-cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* lse, const float* Drow, float* dq,
+// L2row is the forward's lse in the base-2, score-scale-folded form that
+// attn_rowdot writes next to Drow when given lse.
+cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, const float* Drow, float* dq,
                         float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s,
                         const float* rqk = nullptr, const float* rope_cos = nullptr,
                         const float* rope_sin = nullptr);

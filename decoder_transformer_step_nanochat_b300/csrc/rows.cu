@@ -198,10 +198,14 @@ __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __res
   stf(o + j + kHalf + 1, rr * (gn[3] - qn[3] * dot));
 }
 
-// D[b,h,t] = sum_e dout[m, h*128+e] * o[m, h*128+e]  (softmax backward term)
+// D[b,h,t] = sum_e dout[m, h*128+e] * o[m, h*128+e]  (softmax backward term).
+// With lse given, also L2[b,h,t] = lse * log2(e) + 3.5: the row's logsumexp in
+// base-2 units, offset so that exp2(s * log2(e) / sqrt(128) - L2) is the
+// probability already multiplied by the 1/sqrt(128) = 2^-3.5 score scale.
 template <typename T>
 __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ o,
-                              float* __restrict__ Drow, int B, int Tlen, int H) {
+                              float* __restrict__ Drow, int B, int Tlen, int H,
+                              const float* __restrict__ lse, float* __restrict__ L2) {
   int w = blockIdx.x * kRowWarps + threadIdx.x / 32;  // (m, h)
   int lane = threadIdx.x & 31;
   int M = B * Tlen;
@@ -213,7 +217,11 @@ __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ 
   for (int c = 0; c < 4; ++c) s += ldf(dout + base + lane + 32 * c) * ldf(o + base + lane + 32 * c);
   s = warp_sum(s);
   int b = m / Tlen, t = m % Tlen;
-  if (lane == 0) Drow[((size_t)b * H + h) * Tlen + t] = s;
+  const size_t i = ((size_t)b * H + h) * Tlen + t;
+  if (lane == 0) {
+    Drow[i] = s;
+    if (L2) L2[i] = fmaf(lse[i], 1.4426950408889634f, 3.5f);
+  }
 }
 
 // One CTA per row of a materialised fp32 logits block: logsumexp, loss
@@ -412,8 +420,8 @@ cudaError_t qk_norm_rope_bwd(const float* dqk, const T* qkv, const float* rqk, c
 
 template <typename T>
 cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, int H,
-                        cudaStream_t s) {
-  attn_rowdot_k<T><<<row_blocks((long long)B * T_ * H), 32 * kRowWarps, 0, s>>>(dout, o, Drow, B, T_, H);
+                        cudaStream_t s, const float* lse, float* L2) {
+  attn_rowdot_k<T><<<row_blocks((long long)B * T_ * H), 32 * kRowWarps, 0, s>>>(dout, o, Drow, B, T_, H, lse, L2);
   return cudaGetLastError();
 }
 
@@ -464,7 +472,7 @@ cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStr
                                            int, cudaStream_t);                                   \
   template cudaError_t qk_norm_rope_bwd<T>(const float*, const T*, const float*, const float*,   \
                                            const float*, T*, int, int, int, cudaStream_t, int);  \
-  template cudaError_t attn_rowdot<T>(const T*, const T*, float*, int, int, int, cudaStream_t);
+  template cudaError_t attn_rowdot<T>(const T*, const T*, float*, int, int, int, cudaStream_t, const float*, float*);
 NC_INST(float)
 NC_INST(bf16)
 #undef NC_INST

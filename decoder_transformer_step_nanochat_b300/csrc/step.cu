@@ -213,7 +213,7 @@ void plan_workspace(nc_ctx* c) {
   f.dout = take(M * d * e);
   f.dqkv = take(M * 3 * d * e);
   f.dqk = take(M * 2 * d * 4);
-  f.drow = take(M * H * 4);
+  f.drow = take(2 * M * H * 4);  // D rows, then the base-2 lse rows of the bf16 attention backward
   f.tok = take(M * 4);
   f.tgt = take(M * 4);
   // up to 8 k-splits of the largest weight gradient (4d x d), at least 64 MiB
@@ -338,9 +338,10 @@ cudaError_t attn_fwd(nc_ctx* c, const T* qkv, T* o, float* lse) {
 template <typename T>
 cudaError_t attn_bwd(nc_ctx* c, const T* qkv, const T* dout, const float* lse, const float* drow, float* dqk,
                      T* dqkv, const float* rqk = nullptr) {
-  if constexpr (sizeof(T) == 2)
-    return attn_bwd_tc(qkv, dout, lse, drow, dqk, dqk + (size_t)c->M * c->d, dqkv, c->B, c->T, c->H, c->status,
-                       c->stream, rqk, rqk ? c->rope_cos : nullptr, rqk ? c->rope_sin : nullptr);
+  if constexpr (sizeof(T) == 2)  // the tensor-core kernel reads the base-2 lse written after drow
+    return attn_bwd_tc(qkv, dout, drow + (size_t)c->M * c->H, drow, dqk, dqk + (size_t)c->M * c->d, dqkv, c->B,
+                       c->T, c->H, c->status, c->stream, rqk, rqk ? c->rope_cos : nullptr,
+                       rqk ? c->rope_sin : nullptr);
   else
     return attn_bwd_simt<T>(qkv, dout, lse, drow, dqk, dqkv, c->B, c->T, c->H, c->stream);
 }
@@ -502,7 +503,9 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     // attention: x += attn(xn1) Wo^T
     CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
     CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
-    KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + 4.0 * M * H, 1, attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s));
+    KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + (sizeof(T) == 2 ? 12.0 : 4.0) * M * H, 1,
+       attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s, sizeof(T) == 2 ? lse_att : nullptr,
+                      sizeof(T) == 2 ? drow + (size_t)M * H : nullptr));
     const bool fused_k = c->prec == NC_BF16;  // k half of the QK-norm/RoPE backward inside the kernel
     KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), fused_k ? 1 : 2,
        attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv, fused_k ? rqk : nullptr));
@@ -1015,7 +1018,8 @@ nc_status nc_op_attention_bwd(nc_ctx* c, const void* qkv, const void* o, const v
   c->have_fwd = false;
   float* drow = wsp<float>(c, c->off.drow);
   if (c->prec == NC_BF16) {
-    CK(attn_rowdot<bf16>((const bf16*)dout, (const bf16*)o, drow, c->B, c->T, c->H, c->stream));
+    CK(attn_rowdot<bf16>((const bf16*)dout, (const bf16*)o, drow, c->B, c->T, c->H, c->stream, lse,
+                         drow + (size_t)c->M * c->H));
     CK(attn_bwd<bf16>(c, (const bf16*)qkv, (const bf16*)dout, lse, drow, dqk, (bf16*)dqkv));
   } else {
     CK(attn_rowdot<float>((const float*)dout, (const float*)o, drow, c->B, c->T, c->H, c->stream));

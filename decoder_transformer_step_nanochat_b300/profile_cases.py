@@ -3,7 +3,9 @@
   python -m decoder_transformer_step_nanochat_b300.profile_cases CASE [--reps N]
 
 CASE: gemm_qkv (32768 x 3840 x 1280 forward GEMM), gemm_fc (32768 x 5120 x 1280
-with the ReLU^2 epilogue), gemm_dw (1280 x 5120 x 32768 weight gradient),
+with the ReLU^2 epilogue), gemm_relu2_bwd (32768 x 5120 x 1280 with the ReLU^2
+backward epilogue, which reads a), gemm_dw (1280 x 5120 x 32768 weight
+gradient),
 attn_fwd / attn_bwd (batch 16, seq 2048, 10 heads: 252 MB of qkv, larger
 than L2), lmhead_ce (4096 rows x 65536 vocabulary x 1280). Inputs are random
 and device-resident; every launch goes through the library.
@@ -23,7 +25,11 @@ def _gemm(ctx, M, N, K, ak, bk, epi):
     A = torch.randn((M, K) if ak else (K, M), device="cuda").to(torch.bfloat16)
     B = (torch.randn((N, K) if bk else (K, N), device="cuda") * 0.05).to(torch.bfloat16)
     C = torch.empty((M, N), device="cuda", dtype=torch.float32 if epi == nc.NC_EPI_STORE_F32 else torch.bfloat16)
-    C2 = torch.empty((M, N), device="cuda", dtype=torch.bfloat16) if epi == nc.NC_EPI_RELU2 else None
+    C2 = None
+    if epi == nc.NC_EPI_RELU2:
+        C2 = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+    elif epi == nc.NC_EPI_RELU2_BWD:
+        C2 = torch.rand((M, N), device="cuda").to(torch.bfloat16)   # a >= 0
     args = (ctx, M, N, K, A.data_ptr(), K if ak else M, ak, B.data_ptr(), K if bk else N, bk, epi, 1.0, 0.0,
             C.data_ptr(), N, C2.data_ptr() if C2 is not None else None, N if C2 is not None else 0)
     return lambda: nc.nc_op_gemm(*args), (A, B, C, C2)
@@ -31,7 +37,7 @@ def _gemm(ctx, M, N, K, ak, bk, epi):
 
 def main(argv=None):
     ap = argparse.ArgumentParser()
-    ap.add_argument("case", choices=["gemm_qkv", "gemm_fc", "gemm_dw", "attn_fwd", "attn_bwd", "lmhead_ce"])
+    ap.add_argument("case", choices=["gemm_qkv", "gemm_fc", "gemm_relu2_bwd", "gemm_dw", "attn_fwd", "attn_bwd", "lmhead_ce"])
     ap.add_argument("--reps", type=int, default=3)
     a = ap.parse_args(argv)
     B, T, H, V = 16, 2048, 10, 65536
@@ -44,7 +50,9 @@ def main(argv=None):
     if a.case == "gemm_qkv":
         run, keep = _gemm(ctx, 32768, 3 * d, d, 1, 1, nc.NC_EPI_STORE)
     elif a.case == "gemm_fc":
-        run, keep = _gemm(ctx, 32768, 4 * d, d, 1, 1, nc.NC_EPI_RELU2)
+        run, keep = _gemm(ctx, 32768, 4 * d, d, 1, 1, nc.NC_EPI_RELU2A)
+    elif a.case == "gemm_relu2_bwd":
+        run, keep = _gemm(ctx, 32768, 4 * d, d, 1, 0, nc.NC_EPI_RELU2_BWD)
     elif a.case == "gemm_dw":
         run, keep = _gemm(ctx, d, 4 * d, 32768, 0, 0, nc.NC_EPI_STORE_F32)
     elif a.case in ("attn_fwd", "attn_bwd"):
