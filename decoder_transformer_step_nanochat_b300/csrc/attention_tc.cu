@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
     tc::mbar_init(v_full, 1);
     tc::mbar_init(v_empty, 1);
     tc::mbar_init(s_full, 1);
-    tc::mbar_init(p_full, FWD_SOFT);
+    tc::mbar_init(p_full, FWD_SOFT / 32);  // one arrival per softmax warp
     tc::mbar_init(o_full, 1);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
       tc::tmem_st32(tS, reinterpret_cast<const float*>(pk));
       tc::tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
       tc::tc_fence_before();
-      tc::mbar_arrive(p_full);
+      tc::mbar_arrive_warp(p_full);
     }
     bool ok = !failed;
     if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
@@ -376,13 +376,16 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 // and dS'^T = P'^T (dP^T - D) by the softmax warps, where L2 = lse log2(e) +
 // 3.5 makes P' = P/sqrt(128), so dS' = dS/sqrt(128) already carries the score
 // scale of dQ and dK (dV, accumulated from P', is multiplied back by sqrt(128)
-// once per unit); then dV += P'^T dO, dK += dS'^T Q and dQ^T = K^T dS'^T as
-// three interleaved chains. The tensor cores keep a single accumulator chain
-// of small products far below their rate (each product waits on the previous
-// one), so every phase runs two or three independent chains of N = 128
-// products. dQ^T is read out (its TMEM columns released at once), staged
-// transposed and added to the fp32 dq plane with one bulk tensor reduce-add
-// per warp, without waiting for it.
+// once per unit); then dQ^T = K^T dS'^T interleaved with the first halves
+// of dV += P'^T dO and dK += dS'^T Q, and the second halves of dV and dK as
+// two chains while dQ^T is read out. The tensor cores keep a single
+// accumulator chain of small products far below their rate (each product
+// waits on the previous one), so every phase runs two or three independent
+// chains of N = 128 products. dQ^T is read out (its TMEM columns released at
+// once), staged transposed and added to the fp32 dq plane with one bulk tensor
+// reduce-add per warp, without waiting for it. The tensor memory accelerator
+// serves both these reduce-adds and the Q/dO loads; an 8 KB reduce-add reads
+// its staging block only after a few thousand cycles.
 // Between units, the next K/V load as soon as the finished unit's products are
 // done and its first query tile runs while the epilogue warps drain dV/dK;
 // only its first dV/dK products wait for that drain.
@@ -426,13 +429,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* q_full = bars + 2;    // [2]
   uint64_t* q_empty = bars + 4;   // [2]: the stage's dq staging was read (one arrival per softmax warp)
   uint64_t* st_full = bars + 6;   // S^T and dP^T of the query tile complete
-  uint64_t* p_full = bars + 8;    // P^T in TMEM and dS^T in shared memory (all softmax threads)
-  uint64_t* dq_full = bars + 10;  // dV, dK, dQ^T products of the tile complete
-  uint64_t* tm_free = bars + 12;  // dQ^T read out of TMEM (all softmax threads)
+  uint64_t* p_full = bars + 8;    // P^T in TMEM and dS^T in shared memory (every softmax warp)
+  uint64_t* dq_full = bars + 10;  // dQ^T of the tile complete
+  uint64_t* tm_free = bars + 12;  // dQ^T read out of TMEM (every softmax warp)
   uint64_t* acc_full = bars + 14;
   uint64_t* acc_free = bars + 15;
   uint64_t* drain = bars + 16;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 17);
+  uint64_t* tile_done = bars + 17;  // every product of the tile complete (its Q/dO stage unread)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   // unit index of this CTA's ul-th unit at slot ul % 4 (-1: no more units); it
   // is written before the arrive that completes that unit's kv_full phase
@@ -451,12 +455,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       tc::mbar_init(q_empty + s, BWD_SOFT / 32);
     }
     tc::mbar_init(st_full, 1);
-    tc::mbar_init(p_full, BWD_SOFT);
+    tc::mbar_init(p_full, BWD_SOFT / 32);  // one arrival per softmax warp
     tc::mbar_init(dq_full, 1);
-    tc::mbar_init(tm_free, BWD_SOFT);
+    tc::mbar_init(tm_free, BWD_SOFT / 32);
     tc::mbar_init(acc_full, 1);
-    tc::mbar_init(acc_free, BWD_SOFT);
+    tc::mbar_init(acc_free, BWD_SOFT / 32);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(tile_done, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -573,18 +578,26 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             break;
           }
           tc::tc_fence_after();
-          // dV += P^T dO (P^T from TMEM), dK += dS^T Q and dQ^T = K^T dS^T (into
-          // the dP^T columns): three chains, their k-steps (16 queries for dV
-          // and dK, 16 keys for dQ^T) interleaved
+          // dQ^T = K^T dS^T (into the dP^T columns; k-steps of 16 keys) with the
+          // first half of dV += P^T dO (P^T from TMEM) and dK += dS^T Q (k-steps
+          // of 16 queries), three chains interleaved; then the second halves of
+          // dV and dK, two chains, which run while dQ^T is read out
           const bool acc0 = it > 0;
 #pragma unroll
           for (int k = 0; k < TILE / 16; ++k) {
-            tc::mma_bf16_tmem_a(tdV, tS + 64 * (k >> 2) + (k & 3) * 8, desc_mn(adO, k), id_kmn,
-                                (acc0 || k > 0) ? 1u : 0u);
-            tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (acc0 || k > 0) ? 1u : 0u);
+            if (k < 4) {
+              tc::mma_bf16_tmem_a(tdV, tS + k * 8, desc_mn(adO, k), id_kmn, (acc0 || k > 0) ? 1u : 0u);
+              tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, (acc0 || k > 0) ? 1u : 0u);
+            }
             tc::mma_bf16(tdP, desc_mn(aK, k), desc_mn(adSt, k), id_mnmn, k > 0 ? 1u : 0u);
           }
           tc::mma_commit(dq_full);
+#pragma unroll
+          for (int k = 4; k < TILE / 16; ++k) {
+            tc::mma_bf16_tmem_a(tdV, tS + 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn, 1u);
+            tc::mma_bf16(tdK, desc_k(adSt, k), desc_mn(aQ, k), id_kmn, 1u);
+          }
+          tc::mma_commit(tile_done);
         }
         if (failed) break;
         tc::mma_commit(acc_full);  // dV, dK of this unit complete
@@ -670,7 +683,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         fence_async_smem();
         tc::tc_fence_before();
-        tc::mbar_arrive(p_full);
+        tc::mbar_arrive_warp(p_full);
         // while the tensor cores run this tile's dV/dK/dQ: the previous tile's
         // stage may take new Q/dO once this warp's dq reduce-add has read its
         // staging block there
@@ -687,9 +700,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // dQ^T is in registers: its TMEM columns may take the next dP^T at once,
         // while the staging and reduce-add below proceed off that path
         tc::tc_fence_before();
-        tc::mbar_arrive(tm_free);
+        tc::mbar_arrive_warp(tm_free);
         // [64 queries x 32 dims] staged transposed (128-byte swizzle) and added
-        // to the dq plane by one bulk tensor reduce-add
+        // to the dq plane by one bulk tensor reduce-add, once the tile's last
+        // products no longer read its Q/dO stage
+        ok = tc::mbar_wait(tile_done, g & 1, abort_flag, kWaitNs);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         uint8_t* blk = sQ + s * TILE_BYTES + stg_off;
 #pragma unroll
         for (int q = 0; q < 64; ++q)
@@ -816,7 +832,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       // dV/dK may take the next unit's products
       tc::tc_fence_before();
-      tc::mbar_arrive(acc_free);
+      tc::mbar_arrive_warp(acc_free);
     }
     if (lane == 0) tc::bulk_wait_all();  // this warp's dQ reduce-adds have landed
     __syncwarp();

@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tfull + b, 1);
-      tc::mbar_init(tempty + b, 32 * NEPI_WARPS);
+      tc::mbar_init(tempty + b, NEPI_WARPS);  // one arrival per epilogue warp
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -543,7 +543,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive(tempty + ab);
+      tc::mbar_arrive_warp(tempty + ab);
     }
     if (lane == 0) tc::bulk_wait_all();  // this warp's stores have landed
     __syncwarp();
