@@ -13,11 +13,15 @@
 // accumulator with tcgen05.ld (one thread per output row and 128-column half)
 // and run the epilogue. Weight-gradient shapes (few output tiles, K = tokens)
 // split K across CTAs into fp32 partial slabs that a reduction kernel sums.
-// CTAs run as 2-CTA clusters on vertically adjacent tiles: each loads its own
-// A rows and half of the shared B tile, multicast into both CTAs' shared
-// memory, so each CTA pulls 32 KB instead of 48 KB from L2 per k-slice; a
-// stage is free again once the MMAs of both CTAs have committed. Every wait is bounded; on timeout the kernel records
-// DEV_TIMEOUT, unwinds, frees its TMEM and returns.
+// CTAs run as 2-CTA clusters on vertically adjacent tiles with 2-SM products
+// (tcgen05 cta_group::2): one thread of the even CTA issues 256x256x16 MMAs
+// whose A rows come half from each CTA's shared memory and whose B tile is
+// split by columns between them, so each SM stages and reads 32 KB per k-slice
+// instead of 48 KB; each CTA's TMEM receives its own 128 rows. Both CTAs' TMA
+// loads complete on the even CTA's barriers, its commits release the stages
+// and accumulators in both, and the odd CTA's epilogue warps arrive on its
+// accumulator-free barriers. Every wait is bounded; on timeout the kernel
+// records DEV_TIMEOUT, unwinds, frees its TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -30,16 +34,27 @@ namespace nc {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int NEPI_WARPS = 8;           // two per TMEM lane quadrant, each half the columns
 constexpr int NTHREADS = 64 + 32 * NEPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 constexpr int STAGING_BYTES = 4096;  // per epilogue warp: 32 rows x 128 B, 128B-swizzled
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + NEPI_WARPS * STAGING_BYTES + 1024 + 256;
+
+// Pipeline shape per CTA: single CTAs stage A and the whole B tile (4 x 48 KB);
+// a CTA pair running 2-SM products stages its own A rows and its half of B
+// (6 x 32 KB).
+template <int CL>
+struct Pipe {
+  static constexpr int STAGES = CL == 2 ? 6 : 4;
+  static constexpr int B_STAGE = CL == 2 ? B_BYTES / 2 : B_BYTES;
+  static constexpr int STAGE_BYTES = A_BYTES + B_STAGE;
+};
+constexpr int RING_BYTES = 6 * (A_BYTES + B_BYTES / 2);
+static_assert(RING_BYTES == 4 * (A_BYTES + B_BYTES), "both pipelines use the same ring");
+constexpr int SMEM_BYTES = RING_BYTES + NEPI_WARPS * STAGING_BYTES + 1024 + 256;
 
 struct TcParams {
   GemmArgs g;
@@ -197,9 +212,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               const __grid_constant__ TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int STAGES = Pipe<CL>::STAGES, B_STAGE = Pipe<CL>::B_STAGE, STAGE_BYTES = Pipe<CL>::STAGE_BYTES;
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint8_t* sStage = sB + STAGES * B_BYTES;
+  uint8_t* sStage = smem + RING_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + NEPI_WARPS * STAGING_BYTES);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
@@ -217,11 +233,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       tc::mbar_init(full + s, 1);
-      tc::mbar_init(empty + s, CL);  // each CTA of the pair releases the stage
+      tc::mbar_init(empty + s, 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(tfull + b, 1);
-      tc::mbar_init(tempty + b, NEPI_WARPS);  // one arrival per epilogue warp
+      tc::mbar_init(tempty + b, CL * NEPI_WARPS);  // one arrival per epilogue warp (of both CTAs)
     }
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
@@ -232,12 +248,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc::prefetch_tmap(&tb);
   }
   if (warp == 1) {
-    tc::tmem_alloc(tmem_holder, TMEM_COLS);
-    tc::tmem_relinquish();
+    if (CL == 2) {
+      tc::tmem_alloc_pair(tmem_holder, TMEM_COLS);
+      tc::tmem_relinquish_pair();
+    } else {
+      tc::tmem_alloc(tmem_holder, TMEM_COLS);
+      tc::tmem_relinquish();
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
-  if (CL == 2) tc::cluster_sync();  // the peer's barriers exist before any multicast
+  if (CL == 2) tc::cluster_sync();  // the peer's barriers exist before any load or commit reaches them
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   bool failed = false;
@@ -257,27 +278,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int a_off = (int)(bt * g.a_brows), b_off = (int)(bt * g.b_brows);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
-          tc::mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
           const int k0 = kb * BK;
           uint8_t* a = sA + stage * A_BYTES;
-          uint8_t* b = sB + stage * B_BYTES;
+          uint8_t* b = sB + stage * B_STAGE;
+          if (CL == 2) {
+            // own A rows and own half of the B columns; both CTAs' bytes
+            // complete on the even CTA's barrier, which expects them all
+            if (rank == 0) tc::mbar_arrive_expect_tx(full + stage, 2 * STAGE_BYTES);
+            const uint32_t bar = tc::cluster_addr(full + stage, 0);
+            if (A_MN) {
+              tc::tma_load_2d_pair(a, &ta, m0, k0 + a_off, bar);
+              tc::tma_load_2d_pair(a + 8192, &ta, m0 + 64, k0 + a_off, bar);
+            } else {
+              tc::tma_load_2d_pair(a, &ta, k0, m0 + a_off, bar);
+            }
+            const int nh = n0 + (BN / 2) * rank;
+            if (B_MN) {
+              tc::tma_load_2d_pair(b, &tb, nh, k0 + b_off, bar);
+              tc::tma_load_2d_pair(b + 8192, &tb, nh + 64, k0 + b_off, bar);
+            } else {
+              tc::tma_load_2d_pair(b, &tb, k0, nh + b_off, bar);
+            }
+            issued[stage] = true;
+            issued_phase[stage] = phase;
+            if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            continue;
+          }
+          tc::mbar_arrive_expect_tx(full + stage, STAGE_BYTES);
           if (A_MN) {
             tc::tma_load_2d(a, &ta, m0, k0 + a_off, full + stage);
             tc::tma_load_2d(a + 8192, &ta, m0 + 64, k0 + a_off, full + stage);
           } else {
             tc::tma_load_2d(a, &ta, k0, m0 + a_off, full + stage);
           }
-          if (CL == 2) {
-            // this CTA fetches half of the shared B tile for both CTAs
-            if (B_MN) {
-#pragma unroll
-              for (int j = 2 * rank; j < 2 * rank + 2; ++j)
-                tc::tma_load_2d_multicast(b + j * 8192, &tb, n0 + 64 * j, k0 + b_off, full + stage, 0x3);
-            } else {
-              tc::tma_load_2d_multicast(b + rank * (B_BYTES / 2), &tb, k0, n0 + (BN / 2) * rank + b_off, full + stage,
-                                        0x3);
-            }
-          } else if (B_MN) {
+          if (B_MN) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) tc::tma_load_2d(b + j * 8192, &tb, n0 + 64 * j, k0 + b_off, full + stage);
           } else {
@@ -290,15 +324,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       if (failed) {
         *abort_flag = 1;
-        // let every copy this thread started land before the CTA exits
-        for (int s = 0; s < STAGES; ++s)
-          if (issued[s]) tc::mbar_wait(full + s, issued_phase[s], nullptr, kWaitNs);
+        // let every copy this CTA's barriers track land before it exits (the
+        // odd CTA of a pair has none: its copies complete on the peer's)
+        if (CL == 1 || rank == 0)
+          for (int s = 0; s < STAGES; ++s)
+            if (issued[s]) tc::mbar_wait(full + s, issued_phase[s], nullptr, kWaitNs);
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = tc::idesc_bf16(BM, BN, A_MN, B_MN);
+    // (in a CTA pair, the even CTA's thread issues the 2-SM products for both)
+    if (lane == 0 && (CL == 1 || rank == 0)) {
+      const uint32_t idesc = tc::idesc_bf16(CL * BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int cnt = 0;
@@ -315,28 +352,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!tc::mbar_wait(full + stage, phase, abort_flag, kWaitNs)) { failed = true; break; }
           tc::tc_fence_after();
           const uint32_t a_addr = tc::smem_u32(sA + stage * A_BYTES);
-          const uint32_t b_addr = tc::smem_u32(sB + stage * B_BYTES);
+          const uint32_t b_addr = tc::smem_u32(sB + stage * B_STAGE);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             const uint64_t ad = A_MN ? tc::sdesc_sw128(a_addr + k * 2048, 8192, 1024)
                                      : tc::sdesc_sw128(a_addr + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? tc::sdesc_sw128(b_addr + k * 2048, 8192, 1024)
                                      : tc::sdesc_sw128(b_addr + k * 32, 16, 1024);
-            tc::mma_bf16(dtm, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            if (CL == 2) tc::mma_bf16_pair(dtm, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
+            else tc::mma_bf16(dtm, ad, bd, idesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
-          if (CL == 2) tc::mma_commit_multicast(empty + stage, 0x3);  // frees the stage in both CTAs
+          if (CL == 2) tc::mma_commit_pair_multicast(empty + stage, 0x3);  // frees the stage in both CTAs
           else tc::mma_commit(empty + stage);
           any_mma = true;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (failed) break;
-        tc::mma_commit(tfull + ab);
+        if (CL == 2) tc::mma_commit_pair_multicast(tfull + ab, 0x3);  // both CTAs' accumulators
+        else tc::mma_commit(tfull + ab);
       }
       if (failed) {
         *abort_flag = 1;
         if (any_mma) {
           // wait for the MMAs already issued before the TMEM is released
-          tc::mma_commit(drain);
+          if (CL == 2) tc::mma_commit_pair(drain);
+          else tc::mma_commit(drain);
           tc::mbar_wait(drain, 0, nullptr, kWaitNs);
         }
       }
@@ -543,7 +583,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       tc::tc_fence_before();
-      tc::mbar_arrive_warp(tempty + ab);
+      if (CL == 2) tc::mbar_arrive_warp_cluster(tc::cluster_addr(tempty + ab, 0));  // the even CTA's barrier
+      else tc::mbar_arrive_warp(tempty + ab);
     }
     if (lane == 0) tc::bulk_wait_all();  // this warp's stores have landed
     __syncwarp();
@@ -555,13 +596,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
+  // neither CTA of a pair may leave (or free the TMEM) while the other can
+  // still arrive on its barriers or its products still run
+  if (CL == 2) tc::cluster_sync();
   if (warp == 1) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+    if (CL == 2) tc::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tc::tmem_dealloc(tmem_base, TMEM_COLS);
   }
-  // neither CTA of a pair may leave while the other can still multicast
-  // into its shared memory or arrive on its barriers
-  if (CL == 2) tc::cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
