@@ -287,24 +287,58 @@ __global__ void ce_rows_k(const float* __restrict__ logits, const int* __restric
 
 // Combine per-tile softmax partials (max, sum of exp(logit - max), argmax)
 // of every 256-column vocabulary tile into lse, loss and argmax per row.
-__global__ void ce_reduce_k(const float* __restrict__ pm, const float* __restrict__ ps,
-                            const int* __restrict__ pa, const float* __restrict__ pt, const int* __restrict__ tgt,
-                            int nt, float* __restrict__ lse, float* __restrict__ nll, int* __restrict__ amax,
-                            int M) {
-  int m = blockIdx.x * blockDim.x + threadIdx.x;
-  if (m >= M) return;
-  float mx = -INFINITY;
-  int arg = 0;
-  for (int t = 0; t < nt; ++t) {
-    float v = pm[(size_t)t * M + m];
-    if (v > mx) { mx = v; arg = pa[(size_t)t * M + m]; }  // first tile wins ties
+// Combine the per-tile cross-entropy partials of each row: lse = max + log(sum
+// of sum-exp rescaled to that max), argmax (lowest column among ties: the
+// tiles are in column order and a later tile only wins with a strictly
+// larger maximum), nll = lse - target logit. A block covers 32 consecutive
+// rows (one per lane, so every load is one 128-byte row segment); its 8 warps
+// each take a contiguous eighth of the tiles in one online pass, and the 8
+// results are combined in tile order.
+constexpr int kCeWarps = 8;
+__device__ __forceinline__ void ce_merge(float& mx, float& s, int& arg, float m2, float s2, int a2) {
+  if (m2 > mx) {
+    s = s * expf(mx - m2) + s2;  // mx = -inf: s is 0 and so is the product
+    mx = m2;
+    arg = a2;
+  } else if (m2 != -INFINITY) {
+    s += s2 * expf(m2 - mx);
   }
-  float s = 0.f;
-  for (int t = 0; t < nt; ++t) s += ps[(size_t)t * M + m] * expf(pm[(size_t)t * M + m] - mx);
-  float l = mx + logf(s);
-  lse[m] = l;
-  nll[m] = tgt[m] < 0 ? 0.f : l - pt[m];  // a masked position carries no loss
-  amax[m] = arg;
+}
+__global__ void __launch_bounds__(32 * kCeWarps)
+    ce_reduce_k(const float* __restrict__ pm, const float* __restrict__ ps, const int* __restrict__ pa,
+                const float* __restrict__ pt, const int* __restrict__ tgt, int nt, float* __restrict__ lse,
+                float* __restrict__ nll, int* __restrict__ amax, int M) {
+  __shared__ float smx[kCeWarps][32], ss[kCeWarps][32];
+  __shared__ int sarg[kCeWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int m = blockIdx.x * 32 + lane;
+  const int per = (nt + kCeWarps - 1) / kCeWarps;
+  const int t0 = w * per, t1 = min(nt, t0 + per);
+  float mx = -INFINITY, s = 0.f;
+  int arg = 0;
+  if (m < M)
+    for (int t = t0; t < t1; ++t) {
+      const size_t i = (size_t)t * M + m;
+      const float v = pm[i];
+      if (v > mx) {
+        s = s * expf(mx - v) + ps[i];
+        mx = v;
+        arg = pa[i];
+      } else if (v != -INFINITY) {
+        s += ps[i] * expf(v - mx);
+      }
+    }
+  smx[w][lane] = mx;
+  ss[w][lane] = s;
+  sarg[w][lane] = arg;
+  __syncthreads();
+  if (w == 0 && m < M) {
+    for (int k = 1; k < kCeWarps; ++k) ce_merge(mx, s, arg, smx[k][lane], ss[k][lane], sarg[k][lane]);
+    const float l = mx + logf(s);
+    lse[m] = l;
+    nll[m] = tgt[m] < 0 ? 0.f : l - pt[m];  // a masked position carries no loss
+    amax[m] = arg;
+  }
 }
 
 // loss = mean of nll over the positions whose target is not masked (-1),
@@ -435,7 +469,8 @@ cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse,
 cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int* p_arg,
                                const float* p_tgt, const int* tgt, int n_tiles, float* lse, float* nll, int* amax,
                                int M, cudaStream_t s) {
-  ce_reduce_k<<<(M + 255) / 256, 256, 0, s>>>(p_max, p_sum, p_arg, p_tgt, tgt, n_tiles, lse, nll, amax, M);
+  if (M == 0) return cudaSuccess;
+  ce_reduce_k<<<(M + 31) / 32, 32 * kCeWarps, 0, s>>>(p_max, p_sum, p_arg, p_tgt, tgt, n_tiles, lse, nll, amax, M);
   return cudaGetLastError();
 }
 

@@ -204,8 +204,12 @@ void plan_workspace(nc_ctx* c) {
   f.psum = take((size_t)c->ce_tiles * M * 4);
   f.parg = take((size_t)c->ce_tiles * M * 4);
   f.ptgt = take(M * 4);
-  c->ce_rows = (int)(M < 4096 ? M : 4096);
-  f.chunk = take((size_t)c->ce_rows * V * 4);  // fp32 logits (debug) or element-typed g
+  // rows per lm_head / cross-entropy backward chunk: in bf16 the whole batch up to 32,768 rows (g is 2 B per
+  // logit, 4.3 GB at 32,768 x 65,536), so the input- and weight-gradient GEMMs each run once over every row
+  // instead of eight times on a 4096-row slice that fills 1.08 waves of the SMs; the fp32 debug mode
+  // materialises logits, 4096 rows at a time
+  c->ce_rows = (int)(c->prec == NC_BF16 ? (M < 32768 ? M : 32768) : (M < 4096 ? M : 4096));
+  f.chunk = take((size_t)c->ce_rows * V * e);  // fp32 logits (debug) or bf16 g
   f.dx = take(M * d * 4);
   f.dxe = take(M * d * e);
   f.dy = take(M * d * 4);
