@@ -91,7 +91,7 @@ struct AttnParams {
   const bf16* qkv;  // backward: k_hat rows for the in-kernel QK-norm/RoPE backward of k
   bf16* o;        // forward output
   float* lse;     // forward output
-  const float* L2row;  // backward: lse * log2(e) + 3.5 per (b, h, t) (base 2, score scale folded in)
+  const float* L2row;  // backward: -(lse * log2(e) + 3.5) per (b, h, t) (base 2, score scale folded in)
   const float* Drow;
   float* dq;      // backward: fp32 [B*T, d], accumulated with atomics (pre-zeroed)
   float* dk;      // backward: fp32 [B*T, d] (dk_hat), unless the k half is finished in-kernel
@@ -373,8 +373,8 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 //
 // Per query tile: S^T = K Q^T and dP^T = V dO^T, two accumulator chains of
 // 128x128x16 products interleaved; P'^T = exp2(S^T log2(e)/sqrt(128) - L2)
-// and dS'^T = P'^T (dP^T - D) by the softmax warps, where L2 = lse log2(e) +
-// 3.5 makes P' = P/sqrt(128), so dS' = dS/sqrt(128) already carries the score
+// and dS'^T = P'^T (dP^T - D) by the softmax warps (paired fp32 arithmetic),
+// where L2 = lse log2(e) + 3.5 (stored negated) makes P' = P/sqrt(128), so dS' = dS/sqrt(128) already carries the score
 // scale of dQ and dK (dV, accumulated from P', is multiplied back by sqrt(128)
 // once per unit); then dQ^T = K^T dS'^T interleaved with the first halves
 // of dV += P'^T dO and dK += dS'^T Q, and the second halves of dV and dK as
@@ -636,7 +636,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       for (int it = 0; it < u.nit; ++it, ++g) {
         const int qt = u.kt + it;
         const int s = g & 1;
-        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // base-2 lse of this half's 64 query columns
+        const float* Lq = sLD + s * 2 * TILE + ch * 64;        // negated base-2 lse of this half's 64 query columns
         const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
         bool ok = tc::mbar_wait(st_full, g & 1, abort_flag, kWaitNs);
         // the lse / D rows arrived with this tile's Q (already complete here)
@@ -648,15 +648,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int c = 0; c < 2; ++c) {
           float sv[32], dp[32];
           tc::tmem_ld32x2(tS + lane_off + ch * 64 + c * 32, tdP + lane_off + ch * 64 + c * 32, sv, dp);
-          // P' = exp2(S * log2(e)/sqrt(128) - L2) = P / sqrt(128): the score
-          // scale rides on P' into dS' = P' (dP - D) = dS / sqrt(128)
+          // P' = exp2(S * log2(e)/sqrt(128) + nL2) = P / sqrt(128): the score
+          // scale rides on P' into dS' = P' (dP - D) = dS / sqrt(128); the
+          // arithmetic runs on fp32 pairs
+          const uint64_t sl2x2 = tc::f2pack(sl2, sl2);
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) {
             const float4 l0 = *reinterpret_cast<const float4*>(Lq + c * 32 + gq * 8);
             const float4 l1 = *reinterpret_cast<const float4*>(Lq + c * 32 + gq * 8 + 4);
-            const float Lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+            const uint64_t nl[4] = {tc::f2pack(l0.x, l0.y), tc::f2pack(l0.z, l0.w), tc::f2pack(l1.x, l1.y),
+                                    tc::f2pack(l1.z, l1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) sv[gq * 8 + i] = tc::ex2(fmaf(sv[gq * 8 + i], sl2, -Lv[i]));
+            for (int k = 0; k < 4; ++k) {
+              const int i = gq * 8 + 2 * k;
+              const float2 x = tc::f2unpack(tc::ffma2(tc::f2pack(sv[i], sv[i + 1]), sl2x2, nl[k]));
+              sv[i] = tc::ex2(x.x);
+              sv[i + 1] = tc::ex2(x.y);
+            }
           }
           if (diag) {  // the diagonal tile: query q sees key r only if q >= r
 #pragma unroll
@@ -667,9 +675,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           for (int gq = 0; gq < 4; ++gq) {
             const float4 d0 = *reinterpret_cast<const float4*>(Dq + c * 32 + gq * 8);
             const float4 d1 = *reinterpret_cast<const float4*>(Dq + c * 32 + gq * 8 + 4);
-            const float Dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            const uint64_t dd[4] = {tc::f2pack(d0.x, d0.y), tc::f2pack(d0.z, d0.w), tc::f2pack(d1.x, d1.y),
+                                    tc::f2pack(d1.z, d1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dp[gq * 8 + i] = sv[gq * 8 + i] * (dp[gq * 8 + i] - Dv[i]);
+            for (int k = 0; k < 4; ++k) {
+              const int i = gq * 8 + 2 * k;
+              const float2 w = tc::f2unpack(
+                  tc::fmul2(tc::f2pack(sv[i], sv[i + 1]), tc::fsub2(tc::f2pack(dp[i], dp[i + 1]), dd[k])));
+              dp[i] = w.x;
+              dp[i + 1] = w.y;
+            }
             st_tile8(sdSt, r, ch * 8 + c * 4 + gq, pack8(dp + 8 * gq));
           }
           // P'^T of these 32 query columns -> 16 packed bf16 pairs in TMEM

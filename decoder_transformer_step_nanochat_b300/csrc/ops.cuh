@@ -107,8 +107,8 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
 // backward runs in the kernel and the final dk goes to dqkv's k columns.
 // status points at two device words: the status word and, after it, a counter
 // the kernel schedules its work units with (reset here before the launch).
-// L2row is the forward's lse in the base-2, score-scale-folded form that
-// attn_rowdot writes next to Drow when given lse.
+// L2row is the forward's lse in the negated, base-2, score-scale-folded form
+// that attn_rowdot writes next to Drow when given lse.
 cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, const float* Drow, float* dq,
                         float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s,
                         const float* rqk = nullptr, const float* rope_cos = nullptr,

@@ -18,6 +18,14 @@ __device__ __forceinline__ float4 ld4(const bf16* p) {
   float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
   return make_float4(fa.x, fa.y, fb.x, fb.y);
 }
+__device__ __forceinline__ float2 ld2(const float* p) { return *reinterpret_cast<const float2*>(p); }
+__device__ __forceinline__ float2 ld2(const bf16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+__device__ __forceinline__ void st2(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+__device__ __forceinline__ void st2(bf16* p, float2 v) {
+  *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
+}
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 __device__ __forceinline__ void st4(bf16* p, float4 v) {
   __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
@@ -176,9 +184,8 @@ __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __res
   const float2 si = *reinterpret_cast<const float2*>(sn + t * kHalf + j);
   const float2 g1 = *reinterpret_cast<const float2*>(g + j);
   const float2 g2 = *reinterpret_cast<const float2*>(g + j + kHalf);
-  float q1[2], q2[2];
-  q1[0] = ldf(q + j); q1[1] = ldf(q + j + 1);
-  q2[0] = ldf(q + j + kHalf); q2[1] = ldf(q + j + kHalf + 1);
+  const float2 qa = ld2(q + j), qb = ld2(q + j + kHalf);
+  const float q1[2] = {qa.x, qa.y}, q2[2] = {qb.x, qb.y};
   const float c2[2] = {co.x, co.y}, s2[2] = {si.x, si.y};
   const float a1[2] = {g1.x, g1.y}, a2[2] = {g2.x, g2.y};
   float gn[4], qn[4];
@@ -192,16 +199,15 @@ __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __res
   float dot = warp_sum(gn[0] * qn[0] + gn[1] * qn[1] + gn[2] * qn[2] + gn[3] * qn[3]) / (float)kHeadDim;
   float rr = rqk[(size_t)m * 2 * H + wh];
   T* o = dqkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
-  stf(o + j, rr * (gn[0] - qn[0] * dot));
-  stf(o + j + 1, rr * (gn[1] - qn[1] * dot));
-  stf(o + j + kHalf, rr * (gn[2] - qn[2] * dot));
-  stf(o + j + kHalf + 1, rr * (gn[3] - qn[3] * dot));
+  st2(o + j, make_float2(rr * (gn[0] - qn[0] * dot), rr * (gn[1] - qn[1] * dot)));
+  st2(o + j + kHalf, make_float2(rr * (gn[2] - qn[2] * dot), rr * (gn[3] - qn[3] * dot)));
 }
 
 // D[b,h,t] = sum_e dout[m, h*128+e] * o[m, h*128+e]  (softmax backward term).
-// With lse given, also L2[b,h,t] = lse * log2(e) + 3.5: the row's logsumexp in
-// base-2 units, offset so that exp2(s * log2(e) / sqrt(128) - L2) is the
-// probability already multiplied by the 1/sqrt(128) = 2^-3.5 score scale.
+// With lse given, also nL2[b,h,t] = -(lse * log2(e) + 3.5): the row's negated
+// logsumexp in base-2 units, offset so that exp2(s * log2(e) / sqrt(128) + nL2)
+// is the probability already multiplied by the 1/sqrt(128) = 2^-3.5 score
+// scale.
 template <typename T>
 __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ o,
                               float* __restrict__ Drow, int B, int Tlen, int H,
@@ -211,16 +217,14 @@ __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ 
   int M = B * Tlen;
   if (w >= M * H) return;
   int m = w / H, h = w % H;
-  size_t base = (size_t)m * H * kHeadDim + (size_t)h * kHeadDim;
-  float s = 0.f;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) s += ldf(dout + base + lane + 32 * c) * ldf(o + base + lane + 32 * c);
-  s = warp_sum(s);
+  size_t base = (size_t)m * H * kHeadDim + (size_t)h * kHeadDim + 4 * lane;  // 4 consecutive dims per lane
+  const float4 u = ld4(dout + base), v = ld4(o + base);
+  float s = warp_sum(u.x * v.x + u.y * v.y + u.z * v.z + u.w * v.w);
   int b = m / Tlen, t = m % Tlen;
   const size_t i = ((size_t)b * H + h) * Tlen + t;
   if (lane == 0) {
     Drow[i] = s;
-    if (L2) L2[i] = fmaf(lse[i], 1.4426950408889634f, 3.5f);
+    if (L2) L2[i] = -fmaf(lse[i], 1.4426950408889634f, 3.5f);
   }
 }
 

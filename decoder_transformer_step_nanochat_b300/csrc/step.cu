@@ -217,7 +217,7 @@ void plan_workspace(nc_ctx* c) {
   f.dout = take(M * d * e);
   f.dqkv = take(M * 3 * d * e);
   f.dqk = take(M * 2 * d * 4);
-  f.drow = take(2 * M * H * 4);  // D rows, then the base-2 lse rows of the bf16 attention backward
+  f.drow = take(2 * M * H * 4);  // D rows, then the negated base-2 lse rows of the bf16 attention backward
   f.tok = take(M * 4);
   f.tgt = take(M * 4);
   // up to 8 k-splits of the largest weight gradient (4d x d), at least 64 MiB
@@ -342,7 +342,7 @@ cudaError_t attn_fwd(nc_ctx* c, const T* qkv, T* o, float* lse) {
 template <typename T>
 cudaError_t attn_bwd(nc_ctx* c, const T* qkv, const T* dout, const float* lse, const float* drow, float* dqk,
                      T* dqkv, const float* rqk = nullptr) {
-  if constexpr (sizeof(T) == 2)  // the tensor-core kernel reads the base-2 lse written after drow
+  if constexpr (sizeof(T) == 2)  // the tensor-core kernel reads the negated base-2 lse written after drow
     return attn_bwd_tc(qkv, dout, drow + (size_t)c->M * c->H, drow, dqk, dqk + (size_t)c->M * c->d, dqkv, c->B,
                        c->T, c->H, c->status, c->stream, rqk, rqk ? c->rope_cos : nullptr,
                        rqk ? c->rope_sin : nullptr);
