@@ -13,8 +13,12 @@ scaling is weak. Rank 0 prints one JSON line.
 Our arm: K timed steps after W warm-up steps, each one call of
 nc_forward_loss_async + nc_backward on device-resident inputs, timed with
 CUDA events on the library's stream between a barrier and a synchronise.
-The end-to-end figure times nc_train_step_host (tokens copied from pinned
-host memory and the loss read back every step). The per-kernel roofline
+The end-to-end figure times nc_train_step_host_u16: each step copies the
+batch's packed uint16 token rows [B, T+1] (the token-shard format) from
+pinned host memory, widens them on the device into inputs and next-token
+targets, runs forward and backward and reads the loss back (vocabularies
+above 65,536 ids use nc_train_step_host with int32 token and target
+buffers). The per-kernel roofline
 comes from the library's own CUDA-event records of each launch in the timed
 region. The CPU baseline is the oracle on one 2048-token sequence of the
 same workload, timed after the GPU work in this process.
@@ -275,17 +279,29 @@ def our_arm(args):
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
-        h_tok = torch.from_numpy(tok_np).pin_memory()
-        h_tgt = torch.from_numpy(tgt_np).pin_memory()
-        nc.nc_train_step_host(st.ctx, params.data_ptr(), h_tok.data_ptr(), h_tgt.data_ptr(), grads.data_ptr())
+        if w.vocab <= 65536:
+            # the same ids as tok_np / tgt_np, as packed rows
+            h_rows = torch.from_numpy(W.make_packed_tokens(w, seed=rank).view(np.int16)).pin_memory()
+            h2d = h_rows.numel() * 2
+
+            def host_step():
+                nc.nc_train_step_host_u16(st.ctx, params.data_ptr(), h_rows.data_ptr(), grads.data_ptr())
+        else:
+            h_tok = torch.from_numpy(tok_np).pin_memory()
+            h_tgt = torch.from_numpy(tgt_np).pin_memory()
+            h2d = 2 * M * 4
+
+            def host_step():
+                nc.nc_train_step_host(st.ctx, params.data_ptr(), h_tok.data_ptr(), h_tgt.data_ptr(), grads.data_ptr())
+        host_step()
         if ws > 1:
             dist.barrier()
         t0 = time.perf_counter()
         for _ in range(args.steps):
-            nc.nc_train_step_host(st.ctx, params.data_ptr(), h_tok.data_ptr(), h_tgt.data_ptr(), grads.data_ptr())
+            host_step()
         dt_max, _ = reduce_over_ranks(1000.0 * (time.perf_counter() - t0) / args.steps, 0, "cuda")
         e2e = {"value": job_tokens_per_s(ws, M, dt_max), "unit": UNIT,
-               "h2d_bytes_per_step": 2 * M * 4, "d2h_bytes_per_step": 4}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4}
 
     # ---- roofline of the dominant kernel family (live CUDA-event records)
     dom = max(fam, key=lambda k: fam[k][0])

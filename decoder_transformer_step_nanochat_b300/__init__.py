@@ -68,6 +68,9 @@ _SIGS = {
     "nc_forward_loss": (_I, [_P, _P, _P, _P, ctypes.POINTER(_F)]),
     "nc_forward_loss_async": (_I, [_P, _P, _P, _P, _P]),
     "nc_backward": (_I, [_P, _P]),
+    "nc_backward_accumulate": (_I, [_P, _P, _F]),
+    "nc_forward_loss_u16": (_I, [_P, _P, _P, _P]),
+    "nc_train_step_host_u16": (_I, [_P, _P, _P, _P, ctypes.POINTER(_F)]),
     "nc_train_step_host": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(_F)]),
     "nc_get_token_outputs": (_I, [_P, _P, _P, _P]),
     "nc_get_hidden": (_I, [_P, _P]),
@@ -165,6 +168,20 @@ def nc_forward_loss_async(ctx, params, tokens, targets, d_loss):
 
 def nc_backward(ctx, grads):
     _check(lib().nc_backward(ctx, grads), ctx)
+
+
+def nc_backward_accumulate(ctx, grads, scale):
+    _check(lib().nc_backward_accumulate(ctx, grads, scale), ctx)
+
+
+def nc_forward_loss_u16(ctx, params, packed, d_loss):
+    _check(lib().nc_forward_loss_u16(ctx, params, packed, d_loss), ctx)
+
+
+def nc_train_step_host_u16(ctx, params, h_packed, grads) -> float:
+    out = _F()
+    _check(lib().nc_train_step_host_u16(ctx, params, h_packed, grads, ctypes.byref(out)), ctx)
+    return float(out.value)
 
 
 def nc_train_step_host(ctx, params, h_tokens, h_targets, grads) -> float:
@@ -324,6 +341,12 @@ class Step:
 
     def backward(self, grads):
         nc_backward(self.ctx, grads.data_ptr())
+
+    def backward_accumulate(self, grads, scale):
+        nc_backward_accumulate(self.ctx, grads.data_ptr(), scale)
+
+    def forward_loss_u16(self, params, packed, d_loss):
+        nc_forward_loss_u16(self.ctx, params.data_ptr(), packed.data_ptr(), d_loss.data_ptr())
 
     def token_outputs(self):
         import torch

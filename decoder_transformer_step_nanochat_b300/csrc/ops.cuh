@@ -114,6 +114,12 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, c
                         const float* rqk = nullptr, const float* rope_cos = nullptr,
                         const float* rope_sin = nullptr);
 
+// out = *in * scale (one device float).
+cudaError_t scale_scalar(const float* in, float scale, float* out, cudaStream_t s);
+// Packed uint16 token rows [B, T+1] -> int32 inputs tok [B, T] (ids 0..T-1 of
+// each row) and targets tgt [B, T] (ids 1..T).
+cudaError_t unpack_u16(const uint16_t* packed, int B, int T_, int32_t* tok, int32_t* tgt, cudaStream_t s);
+
 // ------------------------------------------------------------------ loss
 cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,
                                 int* amax, int M, int V, int* status, cudaStream_t s);

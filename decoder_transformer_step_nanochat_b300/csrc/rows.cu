@@ -291,6 +291,23 @@ __global__ void ce_rows_k(const float* __restrict__ logits, const int* __restric
 
 // Combine per-tile softmax partials (max, sum of exp(logit - max), argmax)
 // of every 256-column vocabulary tile into lse, loss and argmax per row.
+// out = in * s for one device float (the loss-gradient scale of an
+// accumulating backward: 1 / unmasked count times the caller's scale).
+__global__ void scale_scalar_k(const float* __restrict__ in, float s, float* __restrict__ out) { *out = *in * s; }
+
+// Packed uint16 token rows [B, T+1] -> inputs tok[b, t] = row[b][t] and
+// targets tgt[b, t] = row[b][t + 1] (int32, [B, T]).
+__global__ void unpack_u16_k(const uint16_t* __restrict__ packed, int B, int Tlen, int32_t* __restrict__ tok,
+                             int32_t* __restrict__ tgt) {
+  const long long n = (long long)B * Tlen;
+  for (long long m = blockIdx.x * (long long)blockDim.x + threadIdx.x; m < n; m += (long long)gridDim.x * blockDim.x) {
+    const long long b = m / Tlen, t = m - b * Tlen;
+    const uint16_t* row = packed + b * (Tlen + 1);
+    tok[m] = row[t];
+    tgt[m] = row[t + 1];
+  }
+}
+
 // Combine the per-tile cross-entropy partials of each row: lse = max + log(sum
 // of sum-exp rescaled to that max), argmax (lowest column among ties: the
 // tiles are in column order and a later tile only wins with a strictly
@@ -475,6 +492,20 @@ cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int
                                int M, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   ce_reduce_k<<<(M + 31) / 32, 32 * kCeWarps, 0, s>>>(p_max, p_sum, p_arg, p_tgt, tgt, n_tiles, lse, nll, amax, M);
+  return cudaGetLastError();
+}
+
+cudaError_t scale_scalar(const float* in, float scale, float* out, cudaStream_t s) {
+  scale_scalar_k<<<1, 1, 0, s>>>(in, scale, out);
+  return cudaGetLastError();
+}
+
+cudaError_t unpack_u16(const uint16_t* packed, int B, int T_, int32_t* tok, int32_t* tgt, cudaStream_t s) {
+  const long long n = (long long)B * T_;
+  if (n == 0) return cudaSuccess;
+  long long blocks = (n + 255) / 256;
+  if (blocks > 148 * 8) blocks = 148 * 8;
+  unpack_u16_k<<<(int)blocks, 256, 0, s>>>(packed, B, T_, tok, tgt);
   return cudaGetLastError();
 }
 

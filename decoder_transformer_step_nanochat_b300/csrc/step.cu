@@ -86,7 +86,7 @@ struct nc_ctx {
     size_t xn1, r1, qkv, rqk, o, lse_att, xn2, r2, a;  // per-layer stash (stride below)
     size_t layer_stride;
     size_t x, hf, rf, lse, nll, amax, loss, pmax, psum, parg, ptgt, chunk;
-    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial, inv_count;
+    size_t dx, dxe, dy, du, dout, dqkv, dqk, drow, tok, tgt, partial, inv_count, grad_scale, packed;
   } off{};
   // optimizer scratch: overlays the step's workspace from offset 0 (the
   // stash is dead once the backward has run)
@@ -225,6 +225,8 @@ void plan_workspace(nc_ctx* c) {
   if (c->partial_bytes < (size_t(64) << 20)) c->partial_bytes = size_t(64) << 20;
   f.partial = take(c->partial_bytes);
   f.inv_count = take(4);  // 1 / number of unmasked targets of the last forward
+  f.grad_scale = take(4);  // inv_count times an accumulating backward's scale
+  f.packed = take((size_t)c->B * (c->T + 1) * 2);  // host uint16 token rows staged by nc_train_step_host_u16
   // decode scratch: B rows of the step's activations
   {
     const size_t Bn = c->B;
@@ -382,7 +384,7 @@ nc_status lmhead_ce_forward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt
 // dhf is written in DT (the element type inside the step, fp32 for the op).
 template <typename T, typename DT>
 nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tgt, const float* lse,
-                             int M, const float* d_inv_count, DT* dhf, float* dwlm) {
+                             int M, const float* d_inv_count, DT* dhf, float* dwlm, bool accumulate = false) {
   int d = c->d, V = c->V;
   T* g = wsp<T>(c, c->off.chunk);
   for (int r0 = 0; r0 < M; r0 += c->ce_rows) {
@@ -395,7 +397,7 @@ nc_status lmhead_ce_backward(nc_ctx* c, const T* hf, const T* wlm, const int* tg
     CKS(gemm(c, mk(rows, d, V, g, V, 1, wlm, d, 0, sizeof(DT) == 4 ? EPI_STORE_F32 : EPI_STORE,
                    dhf + (size_t)r0 * d, d)));
     CKS(gemm(c, mk(V, d, rows, g, V, 0, hf + (size_t)r0 * d, d, 0, EPI_STORE_F32, dwlm, d, 1.f,
-                   r0 == 0 ? 0.f : 1.f)));
+                   r0 == 0 && !accumulate ? 0.f : 1.f)));
   }
   return NC_OK;
 }
@@ -463,10 +465,20 @@ nc_status forward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, fl
   return NC_OK;
 }
 
+// G = d(loss)/d(params), or with accumulate G += scale * d(loss)/d(params):
+// the scale enters once, in the loss gradient (every other gradient is linear
+// in it), and every parameter gradient is then added instead of stored.
 template <typename T>
-nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* G) {
+nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, float* G, bool accumulate = false,
+                        float scale = 1.f) {
   int M = c->M, d = c->d, H = c->H, F = c->F, V = c->V, Tn = c->T;
   cudaStream_t s = c->stream;
+  const float gb = accumulate ? 1.f : 0.f;  // beta of every parameter-gradient GEMM
+  const float* gscale = wsp<float>(c, c->off.inv_count);
+  if (scale != 1.f) {
+    CK(scale_scalar(gscale, scale, wsp<float>(c, c->off.grad_scale), s));
+    gscale = wsp<float>(c, c->off.grad_scale);
+  }
   int rows, cols;
   float* dx = wsp<float>(c, c->off.dx);
   T* dxe = wsp<T>(c, c->off.dxe);
@@ -478,8 +490,8 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
   float* drow = wsp<float>(c, c->off.drow);
   const T* hf = wsp<T>(c, c->off.hf);
   size_t o_lm = param_offset(c, 1 + 4 * c->L, &rows, &cols);
-  CKS((lmhead_ce_backward<T, T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, wsp<float>(c, c->off.inv_count),
-                                dy, G + o_lm)));
+  CKS((lmhead_ce_backward<T, T>(c, hf, P + o_lm, tgt, wsp<float>(c, c->off.lse), M, gscale, dy, G + o_lm,
+                                accumulate)));
   KL(NC_FAM_ROWS, (double)M * d * (4 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, hf, wsp<float>(c, c->off.rf), dx, dxe, M, d, 0, s));
   for (int l = c->L - 1; l >= 0; --l) {
     size_t lb = (size_t)l * c->off.layer_stride;
@@ -497,15 +509,15 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     size_t of = param_offset(c, 3 + 4 * l, &rows, &cols);
     size_t op = param_offset(c, 4 + 4 * l, &rows, &cols);
     // MLP: x += relu2(xn2 Wfc^T) Wproj^T
-    CKS(gemm(c, mk(d, F, M, dxe, d, 0, a, F, 0, EPI_STORE_F32, G + op, F)));
+    CKS(gemm(c, mk(d, F, M, dxe, d, 0, a, F, 0, EPI_STORE_F32, G + op, F, 1.f, gb)));
     GemmArgs g1 = mk(M, F, d, dxe, d, 1, P + op, F, 0, EPI_RELU2_BWD, du, F);
     g1.C2 = const_cast<T*>(a); g1.ldc2 = F;  // relu(u) = sqrt(a)
     CKS(gemm(c, g1));
-    CKS(gemm(c, mk(F, d, M, du, F, 0, xn2, d, 0, EPI_STORE_F32, G + of, d)));
+    CKS(gemm(c, mk(F, d, M, du, F, 0, xn2, d, 0, EPI_STORE_F32, G + of, d, 1.f, gb)));
     CKS(gemm(c, mk(M, d, F, du, F, 1, P + of, d, 0, sizeof(T) == 4 ? EPI_STORE_F32 : EPI_STORE, dy, d)));
     KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
     // attention: x += attn(xn1) Wo^T
-    CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d)));
+    CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d, 1.f, gb)));
     CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
     KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + (sizeof(T) == 2 ? 12.0 : 4.0) * M * H, 1,
        attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s, sizeof(T) == 2 ? lse_att : nullptr,
@@ -515,11 +527,11 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
        attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv, fused_k ? rqk : nullptr));
     KL(NC_FAM_ROWS, (fused_k ? 1.0 : 2.0) * M * d * (4 + 2 * sizeof(T)) + 8.0 * M * H, 1,
        qk_norm_rope_bwd<T>(dqk, qkv, rqk, c->rope_cos, c->rope_sin, dqkv, M, Tn, H, s, fused_k ? 1 : 2));
-    CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d)));
+    CKS(gemm(c, mk(3 * d, d, M, dqkv, 3 * d, 0, xn1, d, 0, EPI_STORE_F32, G + oq, d, 1.f, gb)));
     CKS(gemm(c, mk(M, d, 3 * d, dqkv, 3 * d, 1, P + oq, d, 0, sizeof(T) == 4 ? EPI_STORE_F32 : EPI_STORE, dy, d)));
     KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
   }
-  CK(cudaMemsetAsync(G, 0, (size_t)V * d * sizeof(float), s));
+  if (!accumulate) CK(cudaMemsetAsync(G, 0, (size_t)V * d * sizeof(float), s));
   KL(NC_FAM_ROWS, 8.0 * M * d + 4.0 * M, 1, embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s));
   return NC_OK;
 }
@@ -870,6 +882,38 @@ nc_status nc_backward(nc_ctx* c, float* grads) {
   return c->prec == NC_BF16
              ? backward_impl<bf16>(c, static_cast<const bf16*>(c->params), c->tok, c->tgt, grads)
              : backward_impl<float>(c, static_cast<const float*>(c->params), c->tok, c->tgt, grads);
+}
+
+nc_status nc_backward_accumulate(nc_ctx* c, float* grads, float scale) {
+  if (!grads) return fail(NC_ERR_ARG, "grads is null");
+  if (!std::isfinite(scale)) return fail(NC_ERR_ARG, "scale must be finite");
+  CKS(check_ready(c));
+  if (!c->have_fwd) return fail(NC_ERR_STATE, "nc_backward_accumulate needs a successful forward first");
+  return c->prec == NC_BF16
+             ? backward_impl<bf16>(c, static_cast<const bf16*>(c->params), c->tok, c->tgt, grads, true, scale)
+             : backward_impl<float>(c, static_cast<const float*>(c->params), c->tok, c->tgt, grads, true, scale);
+}
+
+nc_status nc_forward_loss_u16(nc_ctx* c, const void* params, const uint16_t* packed, float* d_loss) {
+  if (!params || !packed || !d_loss) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_ready(c));
+  int* dt = wsp<int>(c, c->off.tok);
+  int* dg = wsp<int>(c, c->off.tgt);
+  CK(unpack_u16(packed, c->B, c->T, dt, dg, c->stream));
+  return forward_any(c, params, dt, dg, d_loss);
+}
+
+nc_status nc_train_step_host_u16(nc_ctx* c, const void* params, const uint16_t* h_packed, float* grads,
+                                 float* h_loss) {
+  if (!params || !h_packed || !grads || !h_loss) return fail(NC_ERR_ARG, "null pointer argument");
+  CKS(check_ready(c));
+  uint16_t* dp = wsp<uint16_t>(c, c->off.packed);
+  CK(cudaMemcpyAsync(dp, h_packed, (size_t)c->B * (c->T + 1) * 2, cudaMemcpyHostToDevice, c->stream));
+  float* dl = wsp<float>(c, c->off.loss);
+  CKS(nc_forward_loss_u16(c, params, dp, dl));
+  CKS(nc_backward(c, grads));
+  CK(cudaMemcpyAsync(h_loss, dl, sizeof(float), cudaMemcpyDeviceToHost, c->stream));
+  return read_status(c);
 }
 
 nc_status nc_train_step_host(nc_ctx* c, const void* params, const int32_t* h_tok, const int32_t* h_tgt,

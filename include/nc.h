@@ -121,6 +121,34 @@ nc_status nc_forward_loss_async(nc_ctx* ctx, const void* params, const int32_t* 
  * successful forward. Asynchronous. */
 nc_status nc_backward(nc_ctx* ctx, float* grads);
 
+/* Gradient accumulation over micro-batches (the pages' training loop sums
+ * the gradients of several micro-batches before one optimizer step): as
+ * nc_backward, but ADDS scale * d(loss)/d(params) to grads instead of
+ * overwriting them. The loss of each micro-batch is its own mean over its
+ * unmasked targets, so with scale = 1/n the sum over n calls is the gradient
+ * of the mean of the n micro-batch losses (for micro-batches with equal
+ * unmasked counts, the gradient of the whole batch's mean loss). grads must
+ * hold finite values (zero them before the first micro-batch). NC_ERR_ARG
+ * for a non-finite scale, NC_ERR_STATE without a preceding successful
+ * forward. Asynchronous. */
+nc_status nc_backward_accumulate(nc_ctx* ctx, float* grads, float scale);
+
+/* Forward + loss from packed uint16 token ids, the shard format of the
+ * pages' data loader (ids of a 65,536-entry vocabulary fit 16 bits): packed
+ * is a DEVICE array [batch, seq_len + 1] row-major; row b's ids 0..T-1 are
+ * the inputs and its ids 1..T the next-token targets (no masked targets).
+ * The ids are widened into the context's own token/target buffers, which
+ * the following backward uses; ids >= vocab report NC_ERR_DEVICE as in
+ * nc_forward_loss. The loss goes to DEVICE memory d_loss; asynchronous. */
+nc_status nc_forward_loss_u16(nc_ctx* ctx, const void* params, const uint16_t* packed, float* d_loss);
+
+/* One training step from HOST packed uint16 rows [batch, seq_len + 1]
+ * (ideally pinned; batch*(seq_len+1)*2 bytes are copied to the device):
+ * forward, loss and backward into grads (device, overwritten), the loss to
+ * *h_loss. Synchronises the stream. */
+nc_status nc_train_step_host_u16(nc_ctx* ctx, const void* params, const uint16_t* h_packed, float* grads,
+                                 float* h_loss);
+
 /* One training step from HOST token buffers: copies tokens and targets
  * (host int32 [batch, seq_len], ideally pinned) to the device, runs the
  * forward and backward on device-resident params/grads, and copies the loss

@@ -9,5 +9,5 @@ from .model import (EPS, HEAD_DIM, IGNORE, ROPE_BASE, Shape, backward, causal_at
                     causal_attention_backward, cross_entropy_backward,
                     cross_entropy_rows, forward, layout, param_count, relu2,
                     relu2_backward, rmsnorm, rmsnorm_backward, rope,
-                    rope_angles, rope_backward, step, unpack)
+                    rope_angles, rope_backward, split_packed, step, step_accumulated, unpack)
 from . import infer, optim

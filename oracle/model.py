@@ -28,6 +28,17 @@ pos * 10000^(-j/64), positions from 0 in every sequence, angles formed in
 float64; attention scale 1/sqrt(128); no biases, dropout or logit capping;
 loss = mean over all B*T positions in nats; argmax = lowest index among ties.
 
+Token input ("Streaming Tokenization": the shards hold packed 16-bit token
+ids that the loader reads as they are; "Pretraining": the target of each
+position is the next token): a row of T+1 ids gives the inputs ids[0..T-1]
+and the targets ids[1..T] (split_packed).
+
+Several batches, one update ("Distributed Training": every GPU runs the step
+on its own shard and the gradients are averaged by an all-reduce after the
+backward): step_accumulated averages the losses and gradients of n
+micro-batches, which is what n accumulating backward passes with scale 1/n
+produce on one GPU.
+
 The supervised fine-tuning variant ("Supervised Fine-Tuning (SFT)": the same
 cross-entropy, but only on the assistant's response tokens; the prompt tokens
 are masked from the loss) is expressed by the target id IGNORE (-1): such a
@@ -350,3 +361,23 @@ def step(params, tokens, targets, s: Shape, dtype=np.float64):
     """Convenience: (loss, flat grads, cache)."""
     loss, cache = forward(params, tokens, targets, s, dtype)
     return loss, backward(cache), cache
+
+
+def split_packed(packed):
+    """Packed token rows [B, T+1] -> (inputs [B, T], next-token targets
+    [B, T]) as int32: position t of row b reads id t and predicts id t+1."""
+    ids = np.asarray(packed).astype(np.int64)
+    return ids[:, :-1].astype(np.int32), ids[:, 1:].astype(np.int32)
+
+
+def step_accumulated(params, micro_batches, s: Shape, dtype=np.float64):
+    """Mean loss and mean gradient over micro-batches [(tokens, targets), ...],
+    each micro-batch's loss being its own mean over its positions: the
+    gradient that shard-wise averaging (or accumulation with scale 1/n) forms."""
+    n = len(micro_batches)
+    loss_sum, grad_sum = 0.0, None
+    for tok, tgt in micro_batches:
+        loss, g, _ = step(params, tok, tgt, s, dtype)
+        loss_sum += loss
+        grad_sum = g.astype(np.float64) if grad_sum is None else grad_sum + g
+    return loss_sum / n, grad_sum / n

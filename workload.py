@@ -192,15 +192,28 @@ def zipf_cdf(vocab: int, s: float = 1.1) -> np.ndarray:
     return c / c[-1]
 
 
-def make_tokens(w: Workload, seed: int = 0):
-    """(tokens, targets) int32 [B, T]: Zipf(1.1) ids, targets = next token."""
+def _token_rows(w: Workload, seed: int):
+    """[B, T+1] Zipf(1.1) ids (int64), one row of T+1 ids per sequence."""
     rng = np.random.Generator(np.random.PCG64(seed + 1))
     cdf = zipf_cdf(w.vocab)
     u = rng.random(w.batch * (w.seq_len + 1))
     ids = np.searchsorted(cdf, u, side="right")
-    ids = np.minimum(ids, w.vocab - 1).astype(np.int32)
-    ids = ids.reshape(w.batch, w.seq_len + 1)
+    ids = np.minimum(ids, w.vocab - 1)
+    return ids.reshape(w.batch, w.seq_len + 1)
+
+
+def make_tokens(w: Workload, seed: int = 0):
+    """(tokens, targets) int32 [B, T]: Zipf(1.1) ids, targets = next token."""
+    ids = _token_rows(w, seed).astype(np.int32)
     return np.ascontiguousarray(ids[:, :-1]), np.ascontiguousarray(ids[:, 1:])
+
+
+def make_packed_tokens(w: Workload, seed: int = 0):
+    """The same draw as make_tokens(w, seed), as packed uint16 rows [B, T+1]
+    (the token-shard format: ids of a vocabulary of at most 65,536 entries)."""
+    if w.vocab > 65536:
+        raise ValueError("uint16 rows need vocab <= 65536")
+    return np.ascontiguousarray(_token_rows(w, seed).astype(np.uint16))
 
 
 def model_flops_per_token(w: Workload) -> float:
