@@ -743,71 +743,70 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (p.rqk) {
         // warp ch = 0 finishes dk for whole head rows; warp ch = 1 writes dv
         if (ch == 0) {
-          // dk_hat = acc (dS' carried the score scale); dk_n = R^T dk_hat and k_n = R^T k_hat (k_hat
-          // read back from qkv); dk = rk * (dk_n - k_n * mean(dk_n * k_n)).
-          // Pass 1 rotates 16 pairs at a time back into the dK columns of TMEM
-          // and accumulates the dot; pass 2 finishes and stores.
+          // dk_hat = acc (dS' carried the score scale). With R the RoPE rotation
+          // of the row's position, k_n = R^T k_hat and dk_n = R^T dk_hat, the
+          // RMSNorm backward dk = rk (dk_n - k_n mean(dk_n k_n)) equals
+          // rk R^T (dk_hat - k_hat mean(dk_hat k_hat)): a rotation keeps dot
+          // products, so the mean needs neither the table nor a rotation, and
+          // one pass over the pairs un-rotates and finishes. k_hat is read
+          // back from qkv once and kept packed.
           const int t = u.kt * TILE + r;
           const float* cs = p.rope_cos + (size_t)t * 64;
           const float* sn = p.rope_sin + (size_t)t * 64;
           const bf16* krow = p.qkv + m * 3 * d + d + h * 128;
           const uint32_t tk = tdK + lane_off;
+          uint4 kr[16];  // k_hat, 8 dims per entry
+#pragma unroll
+          for (int q8 = 0; q8 < 16; ++q8) kr[q8] = __ldg(reinterpret_cast<const uint4*>(krow) + q8);
           float dot = 0.f;
 #pragma unroll
-          for (int pass = 0; pass < 2; ++pass) {
-            const float rk = pass ? p.rqk[m * 2 * p.H + p.H + h] : 0.f;
-            const float dmean = dot * (1.f / 128.f);
+          for (int c = 0; c < 4; ++c) {  // 32 dims at a time
+            float g[32];
+            tc::tmem_ld32(tk + c * 32, g);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {  // 16 rotation pairs at a time
-              // operands from global memory first, so their latency overlaps the TMEM load
-              uint4 kr1[2], kr2[2];
-              float4 ca[2], cb[2], sa[2], sb[2];
+            for (int q8 = 0; q8 < 4; ++q8) {
+              float k8[8];
+              unpack8(kr[c * 4 + q8], k8);
 #pragma unroll
-              for (int c8 = 0; c8 < 2; ++c8) {
-                const int q8 = c * 2 + c8;
-                kr1[c8] = __ldg(reinterpret_cast<const uint4*>(krow) + q8);
-                kr2[c8] = __ldg(reinterpret_cast<const uint4*>(krow + 64) + q8);
-                ca[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8);
-                cb[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8 + 1);
-                sa[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8);
-                sb[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8 + 1);
+              for (int i = 0; i < 8; ++i) dot += g[q8 * 8 + i] * k8[i];
+            }
+          }
+          const float rk = p.rqk[m * 2 * p.H + p.H + h];
+          const float dmean = dot * (1.f / 128.f);
+          bf16* row = p.dqkv + m * 3 * d + d + h * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {  // 16 rotation pairs (j, j + 64) at a time
+            // the table first, so its latency overlaps the TMEM load
+            float4 ca[2], cb[2], sa[2], sb[2];
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8) {
+              const int q8 = c * 2 + c8;
+              ca[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8);
+              cb[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8 + 1);
+              sa[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8);
+              sb[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8 + 1);
+            }
+            float g1[16], g2[16];
+            tc::tmem_ld16x2(tk + c * 16, tk + 64 + c * 16, g1, g2);
+#pragma unroll
+            for (int c8 = 0; c8 < 2; ++c8) {
+              float k1[8], k2[8];
+              unpack8(kr[c * 2 + c8], k1);
+              unpack8(kr[8 + c * 2 + c8], k2);
+              const float cc[8] = {ca[c8].x, ca[c8].y, ca[c8].z, ca[c8].w, cb[c8].x, cb[c8].y, cb[c8].z, cb[c8].w};
+              const float ss[8] = {sa[c8].x, sa[c8].y, sa[c8].z, sa[c8].w, sb[c8].x, sb[c8].y, sb[c8].z, sb[c8].w};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int e = c8 * 8 + i;
+                const float w1 = g1[e] - k1[i] * dmean, w2 = g2[e] - k2[i] * dmean;
+                g1[e] = rk * (w1 * cc[i] + w2 * ss[i]);
+                g2[e] = rk * (-w1 * ss[i] + w2 * cc[i]);
               }
-              float g1[16], g2[16];
-              tc::tmem_ld16x2(tk + c * 16, tk + 64 + c * 16, g1, g2);
+            }
 #pragma unroll
-              for (int c8 = 0; c8 < 2; ++c8) {
-                float k1[8], k2[8];
-                unpack8(kr1[c8], k1);
-                unpack8(kr2[c8], k2);
-                const float cc[8] = {ca[c8].x, ca[c8].y, ca[c8].z, ca[c8].w, cb[c8].x, cb[c8].y, cb[c8].z, cb[c8].w};
-                const float ss[8] = {sa[c8].x, sa[c8].y, sa[c8].z, sa[c8].w, sb[c8].x, sb[c8].y, sb[c8].z, sb[c8].w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                  const int e = c8 * 8 + i;
-                  const float kn1 = k1[i] * cc[i] + k2[i] * ss[i];
-                  const float kn2 = -k1[i] * ss[i] + k2[i] * cc[i];
-                  if (pass == 0) {
-                    const float a = g1[e], bb = g2[e];
-                    g1[e] = a * cc[i] + bb * ss[i];
-                    g2[e] = -a * ss[i] + bb * cc[i];
-                    dot += g1[e] * kn1 + g2[e] * kn2;
-                  } else {
-                    g1[e] = rk * (g1[e] - kn1 * dmean);
-                    g2[e] = rk * (g2[e] - kn2 * dmean);
-                  }
-                }
-              }
-              if (pass == 0) {
-                tc::tmem_st16(tk + c * 16, g1);
-                tc::tmem_st16(tk + 64 + c * 16, g2);
-              } else {
-                bf16* row = p.dqkv + m * 3 * d + d + h * 128;
-#pragma unroll
-                for (int gq = 0; gq < 2; ++gq) {
-                  *reinterpret_cast<uint4*>(row + c * 16 + gq * 8) = pack8(g1 + 8 * gq);
-                  *reinterpret_cast<uint4*>(row + 64 + c * 16 + gq * 8) = pack8(g2 + 8 * gq);
-                }
-              }
+            for (int gq = 0; gq < 2; ++gq) {
+              *reinterpret_cast<uint4*>(row + c * 16 + gq * 8) = pack8(g1 + 8 * gq);
+              *reinterpret_cast<uint4*>(row + 64 + c * 16 + gq * 8) = pack8(g2 + 8 * gq);
             }
           }
         } else {
