@@ -221,7 +221,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* c2bar = drain + 1;  // per epilogue warp: its staging buffer holds the C2 chunk it loaded
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(c2bar + NEPI_WARPS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const GemmArgs& g = p.g;
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc::mbar_init(tempty + b, CL * NEPI_WARPS);  // one arrival per epilogue warp (of both CTAs)
     }
     tc::mbar_init(drain, 1);
+    for (int w = 0; w < NEPI_WARPS; ++w) tc::mbar_init(c2bar + w, 1);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -387,6 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int ch = (warp - 2) >> 2;    // which 128-column half of the tile
     const int row = q * 32 + lane;
     Stager stg{sStage + (warp - 2) * STAGING_BYTES, lane};
+    uint32_t c2n = 0;  // C2 chunks this warp has loaded (its barrier's phase)
     int cnt = 0;
     for (int v = v_first; v < p.total && !failed; v += v_step, ++cnt) {
       int bt, m0, nb, split, kb0, kb1;
@@ -508,6 +511,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             float* w = v + h2 * 64;
+            const int nc0 = n0 + h2 * 64;
+            const bool chunk_ok = blk_ok && nc0 < g.N;
+            if (EPI == EPI_RELU2_BWD && chunk_ok) {
+              // this warp's 32 rows x 64 columns of C2 land in its staging
+              // buffer by one tensor load (rows past M and columns past N read
+              // as 0) while the accumulator is read: coalesced, where a row
+              // per thread would cost a wavefront per 16 bytes
+              stg.begin();
+              if (lane == 0) {
+                tc::mbar_arrive_expect_tx(c2bar + (warp - 2), 32 * 128);
+                tc::tma_load_2d(stg.buf, &tc2, nc0, rblk, c2bar + (warp - 2));
+              }
+            }
             if (EPI != EPI_QKNORM_ROPE) {
               if (have_acc) tc::tmem_ld32x2(taddr + h2 * 64, taddr + h2 * 64 + 32, w, w + 32);
               else
@@ -516,22 +532,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
               for (int i = 0; i < 64; ++i) w[i] *= g.alpha;
             }
-            const int nc0 = n0 + h2 * 64;
-            if (!blk_ok || nc0 >= g.N) continue;
+            if (!chunk_ok) continue;
             if (EPI == EPI_RELU2_BWD) {
-              if (row_ok) {
-                const bf16* u = static_cast<const bf16*>(g.C2) + (size_t)m * g.ldc2 + nc0;
+              const bool got = tc::mbar_wait(c2bar + (warp - 2), c2n & 1, abort_flag, kWaitNs);
+              ++c2n;
+              if (!__all_sync(0xffffffffu, got)) {
+                failed = true;
+                *abort_flag = 1;
+              }
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                  float uf[8];
-                  if (nc0 + 8 * j < g.N) unpack8_bf16(*reinterpret_cast<const uint4*>(u + 8 * j), uf);
-                  else
+              for (int j = 0; j < 8; ++j) {
+                float uf[8];
+                unpack8_bf16(*reinterpret_cast<const uint4*>(stg.buf + lane * 128 + ((j ^ (lane & 7)) << 4)), uf);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) uf[i] = 0.f;
-#pragma unroll
-                  // C2 holds a = relu(u)^2, so relu(u) = sqrt(a)
-                  for (int i = 0; i < 8; ++i) w[8 * j + i] *= 2.f * tc::sqrt_approx(fmaxf(uf[i], 0.f));
-                }
+                // C2 holds a = relu(u)^2, so relu(u) = sqrt(a)
+                for (int i = 0; i < 8; ++i) w[8 * j + i] *= 2.f * tc::sqrt_approx(fmaxf(uf[i], 0.f));
               }
             } else if (EPI == EPI_RELU2A) {
 #pragma unroll
@@ -768,7 +783,8 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   CUtensorMap tcm = ta, tcm2 = ta;  // unused maps stay valid copies
   const bool f32out = g.epi == EPI_STORE_F32;
   if (g.epi != EPI_CE_FWD) ok = make_out_map(&tcm, g.C, f32out, g.N, c_rows, g.ldc);
-  if (ok && g.epi == EPI_RELU2) ok = make_out_map(&tcm2, g.C2, false, g.N, g.M, g.ldc2);
+  // RELU2's second output a, or RELU2_BWD's input a (loaded in 32 x 64 chunks)
+  if (ok && (g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD)) ok = make_out_map(&tcm2, g.C2, false, g.N, g.M, g.ldc2);
   if (!ok) return cudaErrorInvalidValue;
   TcParams p;
   p.g = g;
