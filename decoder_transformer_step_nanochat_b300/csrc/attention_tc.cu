@@ -97,7 +97,7 @@ struct AttnParams {
   float* dk;      // backward: fp32 [B*T, d] (dk_hat), unless the k half is finished in-kernel
   bf16* dqkv;     // backward: dv goes to its v columns (and dk to its k columns when finished)
   // finishing the k half in-kernel (QK-norm + RoPE backward of k): needs rstd of
-  // the k heads (rqk [B*T, 2H]) and the RoPE table ([T, 64] cos / sin)
+  // the k heads (rqk [B*T, 2H]) and the RoPE table (angle-major [16][T][4] cos / sin)
   const float* rqk;
   const float* rope_cos;
   const float* rope_sin;
@@ -751,8 +751,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           // one pass over the pairs un-rotates and finishes. k_hat is read
           // back from qkv once and kept packed.
           const int t = u.kt * TILE + r;
-          const float* cs = p.rope_cos + (size_t)t * 64;
-          const float* sn = p.rope_sin + (size_t)t * 64;
+          // angle-major tables [16][T][4]: the warp's 32 positions read 512 contiguous bytes
+          const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos) + t;
+          const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin) + t;
           const bf16* krow = p.qkv + m * 3 * d + d + h * 128;
           const uint32_t tk = tdK + lane_off;
           uint4 kr[16];  // k_hat, 8 dims per entry
@@ -781,10 +782,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
             for (int c8 = 0; c8 < 2; ++c8) {
               const int q8 = c * 2 + c8;
-              ca[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8);
-              cb[c8] = __ldg(reinterpret_cast<const float4*>(cs) + 2 * q8 + 1);
-              sa[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8);
-              sb[c8] = __ldg(reinterpret_cast<const float4*>(sn) + 2 * q8 + 1);
+              ca[c8] = __ldg(cs4 + (size_t)(2 * q8) * p.T);
+              cb[c8] = __ldg(cs4 + (size_t)(2 * q8 + 1) * p.T);
+              sa[c8] = __ldg(sn4 + (size_t)(2 * q8) * p.T);
+              sb[c8] = __ldg(sn4 + (size_t)(2 * q8 + 1) * p.T);
             }
             float g1[16], g2[16];
             tc::tmem_ld16x2(tk + c * 16, tk + 64 + c * 16, g1, g2);

@@ -489,12 +489,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               if (n0 < 2 * g.d_model) {
                 const float rr = rsqrtf(ss * (1.f / 128.f) + kEps);
                 const int t = m % g.seq_len;
-                const float* cs = g.rope_cos + (size_t)t * 64;
-                const float* sn = g.rope_sin + (size_t)t * 64;
+                // angle-major table: the warp's 32 positions read 512 contiguous bytes
+                const float4* cs4 = reinterpret_cast<const float4*>(g.rope_cos) + t;
+                const float4* sn4 = reinterpret_cast<const float4*>(g.rope_sin) + t;
 #pragma unroll
                 for (int j4 = 0; j4 < 16; ++j4) {
-                  const float4 c4 = __ldg(reinterpret_cast<const float4*>(cs) + j4);
-                  const float4 s4 = __ldg(reinterpret_cast<const float4*>(sn) + j4);
+                  const float4 c4 = __ldg(cs4 + (size_t)j4 * g.seq_len);
+                  const float4 s4 = __ldg(sn4 + (size_t)j4 * g.seq_len);
                   const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
                   for (int u = 0; u < 4; ++u) {

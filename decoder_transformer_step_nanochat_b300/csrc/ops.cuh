@@ -37,7 +37,9 @@ struct GemmArgs {
   float* p_max = nullptr; float* p_sum = nullptr; int* p_arg = nullptr;
   float* p_tgt = nullptr;        // [M]: logit of the target column
   // QK-norm + RoPE epilogue
-  const float* rope_cos = nullptr; const float* rope_sin = nullptr;  // [T,64]
+  // angle-major RoPE table [16][seq_len][4]: entry (g, t, u) is angle 4g + u
+  // at position t, so 32 consecutive rows read 512 contiguous bytes
+  const float* rope_cos = nullptr; const float* rope_sin = nullptr;
   float* rqk = nullptr;          // [M, 2H] rstd of q heads then k heads
   int seq_len = 0, d_model = 0;
   // split-K (EPI_STORE_F32 only): splits > 1 writes alpha*partial sums to
@@ -108,7 +110,8 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
 // status points at two device words: the status word and, after it, a counter
 // the kernel schedules its work units with (reset here before the launch).
 // L2row is the forward's lse in the negated, base-2, score-scale-folded form
-// that attn_rowdot writes next to Drow when given lse.
+// that attn_rowdot writes next to Drow when given lse. rope_cos / rope_sin
+// are the angle-major tables [16][T][4] (as in GemmArgs).
 cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, const float* Drow, float* dq,
                         float* dk, bf16* dqkv, int B, int T, int H, int* status, cudaStream_t s,
                         const float* rqk = nullptr, const float* rope_cos = nullptr,

@@ -73,8 +73,10 @@ struct nc_ctx {
   cudaStream_t stream = nullptr;
   int device = -1;
   bool use_tc = false;      // tensor-core GEMMs for the bf16 mode
-  float* rope_cos = nullptr;
+  float* rope_cos = nullptr;   // [T][64]
   float* rope_sin = nullptr;
+  float* rope_cos4 = nullptr;  // the same angles, angle-major [16][T][4] (GEMM and attention epilogues)
+  float* rope_sin4 = nullptr;
   int* status = nullptr;    // device status word
   // workspace
   char* ws = nullptr;
@@ -346,8 +348,8 @@ cudaError_t attn_bwd(nc_ctx* c, const T* qkv, const T* dout, const float* lse, c
                      T* dqkv, const float* rqk = nullptr) {
   if constexpr (sizeof(T) == 2)  // the tensor-core kernel reads the negated base-2 lse written after drow
     return attn_bwd_tc(qkv, dout, drow + (size_t)c->M * c->H, drow, dqk, dqk + (size_t)c->M * c->d, dqkv, c->B,
-                       c->T, c->H, c->status, c->stream, rqk, rqk ? c->rope_cos : nullptr,
-                       rqk ? c->rope_sin : nullptr);
+                       c->T, c->H, c->status, c->stream, rqk, rqk ? c->rope_cos4 : nullptr,
+                       rqk ? c->rope_sin4 : nullptr);
   else
     return attn_bwd_simt<T>(qkv, dout, lse, drow, dqk, dqkv, c->B, c->T, c->H, c->stream);
 }
@@ -430,7 +432,7 @@ nc_status forward_blocks(nc_ctx* c, const T* P, const int* tok) {
     if (c->use_tc) {
       // QK-norm + RoPE fused into the QKV GEMM epilogue
       GemmArgs gq = mk(M, 3 * d, d, xn1, d, 1, Wqkv, d, 1, EPI_QKNORM_ROPE, qkv, 3 * d);
-      gq.rope_cos = c->rope_cos; gq.rope_sin = c->rope_sin; gq.rqk = rqk;
+      gq.rope_cos = c->rope_cos4; gq.rope_sin = c->rope_sin4; gq.rqk = rqk;
       gq.seq_len = Tn; gq.d_model = d;
       CKS(gemm(c, gq));
     } else {
@@ -808,21 +810,34 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
     return fail(NC_ERR_UNSUPPORTED, "this library is built for sm_103a (B300); device is sm_%d%d", prop.major, prop.minor);
   if (c->rope_cos) { cudaFree(c->rope_cos); c->rope_cos = nullptr; }
   if (c->rope_sin) { cudaFree(c->rope_sin); c->rope_sin = nullptr; }
+  if (c->rope_cos4) { cudaFree(c->rope_cos4); c->rope_cos4 = nullptr; }
+  if (c->rope_sin4) { cudaFree(c->rope_sin4); c->rope_sin4 = nullptr; }
   // device words: [0] status, [1] work-unit counter of the persistent attention backward
   if (!c->status) CK(cudaMalloc(&c->status, 16 * sizeof(int)));
   // RoPE table: angle pos * 10000^(-j/64) formed in float64, stored fp32.
+  // Also stored angle-major in groups of four angles, [16][T][4], for the
+  // epilogues whose threads each own one position: consecutive threads then
+  // read consecutive 16-byte pieces.
   std::vector<float> hc((size_t)c->T * kHalf), hs((size_t)c->T * kHalf);
+  std::vector<float> hc4((size_t)c->T * kHalf), hs4((size_t)c->T * kHalf);
   for (int t = 0; t < c->T; ++t)
     for (int j = 0; j < kHalf; ++j) {
       double ang = (double)t * pow(10000.0, -(double)j / (double)kHalf);
       hc[(size_t)t * kHalf + j] = (float)cos(ang);
       hs[(size_t)t * kHalf + j] = (float)sin(ang);
+      const size_t i4 = ((size_t)(j / 4) * c->T + t) * 4 + j % 4;
+      hc4[i4] = hc[(size_t)t * kHalf + j];
+      hs4[i4] = hs[(size_t)t * kHalf + j];
     }
   CK(cudaMalloc(&c->rope_cos, hc.size() * sizeof(float)));
   CK(cudaMalloc(&c->rope_sin, hs.size() * sizeof(float)));
+  CK(cudaMalloc(&c->rope_cos4, hc4.size() * sizeof(float)));
+  CK(cudaMalloc(&c->rope_sin4, hs4.size() * sizeof(float)));
   c->stream = static_cast<cudaStream_t>(stream);
   CK(cudaMemcpyAsync(c->rope_cos, hc.data(), hc.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->rope_sin, hs.data(), hs.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->rope_cos4, hc4.data(), hc4.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
+  CK(cudaMemcpyAsync(c->rope_sin4, hs4.data(), hs4.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemsetAsync(c->status, 0, sizeof(int), c->stream));
   CK(cudaStreamSynchronize(c->stream));
   c->device = dev;
@@ -999,6 +1014,8 @@ void nc_destroy(nc_ctx* c) {
   for (auto e : c->pool) cudaEventDestroy(e);
   if (c->rope_cos) cudaFree(c->rope_cos);
   if (c->rope_sin) cudaFree(c->rope_sin);
+  if (c->rope_cos4) cudaFree(c->rope_cos4);
+  if (c->rope_sin4) cudaFree(c->rope_sin4);
   if (c->status) cudaFree(c->status);
   delete c;
 }
@@ -1023,7 +1040,7 @@ nc_status nc_op_gemm(nc_ctx* c, int M, int N, int K, const void* A, long long ld
   if (epi == EPI_QKNORM_ROPE) {
     g.C2 = nullptr;
     g.rqk = static_cast<float*>(C2);
-    g.rope_cos = c->rope_cos; g.rope_sin = c->rope_sin; g.seq_len = c->T; g.d_model = c->d;
+    g.rope_cos = c->rope_cos4; g.rope_sin = c->rope_sin4; g.seq_len = c->T; g.d_model = c->d;
   }
   return gemm(c, g);
 }
