@@ -273,13 +273,14 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
         for (int i = 0; i < 128; ++i)
           if (i > r) v[i] = -INFINITY;
       }
+      // row maximum: four chains of three-input maxima
       float mx4[4] = {v[0], v[1], v[2], v[3]};
 #pragma unroll
-      for (int i = 4; i < 128; i += 4) {
-        mx4[0] = fmaxf(mx4[0], v[i]);
-        mx4[1] = fmaxf(mx4[1], v[i + 1]);
-        mx4[2] = fmaxf(mx4[2], v[i + 2]);
-        mx4[3] = fmaxf(mx4[3], v[i + 3]);
+      for (int i = 4; i < 128; i += 8) {
+        mx4[0] = tc::fmax3(mx4[0], v[i], v[i + 4]);
+        mx4[1] = tc::fmax3(mx4[1], v[i + 1], v[i + 5]);
+        mx4[2] = tc::fmax3(mx4[2], v[i + 2], v[i + 6]);
+        mx4[3] = tc::fmax3(mx4[3], v[i + 3], v[i + 7]);
       }
       const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
       const bool grow = mx > m + kRescaleLog2;
@@ -299,18 +300,21 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
           }
         }
       }
-      const float nm = -m;
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // P = exp2(S * log2(e)/sqrt(128) - m) on fp32 pairs; the row sum in
+      // two paired accumulators
+      const uint64_t sl2x2 = tc::f2pack(sl2, sl2), nm2 = tc::f2pack(-m, -m);
+      uint64_t rs2[2] = {tc::f2pack(0.f, 0.f), tc::f2pack(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float e0 = tc::ex2(fmaf(v[2 * i], sl2, nm));
-        const float e1 = tc::ex2(fmaf(v[2 * i + 1], sl2, nm));
-        rs[i & 3] += e0 + e1;
+        const float2 x = tc::f2unpack(tc::ffma2(tc::f2pack(v[2 * i], v[2 * i + 1]), sl2x2, nm2));
+        const float e0 = tc::ex2(x.x), e1 = tc::ex2(x.y);
+        rs2[i & 1] = tc::fadd2(rs2[i & 1], tc::f2pack(e0, e1));
         __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
         pk[i] = *reinterpret_cast<uint32_t*>(&h2);
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      const float2 ra = tc::f2unpack(rs2[0]), rb = tc::f2unpack(rs2[1]);
+      l += (ra.x + ra.y) + (rb.x + rb.y);
       tc::tmem_st32(tS, reinterpret_cast<const float*>(pk));
       tc::tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
       tc::tc_fence_before();
