@@ -77,6 +77,8 @@ struct nc_ctx {
   float* rope_sin = nullptr;
   float* rope_cos4 = nullptr;  // the same angles, angle-major [16][T][4] (GEMM and attention epilogues)
   float* rope_sin4 = nullptr;
+  float* dec_rope = nullptr;   // decode RoPE table for dec_rope_len positions: cos [len][64] then sin
+  int dec_rope_len = 0;
   int* status = nullptr;    // device status word
   // workspace
   char* ws = nullptr;
@@ -695,11 +697,21 @@ void rope_table(int n, std::vector<float>& hc, std::vector<float>& hs) {
 template <typename T>
 nc_status prefill_impl(nc_ctx* c, const T* P, const int* tok, char* kv, int max_len, int32_t* next, float* logits) {
   const KvLayout kl = kv_layout(c, max_len);
-  std::vector<float> hc, hs;
-  rope_table(max_len, hc, hs);
-  CK(cudaMemcpyAsync(kv + kl.rc, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, c->stream));
-  CK(cudaMemcpyAsync(kv + kl.rs, hs.data(), hs.size() * 4, cudaMemcpyHostToDevice, c->stream));
-  CK(cudaStreamSynchronize(c->stream));  // the host tables go out of scope
+  // the table for max_len positions is built on the host once per length and
+  // kept on the device; each prefill copies it into the cache device to device
+  if (c->dec_rope_len != max_len) {
+    if (c->dec_rope) { cudaFree(c->dec_rope); c->dec_rope = nullptr; c->dec_rope_len = 0; }
+    std::vector<float> hc, hs;
+    rope_table(max_len, hc, hs);
+    CK(cudaMalloc(&c->dec_rope, 2 * hc.size() * 4));
+    CK(cudaMemcpyAsync(c->dec_rope, hc.data(), hc.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaMemcpyAsync(c->dec_rope + hc.size(), hs.data(), hs.size() * 4, cudaMemcpyHostToDevice, c->stream));
+    CK(cudaStreamSynchronize(c->stream));  // the host tables go out of scope
+    c->dec_rope_len = max_len;
+  }
+  const size_t tab = (size_t)max_len * kHalf;
+  CK(cudaMemcpyAsync(kv + kl.rc, c->dec_rope, tab * 4, cudaMemcpyDeviceToDevice, c->stream));
+  CK(cudaMemcpyAsync(kv + kl.rs, c->dec_rope + tab, tab * 4, cudaMemcpyDeviceToDevice, c->stream));
   CKS(forward_blocks<T>(c, P, tok));
   for (int l = 0; l < c->L; ++l) {
     const T* qkv = wsp<T>(c, (size_t)l * c->off.layer_stride + c->off.qkv);
@@ -1016,6 +1028,7 @@ void nc_destroy(nc_ctx* c) {
   if (c->rope_sin) cudaFree(c->rope_sin);
   if (c->rope_cos4) cudaFree(c->rope_cos4);
   if (c->rope_sin4) cudaFree(c->rope_sin4);
+  if (c->dec_rope) cudaFree(c->dec_rope);
   if (c->status) cudaFree(c->status);
   delete c;
 }

@@ -40,8 +40,10 @@ size_t nc_kv_cache_bytes(const nc_ctx* ctx, int max_len);
  * model, write positions 0..T-1 of the cache and the RoPE table, and the
  * greedy next token of every sequence into next_tokens (device int32 [B]).
  * last_logits (device fp32 [B, vocab], may be NULL) receives the logits of
- * position T-1. Requires T <= max_len <= 65536. Synchronises the stream
- * once, to upload the RoPE table. NC_ERR_DEVICE for an id out of range. */
+ * position T-1. Requires T <= max_len <= 65536. The first call with a given
+ * max_len builds the RoPE table on the host and keeps it on the device (one
+ * stream synchronisation); later calls copy it into the cache on the device
+ * and do not synchronise. NC_ERR_DEVICE for an id out of range. */
 nc_status nc_prefill(nc_ctx* ctx, const void* params, const int32_t* tokens, void* kv_cache, int max_len,
                      int32_t* next_tokens, float* last_logits);
 
