@@ -1,13 +1,14 @@
 // bf16 GEMM on the 5th-generation tensor cores (tcgen05, sm_103a) with the
-// step's fused epilogues: plain store, fp32 store/accumulate, ReLU^2 (stores
-// u and relu(u)^2), ReLU^2 backward, cross-entropy forward partials
-// (per-row max / sum-exp / argmax / target logit over each 256-wide vocabulary
-// tile, so the logits are never written) and cross-entropy backward
-// (softmax - onehot).
+// step's fused epilogues: plain store, fp32 store/accumulate, ReLU^2 (u and
+// relu(u)^2, or relu(u)^2 alone), ReLU^2 backward (dA * 2 sqrt(a), a loaded
+// by TMA), QKV with per-head RMSNorm + RoPE, cross-entropy forward partials
+// (per-row max / sum-exp / argmax / target logit over each 128-column
+// vocabulary half-tile, so the logits are never written), cross-entropy
+// backward (softmax - onehot) and alpha acc + beta C2 (the optimizer).
 //
 // Structure: persistent CTAs (one per SM), 128x256 output tiles, 64-deep k
-// slices of bf16 staged by TMA into 128-byte-swizzled shared memory in a
-// 4-stage mbarrier ring; warp 0 issues TMA, one thread of warp 1 issues
+// slices of bf16 staged by TMA into 128-byte-swizzled shared memory in an
+// mbarrier ring (4 stages for single CTAs, 6 for CTA pairs); warp 0 issues TMA, one thread of warp 1 issues
 // tcgen05.mma into a TMEM accumulator (two 256-column buffers, so the
 // epilogue of tile i overlaps the main loop of tile i+1), warps 2..9 read the
 // accumulator with tcgen05.ld (one thread per output row and 128-column half)

@@ -149,18 +149,6 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// As tma_load_2d, but the tile lands at the same shared-memory offset in
-// every CTA of the cluster named by `mask` and completes bytes on the
-// mbarrier at the same offset in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(void* smem_dst, const CUtensorMap* map, int x, int y,
-                                                      uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
-      : "memory");
-}
-
 // As tma_load_2d, for a CTA pair running 2-SM MMAs: the tile lands in this
 // CTA's shared memory and completes its bytes on the mbarrier at the
 // shared::cluster address `bar_cl`, which may be in the peer CTA.
@@ -309,15 +297,6 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    smem_u32(bar))
-               : "memory");
-}
-
-// Arrive once on the mbarrier at this offset in every CTA of `mask` when
-// every tcgen05.mma this thread issued so far is done.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(mask)
                : "memory");
 }
 
