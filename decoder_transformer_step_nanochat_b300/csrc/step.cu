@@ -824,6 +824,9 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   if (c->rope_sin) { cudaFree(c->rope_sin); c->rope_sin = nullptr; }
   if (c->rope_cos4) { cudaFree(c->rope_cos4); c->rope_cos4 = nullptr; }
   if (c->rope_sin4) { cudaFree(c->rope_sin4); c->rope_sin4 = nullptr; }
+  // the decode table is rebuilt on the (possibly different) device by the next prefill
+  if (c->dec_rope) { cudaFree(c->dec_rope); c->dec_rope = nullptr; }
+  c->dec_rope_len = 0;
   // device words: [0] status, [1] work-unit counter of the persistent attention backward
   if (!c->status) CK(cudaMalloc(&c->status, 16 * sizeof(int)));
   // RoPE table: angle pos * 10000^(-j/64) formed in float64, stored fp32.
