@@ -113,3 +113,28 @@ def test_configure_without_gpu_reports_cuda_error(nc):
         assert ei.value.status == 3  # NC_ERR_CUDA
     finally:
         nc.nc_destroy(ctx)
+
+
+def test_accumulation_and_u16_entry_points_validate_before_device_work(nc):
+    """Null pointers and a non-finite accumulation scale are argument errors;
+    on an unconfigured context the calls report the state error, and nothing
+    reaches a device."""
+    ctx = nc.nc_create(2, 128, 1, 64, 65536)
+    try:
+        for bad in (lambda: nc.nc_backward_accumulate(ctx, None, 0.5),
+                    lambda: nc.nc_backward_accumulate(ctx, 1024, float("nan")),
+                    lambda: nc.nc_backward_accumulate(ctx, 1024, float("inf")),
+                    lambda: nc.nc_forward_loss_u16(ctx, None, 1024, 1024),
+                    lambda: nc.nc_forward_loss_u16(ctx, 1024, None, 1024),
+                    lambda: nc.nc_forward_loss_u16(ctx, 1024, 1024, None)):
+            with pytest.raises(nc.NcError) as ei:
+                bad()
+            assert ei.value.status == 1  # NC_ERR_ARG
+        with pytest.raises(nc.NcError) as ei:
+            nc.nc_backward_accumulate(ctx, 1024, 0.5)
+        assert ei.value.status == 2  # NC_ERR_STATE: not configured
+        with pytest.raises(nc.NcError) as ei:
+            nc.nc_forward_loss_u16(ctx, 1024, 1024, 1024)
+        assert ei.value.status == 2
+    finally:
+        nc.nc_destroy(ctx)
