@@ -4,23 +4,26 @@ cross-entropy + full backward) on B300 GPUs, one process per GPU.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload d20] [--no-cpu-baseline]
+  python bench.py --kernel CASE [--reps N]     (one op of the path, for ncu)
 
 Under torchrun (N > 1) each rank runs an independent replica of the step on
 its own batch (the pages' data-parallel recipe without the gradient
 all-reduce, which is out of scope here), so per-GPU work is fixed and the
 scaling is weak. Rank 0 prints one JSON line.
 
-Our arm: K timed steps after W warm-up steps, each one call of
-nc_forward_loss_async + nc_backward on device-resident inputs, timed with
-CUDA events on the library's stream between a barrier and a synchronise.
+Our arm: one call of nc_forward_loss_async + nc_backward on device-resident
+inputs is captured into a CUDA graph; W warm-up replays, then K timed
+replays with CUDA events between them on the library's stream, between a
+barrier and a synchronise (mean, median, p10 and p90 per step; and, when
+K < 50, a further 50 replays after 10 warm-up replays for the distribution).
+The per-kernel-family times come from K more eager steps in which the
+library brackets every launch with CUDA events.
 The end-to-end figure times nc_train_step_host_u16: each step copies the
 batch's packed uint16 token rows [B, T+1] (the token-shard format) from
 pinned host memory, widens them on the device into inputs and next-token
 targets, runs forward and backward and reads the loss back (vocabularies
 above 65,536 ids use nc_train_step_host with int32 token and target
-buffers). The per-kernel roofline
-comes from the library's own CUDA-event records of each launch in the timed
-region. The CPU baseline is the oracle on one 2048-token sequence of the
+buffers). The CPU baseline is the oracle on one 2048-token sequence of the
 same workload, timed after the GPU work in this process.
 
 Reference arm (--impl reference): the oracle as it stands, on rank 0's host
@@ -67,6 +70,9 @@ def parse_args():
                     help="skip timing the optimizer step (Muon + AdamW) after the fwd+bwd step")
     ap.add_argument("--no-infer", action="store_true",
                     help="skip timing generation (prefill + KV-cache decode steps)")
+    ap.add_argument("--kernel", default=None, choices=sorted(KERNEL_CASES),
+                    help="time one op of the path at the d20 shapes through the C ABI (for ncu captures)")
+    ap.add_argument("--reps", type=int, default=3, help="launches of the --kernel case after one warm-up launch")
     return ap.parse_args()
 
 
@@ -242,19 +248,67 @@ def our_arm(args):
         st.forward_loss_async(params, tok, tgt, d_loss)
         st.backward(grads)
 
-    for _ in range(args.warmup):
+    # one eager step sets the kernels' attributes up; the step is then
+    # captured once into a CUDA graph (no host decision depends on device
+    # data) and replayed: W warm-up replays, then exactly K timed replays
+    with torch.cuda.stream(stream):
         step()
+    torch.cuda.synchronize()
+    n0 = nc.nc_launch_count(st.ctx)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="relaxed"):
+        step()
+    launches_per_step = nc.nc_launch_count(st.ctx) - n0
+    for _ in range(args.warmup):
+        graph.replay()
     torch.cuda.synchronize()
     loss0 = float(d_loss.item())
 
-    # ---- timed region: device-resident inputs
-    nc.nc_profile_enable(st.ctx, True)
+    # ---- timed region: device-resident inputs, per-step CUDA events on the library's stream
     sampler = ClockSampler(local)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     sampler.start()
-    launches0 = nc.nc_launch_count(st.ctx)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with torch.cuda.stream(stream):
+        ev[0].record(stream)
+        for i in range(args.steps):
+            graph.replay()
+            ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    per_step = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    ms = ev[0].elapsed_time(ev[-1]) / args.steps
+    launches = launches_per_step * args.steps
+    ms_max, launches_all = reduce_over_ranks(ms, launches, "cuda")
+    value = job_tokens_per_s(ws, M, ms_max)
+    dist_ms = step_distribution(per_step)
+
+    # the timing protocol of at least 50 replayed steps after 10 warm-up
+    # replays, reported beside the K-step headline when K < 50
+    protocol = None
+    if args.steps < 50:
+        for _ in range(10):
+            graph.replay()
+        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(51)]
+        with torch.cuda.stream(stream):
+            ev2[0].record(stream)
+            for i in range(50):
+                graph.replay()
+                ev2[i + 1].record(stream)
+        torch.cuda.synchronize()
+        protocol = step_distribution([ev2[i].elapsed_time(ev2[i + 1]) for i in range(50)])
+    else:
+        protocol = dict(dist_ms)
+    protocol["tokens_per_s_median"] = job_tokens_per_s(ws, M, protocol["median_ms"])
+    del graph
+
+    # ---- per-kernel-family device time: K eager steps, every launch
+    # bracketed by CUDA events on the library's stream
+    nc.nc_profile_enable(st.ctx, True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         e0.record(stream)
@@ -262,19 +316,12 @@ def our_arm(args):
             step()
         e1.record(stream)
     torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    clocks = sampler.stop()
-    launches = nc.nc_launch_count(st.ctx) - launches0
-    ms = e0.elapsed_time(e1) / args.steps
+    ms_eager = e0.elapsed_time(e1) / args.steps
     fam = {}
     for name, f in (("gemm", nc.NC_FAM_GEMM), ("attn_fwd", nc.NC_FAM_ATTN_FWD),
                     ("attn_bwd", nc.NC_FAM_ATTN_BWD), ("rows", nc.NC_FAM_ROWS)):
         fam[name] = nc.nc_profile_read(st.ctx, f)
     nc.nc_profile_enable(st.ctx, False)
-
-    ms_max, launches_all = reduce_over_ranks(ms, launches, "cuda")
-    value = job_tokens_per_s(ws, M, ms_max)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -303,23 +350,39 @@ def our_arm(args):
         e2e = {"value": job_tokens_per_s(ws, M, dt_max), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4}
 
-    # ---- roofline of the dominant kernel family (live CUDA-event records)
+    # ---- roofline: every family against its bound; the dominant one is the headline
+    steps = args.steps
+    alg = algorithmic_work(w)
+    families = {}
+    for k, (fms, fn, fwork) in fam.items():
+        if fms <= 0:
+            continue
+        per = fms / steps
+        if k == "rows":
+            ach = fwork / (fms / 1000.0) / 1e9
+            families[k] = {"ms_per_step": per, "launches_per_step": fn / steps, "gbs": ach,
+                           "bound": "hbm", "peak": pk["hbm_gbs"], "frac": ach / pk["hbm_gbs"]}
+        else:
+            work = alg[k] * steps  # algorithmic FLOPs (no recompute)
+            ach = work / (fms / 1000.0) / 1e12
+            hw = fwork / (fms / 1000.0) / 1e12
+            families[k] = {"ms_per_step": per, "launches_per_step": fn / steps, "tflops": ach, "tflops_hw": hw,
+                           "bound": "tensor", "peak": pk["bf16_tflops_sustained"],
+                           "frac": ach / pk["bf16_tflops_sustained"]}
     dom = max(fam, key=lambda k: fam[k][0])
-    dms, dn, dwork = fam[dom]
-    if dom == "rows":
-        achieved = dwork / (dms / 1000.0) / 1e9
-        peak, unit, bound = pk["hbm_gbs"], "GB/s", "hbm"
-    else:
-        achieved = dwork / (dms / 1000.0) / 1e12
-        peak, unit, bound = pk["bf16_tflops_sustained"], "TFLOP/s", "tensor"
-    traffic = read_traffic(dom)
-    roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit,
-                "frac": achieved / peak, "peak_kind": f"{pk_kind} ({'sustained bf16' if bound == 'tensor' else 'HBM copy'})",
-                "traffic": traffic, "launches": dn, "avg_launch_ms": dms / max(1, dn),
-                "share_of_step": dms / (ms * args.steps)}
-    families = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps,
-                    ("tflops" if k != "rows" else "gbs"): (v[2] / (v[0] / 1000.0) / (1e12 if k != "rows" else 1e9))
-                    if v[0] > 0 else None} for k, v in fam.items()}
+    dms, dn, _ = fam[dom]
+    fd = families[dom]
+    roofline = {"bound": fd["bound"], "kernel": dom,
+                "achieved": fd["gbs"] if dom == "rows" else fd["tflops"], "peak": fd["peak"],
+                "unit": "GB/s" if dom == "rows" else "TFLOP/s", "frac": fd["frac"],
+                "peak_kind": f"{pk_kind} ({'HBM copy' if dom == 'rows' else 'sustained bf16'})",
+                "traffic": read_traffic(dom), "launches": dn, "avg_launch_ms": dms / max(1, dn),
+                "share_of_step": dms / (ms_eager * steps),
+                "work": "algorithmic: 6*M*(12*L*d^2 + d*V) FLOPs per step for the GEMMs (the lm_head "
+                        "backward's logit recompute excluded; it is in achieved_hw)"}
+    if dom != "rows":
+        roofline["achieved_hw"] = fd["tflops_hw"]
+        roofline["frac_hw"] = fd["tflops_hw"] / fd["peak"]
 
     fpt = W.model_flops_per_token(w)
     mfu = value * fpt / (ws * pk["bf16_tflops"] * 1e12)
@@ -385,12 +448,16 @@ def our_arm(args):
             "config": {"workload": workload_desc(w), "global_batch": w.batch * ws, "seq_len": w.seq_len,
                        "tokens_per_step": M * ws,
                        "parallelism": f"{ws} independent data-parallel replicas (no collective)",
-                       "l2": "inputs larger than L2: the step streams a ~17 GB activation stash"},
+                       "l2": "inputs larger than L2: the step streams a ~17 GB activation stash",
+                       "timing": "one CUDA graph of nc_forward_loss_async + nc_backward, replayed; CUDA events "
+                                 "between replays on the library's stream"},
             "mfu": mfu, "mfu_peak_tflops": pk["bf16_tflops"],
             "mfu_vs_sustained": value * fpt / (ws * pk["bf16_tflops_sustained"] * 1e12),
             "model_flops_per_token": fpt,
             "loss": loss0,
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches_all,
+            "step_ms": dist_ms, "timing_protocol": protocol, "eager_ms_per_step": ms_eager,
+            "launches_per_step": launches_per_step,
             "roofline": roofline, "families": families, "optimizer": opt, "inference": inf,
             "cpu_baseline": cpu,
         }
@@ -399,6 +466,25 @@ def our_arm(args):
     if ws > 1:
         dist.destroy_process_group()
     return 0
+
+
+def step_distribution(per_step_ms):
+    """Median, 10th and 90th percentile and mean of per-step times (ms)."""
+    a = np.asarray(per_step_ms, dtype=np.float64)
+    return {"steps": int(a.size), "median_ms": float(np.median(a)), "p10_ms": float(np.percentile(a, 10)),
+            "p90_ms": float(np.percentile(a, 90)), "mean_ms": float(a.mean())}
+
+
+def algorithmic_work(w: W.Workload) -> dict:
+    """Algorithmic FLOPs of one step per tensor-core family: every linear
+    layer and the lm_head once forward (2 FLOPs per weight and token) and
+    twice backward (input and weight gradients); causal attention over the
+    lower triangle, 2*128*T*(T+1) FLOPs per (sequence, head) for QK^T and PV
+    forward and twice that backward. No recompute is counted."""
+    L, d, V, T, B, H = w.depth, w.d_model, w.vocab, w.seq_len, w.batch, w.n_head
+    M = B * T
+    fwd_attn = 2.0 * 128 * T * (T + 1) * B * H * L
+    return {"gemm": 6.0 * M * (12.0 * L * d * d + d * V), "attn_fwd": fwd_attn, "attn_bwd": 2.0 * fwd_attn}
 
 
 def infer_timing(nc, st, w, params, tok, stream, args, ws, pk):
@@ -518,8 +604,173 @@ def read_traffic(family: str):
         return None
 
 
+# ------------------------------------------------------------------ single ops (for ncu captures)
+
+# Ops of the path at the d20 shapes (batch 16 x seq 2048, d_model 1280, 10
+# heads, vocab 65,536) unless stated: name -> (bound, what one launch moves or
+# computes, description).
+KERNEL_CASES = {
+    "gemm_qkv": ("tensor", "2*M*N*K FLOPs", "32768 x 3840 x 1280 forward GEMM, QK-norm + RoPE epilogue"),
+    "gemm_fc": ("tensor", "2*M*N*K FLOPs", "32768 x 5120 x 1280 forward GEMM, ReLU^2 epilogue (a only)"),
+    "gemm_relu2_bwd": ("tensor", "2*M*N*K FLOPs", "32768 x 5120 x 1280 GEMM with the ReLU^2 backward epilogue"),
+    "gemm_dw": ("tensor", "2*M*N*K FLOPs", "1280 x 5120 x 32768 weight gradient (split-K + splitk_reduce_k)"),
+    "attn_fwd": ("tensor", "2*128*T*(T+1)*B*H FLOPs", "causal attention forward"),
+    "attn_bwd": ("tensor", "4*128*T*(T+1)*B*H FLOPs", "attn_rowdot_k + causal attention backward"),
+    "lmhead_ce": ("tensor", "2*M*V*d FLOPs", "lm_head + CE forward, 4096 rows (GEMM partials + ce_reduce_k)"),
+    "rmsnorm_fwd": ("hbm", "M*d*(4+2) + 4*M bytes", "rmsnorm_fwd_k: fp32 x -> bf16 y, fp32 r"),
+    "rmsnorm_bwd": ("hbm", "M*d*(4+4+2+2+2) + 4*M bytes", "rmsnorm_bwd_k, accumulating into fp32 dx, bf16 copy"),
+    "qk_norm_rope_bwd": ("hbm", "2*M*d*(4+2+2) + 8*M*H bytes", "qk_norm_rope_bwd_k over q and k heads"),
+    "embed_fwd": ("hbm", "M*d*(2+4) + 4*M bytes", "embed_fwd_k: gather of Zipf(1.1) ids into fp32 x"),
+    "embed_bwd": ("hbm", "M*d*(4+4) + 4*M bytes", "embed_bwd_k: float4 atomic scatter of fp32 dx (after a memset)"),
+}
+
+
+def kernel_arm(args):
+    """One op of the path through the C ABI at the d20 shapes on random
+    device-resident inputs: one warm-up launch, then --reps launches timed
+    with CUDA events on the library's stream. Prints one JSON line with the
+    mean time per launch and the algorithmic work per launch."""
+    import torch
+
+    import decoder_transformer_step_nanochat_b300 as nc
+
+    torch.cuda.set_device(0)
+    pk, pk_kind = peaks()
+    case = args.kernel
+    B, T, H, V = 16, 2048, 10, 65536
+    d = H * 128
+    if case == "lmhead_ce":
+        B = 2
+    M = B * T
+    stream = torch.cuda.Stream()
+    # the norm cases need no vocabulary: a small one keeps the context's
+    # workspace (its cross-entropy buffer grows with the vocabulary) small
+    v_ctx = 1024 if case in ("rmsnorm_fwd", "rmsnorm_bwd", "qk_norm_rope_bwd") else V
+    st = nc.Step(1, d, H, T, v_ctx, B, nc.NC_BF16, stream=stream)
+    ctx = st.ctx
+    bf = torch.bfloat16
+    g = torch.Generator(device="cuda").manual_seed(0)
+
+    def randn(*shape, scale=1.0, dtype=bf):
+        return (torch.randn(shape, device="cuda", generator=g) * scale).to(dtype)
+
+    def gemm(Mg, N, K, ak, bk, epi, c_dtype, c2=None):
+        A = randn(*((Mg, K) if ak else (K, Mg)))
+        Bm = randn(*((N, K) if bk else (K, N)), scale=0.05)
+        C = torch.empty((Mg, N), device="cuda", dtype=c_dtype)
+        args_ = (ctx, Mg, N, K, A.data_ptr(), K if ak else Mg, ak, Bm.data_ptr(), K if bk else N, bk, epi, 1.0, 0.0,
+                 C.data_ptr(), N, c2.data_ptr() if c2 is not None else None, c2.shape[1] if c2 is not None else 0)
+        return (lambda: nc.nc_op_gemm(*args_)), (A, Bm, C, c2), 2.0 * Mg * N * K
+
+    if case == "gemm_qkv":
+        rqk = torch.empty((M, 2 * H), device="cuda", dtype=torch.float32)
+        run, keep, work = gemm(M, 3 * d, d, 1, 1, nc.NC_EPI_QKNORM_ROPE, bf, rqk)
+    elif case == "gemm_fc":
+        run, keep, work = gemm(M, 4 * d, d, 1, 1, nc.NC_EPI_RELU2A, bf)
+    elif case == "gemm_relu2_bwd":
+        a = torch.rand((M, 4 * d), device="cuda", generator=g).to(bf)
+        run, keep, work = gemm(M, 4 * d, d, 1, 0, nc.NC_EPI_RELU2_BWD, bf, a)
+    elif case == "gemm_dw":
+        run, keep, work = gemm(d, 4 * d, M, 0, 0, nc.NC_EPI_STORE_F32, torch.float32)
+    elif case in ("attn_fwd", "attn_bwd"):
+        qkv = randn(M, 3 * d)
+        o = torch.empty((M, d), device="cuda", dtype=bf)
+        lse = torch.empty((B, H, T), device="cuda", dtype=torch.float32)
+        dout = randn(M, d)
+        dqk = torch.empty((2, M, d), device="cuda", dtype=torch.float32)
+        dqkv = torch.empty((M, 3 * d), device="cuda", dtype=bf)
+        nc.nc_op_attention_fwd(ctx, qkv.data_ptr(), o.data_ptr(), lse.data_ptr())
+        fwd = 2.0 * 128 * T * (T + 1) * B * H
+        if case == "attn_fwd":
+            def run():
+                nc.nc_op_attention_fwd(ctx, qkv.data_ptr(), o.data_ptr(), lse.data_ptr())
+            work = fwd
+        else:
+            def run():
+                nc.nc_op_attention_bwd(ctx, qkv.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                                       dqk.data_ptr(), dqkv.data_ptr())
+            work = 2.0 * fwd
+        keep = (qkv, o, lse, dout, dqk, dqkv)
+    elif case == "lmhead_ce":
+        hf = randn(M, d)
+        wl = randn(V, d, scale=0.02)
+        tgt = torch.randint(0, V, (M,), device="cuda", dtype=torch.int32, generator=g)
+        lse, nll = torch.empty(M, device="cuda"), torch.empty(M, device="cuda")
+        am = torch.empty(M, device="cuda", dtype=torch.int32)
+
+        def run():
+            nc.nc_op_lmhead_ce_fwd(ctx, hf.data_ptr(), wl.data_ptr(), tgt.data_ptr(), lse.data_ptr(), nll.data_ptr(),
+                                   am.data_ptr())
+        keep, work = (hf, wl, tgt, lse, nll, am), 2.0 * M * V * d
+    else:
+        x = torch.randn((M, d), device="cuda", generator=g)
+        r = torch.rand(M, device="cuda", generator=g) + 0.5
+        if case == "rmsnorm_fwd":
+            y = torch.empty((M, d), device="cuda", dtype=bf)
+
+            def run():
+                nc.nc_op_rmsnorm_fwd(ctx, x.data_ptr(), y.data_ptr(), r.data_ptr())
+            keep, work = (x, y, r), M * d * 6.0 + 4.0 * M
+        elif case == "rmsnorm_bwd":
+            dy, y = randn(M, d), randn(M, d)
+            dxe = torch.empty((M, d), device="cuda", dtype=bf)
+
+            def run():
+                nc.nc_op_rmsnorm_bwd(ctx, dy.data_ptr(), y.data_ptr(), r.data_ptr(), x.data_ptr(), dxe.data_ptr(), 1)
+            keep, work = (x, r, dy, y, dxe), M * d * 14.0 + 4.0 * M
+        elif case == "qk_norm_rope_bwd":
+            dqk = torch.randn((2, M, d), device="cuda", generator=g)
+            qkv = randn(M, 3 * d)
+            rqk = torch.rand((M, 2 * H), device="cuda", generator=g) + 0.5
+            dqkv = torch.empty((M, 3 * d), device="cuda", dtype=bf)
+
+            def run():
+                nc.nc_op_qk_norm_rope_bwd(ctx, dqk.data_ptr(), qkv.data_ptr(), rqk.data_ptr(), dqkv.data_ptr())
+            keep, work = (dqk, qkv, rqk, dqkv), 2.0 * M * d * 8 + 8.0 * M * H
+        else:
+            ids = torch.from_numpy(W.make_tokens(W.WORKLOADS["d20"])[0].reshape(-1).copy()).cuda()
+            if case == "embed_fwd":
+                wte = randn(V, d, scale=0.02)
+
+                def run():
+                    nc.nc_op_embed_fwd(ctx, ids.data_ptr(), wte.data_ptr(), x.data_ptr())
+                keep, work = (x, wte, ids), M * d * 6.0 + 4.0 * M
+            else:
+                dwte = torch.empty((V, d), device="cuda", dtype=torch.float32)
+
+                def run():
+                    nc.nc_op_embed_bwd(ctx, ids.data_ptr(), x.data_ptr(), dwte.data_ptr())
+                keep, work = (x, dwte, ids), M * d * 8.0 + 4.0 * M
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        run()
+    nc.nc_sync(ctx)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.reps):
+            run()
+        e1.record(stream)
+    nc.nc_sync(ctx)
+    ms = e0.elapsed_time(e1) / max(1, args.reps)
+    bound, unit_of_work, desc = KERNEL_CASES[case]
+    if bound == "hbm":
+        ach, peak, unit = work / (ms / 1000.0) / 1e9, pk["hbm_gbs"], "GB/s"
+    else:
+        ach, peak, unit = work / (ms / 1000.0) / 1e12, pk["bf16_tflops"], "TFLOP/s"
+    print(json.dumps({"kernel": case, "desc": desc, "bound": bound, "work_per_launch": work,
+                      "work_unit": unit_of_work, "ms_per_launch": ms, "launches": args.reps, "achieved": ach,
+                      "peak": peak, "peak_kind": f"{pk_kind} ({'HBM copy' if bound == 'hbm' else 'bf16 burst'})",
+                      "unit": unit, "frac": ach / peak}), flush=True)
+    del keep
+    st.close()
+    return 0
+
+
 def main():
     args = parse_args()
+    if args.kernel:
+        return kernel_arm(args)
     if args.impl == "reference":
         return reference_arm(args)
     return our_arm(args)

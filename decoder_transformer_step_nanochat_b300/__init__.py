@@ -73,6 +73,7 @@ _SIGS = {
     "nc_train_step_host_u16": (_I, [_P, _P, _P, _P, ctypes.POINTER(_F)]),
     "nc_train_step_host": (_I, [_P, _P, _P, _P, _P, ctypes.POINTER(_F)]),
     "nc_get_token_outputs": (_I, [_P, _P, _P, _P]),
+    "nc_get_argmax": (_I, [_P, _P]),
     "nc_get_hidden": (_I, [_P, _P]),
     "nc_sync": (_I, [_P]),
     "nc_launch_count": (ctypes.c_ulonglong, [_P]),
@@ -89,6 +90,10 @@ _SIGS = {
     "nc_op_attention_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P]),
     "nc_op_qk_norm_rope_fwd": (_I, [_P, _P, _P]),
     "nc_op_rmsnorm_fwd": (_I, [_P, _P, _P, _P]),
+    "nc_op_rmsnorm_bwd": (_I, [_P, _P, _P, _P, _P, _P, _I]),
+    "nc_op_embed_fwd": (_I, [_P, _P, _P, _P]),
+    "nc_op_embed_bwd": (_I, [_P, _P, _P, _P]),
+    "nc_op_qk_norm_rope_bwd": (_I, [_P, _P, _P, _P, _P]),
     "nc_lmhead_ce_fwd_static": (_I, [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P, _P]),
     "nc_op_gemm_batched": (_I, [_P, _I, _I, _I, _I, _P, _LL, _I, _LL, _P, _LL, _I, _LL, _I, _F, _F, _P, _LL,
                                 _P, _LL, _LL]),
@@ -194,6 +199,10 @@ def nc_get_token_outputs(ctx, d_lse=None, d_nll=None, d_argmax=None):
     _check(lib().nc_get_token_outputs(ctx, d_lse, d_nll, d_argmax), ctx)
 
 
+def nc_get_argmax(ctx, d_argmax):
+    _check(lib().nc_get_argmax(ctx, d_argmax), ctx)
+
+
 def nc_get_hidden(ctx, d_hf):
     _check(lib().nc_get_hidden(ctx, d_hf), ctx)
 
@@ -258,6 +267,22 @@ def nc_op_qk_norm_rope_fwd(ctx, qkv, rqk):
 
 def nc_op_rmsnorm_fwd(ctx, x, y, r):
     _check(lib().nc_op_rmsnorm_fwd(ctx, x, y, r), ctx)
+
+
+def nc_op_rmsnorm_bwd(ctx, dy, y, r, dx, dx_e=None, accumulate=0):
+    _check(lib().nc_op_rmsnorm_bwd(ctx, dy, y, r, dx, dx_e, 1 if accumulate else 0), ctx)
+
+
+def nc_op_embed_fwd(ctx, tok, wte, x):
+    _check(lib().nc_op_embed_fwd(ctx, tok, wte, x), ctx)
+
+
+def nc_op_embed_bwd(ctx, tok, dx, dwte):
+    _check(lib().nc_op_embed_bwd(ctx, tok, dx, dwte), ctx)
+
+
+def nc_op_qk_norm_rope_bwd(ctx, dqk, qkv, rqk, dqkv):
+    _check(lib().nc_op_qk_norm_rope_bwd(ctx, dqk, qkv, rqk, dqkv), ctx)
 
 
 def nc_lmhead_ce_fwd_static(hf, w_lm, tgt, M, d, V, lse, nll, argmax, d_status=None, stream=None):

@@ -827,7 +827,12 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   // the decode table is rebuilt on the (possibly different) device by the next prefill
   if (c->dec_rope) { cudaFree(c->dec_rope); c->dec_rope = nullptr; }
   c->dec_rope_len = 0;
-  // device words: [0] status, [1] work-unit counter of the persistent attention backward
+  // device words: [0] status, [1] work-unit counter of the persistent attention backward.
+  // A context configured again on another device gets them anew there, like the tables above.
+  if (c->status && c->device >= 0 && c->device != dev) {
+    cudaFree(c->status);
+    c->status = nullptr;
+  }
   if (!c->status) CK(cudaMalloc(&c->status, 16 * sizeof(int)));
   // RoPE table: angle pos * 10000^(-j/64) formed in float64, stored fp32.
   // Also stored angle-major in groups of four angles, [16][T][4], for the
@@ -969,6 +974,11 @@ nc_status nc_get_token_outputs(nc_ctx* c, float* d_lse, float* d_nll, int32_t* d
   if (d_nll) CK(cudaMemcpyAsync(d_nll, c->ws + c->off.nll, n, cudaMemcpyDeviceToDevice, c->stream));
   if (d_argmax) CK(cudaMemcpyAsync(d_argmax, c->ws + c->off.amax, n, cudaMemcpyDeviceToDevice, c->stream));
   return NC_OK;
+}
+
+nc_status nc_get_argmax(nc_ctx* c, int32_t* d_argmax) {
+  if (!d_argmax) return fail(NC_ERR_ARG, "d_argmax is null");
+  return nc_get_token_outputs(c, nullptr, nullptr, d_argmax);
 }
 
 nc_status nc_get_hidden(nc_ctx* c, void* d_hf) {
@@ -1122,6 +1132,57 @@ nc_status nc_op_rmsnorm_fwd(nc_ctx* c, const float* x, void* y, float* r) {
   if (!x || !y || !r) return fail(NC_ERR_ARG, "null pointer argument");
   if (c->prec == NC_BF16) CK(rmsnorm_fwd<bf16>(x, (bf16*)y, r, c->M, c->d, c->stream));
   else CK(rmsnorm_fwd<float>(x, (float*)y, r, c->M, c->d, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_op_rmsnorm_bwd(nc_ctx* c, const void* dy, const void* y, const float* r, float* dx, void* dx_e,
+                            int accumulate) {
+  CKS(check_ready(c));
+  if (!dy || !y || !r || !dx) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  const double bytes = (double)c->M * c->d * (4.0 * (accumulate ? 2 : 1) + c->esz * (dx_e ? 3 : 2)) + 4.0 * c->M;
+  if (c->prec == NC_BF16)
+    KL(NC_FAM_ROWS, bytes, 1, rmsnorm_bwd<bf16>((const bf16*)dy, (const bf16*)y, r, dx, (bf16*)dx_e, c->M, c->d,
+                                                accumulate ? 1 : 0, c->stream));
+  else
+    KL(NC_FAM_ROWS, bytes, 1, rmsnorm_bwd<float>((const float*)dy, (const float*)y, r, dx, (float*)dx_e, c->M, c->d,
+                                                 accumulate ? 1 : 0, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_op_embed_fwd(nc_ctx* c, const int32_t* tok, const void* wte, float* x) {
+  CKS(check_ready(c));
+  if (!tok || !wte || !x) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  const double bytes = (double)c->M * c->d * (c->esz + 4) + 4.0 * c->M;
+  if (c->prec == NC_BF16)
+    KL(NC_FAM_ROWS, bytes, 1, embed_fwd<bf16>(tok, (const bf16*)wte, x, c->M, c->d, c->V, c->status, c->stream));
+  else
+    KL(NC_FAM_ROWS, bytes, 1, embed_fwd<float>(tok, (const float*)wte, x, c->M, c->d, c->V, c->status, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_op_embed_bwd(nc_ctx* c, const int32_t* tok, const float* dx, float* dwte) {
+  CKS(check_ready(c));
+  if (!tok || !dx || !dwte) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  CK(cudaMemsetAsync(dwte, 0, (size_t)c->V * c->d * sizeof(float), c->stream));
+  KL(NC_FAM_ROWS, 8.0 * c->M * c->d + 4.0 * c->M, 1,
+     embed_bwd<bf16>(tok, nullptr, dx, dwte, c->M, c->d, c->V, c->stream));
+  return NC_OK;
+}
+
+nc_status nc_op_qk_norm_rope_bwd(nc_ctx* c, const float* dqk, const void* qkv, const float* rqk, void* dqkv) {
+  CKS(check_ready(c));
+  if (!dqk || !qkv || !rqk || !dqkv) return fail(NC_ERR_ARG, "null pointer argument");
+  c->have_fwd = false;
+  const double bytes = 2.0 * c->M * c->d * (4 + 2 * c->esz) + 8.0 * c->M * c->H;
+  if (c->prec == NC_BF16)
+    KL(NC_FAM_ROWS, bytes, 1, qk_norm_rope_bwd<bf16>(dqk, (const bf16*)qkv, rqk, c->rope_cos, c->rope_sin,
+                                                     (bf16*)dqkv, c->M, c->T, c->H, c->stream, 2));
+  else
+    KL(NC_FAM_ROWS, bytes, 1, qk_norm_rope_bwd<float>(dqk, (const float*)qkv, rqk, c->rope_cos, c->rope_sin,
+                                                      (float*)dqkv, c->M, c->T, c->H, c->stream, 2));
   return NC_OK;
 }
 

@@ -162,6 +162,15 @@ nc_status nc_train_step_host(nc_ctx* ctx, const void* params, const int32_t* h_t
  * Any pointer may be NULL. */
 nc_status nc_get_token_outputs(nc_ctx* ctx, float* d_lse, float* d_nll, int32_t* d_argmax);
 
+/* Greedy next-token prediction of the last forward (nanochat explainer,
+ * "Pretraining": the model predicts token N+1 from tokens 1..N): d_argmax
+ * (device int32 [batch*seq_len]) receives, per position, the vocabulary index
+ * of the largest logit, the lowest index among ties. Copied device to device
+ * on the context's stream (asynchronous). NC_ERR_ARG for a NULL d_argmax,
+ * NC_ERR_STATE without a preceding successful forward. nc_get_token_outputs
+ * returns the same ids together with lse and nll. */
+nc_status nc_get_argmax(nc_ctx* ctx, int32_t* d_argmax);
+
 /* Final hidden state of the last forward (the RMS-normalised input of
  * lm_head), copied device-to-device into d_hf: elem [batch*seq_len, d_model]
  * (bf16 in NC_BF16, fp32 in NC_FP32_DEBUG). */

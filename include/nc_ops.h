@@ -108,6 +108,39 @@ nc_status nc_op_qk_norm_rope_fwd(nc_ctx* ctx, void* qkv, float* rqk);
  * y (elem) = x * r, r (fp32 [B*T]) = 1/sqrt(mean(x^2) + 1e-6). */
 nc_status nc_op_rmsnorm_fwd(nc_ctx* ctx, const float* x, void* y, float* r);
 
+/* Backward of the parameter-free RMSNorm y = z * r (nanochat explainer,
+ * "Architecture Choices": RMSNorm; the gradient follows from y = z / rms(z)):
+ * dz = r * (dy - y * mean(dy * y)) per row of M = batch*seq_len rows of
+ * d_model. dy, y: elem [M, d]; r: fp32 [M] from the forward. dx: fp32 [M, d]
+ * receives dz, or dx + dz when accumulate is non-zero (the residual stream's
+ * gradient adds the branch's); dx_e (elem [M, d], may be NULL) gets a copy of
+ * the new dx in the element type. */
+nc_status nc_op_rmsnorm_bwd(nc_ctx* ctx, const void* dy, const void* y, const float* r, float* dx, void* dx_e,
+                            int accumulate);
+
+/* Token embedding lookup (nanochat explainer, "Architecture Choices": untied
+ * token embedding): x[m, :] = wte[tok[m], :] as fp32 (the residual stream),
+ * no scaling or normalisation. tok: int32 [M] in [0, vocab); wte: elem [V, d];
+ * x: fp32 [M, d]. An id out of range writes a zero row and sets the status
+ * word (the next nc_sync returns NC_ERR_DEVICE). */
+nc_status nc_op_embed_fwd(nc_ctx* ctx, const int32_t* tok, const void* wte, float* x);
+
+/* Backward of the lookup: dwte (fp32 [V, d], overwritten) gets, in row id,
+ * the sum of dx[m, :] (fp32 [M, d]) over the positions m with tok[m] = id;
+ * the rows of ids that no position holds are exactly 0. The sums are formed
+ * by atomic adds, so their order (and the last bits) may vary between runs. */
+nc_status nc_op_embed_bwd(nc_ctx* ctx, const int32_t* tok, const float* dx, float* dwte);
+
+/* Backward of the QK-norm + RoPE of nc_op_qk_norm_rope_fwd, for the q and the
+ * k heads: with q_hat = R_pos q / rms(q) (nanochat explainer, "RoPE
+ * Intuition"), dq = r * (dq_n - q_n * mean(dq_n * q_n)) where dq_n = R_pos^T
+ * dq_hat and q_n = R_pos^T q_hat. dqk: fp32 [2, M, d], the dq_hat plane then
+ * the dk_hat plane (as nc_op_attention_bwd writes them); qkv: elem [M, 3d],
+ * the forward's output (q_hat, k_hat, v); rqk: fp32 [M, 2H] from the forward.
+ * dq and dk go to the q and k columns of dqkv (elem [M, 3d]); its v columns
+ * are left as they are. */
+nc_status nc_op_qk_norm_rope_bwd(nc_ctx* ctx, const float* dqk, const void* qkv, const float* rqk, void* dqkv);
+
 /* Fused lm_head + cross-entropy forward that allocates no device memory.
  * The nanochat pages have no counterpart of this call; it exists for callers
  * that must not call cudaMalloc where they need the loss (code inside another
@@ -116,7 +149,10 @@ nc_status nc_op_rmsnorm_fwd(nc_ctx* ctx, const float* x, void* y, float* r);
  * hf: bf16 [M, d]; w_lm: bf16 [V, d] (both 16-byte aligned); tgt: int32 [M];
  * lse, nll: fp32 [M]; argmax: int32 [M] (lowest index among ties);
  * d_status: optional device int32, set to 0, or to 1 if a target id is out of
- * range, or to 2 if a pipeline wait timed out; cuda_stream: a cudaStream_t
+ * range, or to 2 if a pipeline wait timed out. With d_status NULL neither
+ * failure is reported anywhere: the call still returns NC_OK, and a row whose
+ * target id is out of range gets nll = lse (its target logit reads as 0), so
+ * pass d_status unless the targets are known to be valid; cuda_stream: a cudaStream_t
  * (NULL = legacy default stream). d and V must be multiples of 8.
  * Scratch is a 16 MiB array in the library's static device memory, held by
  * every GPU that loads the library until the process exits; a call needs

@@ -95,3 +95,33 @@ def logit_stats(hf_ref, hf_gpu, w_lm, chunk=2048):
             out["margin_" + key][i:i + chunk] = top2[:, 1] - top2[:, 0]
         out["logits_ref"].append(lr)
     return out
+
+
+def check_bf16_step(w: W.Workload, loss, g, lse, nll, am, hf, loss_ref, g_ref, cache, report=None):
+    """The bf16 tolerances of the step against the oracle: |dloss| <= 2e-2
+    nats; every parameter tensor's gradient within rel-L2 3e-2 and cosine
+    0.999; lse within 5e-2 and nll within 6e-2 at every position; argmax
+    identical (a) to the argmax of the logits of the GPU's own final hidden
+    state wherever their top-2 margin exceeds 1e-3 and (b) to the oracle's
+    wherever the oracle margin exceeds 4 x the largest logit difference that
+    the bf16 hidden state causes. `report`, a list, receives the measured
+    figures."""
+    pt = per_tensor(w, g, g_ref)
+    dl = np.abs(lse - cache["lse"])
+    dn = np.abs(nll - cache["nll"])
+    M, d = w.tokens, w.d_model
+    st = logit_stats(cache["hf"].reshape(M, d), hf, cache["P"]["lm_head"])
+    own = st["margin_g"] > 1e-3
+    sure = st["margin_ref"] > 4 * st["max_dlogit"]
+    if report is not None:
+        report.append(dict(loss=loss, loss_ref=loss_ref, max_rel_l2=max(r for _, r, _ in pt),
+                           min_cos=min(c for _, _, c in pt), max_dlse=float(dl.max()), max_dnll=float(dn.max()),
+                           argmax_checked=float(sure.mean()), max_dlogit=st["max_dlogit"]))
+    assert abs(loss - loss_ref) <= 2e-2, (loss, loss_ref)
+    bad = [(n, r, c) for n, r, c in pt if not (r <= 3e-2 and c >= 0.999)]
+    assert not bad, bad
+    assert dl.max() <= 5e-2, dl.max()
+    assert dn.max() <= 6e-2, dn.max()
+    np.testing.assert_array_equal(am[own], st["am_g"][own])
+    assert sure.mean() > 0.3, (sure.mean(), st["max_dlogit"])
+    np.testing.assert_array_equal(am[sure], cache["argmax"][sure])

@@ -37,6 +37,7 @@ def test_library_exports_every_declared_symbol(nc):
     names = declared_functions()
     assert "nc_create" in names and "nc_forward_loss" in names and "nc_backward" in names
     assert "nc_launch_count" in names and "nc_last_error" in names
+    assert "nc_get_argmax" in names and "nc_get_token_outputs" in names
     L = ctypes.CDLL(nc.LIB_PATH)
     missing = [n for n in names if not hasattr(L, n)]
     assert not missing, missing
@@ -136,5 +137,20 @@ def test_accumulation_and_u16_entry_points_validate_before_device_work(nc):
         with pytest.raises(nc.NcError) as ei:
             nc.nc_forward_loss_u16(ctx, 1024, 1024, 1024)
         assert ei.value.status == 2
+    finally:
+        nc.nc_destroy(ctx)
+
+
+def test_argmax_query_validates_before_device_work(nc):
+    """nc_get_argmax: a NULL destination is an argument error; on an
+    unconfigured context (so with no forward to read) it is a state error."""
+    ctx = nc.nc_create(2, 128, 1, 64, 65536)
+    try:
+        with pytest.raises(nc.NcError) as ei:
+            nc.nc_get_argmax(ctx, None)
+        assert ei.value.status == 1  # NC_ERR_ARG
+        with pytest.raises(nc.NcError) as ei:
+            nc.nc_get_argmax(ctx, 1024)
+        assert ei.value.status == 2  # NC_ERR_STATE
     finally:
         nc.nc_destroy(ctx)

@@ -1,9 +1,15 @@
-"""Parity at the full benchmark sizes, in the launch configuration the
-benchmark times (bf16, batch 16 x seq 2048 for depth 20 and 26; batch 8 for
-the GPT-2-small shape).
+"""Parity at the full model sizes.
 
-The oracle cannot run the whole batch, so the checks are ones it can make
-one by one or that hold at any size:
+One sequence (B = 1, T = 2048) of the depth-20 and depth-26 models goes
+through the whole step on both sides: loss, lse / nll / argmax per position
+and every parameter tensor's gradient against the oracle (float32 NumPy),
+with the bf16 tolerances of the step.
+
+In the launch configuration the benchmark times (bf16, batch 16 x seq 2048
+for depth 20 and 26; batch 8 for the GPT-2-small shape), which takes other
+split-K factors and attention schedules, the oracle cannot run the whole
+batch, so the checks are ones it can make one by one or that hold at any
+size:
 * per-position lse / loss of sampled sequences: sequences are independent,
   and by causality the first 256 positions of a sequence depend on nothing
   after them, so the oracle runs just those positions of that sequence;
@@ -19,7 +25,7 @@ import pytest
 
 import oracle
 import workload as W
-from gpu_util import load_nc, rel_l2, shape_of, to_device_i32, to_device_params
+from gpu_util import check_bf16_step, load_nc, rel_l2, run_gpu_step, shape_of, to_device_i32, to_device_params
 
 pytestmark = pytest.mark.gpu
 
@@ -32,6 +38,21 @@ def _step(nc, st, dp, tok, tgt, grads):
     st.backward(grads)
     nc.nc_sync(st.ctx)
     return loss, lse.cpu().numpy(), nll.cpu().numpy(), am.cpu().numpy()
+
+
+@pytest.mark.parametrize("name", ["d20", "d26"])
+def test_full_size_one_sequence_against_oracle(name):
+    """Depth 20 (d_model 1280) and depth 26 (d_model 1664) on one 2048-token
+    sequence: the whole forward, loss and backward against the oracle."""
+    nc = load_nc()
+    w = W.WORKLOADS[name].with_batch(1)
+    p = W.make_params(w)
+    tok, tgt = W.make_tokens(w)
+    out = run_gpu_step(nc, w, p, tok, tgt, nc.NC_BF16)
+    loss_ref, g_ref, cache = oracle.step(p, tok, tgt, shape_of(w), np.float32)
+    rep = []
+    check_bf16_step(w, *out, loss_ref, g_ref, cache, report=rep)
+    print(name, rep[0])
 
 
 @pytest.mark.parametrize("name,sampled", [("gpt2_small", (3,)), ("d20", (0, 11)), ("d26", (5,))])

@@ -214,8 +214,62 @@ def _qkv(rng, B, T, H, prec):
     return rounded(qkv, prec).reshape(B * T, 3 * H * D)
 
 
-@pytest.mark.parametrize("prec,T", [(0, 128), (0, 256), (0, 384), (0, 640), (1, 100)],
-                         ids=["bf16_T128", "bf16_T256", "bf16_T384", "bf16_T640", "fp32_T100"])
+# Element-wise bounds of the attention kernels against the float64 oracle on
+# the same bf16-exact inputs. In bf16 the bound follows the kernels' rounding
+# points, each at most the unit roundoff u = 2^-8 (8 significant bits) of
+# what it rounds:
+#   forward: o = sum_j bf16(p_j) v_j / l with l summed from the unrounded p,
+#     then o is rounded: |o_gpu - o| <= u * sum_j p_j |v_j| + u * |o|;
+#   backward: dS = bf16(p (dP - D_gpu)) where D_gpu = rowsum(dO o_gpu) uses the
+#     kernel's own o, so |dS_gpu - dS| <= u |dS| + p |dD| (dD = D_gpu - D, known
+#     exactly here); dQ, dK sum those errors against |K|, |Q| (times 1/sqrt(128));
+#     dV = sum_t bf16(p_t) dO_t, rounded: u * sum_t p_t |dO_t| + u |dV|.
+# Each bound also carries fp32 accumulation (n * 2^-24 times the sum of the
+# absolute terms) and is checked with a factor 2 of slack; a wrong tile (the
+# diagonal, the last key tile of a ragged T) is off by O(1) of the terms and
+# fails by far. The fp32 debug kernels round nowhere but in fp32 sums.
+U_BF16 = 2.0 ** -8
+
+
+def attention_bounds(q, k, v, do, o_ref, o_gpu, prec):
+    """Per-element error bounds (o, dq, dk, dv) for one sequence, all heads.
+    q, k, v, do: [T, H, D] float64; o_ref the oracle's output; o_gpu the
+    kernel's (which the backward's row sums D use)."""
+    T, H, D = q.shape
+    u = U_BF16 if prec == 0 else 0.0
+    gam = T * 2.0 ** -24
+    sc = 1.0 / np.sqrt(D)
+    mask = np.tril(np.ones((T, T), dtype=bool))
+    bo, bdq, bdk, bdv = (np.empty((T, H, D)) for _ in range(4))
+    for h in range(H):
+        s = (q[:, h] @ k[:, h].T) * sc
+        s = np.where(mask, s, -np.inf)
+        p = np.exp(s - s.max(1, keepdims=True))
+        p /= p.sum(1, keepdims=True)
+        pv = p @ np.abs(v[:, h])
+        bo[:, h] = (u + gam) * pv + u * np.abs(o_ref[:, h])
+        dp = do[:, h] @ v[:, h].T
+        dd_exact = np.sum(do[:, h] * o_ref[:, h], 1)
+        dd_gpu = np.sum(do[:, h] * o_gpu[:, h], 1)
+        ds = p * (dp - dd_exact[:, None])
+        e_ds = u * np.abs(ds) + p * (np.abs(dd_gpu - dd_exact) + gam * np.sum(np.abs(do[:, h] * o_gpu[:, h]), 1))[:, None]
+        a_ds = np.abs(ds) + e_ds
+        bdq[:, h] = sc * (e_ds @ np.abs(k[:, h]) + gam * (a_ds @ np.abs(k[:, h])))
+        bdk[:, h] = sc * (e_ds.T @ np.abs(q[:, h]) + gam * (a_ds.T @ np.abs(q[:, h])))
+        dv = p.T @ do[:, h]
+        bdv[:, h] = (u + gam) * (p.T @ np.abs(do[:, h])) + u * np.abs(dv)
+    return bo, bdq, bdk, bdv
+
+
+def within(got, ref, bound, slack=2.0):
+    err = np.abs(np.asarray(got, dtype=np.float64) - ref)
+    lim = slack * bound + 1e-7 * (np.sqrt(np.mean(ref * ref)) + 1e-30)
+    return bool(np.all(err <= lim)), float(np.max(err / lim))
+
+
+@pytest.mark.parametrize("prec,T", [(0, 128), (0, 256), (0, 384), (0, 640), (0, 2048), (1, 100), (1, 200)],
+                         ids=["bf16_T128", "bf16_T256", "bf16_T384", "bf16_T640", "bf16_T2048", "fp32_T100",
+                              "fp32_T200"])
 def test_attention_fwd_bwd(nc, prec, T):
     import torch
     B, H, D = 2, 2, 128
@@ -237,20 +291,25 @@ def test_attention_fwd_bwd(nc, prec, T):
                                dqk.data_ptr(), dqkv.data_ptr())
         nc.nc_sync(c.ctx)
         o_h, lse_h, dqk_h, dqkv_h = host(o), lse.cpu().numpy(), dqk.cpu().numpy(), host(dqkv)
-        tol = 1e-2 if prec == 0 else 1e-5
         for b in range(B):
             x = qkv.reshape(B, T, 3, H, D)[b].astype(np.float64)
             q, k, v = x[:, 0], x[:, 1], x[:, 2]
             o_ref, lse_ref = oracle.causal_attention(q, k, v)
-            ob = o_h.reshape(B, T, H, D)[b]
-            assert np.linalg.norm(ob - o_ref) <= tol * np.linalg.norm(o_ref)
-            np.testing.assert_allclose(lse_h[b], lse_ref, atol=tol)
-            # the backward is checked with the forward output the kernel produced
+            ob = o_h.reshape(B, T, H, D)[b].astype(np.float64)
             g = dout.reshape(B, T, H, D)[b].astype(np.float64)
+            bo, bdq, bdk, bdv = attention_bounds(q, k, v, g, o_ref, ob, prec)
+            ok, worst = within(ob, o_ref, bo)
+            assert ok, ("o", b, worst)
+            # and in aggregate, where a small systematic error would show
+            assert np.linalg.norm(ob - o_ref) <= (1e-2 if prec == 0 else 1e-5) * np.linalg.norm(o_ref)
+            np.testing.assert_allclose(lse_h[b], lse_ref, atol=1e-3 if prec == 0 else 1e-5)
             dq_r, dk_r, dv_r = oracle.causal_attention_backward(q, k, v, g)
             got = dqk_h.reshape(2, B, T, H, D)[:, b]
-            for gg, rr in ((got[0], dq_r), (got[1], dk_r), (dqkv_h.reshape(B, T, 3, H, D)[b][:, 2], dv_r)):
-                assert np.linalg.norm(gg - rr) <= 2 * tol * np.linalg.norm(rr)
+            for name, gg, rr, bb in (("dq", got[0], dq_r, bdq), ("dk", got[1], dk_r, bdk),
+                                     ("dv", dqkv_h.reshape(B, T, 3, H, D)[b][:, 2], dv_r, bdv)):
+                ok, worst = within(gg, rr, bb)
+                assert ok, (name, b, worst)
+                assert np.linalg.norm(gg - rr) <= (2e-2 if prec == 0 else 2e-5) * np.linalg.norm(rr), name
         assert np.all(dqkv_h.reshape(B, T, 3, d)[:, :, :2] == 0)  # q,k columns untouched
     finally:
         c.close()
@@ -291,9 +350,11 @@ def test_lmhead_cross_entropy(nc, prec):
         sure = (top2[:, 1] - top2[:, 0]) > 1e-4
         np.testing.assert_array_equal(am.cpu().numpy()[sure], am_r[sure])
         dhf_r, dw_r = oracle.cross_entropy_backward(h64, w64, tgt, lse_r)
-        rel = 2e-2 if prec == 0 else 1e-5
-        assert np.linalg.norm(dhf.cpu().numpy() - dhf_r) <= rel * np.linalg.norm(dhf_r)
-        assert np.linalg.norm(dwl.cpu().numpy() - dw_r) <= rel * np.linalg.norm(dw_r)
+        # element-wise: g = softmax - onehot is rounded to bf16 (relative 2^-9)
+        # before both products, whose sums then carry that rounding
+        for name, got, ref in (("dhf", dhf.cpu().numpy(), dhf_r), ("dw_lm", dwl.cpu().numpy(), dw_r)):
+            ok, err = close_enough(got, ref, prec, rel_bf16=2e-2, rel_f32=2e-5)
+            assert ok, (name, err)
     finally:
         c.close()
 
@@ -334,5 +395,133 @@ def test_qk_norm_rope_and_rmsnorm(nc, prec):
         ok, err = close_enough(host(y), yn, prec)
         assert ok, err
         np.testing.assert_allclose(r.cpu().numpy(), rn[:, 0], rtol=1e-5)
+    finally:
+        c.close()
+
+
+# ---------------------------------------------------------------- embedding, RMSNorm and QK-norm/RoPE backward
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+def test_embedding_forward_and_backward(nc, prec):
+    """x = wte[tok] exactly (bf16 -> fp32 is exact); dwte[id] = sum of dx over
+    the positions holding id (the oracle's np.add.at), absent ids exactly 0;
+    an id out of range is reported as a device error, not trapped."""
+    import torch
+    B, T, H, V = 2, 256, 3, 1024
+    d = H * 128
+    M = B * T
+    rng = np.random.default_rng(41)
+    tok = np.minimum(rng.zipf(1.3, M) - 1, V - 1).astype(np.int32)  # repeated ids, a heavy first id
+    wte = rounded(rng.standard_normal((V, d)) * 0.02, prec)
+    dx = rng.standard_normal((M, d)).astype(np.float32)
+    c = Ctx(nc, 1, d, H, T, V, B, prec)
+    try:
+        dtok, dw = torch.from_numpy(tok).cuda(), torch_of(wte, prec, nc)
+        x = torch.full((M, d), np.nan, dtype=torch.float32, device="cuda")
+        nc.nc_op_embed_fwd(c.ctx, dtok.data_ptr(), dw.data_ptr(), x.data_ptr())
+        dwte = torch.full((V, d), 5.0, dtype=torch.float32, device="cuda")  # must be overwritten
+        ddx = torch.from_numpy(dx).cuda()
+        nc.nc_op_embed_bwd(c.ctx, dtok.data_ptr(), ddx.data_ptr(), dwte.data_ptr())
+        nc.nc_sync(c.ctx)
+        np.testing.assert_array_equal(x.cpu().numpy(), wte[tok])
+        ref = np.zeros((V, d))
+        np.add.at(ref, tok, dx.astype(np.float64))
+        got = dwte.cpu().numpy()
+        counts = np.bincount(tok, minlength=V)
+        # fp32 sums of n terms: |err| <= n * 2^-24 * sum |terms| (a loose bound per row)
+        bound = np.zeros((V, d))
+        np.add.at(bound, tok, np.abs(dx.astype(np.float64)))
+        assert np.all(np.abs(got - ref) <= counts[:, None] * 2.0 ** -23 * bound + 1e-30)
+        assert np.all(got[counts == 0] == 0.0)
+        bad = tok.copy()
+        bad[5] = V
+        nc.nc_op_embed_fwd(c.ctx, torch.from_numpy(bad).cuda().data_ptr(), dw.data_ptr(), x.data_ptr())
+        with pytest.raises(nc.NcError) as ei:
+            nc.nc_sync(c.ctx)
+        assert ei.value.status == 5  # NC_ERR_DEVICE
+        assert np.all(x.cpu().numpy()[5] == 0.0)
+    finally:
+        c.close()
+
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+@pytest.mark.parametrize("accumulate", [0, 1], ids=["store", "accumulate"])
+def test_rmsnorm_backward(nc, prec, accumulate):
+    """dz = r (dy - y mean(dy y)) (+ dx when accumulating), element-wise
+    against the oracle's rmsnorm_backward on the same rounded y and dy."""
+    import torch
+    B, T, H = 2, 256, 3
+    d = H * 128
+    M = B * T
+    rng = np.random.default_rng(43 + accumulate)
+    z = rng.standard_normal((M, d)) * 3
+    y, r = oracle.rmsnorm(z)
+    y = rounded(y, prec)
+    dy = rounded(rng.standard_normal((M, d)) * 0.1, prec)
+    dx0 = rng.standard_normal((M, d)).astype(np.float32)
+    c = Ctx(nc, 1, d, H, T, 1024, B, prec)
+    try:
+        elem = torch.bfloat16 if prec == 0 else torch.float32
+        ddy, dyv = torch_of(dy, prec, nc), torch_of(y, prec, nc)
+        dr = torch.from_numpy(r[:, 0].astype(np.float32)).cuda()
+        dx = torch.from_numpy(dx0.copy()).cuda()
+        dxe = torch.zeros((M, d), dtype=elem, device="cuda")
+        nc.nc_op_rmsnorm_bwd(c.ctx, ddy.data_ptr(), dyv.data_ptr(), dr.data_ptr(), dx.data_ptr(), dxe.data_ptr(),
+                             accumulate)
+        nc.nc_sync(c.ctx)
+        ref = oracle.rmsnorm_backward(dy.astype(np.float64), y.astype(np.float64),
+                                      r.astype(np.float32).astype(np.float64))
+        if accumulate:
+            ref = ref + dx0
+        ok, err = close_enough(dx.cpu().numpy(), ref, 1, rel_f32=2e-5)
+        assert ok, err
+        ok, err = close_enough(host(dxe), ref, prec, rel_bf16=8e-3, rel_f32=2e-5)
+        assert ok, err
+    finally:
+        c.close()
+
+
+@pytest.mark.parametrize("prec", [0, 1], ids=["bf16", "fp32"])
+def test_qk_norm_rope_backward(nc, prec):
+    """dq = r (dq_n - q_n mean(dq_n q_n)) with dq_n, q_n the inverse rotation
+    of dq_hat and of the stored q_hat, for q and k heads, element-wise against
+    the oracle's rope_backward and rmsnorm_backward; v columns untouched."""
+    import torch
+    B, T, H = 2, 256, 3
+    d, D = H * 128, 128
+    M = B * T
+    rng = np.random.default_rng(47)
+    raw = rng.standard_normal((B, T, 3, H, D)) * 0.7
+    cos, sin = oracle.rope_angles(T)
+    qkv = raw.copy()
+    rqk = np.empty((B, T, 2, H))
+    for which in (0, 1):
+        for b in range(B):
+            n, rr = oracle.rmsnorm(raw[b, :, which])
+            qkv[b, :, which] = oracle.rope(n, cos, sin)
+            rqk[b, :, which] = rr[..., 0]
+    qkv = rounded(qkv.reshape(M, 3 * d), prec)
+    rqk = rqk.reshape(M, 2 * H).astype(np.float32)
+    dqk = rng.standard_normal((2, M, d)).astype(np.float32)
+    c = Ctx(nc, 1, d, H, T, 1024, B, prec)
+    try:
+        elem = torch.bfloat16 if prec == 0 else torch.float32
+        dq_ = torch.from_numpy(dqk).cuda()
+        dqkv = torch.full((M, 3 * d), 9.0, dtype=elem, device="cuda")
+        nc.nc_op_qk_norm_rope_bwd(c.ctx, dq_.data_ptr(), torch_of(qkv, prec, nc).data_ptr(),
+                                  torch.from_numpy(rqk).cuda().data_ptr(), dqkv.data_ptr())
+        nc.nc_sync(c.ctx)
+        got = host(dqkv).reshape(B, T, 3, H, D)
+        src = qkv.reshape(B, T, 3, H, D).astype(np.float64)
+        for which in (0, 1):
+            for b in range(B):
+                g = dqk[which].reshape(B, T, H, D)[b].astype(np.float64)
+                gn = oracle.rope_backward(g, cos, sin)
+                qn = oracle.rope_backward(src[b, :, which], cos, sin)
+                rr = rqk.reshape(B, T, 2, H)[b, :, which].astype(np.float64)[..., None]
+                ref = oracle.rmsnorm_backward(gn, qn, rr)
+                ok, err = close_enough(got[b, :, which], ref, prec, rel_bf16=8e-3, rel_f32=2e-5)
+                assert ok, (which, b, err)
+        assert np.all(got[:, :, 2] == 9.0)
     finally:
         c.close()

@@ -3,15 +3,19 @@
 Callers that cannot call cudaMalloc at the point where they need the loss
 (code inside another framework's memory pool or allocation budget) use this
 entry point: its scratch lives in a static device array of the library. The
-test checks it, through the C ABI, against the workspace-based entry point
-nc_op_lmhead_ce_fwd on two calls in a row with different inputs, so a call
-that left stale scratch behind would show. It must pass in a fresh process
-and after the other tests.
+test checks it, through the C ABI, on two calls in a row with different
+inputs (so a call that left stale scratch behind would show), against the
+oracle's cross-entropy rows in float64 at row counts that take the
+single-CTA path (100 rows), a ragged last row block (1000 rows) and the
+largest request the static buffer holds at V = 65,536 (2,728 rows), and
+against the workspace-based entry point nc_op_lmhead_ce_fwd at 2,048 rows.
+It must pass in a fresh process and after the other tests.
 """
 
 import numpy as np
 import pytest
 
+import oracle
 import workload as W
 from gpu_util import load_nc
 
@@ -24,6 +28,47 @@ def _inputs(rng, M, d, V):
     wl = W.round_bf16(rng.standard_normal((V, d)) * 0.05)
     tgt = rng.integers(0, V, M).astype(np.int32)
     return hf, wl, tgt
+
+
+def _check_against_oracle(hf, wl, tgt, lse, nll, am):
+    h64, w64 = hf.astype(np.float64), wl.astype(np.float64)
+    lse_r, nll_r, am_r = oracle.cross_entropy_rows(h64, w64, tgt)
+    np.testing.assert_allclose(lse, lse_r, atol=1e-3)
+    np.testing.assert_allclose(nll, nll_r, atol=1e-3)
+    lg = h64 @ w64.T
+    top2 = np.partition(lg, -2, axis=1)[:, -2:]
+    sure = (top2[:, 1] - top2[:, 0]) > 1e-4
+    assert sure.mean() > 0.9
+    np.testing.assert_array_equal(am[sure], am_r[sure])
+
+
+def _static_call(nc, dh, dw, dt, M, d, V):
+    import torch
+    lse = torch.full((M,), np.nan, dtype=torch.float32, device="cuda")
+    nll = torch.full((M,), np.nan, dtype=torch.float32, device="cuda")
+    am = torch.full((M,), -1, dtype=torch.int32, device="cuda")
+    status = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    nc.nc_lmhead_ce_fwd_static(dh.data_ptr(), dw.data_ptr(), dt.data_ptr(), M, d, V, lse.data_ptr(),
+                               nll.data_ptr(), am.data_ptr(), status.data_ptr(), None)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return lse.cpu().numpy(), nll.cpu().numpy(), am.cpu().numpy()
+
+
+@pytest.mark.parametrize("M", [100, 1000, 2728])
+def test_static_scratch_ce_matches_oracle_on_two_calls(M):
+    import torch
+    nc = load_nc()
+    d, V = 256, 65536
+    rng = np.random.default_rng(77 + M)
+    for call in range(2):
+        hf, wl, tgt = _inputs(rng, M, d, V)
+        dh = torch.from_numpy(hf).to(torch.bfloat16).cuda()
+        dw = torch.from_numpy(wl).to(torch.bfloat16).cuda()
+        dt = torch.from_numpy(tgt).cuda()
+        lse, nll, am = _static_call(nc, dh, dw, dt, M, d, V)
+        assert np.all(np.isfinite(lse)) and np.all(np.isfinite(nll))
+        _check_against_oracle(hf, wl, tgt, lse, nll, am)
 
 
 def test_static_scratch_ce_matches_workspace_entry_point_on_two_calls():
@@ -64,6 +109,7 @@ def test_static_scratch_ce_matches_workspace_entry_point_on_two_calls():
             top2 = np.partition(lg, -2, axis=1)[:, -2:]
             sure = (top2[:, 1] - top2[:, 0]) > 1e-4
             np.testing.assert_array_equal(a1[sure], a0[sure])
+            _check_against_oracle(hf, wl, tgt, l1, n1, a1)
     finally:
         step.close()
 
