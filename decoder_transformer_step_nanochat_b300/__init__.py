@@ -81,6 +81,7 @@ _SIGS = {
     "nc_profile_read": (_I, [_P, _I, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(_LL),
                             ctypes.POINTER(ctypes.c_double)]),
     "nc_profile_reset": (_I, [_P]),
+    "nc_set_pipeline_wait_limit": (_I, [ctypes.c_ulonglong]),
     "nc_last_error": (ctypes.c_char_p, [_P]),
     "nc_destroy": (None, [_P]),
     "nc_op_gemm": (_I, [_P, _I, _I, _I, _P, _LL, _I, _P, _LL, _I, _I, _F, _F, _P, _LL, _P, _LL, _P, _P]),
@@ -228,6 +229,10 @@ def nc_profile_read(ctx, family):
 
 def nc_profile_reset(ctx):
     _check(lib().nc_profile_reset(ctx), ctx)
+
+
+def nc_set_pipeline_wait_limit(ns):
+    _check(lib().nc_set_pipeline_wait_limit(ns))
 
 
 def nc_last_error(ctx=None) -> str:

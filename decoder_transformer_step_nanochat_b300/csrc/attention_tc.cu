@@ -32,6 +32,10 @@ constexpr int TILE = 128;
 constexpr int HALF_BYTES = TILE * 128;        // 128 rows x 128 B
 constexpr int TILE_BYTES = 2 * HALF_BYTES;    // 32 KB
 constexpr uint64_t kWaitNs = 2000000000ull;
+// Limit of the pipeline waits (those an abort can end), in ns; kWaitNs
+// unless a test lowers it through the setter below. Teardown waits (for the
+// copies and products a CTA has in flight) always use kWaitNs.
+__device__ uint64_t g_pipe_wait_ns = kWaitNs;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kSqrt128 = 11.313708498984761f;
@@ -138,6 +142,7 @@ constexpr int FWD_KST = 1, FWD_VST = 1;
 __global__ void __launch_bounds__(FWD_THREADS, 2)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint64_t wait_ns = g_pipe_wait_ns;
   if (tc::smem_u32(smem_raw) & 1023) {
     if (threadIdx.x == 0) set_status(p.status, DEV_BAD_LAUNCH);
     return;
@@ -206,7 +211,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
       }
       int last = -1;
       for (int j = 0; j < nkv; ++j) {
-        if (!tc::mbar_wait(empty, (j & 1) ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+        if (!tc::mbar_wait(empty, (j & 1) ^ 1, abort_flag, wait_ns)) { failed = true; break; }
         const int kr = b * p.T + j * TILE;
         tc::mbar_arrive_expect_tx(full, TILE_BYTES);
         tc::tma_load_2d(buf, &tqkv, col, kr, full);
@@ -222,12 +227,12 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
       const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);
       bool any = false;
-      if (!tc::mbar_wait(q_full, 0, abort_flag, kWaitNs)) failed = true;
+      if (!tc::mbar_wait(q_full, 0, abort_flag, wait_ns)) failed = true;
       for (int j = 0; j <= nkv && !failed; ++j) {
         if (j > 0) {  // O += P(j-1) V(j-1), P read from the first 64 columns of S
           const int i = j - 1;
-          if (!tc::mbar_wait(v_full, i & 1, abort_flag, kWaitNs)) { failed = true; break; }
-          if (!tc::mbar_wait(p_full, i & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(v_full, i & 1, abort_flag, wait_ns)) { failed = true; break; }
+          if (!tc::mbar_wait(p_full, i & 1, abort_flag, wait_ns)) { failed = true; break; }
           tc::tc_fence_after();
           const uint32_t aV = tc::smem_u32(sV);
 #pragma unroll
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
           tc::mma_commit(v_empty);
         }
         if (j < nkv) {
-          if (!tc::mbar_wait(k_full, j & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(k_full, j & 1, abort_flag, wait_ns)) { failed = true; break; }
           tc::tc_fence_after();
           mma_tile(tmem, tc::smem_u32(sQ), false, tc::smem_u32(sK), false, idesc, false);
           any = true;
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
     const float sl2 = kLog2e * rsqrtf(128.f);
     float m = -INFINITY, l = 0.f;
     for (int j = 0; j <= qt; ++j) {
-      bool ok = tc::mbar_wait(s_full, j & 1, abort_flag, kWaitNs);
+      bool ok = tc::mbar_wait(s_full, j & 1, abort_flag, wait_ns);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
       float v[128];
@@ -321,7 +326,7 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
       tc::mbar_arrive_warp(p_full);
     }
     bool ok = !failed;
-    if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, kWaitNs);
+    if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, wait_ns);
     if (__all_sync(0xffffffffu, ok)) {
       tc::tc_fence_after();
       const float inv = 1.f / l;
@@ -416,6 +421,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
                   const __grid_constant__ CUtensorMap tdq, const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint64_t wait_ns = g_pipe_wait_ns;
   if (tc::smem_u32(smem_raw) & 1023) {  // see the forward kernel
     if (threadIdx.x == 0) set_status(p.status, DEV_BAD_LAUNCH);
     return;
@@ -496,14 +502,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (v >= nunits) v = -1;
         // K and V of the previous unit are free once its last products finished
         // (and by then every role has read the older ring slots)
-        if (ul > 0 && !tc::mbar_wait(kv_empty, (ul - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        if (ul > 0 && !tc::mbar_wait(kv_empty, (ul - 1) & 1, abort_flag, wait_ns)) { failed = true; break; }
         unit_ring[ul & 3] = v;
         if (v < 0) {
           // end marker: complete the phases the MMA thread (kv_full) and the
           // softmax warps (q_full of the next tile) wait on next; that query
           // stage's previous phase must be over first (its tile consumed)
           tc::mbar_arrive(kv_full);
-          if (g >= 2 && !tc::mbar_wait(q_empty + (g & 1), ((g >> 1) & 1) ^ 1, abort_flag, kWaitNs)) {
+          if (g >= 2 && !tc::mbar_wait(q_empty + (g & 1), ((g >> 1) & 1) ^ 1, abort_flag, wait_ns)) {
             failed = true;
             break;
           }
@@ -520,7 +526,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         for (int it = 0; it < u.nit; ++it, ++g) {
           const int s = g & 1;
           const uint32_t ph = (g >> 1) & 1;
-          if (!tc::mbar_wait(q_empty + s, ph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(q_empty + s, ph ^ 1, abort_flag, wait_ns)) { failed = true; break; }
           const int qr = u.b * p.T + (u.kt + it) * TILE;
           const size_t lrow = ((size_t)u.b * p.H + u.h) * p.T + (size_t)(u.kt + it) * TILE;
           tc::mbar_arrive_expect_tx(q_full + s, 2 * TILE_BYTES + 2 * TILE * 4);
@@ -552,18 +558,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       bool any = false;
       int g = 0, ul = 0;
       for (;; ++ul) {
-        if (!tc::mbar_wait(kv_full, ul & 1, abort_flag, kWaitNs)) { failed = true; break; }
+        if (!tc::mbar_wait(kv_full, ul & 1, abort_flag, wait_ns)) { failed = true; break; }
         const int v = unit_ring[ul & 3];
         if (v < 0) break;
         const BwdUnit u = bwd_unit(p, v);
         for (int it = 0; it < u.nit; ++it, ++g) {
           const int s = g & 1;
           const uint32_t aQ = tc::smem_u32(sQ + s * TILE_BYTES), adO = tc::smem_u32(sdO + s * TILE_BYTES);
-          if (!tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, wait_ns)) { failed = true; break; }
           // dP^T replaces dQ^T of the previous tile: wait until it was read out
           // (S^T replaces P^T, whose reader dV was issued before, and tcgen05
           // products of one thread run in issue order)
-          if (g > 0 && !tc::mbar_wait(tm_free, (g - 1) & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (g > 0 && !tc::mbar_wait(tm_free, (g - 1) & 1, abort_flag, wait_ns)) { failed = true; break; }
           tc::tc_fence_after();
           // S^T = K Q^T and dP^T = V dO^T over the whole 128-query tile: two
           // independent accumulator chains, interleaved
@@ -574,10 +580,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           }
           any = true;
           tc::mma_commit(st_full);
-          if (!tc::mbar_wait(p_full, g & 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(p_full, g & 1, abort_flag, wait_ns)) { failed = true; break; }
           // the first dV/dK of a unit overwrite the accumulators of the previous
           // one: wait until the epilogue warps have read them out
-          if (it == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, kWaitNs)) {
+          if (it == 0 && ul > 0 && !tc::mbar_wait(acc_free, (ul - 1) & 1, abort_flag, wait_ns)) {
             failed = true;
             break;
           }
@@ -631,7 +637,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       // the first query tile of the next unit (or the end marker) is announced
       // on that tile's q_full phase
       {
-        const bool ok = tc::mbar_wait(q_full + (g & 1), (g >> 1) & 1, abort_flag, kWaitNs);
+        const bool ok = tc::mbar_wait(q_full + (g & 1), (g >> 1) & 1, abort_flag, wait_ns);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       }
       const int v = unit_ring[ul & 3];
@@ -642,9 +648,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const int s = g & 1;
         const float* Lq = sLD + s * 2 * TILE + ch * 64;        // negated base-2 lse of this half's 64 query columns
         const float* Dq = sLD + s * 2 * TILE + TILE + ch * 64; // D of the same columns
-        bool ok = tc::mbar_wait(st_full, g & 1, abort_flag, kWaitNs);
+        bool ok = tc::mbar_wait(st_full, g & 1, abort_flag, wait_ns);
         // the lse / D rows arrived with this tile's Q (already complete here)
-        ok = ok && tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, kWaitNs);
+        ok = ok && tc::mbar_wait(q_full + s, (g >> 1) & 1, abort_flag, wait_ns);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         tc::tc_fence_after();
         const bool diag = (it == 0);
@@ -710,7 +716,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tc::bulk_wait_read();
           tc::mbar_arrive(q_empty + (s ^ 1));
         }
-        ok = tc::mbar_wait(dq_full, g & 1, abort_flag, kWaitNs);
+        ok = tc::mbar_wait(dq_full, g & 1, abort_flag, wait_ns);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         tc::tc_fence_after();
         // dQ^T of this half: TMEM lane = head dim 32*q4 + lane, column = query
@@ -723,7 +729,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // [64 queries x 32 dims] staged transposed (128-byte swizzle) and added
         // to the dq plane by one bulk tensor reduce-add, once the tile's last
         // products no longer read its Q/dO stage
-        ok = tc::mbar_wait(tile_done, g & 1, abort_flag, kWaitNs);
+        ok = tc::mbar_wait(tile_done, g & 1, abort_flag, wait_ns);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         uint8_t* blk = sQ + s * TILE_BYTES + stg_off;
 #pragma unroll
@@ -739,7 +745,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       if (failed) break;
       // ---- this unit's dK / dV, read out while the next unit's first query
       // tile already runs on the tensor cores
-      bool ok = tc::mbar_wait(acc_full, ul & 1, abort_flag, kWaitNs);
+      bool ok = tc::mbar_wait(acc_full, ul & 1, abort_flag, wait_ns);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
       const size_t m = (size_t)u.krow0 + r;
@@ -868,6 +874,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 // ============================================================== host side
+
+}  // namespace
+
+cudaError_t attn_tc_set_wait_limit(uint64_t ns) {
+  const uint64_t v = ns ? ns : kWaitNs;
+  return cudaMemcpyToSymbol(g_pipe_wait_ns, &v, sizeof(v));
+}
+
+namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
 std::once_flag g_enc_once;

@@ -42,6 +42,10 @@ constexpr int NEPI_WARPS = 8;           // two per TMEM lane quadrant, each half
 constexpr int NTHREADS = 64 + 32 * NEPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column fp32 accumulators
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+// Limit of the pipeline waits (those an abort can end), in ns; kWaitNs
+// unless a test lowers it through the setter below. Teardown waits (for the
+// copies and products a CTA has in flight) always use kWaitNs.
+__device__ uint64_t g_pipe_wait_ns = kWaitNs;
 constexpr int STAGING_BYTES = 4096;  // per epilogue warp: 32 rows x 128 B, 128B-swizzled
 
 // Pipeline shape per CTA: single CTAs stage A and the whole B tile (4 x 48 KB);
@@ -227,6 +231,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const GemmArgs& g = p.g;
+  const uint64_t wait_ns = g_pipe_wait_ns;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int rank = (CL == 2) ? (int)tc::cluster_ctarank() : 0;
   const int v_first = (CL == 2) ? (int)blockIdx.x / 2 : (int)blockIdx.x;
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int n0 = nb * BN;
         const int a_off = (int)(bt * g.a_brows), b_off = (int)(bt * g.b_brows);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(empty + stage, phase ^ 1, abort_flag, wait_ns)) { failed = true; break; }
           const int k0 = kb * BK;
           uint8_t* a = sA + stage * A_BYTES;
           uint8_t* b = sB + stage * B_STAGE;
@@ -348,11 +353,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         unit_of<CL>(p, v, rank, bt, m0, nb, split, kb0, kb1);
         const int ab = cnt & 1;
         const uint32_t aph = (cnt >> 1) & 1;
-        if (!tc::mbar_wait(tempty + ab, aph ^ 1, abort_flag, kWaitNs)) { failed = true; break; }
+        if (!tc::mbar_wait(tempty + ab, aph ^ 1, abort_flag, wait_ns)) { failed = true; break; }
         tc::tc_fence_after();
         const uint32_t dtm = tmem_base + ab * BN;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!tc::mbar_wait(full + stage, phase, abort_flag, kWaitNs)) { failed = true; break; }
+          if (!tc::mbar_wait(full + stage, phase, abort_flag, wait_ns)) { failed = true; break; }
           tc::tc_fence_after();
           const uint32_t a_addr = tc::smem_u32(sA + stage * A_BYTES);
           const uint32_t b_addr = tc::smem_u32(sB + stage * B_STAGE);
@@ -398,7 +403,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int ab = cnt & 1;
       const uint32_t aph = (cnt >> 1) & 1;
       const int n0 = nb * BN + ch * (BN / 2);
-      const bool ok = tc::mbar_wait(tfull + ab, aph, abort_flag, kWaitNs);
+      const bool ok = tc::mbar_wait(tfull + ab, aph, abort_flag, wait_ns);
       if (!__all_sync(0xffffffffu, ok)) { failed = true; *abort_flag = 1; break; }
       tc::tc_fence_after();
       const int m = m0 + row;
@@ -536,11 +541,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             if (!chunk_ok) continue;
             if (EPI == EPI_RELU2_BWD) {
-              const bool got = tc::mbar_wait(c2bar + (warp - 2), c2n & 1, abort_flag, kWaitNs);
+              const bool got = tc::mbar_wait(c2bar + (warp - 2), c2n & 1, abort_flag, wait_ns);
               ++c2n;
               if (!__all_sync(0xffffffffu, got)) {
                 failed = true;
                 *abort_flag = 1;
+                // the tile load this warp started lands before the CTA can leave
+                if (!got) tc::mbar_wait(c2bar + (warp - 2), (c2n - 1) & 1, nullptr, kWaitNs);
               }
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
@@ -622,6 +629,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     else tc::tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
+
+}  // namespace
+
+cudaError_t gemm_tc_set_wait_limit(uint64_t ns) {
+  const uint64_t v = ns ? ns : kWaitNs;
+  return cudaMemcpyToSymbol(g_pipe_wait_ns, &v, sizeof(v));
+}
+
+namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;

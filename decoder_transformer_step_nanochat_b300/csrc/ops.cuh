@@ -101,6 +101,14 @@ template <typename T>
 cudaError_t attn_bwd_simt(const T* qkv, const T* dout, const float* lse, const float* Drow,
                           float* dqk, T* dqkv, int B, int T_, int H, cudaStream_t s);
 
+// Limit (ns) of the pipeline waits of the kernels launched after the call
+// (0: the default of 2 s), one setter per kernel file. A test hook: the
+// teardown waits keep the default, and CTA pairs (GEMMs of more than 128 rows)
+// must not run under a short limit (a pair's unwinding waits for the copies of
+// the phases the even CTA armed, not for copies the odd CTA started alone).
+cudaError_t gemm_tc_set_wait_limit(uint64_t ns);
+cudaError_t attn_tc_set_wait_limit(uint64_t ns);
+
 // tcgen05 flash attention (bf16, T % 128 == 0).
 bool attn_tc_supports(int T);
 cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int H, int* status, cudaStream_t s);

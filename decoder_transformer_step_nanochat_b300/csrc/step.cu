@@ -1032,6 +1032,14 @@ nc_status nc_profile_reset(nc_ctx* c) {
   return NC_OK;
 }
 
+nc_status nc_set_pipeline_wait_limit(unsigned long long ns) {
+  CK(cudaDeviceSynchronize());  // no kernel of this library may be running while the limit changes
+  CK(gemm_tc_set_wait_limit(ns));
+  CK(attn_tc_set_wait_limit(ns));
+  CK(cudaDeviceSynchronize());
+  return NC_OK;
+}
+
 const char* nc_last_error(const nc_ctx*) { return g_err.c_str(); }
 
 void nc_destroy(nc_ctx* c) {

@@ -61,14 +61,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase of `bar` with the given parity to complete. Gives up
 // after `limit_ns` nanoseconds or when *abort becomes non-zero; returns false
-// then (the caller records the failure and unwinds).
+// then (the caller records the failure and unwinds). The clock and the abort
+// flag are read every 64 polls, or on every poll when the limit is below a
+// microsecond (a test's short limit then ends the wait at once).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
+  const bool short_limit = limit_ns < 1000;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
+    if (short_limit || (it & 63) == 0) {
       if (abort && *abort) return false;
       if (globaltimer() - t0 > limit_ns) return false;
     }

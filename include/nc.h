@@ -208,6 +208,19 @@ nc_status nc_profile_read(nc_ctx* ctx, int family, double* ms, long long* launch
 /* Synchronise and clear the recorded launches (profiling stays as set). */
 nc_status nc_profile_reset(nc_ctx* ctx);
 
+/* Test hook for the failure path: set the time limit (ns) of every pipeline
+ * wait (TMA stage, accumulator and softmax hand-offs) of the tensor-core
+ * kernels launched afterwards on the current device, for every context; 0
+ * restores the default of 2 s. Below 1000 ns a wait gives up at its first
+ * unsuccessful poll, so a launch reports NC_ERR_TIMEOUT at the next
+ * synchronising call (its kernels unwind: the waits for the copies and
+ * products already in flight keep the default limit, and TMEM is freed).
+ * Only the attention kernels and GEMMs of at most 128 rows may run under a
+ * short limit: a GEMM of more rows runs in CTA pairs, whose unwinding waits
+ * only for the copies of the phases the even CTA of the pair armed.
+ * Synchronises the device. */
+nc_status nc_set_pipeline_wait_limit(unsigned long long ns);
+
 /* Message for the calling thread's last failing call ("" if none). */
 const char* nc_last_error(const nc_ctx* ctx);
 
