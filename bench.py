@@ -70,6 +70,8 @@ def parse_args():
                     help="skip timing the optimizer step (Muon + AdamW) after the fwd+bwd step")
     ap.add_argument("--no-infer", action="store_true",
                     help="skip timing generation (prefill + KV-cache decode steps)")
+    ap.add_argument("--protocol-steps", type=int, default=50,
+                    help="replayed steps of the timing-distribution block run when --steps is smaller (0: none)")
     ap.add_argument("--kernel", default=None, choices=sorted(KERNEL_CASES),
                     help="time one op of the path at the d20 shapes through the C ABI (for ncu captures)")
     ap.add_argument("--reps", type=int, default=3, help="launches of the --kernel case after one warm-up launch")
@@ -290,20 +292,23 @@ def our_arm(args):
     # the timing protocol of at least 50 replayed steps after 10 warm-up
     # replays, reported beside the K-step headline when K < 50
     protocol = None
-    if args.steps < 50:
+    npro = args.protocol_steps
+    if 0 < args.steps < npro:
         for _ in range(10):
             graph.replay()
-        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(51)]
+        torch.cuda.synchronize()
+        ev2 = [torch.cuda.Event(enable_timing=True) for _ in range(npro + 1)]
         with torch.cuda.stream(stream):
             ev2[0].record(stream)
-            for i in range(50):
+            for i in range(npro):
                 graph.replay()
                 ev2[i + 1].record(stream)
         torch.cuda.synchronize()
-        protocol = step_distribution([ev2[i].elapsed_time(ev2[i + 1]) for i in range(50)])
-    else:
+        protocol = step_distribution([ev2[i].elapsed_time(ev2[i + 1]) for i in range(npro)])
+    elif npro > 0:
         protocol = dict(dist_ms)
-    protocol["tokens_per_s_median"] = job_tokens_per_s(ws, M, protocol["median_ms"])
+    if protocol is not None:
+        protocol["tokens_per_s_median"] = job_tokens_per_s(ws, M, protocol["median_ms"])
     del graph
 
     # ---- per-kernel-family device time: K eager steps, every launch

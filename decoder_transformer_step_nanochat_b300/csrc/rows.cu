@@ -163,68 +163,133 @@ __global__ void qk_norm_rope_fwd_k(T* __restrict__ qkv, float* __restrict__ rqk,
 // Backward of q_hat = rope(rmsnorm(q)): dq_n = R^T dq_hat, q_n = R^T q_hat,
 // dq = r * (dq_n - q_n * mean(dq_n * q_n)). dqk is fp32 [2, M, d] (dq_hat
 // plane, then dk_hat plane); results go to the q,k columns of dqkv[M,3d].
+// One warp per (token, q or k): the position's rotation angles are read once
+// and the token's heads are taken four at a time, with all their loads issued
+// before the arithmetic (a warp-per-head layout kept too few bytes in flight).
+// Lane L owns the rotation pairs j = 2L, 2L+1 (partners j+64), so every access
+// is a coalesced 2-element vector; heads = 1 covers only the q heads.
 template <typename T>
 __global__ void qk_norm_rope_bwd_k(const float* __restrict__ dqk, const T* __restrict__ qkv,
                                    const float* __restrict__ rqk, const float* __restrict__ cs,
                                    const float* __restrict__ sn, T* __restrict__ dqkv, int M,
                                    int Tlen, int H, int heads) {
-  // lane L owns the rotation pairs j = 2L and 2L+1 (partners 2L+64, 2L+65),
-  // so every access is a coalesced 2-element vector; heads = 1 covers only
-  // the q heads of each row
-  int w = blockIdx.x * kRowWarps + threadIdx.x / 32;
-  int lane = threadIdx.x & 31;
-  if (w >= M * heads * H) return;
-  int m = w / (heads * H), wh = w % (heads * H);
-  int d = H * kHeadDim;
-  const int which = wh / H, hh = wh % H;
-  const float* g = dqk + (size_t)which * M * d + (size_t)m * d + (size_t)hh * kHeadDim;
-  const T* q = qkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
+  const int w = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= M * heads) return;
+  const int m = w / heads, which = w % heads;
+  const int d = H * kHeadDim;
   const int t = m % Tlen, j = 2 * lane;
   const float2 co = *reinterpret_cast<const float2*>(cs + t * kHalf + j);
   const float2 si = *reinterpret_cast<const float2*>(sn + t * kHalf + j);
-  const float2 g1 = *reinterpret_cast<const float2*>(g + j);
-  const float2 g2 = *reinterpret_cast<const float2*>(g + j + kHalf);
-  const float2 qa = ld2(q + j), qb = ld2(q + j + kHalf);
-  const float q1[2] = {qa.x, qa.y}, q2[2] = {qb.x, qb.y};
   const float c2[2] = {co.x, co.y}, s2[2] = {si.x, si.y};
-  const float a1[2] = {g1.x, g1.y}, a2[2] = {g2.x, g2.y};
-  float gn[4], qn[4];
+  const float* gbase = dqk + (size_t)which * M * d + (size_t)m * d;
+  const T* qbase = qkv + (size_t)m * 3 * d + (size_t)which * d;
+  T* obase = dqkv + (size_t)m * 3 * d + (size_t)which * d;
+  const float* rbase = rqk + (size_t)m * 2 * H + (size_t)which * H;
+  for (int h0 = 0; h0 < H; h0 += 4) {
+    float2 g1[4], g2[4], qa[4], qb[4];
+    float rr[4];
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    gn[u] = a1[u] * c2[u] + a2[u] * s2[u];
-    gn[u + 2] = -a1[u] * s2[u] + a2[u] * c2[u];
-    qn[u] = q1[u] * c2[u] + q2[u] * s2[u];
-    qn[u + 2] = -q1[u] * s2[u] + q2[u] * c2[u];
+    for (int i = 0; i < 4; ++i) {
+      const int h = h0 + i;
+      if (h < H) {
+        const float* g = gbase + h * kHeadDim;
+        const T* q = qbase + h * kHeadDim;
+        g1[i] = *reinterpret_cast<const float2*>(g + j);
+        g2[i] = *reinterpret_cast<const float2*>(g + j + kHalf);
+        qa[i] = ld2(q + j);
+        qb[i] = ld2(q + j + kHalf);
+        rr[i] = rbase[h];
+      } else {
+        g1[i] = g2[i] = qa[i] = qb[i] = make_float2(0.f, 0.f);
+        rr[i] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float q1[2] = {qa[i].x, qa[i].y}, q2[2] = {qb[i].x, qb[i].y};
+      const float a1[2] = {g1[i].x, g1[i].y}, a2[2] = {g2[i].x, g2[i].y};
+      float gn[4], qn[4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        gn[u] = a1[u] * c2[u] + a2[u] * s2[u];
+        gn[u + 2] = -a1[u] * s2[u] + a2[u] * c2[u];
+        qn[u] = q1[u] * c2[u] + q2[u] * s2[u];
+        qn[u + 2] = -q1[u] * s2[u] + q2[u] * c2[u];
+      }
+      const float dot = warp_sum(gn[0] * qn[0] + gn[1] * qn[1] + gn[2] * qn[2] + gn[3] * qn[3]) / (float)kHeadDim;
+      const int h = h0 + i;
+      if (h < H) {
+        T* o = obase + h * kHeadDim;
+        st2(o + j, make_float2(rr[i] * (gn[0] - qn[0] * dot), rr[i] * (gn[1] - qn[1] * dot)));
+        st2(o + j + kHalf, make_float2(rr[i] * (gn[2] - qn[2] * dot), rr[i] * (gn[3] - qn[3] * dot)));
+      }
+    }
   }
-  float dot = warp_sum(gn[0] * qn[0] + gn[1] * qn[1] + gn[2] * qn[2] + gn[3] * qn[3]) / (float)kHeadDim;
-  float rr = rqk[(size_t)m * 2 * H + wh];
-  T* o = dqkv + (size_t)m * 3 * d + (size_t)wh * kHeadDim;
-  st2(o + j, make_float2(rr * (gn[0] - qn[0] * dot), rr * (gn[1] - qn[1] * dot)));
-  st2(o + j + kHalf, make_float2(rr * (gn[2] - qn[2] * dot), rr * (gn[3] - qn[3] * dot)));
+}
+
+__device__ __forceinline__ void ld8(const bf16* p, float* f) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+    f[2 * i] = x.x;
+    f[2 * i + 1] = x.y;
+  }
+}
+__device__ __forceinline__ void ld8(const float* p, float* f) {
+  const float4 a = ld4(p), b = ld4(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
 // D[b,h,t] = sum_e dout[m, h*128+e] * o[m, h*128+e]  (softmax backward term).
 // With lse given, also nL2[b,h,t] = -(lse * log2(e) + 3.5): the row's negated
 // logsumexp in base-2 units, offset so that exp2(s * log2(e) / sqrt(128) + nL2)
 // is the probability already multiplied by the 1/sqrt(128) = 2^-3.5 score
-// scale.
+// scale. One warp per token row and all its heads: the warp's halves take
+// heads 2i and 2i+1, a lane 8 consecutive dims, and the loads of four head
+// pairs are issued before any sum (one warp per (token, head) kept 512 bytes
+// in flight per warp).
 template <typename T>
 __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ o,
                               float* __restrict__ Drow, int B, int Tlen, int H,
                               const float* __restrict__ lse, float* __restrict__ L2) {
-  int w = blockIdx.x * kRowWarps + threadIdx.x / 32;  // (m, h)
-  int lane = threadIdx.x & 31;
-  int M = B * Tlen;
-  if (w >= M * H) return;
-  int m = w / H, h = w % H;
-  size_t base = (size_t)m * H * kHeadDim + (size_t)h * kHeadDim + 4 * lane;  // 4 consecutive dims per lane
-  const float4 u = ld4(dout + base), v = ld4(o + base);
-  float s = warp_sum(u.x * v.x + u.y * v.y + u.z * v.z + u.w * v.w);
-  int b = m / Tlen, t = m % Tlen;
-  const size_t i = ((size_t)b * H + h) * Tlen + t;
-  if (lane == 0) {
-    Drow[i] = s;
-    if (L2) L2[i] = -fmaf(lse[i], 1.4426950408889634f, 3.5f);
+  const int m = blockIdx.x * kRowWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const int M = B * Tlen;
+  if (m >= M) return;
+  const int half = lane >> 4, l16 = lane & 15;
+  const int b = m / Tlen, t = m % Tlen;
+  const size_t row = (size_t)m * H * kHeadDim + l16 * 8;
+  for (int h0 = 0; h0 < H; h0 += 8) {
+    float u[4][8], v[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int h = h0 + 2 * i + half;
+      if (h < H) {
+        ld8(dout + row + (size_t)h * kHeadDim, u[i]);
+        ld8(o + row + (size_t)h * kHeadDim, v[i]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) u[i][e] = v[i][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sum += u[i][e] * v[i][e];
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      const int h = h0 + 2 * i + half;
+      if (l16 == 0 && h < H) {
+        const size_t idx = ((size_t)b * H + h) * Tlen + t;
+        Drow[idx] = sum;
+        if (L2) L2[idx] = -fmaf(lse[idx], 1.4426950408889634f, 3.5f);
+      }
+    }
   }
 }
 
@@ -468,15 +533,15 @@ cudaError_t qk_norm_rope_fwd(T* qkv, float* rqk, const float* cs, const float* s
 template <typename T>
 cudaError_t qk_norm_rope_bwd(const float* dqk, const T* qkv, const float* rqk, const float* cs,
                              const float* sn, T* dqkv, int M, int T_, int H, cudaStream_t s, int heads) {
-  qk_norm_rope_bwd_k<T><<<row_blocks((long long)M * heads * H), 32 * kRowWarps, 0, s>>>(dqk, qkv, rqk, cs, sn, dqkv, M,
-                                                                                    T_, H, heads);
+  qk_norm_rope_bwd_k<T><<<row_blocks((long long)M * heads), 32 * kRowWarps, 0, s>>>(dqk, qkv, rqk, cs, sn, dqkv, M,
+                                                                                T_, H, heads);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, int H,
                         cudaStream_t s, const float* lse, float* L2) {
-  attn_rowdot_k<T><<<row_blocks((long long)B * T_ * H), 32 * kRowWarps, 0, s>>>(dout, o, Drow, B, T_, H, lse, L2);
+  attn_rowdot_k<T><<<row_blocks((long long)B * T_), 32 * kRowWarps, 0, s>>>(dout, o, Drow, B, T_, H, lse, L2);
   return cudaGetLastError();
 }
 
