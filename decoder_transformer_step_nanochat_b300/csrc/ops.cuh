@@ -69,6 +69,14 @@ template <typename T> cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s);
 bool gemm_tc_supports(const GemmArgs& g);
 
+// Weight-streaming product of the decode step: C (fp32) = alpha * A W^T (+ beta * C)
+// for M <= 16 rows of A (bf16 [M, K], K-major) and W (bf16 [N, K], K-major),
+// K a multiple of 32, 16-byte aligned operands; one launch, deterministic.
+// sms: the device's SM count (sizes the column groups).
+bool skinny_gemm_supports(int M, int N, int K, long long lda, long long ldw, const void* A, const void* W);
+cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
+                        int N, int K, float alpha, float beta, int sms, cudaStream_t s);
+
 // ------------------------------------------------------------------ rows
 template <typename T>
 cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int V, int* status,

@@ -72,6 +72,7 @@ struct nc_ctx {
   int B = 0, M = 0, prec = -1, esz = 0;
   cudaStream_t stream = nullptr;
   int device = -1;
+  int sms = 148;            // SM count of the configured device
   bool use_tc = false;      // tensor-core GEMMs for the bf16 mode
   float* rope_cos = nullptr;   // [T][64]
   float* rope_sin = nullptr;
@@ -667,8 +668,30 @@ KvLayout kv_layout(const nc_ctx* c, int max_len) {
   return k;
 }
 
+// One product of the decode step, C (fp32 [B, N]) = A W^T (+ beta C) with A
+// (elem [B, K]) one row per sequence: the weight-streaming kernel in bf16 for
+// up to 16 rows, the step's GEMM otherwise. Timed as decode GEMM work, counted
+// in weight bytes streamed.
+template <typename T>
+nc_status dec_gemm(nc_ctx* c, int N, int K, const T* A, const T* W, float* C, float beta) {
+  const int Bn = c->B;
+  if constexpr (sizeof(T) == 2) {
+    if (skinny_gemm_supports(Bn, N, K, K, K, A, W)) {
+      KL(NC_FAM_DEC_GEMM, (double)N * K * sizeof(T), 1,
+         skinny_gemm(A, K, W, K, C, N, Bn, N, K, 1.f, beta, c->sms, c->stream));
+      return NC_OK;
+    }
+  }
+  c->gemm_fam = NC_FAM_DEC_GEMM;
+  nc_status st = gemm(c, mk(Bn, N, K, A, K, 1, W, K, 1, EPI_STORE_F32, C, N, 1.f, beta));
+  c->gemm_fam = NC_FAM_GEMM;
+  return st;
+}
+
 // Greedy head over B rows of final hidden state: argmax (lowest index on
-// ties) into next; fp32 logits too when requested.
+// ties) into next; fp32 logits too when requested. With the weight-streaming
+// product the logits of the B rows are formed in fp32 (in the caller's buffer
+// when given, else in the workspace) and reduced per row.
 template <typename T>
 nc_status decode_head(nc_ctx* c, const T* P, const T* hf, int32_t* next, float* logits) {
   const int Bn = c->B, d = c->d, V = c->V;
@@ -676,6 +699,14 @@ nc_status decode_head(nc_ctx* c, const T* P, const T* hf, int32_t* next, float* 
   const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
   int* tgt = wsp<int>(c, c->dec.tgt);  // -1: no target, only lse and argmax
   CK(cudaMemsetAsync(tgt, 0xff, (size_t)Bn * sizeof(int), c->stream));
+  if (c->prec == NC_BF16 && skinny_gemm_supports(Bn, V, d, d, d, hf, Wlm)) {
+    float* lg = logits ? logits : wsp<float>(c, c->off.chunk);
+    CKS(dec_gemm<T>(c, V, d, hf, Wlm, lg, 0.f));
+    KL(NC_FAM_DEC_ROWS, 4.0 * Bn * V, 1,
+       ce_rows_from_logits(lg, tgt, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next, Bn, V, c->status,
+                           c->stream));
+    return NC_OK;
+  }
   c->gemm_fam = NC_FAM_DEC_GEMM;
   nc_status st = lmhead_ce_forward<T>(c, hf, Wlm, tgt, Bn, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next);
   if (st == NC_OK && logits) st = gemm(c, mk(Bn, V, d, hf, d, 1, Wlm, d, 1, EPI_STORE_F32, logits, V));
@@ -755,28 +786,16 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
     T* K = reinterpret_cast<T*>(kv + (size_t)2 * l * kl.per);
     T* Vc = reinterpret_cast<T*>(kv + (size_t)(2 * l + 1) * kl.per);
     KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    c->gemm_fam = NC_FAM_DEC_GEMM;
-    nc_status st = gemm(c, mk(Bn, 3 * d, d, xn, d, 1, Wqkv, d, 1, EPI_STORE_F32, qkv, 3 * d));
-    c->gemm_fam = NC_FAM_GEMM;
-    CKS(st);
+    CKS(dec_gemm<T>(c, 3 * d, d, xn, Wqkv, qkv, 0.f));
     KL(NC_FAM_DEC_ROWS, (double)Bn * 3 * d * (4 + e), 1,
        decode_qkv<T>(qkv, qh, K, Vc, rc, rs, Bn, H, pos, d_pos, max_len, c->status, s));
     KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * ((d_pos ? max_len : pos) + 1) * e, 2,
        attn_decode<T>(qh, K, Vc, part, o, Bn, H, pos, d_pos, max_len, kDecodeChunk, s));
-    c->gemm_fam = NC_FAM_DEC_GEMM;
-    st = gemm(c, mk(Bn, d, d, o, d, 1, Wo, d, 1, EPI_STORE_F32, x, d, 1.f, 1.f));
-    c->gemm_fam = NC_FAM_GEMM;
-    CKS(st);
+    CKS(dec_gemm<T>(c, d, d, o, Wo, x, 1.f));
     KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    c->gemm_fam = NC_FAM_DEC_GEMM;
-    st = gemm(c, mk(Bn, F, d, xn, d, 1, Wfc, d, 1, EPI_STORE_F32, u, F));
-    c->gemm_fam = NC_FAM_GEMM;
-    CKS(st);
+    CKS(dec_gemm<T>(c, F, d, xn, Wfc, u, 0.f));
     KL(NC_FAM_DEC_ROWS, (double)Bn * F * (4 + e), 1, relu2_rows<T>(u, a, (long long)Bn * F, s));
-    c->gemm_fam = NC_FAM_DEC_GEMM;
-    st = gemm(c, mk(Bn, d, F, a, F, 1, Wproj, F, 1, EPI_STORE_F32, x, d, 1.f, 1.f));
-    c->gemm_fam = NC_FAM_GEMM;
-    CKS(st);
+    CKS(dec_gemm<T>(c, d, F, a, Wproj, x, 1.f));
   }
   KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, hf, r, Bn, d, s));
   CKS(decode_head<T>(c, P, hf, next, logits));
@@ -861,6 +880,7 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   CK(cudaMemsetAsync(c->status, 0, sizeof(int), c->stream));
   CK(cudaStreamSynchronize(c->stream));
   c->device = dev;
+  c->sms = prop.multiProcessorCount > 0 ? prop.multiProcessorCount : 148;
   c->B = batch; c->M = batch * c->T; c->prec = precision;
   c->esz = precision == NC_BF16 ? 2 : 4;
   c->use_tc = precision == NC_BF16;

@@ -77,9 +77,12 @@ def test_tiny_fp32_generation_matches_oracle():
         np.testing.assert_array_equal(ids[:, i], np.argmax(r, -1))
 
 
-def test_small_bf16_generation_matches_oracle():
+@pytest.mark.parametrize("batch", [8, 1, 20], ids=["batch8", "batch1", "batch20"])
+def test_small_bf16_generation_matches_oracle(batch):
+    """Batches of up to 16 sequences take the weight-streaming decode products
+    (one to sixteen rows), larger ones the tensor-core GEMM."""
     nc = load_nc()
-    w = W.WORKLOADS["small"]
+    w = W.WORKLOADS["small"].with_batch(batch)
     p = W.make_params(w)
     tok, _ = W.make_tokens(w)
     feed = W.make_decode_tokens(w, 4)
