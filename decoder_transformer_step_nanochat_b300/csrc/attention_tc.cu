@@ -111,23 +111,28 @@ struct AttnParams {
 
 // ============================================================== forward
 //
-// One CTA per (b, h, 128-query tile), two CTAs per SM: the tensor cores
-// interleave the independent products of the two CTAs, which a single
-// accumulator chain cannot keep busy (a 128x128x16 MMA issued back to back
-// into one accumulator runs at about 58% of the tensor rate; two chains
-// reach it). Eight warps: warp 0 loads Q and K, warp 2 loads V, one thread
-// of warp 1 issues the MMAs, warps 4-7 run the softmax with one thread per
-// query row (TMEM lane = row), so a row's max and sum never leave its thread.
-// TMEM (256 columns per CTA): S [0,128), with P written back over its first
-// 64 columns as packed bf16 that O += P V reads straight from TMEM, and O
+// Persistent: two CTAs per SM, each taking work items (b, h, 128-query tile)
+// from a global counter in (batch, head)-major order, heaviest query tile
+// first within a head. The tensor cores interleave the independent products
+// of the SM's two CTAs, which a single accumulator chain cannot keep busy (a
+// 128x128x16 MMA issued back to back into one accumulator runs at about 58%
+// of the tensor rate; two chains reach it). Eight warps: warp 0 draws the
+// items and loads Q and K, warp 2 loads V, one thread of warp 1 issues the
+// MMAs, warps 4-7 run the softmax with one thread per query row (TMEM lane =
+// row), so a row's max and sum never leave its thread, and write O. TMEM (256
+// columns per CTA, allocated once): S [0,128), with P written back over its
+// first 64 columns as packed bf16 that O += P V reads straight from TMEM, and O
 // [128,256). Shared memory: Q and single K and V buffers (96 KB).
 //
-// MMA order: S(0), then per key tile j >= 1: PV(j-1), S(j). A commit covers
-// every MMA issued before it, so once S(j) is seen complete PV(j-1) has
-// landed too: O is quiescent while the softmax may rescale it, and P(j-1)
-// was read before S(j) overwrote it. The softmax keeps per row a reference
-// maximum m (log2 units); only when a tile's maximum exceeds m by more than
-// 8 does it move m up and rescale the row of O and the running sum.
+// MMA order per item: S(0), then per key tile j >= 1: PV(j-1), S(j), then the
+// last PV. A commit covers every MMA issued before it, so once S(j) is seen
+// complete PV(j-1) has landed too: O is quiescent while the softmax may
+// rescale it, and P(j-1) was read before S(j) overwrote it. The softmax keeps
+// per row a reference maximum m (log2 units); only when a tile's maximum
+// exceeds m by more than 8 does it move m up and rescale the row of O and the
+// running sum. Between items: the next Q and first K load once the last S(j)
+// has read Q and K, and the next item's S(0) runs while the softmax warps
+// read O out; its first PV waits until they have (o_free).
 
 constexpr float kRescaleLog2 = 8.f;
 constexpr int FWD_WARPS = 8;
@@ -138,6 +143,19 @@ constexpr int FWD_SOFT = 128;
 constexpr int FWD_REG_LAUNCH = 128, FWD_REG_LOW = 56, FWD_REG_HIGH = 200;
 static_assert(128 * FWD_REG_LOW + 128 * FWD_REG_HIGH <= FWD_THREADS * FWD_REG_LAUNCH, "register split");
 constexpr int FWD_KST = 1, FWD_VST = 1;
+
+struct FwdItem {
+  int b, h, qt, row0;
+};
+__device__ __forceinline__ FwdItem fwd_item(const AttnParams& p, int v) {
+  FwdItem it;
+  const int bh = v / p.nq;
+  it.b = bh / p.H;
+  it.h = bh % p.H;
+  it.qt = p.nq - 1 - v % p.nq;
+  it.row0 = it.b * p.T + it.qt * TILE;
+  return it;
+}
 
 __global__ void __launch_bounds__(FWD_THREADS, 2)
     attn_fwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ AttnParams p) {
@@ -152,26 +170,30 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
   uint8_t* sK = sQ + TILE_BYTES;
   uint8_t* sV = sK + TILE_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + TILE_BYTES);
-  uint64_t* q_full = bars + 0;
+  uint64_t* q_full = bars + 0;   // Q of an item landed (and the item announced)
   uint64_t* k_full = bars + 1;
   uint64_t* k_empty = bars + 2;
   uint64_t* v_full = bars + 3;
   uint64_t* v_empty = bars + 4;
   uint64_t* s_full = bars + 5;
   uint64_t* p_full = bars + 6;
-  uint64_t* o_full = bars + 7;
+  uint64_t* o_full = bars + 7;   // the item's last PV done
   uint64_t* drain = bars + 8;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 9);
+  uint64_t* q_empty = bars + 9;  // the item's last S done (Q free)
+  uint64_t* o_free = bars + 10;  // O read out (one arrival per softmax warp)
+  // the V loader and each softmax warp have read the item's announcement: an
+  // item's q_full phase may complete before a role that lags (behind an O
+  // read-out) polls it, so the next phase waits for all of them
+  uint64_t* q_seen = bars + 11;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 12);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  // item index of this CTA's i-th item at slot i % 4 (-1: no more items),
+  // written before the arrival that completes that item's q_full phase
+  volatile int* item_ring = reinterpret_cast<volatile int*>(tmem_holder + 2);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  // (batch, head)-major order: the CTAs running together share one head's K/V
-  // in L2; within a head the heaviest query tiles go first
-  const int bh = (int)(blockIdx.x / p.nq), b = bh / p.H, h = bh % p.H;
-  const int qt = p.nq - 1 - (int)(blockIdx.x % p.nq);
-  const int nkv = qt + 1;
   const int d = p.H * 128;
-  const int row0 = b * p.T + qt * TILE;
+  const int nitems = p.B * p.H * p.nq;
 
   if (threadIdx.x == 0) {
     tc::mbar_init(q_full, 1);
@@ -183,6 +205,9 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
     tc::mbar_init(p_full, FWD_SOFT / 32);  // one arrival per softmax warp
     tc::mbar_init(o_full, 1);
     tc::mbar_init(drain, 1);
+    tc::mbar_init(q_empty, 1);
+    tc::mbar_init(o_free, FWD_SOFT / 32);
+    tc::mbar_init(q_seen, 1 + FWD_SOFT / 32);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -197,60 +222,111 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
   bool failed = false;
   if (warp < 4) {
     tc::setmaxnreg_dec<FWD_REG_LOW>();
-    if ((warp == 0 || warp == 2) && lane == 0) {
-      const bool kside = warp == 0;
-      uint64_t* full = kside ? k_full : v_full;
-      uint64_t* empty = kside ? k_empty : v_empty;
-      uint8_t* buf = kside ? sK : sV;
-      const int col = (kside ? d : 2 * d) + h * 128;
+    if (warp == 0 && lane == 0) {
+      // ---- items, Q and K
       tc::prefetch_tmap(&tqkv);
-      if (kside) {
+      int jg = 0;                 // key tiles issued over all items
+      int q_last = -1;            // last item whose Q load was issued
+      for (int i = 0;; ++i) {
+        int v = atomicAdd(p.sched, 1);
+        if (v >= nitems) v = -1;
+        // Q is free once the previous item's last S product is done, and the
+        // next announcement waits until every role has read the previous one
+        if (i > 0 && !tc::mbar_wait(q_empty, (i - 1) & 1, abort_flag, wait_ns)) { failed = true; break; }
+        if (i > 0 && !tc::mbar_wait(q_seen, (i - 1) & 1, abort_flag, wait_ns)) { failed = true; break; }
+        item_ring[i & 3] = v;
+        if (v < 0) {
+          tc::mbar_arrive(q_full);  // the end marker, on the phase every role waits on next
+          break;
+        }
+        const FwdItem it = fwd_item(p, v);
         tc::mbar_arrive_expect_tx(q_full, TILE_BYTES);
-        tc::tma_load_2d(sQ, &tqkv, h * 128, row0, q_full);
-        tc::tma_load_2d(sQ + HALF_BYTES, &tqkv, h * 128 + 64, row0, q_full);
-      }
-      int last = -1;
-      for (int j = 0; j < nkv; ++j) {
-        if (!tc::mbar_wait(empty, (j & 1) ^ 1, abort_flag, wait_ns)) { failed = true; break; }
-        const int kr = b * p.T + j * TILE;
-        tc::mbar_arrive_expect_tx(full, TILE_BYTES);
-        tc::tma_load_2d(buf, &tqkv, col, kr, full);
-        tc::tma_load_2d(buf + HALF_BYTES, &tqkv, col + 64, kr, full);
-        last = j;
+        tc::tma_load_2d(sQ, &tqkv, it.h * 128, it.row0, q_full);
+        tc::tma_load_2d(sQ + HALF_BYTES, &tqkv, it.h * 128 + 64, it.row0, q_full);
+        q_last = i;
+        for (int j = 0; j <= it.qt; ++j, ++jg) {
+          if (!tc::mbar_wait(k_empty, (jg & 1) ^ 1, abort_flag, wait_ns)) { failed = true; break; }
+          const int kr = it.b * p.T + j * TILE;
+          tc::mbar_arrive_expect_tx(k_full, TILE_BYTES);
+          tc::tma_load_2d(sK, &tqkv, d + it.h * 128, kr, k_full);
+          tc::tma_load_2d(sK + HALF_BYTES, &tqkv, d + it.h * 128 + 64, kr, k_full);
+        }
+        if (failed) break;
       }
       if (failed) {
         *abort_flag = 1;
-        if (kside) tc::mbar_wait(q_full, 0, nullptr, kWaitNs);
-        if (last >= 0) tc::mbar_wait(full, last & 1, nullptr, kWaitNs);
+        // the copies this thread started land before the CTA exits (one Q and
+        // one K buffer: only the last of each can be in flight)
+        if (q_last >= 0) tc::mbar_wait(q_full, q_last & 1, nullptr, kWaitNs);
+        if (jg > 0) tc::mbar_wait(k_full, (jg - 1) & 1, nullptr, kWaitNs);
+      }
+    } else if (warp == 2 && lane == 0) {
+      // ---- V
+      int jg = 0;
+      for (int i = 0;; ++i) {
+        if (!tc::mbar_wait(q_full, i & 1, abort_flag, wait_ns)) { failed = true; break; }
+        const int v = item_ring[i & 3];
+        if (v < 0) break;
+        tc::mbar_arrive(q_seen);
+        const FwdItem it = fwd_item(p, v);
+        for (int j = 0; j <= it.qt; ++j, ++jg) {
+          if (!tc::mbar_wait(v_empty, (jg & 1) ^ 1, abort_flag, wait_ns)) { failed = true; break; }
+          const int kr = it.b * p.T + j * TILE;
+          tc::mbar_arrive_expect_tx(v_full, TILE_BYTES);
+          tc::tma_load_2d(sV, &tqkv, 2 * d + it.h * 128, kr, v_full);
+          tc::tma_load_2d(sV + HALF_BYTES, &tqkv, 2 * d + it.h * 128 + 64, kr, v_full);
+        }
+        if (failed) break;
+      }
+      if (failed) {
+        *abort_flag = 1;
+        if (jg > 0) tc::mbar_wait(v_full, (jg - 1) & 1, nullptr, kWaitNs);
       }
     } else if (warp == 1 && lane == 0) {
+      // ---- MMA issuer
       const uint32_t idesc = tc::idesc_bf16(128, 128, 0, 0);
       const uint32_t idesc_pv = tc::idesc_bf16(128, 128, 0, 1);
       bool any = false;
-      if (!tc::mbar_wait(q_full, 0, abort_flag, wait_ns)) failed = true;
-      for (int j = 0; j <= nkv && !failed; ++j) {
-        if (j > 0) {  // O += P(j-1) V(j-1), P read from the first 64 columns of S
-          const int i = j - 1;
-          if (!tc::mbar_wait(v_full, i & 1, abort_flag, wait_ns)) { failed = true; break; }
-          if (!tc::mbar_wait(p_full, i & 1, abort_flag, wait_ns)) { failed = true; break; }
-          tc::tc_fence_after();
-          const uint32_t aV = tc::smem_u32(sV);
+      int jg = 0;  // key tiles over all items (the s_full / p_full / K / V phases)
+      for (int i = 0;; ++i) {
+        if (!tc::mbar_wait(q_full, i & 1, abort_flag, wait_ns)) { failed = true; break; }
+        const int v = item_ring[i & 3];
+        if (v < 0) break;
+        const int nkv = fwd_item(p, v).qt + 1;
+        const int j0 = jg;  // global index of this item's first key tile
+        for (int j = 0; j <= nkv && !failed; ++j) {
+          if (j > 0) {  // O += P(j-1) V(j-1), P read from the first 64 columns of S
+            const int gi = j0 + j - 1;
+            if (!tc::mbar_wait(v_full, gi & 1, abort_flag, wait_ns)) { failed = true; break; }
+            if (!tc::mbar_wait(p_full, gi & 1, abort_flag, wait_ns)) { failed = true; break; }
+            // the item's first PV overwrites O: the previous item's O must be read out
+            if (j == 1 && i > 0 && !tc::mbar_wait(o_free, (i - 1) & 1, abort_flag, wait_ns)) {
+              failed = true;
+              break;
+            }
+            tc::tc_fence_after();
+            const uint32_t aV = tc::smem_u32(sV);
 #pragma unroll
-          for (int k = 0; k < TILE / 16; ++k)
-            tc::mma_bf16_tmem_a(tmem + 128, tmem + k * 8, desc_mn(aV, k), idesc_pv, (i > 0 || k > 0) ? 1u : 0u);
-          any = true;
-          tc::mma_commit(v_empty);
+            for (int k = 0; k < TILE / 16; ++k)
+              tc::mma_bf16_tmem_a(tmem + 128, tmem + k * 8, desc_mn(aV, k), idesc_pv, (j > 1 || k > 0) ? 1u : 0u);
+            any = true;
+            tc::mma_commit(v_empty);
+          }
+          if (j < nkv) {
+            const int gi = j0 + j;
+            if (!tc::mbar_wait(k_full, gi & 1, abort_flag, wait_ns)) { failed = true; break; }
+            tc::tc_fence_after();
+            mma_tile(tmem, tc::smem_u32(sQ), false, tc::smem_u32(sK), false, idesc, false);
+            any = true;
+            tc::mma_commit(s_full);
+            tc::mma_commit(k_empty);
+            if (j == nkv - 1) tc::mma_commit(q_empty);  // Q no longer read
+          }
         }
-        if (j < nkv) {
-          if (!tc::mbar_wait(k_full, j & 1, abort_flag, wait_ns)) { failed = true; break; }
-          tc::tc_fence_after();
-          mma_tile(tmem, tc::smem_u32(sQ), false, tc::smem_u32(sK), false, idesc, false);
-          any = true;
-          tc::mma_commit(s_full);
-          tc::mma_commit(k_empty);
-        }
+        if (failed) break;
+        jg = j0 + nkv;
+        tc::mma_commit(o_full);
       }
-      if (!failed) tc::mma_commit(o_full);
       if (failed) {
         *abort_flag = 1;
         if (any) {
@@ -266,71 +342,82 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t tS = tmem + lane_off, tO = tmem + 128 + lane_off;
     const float sl2 = kLog2e * rsqrtf(128.f);
-    float m = -INFINITY, l = 0.f;
-    for (int j = 0; j <= qt; ++j) {
-      bool ok = tc::mbar_wait(s_full, j & 1, abort_flag, wait_ns);
-      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-      tc::tc_fence_after();
-      float v[128];
-      tc::tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, v, v + 32, v + 64, v + 96);
-      if (j == qt) {
-#pragma unroll
-        for (int i = 0; i < 128; ++i)
-          if (i > r) v[i] = -INFINITY;
+    int jg = 0;
+    for (int i = 0;; ++i) {
+      {
+        const bool ok = tc::mbar_wait(q_full, i & 1, abort_flag, wait_ns);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       }
-      // row maximum: four chains of three-input maxima
-      float mx4[4] = {v[0], v[1], v[2], v[3]};
+      const int v = item_ring[i & 3];
+      if (v < 0) break;
+      tc::mbar_arrive_warp(q_seen);
+      const FwdItem it = fwd_item(p, v);
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j <= it.qt; ++j, ++jg) {
+        bool ok = tc::mbar_wait(s_full, jg & 1, abort_flag, wait_ns);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+        tc::tc_fence_after();
+        float v128[128];
+        tc::tmem_ld32x4(tS, tS + 32, tS + 64, tS + 96, v128, v128 + 32, v128 + 64, v128 + 96);
+        if (j == it.qt) {
 #pragma unroll
-      for (int i = 4; i < 128; i += 8) {
-        mx4[0] = tc::fmax3(mx4[0], v[i], v[i + 4]);
-        mx4[1] = tc::fmax3(mx4[1], v[i + 1], v[i + 5]);
-        mx4[2] = tc::fmax3(mx4[2], v[i + 2], v[i + 6]);
-        mx4[3] = tc::fmax3(mx4[3], v[i + 3], v[i + 7]);
-      }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
-      const bool grow = mx > m + kRescaleLog2;
-      if (__any_sync(0xffffffffu, grow)) {
-        const float m_new = grow ? mx : m;
-        const float alpha = exp2f(m - m_new);
-        l *= alpha;
-        m = m_new;
-        if (j > 0) {
+          for (int c = 0; c < 128; ++c)
+            if (c > r) v128[c] = -INFINITY;
+        }
+        // row maximum: four chains of three-input maxima
+        float mx4[4] = {v128[0], v128[1], v128[2], v128[3]};
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tc::tmem_ld32(tO + c * 32, o);
+        for (int c = 4; c < 128; c += 8) {
+          mx4[0] = tc::fmax3(mx4[0], v128[c], v128[c + 4]);
+          mx4[1] = tc::fmax3(mx4[1], v128[c + 1], v128[c + 5]);
+          mx4[2] = tc::fmax3(mx4[2], v128[c + 2], v128[c + 6]);
+          mx4[3] = tc::fmax3(mx4[3], v128[c + 3], v128[c + 7]);
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+        const bool grow = mx > m + kRescaleLog2;
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? mx : m;
+          const float alpha = exp2f(m - m_new);
+          l *= alpha;
+          m = m_new;
+          if (j > 0) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] *= alpha;
-            tc::tmem_st32(tO + c * 32, o);
+            for (int c = 0; c < 4; ++c) {
+              float o[32];
+              tc::tmem_ld32(tO + c * 32, o);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] *= alpha;
+              tc::tmem_st32(tO + c * 32, o);
+            }
           }
         }
-      }
-      // P = exp2(S * log2(e)/sqrt(128) - m) on fp32 pairs; the row sum in
-      // two paired accumulators
-      const uint64_t sl2x2 = tc::f2pack(sl2, sl2), nm2 = tc::f2pack(-m, -m);
-      uint64_t rs2[2] = {tc::f2pack(0.f, 0.f), tc::f2pack(0.f, 0.f)};
-      uint32_t pk[64];
+        // P = exp2(S * log2(e)/sqrt(128) - m) on fp32 pairs; the row sum in
+        // two paired accumulators
+        const uint64_t sl2x2 = tc::f2pack(sl2, sl2), nm2 = tc::f2pack(-m, -m);
+        uint64_t rs2[2] = {tc::f2pack(0.f, 0.f), tc::f2pack(0.f, 0.f)};
+        uint32_t pk[64];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float2 x = tc::f2unpack(tc::ffma2(tc::f2pack(v[2 * i], v[2 * i + 1]), sl2x2, nm2));
-        const float e0 = tc::ex2(x.x), e1 = tc::ex2(x.y);
-        rs2[i & 1] = tc::fadd2(rs2[i & 1], tc::f2pack(e0, e1));
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
-        pk[i] = *reinterpret_cast<uint32_t*>(&h2);
+        for (int c = 0; c < 64; ++c) {
+          const float2 x = tc::f2unpack(tc::ffma2(tc::f2pack(v128[2 * c], v128[2 * c + 1]), sl2x2, nm2));
+          const float e0 = tc::ex2(x.x), e1 = tc::ex2(x.y);
+          rs2[c & 1] = tc::fadd2(rs2[c & 1], tc::f2pack(e0, e1));
+          __nv_bfloat162 h2 = __floats2bfloat162_rn(e0, e1);
+          pk[c] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        const float2 ra = tc::f2unpack(rs2[0]), rb = tc::f2unpack(rs2[1]);
+        l += (ra.x + ra.y) + (rb.x + rb.y);
+        tc::tmem_st32(tS, reinterpret_cast<const float*>(pk));
+        tc::tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
+        tc::tc_fence_before();
+        tc::mbar_arrive_warp(p_full);
       }
-      const float2 ra = tc::f2unpack(rs2[0]), rb = tc::f2unpack(rs2[1]);
-      l += (ra.x + ra.y) + (rb.x + rb.y);
-      tc::tmem_st32(tS, reinterpret_cast<const float*>(pk));
-      tc::tmem_st32(tS + 32, reinterpret_cast<const float*>(pk + 32));
-      tc::tc_fence_before();
-      tc::mbar_arrive_warp(p_full);
-    }
-    bool ok = !failed;
-    if (ok) ok = tc::mbar_wait(o_full, 0, abort_flag, wait_ns);
-    if (__all_sync(0xffffffffu, ok)) {
+      if (failed) break;
+      // ---- O of this item: normalise and store; then O may take the next item's products
+      bool ok = tc::mbar_wait(o_full, i & 1, abort_flag, wait_ns);
+      if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       tc::tc_fence_after();
       const float inv = 1.f / l;
-      bf16* orow = p.o + (size_t)(row0 + r) * d + h * 128;
+      bf16* orow = p.o + (size_t)(it.row0 + r) * d + it.h * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float o[32];
@@ -339,15 +426,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
         for (int g = 0; g < 4; ++g) {
           float w8[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) w8[i] = o[g * 8 + i] * inv;
+          for (int e = 0; e < 8; ++e) w8[e] = o[g * 8 + e] * inv;
           *reinterpret_cast<uint4*>(orow + c * 32 + g * 8) = pack8(w8);
         }
       }
-      p.lse[((size_t)b * p.H + h) * p.T + qt * TILE + r] = (m + log2f(l)) * kLn2;
-    } else {
-      failed = true;
-      *abort_flag = 1;
+      p.lse[((size_t)it.b * p.H + it.h) * p.T + it.qt * TILE + r] = (m + log2f(l)) * kLn2;
+      tc::tc_fence_before();
+      tc::mbar_arrive_warp(o_free);
     }
+    if (failed) *abort_flag = 1;
   }
 
   if (failed) set_status(p.status, DEV_TIMEOUT);
@@ -925,9 +1012,22 @@ cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int 
   AttnParams p{};
   p.B = B; p.T = T; p.H = H; p.nq = T / TILE;
   p.o = o; p.lse = lse; p.status = status;
+  // persistent: two CTAs per SM (at most one per item), items drawn from a
+  // counter (the third device word) that starts at zero
+  p.sched = status + 2;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_k, cudaFuncAttributeMaxDynamicSharedMemorySize, FWD_SMEM);
   if (e != cudaSuccess) return e;
-  attn_fwd_tc_k<<<B * H * p.nq, FWD_THREADS, FWD_SMEM, s>>>(tq, p);
+  e = cudaMemsetAsync(p.sched, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  const int items = B * H * p.nq;
+  attn_fwd_tc_k<<<items < 2 * sms ? items : 2 * sms, FWD_THREADS, FWD_SMEM, s>>>(tq, p);
   return cudaGetLastError();
 }
 

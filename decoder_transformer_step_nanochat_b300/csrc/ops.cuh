@@ -119,6 +119,8 @@ cudaError_t attn_tc_set_wait_limit(uint64_t ns);
 
 // tcgen05 flash attention (bf16, T % 128 == 0).
 bool attn_tc_supports(int T);
+// status points at three device words: the status word, the backward's work
+// counter and the forward's (reset here before the launch).
 cudaError_t attn_fwd_tc(const bf16* qkv, bf16* o, float* lse, int B, int T, int H, int* status, cudaStream_t s);
 // dq (zeroed here, then accumulated) is fp32 [B*T, d]; dv goes to dqkv's v columns. Without rqk,
 // dk_hat goes to the fp32 plane dk; with rqk (+ the RoPE table) the k half of the QK-norm + RoPE

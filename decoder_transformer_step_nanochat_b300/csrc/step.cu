@@ -846,7 +846,7 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   // the decode table is rebuilt on the (possibly different) device by the next prefill
   if (c->dec_rope) { cudaFree(c->dec_rope); c->dec_rope = nullptr; }
   c->dec_rope_len = 0;
-  // device words: [0] status, [1] work-unit counter of the persistent attention backward.
+  // device words: [0] status, [1] and [2] work counters of the persistent attention backward and forward.
   // A context configured again on another device gets them anew there, like the tables above.
   if (c->status && c->device >= 0 && c->device != dev) {
     cudaFree(c->status);
