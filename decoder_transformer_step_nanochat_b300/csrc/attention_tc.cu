@@ -486,6 +486,15 @@ __global__ void __launch_bounds__(FWD_THREADS, 2)
 // done and its first query tile runs while the epilogue warps drain dV/dK;
 // only its first dV/dK products wait for that drain.
 
+// Warm L2 with a tile the kernel will load later (no shared memory written,
+// nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 constexpr int BWD_WARPS = 10;
 constexpr int BWD_THREADS = 32 * BWD_WARPS;
 constexpr int BWD_SOFT = 32 * (BWD_WARPS - 2);  // 256 softmax threads
@@ -533,7 +542,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* acc_free = bars + 15;
   uint64_t* drain = bars + 16;
   uint64_t* tile_done = bars + 17;  // every product of the tile complete (its Q/dO stage unread)
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 18);
+  uint64_t* xch = bars + 18;        // both warpgroups' partial dk row dots written (one arrival per warp)
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   // unit index of this CTA's ul-th unit at slot ul % 4 (-1: no more units); it
   // is written before the arrive that completes that unit's kv_full phase
@@ -559,6 +569,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tc::mbar_init(acc_free, BWD_SOFT / 32);
     tc::mbar_init(drain, 1);
     tc::mbar_init(tile_done, 1);
+    tc::mbar_init(xch, BWD_SOFT / 32);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -587,6 +598,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       for (;; ++ul) {
         int v = atomicAdd(p.sched, 1);
         if (v >= nunits) v = -1;
+        if (v >= 0) {
+          // the unit's K and V head for L2 now; their loads follow once the
+          // previous unit's last products have released the buffers
+          const BwdUnit un = bwd_unit(p, v);
+          tma_prefetch_2d(&tqkv, d + un.h * 128, un.krow0);
+          tma_prefetch_2d(&tqkv, d + un.h * 128 + 64, un.krow0);
+          tma_prefetch_2d(&tqkv, 2 * d + un.h * 128, un.krow0);
+          tma_prefetch_2d(&tqkv, 2 * d + un.h * 128 + 64, un.krow0);
+        }
         // K and V of the previous unit are free once its last products finished
         // (and by then every role has read the older ring slots)
         if (ul > 0 && !tc::mbar_wait(kv_empty, (ul - 1) & 1, abort_flag, wait_ns)) { failed = true; break; }
@@ -689,6 +709,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             tc::mma_bf16(tdP, desc_mn(aK, k), desc_mn(adSt, k), id_mnmn, k > 0 ? 1u : 0u);
           }
           tc::mma_commit(dq_full);
+          // the unit's last tile: nothing after dQ^T reads K or V (dV and dK read
+          // P^T, dO, dS^T and Q), so the next unit's K/V may load now
+          if (it + 1 == u.nit) tc::mma_commit(kv_empty);
 #pragma unroll
           for (int k = 4; k < TILE / 16; ++k) {
             tc::mma_bf16_tmem_a(tdV, tS + 64 + (k & 3) * 8, desc_mn(adO, k), id_kmn, 1u);
@@ -698,7 +721,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         if (failed) break;
         tc::mma_commit(acc_full);  // dV, dK of this unit complete
-        tc::mma_commit(kv_empty);  // and K, V no longer read
       }
       if (failed) {
         *abort_flag = 1;
@@ -838,91 +860,86 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const size_t m = (size_t)u.krow0 + r;
       const int h = u.h;
       if (p.rqk) {
-        // warp ch = 0 finishes dk for whole head rows; warp ch = 1 writes dv
-        if (ch == 0) {
-          // dk_hat = acc (dS' carried the score scale). With R the RoPE rotation
-          // of the row's position, k_n = R^T k_hat and dk_n = R^T dk_hat, the
-          // RMSNorm backward dk = rk (dk_n - k_n mean(dk_n k_n)) equals
-          // rk R^T (dk_hat - k_hat mean(dk_hat k_hat)): a rotation keeps dot
-          // products, so the mean needs neither the table nor a rotation, and
-          // one pass over the pairs un-rotates and finishes. k_hat is read
-          // back from qkv once and kept packed.
-          const int t = u.kt * TILE + r;
-          // angle-major tables [16][T][4]: the warp's 32 positions read 512 contiguous bytes
-          const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos) + t;
-          const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin) + t;
-          const bf16* krow = p.qkv + m * 3 * d + d + h * 128;
-          const uint32_t tk = tdK + lane_off;
-          uint4 kr[16];  // k_hat, 8 dims per entry
+        // dk_hat = acc (dS' carried the score scale). With R the RoPE rotation
+        // of the row's position, k_n = R^T k_hat and dk_n = R^T dk_hat, the
+        // RMSNorm backward dk = rk (dk_n - k_n mean(dk_n k_n)) equals
+        // rk R^T (dk_hat - k_hat mean(dk_hat k_hat)): a rotation keeps dot
+        // products, so the mean needs neither the table nor a rotation.
+        // Warpgroup ch finishes the rotation pairs (j, j + 64) with j in
+        // [32 ch, 32 ch + 32) and writes dv dims [64 ch, 64 ch + 64). The two
+        // partial dots of a row meet through one float per row in the idle
+        // dS^T buffer, in the half that the reading thread itself overwrites
+        // next (so no later write can race the read), and are added in
+        // warpgroup order.
+        const int t = u.kt * TILE + r;
+        const int j0 = 32 * ch;
+        const bf16* krow = p.qkv + m * 3 * d + d + h * 128;
+        const uint32_t tk = tdK + lane_off;
+        uint4 klo[4], khi[4];  // k_hat dims j0..j0+31 and 64+j0..64+j0+31
 #pragma unroll
-          for (int q8 = 0; q8 < 16; ++q8) kr[q8] = __ldg(reinterpret_cast<const uint4*>(krow) + q8);
-          float dot = 0.f;
+        for (int q8 = 0; q8 < 4; ++q8) {
+          klo[q8] = __ldg(reinterpret_cast<const uint4*>(krow + j0) + q8);
+          khi[q8] = __ldg(reinterpret_cast<const uint4*>(krow + 64 + j0) + q8);
+        }
+        float glo[32], ghi[32];
+        tc::tmem_ld32x2(tk + j0, tk + 64 + j0, glo, ghi);
+        float part = 0.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // 32 dims at a time
-            float g[32];
-            tc::tmem_ld32(tk + c * 32, g);
+        for (int q8 = 0; q8 < 4; ++q8) {
+          float k1[8], k2[8];
+          unpack8(klo[q8], k1);
+          unpack8(khi[q8], k2);
 #pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              float k8[8];
-              unpack8(kr[c * 4 + q8], k8);
+          for (int i = 0; i < 8; ++i) part += glo[q8 * 8 + i] * k1[i] + ghi[q8 * 8 + i] * k2[i];
+        }
+        float* mine = reinterpret_cast<float*>(sdSt + (1 - ch) * HALF_BYTES + r * 128);
+        const volatile float* other = reinterpret_cast<const volatile float*>(sdSt + ch * HALF_BYTES + r * 128);
+        *mine = part;
+        tc::mbar_arrive_warp(xch);
+        ok = tc::mbar_wait(xch, ul & 1, abort_flag, wait_ns);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+        const float po = *other;
+        const float dot = ch == 0 ? part + po : po + part;
+        const float rk = p.rqk[m * 2 * p.H + p.H + h];
+        const float dmean = dot * (1.f / 128.f);
+        // angle-major tables [16][T][4]: angles j0..j0+31 are groups j0/4..j0/4+7,
+        // and the warp's 32 positions read 512 contiguous bytes per group
+        const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos) + t;
+        const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin) + t;
+        bf16* rowk = p.dqkv + m * 3 * d + d + h * 128;
 #pragma unroll
-              for (int i = 0; i < 8; ++i) dot += g[q8 * 8 + i] * k8[i];
-            }
+        for (int q8 = 0; q8 < 4; ++q8) {  // 8 rotation pairs at a time
+          const float4 ca = __ldg(cs4 + (size_t)(j0 / 4 + 2 * q8) * p.T);
+          const float4 cb = __ldg(cs4 + (size_t)(j0 / 4 + 2 * q8 + 1) * p.T);
+          const float4 sa = __ldg(sn4 + (size_t)(j0 / 4 + 2 * q8) * p.T);
+          const float4 sb = __ldg(sn4 + (size_t)(j0 / 4 + 2 * q8 + 1) * p.T);
+          const float cc[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+          const float ss[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+          float k1[8], k2[8], o1[8], o2[8];
+          unpack8(klo[q8], k1);
+          unpack8(khi[q8], k2);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float w1 = glo[q8 * 8 + i] - k1[i] * dmean, w2 = ghi[q8 * 8 + i] - k2[i] * dmean;
+            o1[i] = rk * (w1 * cc[i] + w2 * ss[i]);
+            o2[i] = rk * (-w1 * ss[i] + w2 * cc[i]);
           }
-          const float rk = p.rqk[m * 2 * p.H + p.H + h];
-          const float dmean = dot * (1.f / 128.f);
-          bf16* row = p.dqkv + m * 3 * d + d + h * 128;
+          *reinterpret_cast<uint4*>(rowk + j0 + q8 * 8) = pack8(o1);
+          *reinterpret_cast<uint4*>(rowk + 64 + j0 + q8 * 8) = pack8(o2);
+        }
+        bf16* rowv = p.dqkv + m * 3 * d + 2 * d + h * 128 + 64 * ch;
+        {
+          float a[32], bb[32];
+          tc::tmem_ld32x2(tdV + lane_off + 64 * ch, tdV + lane_off + 64 * ch + 32, a, bb);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {  // 16 rotation pairs (j, j + 64) at a time
-            // the table first, so its latency overlaps the TMEM load
-            float4 ca[2], cb[2], sa[2], sb[2];
-#pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) {
-              const int q8 = c * 2 + c8;
-              ca[c8] = __ldg(cs4 + (size_t)(2 * q8) * p.T);
-              cb[c8] = __ldg(cs4 + (size_t)(2 * q8 + 1) * p.T);
-              sa[c8] = __ldg(sn4 + (size_t)(2 * q8) * p.T);
-              sb[c8] = __ldg(sn4 + (size_t)(2 * q8 + 1) * p.T);
-            }
-            float g1[16], g2[16];
-            tc::tmem_ld16x2(tk + c * 16, tk + 64 + c * 16, g1, g2);
-#pragma unroll
-            for (int c8 = 0; c8 < 2; ++c8) {
-              float k1[8], k2[8];
-              unpack8(kr[c * 2 + c8], k1);
-              unpack8(kr[8 + c * 2 + c8], k2);
-              const float cc[8] = {ca[c8].x, ca[c8].y, ca[c8].z, ca[c8].w, cb[c8].x, cb[c8].y, cb[c8].z, cb[c8].w};
-              const float ss[8] = {sa[c8].x, sa[c8].y, sa[c8].z, sa[c8].w, sb[c8].x, sb[c8].y, sb[c8].z, sb[c8].w};
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const int e = c8 * 8 + i;
-                const float w1 = g1[e] - k1[i] * dmean, w2 = g2[e] - k2[i] * dmean;
-                g1[e] = rk * (w1 * cc[i] + w2 * ss[i]);
-                g2[e] = rk * (-w1 * ss[i] + w2 * cc[i]);
-              }
-            }
-#pragma unroll
-            for (int gq = 0; gq < 2; ++gq) {
-              *reinterpret_cast<uint4*>(row + c * 16 + gq * 8) = pack8(g1 + 8 * gq);
-              *reinterpret_cast<uint4*>(row + 64 + c * 16 + gq * 8) = pack8(g2 + 8 * gq);
-            }
+          for (int i = 0; i < 32; ++i) {  // dV accumulated P' = P / sqrt(128)
+            a[i] *= kSqrt128;
+            bb[i] *= kSqrt128;
           }
-        } else {
-          bf16* row = p.dqkv + m * 3 * d + 2 * d + h * 128;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            float a[32], bb[32];
-            tc::tmem_ld32x2(tdV + lane_off + c * 64, tdV + lane_off + c * 64 + 32, a, bb);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {  // dV accumulated P' = P / sqrt(128)
-              a[i] *= kSqrt128;
-              bb[i] *= kSqrt128;
-            }
-#pragma unroll
-            for (int gq = 0; gq < 4; ++gq) {
-              *reinterpret_cast<uint4*>(row + c * 64 + gq * 8) = pack8(a + 8 * gq);
-              *reinterpret_cast<uint4*>(row + c * 64 + 32 + gq * 8) = pack8(bb + 8 * gq);
-            }
+          for (int gq = 0; gq < 4; ++gq) {
+            *reinterpret_cast<uint4*>(rowv + gq * 8) = pack8(a + 8 * gq);
+            *reinterpret_cast<uint4*>(rowv + 32 + gq * 8) = pack8(bb + 8 * gq);
           }
         }
       } else {
