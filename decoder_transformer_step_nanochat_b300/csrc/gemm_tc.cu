@@ -73,8 +73,12 @@ struct TcParams {
 // k-blocks [kb0, kb1). Order, for L2 reuse of the operand panels: split-major
 // (the units running together share one k-range), then problem, then groups
 // of kGroupRows row blocks (or row pairs) that sweep every column block
-// together, rows fastest.
-constexpr int kGroupRows = 16;
+// together, rows fastest. With about 74 pairs running at once, 8 rows per
+// group keep the set of tiles in flight near square on the wide products
+// (QKV, MLP up, lm_head), so fewer A and B panels stream at once: measured on
+// the d20 step, GEMM time 74.8 ms with 16 rows, 74.3 with 8, 75.1 with 6 or 10,
+// 75.2 with 32, 78.1 with 64.
+constexpr int kGroupRows = 8;
 
 template <int CL>
 __device__ __forceinline__ void unit_of(const TcParams& p, int v, int rank, int& bt, int& m0, int& nb, int& split,
