@@ -5,11 +5,12 @@
 //
 //   kv_from_qkv      prefill: copy k_hat and v of one layer's stash into the
 //                    cache layout [B][H][max_len][128]
-//   decode_qkv       decode: per-head RMSNorm + RoPE of q and k at the step's
-//                    position; q_hat out, k_hat and v appended to the cache
-//   attn_decode      flash-decoding: each CTA scores one chunk of cached
-//                    positions of one (sequence, head) and leaves a partial
-//                    (max, sum, o); attn_decode_combine merges the chunks
+//   attn_decode      decode, one launch per layer: q_hat and k_hat of the
+//                    step's token (per-head RMSNorm + RoPE at its position)
+//                    from the fp32 qkv row, k_hat and v appended to the cache,
+//                    then flash-decoding: each CTA scores one chunk of cached
+//                    positions of one (sequence, head), and the last CTA of
+//                    the (sequence, head) to finish merges the chunks
 //   relu2_rows       a = max(u, 0)^2 from the fp32 up-projection
 //   gather_last      prefill: the last position's hidden row of each sequence
 //
@@ -62,34 +63,16 @@ __global__ void kv_from_qkv_k(const T* __restrict__ qkv, T* __restrict__ K, T* _
   }
 }
 
-// One warp per (sequence b, head h, kind): kind 0 = q, 1 = k (normed and
-// rotated at position pos), 2 = v. Lane L holds dims 4L..4L+3; the RoPE
-// partner of dim j < 64 is j + 64, held by lane L ^ 16.
-template <typename T>
-__global__ void decode_qkv_k(const float* __restrict__ qkv, T* __restrict__ qh, T* __restrict__ K, T* __restrict__ Vc,
-                             const float* __restrict__ rc, const float* __restrict__ rs, int B, int H, int pos_arg,
-                             const int* __restrict__ d_pos, int max_len, int* status) {
-  const int pos = d_pos ? *d_pos : pos_arg;
-  if (pos < 0 || pos >= max_len) {  // a device position past the cache: report, touch nothing
-    if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, DEV_BAD_TOKEN);
-    return;
-  }
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= B * H * 3) return;
-  const int kind = wid % 3, bh = wid / 3, b = bh / H, h = bh % H;
-  const int d = H * 128;
-  float4 v = ld4e(qkv + (size_t)b * 3 * d + kind * d + h * 128 + lane * 4);
-  const size_t cache_row = (((size_t)b * H + h) * max_len + pos) * 128 + lane * 4;
-  if (kind == 2) {
-    st4e(Vc + cache_row, v);
-    return;
-  }
+// RMSNorm over one head's 128 dims, then the rotation by the angles of
+// position pos (first half x1 c - x2 s, second half x1 s + x2 c), on one warp:
+// lane L holds dims 4L..4L+3 and the partner of dim j < 64, j + 64, sits in
+// lane L ^ 16.
+__device__ __forceinline__ float4 head_norm_rope(float4 v, const float* __restrict__ rc,
+                                                 const float* __restrict__ rs, int pos, int lane) {
   float ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   ss = warp_sum(ss);
   const float r = rsqrtf(ss * (1.f / 128.f) + kEps);
   v.x *= r; v.y *= r; v.z *= r; v.w *= r;
-  // partner values (dims j +- 64)
   float4 w;
   w.x = __shfl_xor_sync(0xffffffffu, v.x, 16);
   w.y = __shfl_xor_sync(0xffffffffu, v.y, 16);
@@ -99,43 +82,81 @@ __global__ void decode_qkv_k(const float* __restrict__ qkv, T* __restrict__ qh, 
   const float4 c = ld4e(rc + (size_t)pos * 64 + j0);
   const float4 s = ld4e(rs + (size_t)pos * 64 + j0);
   float4 o;
-  if (lane < 16) {  // first half: x1 c - x2 s
+  if (lane < 16) {
     o.x = v.x * c.x - w.x * s.x; o.y = v.y * c.y - w.y * s.y;
     o.z = v.z * c.z - w.z * s.z; o.w = v.w * c.w - w.w * s.w;
-  } else {          // second half: x1 s + x2 c (x1 is the partner)
+  } else {  // x1 is the partner
     o.x = w.x * s.x + v.x * c.x; o.y = w.y * s.y + v.y * c.y;
     o.z = w.z * s.z + v.z * c.z; o.w = w.w * s.w + v.w * c.w;
   }
-  if (kind == 0) st4e(qh + (size_t)b * d + h * 128 + lane * 4, o);
-  else st4e(K + cache_row, o);
+  return o;
+}
+
+// the value as the cache element type holds it
+__device__ __forceinline__ float4 as_elem(float4 v, const float*) { return v; }
+__device__ __forceinline__ float4 as_elem(float4 v, const bf16*) {
+  const float2 a = __bfloat1622float2(__floats2bfloat162_rn(v.x, v.y));
+  const float2 b = __bfloat1622float2(__floats2bfloat162_rn(v.z, v.w));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ float4 ld4cg(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+__device__ __forceinline__ float4 ld4cg(const bf16* p) {
+  const uint2 u = __ldcg(reinterpret_cast<const uint2*>(p));
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
 }
 
 constexpr int kDecWarps = 4;
 
-// Partial attention of one chunk of cached positions [c*chunk, min(...,
-// pos + 1)) for one (b, h): each warp walks a quarter of the chunk, four
-// positions at a time, keeping an online softmax in the log2 domain; the
-// warps then merge through shared memory. Partial = (m, l, -, -, o[128]).
+// Attention of the step's token for one (sequence b, head h) over one chunk
+// of cached positions [c*chunk, min(c*chunk + chunk, pos + 1)), from the fp32
+// qkv row of the token:
+//  - every warp forms q_hat = RoPE(RMSNorm(q)) of the head (rounded to the
+//    cache element type, as the prefill's attention reads it);
+//  - the CTA of the chunk holding pos first appends k_hat and v of the token
+//    to the cache at pos (warps 0 and 1), so it reads them back like any
+//    other position;
+//  - each warp walks a quarter of the chunk, four positions at a time, with
+//    an online softmax in the log2 domain; the warps merge through shared
+//    memory into the chunk's (max, sum, o[128]);
+//  - with one chunk the CTA writes o; otherwise it leaves its partial in part
+//    and the CTA that counts itself last for this (b, h) on cnt[b H + h]
+//    merges the chunks in chunk order (so the result does not depend on
+//    scheduling), writes o and sets the counter back to 0.
+// A position outside [0, max_len) sets DEV_BAD_TOKEN and touches nothing.
+// The cache is read through L2 only (ld.global.cg): this launch writes it.
 template <typename T>
 __global__ void __launch_bounds__(32 * kDecWarps)
-    attn_decode_k(const T* __restrict__ qh, const T* __restrict__ K, const T* __restrict__ Vc,
-                  float* __restrict__ part, int H, int pos_arg, const int* __restrict__ d_pos, int max_len, int chunk,
-                  int nchunks) {
+    attn_decode_k(const float* __restrict__ qkv, const float* __restrict__ rc, const float* __restrict__ rs, T* K,
+                  T* Vc, float* part, int* cnt, T* __restrict__ out, int H, int pos_arg, const int* __restrict__ d_pos,
+                  int max_len, int chunk, int nchunks, int* status) {
   __shared__ float sm_m[kDecWarps], sm_l[kDecWarps];
   __shared__ float sm_o[kDecWarps][128];
+  __shared__ int is_last;
   const int bh = blockIdx.x, c = blockIdx.y;
   const int pos = d_pos ? *d_pos : pos_arg;
-  if (pos < 0 || pos >= max_len) return;  // reported by decode_qkv
+  if (pos < 0 || pos >= max_len) {
+    if (bh == 0 && c == 0 && threadIdx.x == 0) set_status(status, DEV_BAD_TOKEN);
+    return;
+  }
   if (c * chunk > pos) return;  // a fixed grid (device position): chunks past pos are unused
+  const int n_act = pos / chunk + 1;
   const int b = bh / H, h = bh % H;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int d = H * 128;
-  const int t0 = c * chunk, t1 = min(t0 + chunk, pos + 1);
+  const float* qrow = qkv + (size_t)b * 3 * d + h * 128 + lane * 4;
+  T* Kb = K + ((size_t)b * H + h) * max_len * 128 + lane * 4;
+  T* Vb = Vc + ((size_t)b * H + h) * max_len * 128 + lane * 4;
+  if (c == n_act - 1) {  // this chunk holds pos: append the token's k_hat and v
+    if (warp == 0) st4e(Kb + (size_t)pos * 128, head_norm_rope(ld4e(qrow + d), rc, rs, pos, lane));
+    else if (warp == 1) st4e(Vb + (size_t)pos * 128, ld4e(qrow + 2 * d));
+    __syncthreads();
+  }
   const float sc = kLog2eD * rsqrtf(128.f);
-  float4 q = ld4e(qh + (size_t)b * d + h * 128 + lane * 4);
+  float4 q = as_elem(head_norm_rope(ld4e(qrow), rc, rs, pos, lane), static_cast<const T*>(nullptr));
   q.x *= sc; q.y *= sc; q.z *= sc; q.w *= sc;
-  const T* Kb = K + ((size_t)b * H + h) * max_len * 128 + lane * 4;
-  const T* Vb = Vc + ((size_t)b * H + h) * max_len * 128 + lane * 4;
+  const int t0 = c * chunk, t1 = min(t0 + chunk, pos + 1);
   float m = -INFINITY, l = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   // this warp's positions: t0 + warp*4 + 16*i + u, u in 0..3
@@ -146,8 +167,8 @@ __global__ void __launch_bounds__(32 * kDecWarps)
     for (int u = 0; u < 4; ++u) {
       const int t = tb + u;
       if (t < t1) {
-        const float4 k = ld4e(Kb + (size_t)t * 128);
-        v4[u] = ld4e(Vb + (size_t)t * 128);
+        const float4 k = ld4cg(Kb + (size_t)t * 128);
+        v4[u] = ld4cg(Vb + (size_t)t * 128);
         s4[u] = q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w;
       } else {
         v4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -184,6 +205,7 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   sm_o[warp][lane * 4 + 2] = o.z;
   sm_o[warp][lane * 4 + 3] = o.w;
   __syncthreads();
+  T* orow = out + (size_t)b * d + h * 128 + lane * 4;
   if (warp == 0) {
     float M = -INFINITY;
 #pragma unroll
@@ -199,41 +221,40 @@ __global__ void __launch_bounds__(32 * kDecWarps)
       O.z += f * sm_o[w][lane * 4 + 2];
       O.w += f * sm_o[w][lane * 4 + 3];
     }
-    float* pp = part + ((size_t)bh * nchunks + c) * kPart;
-    if (lane == 0) {
-      pp[0] = M;
-      pp[1] = L;
+    if (n_act == 1) {
+      const float inv = 1.f / L;
+      st4e(orow, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
+    } else {
+      float* pp = part + ((size_t)bh * nchunks + c) * kPart;
+      if (lane == 0) {
+        pp[0] = M;
+        pp[1] = L;
+      }
+      st4e(pp + 4 + lane * 4, O);
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) is_last = atomicAdd(cnt + bh, 1) == n_act - 1;
+      __syncwarp();
+      if (is_last) {  // every chunk's partial is in part: merge them in chunk order
+        __threadfence();
+        const float* pb = part + (size_t)bh * nchunks * kPart;
+        float Mx = -INFINITY;
+        for (int k = 0; k < n_act; ++k) Mx = fmaxf(Mx, __ldcg(pb + (size_t)k * kPart));
+        float Lt = 0.f;
+        float4 Ot = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < n_act; ++k) {
+          const float mk = __ldcg(pb + (size_t)k * kPart);
+          const float f = mk == -INFINITY ? 0.f : exp2f(mk - Mx);
+          Lt += f * __ldcg(pb + (size_t)k * kPart + 1);
+          const float4 ok = ld4cg(pb + (size_t)k * kPart + 4 + lane * 4);
+          Ot.x += f * ok.x; Ot.y += f * ok.y; Ot.z += f * ok.z; Ot.w += f * ok.w;
+        }
+        const float inv = 1.f / Lt;
+        st4e(orow, make_float4(Ot.x * inv, Ot.y * inv, Ot.z * inv, Ot.w * inv));
+        if (lane == 0) cnt[bh] = 0;
+      }
     }
-    st4e(pp + 4 + lane * 4, O);
   }
-}
-
-// One warp per (b, h): merge the chunk partials into o = sum_c w_c O_c / sum_c w_c L_c.
-template <typename T>
-__global__ void attn_decode_combine_k(const float* __restrict__ part, T* __restrict__ out, int BH, int H,
-                                      int nchunks_grid, const int* __restrict__ d_pos, int chunk) {
-  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (wid >= BH) return;
-  // partials are laid out with the grid's chunk count; only the chunks up to pos hold data
-  const int pd = d_pos ? *d_pos : 0;
-  const int nchunks = d_pos ? min(nchunks_grid, (max(pd, 0) + chunk) / chunk) : nchunks_grid;
-  const int stride = nchunks_grid;
-  const float* pp = part + (size_t)wid * stride * kPart;
-  float M = -INFINITY;
-  for (int c = 0; c < nchunks; ++c) M = fmaxf(M, pp[(size_t)c * kPart]);
-  float L = 0.f;
-  float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int c = 0; c < nchunks; ++c) {
-    const float mc = pp[(size_t)c * kPart];
-    const float f = mc == -INFINITY ? 0.f : exp2f(mc - M);
-    L += f * pp[(size_t)c * kPart + 1];
-    const float4 oc = ld4e(pp + (size_t)c * kPart + 4 + lane * 4);
-    O.x += f * oc.x; O.y += f * oc.y; O.z += f * oc.z; O.w += f * oc.w;
-  }
-  const float inv = 1.f / L;
-  const int b = wid / H, h = wid % H;
-  st4e(out + (size_t)b * H * 128 + h * 128 + lane * 4, make_float4(O.x * inv, O.y * inv, O.z * inv, O.w * inv));
 }
 
 template <typename T>
@@ -271,24 +292,13 @@ cudaError_t kv_from_qkv(const T* qkv, T* K, T* Vc, int B, int Tn, int H, int max
 }
 
 template <typename T>
-cudaError_t decode_qkv(const float* qkv, T* qh, T* K, T* Vc, const float* rc, const float* rs, int B, int H, int pos,
-                       const int* d_pos, int max_len, int* status, cudaStream_t s) {
-  const int warps = B * H * 3;
-  decode_qkv_k<T><<<(warps + 7) / 8, 256, 0, s>>>(qkv, qh, K, Vc, rc, rs, B, H, pos, d_pos, max_len, status);
-  return cudaGetLastError();
-}
-
-template <typename T>
-cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos,
-                        const int* d_pos, int max_len, int chunk, cudaStream_t s) {
+cudaError_t attn_decode(const float* qkv, const float* rc, const float* rs, T* K, T* Vc, float* part, int* cnt, T* out,
+                        int B, int H, int pos, const int* d_pos, int max_len, int chunk, int* status, cudaStream_t s) {
   // with a device position the grid covers max_len (a graph replays it at any position)
   const int span = d_pos ? max_len : pos + 1;
   const int nchunks = (span + chunk - 1) / chunk;
-  attn_decode_k<T><<<dim3(B * H, nchunks), 32 * kDecWarps, 0, s>>>(qh, K, Vc, part, H, pos, d_pos, max_len, chunk,
-                                                                   nchunks);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  attn_decode_combine_k<T><<<(B * H + 7) / 8, 256, 0, s>>>(part, out, B * H, H, nchunks, d_pos, chunk);
+  attn_decode_k<T><<<dim3(B * H, nchunks), 32 * kDecWarps, 0, s>>>(qkv, rc, rs, K, Vc, part, cnt, out, H, pos, d_pos,
+                                                                   max_len, chunk, nchunks, status);
   return cudaGetLastError();
 }
 
@@ -315,10 +325,8 @@ cudaError_t gather_last(const T* hf, T* out, int B, int Tn, int d, cudaStream_t 
 
 #define NC_DEC_INST(T)                                                                                         \
   template cudaError_t kv_from_qkv<T>(const T*, T*, T*, int, int, int, int, cudaStream_t);                   \
-  template cudaError_t decode_qkv<T>(const float*, T*, T*, T*, const float*, const float*, int, int, int,     \
-                                     const int*, int, int*, cudaStream_t);                                   \
-  template cudaError_t attn_decode<T>(const T*, const T*, const T*, float*, T*, int, int, int, const int*, int, \
-                                      int, cudaStream_t);                                                    \
+  template cudaError_t attn_decode<T>(const float*, const float*, const float*, T*, T*, float*, int*, T*, int, \
+                                      int, int, const int*, int, int, int*, cudaStream_t);                     \
   template cudaError_t relu2_rows<T>(const float*, T*, long long, cudaStream_t);                               \
   template cudaError_t gather_last<T>(const T*, T*, int, int, int, cudaStream_t);
 NC_DEC_INST(float)

@@ -72,10 +72,12 @@ bool gemm_tc_supports(const GemmArgs& g);
 // Weight-streaming product of the decode step: C (fp32) = alpha * A W^T (+ beta * C)
 // for M <= 16 rows of A (bf16 [M, K], K-major) and W (bf16 [N, K], K-major),
 // K a multiple of 32, 16-byte aligned operands; one launch, deterministic.
-// sms: the device's SM count (sizes the column groups).
+// sms: the device's SM count (sizes the column groups). With relu2 given,
+// the product u = alpha * A W^T leaves as relu2[m, n] = bf16(max(u, 0)^2)
+// (row stride ldc) and C is not touched.
 bool skinny_gemm_supports(int M, int N, int K, long long lda, long long ldw, const void* A, const void* W);
 cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
-                        int N, int K, float alpha, float beta, int sms, cudaStream_t s);
+                        int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2 = nullptr);
 
 // ------------------------------------------------------------------ rows
 template <typename T>
@@ -142,8 +144,12 @@ cudaError_t scale_scalar(const float* in, float scale, float* out, cudaStream_t 
 cudaError_t unpack_u16(const uint16_t* packed, int B, int T_, int32_t* tok, int32_t* tgt, cudaStream_t s);
 
 // ------------------------------------------------------------------ loss
-cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,
-                                int* amax, int M, int V, int* status, cudaStream_t s);
+// part (16 bytes x kCeMaxSegments per row) and counter (a device int at 0)
+// may be null; given, rows are split over more CTAs when there are few of them
+constexpr int kCeMaxSegments = 512;
+cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll, int* amax, int M, int V,
+                                int* status, cudaStream_t s, float* part = nullptr, int* counter = nullptr,
+                                int sms = 148);
 // rows whose target is negative (masked) get nll 0
 cudaError_t ce_reduce_partials(const float* p_max, const float* p_sum, const int* p_arg,
                                const float* p_tgt, const int* tgt, int n_tiles, float* lse, float* nll,
@@ -158,19 +164,18 @@ cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStr
 // cache layout per layer: K and V each [B][H][max_len][128] (elem)
 template <typename T>
 cudaError_t kv_from_qkv(const T* qkv, T* K, T* Vc, int B, int Tn, int H, int max_len, cudaStream_t s);
-// qkv fp32 [B, 3d] of the step's token -> q_hat elem [B, d]; k_hat, v into the cache at pos
-// the position is pos, or *d_pos when d_pos is not null (graph-replayable
-// launches); a position outside [0, max_len) sets DEV_BAD_TOKEN and writes nothing
-template <typename T>
-cudaError_t decode_qkv(const float* qkv, T* qh, T* K, T* Vc, const float* rc, const float* rs, int B, int H, int pos,
-                       const int* d_pos, int max_len, int* status, cudaStream_t s);
-// o elem [B, d] = attention of q_hat over cached positions 0..pos; part holds
-// B*H*ceil((pos+1)/chunk) partials of 132 floats
+// Decode attention of one layer: from qkv fp32 [B, 3d] of the step's token,
+// k_hat and v go into the cache at pos and o elem [B, d] = attention of q_hat
+// over cached positions 0..pos. The position is pos, or *d_pos when d_pos is
+// not null (graph-replayable launches); one outside [0, max_len) sets
+// DEV_BAD_TOKEN and writes nothing. part holds B*H*ceil(span/chunk) partials
+// of 132 floats (span = max_len with d_pos, else pos + 1); cnt holds B*H ints
+// that must be 0 before the first call (each call leaves them at 0).
 constexpr int kDecodeChunk = 256;
 constexpr int kDecodePartFloats = 132;
 template <typename T>
-cudaError_t attn_decode(const T* qh, const T* K, const T* Vc, float* part, T* out, int B, int H, int pos,
-                        const int* d_pos, int max_len, int chunk, cudaStream_t s);
+cudaError_t attn_decode(const float* qkv, const float* rc, const float* rs, T* K, T* Vc, float* part, int* cnt, T* out,
+                        int B, int H, int pos, const int* d_pos, int max_len, int chunk, int* status, cudaStream_t s);
 // *d_pos += 1 (one thread)
 cudaError_t advance_pos(int* d_pos, cudaStream_t s);
 template <typename T>

@@ -293,69 +293,6 @@ __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ 
   }
 }
 
-// One CTA per row of a materialised fp32 logits block: logsumexp, loss
-// lse - logit[target], argmax (lowest index among ties).
-__global__ void ce_rows_k(const float* __restrict__ logits, const int* __restrict__ tgt,
-                          float* __restrict__ lse, float* __restrict__ nll, int* __restrict__ amax,
-                          int V, int* status) {
-  __shared__ float sv[32];
-  __shared__ int si[32];
-  int m = blockIdx.x;
-  const float* row = logits + (size_t)m * V;
-  float best = -INFINITY;
-  int bi = 0x7fffffff;
-  for (int n = threadIdx.x; n < V; n += blockDim.x) {
-    float v = row[n];
-    if (v > best) { best = v; bi = n; }
-  }
-  // warp then block argmax with lowest-index tie break
-  for (int o = 16; o > 0; o >>= 1) {
-    float ov = __shfl_xor_sync(0xffffffffu, best, o);
-    int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
-  }
-  int wid = threadIdx.x / 32, lane = threadIdx.x & 31, nw = blockDim.x / 32;
-  if (lane == 0) { sv[wid] = best; si[wid] = bi; }
-  __syncthreads();
-  if (wid == 0) {
-    best = lane < nw ? sv[lane] : -INFINITY;
-    bi = lane < nw ? si[lane] : 0x7fffffff;
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, best, o);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
-    }
-    if (lane == 0) { sv[0] = best; si[0] = bi; }
-  }
-  __syncthreads();
-  float mx = sv[0];
-  int amx = si[0];
-  __syncthreads();
-  float s = 0.f;
-  for (int n = threadIdx.x; n < V; n += blockDim.x) s += expf(row[n] - mx);
-  s = warp_sum(s);
-  if (lane == 0) sv[wid] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < nw; ++i) tot += sv[i];
-    float l = mx + logf(tot);
-    int t = tgt[m];
-    lse[m] = l;
-    amax[m] = amx;
-    if (t == -1) {
-      nll[m] = 0.f;  // masked position: no loss
-    } else if (t < 0 || t >= V) {
-      set_status(status, DEV_BAD_TOKEN);
-      nll[m] = 0.f;
-    } else {
-      nll[m] = l - row[t];
-    }
-  }
-}
-
-// Combine per-tile softmax partials (max, sum of exp(logit - max), argmax)
-// of every 256-column vocabulary tile into lse, loss and argmax per row.
 // out = in * s for one device float (the loss-gradient scale of an
 // accumulating backward: 1 / unmasked count times the caller's scale).
 __global__ void scale_scalar_k(const float* __restrict__ in, float s, float* __restrict__ out) { *out = *in * s; }
@@ -425,6 +362,136 @@ __global__ void __launch_bounds__(32 * kCeWarps)
     nll[m] = tgt[m] < 0 ? 0.f : l - pt[m];  // a masked position carries no loss
     amax[m] = arg;
   }
+}
+
+// Two running (maximum, sum of exp(x - maximum), argmax) states of column
+// sets in no particular order: the argmax tie goes to the lower column.
+__device__ __forceinline__ void ce_merge_any(float& mx, float& s, int& arg, float m2, float s2, int a2) {
+  if (m2 == -INFINITY) return;
+  if (mx == -INFINITY) { mx = m2; s = s2; arg = a2; return; }
+  const float nm = fmaxf(mx, m2);
+  s = s * expf(mx - nm) + s2 * expf(m2 - nm);
+  if (m2 > mx || (m2 == mx && a2 < arg)) arg = a2;
+  mx = nm;
+}
+
+// Cross-entropy rows of a materialised fp32 logits block [M, V]: logsumexp,
+// loss lse - logit[target] (0 for a masked target -1), argmax (lowest column
+// among ties). CTA (seg, m) reads columns [seg L, min(V, seg L + L)) of row m
+// once, each thread keeping a running maximum and the sum of exp(x - maximum)
+// (rescaled when the maximum grows) over its 16-byte pieces, four in flight.
+// With one segment per row the CTA finishes its row. With S > 1 segments
+// (few rows: the segments spread a row over many SMs) each CTA leaves its
+// (maximum, sum, argmax, target logit) in part[m S + seg], and the CTA that
+// counts itself last on *counter merges every row's segments in column order
+// (the result does not depend on scheduling) and sets the counter back to 0.
+constexpr int kCeRowThreads = 256;
+__global__ void __launch_bounds__(kCeRowThreads)
+    ce_rows_k(const float* __restrict__ logits, const int* __restrict__ tgt, float* __restrict__ lse,
+              float* __restrict__ nll, int* __restrict__ amax, int M, int V, int L, int S, float4* part, int* counter,
+              int* status) {
+  __shared__ float smx[kCeRowThreads / 32], ssum[kCeRowThreads / 32];
+  __shared__ int sarg[kCeRowThreads / 32];
+  __shared__ int is_last;
+  const int seg = blockIdx.x, m = blockIdx.y;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const float* row = logits + (size_t)m * V;
+  const int lo = seg * L, hi = min(V, lo + L);
+  float mx = -INFINITY, s = 0.f;
+  int arg = 0x7fffffff;
+  if ((V & 3) == 0) {  // L is a multiple of 4: every piece is whole and aligned
+    constexpr int kStep = 4 * kCeRowThreads;
+    for (int n0 = lo + 4 * threadIdx.x; n0 < hi; n0 += 4 * kStep) {
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = n0 + u * kStep;
+        v[u] = n < hi ? ld4(row + n) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int n = n0 + u * kStep;
+        if (n >= hi) break;
+        const float gm = fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w));
+        if (gm > mx) {
+          s *= expf(mx - gm);  // 0 while mx = -inf
+          mx = gm;
+          arg = v[u].x == gm ? n : v[u].y == gm ? n + 1 : v[u].z == gm ? n + 2 : n + 3;
+        }
+        s += expf(v[u].x - mx) + expf(v[u].y - mx) + expf(v[u].z - mx) + expf(v[u].w - mx);
+      }
+    }
+  } else {
+    for (int n = lo + threadIdx.x; n < hi; n += kCeRowThreads) {
+      const float x = row[n];
+      if (x > mx) {
+        s *= expf(mx - x);
+        mx = x;
+        arg = n;
+      }
+      s += expf(x - mx);
+    }
+  }
+  // this CTA's state: warps, then warp 0 over the warps
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float om = __shfl_xor_sync(0xffffffffu, mx, o), os = __shfl_xor_sync(0xffffffffu, s, o);
+    const int oa = __shfl_xor_sync(0xffffffffu, arg, o);
+    ce_merge_any(mx, s, arg, om, os, oa);
+  }
+  if (lane == 0) {
+    smx[wid] = mx;
+    ssum[wid] = s;
+    sarg[wid] = arg;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kCeRowThreads / 32; ++w) ce_merge_any(mx, s, arg, smx[w], ssum[w], sarg[w]);
+    const int t = tgt[m];
+    if (S == 1) {
+      const float l = mx + logf(s);
+      lse[m] = l;
+      amax[m] = arg;
+      if (t == -1) {
+        nll[m] = 0.f;  // masked position: no loss
+      } else if (t < 0 || t >= V) {
+        set_status(status, DEV_BAD_TOKEN);
+        nll[m] = 0.f;
+      } else {
+        nll[m] = l - row[t];
+      }
+    } else {
+      const float tl = (t >= lo && t < hi) ? row[t] : 0.f;
+      part[(size_t)m * S + seg] = make_float4(mx, s, __int_as_float(arg), tl);
+      __threadfence();
+      is_last = atomicAdd(counter, 1) == S * M - 1;
+    }
+  }
+  if (S == 1) return;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  for (int r = threadIdx.x; r < M; r += kCeRowThreads) {
+    float rm = -INFINITY, rs = 0.f;
+    int ra = 0;
+    for (int k = 0; k < S; ++k) {  // column order: a later segment wins a tie only with a larger maximum
+      const float4 q = __ldcg(part + (size_t)r * S + k);
+      ce_merge(rm, rs, ra, q.x, q.y, __float_as_int(q.z));
+    }
+    const float l = rm + logf(rs);
+    const int t = tgt[r];
+    lse[r] = l;
+    amax[r] = ra;
+    if (t == -1) {
+      nll[r] = 0.f;
+    } else if (t < 0 || t >= V) {
+      set_status(status, DEV_BAD_TOKEN);
+      nll[r] = 0.f;
+    } else {
+      nll[r] = l - __ldcg(part + (size_t)r * S + t / L).w;
+    }
+  }
+  if (threadIdx.x == 0) *counter = 0;
 }
 
 // loss = mean of nll over the positions whose target is not masked (-1),
@@ -545,10 +612,21 @@ cudaError_t attn_rowdot(const T* dout, const T* o, float* Drow, int B, int T_, i
   return cudaGetLastError();
 }
 
-cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll,
-                                int* amax, int M, int V, int* status, cudaStream_t s) {
+cudaError_t ce_rows_from_logits(const float* logits, const int* tgt, float* lse, float* nll, int* amax, int M, int V,
+                                int* status, cudaStream_t s, float* part, int* counter, int sms) {
   if (M == 0) return cudaSuccess;
-  ce_rows_k<<<M, 512, 0, s>>>(logits, tgt, lse, nll, amax, V, status);
+  if (M > 65535 || V < 1) return cudaErrorInvalidValue;
+  // segments per row: enough CTAs for two per SM, at least 1024 columns each
+  int S = 1;
+  if (part && counter && M < 2 * sms) {
+    S = (2 * sms + M - 1) / M;
+    if (S > kCeMaxSegments) S = kCeMaxSegments;
+    if (S > V / 1024) S = V / 1024 > 1 ? V / 1024 : 1;
+  }
+  const int L = ((V + S - 1) / S + 3) & ~3;
+  S = (V + L - 1) / L;  // no empty segment
+  ce_rows_k<<<dim3(S, M), kCeRowThreads, 0, s>>>(logits, tgt, lse, nll, amax, M, V, L, S,
+                                                 reinterpret_cast<float4*>(part), counter, status);
   return cudaGetLastError();
 }
 

@@ -9,7 +9,8 @@
 // A use the same permutation. A CTA owns 8 * NT columns (NT n8 tiles) and its
 // 16 warps take the 32-wide k chunks round robin; the warps' partial sums are
 // added in shared memory in a fixed order (deterministic), so each product is
-// one launch. NT is chosen per product so that the CTAs cover the SMs.
+// one launch. NT is chosen per product so that the CTAs cover the SMs. The
+// MLP up-projection may leave as relu(u)^2 in bf16 directly.
 #include "ops.cuh"
 
 namespace nc {
@@ -29,7 +30,7 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, const uint
 template <int NT>
 __global__ void __launch_bounds__(32 * SK_WARPS)
     skinny_gemm_k(const bf16* __restrict__ A, long long lda, const bf16* __restrict__ W, long long ldw, float* C,
-                  long long ldc, int M, int N, int K, float alpha, float beta) {
+                  long long ldc, int M, int N, int K, float alpha, float beta, bf16* __restrict__ relu2) {
   constexpr int CW = 8 * NT;  // columns of this CTA
   __shared__ float red[SK_WARPS][16][CW];
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
@@ -98,6 +99,11 @@ __global__ void __launch_bounds__(32 * SK_WARPS)
     float s = 0.f;
 #pragma unroll
     for (int w = 0; w < SK_WARPS; ++w) s += red[w][m][nn];
+    if (relu2) {
+      const float u = fmaxf(alpha * s, 0.f);
+      relu2[(size_t)m * ldc + n] = __float2bfloat16_rn(u * u);
+      continue;
+    }
     float* c = C + (size_t)m * ldc + n;
     *c = beta != 0.f ? alpha * s + beta * *c : alpha * s;
   }
@@ -111,17 +117,17 @@ bool skinny_gemm_supports(int M, int N, int K, long long lda, long long ldw, con
 }
 
 cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
-                        int N, int K, float alpha, float beta, int sms, cudaStream_t s) {
+                        int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2) {
   // the widest column group that still gives every SM a CTA
   const int nt = (N + 31) / 32 >= sms ? 4 : ((N + 15) / 16 >= sms ? 2 : 1);
   const int cw = 8 * nt;
   const int blocks = (N + cw - 1) / cw;
   if (nt == 4)
-    skinny_gemm_k<4><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta);
+    skinny_gemm_k<4><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta, relu2);
   else if (nt == 2)
-    skinny_gemm_k<2><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta);
+    skinny_gemm_k<2><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta, relu2);
   else
-    skinny_gemm_k<1><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta);
+    skinny_gemm_k<1><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta, relu2);
   return cudaGetLastError();
 }
 

@@ -100,7 +100,7 @@ struct nc_ctx {
   } opt{};
   // decode scratch (one token per sequence), after the step's layout
   struct DecOff {
-    size_t x, r, xn, qkv, qh, o, u, a, hf, lse, nll, tgt;
+    size_t x, r, xn, qkv, o, u, a, hf, lse, nll, tgt, cep;
   } dec{};
   // optimizer hyper-parameters fixed per context (nc_optim_set_hparams)
   float opt_b1 = 0.9f, opt_b2 = 0.999f, opt_eps = 1e-8f, opt_mu = 0.95f;
@@ -240,14 +240,14 @@ void plan_workspace(nc_ctx* c) {
     q.r = take(Bn * 4);
     q.xn = take(Bn * d * e);
     q.qkv = take(Bn * 3 * d * 4);
-    q.qh = take(Bn * d * e);
     q.o = take(Bn * d * e);
-    q.u = take(Bn * F * 4);
+    q.u = take(Bn * F * 4);  // fp32 up-projection when ReLU^2 is not fused into it
     q.a = take(Bn * F * e);
     q.hf = take(Bn * d * e);
     q.lse = take(Bn * 4);
     q.nll = take(Bn * 4);
     q.tgt = take(Bn * 4);
+    q.cep = take(Bn * kCeMaxSegments * 16);  // cross-entropy row segments of the greedy head
   }
   c->ws_need = o;
   // optimizer scratch, from offset 0
@@ -650,7 +650,7 @@ nc_status optim_step(nc_ctx* c, T* param, const float* grads, float* state, int 
 // RoPE table for max_len positions (cos, sin fp32 [max_len, 64]); then the
 // attention partials of one decode step.
 struct KvLayout {
-  size_t per, rc, rs, part, total;
+  size_t per, rc, rs, part, cnt, total;
 };
 KvLayout kv_layout(const nc_ctx* c, int max_len) {
   KvLayout k;
@@ -664,6 +664,8 @@ KvLayout kv_layout(const nc_ctx* c, int max_len) {
   k.part = o;
   const size_t nch = (ml + kDecodeChunk - 1) / kDecodeChunk;
   o += align_up(Bn * H * nch * kDecodePartFloats * 4);
+  k.cnt = o;  // per (sequence, head): chunks of the decode attention done (0 between calls)
+  o += align_up(Bn * H * 4);
   k.total = o;
   return k;
 }
@@ -672,20 +674,24 @@ KvLayout kv_layout(const nc_ctx* c, int max_len) {
 // (elem [B, K]) one row per sequence: the weight-streaming kernel in bf16 for
 // up to 16 rows, the step's GEMM otherwise. Timed as decode GEMM work, counted
 // in weight bytes streamed.
+// With relu2 given the product leaves as relu2 = relu(A W^T)^2 (elem [B, N]):
+// fused into the weight-streaming kernel, else through C and a row kernel.
 template <typename T>
-nc_status dec_gemm(nc_ctx* c, int N, int K, const T* A, const T* W, float* C, float beta) {
+nc_status dec_gemm(nc_ctx* c, int N, int K, const T* A, const T* W, float* C, float beta, T* relu2 = nullptr) {
   const int Bn = c->B;
   if constexpr (sizeof(T) == 2) {
     if (skinny_gemm_supports(Bn, N, K, K, K, A, W)) {
       KL(NC_FAM_DEC_GEMM, (double)N * K * sizeof(T), 1,
-         skinny_gemm(A, K, W, K, C, N, Bn, N, K, 1.f, beta, c->sms, c->stream));
+         skinny_gemm(A, K, W, K, C, N, Bn, N, K, 1.f, beta, c->sms, c->stream, relu2));
       return NC_OK;
     }
   }
   c->gemm_fam = NC_FAM_DEC_GEMM;
   nc_status st = gemm(c, mk(Bn, N, K, A, K, 1, W, K, 1, EPI_STORE_F32, C, N, 1.f, beta));
   c->gemm_fam = NC_FAM_GEMM;
-  return st;
+  CKS(st);
+  if (relu2) KL(NC_FAM_DEC_ROWS, (double)Bn * N * (4 + c->esz), 1, relu2_rows<T>(C, relu2, (long long)Bn * N, c->stream));
+  return NC_OK;
 }
 
 // Greedy head over B rows of final hidden state: argmax (lowest index on
@@ -704,7 +710,7 @@ nc_status decode_head(nc_ctx* c, const T* P, const T* hf, int32_t* next, float* 
     CKS(dec_gemm<T>(c, V, d, hf, Wlm, lg, 0.f));
     KL(NC_FAM_DEC_ROWS, 4.0 * Bn * V, 1,
        ce_rows_from_logits(lg, tgt, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next, Bn, V, c->status,
-                           c->stream));
+                           c->stream, wsp<float>(c, c->dec.cep), c->status + 3, c->sms));
     return NC_OK;
   }
   c->gemm_fam = NC_FAM_DEC_GEMM;
@@ -743,6 +749,7 @@ nc_status prefill_impl(nc_ctx* c, const T* P, const int* tok, char* kv, int max_
   const size_t tab = (size_t)max_len * kHalf;
   CK(cudaMemcpyAsync(kv + kl.rc, c->dec_rope, tab * 4, cudaMemcpyDeviceToDevice, c->stream));
   CK(cudaMemcpyAsync(kv + kl.rs, c->dec_rope + tab, tab * 4, cudaMemcpyDeviceToDevice, c->stream));
+  CK(cudaMemsetAsync(kv + kl.cnt, 0, (size_t)c->B * c->H * 4, c->stream));
   CKS(forward_blocks<T>(c, P, tok));
   for (int l = 0; l < c->L; ++l) {
     const T* qkv = wsp<T>(c, (size_t)l * c->off.layer_stride + c->off.qkv);
@@ -768,7 +775,6 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
   float* r = wsp<float>(c, c->dec.r);
   T* xn = wsp<T>(c, c->dec.xn);
   float* qkv = wsp<float>(c, c->dec.qkv);
-  T* qh = wsp<T>(c, c->dec.qh);
   T* o = wsp<T>(c, c->dec.o);
   float* u = wsp<float>(c, c->dec.u);
   T* a = wsp<T>(c, c->dec.a);
@@ -776,6 +782,7 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
   const float* rc = reinterpret_cast<const float*>(kv + kl.rc);
   const float* rs = reinterpret_cast<const float*>(kv + kl.rs);
   float* part = reinterpret_cast<float*>(kv + kl.part);
+  int* cnt = reinterpret_cast<int*>(kv + kl.cnt);
   KL(NC_FAM_DEC_ROWS, (double)Bn * d * (e + 4) + 4.0 * Bn, 1, embed_fwd<T>(tok, P, x, Bn, d, V, c->status, s));
   int rows, cols;
   for (int l = 0; l < c->L; ++l) {
@@ -787,14 +794,11 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
     T* Vc = reinterpret_cast<T*>(kv + (size_t)(2 * l + 1) * kl.per);
     KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
     CKS(dec_gemm<T>(c, 3 * d, d, xn, Wqkv, qkv, 0.f));
-    KL(NC_FAM_DEC_ROWS, (double)Bn * 3 * d * (4 + e), 1,
-       decode_qkv<T>(qkv, qh, K, Vc, rc, rs, Bn, H, pos, d_pos, max_len, c->status, s));
-    KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * ((d_pos ? max_len : pos) + 1) * e, 2,
-       attn_decode<T>(qh, K, Vc, part, o, Bn, H, pos, d_pos, max_len, kDecodeChunk, s));
+    KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * ((d_pos ? max_len : pos) + 1) * e, 1,
+       attn_decode<T>(qkv, rc, rs, K, Vc, part, cnt, o, Bn, H, pos, d_pos, max_len, kDecodeChunk, c->status, s));
     CKS(dec_gemm<T>(c, d, d, o, Wo, x, 1.f));
     KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    CKS(dec_gemm<T>(c, F, d, xn, Wfc, u, 0.f));
-    KL(NC_FAM_DEC_ROWS, (double)Bn * F * (4 + e), 1, relu2_rows<T>(u, a, (long long)Bn * F, s));
+    CKS(dec_gemm<T>(c, F, d, xn, Wfc, u, 0.f, a));
     CKS(dec_gemm<T>(c, d, F, a, Wproj, x, 1.f));
   }
   KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, hf, r, Bn, d, s));
@@ -846,7 +850,8 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   // the decode table is rebuilt on the (possibly different) device by the next prefill
   if (c->dec_rope) { cudaFree(c->dec_rope); c->dec_rope = nullptr; }
   c->dec_rope_len = 0;
-  // device words: [0] status, [1] and [2] work counters of the persistent attention backward and forward.
+  // device words: [0] status, [1] and [2] work counters of the persistent attention backward and forward,
+  // [3] the finished-CTA count of the split cross-entropy rows (left at 0 by each launch).
   // A context configured again on another device gets them anew there, like the tables above.
   if (c->status && c->device >= 0 && c->device != dev) {
     cudaFree(c->status);
@@ -877,7 +882,7 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   CK(cudaMemcpyAsync(c->rope_sin, hs.data(), hs.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->rope_cos4, hc4.data(), hc4.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->rope_sin4, hs4.data(), hs4.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
-  CK(cudaMemsetAsync(c->status, 0, sizeof(int), c->stream));
+  CK(cudaMemsetAsync(c->status, 0, 16 * sizeof(int), c->stream));
   CK(cudaStreamSynchronize(c->stream));
   c->device = dev;
   c->sms = prop.multiProcessorCount > 0 ? prop.multiProcessorCount : 148;
