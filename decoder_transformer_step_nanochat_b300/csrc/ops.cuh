@@ -72,12 +72,18 @@ bool gemm_tc_supports(const GemmArgs& g);
 // Weight-streaming product of the decode step: C (fp32) = alpha * A W^T (+ beta * C)
 // for M <= 16 rows of A (bf16 [M, K], K-major) and W (bf16 [N, K], K-major),
 // K a multiple of 32, 16-byte aligned operands; one launch, deterministic.
-// sms: the device's SM count (sizes the column groups). With relu2 given,
-// the product u = alpha * A W^T leaves as relu2[m, n] = bf16(max(u, 0)^2)
-// (row stride ldc) and C is not touched.
+// sms: the device's SM count (the persistent grid). With relu2 given, the
+// product u = alpha * A W^T leaves as relu2[m, n] = bf16(max(u, 0)^2) (row
+// stride ldc) and C is not touched. K longer than 2048 runs in k-ranges whose
+// partial sums need part (skinny_scratch_floats(N, K) floats) and cnt
+// (skinny_counters(N) ints, 0 before the first call; each call leaves them 0).
+// A wait past its limit sets DEV_TIMEOUT in *status.
 bool skinny_gemm_supports(int M, int N, int K, long long lda, long long ldw, const void* A, const void* W);
+size_t skinny_scratch_floats(int N, int K);
+int skinny_counters(int N);
 cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
-                        int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2 = nullptr);
+                        int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2, float* part,
+                        int* cnt, int* status);
 
 // ------------------------------------------------------------------ rows
 template <typename T>

@@ -1,23 +1,58 @@
 // Weight-streaming products of the decode step: C[m, n] = alpha * sum_k A[m, k] W[n, k]
 // (+ beta * C) for at most 16 rows m (one token per sequence), bf16 operands,
-// fp32 output. The product is bound by streaming W once from HBM (2 bytes per
-// weight for 2 * rows FLOPs), so it runs on the warp-level tensor-core MMA
-// (m16n8k16, fp32 accumulate) with W read straight from global memory in
-// 16-byte pieces: a lane loads 8 consecutive k of one W row, which form the
-// two k16 fragments of one 32-wide k chunk under a fixed permutation of k
-// inside the chunk (the sum over k does not depend on its order); the rows of
-// A use the same permutation. A CTA owns 8 * NT columns (NT n8 tiles) and its
-// 16 warps take the 32-wide k chunks round robin; the warps' partial sums are
-// added in shared memory in a fixed order (deterministic), so each product is
-// one launch. NT is chosen per product so that the CTAs cover the SMs. The
-// MLP up-projection may leave as relu(u)^2 in bf16 directly.
+// fp32 output, or relu(.)^2 in bf16 for the MLP up-projection. The product is
+// bound by streaming W once from HBM (2 bytes per weight for 2 * rows FLOPs).
+//
+// Work items are (k-range, 16-column block) pairs, k-range-major; persistent
+// CTAs (one per SM) take items round robin. The 16 W rows x k-range of an
+// item are brought into shared memory by 16 untiled bulk copies (one per row)
+// that complete on the item's mbarrier, in a ring of up to 4 stages, so an
+// SM keeps the next items' weight reads (100+ KB) in flight while it works on
+// the current one. (Per-thread 16-byte loads kept too few requests in flight:
+// each warp load touched eight half lines, and the products ran at 1.2-1.4
+// TB/s.) A staged row is padded by 64 bytes, so the 16-byte fragment reads of
+// a warp's eight rows fall in distinct banks.
+//
+// The sum runs on the warp-level tensor-core MMA (m16n8k16, fp32 accumulate):
+// a lane reads 8 consecutive k of one W row, which form the two k16 fragments
+// of a 32-wide k chunk under a fixed permutation of k inside the chunk (the
+// sum over k does not depend on its order); the A rows use the same
+// permutation and stay in registers across the items of one k-range. The 16
+// warps take the chunks of the k-range round robin; their partial sums are
+// added in shared memory in warp order. With one k-range per product the CTA
+// writes the outputs; with several, each item leaves its partial sums and the
+// CTA that completes a column block last (a counter per block, left at zero)
+// adds the k-ranges in order. Every result is independent of scheduling.
 #include "ops.cuh"
+#include "tc_ptx.cuh"
 
 namespace nc {
 namespace {
 
 constexpr int SK_WARPS = 16;
-constexpr int SK_UNROLL = 4;  // 32-wide k chunks per round (loads in flight)
+constexpr int SK_THREADS = 32 * SK_WARPS;
+constexpr int SK_CW = 16;                          // columns per item: two n8 tiles
+constexpr int SK_KCH = 4;                          // k chunks per warp and item, at most
+constexpr int SK_KC_MAX = SK_WARPS * SK_KCH * 32;  // longest k-range: 2048
+constexpr int SK_PAD = 64;                         // bytes after each staged row
+constexpr int SK_RED_BYTES = 2 * SK_WARPS * 16 * SK_CW * 4;  // double-buffered warp partials
+constexpr int SK_SMEM_MAX = 227 * 1024 - 1024;  // dynamic part, leaving room for the static words
+constexpr uint64_t kSkWaitNs = 2000000000ull;
+
+struct SkParams {
+  const bf16* A;
+  const bf16* W;
+  float* C;
+  bf16* relu2;
+  float* part;  // [nks][16][N] partial sums (nks > 1)
+  int* cnt;     // [ncb] finished k-ranges per column block (nks > 1)
+  int* status;
+  long long lda, ldw, ldc;
+  int M, N, K;
+  float alpha, beta;
+  int ncb, nks, KC, items, ns, row_bytes, stage_bytes;
+  int whole;  // one k-range and rows packed (ldw == K): an item is one contiguous copy
+};
 
 __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, const uint32_t* b) {
   asm volatile(
@@ -27,86 +62,175 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, const uint
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
-template <int NT>
-__global__ void __launch_bounds__(32 * SK_WARPS)
-    skinny_gemm_k(const bf16* __restrict__ A, long long lda, const bf16* __restrict__ W, long long ldw, float* C,
-                  long long ldc, int M, int N, int K, float alpha, float beta, bf16* __restrict__ relu2) {
-  constexpr int CW = 8 * NT;  // columns of this CTA
-  __shared__ float red[SK_WARPS][16][CW];
-  const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  const int n0 = blockIdx.x * CW;
-  const int nchunks = K / 32;
-  // this lane's W rows (one per n8 tile) and A rows (g, g + 8; zero beyond M)
-  const bf16* wrow[NT];
-  bool wok[NT];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    const int n = n0 + 8 * j + g;
-    wok[j] = n < N;
-    wrow[j] = W + (size_t)(wok[j] ? n : 0) * ldw;
+// the output value as stored: fp32 C (alpha, beta) or bf16 relu(alpha v)^2
+__device__ __forceinline__ void sk_store(const SkParams& p, int m, int n, float v) {
+  const size_t o = (size_t)m * p.ldc + n;
+  if (p.relu2) {
+    const float u = fmaxf(p.alpha * v, 0.f);
+    p.relu2[o] = __float2bfloat16_rn(u * u);
+  } else {
+    p.C[o] = p.beta != 0.f ? p.alpha * v + p.beta * p.C[o] : p.alpha * v;
   }
-  const bool a0ok = g < M, a1ok = g + 8 < M;
-  const bf16* arow0 = A + (size_t)(a0ok ? g : 0) * lda;
-  const bf16* arow1 = A + (size_t)(a1ok ? g + 8 : 0) * lda;
-  float acc[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int c0 = warp; c0 < nchunks; c0 += SK_WARPS * SK_UNROLL) {
-    uint4 wv[SK_UNROLL][NT], av[SK_UNROLL][2];
-#pragma unroll
-    for (int u = 0; u < SK_UNROLL; ++u) {
-      const int ch = c0 + u * SK_WARPS;
-      const bool in = ch < nchunks;
-      const int k = ch * 32 + 8 * t;
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-        wv[u][j] = (in && wok[j]) ? __ldg(reinterpret_cast<const uint4*>(wrow[j] + k)) : zero;
-      av[u][0] = (in && a0ok) ? __ldg(reinterpret_cast<const uint4*>(arow0 + k)) : zero;
-      av[u][1] = (in && a1ok) ? __ldg(reinterpret_cast<const uint4*>(arow1 + k)) : zero;
+}
+
+// thread 0: the bulk copies of item i into stage s
+__device__ __forceinline__ void sk_issue(const SkParams& p, uint8_t* stages, uint64_t* full, int i, int s) {
+  const int kr = i / p.ncb, cb = i - kr * p.ncb;
+  const int k0 = kr * p.KC, kn = min(p.KC, p.K - k0);
+  const int n0 = cb * SK_CW, rows = min(SK_CW, p.N - n0);
+  tc::mbar_arrive_expect_tx(full + s, (uint32_t)(rows * kn * 2));
+  uint8_t* dst = stages + (size_t)s * p.stage_bytes;
+  if (p.whole) {
+    tc::bulk_load(dst, p.W + (size_t)n0 * p.ldw, (uint32_t)(rows * kn * 2), full + s);
+    return;
+  }
+  for (int r = 0; r < rows; ++r)
+    tc::bulk_load(dst + (size_t)r * p.row_bytes, p.W + (size_t)(n0 + r) * p.ldw + k0, (uint32_t)(kn * 2), full + s);
+}
+
+__global__ void __launch_bounds__(SK_THREADS, 1) skinny_gemm_k(const SkParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint8_t* stages = smem;
+  float* red = reinterpret_cast<float*>(smem + (size_t)p.ns * p.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.ns * p.stage_bytes + SK_RED_BYTES);
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int first = blockIdx.x, step = gridDim.x;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.ns; ++s) tc::mbar_init(full + s, 1);
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int j = 0; j < p.ns; ++j) {
+      const int i = first + j * step;
+      if (i < p.items) sk_issue(p, stages, full, i, j);
     }
+  // A fragments of this warp's chunks (rows g and g + 8, zero past M) for the k-range a_kr
+  uint4 af[SK_KCH][2];
+  int a_kr = -1;
+  const bool a0ok = g < p.M, a1ok = g + 8 < p.M;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  int it = 0;
+  for (int i = first; i < p.items; i += step, ++it) {
+    const int s = it % p.ns;
+    const uint32_t ph = (uint32_t)(it / p.ns) & 1;
+    const int kr = i / p.ncb, cb = i - kr * p.ncb;
+    const int k0 = kr * p.KC, nch = min(p.KC, p.K - k0) / 32;
+    const int n0 = cb * SK_CW;
+    if (kr != a_kr) {
 #pragma unroll
-    for (int u = 0; u < SK_UNROLL; ++u) {
+      for (int u = 0; u < SK_KCH; ++u) {
+        const int c = warp + SK_WARPS * u;
+        const bool in = c < nch;
+        const size_t k = (size_t)k0 + c * 32 + 8 * t;
+        af[u][0] = (in && a0ok) ? __ldg(reinterpret_cast<const uint4*>(p.A + (size_t)g * p.lda + k)) : zero;
+        af[u][1] = (in && a1ok) ? __ldg(reinterpret_cast<const uint4*>(p.A + (size_t)(g + 8) * p.lda + k)) : zero;
+      }
+      a_kr = kr;
+    }
+    const bool ok = tc::mbar_wait(full + s, ph, nullptr, kSkWaitNs);
+    if (__syncthreads_or(!ok)) {
+      // give up: report, and let the copies already issued land before the CTA leaves
+      if (threadIdx.x == 0) {
+        set_status(p.status, DEV_TIMEOUT);
+        for (int j = 0; j < p.ns; ++j) {
+          const int ij = i + j * step;
+          if (ij < p.items) tc::mbar_wait(full + (it + j) % p.ns, (uint32_t)((it + j) / p.ns) & 1, nullptr, kSkWaitNs);
+        }
+      }
+      __syncthreads();
+      return;
+    }
+    const uint8_t* sw = stages + (size_t)s * p.stage_bytes;
+    float acc[2][4];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+#pragma unroll
+    for (int u = 0; u < SK_KCH; ++u) {
+      const int c = warp + SK_WARPS * u;
+      if (c >= nch) break;
       // k16 step 0 takes physical k 8t..8t+3 of the chunk, step 1 takes 8t+4..8t+7:
       // fragment registers {k 2t,2t+1} <- pieces .x/.z, {k 2t+8,2t+9} <- .y/.w
-      const uint32_t a_s0[4] = {av[u][0].x, av[u][1].x, av[u][0].y, av[u][1].y};
-      const uint32_t a_s1[4] = {av[u][0].z, av[u][1].z, av[u][0].w, av[u][1].w};
+      const uint32_t a_s0[4] = {af[u][0].x, af[u][1].x, af[u][0].y, af[u][1].y};
+      const uint32_t a_s1[4] = {af[u][0].z, af[u][1].z, af[u][0].w, af[u][1].w};
 #pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const uint32_t b_s0[2] = {wv[u][j].x, wv[u][j].y};
-        const uint32_t b_s1[2] = {wv[u][j].z, wv[u][j].w};
+      for (int j = 0; j < 2; ++j) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(sw + (size_t)(8 * j + g) * p.row_bytes + (c * 32 + 8 * t) * 2);
+        const uint32_t b_s0[2] = {wv.x, wv.y};
+        const uint32_t b_s1[2] = {wv.z, wv.w};
         mma16816(acc[j], a_s0, b_s0);
         mma16816(acc[j], a_s1, b_s1);
       }
     }
-  }
-  // D fragment: rows g, g+8; columns 2t, 2t+1 of each n8 tile
+    // D fragment: rows g, g+8; columns 2t, 2t+1 of each n8 tile
+    float* rb = red + (size_t)(it & 1) * SK_WARPS * 16 * SK_CW;
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    red[warp][g][8 * j + 2 * t] = acc[j][0];
-    red[warp][g][8 * j + 2 * t + 1] = acc[j][1];
-    red[warp][g + 8][8 * j + 2 * t] = acc[j][2];
-    red[warp][g + 8][8 * j + 2 * t + 1] = acc[j][3];
-  }
-  __syncthreads();
-  // the 16 warps' partial sums in warp order, one output per thread
-  for (int i = threadIdx.x; i < 16 * CW; i += 32 * SK_WARPS) {
-    const int m = i / CW, nn = i % CW, n = n0 + nn;
-    if (m >= M || n >= N) continue;
-    float s = 0.f;
+    for (int j = 0; j < 2; ++j) {
+      float* r0 = rb + ((size_t)warp * 16 + g) * SK_CW + 8 * j + 2 * t;
+      float* r1 = rb + ((size_t)warp * 16 + g + 8) * SK_CW + 8 * j + 2 * t;
+      r0[0] = acc[j][0];
+      r0[1] = acc[j][1];
+      r1[0] = acc[j][2];
+      r1[1] = acc[j][3];
+    }
+    __syncthreads();
+    // the stage is free: it takes item i + ns * step
+    if (threadIdx.x == 0) {
+      const int ni = i + p.ns * step;
+      if (ni < p.items) sk_issue(p, stages, full, ni, s);
+    }
+    // the 16 warps' partial sums in warp order, one output per thread
+    const int m = threadIdx.x / SK_CW, nn = threadIdx.x % SK_CW, n = n0 + nn;
+    float v = 0.f;
+    if (threadIdx.x < 16 * SK_CW) {
 #pragma unroll
-    for (int w = 0; w < SK_WARPS; ++w) s += red[w][m][nn];
-    if (relu2) {
-      const float u = fmaxf(alpha * s, 0.f);
-      relu2[(size_t)m * ldc + n] = __float2bfloat16_rn(u * u);
+      for (int w = 0; w < SK_WARPS; ++w) v += rb[((size_t)w * 16 + m) * SK_CW + nn];
+    }
+    if (p.nks == 1) {
+      if (threadIdx.x < 16 * SK_CW && m < p.M && n < p.N) sk_store(p, m, n, v);
       continue;
     }
-    float* c = C + (size_t)m * ldc + n;
-    *c = beta != 0.f ? alpha * s + beta * *c : alpha * s;
+    if (threadIdx.x < 16 * SK_CW && n < p.N) p.part[((size_t)kr * 16 + m) * p.N + n] = v;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(p.cnt + cb, 1) == p.nks - 1;
+    __syncthreads();
+    if (s_last) {  // every k-range of this column block is in part: add them in order
+      __threadfence();
+      if (threadIdx.x < 16 * SK_CW && m < p.M && n < p.N) {
+        float sum = 0.f;
+        for (int r = 0; r < p.nks; ++r) sum += __ldcg(p.part + ((size_t)r * 16 + m) * p.N + n);
+        sk_store(p, m, n, sum);
+      }
+      if (threadIdx.x == 0) p.cnt[cb] = 0;
+    }
   }
+}
+
+struct SkShape {
+  int ncb, nks, KC, row_bytes, stage_bytes, ns, whole;
+};
+
+// whole: packed rows (ldw == K) in a single k-range, staged as one copy per
+// item with unpadded rows (the fragment reads then meet 2-way bank conflicts
+// when 2K is a multiple of 128, a few per item; one copy per item costs far
+// less than sixteen)
+SkShape sk_shape(int N, int K, long long ldw) {
+  SkShape sh;
+  sh.ncb = (N + SK_CW - 1) / SK_CW;
+  sh.nks = (K + SK_KC_MAX - 1) / SK_KC_MAX;
+  sh.KC = ((K + sh.nks - 1) / sh.nks + 63) / 64 * 64;
+  if (sh.KC > SK_KC_MAX) sh.KC = SK_KC_MAX;
+  sh.whole = sh.nks == 1 && ldw == K;
+  sh.row_bytes = sh.whole ? 2 * K : 2 * sh.KC + SK_PAD;
+  sh.stage_bytes = SK_CW * sh.row_bytes;
+  sh.ns = (SK_SMEM_MAX - SK_RED_BYTES - 256) / sh.stage_bytes;
+  if (sh.ns > 4) sh.ns = 4;
+  return sh;
 }
 
 }  // namespace
@@ -116,18 +240,40 @@ bool skinny_gemm_supports(int M, int N, int K, long long lda, long long ldw, con
          (reinterpret_cast<uintptr_t>(A) & 15) == 0 && (reinterpret_cast<uintptr_t>(W) & 15) == 0;
 }
 
+size_t skinny_scratch_floats(int N, int K) {
+  const SkShape sh = sk_shape(N, K, K);
+  return sh.nks > 1 ? (size_t)sh.nks * 16 * N : 0;
+}
+
+int skinny_counters(int N) { return (N + SK_CW - 1) / SK_CW; }
+
 cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
-                        int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2) {
-  // the widest column group that still gives every SM a CTA
-  const int nt = (N + 31) / 32 >= sms ? 4 : ((N + 15) / 16 >= sms ? 2 : 1);
-  const int cw = 8 * nt;
-  const int blocks = (N + cw - 1) / cw;
-  if (nt == 4)
-    skinny_gemm_k<4><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta, relu2);
-  else if (nt == 2)
-    skinny_gemm_k<2><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta, relu2);
-  else
-    skinny_gemm_k<1><<<blocks, 32 * SK_WARPS, 0, s>>>(A, lda, W, ldw, C, ldc, M, N, K, alpha, beta, relu2);
+                        int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2, float* part,
+                        int* cnt, int* status) {
+  const SkShape sh = sk_shape(N, K, ldw);
+  if (sh.ns < 1) return cudaErrorNotSupported;
+  if (sh.nks > 1 && (!part || !cnt)) return cudaErrorInvalidValue;
+  SkParams p;
+  p.A = A; p.W = W; p.C = C; p.relu2 = relu2; p.part = part; p.cnt = cnt; p.status = status;
+  p.lda = lda; p.ldw = ldw; p.ldc = ldc;
+  p.M = M; p.N = N; p.K = K; p.alpha = alpha; p.beta = beta;
+  p.ncb = sh.ncb; p.nks = sh.nks; p.KC = sh.KC; p.items = sh.ncb * sh.nks;
+  p.ns = sh.ns; p.row_bytes = sh.row_bytes; p.stage_bytes = sh.stage_bytes; p.whole = sh.whole;
+  const int smem = sh.ns * sh.stage_bytes + SK_RED_BYTES + 8 * sh.ns;
+  // the dynamic shared-memory limit is a per-device function attribute: raised
+  // when a launch needs more than the device's setting so far
+  static int attr_dev = -1, attr_bytes = 0;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != attr_dev || smem > attr_bytes) {
+    e = cudaFuncSetAttribute(skinny_gemm_k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+    attr_bytes = smem;
+  }
+  const int grid = p.items < sms ? p.items : sms;
+  skinny_gemm_k<<<grid, SK_THREADS, smem, s>>>(p);
   return cudaGetLastError();
 }
 

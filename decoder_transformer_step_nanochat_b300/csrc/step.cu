@@ -11,6 +11,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <algorithm>
 #include <new>
 #include <string>
 #include <vector>
@@ -650,7 +651,7 @@ nc_status optim_step(nc_ctx* c, T* param, const float* grads, float* state, int 
 // RoPE table for max_len positions (cos, sin fp32 [max_len, 64]); then the
 // attention partials of one decode step.
 struct KvLayout {
-  size_t per, rc, rs, part, cnt, total;
+  size_t per, rc, rs, part, cnt, skp, skc, total;
 };
 KvLayout kv_layout(const nc_ctx* c, int max_len) {
   KvLayout k;
@@ -666,6 +667,18 @@ KvLayout kv_layout(const nc_ctx* c, int max_len) {
   o += align_up(Bn * H * nch * kDecodePartFloats * 4);
   k.cnt = o;  // per (sequence, head): chunks of the decode attention done (0 between calls)
   o += align_up(Bn * H * 4);
+  // k-range partial sums and per-column-block counters of the weight-streaming products
+  size_t skf = 0, skn = 0;
+  const int d = c->d, F = c->F, V = c->V;
+  const int shapes[5][2] = {{3 * d, d}, {d, d}, {F, d}, {d, F}, {V, d}};
+  for (const auto& nk : shapes) {
+    skf = std::max(skf, skinny_scratch_floats(nk[0], nk[1]));
+    skn = std::max(skn, (size_t)skinny_counters(nk[0]));
+  }
+  k.skp = o;
+  o += align_up(skf * 4);
+  k.skc = o;
+  o += align_up(skn * 4);
   k.total = o;
   return k;
 }
@@ -676,13 +689,17 @@ KvLayout kv_layout(const nc_ctx* c, int max_len) {
 // in weight bytes streamed.
 // With relu2 given the product leaves as relu2 = relu(A W^T)^2 (elem [B, N]):
 // fused into the weight-streaming kernel, else through C and a row kernel.
+// kv: the KV cache buffer, whose scratch holds the weight-streaming kernel's
+// k-range partial sums and counters.
 template <typename T>
-nc_status dec_gemm(nc_ctx* c, int N, int K, const T* A, const T* W, float* C, float beta, T* relu2 = nullptr) {
+nc_status dec_gemm(nc_ctx* c, char* kv, const KvLayout& kl, int N, int K, const T* A, const T* W, float* C,
+                   float beta, T* relu2 = nullptr) {
   const int Bn = c->B;
   if constexpr (sizeof(T) == 2) {
     if (skinny_gemm_supports(Bn, N, K, K, K, A, W)) {
       KL(NC_FAM_DEC_GEMM, (double)N * K * sizeof(T), 1,
-         skinny_gemm(A, K, W, K, C, N, Bn, N, K, 1.f, beta, c->sms, c->stream, relu2));
+         skinny_gemm(A, K, W, K, C, N, Bn, N, K, 1.f, beta, c->sms, c->stream, relu2,
+                     reinterpret_cast<float*>(kv + kl.skp), reinterpret_cast<int*>(kv + kl.skc), c->status));
       return NC_OK;
     }
   }
@@ -699,15 +716,15 @@ nc_status dec_gemm(nc_ctx* c, int N, int K, const T* A, const T* W, float* C, fl
 // product the logits of the B rows are formed in fp32 (in the caller's buffer
 // when given, else in the workspace) and reduced per row.
 template <typename T>
-nc_status decode_head(nc_ctx* c, const T* P, const T* hf, int32_t* next, float* logits) {
+nc_status decode_head(nc_ctx* c, char* kv, const KvLayout& kl, const T* P, const T* hf, int32_t* next,
+                      float* logits) {
   const int Bn = c->B, d = c->d, V = c->V;
   int rows, cols;
   const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
-  int* tgt = wsp<int>(c, c->dec.tgt);  // -1: no target, only lse and argmax
-  CK(cudaMemsetAsync(tgt, 0xff, (size_t)Bn * sizeof(int), c->stream));
+  const int* tgt = wsp<int>(c, c->dec.tgt);  // all -1 (set by the caller): only lse and argmax
   if (c->prec == NC_BF16 && skinny_gemm_supports(Bn, V, d, d, d, hf, Wlm)) {
     float* lg = logits ? logits : wsp<float>(c, c->off.chunk);
-    CKS(dec_gemm<T>(c, V, d, hf, Wlm, lg, 0.f));
+    CKS(dec_gemm<T>(c, kv, kl, V, d, hf, Wlm, lg, 0.f));
     KL(NC_FAM_DEC_ROWS, 4.0 * Bn * V, 1,
        ce_rows_from_logits(lg, tgt, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next, Bn, V, c->status,
                            c->stream, wsp<float>(c, c->dec.cep), c->status + 3, c->sms));
@@ -750,6 +767,7 @@ nc_status prefill_impl(nc_ctx* c, const T* P, const int* tok, char* kv, int max_
   CK(cudaMemcpyAsync(kv + kl.rc, c->dec_rope, tab * 4, cudaMemcpyDeviceToDevice, c->stream));
   CK(cudaMemcpyAsync(kv + kl.rs, c->dec_rope + tab, tab * 4, cudaMemcpyDeviceToDevice, c->stream));
   CK(cudaMemsetAsync(kv + kl.cnt, 0, (size_t)c->B * c->H * 4, c->stream));
+  CK(cudaMemsetAsync(kv + kl.skc, 0, kl.total - kl.skc, c->stream));
   CKS(forward_blocks<T>(c, P, tok));
   for (int l = 0; l < c->L; ++l) {
     const T* qkv = wsp<T>(c, (size_t)l * c->off.layer_stride + c->off.qkv);
@@ -759,7 +777,8 @@ nc_status prefill_impl(nc_ctx* c, const T* P, const int* tok, char* kv, int max_
   }
   T* hl = wsp<T>(c, c->dec.hf);
   KL(NC_FAM_DEC_ROWS, 2.0 * c->B * c->d * c->esz, 1, gather_last<T>(wsp<T>(c, c->off.hf), hl, c->B, c->T, c->d, c->stream));
-  return decode_head<T>(c, P, hl, next, logits);
+  CK(cudaMemsetAsync(wsp<int>(c, c->dec.tgt), 0xff, (size_t)c->B * sizeof(int), c->stream));
+  return decode_head<T>(c, kv, kl, P, hl, next, logits);
 }
 
 // pos: the step's position, or -1 with d_pos: read it from device memory and
@@ -783,6 +802,8 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
   const float* rs = reinterpret_cast<const float*>(kv + kl.rs);
   float* part = reinterpret_cast<float*>(kv + kl.part);
   int* cnt = reinterpret_cast<int*>(kv + kl.cnt);
+  // the greedy head's targets: -1 (no target, only lse and argmax)
+  CK(cudaMemsetAsync(wsp<int>(c, c->dec.tgt), 0xff, (size_t)Bn * sizeof(int), s));
   KL(NC_FAM_DEC_ROWS, (double)Bn * d * (e + 4) + 4.0 * Bn, 1, embed_fwd<T>(tok, P, x, Bn, d, V, c->status, s));
   int rows, cols;
   for (int l = 0; l < c->L; ++l) {
@@ -793,16 +814,16 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
     T* K = reinterpret_cast<T*>(kv + (size_t)2 * l * kl.per);
     T* Vc = reinterpret_cast<T*>(kv + (size_t)(2 * l + 1) * kl.per);
     KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    CKS(dec_gemm<T>(c, 3 * d, d, xn, Wqkv, qkv, 0.f));
+    CKS(dec_gemm<T>(c, kv, kl, 3 * d, d, xn, Wqkv, qkv, 0.f));
     KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * ((d_pos ? max_len : pos) + 1) * e, 1,
        attn_decode<T>(qkv, rc, rs, K, Vc, part, cnt, o, Bn, H, pos, d_pos, max_len, kDecodeChunk, c->status, s));
-    CKS(dec_gemm<T>(c, d, d, o, Wo, x, 1.f));
+    CKS(dec_gemm<T>(c, kv, kl, d, d, o, Wo, x, 1.f));
     KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    CKS(dec_gemm<T>(c, F, d, xn, Wfc, u, 0.f, a));
-    CKS(dec_gemm<T>(c, d, F, a, Wproj, x, 1.f));
+    CKS(dec_gemm<T>(c, kv, kl, F, d, xn, Wfc, u, 0.f, a));
+    CKS(dec_gemm<T>(c, kv, kl, d, F, a, Wproj, x, 1.f));
   }
   KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, hf, r, Bn, d, s));
-  CKS(decode_head<T>(c, P, hf, next, logits));
+  CKS(decode_head<T>(c, kv, kl, P, hf, next, logits));
   if (d_pos) KL(NC_FAM_DEC_ROWS, 8.0, 1, advance_pos(d_pos, s));
   return NC_OK;
 }
