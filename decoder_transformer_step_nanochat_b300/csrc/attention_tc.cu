@@ -76,6 +76,22 @@ __device__ __forceinline__ void unpack8(uint4 u, float* f) {
   }
 }
 
+// One 32-bit column of this thread's TMEM lane: store (then wait) and load.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(__float_as_uint(v)) : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r)
+      : "r"(taddr)
+      : "memory");
+  return __uint_as_float(r);
+}
+
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -515,7 +531,8 @@ __device__ __forceinline__ BwdUnit bwd_unit(const AttnParams& p, int v) {
 
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     attn_bwd_tc_k(const __grid_constant__ CUtensorMap tqkv, const __grid_constant__ CUtensorMap tdo,
-                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ AttnParams p) {
+                  const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdkv,
+                  const __grid_constant__ AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint64_t wait_ns = g_pipe_wait_ns;
   if (tc::smem_u32(smem_raw) & 1023) {  // see the forward kernel
@@ -542,7 +559,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   uint64_t* acc_free = bars + 15;
   uint64_t* drain = bars + 16;
   uint64_t* tile_done = bars + 17;  // every product of the tile complete (its Q/dO stage unread)
-  uint64_t* xch = bars + 18;        // both warpgroups' partial dk row dots written (one arrival per warp)
+  uint64_t* pair = bars + 22;       // [4]: the two warps (one per warpgroup) of a 32-row block
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 19);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   // unit index of this CTA's ul-th unit at slot ul % 4 (-1: no more units); it
@@ -569,7 +586,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     tc::mbar_init(acc_free, BWD_SOFT / 32);
     tc::mbar_init(drain, 1);
     tc::mbar_init(tile_done, 1);
-    tc::mbar_init(xch, BWD_SOFT / 32);
+    for (int q = 0; q < 4; ++q) tc::mbar_init(pair + q, 2);  // one arrival per warp
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -866,20 +883,48 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         // rk R^T (dk_hat - k_hat mean(dk_hat k_hat)): a rotation keeps dot
         // products, so the mean needs neither the table nor a rotation.
         // Warpgroup ch finishes the rotation pairs (j, j + 64) with j in
-        // [32 ch, 32 ch + 32) and writes dv dims [64 ch, 64 ch + 64). The two
-        // partial dots of a row meet through one float per row in the idle
-        // dS^T buffer, in the half that the reading thread itself overwrites
-        // next (so no later write can race the read), and are added in
-        // warpgroup order.
+        // [32 ch, 32 ch + 32) and dv dims [64 ch, 64 ch + 64). Both leave
+        // through the idle dS^T buffer, staged bf16 in the tile layout and
+        // written by tensor copies of 32 rows x 64 dims (lane 1 issues them,
+        // so their completion is tracked apart from lane 0's dq reduce-adds):
+        // first each warp's dV block; then, once both warps of the row block
+        // have seen their dV blocks read, the dK rows of the block. The two
+        // warps of a row block (one per warpgroup) meet on pair[q4] four
+        // times per unit; their partial row dots pass through TMEM, each in
+        // the first dV column that its writer has already read.
         const int t = u.kt * TILE + r;
         const int j0 = 32 * ch;
         const bf16* krow = p.qkv + m * 3 * d + d + h * 128;
         const uint32_t tk = tdK + lane_off;
+        uint64_t* pb = pair + q4;
+        const int yblk = u.krow0 + 32 * q4;  // first row of this warp's block
         uint4 klo[4], khi[4];  // k_hat dims j0..j0+31 and 64+j0..64+j0+31
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           klo[q8] = __ldg(reinterpret_cast<const uint4*>(krow + j0) + q8);
           khi[q8] = __ldg(reinterpret_cast<const uint4*>(krow + 64 + j0) + q8);
+        }
+        const float rk = p.rqk[m * 2 * p.H + p.H + h];
+        // dV first: it needs no loads, so the k_hat row and rk arrive meanwhile
+        {
+          float a[32], bb[32];
+          tc::tmem_ld32x2(tdV + lane_off + 64 * ch, tdV + lane_off + 64 * ch + 32, a, bb);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {  // dV accumulated P' = P / sqrt(128)
+            a[i] *= kSqrt128;
+            bb[i] *= kSqrt128;
+          }
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            st_tile8(sdSt, r, 8 * ch + gq, pack8(a + 8 * gq));
+            st_tile8(sdSt, r, 8 * ch + 4 + gq, pack8(bb + 8 * gq));
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 1) {
+          tc::tma_store_2d(&tdkv, sdSt + ch * HALF_BYTES + q4 * 32 * 128, 2 * d + h * 128 + 64 * ch, yblk);
+          tc::bulk_commit();
         }
         float glo[32], ghi[32];
         tc::tmem_ld32x2(tk + j0, tk + 64 + j0, glo, ghi);
@@ -892,21 +937,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) part += glo[q8 * 8 + i] * k1[i] + ghi[q8 * 8 + i] * k2[i];
         }
-        float* mine = reinterpret_cast<float*>(sdSt + (1 - ch) * HALF_BYTES + r * 128);
-        const volatile float* other = reinterpret_cast<const volatile float*>(sdSt + ch * HALF_BYTES + r * 128);
-        *mine = part;
-        tc::mbar_arrive_warp(xch);
-        ok = tc::mbar_wait(xch, ul & 1, abort_flag, wait_ns);
+        tmem_st1(tdV + lane_off + 64 * ch, part);
+        tc::tc_fence_before();
+        tc::mbar_arrive_warp(pb);
+        ok = tc::mbar_wait(pb, 0, abort_flag, wait_ns);
         if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
-        const float po = *other;
+        tc::tc_fence_after();
+        const float po = tmem_ld1(tdV + lane_off + 64 * (1 - ch));
+        // every TMEM read of the unit is done: dV/dK may take the next unit's products
+        tc::tc_fence_before();
+        tc::mbar_arrive_warp(acc_free);
         const float dot = ch == 0 ? part + po : po + part;
-        const float rk = p.rqk[m * 2 * p.H + p.H + h];
         const float dmean = dot * (1.f / 128.f);
+        // the dK rows go where both warps' dV blocks were: once those are read
+        if (lane == 1) tc::bulk_wait_read();
+        __syncwarp();
+        tc::mbar_arrive_warp(pb);
+        ok = tc::mbar_wait(pb, 1, abort_flag, wait_ns);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
         // angle-major tables [16][T][4]: angles j0..j0+31 are groups j0/4..j0/4+7,
         // and the warp's 32 positions read 512 contiguous bytes per group
         const float4* cs4 = reinterpret_cast<const float4*>(p.rope_cos) + t;
         const float4* sn4 = reinterpret_cast<const float4*>(p.rope_sin) + t;
-        bf16* rowk = p.dqkv + m * 3 * d + d + h * 128;
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {  // 8 rotation pairs at a time
           const float4 ca = __ldg(cs4 + (size_t)(j0 / 4 + 2 * q8) * p.T);
@@ -924,24 +976,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             o1[i] = rk * (w1 * cc[i] + w2 * ss[i]);
             o2[i] = rk * (-w1 * ss[i] + w2 * cc[i]);
           }
-          *reinterpret_cast<uint4*>(rowk + j0 + q8 * 8) = pack8(o1);
-          *reinterpret_cast<uint4*>(rowk + 64 + j0 + q8 * 8) = pack8(o2);
+          st_tile8(sdSt, r, 4 * ch + q8, pack8(o1));       // dims j0 + 8 q8 .. (first half)
+          st_tile8(sdSt, r, 8 + 4 * ch + q8, pack8(o2));   // dims 64 + j0 + 8 q8 .. (second half)
         }
-        bf16* rowv = p.dqkv + m * 3 * d + 2 * d + h * 128 + 64 * ch;
-        {
-          float a[32], bb[32];
-          tc::tmem_ld32x2(tdV + lane_off + 64 * ch, tdV + lane_off + 64 * ch + 32, a, bb);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {  // dV accumulated P' = P / sqrt(128)
-            a[i] *= kSqrt128;
-            bb[i] *= kSqrt128;
-          }
-#pragma unroll
-          for (int gq = 0; gq < 4; ++gq) {
-            *reinterpret_cast<uint4*>(rowv + gq * 8) = pack8(a + 8 * gq);
-            *reinterpret_cast<uint4*>(rowv + 32 + gq * 8) = pack8(bb + 8 * gq);
-          }
+        fence_async_smem();
+        tc::mbar_arrive_warp(pb);
+        ok = tc::mbar_wait(pb, 0, abort_flag, wait_ns);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
+        if (ch == 0 && lane == 1) {
+          tc::tma_store_2d(&tdkv, sdSt + q4 * 32 * 128, d + h * 128, yblk);
+          tc::tma_store_2d(&tdkv, sdSt + HALF_BYTES + q4 * 32 * 128, d + h * 128 + 64, yblk);
+          tc::bulk_commit();
+          tc::bulk_wait_read();
         }
+        __syncwarp();
+        // the block's staging is read: the buffer may take the next dS^T
+        tc::mbar_arrive_warp(pb);
+        ok = tc::mbar_wait(pb, 1, abort_flag, wait_ns);
+        if (!__all_sync(0xffffffffu, ok)) { failed = true; break; }
       } else {
         float* dkrow = p.dk + m * d + h * 128 + ch * 64;
         bf16* dvrow = p.dqkv + m * 3 * d + 2 * d + h * 128 + ch * 64;
@@ -958,12 +1010,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
           for (int gq = 0; gq < 4; ++gq) *reinterpret_cast<uint4*>(dvrow + c * 32 + gq * 8) = pack8(w + 8 * gq);
         }
+        // dV/dK may take the next unit's products
+        tc::tc_fence_before();
+        tc::mbar_arrive_warp(acc_free);
       }
-      // dV/dK may take the next unit's products
-      tc::tc_fence_before();
-      tc::mbar_arrive_warp(acc_free);
     }
-    if (lane == 0) tc::bulk_wait_all();  // this warp's dQ reduce-adds have landed
+    if (lane <= 1) tc::bulk_wait_all();  // this warp's dQ reduce-adds and dK/dV stores have landed
     __syncwarp();
     if (failed) *abort_flag = 1;
   }
@@ -1068,6 +1120,19 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, c
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // dqkv bf16 [B*T, 3d]: 64-dim x 32-row boxes, 128-byte swizzle (the tile
+  // layout), for the k and v gradients of the fused QK-norm/RoPE path
+  CUtensorMap tdkv = tq;
+  if (rqk) {
+    cuuint64_t dims[2] = {3ull * H * 128, (uint64_t)B * T};
+    cuuint64_t strides[1] = {3ull * H * 128 * 2};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t es[2] = {1, 1};
+    if (g_enc(&tdkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, dqkv, dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
   AttnParams p{};
   p.B = B; p.T = T; p.H = H; p.nq = T / TILE;
   p.qkv = qkv;
@@ -1091,7 +1156,7 @@ cudaError_t attn_bwd_tc(const bf16* qkv, const bf16* dout, const float* L2row, c
     if (sms <= 0) sms = 148;
   }
   const int units = B * H * p.nq;
-  attn_bwd_tc_k<<<units < sms ? units : sms, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, tdq, p);
+  attn_bwd_tc_k<<<units < sms ? units : sms, BWD_THREADS, BWD_SMEM, s>>>(tq, tdo, tdq, tdkv, p);
   return cudaGetLastError();
 }
 
