@@ -89,9 +89,16 @@ cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long l
 template <typename T>
 cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int V, int* status,
                       cudaStream_t s);
+// dwte[tok[m]] += dx[m] (dwte zeroed first unless accumulating). With keys
+// (M uint32) and part (M x d fp32) scratch, the sum per id runs in ascending
+// position order with a fixed grouping (deterministic) when d % 4 == 0, the
+// position and id bit counts fit 32 bits and the sort fits kEmbSortSmem bytes
+// of shared memory; otherwise by float atomics.
+constexpr size_t kEmbSortSmem = 192 * 1024;
 template <typename T>
 cudaError_t embed_bwd(const int* tok, const T* dx_unused, const float* dx, float* dwte, int M,
-                      int d, int V, cudaStream_t s);
+                      int d, int V, cudaStream_t s, unsigned* keys = nullptr, float* part = nullptr);
+int embed_bwd_launches(int M, int d, int V, bool scratch);
 template <typename T>
 cudaError_t rmsnorm_fwd(const float* x, T* y, float* r, int M, int d, cudaStream_t s);
 // dx (f32) = (accumulate ? dx : 0) + r*(dy - y*mean(dy*y)); also dx_e = elem copy (if non-null)

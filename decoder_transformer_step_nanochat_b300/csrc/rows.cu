@@ -74,6 +74,131 @@ __global__ void embed_bwd_k(const int* __restrict__ tok, const float* __restrict
   }
 }
 
+// Deterministic embedding gradient, dwte[id] += sum of dx[m] over the
+// positions m holding id, in ascending m with a fixed grouping, so the
+// result does not depend on scheduling (float atomics would add in arrival
+// order). Three launches:
+//  1. embed_sort_k (one CTA): keys (id << mbits) | m, unique per position,
+//     bitonic-sorted in shared memory; out-of-range ids become the largest
+//     key and sort last. Sorted by key is sorted by (id, m).
+//  2. embed_piece_k: the sorted list is cut into pieces of kEmbPiece
+//     entries; a warp sums, for one piece and one 512-column block, the dx
+//     rows of each run of equal ids in order, and leaves the run's sum in
+//     part at the row of the run's first sorted entry in the piece.
+//  3. embed_gather_k: the warp of an id's first sorted entry adds the id's
+//     piece sums in piece order (its own, then the one at each later piece
+//     start the run still covers) into dwte[id].
+constexpr int kEmbPiece = 32;
+constexpr int kEmbCols = 512;  // columns per warp task: 4 float4 per lane
+constexpr unsigned kEmbNone = 0xffffffffu;
+
+__global__ void __launch_bounds__(1024) embed_sort_k(const int* __restrict__ tok, int M, int V, int mbits, int N,
+                                                     unsigned* __restrict__ keys) {
+  extern __shared__ unsigned sk[];
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    unsigned k = kEmbNone;
+    if (i < M) {
+      const int id = tok[i];
+      if (id >= 0 && id < V) k = ((unsigned)id << mbits) | (unsigned)i;
+    }
+    sk[i] = k;
+  }
+  __syncthreads();
+  for (int k = 2; k <= N; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < N / 2; i += blockDim.x) {
+        const int lo = ((i & ~(j - 1)) << 1) | (i & (j - 1)), hi = lo | j;
+        const unsigned a = sk[lo], b = sk[hi];
+        if ((a > b) == ((lo & k) == 0)) {  // ascending where bit k of lo is clear
+          sk[lo] = b;
+          sk[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  for (int i = threadIdx.x; i < M; i += blockDim.x) keys[i] = sk[i];
+}
+
+__device__ __forceinline__ void emb_add_row(float4* acc, const float* row, int c0, int d, int lane) {
+#pragma unroll
+  for (int q = 0; q < kEmbCols / 128; ++q) {
+    const int c = c0 + q * 128 + lane * 4;
+    if (c < d) {
+      const float4 v = ld4(row + c);
+      acc[q].x += v.x; acc[q].y += v.y; acc[q].z += v.z; acc[q].w += v.w;
+    }
+  }
+}
+__device__ __forceinline__ void emb_put_row(float* row, const float4* acc, int c0, int d, int lane) {
+#pragma unroll
+  for (int q = 0; q < kEmbCols / 128; ++q) {
+    const int c = c0 + q * 128 + lane * 4;
+    if (c < d) st4(row + c, acc[q]);
+  }
+}
+
+// warp task w = piece * ncb + column block
+__global__ void embed_piece_k(const unsigned* __restrict__ keys, const float* __restrict__ dx, float* __restrict__ part,
+                              int M, int d, int mbits, int ncb) {
+  const long long w = (long long)blockIdx.x * kRowWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  const long long tasks = (long long)((M + kEmbPiece - 1) / kEmbPiece) * ncb;
+  if (w >= tasks) return;
+  const int piece = (int)(w / ncb), c0 = (int)(w % ncb) * kEmbCols;
+  const int i0 = piece * kEmbPiece, i1 = min(M, i0 + kEmbPiece);
+  const unsigned mmask = (1u << mbits) - 1;
+  float4 acc[kEmbCols / 128];
+#pragma unroll
+  for (int q = 0; q < kEmbCols / 128; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int run = i0;
+  unsigned cur = keys[i0] == kEmbNone ? kEmbNone : keys[i0] >> mbits;
+  for (int i = i0; i < i1; ++i) {
+    const unsigned key = keys[i];
+    if (key == kEmbNone) break;  // the rest of the list is out-of-range ids
+    const unsigned id = key >> mbits;
+    if (id != cur) {  // a new run: leave the finished one's sum
+      emb_put_row(part + (size_t)run * d, acc, c0, d, lane);
+#pragma unroll
+      for (int q = 0; q < kEmbCols / 128; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+      run = i;
+      cur = id;
+    }
+    emb_add_row(acc, dx + (size_t)(key & mmask) * d, c0, d, lane);
+  }
+  if (cur != kEmbNone) emb_put_row(part + (size_t)run * d, acc, c0, d, lane);
+}
+
+// warp task w = sorted entry * ncb + column block; only an id's first entry works
+__global__ void embed_gather_k(const unsigned* __restrict__ keys, const float* __restrict__ part,
+                               float* __restrict__ dwte, int M, int d, int mbits, int ncb) {
+  const long long w = (long long)blockIdx.x * kRowWarps + threadIdx.x / 32;
+  const int lane = threadIdx.x & 31;
+  if (w >= (long long)M * ncb) return;
+  const int i = (int)(w / ncb), c0 = (int)(w % ncb) * kEmbCols;
+  const unsigned key = keys[i];
+  if (key == kEmbNone) return;
+  const unsigned id = key >> mbits;
+  if (i > 0 && (keys[i - 1] >> mbits) == id && keys[i - 1] != kEmbNone) return;
+  float4 acc[kEmbCols / 128];
+#pragma unroll
+  for (int q = 0; q < kEmbCols / 128; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  emb_add_row(acc, part + (size_t)i * d, c0, d, lane);
+  for (int q0 = (i / kEmbPiece + 1) * kEmbPiece; q0 < M; q0 += kEmbPiece) {
+    const unsigned kq = keys[q0];
+    if (kq == kEmbNone || (kq >> mbits) != id) break;  // the run ended before this piece
+    emb_add_row(acc, part + (size_t)q0 * d, c0, d, lane);
+  }
+  float* row = dwte + (size_t)id * d;
+#pragma unroll
+  for (int q = 0; q < kEmbCols / 128; ++q) {
+    const int c = c0 + q * 128 + lane * 4;
+    if (c < d) {
+      const float4 o = ld4(row + c);
+      st4(row + c, make_float4(o.x + acc[q].x, o.y + acc[q].y, o.z + acc[q].z, o.w + acc[q].w));
+    }
+  }
+}
+
 // y = x * r, r = 1/sqrt(mean(x^2) + eps).
 template <typename T>
 __global__ void rmsnorm_fwd_k(const float* __restrict__ x, T* __restrict__ y, float* __restrict__ r,
@@ -570,10 +695,52 @@ cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int 
   return cudaGetLastError();
 }
 
+namespace {
+struct EmbPlan {
+  int mbits, N;
+  bool sorted;
+};
+EmbPlan emb_plan(int M, int d, int V, bool scratch) {
+  EmbPlan pl;
+  int vbits = 1;
+  pl.mbits = 1;
+  while ((1LL << pl.mbits) < M) ++pl.mbits;
+  while ((1LL << vbits) < V) ++vbits;
+  pl.N = 1;
+  while (pl.N < M) pl.N <<= 1;
+  pl.sorted = scratch && d % 4 == 0 && pl.mbits + vbits <= 32 && (size_t)pl.N * 4 <= kEmbSortSmem;
+  return pl;
+}
+}  // namespace
+
+int embed_bwd_launches(int M, int d, int V, bool scratch) {
+  if (M == 0) return 0;
+  return emb_plan(M, d, V, scratch).sorted ? 3 : 1;
+}
+
 template <typename T>
 cudaError_t embed_bwd(const int* tok, const T*, const float* dx, float* dwte, int M, int d, int V,
-                      cudaStream_t s) {
-  embed_bwd_k<<<row_blocks(M), 32 * kRowWarps, 0, s>>>(tok, dx, dwte, M, d, V);
+                      cudaStream_t s, unsigned* keys, float* part) {
+  if (M == 0) return cudaSuccess;
+  const EmbPlan pl = emb_plan(M, d, V, keys && part);
+  const int mbits = pl.mbits, N = pl.N;
+  if (!pl.sorted) {  // float atomics: the summation order follows arrival
+    embed_bwd_k<<<row_blocks(M), 32 * kRowWarps, 0, s>>>(tok, dx, dwte, M, d, V);
+    return cudaGetLastError();
+  }
+  cudaError_t e = cudaFuncSetAttribute(embed_sort_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(N * 4));
+  if (e != cudaSuccess) return e;
+  embed_sort_k<<<1, 1024, (size_t)N * 4, s>>>(tok, M, V, mbits, N, keys);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int ncb = (d + kEmbCols - 1) / kEmbCols;
+  const long long pt = (long long)((M + kEmbPiece - 1) / kEmbPiece) * ncb;
+  embed_piece_k<<<(int)((pt + kRowWarps - 1) / kRowWarps), 32 * kRowWarps, 0, s>>>(keys, dx, part, M, d, mbits, ncb);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long gt = (long long)M * ncb;
+  embed_gather_k<<<(int)((gt + kRowWarps - 1) / kRowWarps), 32 * kRowWarps, 0, s>>>(keys, part, dwte, M, d, mbits,
+                                                                                    ncb);
   return cudaGetLastError();
 }
 
@@ -677,7 +844,7 @@ cudaError_t check_ids(const int* ids, int n, int lo, int V, int* status, cudaStr
   template cudaError_t embed_fwd<T>(const int*, const T*, float*, int, int, int, int*,          \
                                     cudaStream_t);                                               \
   template cudaError_t embed_bwd<T>(const int*, const T*, const float*, float*, int, int, int,  \
-                                    cudaStream_t);                                               \
+                                    cudaStream_t, unsigned*, float*);                            \
   template cudaError_t rmsnorm_fwd<T>(const float*, T*, float*, int, int, cudaStream_t);         \
   template cudaError_t rmsnorm_bwd<T>(const T*, const T*, const float*, float*, T*, int,         \
                                       int, int, cudaStream_t);                                   \

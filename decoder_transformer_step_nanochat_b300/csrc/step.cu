@@ -538,7 +538,9 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn1, r1, dx, dxe, M, d, 1, s));
   }
   if (!accumulate) CK(cudaMemsetAsync(G, 0, (size_t)V * d * sizeof(float), s));
-  KL(NC_FAM_ROWS, 8.0 * M * d + 4.0 * M, 1, embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s));
+  // deterministic scatter: sort keys in the D-row buffer, run sums in the dq/dk plane (both dead here)
+  KL(NC_FAM_ROWS, 8.0 * M * d + 4.0 * M, embed_bwd_launches(M, d, V, true),
+     embed_bwd<T>(tok, nullptr, dx, G, M, d, V, s, reinterpret_cast<unsigned*>(drow), dqk));
   return NC_OK;
 }
 
@@ -1221,8 +1223,9 @@ nc_status nc_op_embed_bwd(nc_ctx* c, const int32_t* tok, const float* dx, float*
   if (!tok || !dx || !dwte) return fail(NC_ERR_ARG, "null pointer argument");
   c->have_fwd = false;
   CK(cudaMemsetAsync(dwte, 0, (size_t)c->V * c->d * sizeof(float), c->stream));
-  KL(NC_FAM_ROWS, 8.0 * c->M * c->d + 4.0 * c->M, 1,
-     embed_bwd<bf16>(tok, nullptr, dx, dwte, c->M, c->d, c->V, c->stream));
+  KL(NC_FAM_ROWS, 8.0 * c->M * c->d + 4.0 * c->M, embed_bwd_launches(c->M, c->d, c->V, true),
+     embed_bwd<bf16>(tok, nullptr, dx, dwte, c->M, c->d, c->V, c->stream, wsp<unsigned>(c, c->off.drow),
+                     wsp<float>(c, c->off.dqk)));
   return NC_OK;
 }
 
