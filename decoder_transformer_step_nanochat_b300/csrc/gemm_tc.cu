@@ -65,6 +65,12 @@ struct TcParams {
   GemmArgs g;
   int num_m, num_n, num_kb, total;  // total = tiles * splits work units
   int splits, kb_per_split;
+  // k-splits added into C in split order inside the kernel (no partial slabs):
+  // split 0 stores (or adds, beta = 1), split s > 0 adds once the tile's
+  // counter shows every warp of splits 0..s-1 done; the counter of a 128-row
+  // tile is left at 0 by its last writer
+  int ordered;
+  int* tile_done;
 };
 
 // Work unit v of a CTA (CL = 1) or of a CTA pair (CL = 2: the two CTAs of a
@@ -209,6 +215,23 @@ struct Stager {
     }
   }
 };
+
+// Poll a tile counter (acquire, device scope) until it reaches target; gives
+// up like the pipeline waits (limit or abort flag).
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, volatile int* abort, uint64_t limit_ns) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  if (v >= target) return true;
+  const uint64_t t0 = tc::globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (limit_ns < 1000 || (it & 63) == 0) {
+      if (abort && *abort) return false;
+      if (tc::globaltimer() - t0 > limit_ns) return false;
+    }
+  }
+}
 
 __device__ __forceinline__ uint4 f4u(float a, float b, float c, float d) {
   return make_uint4(__float_as_uint(a), __float_as_uint(b), __float_as_uint(c), __float_as_uint(d));
@@ -458,6 +481,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int rblk = rblk_local + (int)(bt * g.c_brows);  // in the stacked output
         if (EPI == EPI_STORE_F32) {
           const bool direct = (p.splits == 1 && g.beta != 0.f && g.beta != 1.f);
+          int* ctr = p.ordered ? p.tile_done + (m0 / BM) * p.num_n + nb : nullptr;
+          if (p.ordered && split > 0) {
+            // the tile's earlier splits (all NEPI_WARPS warps each) are in C
+            bool got = true;
+            if (lane == 0) got = wait_count(ctr, split * NEPI_WARPS, abort_flag, wait_ns);
+            if (!__all_sync(0xffffffffu, __shfl_sync(0xffffffffu, got, 0))) { failed = true; *abort_flag = 1; break; }
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+          }
           for (int c = 0; c < 4; ++c) {
             float v[32];
             if (have_acc) tc::tmem_ld32(taddr + c * 32, v);
@@ -475,8 +506,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             stg.begin();
 #pragma unroll
             for (int j = 0; j < 8; ++j) stg.put(j, f4u(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-            if (p.splits > 1) stg.store3(&tc2, nc0, rblk, split);    // this split's partial slab
-            else stg.store(&tc_, nc0, rblk, g.beta == 1.f);          // C = acc, or C += acc
+            if (p.ordered) stg.store(&tc_, nc0, rblk, split > 0 || g.beta == 1.f);  // in split order
+            else if (p.splits > 1) stg.store3(&tc2, nc0, rblk, split);    // this split's partial slab
+            else stg.store(&tc_, nc0, rblk, g.beta == 1.f);               // C = acc, or C += acc
+          }
+          if (p.ordered) {
+            // this warp's part of the tile is in C: count it (the last writer resets the counter)
+            if (lane == 0) {
+              tc::bulk_wait_all();
+              asm volatile("fence.proxy.async.global;" ::: "memory");
+              __threadfence();
+              if (atomicAdd(ctr, 1) == p.splits * NEPI_WARPS - 1) atomicExch(ctr, 0);
+            }
+            __syncwarp();
           }
         } else {
           // bf16 outputs: two chunks of 64 columns
@@ -751,6 +793,13 @@ int max_clusters(KernFn fn) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// k-splits summed into C inside the kernel, in split order (see TcParams)
+bool split_in_kernel(const GemmArgs& g, int splits) {
+  if (splits < 2 || !g.tile_done || g.batch != 1 || (g.beta != 0.f && g.beta != 1.f)) return false;
+  const long long tiles = (long long)((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+  return tiles <= kGemmTileCap;
+}
+
 }  // namespace
 
 bool gemm_tc_supports(const GemmArgs& g) {
@@ -774,7 +823,7 @@ bool gemm_tc_supports(const GemmArgs& g) {
   }
   if (g.epi == EPI_AXPBY && (!g.C2 || g.ldc2 % 8 || !aligned16(g.C2))) return false;
   if (g.epi == EPI_CE_FWD) return g.p_max && g.p_sum && g.p_arg && g.p_tgt && g.row_i;
-  if (g.splits > 1 && (g.epi != EPI_STORE_F32 || !g.partial || g.N % 4)) return false;
+  if (g.splits > 1 && (g.epi != EPI_STORE_F32 || (!g.partial && !g.tile_done) || g.N % 4)) return false;
   if (g.ldc % 8 || !aligned16(g.C)) return false;
   if ((g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD) && (g.ldc2 % 8 || !aligned16(g.C2))) return false;
   if (g.epi == EPI_CE_BWD && (!g.row_f || !g.row_i)) return false;
@@ -813,9 +862,12 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   p.num_m = (g.M + BM - 1) / BM;
   p.num_n = (g.N + BN - 1) / BN;
   p.num_kb = (g.K + BK - 1) / BK;
-  p.splits = (g.splits > 1 && g.epi == EPI_STORE_F32 && g.partial) ? g.splits : 1;
+  p.splits = (g.splits > 1 && g.epi == EPI_STORE_F32 && (g.partial || g.tile_done)) ? g.splits : 1;
   p.kb_per_split = (p.num_kb + p.splits - 1) / p.splits;
-  if (p.splits > 1 && !make_partial_map(&tcm2, g.partial, g.N, g.M, p.splits)) return cudaErrorInvalidValue;
+  p.ordered = split_in_kernel(g, p.splits);
+  p.tile_done = p.ordered ? g.tile_done : nullptr;
+  if (p.splits > 1 && !p.ordered && !make_partial_map(&tcm2, g.partial, g.N, g.M, p.splits))
+    return cudaErrorInvalidValue;
   KernFn fn = CLn == 2 ? pick_kernel<2>(g.epi, !g.a_kmajor, !g.b_kmajor) : pick_kernel<1>(g.epi, !g.a_kmajor, !g.b_kmajor);
   if (!fn) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn), cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -845,8 +897,14 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
     fn<<<grid, NTHREADS, SMEM_BYTES, s>>>(ta, tb, tcm, tcm2, p);
     e = cudaGetLastError();
   }
-  if (e != cudaSuccess || p.splits == 1) return e;
+  if (e != cudaSuccess || p.splits == 1 || p.ordered) return e;
   return splitk_reduce(g.partial, p.splits, static_cast<float*>(g.C), g.ldc, g.M, g.N, g.beta, s);
+}
+
+int gemm_tc_launches(const GemmArgs& g) {
+  if (g.M == 0 || g.N == 0) return 0;
+  const int splits = (g.splits > 1 && g.epi == EPI_STORE_F32 && (g.partial || g.tile_done)) ? g.splits : 1;
+  return (splits > 1 && !split_in_kernel(g, splits)) ? 2 : 1;
 }
 
 // Choose k-splits for fp32-output GEMMs whose output tiles underfill the SMs

@@ -46,6 +46,10 @@ struct GemmArgs {
   // `partial` ([splits, M, N] fp32) and a reduction kernel forms C.
   int splits = 1;
   float* partial = nullptr;
+  // with tile_done (kGemmTileCap zeroed ints) and beta 0 or 1, the splits are
+  // instead added into C in split order inside the kernel (no partial slabs,
+  // no reduction launch); each launch leaves the counters at 0
+  int* tile_done = nullptr;
   // batched problems (EPI_STORE / EPI_AXPBY, M % 128 == 0 on the tensor
   // cores): `batch` independent GEMMs whose operands are stacked along their
   // outer (row) dimension; problem i reads A rows from i*a_brows, B rows from
@@ -67,6 +71,9 @@ template <typename T> cudaError_t gemm_simt(const GemmArgs& g, cudaStream_t s);
 // tcgen05 / TMEM / TMA GEMM for bf16 operands. Returns cudaErrorNotSupported
 // for shapes it cannot serve (the caller treats that as a hard error).
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s);
+constexpr int kGemmTileCap = 16384;  // 128 x 256 output tiles with an in-kernel split-K counter
+// launches gemm_tc makes for g: 2 when a split-K reduction kernel follows
+int gemm_tc_launches(const GemmArgs& g);
 bool gemm_tc_supports(const GemmArgs& g);
 
 // Weight-streaming product of the decode step: C (fp32) = alpha * A W^T (+ beta * C)
@@ -92,9 +99,9 @@ cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int 
 // dwte[tok[m]] += dx[m] (dwte zeroed first unless accumulating). With keys
 // (M uint32) and part (M x d fp32) scratch, the sum per id runs in ascending
 // position order with a fixed grouping (deterministic) when d % 4 == 0, the
-// position and id bit counts fit 32 bits and the sort fits kEmbSortSmem bytes
-// of shared memory; otherwise by float atomics.
-constexpr size_t kEmbSortSmem = 192 * 1024;
+// position and id bit counts fit 32 bits and M <= 1024 * kEmbMaxChunks;
+// otherwise by float atomics.
+constexpr int kEmbMaxChunks = 1024;
 template <typename T>
 cudaError_t embed_bwd(const int* tok, const T* dx_unused, const float* dx, float* dwte, int M,
                       int d, int V, cudaStream_t s, unsigned* keys = nullptr, float* part = nullptr);

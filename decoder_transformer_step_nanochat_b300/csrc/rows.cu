@@ -78,45 +78,88 @@ __global__ void embed_bwd_k(const int* __restrict__ tok, const float* __restrict
 // positions m holding id, in ascending m with a fixed grouping, so the
 // result does not depend on scheduling (float atomics would add in arrival
 // order). Three launches:
-//  1. embed_sort_k (one CTA): keys (id << mbits) | m, unique per position,
-//     bitonic-sorted in shared memory; out-of-range ids become the largest
-//     key and sort last. Sorted by key is sorted by (id, m).
+//  1. keys (id << mbits) | m, unique per position, sorted: chunks of 1024
+//     positions in shared memory, then each key placed by its rank across
+//     the chunks; out-of-range ids become the largest key and are dropped.
+//     Sorted by key is sorted by (id, m).
 //  2. embed_piece_k: the sorted list is cut into pieces of kEmbPiece
 //     entries; a warp sums, for one piece and one 512-column block, the dx
 //     rows of each run of equal ids in order, and leaves the run's sum in
 //     part at the row of the run's first sorted entry in the piece.
-//  3. embed_gather_k: the warp of an id's first sorted entry adds the id's
-//     piece sums in piece order (its own, then the one at each later piece
-//     start the run still covers) into dwte[id].
+//  3. embed_gather_k: the warps of an id's first sorted entry (one per 128
+//     columns) add the id's piece sums in piece order (its own, then the one
+//     at each later piece start the run still covers) into dwte[id].
 constexpr int kEmbPiece = 32;
 constexpr int kEmbCols = 512;  // columns per warp task: 4 float4 per lane
 constexpr unsigned kEmbNone = 0xffffffffu;
 
-__global__ void __launch_bounds__(1024) embed_sort_k(const int* __restrict__ tok, int M, int V, int mbits, int N,
-                                                     unsigned* __restrict__ keys) {
-  extern __shared__ unsigned sk[];
-  for (int i = threadIdx.x; i < N; i += blockDim.x) {
-    unsigned k = kEmbNone;
-    if (i < M) {
-      const int id = tok[i];
-      if (id >= 0 && id < V) k = ((unsigned)id << mbits) | (unsigned)i;
-    }
-    sk[i] = k;
+// 1a. each CTA sorts one chunk of kEmbChunk consecutive positions' keys
+// (bitonic network in shared memory, one key per thread)
+constexpr int kEmbChunk = 1024;
+constexpr size_t kEmbRankSmem = 192 * 1024;  // the rank pass stages up to 48 sorted chunks
+__global__ void __launch_bounds__(kEmbChunk) embed_sort_chunk_k(const int* __restrict__ tok, int M, int V, int mbits,
+                                                               unsigned* __restrict__ chunks) {
+  __shared__ unsigned sk[kEmbChunk];
+  const int i = threadIdx.x;
+  const int m = blockIdx.x * kEmbChunk + i;
+  unsigned key = kEmbNone;
+  if (m < M) {
+    const int id = tok[m];
+    if (id >= 0 && id < V) key = ((unsigned)id << mbits) | (unsigned)m;
   }
+  sk[i] = key;
   __syncthreads();
-  for (int k = 2; k <= N; k <<= 1)
+  for (int k = 2; k <= kEmbChunk; k <<= 1)
     for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < N / 2; i += blockDim.x) {
-        const int lo = ((i & ~(j - 1)) << 1) | (i & (j - 1)), hi = lo | j;
-        const unsigned a = sk[lo], b = sk[hi];
-        if ((a > b) == ((lo & k) == 0)) {  // ascending where bit k of lo is clear
-          sk[lo] = b;
-          sk[hi] = a;
+      const int pj = i ^ j;
+      if (pj > i) {
+        const unsigned a = sk[i], b = sk[pj];
+        if ((a > b) == ((i & k) == 0)) {  // ascending where bit k of i is clear
+          sk[i] = b;
+          sk[pj] = a;
         }
       }
       __syncthreads();
     }
-  for (int i = threadIdx.x; i < M; i += blockDim.x) keys[i] = sk[i];
+  chunks[(size_t)blockIdx.x * kEmbChunk + i] = sk[i];
+}
+
+// 1b. a key's place in the whole sorted list is its index in its sorted chunk
+// plus, for every other chunk, the number of that chunk's keys below it
+// (binary search); the keys are unique, so the places are a permutation.
+// keys[] beyond the valid keys must hold kEmbNone already.
+template <bool SMEM>
+__global__ void __launch_bounds__(1024) embed_rank_k(const unsigned* __restrict__ chunks, int nchunks,
+                                                     unsigned* __restrict__ keys) {
+  extern __shared__ unsigned sc[];  // every sorted chunk, when they fit
+  const unsigned* src = chunks;
+  if (SMEM) {
+    for (int i = threadIdx.x; i < nchunks * kEmbChunk; i += blockDim.x) sc[i] = chunks[i];
+    __syncthreads();
+    src = sc;
+  }
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= nchunks * kEmbChunk) return;
+  const unsigned key = src[e];
+  if (key == kEmbNone) return;
+  const int c = e / kEmbChunk;
+  int rank = e - c * kEmbChunk;
+  for (int c2 = 0; c2 < nchunks; ++c2) {
+    if (c2 == c) continue;
+    const unsigned* s = src + (size_t)c2 * kEmbChunk;
+    int lo = 0, n = kEmbChunk;  // first index with s[index] >= key
+    while (n > 0) {
+      const int h = n >> 1;
+      if (s[lo + h] < key) {
+        lo += h + 1;
+        n -= h + 1;
+      } else {
+        n = h;
+      }
+    }
+    rank += lo;
+  }
+  keys[rank] = key;
 }
 
 __device__ __forceinline__ void emb_add_row(float4* acc, const float* row, int c0, int d, int lane) {
@@ -168,34 +211,46 @@ __global__ void embed_piece_k(const unsigned* __restrict__ keys, const float* __
   if (cur != kEmbNone) emb_put_row(part + (size_t)run * d, acc, c0, d, lane);
 }
 
-// warp task w = sorted entry * ncb + column block; only an id's first entry works
+// warp task w = sorted entry * ncg + 128-column group; only an id's first
+// entry works. The piece starts the run still covers are checked 32 at a
+// time (one per lane); their sums are then added in piece order, 16 rows'
+// loads in flight before the adds (a long run of a frequent id would
+// otherwise be a chain of dependent loads).
+constexpr int kEmbGatherRows = 16;
 __global__ void embed_gather_k(const unsigned* __restrict__ keys, const float* __restrict__ part,
-                               float* __restrict__ dwte, int M, int d, int mbits, int ncb) {
+                               float* __restrict__ dwte, int M, int d, int mbits, int ncg) {
   const long long w = (long long)blockIdx.x * kRowWarps + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
-  if (w >= (long long)M * ncb) return;
-  const int i = (int)(w / ncb), c0 = (int)(w % ncb) * kEmbCols;
+  if (w >= (long long)M * ncg) return;
+  const int i = (int)(w / ncg);
+  const int c = (int)(w % ncg) * 128 + lane * 4;
   const unsigned key = keys[i];
   if (key == kEmbNone) return;
   const unsigned id = key >> mbits;
   if (i > 0 && (keys[i - 1] >> mbits) == id && keys[i - 1] != kEmbNone) return;
-  float4 acc[kEmbCols / 128];
+  const bool col = c < d;
+  float4 acc = col ? ld4(part + (size_t)i * d + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = (i / kEmbPiece + 1) * kEmbPiece; q0 < M; q0 += 32 * kEmbPiece) {
+    const int q = q0 + lane * kEmbPiece;
+    const unsigned kq = q < M ? keys[q] : kEmbNone;
+    const unsigned same = __ballot_sync(0xffffffffu, kq != kEmbNone && (kq >> mbits) == id);
+    const int n = same == 0xffffffffu ? 32 : __ffs(~same) - 1;  // the run is contiguous
+    for (int t0 = 0; t0 < n; t0 += kEmbGatherRows) {
+      if (!col) continue;
+      float4 r[kEmbGatherRows];
 #pragma unroll
-  for (int q = 0; q < kEmbCols / 128; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  emb_add_row(acc, part + (size_t)i * d, c0, d, lane);
-  for (int q0 = (i / kEmbPiece + 1) * kEmbPiece; q0 < M; q0 += kEmbPiece) {
-    const unsigned kq = keys[q0];
-    if (kq == kEmbNone || (kq >> mbits) != id) break;  // the run ended before this piece
-    emb_add_row(acc, part + (size_t)q0 * d, c0, d, lane);
-  }
-  float* row = dwte + (size_t)id * d;
+      for (int t = 0; t < kEmbGatherRows; ++t)  // rows past the run repeat its last one (not added)
+        r[t] = ld4(part + (size_t)(q0 + min(t0 + t, n - 1) * kEmbPiece) * d + c);
 #pragma unroll
-  for (int q = 0; q < kEmbCols / 128; ++q) {
-    const int c = c0 + q * 128 + lane * 4;
-    if (c < d) {
-      const float4 o = ld4(row + c);
-      st4(row + c, make_float4(o.x + acc[q].x, o.y + acc[q].y, o.z + acc[q].z, o.w + acc[q].w));
+      for (int t = 0; t < kEmbGatherRows; ++t)
+        if (t0 + t < n) { acc.x += r[t].x; acc.y += r[t].y; acc.z += r[t].z; acc.w += r[t].w; }
     }
+    if (n < 32) break;
+  }
+  if (col) {
+    float* row = dwte + (size_t)id * d + c;
+    const float4 o = ld4(row);
+    st4(row, make_float4(o.x + acc.x, o.y + acc.y, o.z + acc.z, o.w + acc.w));
   }
 }
 
@@ -697,7 +752,7 @@ cudaError_t embed_fwd(const int* tok, const T* wte, float* x, int M, int d, int 
 
 namespace {
 struct EmbPlan {
-  int mbits, N;
+  int mbits, nchunks;
   bool sorted;
 };
 EmbPlan emb_plan(int M, int d, int V, bool scratch) {
@@ -706,16 +761,15 @@ EmbPlan emb_plan(int M, int d, int V, bool scratch) {
   pl.mbits = 1;
   while ((1LL << pl.mbits) < M) ++pl.mbits;
   while ((1LL << vbits) < V) ++vbits;
-  pl.N = 1;
-  while (pl.N < M) pl.N <<= 1;
-  pl.sorted = scratch && d % 4 == 0 && pl.mbits + vbits <= 32 && (size_t)pl.N * 4 <= kEmbSortSmem;
+  pl.nchunks = (M + kEmbChunk - 1) / kEmbChunk;
+  pl.sorted = scratch && d % 4 == 0 && pl.mbits + vbits <= 32 && pl.nchunks <= kEmbMaxChunks;
   return pl;
 }
 }  // namespace
 
 int embed_bwd_launches(int M, int d, int V, bool scratch) {
   if (M == 0) return 0;
-  return emb_plan(M, d, V, scratch).sorted ? 3 : 1;
+  return emb_plan(M, d, V, scratch).sorted ? 4 : 1;
 }
 
 template <typename T>
@@ -723,14 +777,26 @@ cudaError_t embed_bwd(const int* tok, const T*, const float* dx, float* dwte, in
                       cudaStream_t s, unsigned* keys, float* part) {
   if (M == 0) return cudaSuccess;
   const EmbPlan pl = emb_plan(M, d, V, keys && part);
-  const int mbits = pl.mbits, N = pl.N;
+  const int mbits = pl.mbits, nch = pl.nchunks;
   if (!pl.sorted) {  // float atomics: the summation order follows arrival
     embed_bwd_k<<<row_blocks(M), 32 * kRowWarps, 0, s>>>(tok, dx, dwte, M, d, V);
     return cudaGetLastError();
   }
-  cudaError_t e = cudaFuncSetAttribute(embed_sort_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(N * 4));
+  // the sorted chunks sit in part (dead until the run sums), keys fill from kEmbNone
+  unsigned* chunks = reinterpret_cast<unsigned*>(part);
+  cudaError_t e = cudaMemsetAsync(keys, 0xff, (size_t)M * sizeof(unsigned), s);
   if (e != cudaSuccess) return e;
-  embed_sort_k<<<1, 1024, (size_t)N * 4, s>>>(tok, M, V, mbits, N, keys);
+  embed_sort_chunk_k<<<nch, kEmbChunk, 0, s>>>(tok, M, V, mbits, chunks);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const size_t rank_smem = (size_t)nch * kEmbChunk * sizeof(unsigned);
+  if (rank_smem <= kEmbRankSmem) {
+    e = cudaFuncSetAttribute(embed_rank_k<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kEmbRankSmem);
+    if (e != cudaSuccess) return e;
+    embed_rank_k<true><<<nch, kEmbChunk, rank_smem, s>>>(chunks, nch, keys);
+  } else {
+    embed_rank_k<false><<<nch, kEmbChunk, 0, s>>>(chunks, nch, keys);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int ncb = (d + kEmbCols - 1) / kEmbCols;
@@ -738,9 +804,10 @@ cudaError_t embed_bwd(const int* tok, const T*, const float* dx, float* dwte, in
   embed_piece_k<<<(int)((pt + kRowWarps - 1) / kRowWarps), 32 * kRowWarps, 0, s>>>(keys, dx, part, M, d, mbits, ncb);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const long long gt = (long long)M * ncb;
+  const int ncg = (d + 127) / 128;
+  const long long gt = (long long)M * ncg;
   embed_gather_k<<<(int)((gt + kRowWarps - 1) / kRowWarps), 32 * kRowWarps, 0, s>>>(keys, part, dwte, M, d, mbits,
-                                                                                    ncb);
+                                                                                    ncg);
   return cudaGetLastError();
 }
 

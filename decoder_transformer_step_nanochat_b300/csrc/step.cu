@@ -82,6 +82,7 @@ struct nc_ctx {
   float* dec_rope = nullptr;   // decode RoPE table for dec_rope_len positions: cos [len][64] then sin
   int dec_rope_len = 0;
   int* status = nullptr;    // device status word
+  int* tile_done = nullptr;  // kGemmTileCap split-K tile counters of the GEMM (0 between launches)
   // workspace
   char* ws = nullptr;
   size_t ws_bytes = 0, ws_need = 0;
@@ -282,6 +283,8 @@ nc_status read_status(nc_ctx* c) {
   CK(cudaStreamSynchronize(c->stream));
   if (st == DEV_OK) return NC_OK;
   CK(cudaMemsetAsync(c->status, 0, sizeof(int), c->stream));
+  // a GEMM that gave up may have left split-K tile counters part-way
+  if (st == DEV_TIMEOUT && c->tile_done) CK(cudaMemsetAsync(c->tile_done, 0, kGemmTileCap * sizeof(int), c->stream));
   CK(cudaStreamSynchronize(c->stream));
   if (st == DEV_TIMEOUT) return fail(NC_ERR_TIMEOUT, "a device pipeline wait exceeded its iteration limit");
   if (st == DEV_BAD_TOKEN) return fail(NC_ERR_DEVICE, "a token or target id is outside [0, vocab)");
@@ -303,6 +306,7 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
       if (sp > 1 && (size_t)sp * g.M * g.N * 4 <= c->partial_bytes) {
         g.splits = sp;
         g.partial = wsp<float>(c, c->off.partial);
+        g.tile_done = c->tile_done;  // in-kernel ordered reduction where it applies
       }
     }
     if (!gemm_tc_supports(g))
@@ -312,7 +316,8 @@ nc_status gemm(nc_ctx* c, GemmArgs g) {
     e = gemm_simt<bf16>(g, c->stream);
   }
   if (e != cudaSuccess) return fail(NC_ERR_CUDA, "gemm M=%d N=%d K=%d epi=%d: %s", g.M, g.N, g.K, g.epi, cudaGetErrorString(e));
-  int n = (g.M > 0 && g.N > 0) ? (g.splits > 1 ? 2 : 1) : 0;  // split-K adds its reduction kernel
+  // a split-K reduction kernel, where one follows, counts as a second launch
+  int n = c->use_tc && c->prec != NC_FP32_DEBUG ? gemm_tc_launches(g) : ((g.M > 0 && g.N > 0) ? 1 : 0);
   // decode GEMMs stream their weights: their work is counted in bytes
   const double work = c->gemm_fam == NC_FAM_DEC_GEMM ? (double)g.N * g.K * c->esz
                                                      : 2.0 * g.M * g.N * (double)g.K * g.batch;
@@ -879,8 +884,11 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   if (c->status && c->device >= 0 && c->device != dev) {
     cudaFree(c->status);
     c->status = nullptr;
+    if (c->tile_done) cudaFree(c->tile_done);
+    c->tile_done = nullptr;
   }
   if (!c->status) CK(cudaMalloc(&c->status, 16 * sizeof(int)));
+  if (!c->tile_done) CK(cudaMalloc(&c->tile_done, kGemmTileCap * sizeof(int)));
   // RoPE table: angle pos * 10000^(-j/64) formed in float64, stored fp32.
   // Also stored angle-major in groups of four angles, [16][T][4], for the
   // epilogues whose threads each own one position: consecutive threads then
@@ -906,6 +914,7 @@ nc_status nc_configure(nc_ctx* c, int batch, int precision, void* stream) {
   CK(cudaMemcpyAsync(c->rope_cos4, hc4.data(), hc4.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemcpyAsync(c->rope_sin4, hs4.data(), hs4.size() * sizeof(float), cudaMemcpyHostToDevice, c->stream));
   CK(cudaMemsetAsync(c->status, 0, 16 * sizeof(int), c->stream));
+  CK(cudaMemsetAsync(c->tile_done, 0, kGemmTileCap * sizeof(int), c->stream));
   CK(cudaStreamSynchronize(c->stream));
   c->device = dev;
   c->sms = prop.multiProcessorCount > 0 ? prop.multiProcessorCount : 148;
@@ -1099,6 +1108,7 @@ void nc_destroy(nc_ctx* c) {
   if (c->rope_sin4) cudaFree(c->rope_sin4);
   if (c->dec_rope) cudaFree(c->dec_rope);
   if (c->status) cudaFree(c->status);
+  if (c->tile_done) cudaFree(c->tile_done);
   delete c;
 }
 

@@ -139,17 +139,20 @@ def test_gemm_degenerate_sizes(nc, prec):
         c.close()
 
 
+@pytest.mark.parametrize("beta", [0.5, 0.0, 1.0], ids=["beta_half", "beta0", "beta1"])
 @pytest.mark.parametrize("ak,bk", [(0, 0), (1, 0)], ids=["MN_ab", "NN_b"])
-def test_gemm_split_k_weight_gradient_shape(nc, ak, bk):
+def test_gemm_split_k_weight_gradient_shape(nc, ak, bk, beta):
     # few output tiles and a long K (the weight-gradient shape): the library
-    # splits K into partial sums and reduces them in a fixed order
+    # splits K into partial sums and adds them in a fixed order (with beta 0
+    # or 1 inside the kernel, split after split; otherwise by a reduction
+    # kernel over partial slabs)
     import torch
     M, N, K = 256, 264, 4160
     rng = np.random.default_rng(31 + ak)
     A = rounded(rng.standard_normal((M, K)) * 0.5, 0)
     Bm = rounded(rng.standard_normal((N, K)) * 0.5, 0)
     C0 = rng.standard_normal((M, N)).astype(np.float32)
-    ref = 0.25 * (A.astype(np.float64) @ Bm.astype(np.float64).T) + 0.5 * C0
+    ref = 0.25 * (A.astype(np.float64) @ Bm.astype(np.float64).T) + beta * C0
     c = Ctx(nc, 1, 128, 1, 128, 1024, 1, 0)
     try:
         dA = torch_of(A if ak else np.ascontiguousarray(A.T), 0, nc)
@@ -158,7 +161,7 @@ def test_gemm_split_k_weight_gradient_shape(nc, ak, bk):
         for _ in range(2):
             C = torch.from_numpy(C0.copy()).cuda()
             nc.nc_op_gemm(c.ctx, M, N, K, dA.data_ptr(), K if ak else M, ak, dB.data_ptr(), K if bk else N, bk,
-                          1, 0.25, 0.5, C.data_ptr(), N)
+                          1, 0.25, beta, C.data_ptr(), N)
             nc.nc_sync(c.ctx)
             outs.append(C.cpu().numpy())
         ok, err = close_enough(outs[0], ref, 1, rel_f32=5e-5)
