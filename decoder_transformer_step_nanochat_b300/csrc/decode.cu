@@ -148,6 +148,17 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   const float* qrow = qkv + (size_t)b * 3 * d + h * 128 + lane * 4;
   T* Kb = K + ((size_t)b * H + h) * max_len * 128 + lane * 4;
   T* Vb = Vc + ((size_t)b * H + h) * max_len * 128 + lane * 4;
+  const int t0 = c * chunk, t1 = min(t0 + chunk, pos + 1);
+  {
+    // the cache rows of this warp's first two rounds start towards L2 while
+    // q_hat (and, in the last chunk, k_hat and v) are formed: one line per lane
+    const int t = t0 + warp * 4 + (lane & 3) + ((lane >> 4) & 1) * 4 * kDecWarps;
+    const size_t off = (size_t)t * 128 * sizeof(T) + ((lane >> 2) & 1) * 128;
+    if (t < t1 && off < 128 * sizeof(T) * (size_t)(t + 1)) {
+      const char* base = reinterpret_cast<const char*>((lane & 8) ? Vb - lane * 4 : Kb - lane * 4);
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(base + off));
+    }
+  }
   if (c == n_act - 1) {  // this chunk holds pos: append the token's k_hat and v
     if (warp == 0) st4e(Kb + (size_t)pos * 128, head_norm_rope(ld4e(qrow + d), rc, rs, pos, lane));
     else if (warp == 1) st4e(Vb + (size_t)pos * 128, ld4e(qrow + 2 * d));
@@ -156,7 +167,6 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   const float sc = kLog2eD * rsqrtf(128.f);
   float4 q = as_elem(head_norm_rope(ld4e(qrow), rc, rs, pos, lane), static_cast<const T*>(nullptr));
   q.x *= sc; q.y *= sc; q.z *= sc; q.w *= sc;
-  const int t0 = c * chunk, t1 = min(t0 + chunk, pos + 1);
   float m = -INFINITY, l = 0.f;
   float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
   // this warp's positions: t0 + warp*4 + 16*i + u, u in 0..3

@@ -84,13 +84,18 @@ bool gemm_tc_supports(const GemmArgs& g);
 // stride ldc) and C is not touched. K longer than 2048 runs in k-ranges whose
 // partial sums need part (skinny_scratch_floats(N, K) floats) and cnt
 // (skinny_counters(N) ints, 0 before the first call; each call leaves them 0).
-// A wait past its limit sets DEV_TIMEOUT in *status.
+// A wait past its limit sets DEV_TIMEOUT in *status. With xres (fp32 [M, K],
+// row stride lda) the kernel forms A itself as bf16(xres * r), r the row's
+// RMSNorm scale 1/sqrt(mean(xres^2) + eps) (the sum of squares in another
+// order than rmsnorm_fwd's), when skinny_gemm_norm_ok(N, K).
 bool skinny_gemm_supports(int M, int N, int K, long long lda, long long ldw, const void* A, const void* W);
 size_t skinny_scratch_floats(int N, int K);
+// xres (the fused RMSNorm) needs the whole row in one k-range: K <= 2048
+bool skinny_gemm_norm_ok(int N, int K);
 int skinny_counters(int N);
 cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
                         int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2, float* part,
-                        int* cnt, int* status);
+                        int* cnt, int* status, const float* xres = nullptr);
 
 // ------------------------------------------------------------------ rows
 template <typename T>

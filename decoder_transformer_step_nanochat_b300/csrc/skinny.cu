@@ -41,6 +41,7 @@ constexpr uint64_t kSkWaitNs = 2000000000ull;
 
 struct SkParams {
   const bf16* A;
+  const float* xres;  // if set, A = bf16(xres * r) with r the row's RMSNorm scale (A unused)
   const bf16* W;
   float* C;
   bf16* relu2;
@@ -60,6 +61,14 @@ __device__ __forceinline__ void mma16816(float* d, const uint32_t* a, const uint
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// eight fp32 values times a scale, as packed bf16
+__device__ __forceinline__ uint4 pack8s(const float* v, float r) {
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(v[0] * r, v[1] * r), h1 = __floats2bfloat162_rn(v[2] * r, v[3] * r);
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[4] * r, v[5] * r), h3 = __floats2bfloat162_rn(v[6] * r, v[7] * r);
+  return make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                    *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
 }
 
 // the output value as stored: fp32 C (alpha, beta) or bf16 relu(alpha v)^2
@@ -94,6 +103,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) skinny_gemm_k(const SkParams p)
   float* red = reinterpret_cast<float*>(smem + (size_t)p.ns * p.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)p.ns * p.stage_bytes + SK_RED_BYTES);
   __shared__ int s_last;
+  __shared__ float s_ss[SK_WARPS][16];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int first = blockIdx.x, step = gridDim.x;
@@ -112,6 +122,58 @@ __global__ void __launch_bounds__(SK_THREADS, 1) skinny_gemm_k(const SkParams p)
   int a_kr = -1;
   const bool a0ok = g < p.M, a1ok = g + 8 < p.M;
   const uint4 zero = make_uint4(0, 0, 0, 0);
+  if (p.xres) {
+    // A = bf16(x r), r = 1/sqrt(mean(x^2) + eps) per row, from the fp32
+    // residual rows (one k-range covers the row): each warp loads its
+    // chunks' x once, the rows' sums of squares are added warp by warp in
+    // warp order through shared memory, then the fragments are scaled
+    float xf[SK_KCH][2][8];
+    float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < SK_KCH; ++u) {
+      const int c = warp + SK_WARPS * u;
+      const bool in = c * 32 < p.K;
+      const size_t k = (size_t)c * 32 + 8 * t;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const bool ok = in && (h ? a1ok : a0ok);
+        const float* xr = p.xres + (size_t)(g + 8 * h) * p.lda + k;
+        const float4 lo = ok ? *reinterpret_cast<const float4*>(xr) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 hi = ok ? *reinterpret_cast<const float4*>(xr + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xf[u][h][0] = lo.x; xf[u][h][1] = lo.y; xf[u][h][2] = lo.z; xf[u][h][3] = lo.w;
+        xf[u][h][4] = hi.x; xf[u][h][5] = hi.y; xf[u][h][6] = hi.z; xf[u][h][7] = hi.w;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < SK_KCH; ++u)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        ss0 += xf[u][0][e] * xf[u][0][e];
+        ss1 += xf[u][1][e] * xf[u][1][e];
+      }
+    ss0 += __shfl_xor_sync(0xffffffffu, ss0, 1);
+    ss1 += __shfl_xor_sync(0xffffffffu, ss1, 1);
+    ss0 += __shfl_xor_sync(0xffffffffu, ss0, 2);
+    ss1 += __shfl_xor_sync(0xffffffffu, ss1, 2);
+    if (t == 0) {
+      s_ss[warp][g] = ss0;
+      s_ss[warp][g + 8] = ss1;
+    }
+    __syncthreads();
+    float tot0 = 0.f, tot1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < SK_WARPS; ++w) {
+      tot0 += s_ss[w][g];
+      tot1 += s_ss[w][g + 8];
+    }
+    const float r0 = rsqrtf(tot0 / (float)p.K + kEps), r1 = rsqrtf(tot1 / (float)p.K + kEps);
+#pragma unroll
+    for (int u = 0; u < SK_KCH; ++u) {
+      af[u][0] = pack8s(xf[u][0], r0);
+      af[u][1] = pack8s(xf[u][1], r1);
+    }
+    a_kr = 0;
+  }
   int it = 0;
   for (int i = first; i < p.items; i += step, ++it) {
     const int s = it % p.ns;
@@ -247,14 +309,17 @@ size_t skinny_scratch_floats(int N, int K) {
 
 int skinny_counters(int N) { return (N + SK_CW - 1) / SK_CW; }
 
+bool skinny_gemm_norm_ok(int N, int K) { return sk_shape(N, K, K).nks == 1; }
+
 cudaError_t skinny_gemm(const bf16* A, long long lda, const bf16* W, long long ldw, float* C, long long ldc, int M,
                         int N, int K, float alpha, float beta, int sms, cudaStream_t s, bf16* relu2, float* part,
-                        int* cnt, int* status) {
+                        int* cnt, int* status, const float* xres) {
   const SkShape sh = sk_shape(N, K, ldw);
   if (sh.ns < 1) return cudaErrorNotSupported;
   if (sh.nks > 1 && (!part || !cnt)) return cudaErrorInvalidValue;
+  if (xres && sh.nks > 1) return cudaErrorNotSupported;  // the row norm needs the whole row in one k-range
   SkParams p;
-  p.A = A; p.W = W; p.C = C; p.relu2 = relu2; p.part = part; p.cnt = cnt; p.status = status;
+  p.A = A; p.xres = xres; p.W = W; p.C = C; p.relu2 = relu2; p.part = part; p.cnt = cnt; p.status = status;
   p.lda = lda; p.ldw = ldw; p.ldc = ldc;
   p.M = M; p.N = N; p.K = K; p.alpha = alpha; p.beta = beta;
   p.ncb = sh.ncb; p.nks = sh.nks; p.KC = sh.KC; p.items = sh.ncb * sh.nks;

@@ -696,20 +696,26 @@ KvLayout kv_layout(const nc_ctx* c, int max_len) {
 // in weight bytes streamed.
 // With relu2 given the product leaves as relu2 = relu(A W^T)^2 (elem [B, N]):
 // fused into the weight-streaming kernel, else through C and a row kernel.
-// kv: the KV cache buffer, whose scratch holds the weight-streaming kernel's
-// k-range partial sums and counters.
+// With xres given (the fp32 residual rows), A is their RMSNorm: formed inside
+// the weight-streaming kernel, else written to A by the row kernel first (r
+// receives the row scales). kv: the KV cache buffer, whose scratch holds the
+// weight-streaming kernel's k-range partial sums and counters.
 template <typename T>
 nc_status dec_gemm(nc_ctx* c, char* kv, const KvLayout& kl, int N, int K, const T* A, const T* W, float* C,
-                   float beta, T* relu2 = nullptr) {
+                   float beta, T* relu2 = nullptr, const float* xres = nullptr, float* r = nullptr) {
   const int Bn = c->B;
   if constexpr (sizeof(T) == 2) {
-    if (skinny_gemm_supports(Bn, N, K, K, K, A, W)) {
+    if (skinny_gemm_supports(Bn, N, K, K, K, A, W) &&
+        (!xres || ((reinterpret_cast<uintptr_t>(xres) & 15) == 0 && skinny_gemm_norm_ok(N, K)))) {
       KL(NC_FAM_DEC_GEMM, (double)N * K * sizeof(T), 1,
          skinny_gemm(A, K, W, K, C, N, Bn, N, K, 1.f, beta, c->sms, c->stream, relu2,
-                     reinterpret_cast<float*>(kv + kl.skp), reinterpret_cast<int*>(kv + kl.skc), c->status));
+                     reinterpret_cast<float*>(kv + kl.skp), reinterpret_cast<int*>(kv + kl.skc), c->status, xres));
       return NC_OK;
     }
   }
+  if (xres)
+    KL(NC_FAM_DEC_ROWS, (double)Bn * K * (4 + c->esz), 1,
+       rmsnorm_fwd<T>(xres, const_cast<T*>(A), r, Bn, K, c->stream));
   c->gemm_fam = NC_FAM_DEC_GEMM;
   nc_status st = gemm(c, mk(Bn, N, K, A, K, 1, W, K, 1, EPI_STORE_F32, C, N, 1.f, beta));
   c->gemm_fam = NC_FAM_GEMM;
@@ -724,19 +730,21 @@ nc_status dec_gemm(nc_ctx* c, char* kv, const KvLayout& kl, int N, int K, const 
 // when given, else in the workspace) and reduced per row.
 template <typename T>
 nc_status decode_head(nc_ctx* c, char* kv, const KvLayout& kl, const T* P, const T* hf, int32_t* next,
-                      float* logits) {
+                      float* logits, const float* xres = nullptr, float* r = nullptr) {
   const int Bn = c->B, d = c->d, V = c->V;
   int rows, cols;
   const T* Wlm = P + param_offset(c, 1 + 4 * c->L, &rows, &cols);
   const int* tgt = wsp<int>(c, c->dec.tgt);  // all -1 (set by the caller): only lse and argmax
   if (c->prec == NC_BF16 && skinny_gemm_supports(Bn, V, d, d, d, hf, Wlm)) {
     float* lg = logits ? logits : wsp<float>(c, c->off.chunk);
-    CKS(dec_gemm<T>(c, kv, kl, V, d, hf, Wlm, lg, 0.f));
+    CKS(dec_gemm<T>(c, kv, kl, V, d, hf, Wlm, lg, 0.f, nullptr, xres, r));
     KL(NC_FAM_DEC_ROWS, 4.0 * Bn * V, 1,
        ce_rows_from_logits(lg, tgt, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next, Bn, V, c->status,
                            c->stream, wsp<float>(c, c->dec.cep), c->status + 3, c->sms));
     return NC_OK;
   }
+  if (xres)
+    KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + c->esz), 1, rmsnorm_fwd<T>(xres, const_cast<T*>(hf), r, Bn, d, c->stream));
   c->gemm_fam = NC_FAM_DEC_GEMM;
   nc_status st = lmhead_ce_forward<T>(c, hf, Wlm, tgt, Bn, wsp<float>(c, c->dec.lse), wsp<float>(c, c->dec.nll), next);
   if (st == NC_OK && logits) st = gemm(c, mk(Bn, V, d, hf, d, 1, Wlm, d, 1, EPI_STORE_F32, logits, V));
@@ -820,17 +828,15 @@ nc_status decode_impl(nc_ctx* c, const T* P, const int* tok, int pos, int* d_pos
     const T* Wproj = P + param_offset(c, 4 + 4 * l, &rows, &cols);
     T* K = reinterpret_cast<T*>(kv + (size_t)2 * l * kl.per);
     T* Vc = reinterpret_cast<T*>(kv + (size_t)(2 * l + 1) * kl.per);
-    KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    CKS(dec_gemm<T>(c, kv, kl, 3 * d, d, xn, Wqkv, qkv, 0.f));
+    // each RMSNorm rides in the product that consumes it (the kernel normalises x itself)
+    CKS(dec_gemm<T>(c, kv, kl, 3 * d, d, xn, Wqkv, qkv, 0.f, nullptr, x, r));
     KL(NC_FAM_DEC_ATTN, 2.0 * Bn * d * ((d_pos ? max_len : pos) + 1) * e, 1,
        attn_decode<T>(qkv, rc, rs, K, Vc, part, cnt, o, Bn, H, pos, d_pos, max_len, kDecodeChunk, c->status, s));
     CKS(dec_gemm<T>(c, kv, kl, d, d, o, Wo, x, 1.f));
-    KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, xn, r, Bn, d, s));
-    CKS(dec_gemm<T>(c, kv, kl, F, d, xn, Wfc, u, 0.f, a));
+    CKS(dec_gemm<T>(c, kv, kl, F, d, xn, Wfc, u, 0.f, a, x, r));
     CKS(dec_gemm<T>(c, kv, kl, d, F, a, Wproj, x, 1.f));
   }
-  KL(NC_FAM_DEC_ROWS, (double)Bn * d * (4 + e), 1, rmsnorm_fwd<T>(x, hf, r, Bn, d, s));
-  CKS(decode_head<T>(c, kv, kl, P, hf, next, logits));
+  CKS(decode_head<T>(c, kv, kl, P, hf, next, logits, x, r));
   if (d_pos) KL(NC_FAM_DEC_ROWS, 8.0, 1, advance_pos(d_pos, s));
   return NC_OK;
 }
