@@ -443,21 +443,51 @@ __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ 
   const int half = lane >> 4, l16 = lane & 15;
   const int b = m / Tlen, t = m % Tlen;
   const size_t row = (size_t)m * H * kHeadDim + l16 * 8;
-  for (int h0 = 0; h0 < H; h0 += 8) {
-    float u[4][8], v[4][8];
+  // head pairs per round: six in bf16 (the d20 model's ten heads in one round,
+  // raw 16-byte loads all issued first), four in fp32
+  constexpr int RP = sizeof(T) == 2 ? 6 : 4;
+  for (int h0 = 0; h0 < H; h0 += 2 * RP) {
+    float lsev[RP];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RP; ++i) {  // the lse rows early, off the end of the chain
       const int h = h0 + 2 * i + half;
-      if (h < H) {
-        ld8(dout + row + (size_t)h * kHeadDim, u[i]);
-        ld8(o + row + (size_t)h * kHeadDim, v[i]);
-      } else {
+      lsev[i] = (L2 && l16 == 0 && h < H) ? lse[((size_t)b * H + h) * Tlen + t] : 0.f;
+    }
+    uint4 ru[RP], rv[RP];
+    float u[RP][8], v[RP][8];
+    if constexpr (sizeof(T) == 2) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) u[i][e] = v[i][e] = 0.f;
+      for (int i = 0; i < RP; ++i) {
+        const int h = h0 + 2 * i + half;
+        ru[i] = h < H ? *reinterpret_cast<const uint4*>(dout + row + (size_t)h * kHeadDim) : make_uint4(0, 0, 0, 0);
+        rv[i] = h < H ? *reinterpret_cast<const uint4*>(o + row + (size_t)h * kHeadDim) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < RP; ++i) {
+        const uint32_t wu[4] = {ru[i].x, ru[i].y, ru[i].z, ru[i].w}, wv[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wu[q]));
+          const float2 c = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wv[q]));
+          u[i][2 * q] = a.x; u[i][2 * q + 1] = a.y;
+          v[i][2 * q] = c.x; v[i][2 * q + 1] = c.y;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < RP; ++i) {
+        const int h = h0 + 2 * i + half;
+        if (h < H) {
+          ld8(dout + row + (size_t)h * kHeadDim, u[i]);
+          ld8(o + row + (size_t)h * kHeadDim, v[i]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[i][e] = v[i][e] = 0.f;
+        }
       }
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < RP; ++i) {
       float sum = 0.f;
 #pragma unroll
       for (int e = 0; e < 8; ++e) sum += u[i][e] * v[i][e];
@@ -467,7 +497,7 @@ __global__ void attn_rowdot_k(const T* __restrict__ dout, const T* __restrict__ 
       if (l16 == 0 && h < H) {
         const size_t idx = ((size_t)b * H + h) * Tlen + t;
         Drow[idx] = sum;
-        if (L2) L2[idx] = -fmaf(lse[idx], 1.4426950408889634f, 3.5f);
+        if (L2) L2[idx] = -fmaf(lsev[i], 1.4426950408889634f, 3.5f);
       }
     }
   }
