@@ -561,12 +561,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
             }
           }
+          float rdot = 0.f;  // EPI_ROWDOT: this row's dot over the warp's head
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             float* w = v + h2 * 64;
             const int nc0 = n0 + h2 * 64;
             const bool chunk_ok = blk_ok && nc0 < g.N;
-            if (EPI == EPI_RELU2_BWD && chunk_ok) {
+            if ((EPI == EPI_RELU2_BWD || EPI == EPI_ROWDOT) && chunk_ok) {
               // this warp's 32 rows x 64 columns of C2 land in its staging
               // buffer by one tensor load (rows past M and columns past N read
               // as 0) while the accumulator is read: coalesced, where a row
@@ -586,7 +587,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               for (int i = 0; i < 64; ++i) w[i] *= g.alpha;
             }
             if (!chunk_ok) continue;
-            if (EPI == EPI_RELU2_BWD) {
+            if (EPI == EPI_RELU2_BWD || EPI == EPI_ROWDOT) {
               const bool got = tc::mbar_wait(c2bar + (warp - 2), c2n & 1, abort_flag, wait_ns);
               ++c2n;
               if (!__all_sync(0xffffffffu, got)) {
@@ -595,6 +596,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 // the tile load this warp started lands before the CTA can leave
                 if (!got) tc::mbar_wait(c2bar + (warp - 2), (c2n - 1) & 1, nullptr, kWaitNs);
               }
+            }
+            if (EPI == EPI_ROWDOT) {
+              // the row's dot of C, as it is stored (bf16), with its C2 (o) row over this head
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                float of[8];
+                unpack8_bf16(*reinterpret_cast<const uint4*>(stg.buf + lane * 128 + ((j ^ (lane & 7)) << 4)), of);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) rdot += __bfloat162float(__float2bfloat16_rn(w[8 * j + i])) * of[i];
+              }
+            }
+            if (EPI == EPI_RELU2_BWD) {
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 float uf[8];
@@ -649,6 +662,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
               }
               stg.store(&tc2, nc0, rblk, false);
             }
+          }
+          if (EPI == EPI_ROWDOT && row_ok && n0 < g.N) {  // the warp's 128 columns are one head
+            const int H = g.N / 128, bq = m / g.seq_len, t = m - bq * g.seq_len;
+            const size_t idx = ((size_t)bq * H + n0 / 128) * g.seq_len + t;
+            g.rd_D[idx] = rdot;
+            if (g.rd_L2) g.rd_L2[idx] = -fmaf(g.rd_lse[idx], 1.4426950408889634f, 3.5f);
           }
         }
       }
@@ -762,6 +781,7 @@ KernFn pick_kernel(int epi, int a_mn, int b_mn) {
     case EPI_QKNORM_ROPE: return pick<EPI_QKNORM_ROPE, CL>(a_mn, b_mn);
     case EPI_AXPBY: return pick<EPI_AXPBY, CL>(a_mn, b_mn);
     case EPI_RELU2A: return pick<EPI_RELU2A, CL>(a_mn, b_mn);
+    case EPI_ROWDOT: return pick<EPI_ROWDOT, CL>(a_mn, b_mn);
     default: return nullptr;
   }
 }
@@ -825,12 +845,16 @@ bool gemm_tc_supports(const GemmArgs& g) {
   if (g.epi == EPI_CE_FWD) return g.p_max && g.p_sum && g.p_arg && g.p_tgt && g.row_i;
   if (g.splits > 1 && (g.epi != EPI_STORE_F32 || (!g.partial && !g.tile_done) || g.N % 4)) return false;
   if (g.ldc % 8 || !aligned16(g.C)) return false;
-  if ((g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD) && (g.ldc2 % 8 || !aligned16(g.C2))) return false;
+  if ((g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD || g.epi == EPI_ROWDOT) && (!g.C2 || g.ldc2 % 8 || !aligned16(g.C2)))
+    return false;
+  if (g.epi == EPI_ROWDOT &&
+      (g.N % 128 || g.seq_len < 1 || g.M % g.seq_len || !g.rd_D || (g.rd_L2 == nullptr) != (g.rd_lse == nullptr)))
+    return false;
   if (g.epi == EPI_CE_BWD && (!g.row_f || !g.row_i)) return false;
   if (g.epi == EPI_QKNORM_ROPE &&
       (!g.rope_cos || !g.rope_sin || !g.rqk || g.seq_len < 1 || g.d_model % 128 || g.N != 3 * g.d_model))
     return false;
-  return g.epi >= EPI_STORE && g.epi <= EPI_RELU2A;
+  return g.epi >= EPI_STORE && g.epi <= EPI_ROWDOT;
 }
 
 cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
@@ -855,7 +879,8 @@ cudaError_t gemm_tc(const GemmArgs& g, cudaStream_t s) {
   const bool f32out = g.epi == EPI_STORE_F32;
   if (g.epi != EPI_CE_FWD) ok = make_out_map(&tcm, g.C, f32out, g.N, c_rows, g.ldc);
   // RELU2's second output a, or RELU2_BWD's input a (loaded in 32 x 64 chunks)
-  if (ok && (g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD)) ok = make_out_map(&tcm2, g.C2, false, g.N, g.M, g.ldc2);
+  if (ok && (g.epi == EPI_RELU2 || g.epi == EPI_RELU2_BWD || g.epi == EPI_ROWDOT))
+    ok = make_out_map(&tcm2, g.C2, false, g.N, g.M, g.ldc2);
   if (!ok) return cudaErrorInvalidValue;
   TcParams p;
   p.g = g;

@@ -20,6 +20,8 @@ enum Epi : int {
   EPI_QKNORM_ROPE = 6, // C (elem) = qkv with per-head RMSNorm + RoPE on the q,k columns
   EPI_AXPBY = 7,       // C (elem) = alpha*acc + beta*C2 (C2 elem, same shape as C)
   EPI_RELU2A = 8,      // C (elem) = max(alpha*acc, 0)^2 only (the step keeps a, not u)
+  EPI_ROWDOT = 9,      // C (elem) = alpha*acc; rd_D[b,h,t] = sum over head h's 128 columns of C (as stored) * C2,
+                       // rd_L2 = -(rd_lse * log2(e) + 3.5) (tensor-core path; rows m = b*seq_len + t)
 };
 
 struct GemmArgs {
@@ -42,6 +44,8 @@ struct GemmArgs {
   const float* rope_cos = nullptr; const float* rope_sin = nullptr;
   float* rqk = nullptr;          // [M, 2H] rstd of q heads then k heads
   int seq_len = 0, d_model = 0;
+  // row dot of the attention backward (EPI_ROWDOT): [B, N/128, seq_len] fp32 each
+  float* rd_D = nullptr; float* rd_L2 = nullptr; const float* rd_lse = nullptr;
   // split-K (EPI_STORE_F32 only): splits > 1 writes alpha*partial sums to
   // `partial` ([splits, M, N] fp32) and a reduction kernel forms C.
   int splits = 1;

@@ -529,10 +529,23 @@ nc_status backward_impl(nc_ctx* c, const T* P, const int* tok, const int* tgt, f
     KL(NC_FAM_ROWS, (double)M * d * (8 + 3 * sizeof(T)) + 4.0 * M, 1, rmsnorm_bwd<T>(dy, xn2, r2, dx, dxe, M, d, 1, s));
     // attention: x += attn(xn1) Wo^T
     CKS(gemm(c, mk(d, d, M, dxe, d, 0, o, d, 0, EPI_STORE_F32, G + oo, d, 1.f, gb)));
-    CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
-    KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + (sizeof(T) == 2 ? 12.0 : 4.0) * M * H, 1,
-       attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s, sizeof(T) == 2 ? lse_att : nullptr,
-                      sizeof(T) == 2 ? drow + (size_t)M * H : nullptr));
+    if (sizeof(T) == 2 && c->use_tc && c->prec == NC_BF16) {
+      // dout with the attention backward's row terms in its epilogue: D = rowsum(dout o) per head
+      // and the negated base-2 lse rows, with o loaded by tensor copies beside the accumulator
+      GemmArgs gd = mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_ROWDOT, dout, d);
+      gd.C2 = const_cast<T*>(o);
+      gd.ldc2 = d;
+      gd.seq_len = Tn;
+      gd.rd_D = drow;
+      gd.rd_L2 = drow + (size_t)M * H;
+      gd.rd_lse = lse_att;
+      CKS(gemm(c, gd));
+    } else {
+      CKS(gemm(c, mk(M, d, d, dxe, d, 1, P + oo, d, 0, EPI_STORE, dout, d)));
+      KL(NC_FAM_ROWS, 2.0 * M * d * sizeof(T) + (sizeof(T) == 2 ? 12.0 : 4.0) * M * H, 1,
+         attn_rowdot<T>(dout, o, drow, c->B, Tn, H, s, sizeof(T) == 2 ? lse_att : nullptr,
+                        sizeof(T) == 2 ? drow + (size_t)M * H : nullptr));
+    }
     const bool fused_k = c->prec == NC_BF16;  // k half of the QK-norm/RoPE backward inside the kernel
     KL(NC_FAM_ATTN_BWD, 2.0 * attn_fwd_flops(c), fused_k ? 1 : 2,
        attn_bwd<T>(c, qkv, dout, lse_att, drow, dqk, dqkv, fused_k ? rqk : nullptr));
