@@ -813,11 +813,18 @@ int max_clusters(KernFn fn) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
-// k-splits summed into C inside the kernel, in split order (see TcParams)
+// k-splits summed into C inside the kernel, in split order (see TcParams).
+// Only where one split's work units fill the resident CTA pairs: then split
+// s of a tile runs a wave after split s - 1 and finds it done. With fewer
+// tiles the splits of a tile run side by side and their epilogues would
+// queue one behind the other (measured: the 256-wide model's step 1.8 ->
+// 2.3 ms), so those keep the partial slabs and the reduction kernel.
 bool split_in_kernel(const GemmArgs& g, int splits) {
   if (splits < 2 || !g.tile_done || g.batch != 1 || (g.beta != 0.f && g.beta != 1.f)) return false;
-  const long long tiles = (long long)((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
-  return tiles <= kGemmTileCap;
+  const long long rows = (g.M + BM - 1) / BM, cols = (g.N + BN - 1) / BN;
+  if (rows * cols > kGemmTileCap) return false;
+  const long long units = (g.M > BM ? (rows + 1) / 2 : rows) * cols;  // CTA-pair units of one split
+  return units >= (g_num_sms > 0 ? g_num_sms : 148) / 2;
 }
 
 }  // namespace
