@@ -4,7 +4,9 @@
 // by TMA), QKV with per-head RMSNorm + RoPE, cross-entropy forward partials
 // (per-row max / sum-exp / argmax / target logit over each 128-column
 // vocabulary half-tile, so the logits are never written), cross-entropy
-// backward (softmax - onehot) and alpha acc + beta C2 (the optimizer).
+// backward (softmax - onehot), alpha acc + beta C2 (the optimizer) and the
+// attention backward's row terms beside dout (rowsum(dout o) per head, o loaded
+// by TMA, and the negated base-2 lse rows).
 //
 // Structure: persistent CTAs (one per SM), 128x256 output tiles, 64-deep k
 // slices of bf16 staged by TMA into 128-byte-swizzled shared memory in an
@@ -13,7 +15,9 @@
 // epilogue of tile i overlaps the main loop of tile i+1), warps 2..9 read the
 // accumulator with tcgen05.ld (one thread per output row and 128-column half)
 // and run the epilogue. Weight-gradient shapes (few output tiles, K = tokens)
-// split K across CTAs into fp32 partial slabs that a reduction kernel sums.
+// split K across CTAs; where one split's units fill the SMs the splits are
+// added into C inside the kernel in split order (per-tile counters), else
+// into fp32 partial slabs that a reduction kernel sums.
 // CTAs run as 2-CTA clusters on vertically adjacent tiles with 2-SM products
 // (tcgen05 cta_group::2): one thread of the even CTA issues 256x256x16 MMAs
 // whose A rows come half from each CTA's shared memory and whose B tile is
