@@ -618,7 +618,7 @@ KERNEL_CASES = {
     "gemm_qkv": ("tensor", "2*M*N*K FLOPs", "32768 x 3840 x 1280 forward GEMM, QK-norm + RoPE epilogue"),
     "gemm_fc": ("tensor", "2*M*N*K FLOPs", "32768 x 5120 x 1280 forward GEMM, ReLU^2 epilogue (a only)"),
     "gemm_relu2_bwd": ("tensor", "2*M*N*K FLOPs", "32768 x 5120 x 1280 GEMM with the ReLU^2 backward epilogue"),
-    "gemm_dw": ("tensor", "2*M*N*K FLOPs", "1280 x 5120 x 32768 weight gradient (split-K + splitk_reduce_k)"),
+    "gemm_dw": ("tensor", "2*M*N*K FLOPs", "1280 x 5120 x 32768 weight gradient (k-splits summed in the kernel)"),
     "attn_fwd": ("tensor", "2*128*T*(T+1)*B*H FLOPs", "causal attention forward"),
     "attn_bwd": ("tensor", "4*128*T*(T+1)*B*H FLOPs", "attn_rowdot_k + causal attention backward"),
     "lmhead_ce": ("tensor", "2*M*V*d FLOPs", "lm_head + CE forward, 4096 rows (GEMM partials + ce_reduce_k)"),
@@ -626,7 +626,8 @@ KERNEL_CASES = {
     "rmsnorm_bwd": ("hbm", "M*d*(4+4+2+2+2) + 4*M bytes", "rmsnorm_bwd_k, accumulating into fp32 dx, bf16 copy"),
     "qk_norm_rope_bwd": ("hbm", "2*M*d*(4+2+2) + 8*M*H bytes", "qk_norm_rope_bwd_k over q and k heads"),
     "embed_fwd": ("hbm", "M*d*(2+4) + 4*M bytes", "embed_fwd_k: gather of Zipf(1.1) ids into fp32 x"),
-    "embed_bwd": ("hbm", "M*d*(4+4) + 4*M bytes", "embed_bwd_k: float4 atomic scatter of fp32 dx (after a memset)"),
+    "embed_bwd": ("hbm", "M*d*(4+4) + 4*M bytes",
+                  "deterministic embedding gradient: key sort, run sums, per-id merge (after a memset of dW_te)"),
 }
 
 
