@@ -49,7 +49,7 @@ typedef enum {
   NC_ERR_CUDA = 3,        /* a CUDA runtime call failed (message has the code) */
   NC_ERR_TIMEOUT = 4,     /* a device pipeline wait exceeded its limit */
   NC_ERR_DEVICE = 5,      /* device-side check failed (e.g. token id >= vocab) */
-  NC_ERR_UNSUPPORTED = 6  /* valid request this build does not implement */
+  NC_ERR_UNSUPPORTED = 6  /* valid request the library does not serve     */
 } nc_status;
 
 /* Precision modes for nc_configure. */
