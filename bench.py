@@ -381,7 +381,7 @@ def our_arm(args):
                 "achieved": fd["gbs"] if dom == "rows" else fd["tflops"], "peak": fd["peak"],
                 "unit": "GB/s" if dom == "rows" else "TFLOP/s", "frac": fd["frac"],
                 "peak_kind": f"{pk_kind} ({'HBM copy' if dom == 'rows' else 'sustained bf16'})",
-                "traffic": read_traffic(dom), "launches": dn, "avg_launch_ms": dms / max(1, dn),
+                "traffic": read_traffic(dom, w.name), "launches": dn, "avg_launch_ms": dms / max(1, dn),
                 "share_of_step": dms / (ms_eager * steps),
                 "work": "algorithmic: 6*M*(12*L*d^2 + d*V) FLOPs per step for the GEMMs (the lm_head "
                         "backward's logit recompute excluded; it is in achieved_hw)"}
@@ -578,9 +578,10 @@ def infer_timing(nc, st, w, params, tok, stream, args, ws, pk):
     }
 
 
-def read_traffic(family: str):
+def read_traffic(family: str, workload: str):
     """Per-launch DRAM bytes from the committed ncu summary of this kernel
-    family, or None when absent or taken on a different kernel source."""
+    family, or None when absent, taken on a different kernel source, or taken
+    on another workload."""
     path = os.path.join(ROOT, "profiles", f"traffic_{family}.txt")
     if not os.path.exists(path):
         return None
@@ -590,6 +591,8 @@ def read_traffic(family: str):
             if ":" in line:
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
+    if kv.get("workload", workload) != workload:
+        return None
     src = kv.get("source_sha256")
     files = kv.get("source_files", "").split()
     if not src or not files:
